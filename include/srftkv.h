@@ -1,0 +1,180 @@
+/*
+ * srftkv.h -- C ABI of libsrftkv, a GB300 (sm_103a) library for
+ * rotate-then-quantize compression of the LLM KV cache and for decode
+ * attention that reads the compressed cache directly.
+ *
+ * Method sources (page title -- section):
+ *  [WQF] "When Quantization Is Free: An int4 KV Cache That Outruns fp16 on
+ *        Apple Silicon" (summary of arXiv 2605.05699) -- Methodology 1
+ *        (SRFT(x) = pack(F . diag(s) . x), F the unitary DFT, s a fixed
+ *        random sign vector), Methodology 2 (the fused kernel: sign multiply,
+ *        log2(d/2) radix-2 Stockham FFT stages, Hermitian packing, per-channel
+ *        lambda, per-group absmax, signed int4/int8 rounding, nibble packing),
+ *        Methodology 3 (per-channel lambda combined with groups of 16).
+ *  [GEM] "Gemini on-device quantization, KV cache, Apple Silicon" -- section
+ *        "Flash Attention and Metal kernel fusion" (tiled attention with an
+ *        online softmax) and "INT8/INT4 quantization strategy" (the memory
+ *        formula).
+ *  [KVS] "Efficient LLM inference on Apple Silicon: KVSplit key techniques"
+ *        -- "Key findings" (8-bit keys with 4-bit values, K8V4).
+ *  [TQ]  "TurboQuant mobile KV cache compression: quantized deployment and
+ *        latency optimisation on M5 Pro and iOS" -- quantization strategy
+ *        section (online quantization of each newly generated token).
+ *  [AQT] "No.9: how Apple fits a 3 GB model into a phone" -- section
+ *        "Multi-plane tensor: data and scale factors together" (a quantized
+ *        tensor is a data plane plus a scale plane).
+ *
+ * Readings where the pages leave a step open (the library and its test
+ * oracle implement each one independently):
+ *  - sign vector: s_i = -1 iff bit 63 of output i (from 0) of a splitmix64
+ *    generator seeded with sign_seed is set (Steele, Lea & Flood 2014);
+ *  - forward DFT uses exp(-2 pi i nk/d)/sqrt(d);
+ *  - packing: p0 = y_0, p1 = y_{d/2}, p_{2k} = sqrt2 Re y_k,
+ *    p_{2k+1} = sqrt2 Im y_k (k = 1..d/2-1): an orthogonal real map;
+ *  - z_i = lambda_i * p_i; scale_j = max_{i in group j} |z_i| / Q with
+ *    Q = 2^(bits-1)-1; q_i = rint(z_i / scale_j) in [-Q, Q]; zero group ->
+ *    scale 0 and codes 0;
+ *  - int4: two's-complement nibbles, even coordinate in the low nibble;
+ *    int8: two's-complement bytes;
+ *  - scales are fp32; softmax scale defaults to 1/sqrt(d); a query with
+ *    sequence length 0 gets a zero output.
+ *
+ * General conventions
+ *  - Every pointer argument that names tensor data is a DEVICE pointer
+ *    owned by the caller; the library allocates no device memory and keeps
+ *    no state between calls except per-device capability checks.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Work is enqueued without host synchronisation; device-side
+ *    faults surface on the caller's next synchronisation.
+ *  - Return codes: SRFTKV_OK, or a negative SRFTKV_ERR_*; on any error no
+ *    work has been enqueued and srftkv_last_error() describes it.
+ *  - Inputs must be finite; NaN/Inf behaviour is unspecified.
+ *  - Supported sizes: d in {16, 32, 64, 128, 256} for the codec and the
+ *    transform, d in {64, 128, 256} for attention; group a power of two,
+ *    16 <= group <= d; bits in {4, 8} for packed sides.
+ */
+#ifndef SRFTKV_H
+#define SRFTKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SRFTKV_OK 0
+#define SRFTKV_ERR_INVALID (-1) /* bad size, pointer, alignment or bit width */
+#define SRFTKV_ERR_CUDA (-2)    /* a CUDA call or launch failed */
+#define SRFTKV_ERR_DEVICE (-3)  /* current device is not sm_103 */
+
+/*
+ * One side (K or V) of a packed cache, stored as two planes ([AQT]):
+ *   codes  : uint8 [n_outer][t_cap][H][d*bits/8]  (row start 16-byte aligned
+ *            when d*bits/8 >= 16, else d*bits/8-byte aligned)
+ *   scales : fp32  [n_outer][t_cap][H][d/group]   (16-byte aligned when
+ *            d/group >= 4, else 4*d/group-byte aligned)
+ * n_outer is the layer index for the codec calls and the batch index for
+ * attention.  A side with bits == 16 (attention only) is a raw fp16 cache
+ * [B][t_cap][Hkv][d] passed in `codes`, without rotation or scales.
+ */
+typedef struct srftkv_side {
+    void* x;                     /* quantize: fp16 input [n_outer][n_tokens][H][d] (read);
+                                    dequantize: fp16 output, same layout (written);
+                                    attention: unused */
+    const float* lambda;         /* per-channel lambda, element (o, h, i) at
+                                    lambda[o*lambda_outer_stride + h*d + i]; must be > 0;
+                                    NULL means all ones ([WQF] Methodology 3) */
+    int64_t lambda_outer_stride; /* 0 broadcasts one [H][d] table over n_outer */
+    int bits;                    /* 4 or 8 (16 = raw fp16 cache, attention only) */
+    void* codes;                 /* code plane (see above) */
+    float* scales;               /* scale plane (see above) */
+} srftkv_side;
+
+/*
+ * srft_kv_quantize -- encode fp16 head vectors into the packed cache
+ * ([WQF] Methodology 1-3; K8V4 via bits per side [KVS]; appending one token
+ * per step is n_tokens = 1 at t_offset = current length [TQ]).
+ * For each side that is not NULL and every (o, t, h) with t < n_tokens:
+ *   p = SRFT(x[o][t][h]); z = lambda[o][h] * p; per group j of `group`
+ *   coordinates: scales[o][t_offset+t][h][j] = max|z| / Q and
+ *   codes[o][t_offset+t][h] = packed rint(z / scale).
+ * Both sides are encoded by one kernel launch.  Requires
+ * 0 <= t_offset, t_offset + n_tokens <= t_cap, and x rows 16-byte aligned.
+ * n_outer == 0 or n_tokens == 0 is a no-op that returns SRFTKV_OK.
+ */
+int srft_kv_quantize(const srftkv_side* k, const srftkv_side* v, int n_outer, int n_tokens,
+                     int H, int d, int group, int t_cap, int t_offset, uint64_t sign_seed,
+                     void* stream);
+
+/*
+ * srft_kv_dequantize -- decode tokens [t_offset, t_offset+n_tokens) of the
+ * packed cache back to fp16 ([WQF] Methodology 2, run backwards):
+ *   x_hat = diag(s) . F^{-1} . unpack((codes * scale) / lambda)
+ * written to side->x as [n_outer][n_tokens][H][d].  Same size rules as
+ * srft_kv_quantize.
+ */
+int srft_kv_dequantize(const srftkv_side* k, const srftkv_side* v, int n_outer, int n_tokens,
+                       int H, int d, int group, int t_cap, int t_offset, uint64_t sign_seed,
+                       void* stream);
+
+/*
+ * q4kv_decode_attention -- one decode step of attention that reads the
+ * packed cache directly ([GEM] Flash Attention section: tiles of tokens with
+ * an online softmax; [WQF] Methodology 1: SRFT is orthogonal, so
+ * q . k_hat = SRFT(q) . (z_hat / lambda) and the cache is never rotated
+ * back per token).
+ *   q        : fp16 [B][Hq][d]
+ *   out      : fp32 [B][Hq][d], out[b][h] = sum_t softmax_t(sm_scale * q.k_hat_t) v_hat_t
+ *              over t < seq_lens[b], with query head h reading kv head
+ *              h / (Hq/Hkv); k_hat, v_hat are the dequantised (unrotated) cache.
+ *   k, v     : packed sides (bits 4 or 8) or both raw fp16 (bits 16);
+ *              the x field is ignored.
+ *   seq_lens : device int32 [B], each in [0, t_cap]; NULL means t_cap for all.
+ *   sm_scale : softmax scale; <= 0 selects 1/sqrt(d).
+ *   n_splits : number of context splits (split-K) per (b, kv head); 0 picks
+ *              one from the device's SM count, B*Hkv and t_cap.
+ *   workspace: device scratch of at least
+ *              q4kv_decode_attention_workspace_size(...) bytes (16-byte aligned)
+ *              for the per-split partial results; contents need not be
+ *              initialised and are overwritten.
+ * Requires Hq % Hkv == 0 and Hq/Hkv <= 8.
+ */
+int q4kv_decode_attention(const void* q, float* out, const srftkv_side* k, const srftkv_side* v,
+                          int B, int Hq, int Hkv, int d, int group, int t_cap,
+                          const int* seq_lens, float sm_scale, uint64_t sign_seed, int n_splits,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace q4kv_decode_attention needs for these sizes (n_splits 0 = the
+ * automatic choice on the current device).  Returns 0 for invalid sizes. */
+size_t q4kv_decode_attention_workspace_size(int B, int Hq, int Hkv, int d, int t_cap, int n_splits);
+
+/* Bytes of one packed vector: code plane d*bits/8 and scale plane 4*d/group.
+ * Host-only; returns SRFTKV_OK or SRFTKV_ERR_INVALID. */
+int srft_kv_vector_bytes(int d, int bits, int group, size_t* code_bytes, size_t* scale_bytes);
+
+/*
+ * srft_transform -- the bare transform, for testing ([WQF] Methodology 1).
+ * x : fp16 [n][d] (16-byte aligned rows); y : fp32 [n][d].
+ * inverse == 0: y = SRFT(x) (packed coordinates p);
+ * inverse != 0: y = SRFT^{-1}(x) = diag(s) . F^{-1} . unpack(x).
+ */
+int srft_transform(const void* x, float* y, int n, int d, uint64_t sign_seed, int inverse,
+                   void* stream);
+
+/* Message for the last non-zero return on this host thread ("" if none). */
+const char* srftkv_last_error(void);
+
+/*
+ * srftkv_device_fault -- copies the library's device-side fault word for the
+ * current device into *fault (0 = none) and clears it.  A kernel whose
+ * bounded wait on an asynchronous copy gives up sets a bit here and returns
+ * instead of waiting forever.  Synchronises the current device.
+ */
+int srftkv_device_fault(unsigned int* fault);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SRFTKV_H */

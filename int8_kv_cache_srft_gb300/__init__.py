@@ -1,0 +1,168 @@
+"""int8_kv_cache_srft_gb300 -- Python binding of libsrftkv (GB300, sm_103a).
+
+A thin ctypes layer over the C ABI in ``include/srftkv.h``: it turns torch
+tensors into device pointers and the current torch stream into a
+cudaStream_t, calls the entry point of the same name and raises on a
+non-zero return.  All arithmetic happens in the library's CUDA kernels;
+there is no CPU or PyTorch fallback, and importing this package fails
+loudly when the library has not been built (``python -m
+int8_kv_cache_srft_gb300.build``).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsrftkv.so")
+
+SRFTKV_OK = 0
+SRFTKV_ERR_INVALID = -1
+SRFTKV_ERR_CUDA = -2
+SRFTKV_ERR_DEVICE = -3
+
+
+class SrftKvError(RuntimeError):
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__(f"{fn} returned {code}: {msg}")
+        self.code = code
+
+
+class _Side(ctypes.Structure):
+    _fields_ = [
+        ("x", ctypes.c_void_p),
+        ("lambda_", ctypes.c_void_p),
+        ("lambda_outer_stride", ctypes.c_int64),
+        ("bits", ctypes.c_int),
+        ("codes", ctypes.c_void_p),
+        ("scales", ctypes.c_void_p),
+    ]
+
+
+_lib = None
+
+
+def library() -> ctypes.CDLL:
+    """Load libsrftkv.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with `python -m int8_kv_cache_srft_gb300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    i, u64, vp, sz = ctypes.c_int, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_size_t
+    sp = ctypes.POINTER(_Side)
+    lib.srft_kv_quantize.argtypes = [sp, sp, i, i, i, i, i, i, i, u64, vp]
+    lib.srft_kv_dequantize.argtypes = [sp, sp, i, i, i, i, i, i, i, u64, vp]
+    lib.q4kv_decode_attention.argtypes = [vp, vp, sp, sp, i, i, i, i, i, i, vp, ctypes.c_float, u64, i, vp, sz, vp]
+    lib.q4kv_decode_attention_workspace_size.argtypes = [i, i, i, i, i, i]
+    lib.q4kv_decode_attention_workspace_size.restype = sz
+    lib.srft_kv_vector_bytes.argtypes = [i, i, i, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+    lib.srft_transform.argtypes = [vp, vp, i, i, u64, i, vp]
+    lib.srftkv_last_error.restype = ctypes.c_char_p
+    lib.srftkv_device_fault.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+    for name in ("srft_kv_quantize", "srft_kv_dequantize", "q4kv_decode_attention", "srft_kv_vector_bytes",
+                 "srft_transform", "srftkv_device_fault"):
+        getattr(lib, name).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _check(fn: str, rc: int) -> None:
+    if rc != SRFTKV_OK:
+        raise SrftKvError(fn, rc, library().srftkv_last_error().decode())
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+@dataclass
+class Side:
+    """One side (K or V) of a packed cache: the code plane, the scale plane,
+    an optional per-channel lambda and, for the codec calls, the fp16 rows."""
+
+    codes: torch.Tensor            # uint8 [n_outer][t_cap][H][d*bits/8] (or fp16 [B][t_cap][Hkv][d] for bits 16)
+    scales: torch.Tensor | None    # fp32 [n_outer][t_cap][H][d/group]
+    bits: int
+    x: torch.Tensor | None = None  # fp16 [n_outer][n_tokens][H][d]
+    lam: torch.Tensor | None = None  # fp32 [n_lam][H][d]; n_lam == 1 broadcasts
+    lam_outer_stride: int | None = None
+
+    def to_c(self) -> _Side:
+        stride = self.lam_outer_stride
+        if stride is None:
+            stride = 0 if self.lam is None or self.lam.shape[0] == 1 else self.lam.shape[1] * self.lam.shape[2]
+        return _Side(_ptr(self.x), _ptr(self.lam), stride, self.bits, _ptr(self.codes), _ptr(self.scales))
+
+
+def alloc_side(n_outer: int, t_cap: int, H: int, d: int, bits: int, group: int, device="cuda") -> Side:
+    """Allocate empty code and scale planes for one side."""
+    if bits == 16:
+        return Side(torch.empty((n_outer, t_cap, H, d), dtype=torch.float16, device=device), None, 16)
+    codes = torch.empty((n_outer, t_cap, H, d * bits // 8), dtype=torch.uint8, device=device)
+    scales = torch.empty((n_outer, t_cap, H, d // group), dtype=torch.float32, device=device)
+    return Side(codes, scales, bits)
+
+
+def _sidep(s: Side | None):
+    return None if s is None else ctypes.pointer(s.to_c())
+
+
+def srft_kv_quantize(k: Side | None, v: Side | None, n_outer: int, n_tokens: int, H: int, d: int, group: int,
+                     t_cap: int, t_offset: int, sign_seed: int, stream=None) -> None:
+    rc = library().srft_kv_quantize(_sidep(k), _sidep(v), n_outer, n_tokens, H, d, group, t_cap, t_offset,
+                                    sign_seed, _stream(stream))
+    _check("srft_kv_quantize", rc)
+
+
+def srft_kv_dequantize(k: Side | None, v: Side | None, n_outer: int, n_tokens: int, H: int, d: int, group: int,
+                       t_cap: int, t_offset: int, sign_seed: int, stream=None) -> None:
+    rc = library().srft_kv_dequantize(_sidep(k), _sidep(v), n_outer, n_tokens, H, d, group, t_cap, t_offset,
+                                      sign_seed, _stream(stream))
+    _check("srft_kv_dequantize", rc)
+
+
+def q4kv_decode_attention_workspace_size(B: int, Hq: int, Hkv: int, d: int, t_cap: int, n_splits: int = 0) -> int:
+    return int(library().q4kv_decode_attention_workspace_size(B, Hq, Hkv, d, t_cap, n_splits))
+
+
+def q4kv_decode_attention(q: torch.Tensor, out: torch.Tensor, k: Side, v: Side, B: int, Hq: int, Hkv: int, d: int,
+                          group: int, t_cap: int, seq_lens: torch.Tensor | None, sm_scale: float, sign_seed: int,
+                          n_splits: int, workspace: torch.Tensor, stream=None) -> None:
+    rc = library().q4kv_decode_attention(_ptr(q), _ptr(out), _sidep(k), _sidep(v), B, Hq, Hkv, d, group, t_cap,
+                                         _ptr(seq_lens), sm_scale, sign_seed, n_splits, _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("q4kv_decode_attention", rc)
+
+
+def srft_kv_vector_bytes(d: int, bits: int, group: int) -> tuple[int, int]:
+    cb, sb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check("srft_kv_vector_bytes", library().srft_kv_vector_bytes(d, bits, group, ctypes.byref(cb), ctypes.byref(sb)))
+    return cb.value, sb.value
+
+
+def srft_transform(x: torch.Tensor, y: torch.Tensor, n: int, d: int, sign_seed: int, inverse: bool,
+                   stream=None) -> None:
+    rc = library().srft_transform(_ptr(x), _ptr(y), n, d, sign_seed, int(bool(inverse)), _stream(stream))
+    _check("srft_transform", rc)
+
+
+def srftkv_device_fault() -> int:
+    f = ctypes.c_uint(0)
+    _check("srftkv_device_fault", library().srftkv_device_fault(ctypes.byref(f)))
+    return f.value
+
+
+def srftkv_last_error() -> str:
+    return library().srftkv_last_error().decode()

@@ -1,0 +1,272 @@
+// api.cu -- the C ABI of libsrftkv: argument validation, the sign vector,
+// TMA tensor-map encoding, device checks and error reporting.  The entry
+// points are declared and documented in include/srftkv.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+
+namespace srftkv {
+
+// ---------------------------------------------------------------------------
+// Errors
+// ---------------------------------------------------------------------------
+static thread_local char t_err[512] = "";
+
+void set_error(const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_err, sizeof(t_err), fmt, ap);
+    va_end(ap);
+}
+
+static int invalid(const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_err, sizeof(t_err), fmt, ap);
+    va_end(ap);
+    return SRFTKV_ERR_INVALID;
+}
+
+// ---------------------------------------------------------------------------
+// Sign vector: s_i = -1 iff bit 63 of output i of splitmix64(seed) is set.
+// splitmix64 (Steele, Lea & Flood, OOPSLA 2014): the state advances by the
+// golden-ratio increment and each output is the state passed through two
+// xor-shift-multiply rounds and a final xor-shift.
+// ---------------------------------------------------------------------------
+static uint64_t splitmix64_output(uint64_t state) {
+    uint64_t z = state;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+void sign_masks(int d, uint64_t seed, uint32_t* words) {
+    uint64_t state = seed;
+    for (int i = 0; i < d; ++i) {
+        state += 0x9E3779B97F4A7C15ull;
+        const bool neg = (splitmix64_output(state) >> 63) != 0;
+        if (neg) words[i / 2] |= (i & 1) ? 0x80000000u : 0x00008000u;
+        else words[i / 2] &= (i & 1) ? ~0x80000000u : ~0x00008000u;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Device checks
+// ---------------------------------------------------------------------------
+struct DevInfo {
+    int checked = 0;
+    int ok = 0;
+    int sms = 0;
+};
+static DevInfo g_dev[64];
+static std::mutex g_dev_mu;
+
+static int current_device_ok() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        set_error("no current CUDA device");
+        return SRFTKV_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DevInfo& di = g_dev[dev];
+    if (!di.checked) {
+        cudaDeviceProp p;
+        if (cudaGetDeviceProperties(&p, dev) != cudaSuccess) {
+            set_error("cudaGetDeviceProperties failed");
+            return SRFTKV_ERR_CUDA;
+        }
+        di.ok = (p.major == 10 && p.minor == 3);
+        di.sms = p.multiProcessorCount;
+        di.checked = 1;
+        if (!di.ok) snprintf(t_err, sizeof(t_err), "device %d is sm_%d%d, this library is built for sm_103a", dev, p.major, p.minor);
+    }
+    if (!di.ok) {
+        set_error("current device is not sm_103 (GB300)");
+        return SRFTKV_ERR_DEVICE;
+    }
+    return SRFTKV_OK;
+}
+
+int device_sm_count() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && g_dev[dev].checked) return g_dev[dev].sms;
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+}
+
+// ---------------------------------------------------------------------------
+// TMA tensor maps
+// ---------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+static std::once_flag g_encode_once;
+
+static PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode;
+}
+
+bool encode_row_map(CUtensorMap* map, void* base, int d, long long rows_per_outer, int n_outer, int box_rows) {
+    auto enc = encoder();
+    if (!enc) {
+        set_error("cuTensorMapEncodeTiled is unavailable from the driver");
+        return false;
+    }
+    CUresult r;
+    if (d <= 128) {
+        const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows_per_outer, (cuuint64_t)n_outer};
+        const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows_per_outer * d * 2};
+        const cuuint32_t box[3] = {(cuuint32_t)(d + 8), (cuuint32_t)box_rows, 1};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        const int half = d / 2;
+        const cuuint64_t dims[4] = {(cuuint64_t)half, 2, (cuuint64_t)rows_per_outer, (cuuint64_t)n_outer};
+        const cuuint64_t strides[3] = {(cuuint64_t)half * 2, (cuuint64_t)d * 2, (cuuint64_t)rows_per_outer * d * 2};
+        const cuuint32_t box[4] = {(cuuint32_t)(half + 8), 2, (cuuint32_t)box_rows, 1};
+        const cuuint32_t estr[4] = {1, 1, 1, 1};
+        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    if (r != CUDA_SUCCESS) {
+        set_error("cuTensorMapEncodeTiled failed (CUresult %d) for d=%d rows=%lld outer=%d", (int)r, d, rows_per_outer,
+                  n_outer);
+        return false;
+    }
+    return true;
+}
+
+// ---------------------------------------------------------------------------
+// Validation helpers
+// ---------------------------------------------------------------------------
+static bool pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
+static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+static size_t min_sz(size_t a, size_t b) { return a < b ? a : b; }
+
+static int check_codec_sizes(int n_outer, int n_tokens, int H, int d, int group, int t_cap, int t_offset) {
+    if (d != 16 && d != 32 && d != 64 && d != 128 && d != 256) return invalid("d must be one of 16, 32, 64, 128, 256 (got %d)", d);
+    if (!pow2(group) || group < 16 || group > d) return invalid("group must be a power of two with 16 <= group <= d (got %d)", group);
+    if (n_outer < 0 || n_tokens < 0 || H <= 0) return invalid("n_outer, n_tokens must be >= 0 and H > 0");
+    if (t_offset < 0 || t_cap < 0 || (long long)t_offset + n_tokens > t_cap)
+        return invalid("need 0 <= t_offset and t_offset + n_tokens <= t_cap (t_offset=%d n_tokens=%d t_cap=%d)", t_offset,
+                       n_tokens, t_cap);
+    const long long rows = (long long)n_tokens * H, crow = (long long)t_cap * H;
+    if (rows > (1ll << 31) - 64 || crow > (1ll << 31) - 64 || (long long)n_outer * ((rows + 31) / 32) * 2 > (1ll << 31) - 1)
+        return invalid("sizes too large for 32-bit tile indexing");
+    return SRFTKV_OK;
+}
+
+static int check_side(const srftkv_side* s, const char* name, int d, int group, bool need_x) {
+    if (s->bits != 4 && s->bits != 8) return invalid("%s: bits must be 4 or 8 (got %d)", name, s->bits);
+    if (!s->codes || !s->scales) return invalid("%s: codes and scales must not be NULL", name);
+    if (need_x && !s->x) return invalid("%s: x must not be NULL", name);
+    const size_t crow = (size_t)d * s->bits / 8, srow = (size_t)(d / group) * 4;
+    if (!aligned(s->codes, min_sz(16, crow))) return invalid("%s: codes must be %zu-byte aligned", name, min_sz(16, crow));
+    if (!aligned(s->scales, min_sz(16, srow))) return invalid("%s: scales must be %zu-byte aligned", name, min_sz(16, srow));
+    if (need_x && !aligned(s->x, 16)) return invalid("%s: x must be 16-byte aligned", name);
+    if (s->lambda && (!aligned(s->lambda, 16) || (s->lambda_outer_stride % 4) != 0 || s->lambda_outer_stride < 0))
+        return invalid("%s: lambda must be 16-byte aligned with a non-negative outer stride that is a multiple of 4", name);
+    return SRFTKV_OK;
+}
+
+static int codec_common(const srftkv_side* k, const srftkv_side* v, int n_outer, int n_tokens, int H, int d, int group,
+                        int t_cap, int t_offset, uint64_t seed, void* stream, bool quantize) {
+    int rc = check_codec_sizes(n_outer, n_tokens, H, d, group, t_cap, t_offset);
+    if (rc) return rc;
+    if (!k && !v) return invalid("at least one of k, v must be given");
+    CodecCall c;
+    std::memset(&c, 0, sizeof(c));
+    c.n_sides = 0;
+    const srftkv_side* sides[2] = {k, v};
+    const char* names[2] = {"k", "v"};
+    for (int i = 0; i < 2; ++i) {
+        if (!sides[i]) continue;
+        rc = check_side(sides[i], names[i], d, group, true);
+        if (rc) return rc;
+        CodecSideDesc& s = c.side[c.n_sides++];
+        s.x = sides[i]->x;
+        s.codes = static_cast<uint8_t*>(sides[i]->codes);
+        s.scales = sides[i]->scales;
+        s.lambda = sides[i]->lambda;
+        s.lambda_outer_stride = sides[i]->lambda_outer_stride;
+        s.bits = sides[i]->bits;
+    }
+    if (n_outer == 0 || n_tokens == 0) return SRFTKV_OK;
+    rc = current_device_ok();
+    if (rc) return rc;
+    c.n_outer = n_outer;
+    c.n_tokens = n_tokens;
+    c.H = H;
+    c.d = d;
+    c.group = group;
+    c.t_cap = t_cap;
+    c.t_offset = t_offset;
+    c.seed = seed;
+    c.stream = static_cast<cudaStream_t>(stream);
+    return quantize ? codec_quantize(c) : codec_dequantize(c);
+}
+
+}  // namespace srftkv
+
+using namespace srftkv;
+
+extern "C" {
+
+int srft_kv_quantize(const srftkv_side* k, const srftkv_side* v, int n_outer, int n_tokens, int H, int d, int group,
+                     int t_cap, int t_offset, uint64_t sign_seed, void* stream) {
+    return codec_common(k, v, n_outer, n_tokens, H, d, group, t_cap, t_offset, sign_seed, stream, true);
+}
+
+int srft_kv_dequantize(const srftkv_side* k, const srftkv_side* v, int n_outer, int n_tokens, int H, int d, int group,
+                       int t_cap, int t_offset, uint64_t sign_seed, void* stream) {
+    return codec_common(k, v, n_outer, n_tokens, H, d, group, t_cap, t_offset, sign_seed, stream, false);
+}
+
+int srft_kv_vector_bytes(int d, int bits, int group, size_t* code_bytes, size_t* scale_bytes) {
+    if (d != 16 && d != 32 && d != 64 && d != 128 && d != 256) return invalid("d must be one of 16, 32, 64, 128, 256");
+    if (bits != 4 && bits != 8) return invalid("bits must be 4 or 8");
+    if (!pow2(group) || group < 16 || group > d) return invalid("group must be a power of two with 16 <= group <= d");
+    if (code_bytes) *code_bytes = (size_t)d * bits / 8;
+    if (scale_bytes) *scale_bytes = (size_t)(d / group) * 4;
+    return SRFTKV_OK;
+}
+
+int srft_transform(const void* x, float* y, int n, int d, uint64_t sign_seed, int inverse, void* stream) {
+    if (d != 16 && d != 32 && d != 64 && d != 128 && d != 256) return invalid("d must be one of 16, 32, 64, 128, 256");
+    if (n < 0) return invalid("n must be >= 0");
+    if (n == 0) return SRFTKV_OK;
+    if (!x || !y) return invalid("x and y must not be NULL");
+    if (!aligned(x, 16) || !aligned(y, 16)) return invalid("x and y must be 16-byte aligned");
+    const int rc = current_device_ok();
+    if (rc) return rc;
+    return transform_launch(x, y, n, d, sign_seed, inverse != 0, static_cast<cudaStream_t>(stream));
+}
+
+const char* srftkv_last_error(void) { return t_err; }
+
+int srftkv_device_fault(unsigned int* fault) {
+    if (!fault) return invalid("fault must not be NULL");
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        set_error("cudaDeviceSynchronize failed");
+        return SRFTKV_ERR_CUDA;
+    }
+    *fault = codec_take_fault();
+    return SRFTKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,232 @@
+"""GPU parity of the codec kernels (quantize, dequantize, bare transform)
+against the fp64 oracle, through the C ABI.
+
+Sizes: the full tiny workload, reduced versions of the Gemma-, Qwen- and
+K8V4-shaped workloads that span many 32-row tiles with ragged tails, and the
+full-size Qwen-shaped and K8V4 caches in the launch configuration the
+benchmark uses, checked on seeded samples of rows.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import srft_oracle as O
+from int8_kv_cache_srft_gb300 import inputs as I
+from tests.parity import assert_codes, assert_dequant_within_step, assert_reconstruction_bound, assert_scales
+
+pytestmark = pytest.mark.gpu
+
+K = None
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    global K
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    import int8_kv_cache_srft_gb300 as mod
+
+    mod.library()
+    K = mod
+    yield
+    assert K.srftkv_device_fault() == 0
+
+
+def _np(t):
+    return t.detach().cpu().numpy()
+
+
+def _quantize_gpu(x_k, x_v, lam_k, lam_v, bits_k, bits_v, group, seed, t_cap=None, t_offset=0, sentinel=0xAB):
+    n_outer, T, H, d = x_k.shape
+    t_cap = T if t_cap is None else t_cap
+    sk = K.alloc_side(n_outer, t_cap, H, d, bits_k, group)
+    sv = K.alloc_side(n_outer, t_cap, H, d, bits_v, group)
+    for s in (sk, sv):
+        s.codes.fill_(sentinel)
+        s.scales.fill_(-1.0)
+    sk.x, sv.x = x_k.cuda(), x_v.cuda()
+    sk.lam = None if lam_k is None else lam_k.cuda()
+    sv.lam = None if lam_v is None else lam_v.cuda()
+    K.srft_kv_quantize(sk, sv, n_outer, T, H, d, group, t_cap, t_offset, seed)
+    torch.cuda.synchronize()
+    return sk, sv
+
+
+def _oracle(x, lam, bits, group, seed):
+    lam_b = None if lam is None else _np(lam)[:, None, :, :]
+    return O.srft_kv_quantize(_np(x).astype(np.float64), lam_b, bits, group, seed), lam_b
+
+
+def _check_side(side, x, lam, bits, group, seed, t_offset=0):
+    T = x.shape[1]
+    enc, lam_b = _oracle(x, lam, bits, group, seed)
+    codes = _np(side.codes)[:, t_offset : t_offset + T]
+    scales = _np(side.scales)[:, t_offset : t_offset + T]
+    assert_scales(scales, enc["scales"])
+    st = assert_codes(codes, enc["r"], bits)
+    return enc, lam_b, st
+
+
+@pytest.mark.parametrize("d", (16, 32, 64, 128, 256))
+@pytest.mark.parametrize("inverse", (False, True))
+def test_transform_matches_oracle(d, inverse):
+    g = torch.Generator().manual_seed(d)
+    n = 1000  # ragged: not a multiple of the 128-thread block
+    x = (torch.randn((n, d), generator=g) * 3).to(torch.float16)
+    y = torch.empty((n, d), dtype=torch.float32, device="cuda")
+    K.srft_transform(x.cuda(), y, n, d, 7, inverse)
+    torch.cuda.synchronize()
+    xd = _np(x).astype(np.float64)
+    ref = O.srft_inverse(xd, 7) if inverse else O.srft_forward(xd, 7)
+    err = np.abs(_np(y) - ref).max(axis=-1)
+    assert np.all(err <= 2e-6 * np.linalg.norm(xd, axis=-1) + 1e-7)
+
+
+def test_tiny_round_trip_workload():
+    w = I.TINY
+    xk, xv = I.kv_side(w, "k"), I.kv_side(w, "v")
+    sk, sv = _quantize_gpu(xk, xv, None, None, 4, 4, w.group, w.sign_seed)
+    for side, x in ((sk, xk), (sv, xv)):
+        enc, _, _ = _check_side(side, x, None, 4, w.group, w.sign_seed)
+        out = torch.empty_like(side.x)
+        dq = K.Side(side.codes, side.scales, 4, x=out)
+        K.srft_kv_dequantize(dq, None, 1, w.tokens, w.kv_heads, w.d, w.group, w.tokens, 0, w.sign_seed)
+        torch.cuda.synchronize()
+        xg = _np(out).astype(np.float64)
+        ref_hat = O.srft_kv_dequantize(enc["codes"], enc["scales"], None, 4, w.group, w.sign_seed)
+        assert_dequant_within_step(xg, ref_hat, enc["scales"], None, w.group)
+        assert_reconstruction_bound(xg, _np(x), enc["scales"], None, w.group)
+        # tight: the GPU decode of the GPU codes against the oracle decode of the same codes
+        ref = O.srft_kv_dequantize(_np(side.codes), _np(side.scales).astype(np.float64), None, 4, w.group, w.sign_seed)
+        assert np.abs(xg - ref).max() <= np.abs(ref).max() * 2.0**-10 + 1e-5
+
+
+CASES = [(d, bits, group, lam) for d in (16, 32, 64, 128, 256) for bits in (4, 8)
+         for group in sorted({16, d}) for lam in (False, True)]
+
+
+@pytest.mark.parametrize("d,bits,group,lam", CASES)
+def test_quantize_dequantize_ragged(d, bits, group, lam):
+    """2 outer x 37 tokens x 3 heads = 111 rows per outer (ragged tiles), written at t_offset 5 of t_cap 50."""
+    w = I.Workload("ragged", n_outer=2, tokens=37, kv_heads=3, d=d, lam=lam, data_seed=d + bits,
+                   outlier_kind="scale", outlier_channels=2, outlier_factor=30.0)
+    xk, xv = I.kv_side(w, "k"), I.kv_side(w, "v")
+    lk, lv = I.lam_table(w, "k"), I.lam_table(w, "v")
+    bits_v = 12 - bits  # the other width on the V side: exercises one launch with mixed widths
+    sk, sv = _quantize_gpu(xk, xv, lk, lv, bits, bits_v, group, 11, t_cap=50, t_offset=5)
+    for side, x, lam_t, b in ((sk, xk, lk, bits), (sv, xv, lv, bits_v)):
+        enc, lam_b, _ = _check_side(side, x, lam_t, b, group, 11, t_offset=5)
+        codes = _np(side.codes)
+        assert (codes[:, :5] == 0xAB).all() and (codes[:, 42:] == 0xAB).all(), "rows outside the window were written"
+        out = torch.empty_like(side.x)
+        dq = K.Side(side.codes, side.scales, b, x=out, lam=side.lam)
+        K.srft_kv_dequantize(dq, None, 2, 37, 3, d, group, 50, 5, 11)
+        torch.cuda.synchronize()
+        lam_full = None if lam_b is None else np.broadcast_to(lam_b, x.shape)
+        ref_hat = O.srft_kv_dequantize(enc["codes"], enc["scales"], lam_b, b, group, 11)
+        assert_dequant_within_step(_np(out), ref_hat, enc["scales"], lam_full, group)
+        assert_reconstruction_bound(_np(out), _np(x), enc["scales"], lam_full, group)
+
+
+def test_zero_rows_and_empty_calls():
+    x = torch.zeros((1, 40, 2, 128), dtype=torch.float16)
+    sk, sv = _quantize_gpu(x, x, None, None, 4, 8, 16, 3)
+    assert not _np(sk.scales).any() and not _np(sk.codes).any()
+    assert not _np(sv.scales).any() and not _np(sv.codes).any()
+    # n_tokens == 0 and n_outer == 0 are no-ops
+    K.srft_kv_quantize(sk, sv, 1, 0, 2, 128, 16, 40, 0, 3)
+    K.srft_kv_quantize(sk, sv, 0, 40, 2, 128, 16, 40, 0, 3)
+    torch.cuda.synchronize()
+    assert not _np(sk.codes).any()
+
+
+def test_gemma_shaped_reduced():
+    w = I.GEMMA
+    xk, xv = I.kv_side(w, "k", n_outer=3, tokens=300), I.kv_side(w, "v", n_outer=3, tokens=300)
+    sk, sv = _quantize_gpu(xk, xv, None, None, 4, 4, 16, w.sign_seed)
+    for side, x in ((sk, xk), (sv, xv)):
+        _check_side(side, x, None, 4, 16, w.sign_seed)
+
+
+def test_qwen_shaped_reduced_with_lambda():
+    w = I.QWEN
+    xk, xv = I.kv_side(w, "k", n_outer=2, tokens=700), I.kv_side(w, "v", n_outer=2, tokens=700)
+    lk, lv = I.lam_table(w, "k", n_outer=2), I.lam_table(w, "v", n_outer=2)
+    sk, sv = _quantize_gpu(xk, xv, lk, lv, 4, 4, 16, w.sign_seed)
+    for side, x, lam in ((sk, xk, lk), (sv, xv, lv)):
+        _check_side(side, x, lam, 4, 16, w.sign_seed)
+
+
+def _sample_rows(n_rows, k, seed):
+    rng = np.random.default_rng(seed)
+    return np.unique(np.concatenate([rng.integers(0, n_rows, k), [0, n_rows - 1]]))
+
+
+def test_qwen_shaped_full_size_sampled():
+    """The full 28 x 32768 x 2 x 128 cache with lambda, quantised in one launch; 3000 sampled rows per side
+    against the oracle, then the dequantised rows within one step and the reconstruction MSE reported."""
+    w = I.QWEN
+    xk, xv = I.kv_side(w, "k", device="cuda"), I.kv_side(w, "v", device="cuda")
+    lk, lv = I.lam_table(w, "k", device="cuda"), I.lam_table(w, "v", device="cuda")
+    n_outer, T, H, d = xk.shape
+    sk, sv = K.alloc_side(n_outer, T, H, d, 4, 16), K.alloc_side(n_outer, T, H, d, 4, 16)
+    sk.x, sv.x, sk.lam, sv.lam = xk, xv, lk, lv
+    K.srft_kv_quantize(sk, sv, n_outer, T, H, d, 16, T, 0, w.sign_seed)
+    outk, outv = torch.empty_like(xk), torch.empty_like(xv)
+    K.srft_kv_dequantize(K.Side(sk.codes, sk.scales, 4, x=outk, lam=lk), K.Side(sv.codes, sv.scales, 4, x=outv, lam=lv),
+                         n_outer, T, H, d, 16, T, 0, w.sign_seed)
+    torch.cuda.synchronize()
+    rows = _sample_rows(n_outer * T * H, 3000, 33)
+    for side, x, lam, out in ((sk, xk, lk, outk), (sv, xv, lv, outv)):
+        xs = _np(x.reshape(-1, d)[rows]).astype(np.float64)
+        o_idx, h_idx = rows // (T * H), rows % H
+        lam_rows = _np(lam)[o_idx, h_idx]
+        enc = O.srft_kv_quantize(xs, lam_rows, 4, 16, w.sign_seed)
+        assert_scales(_np(side.scales.reshape(-1, d // 16)[rows]), enc["scales"])
+        assert_codes(_np(side.codes.reshape(-1, d // 2)[rows]), enc["r"], 4)
+        xg = _np(out.reshape(-1, d)[rows]).astype(np.float64)
+        ref_hat = O.srft_kv_dequantize(enc["codes"], enc["scales"], lam_rows, 4, 16, w.sign_seed)
+        assert_dequant_within_step(xg, ref_hat, enc["scales"], lam_rows, 16)
+        assert_reconstruction_bound(xg, xs, enc["scales"], lam_rows, 16)
+        # reconstruction MSE of the GPU path and of the oracle agree closely
+        mse_gpu, mse_ref = float(((xg - xs) ** 2).mean()), float(((ref_hat - xs) ** 2).mean())
+        assert abs(mse_gpu - mse_ref) <= 0.02 * mse_ref
+
+
+def test_k8v4_append_onto_prebuilt_cache():
+    """7B-like cache: 32 layers x 8192 tokens x 8 heads prebuilt (K int8, V int4), then three single-token
+    appends at t = 8192, 8193, 8194 of a 9216-token cache; earlier rows must not change."""
+    w = I.K8V4
+    n_outer, T, H, d, t_cap = w.n_outer, w.tokens, w.kv_heads, w.d, w.t_cap
+    xk, xv = I.kv_side(w, "k", device="cuda"), I.kv_side(w, "v", device="cuda")
+    sk, sv = K.alloc_side(n_outer, t_cap, H, d, 8, 16), K.alloc_side(n_outer, t_cap, H, d, 4, 16)
+    sk.x, sv.x = xk, xv
+    K.srft_kv_quantize(sk, sv, n_outer, T, H, d, 16, t_cap, 0, w.sign_seed)
+    torch.cuda.synchronize()
+    before_k = sk.codes[:, :T].clone()
+    before_v = sv.scales[:, :T].clone()
+    g = torch.Generator(device="cuda").manual_seed(44)
+    new = []
+    for step in range(3):
+        nk = torch.randn((n_outer, 1, H, d), generator=g, device="cuda").half()
+        nv = torch.randn((n_outer, 1, H, d), generator=g, device="cuda").half()
+        ak, av = K.Side(sk.codes, sk.scales, 8, x=nk), K.Side(sv.codes, sv.scales, 4, x=nv)
+        K.srft_kv_quantize(ak, av, n_outer, 1, H, d, 16, t_cap, T + step, w.sign_seed)
+        new.append((nk, nv))
+    torch.cuda.synchronize()
+    assert torch.equal(before_k, sk.codes[:, :T]) and torch.equal(before_v, sv.scales[:, :T])
+    for step, (nk, nv) in enumerate(new):
+        for side, x, bits in ((sk, nk, 8), (sv, nv, 4)):
+            enc = O.srft_kv_quantize(_np(x).astype(np.float64), None, bits, 16, w.sign_seed)
+            assert_scales(_np(side.scales[:, T + step : T + step + 1]), enc["scales"])
+            assert_codes(_np(side.codes[:, T + step : T + step + 1]), enc["r"], bits)
+    # sampled prefix rows against the oracle
+    rows = _sample_rows(n_outer * T * H, 1000, 45)
+    for side, x, bits in ((sk, xk, 8), (sv, xv, 4)):
+        xs = _np(x.reshape(-1, d)[rows]).astype(np.float64)
+        enc = O.srft_kv_quantize(xs, None, bits, 16, w.sign_seed)
+        o_idx, rem = rows // (T * H), rows % (T * H)
+        crow = (o_idx * t_cap * H + rem)
+        assert_codes(_np(side.codes.reshape(-1, d * bits // 8)[crow]), enc["r"], bits)
+        assert_scales(_np(side.scales.reshape(-1, d // 16)[crow]), enc["scales"])
