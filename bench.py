@@ -1,0 +1,390 @@
+#!/usr/bin/env python3
+"""Benchmark of the SRFT KV-cache hot path on GB300.
+
+One step = one pass of the whole path over the packed-cache decode workload
+(B=16 sequences, 32 query heads, 8 kv heads, d=128, 131072 cached tokens):
+  1. srft_kv_quantize   : encode the whole fp16 K/V cache (2 x 16.8 M head
+                          vectors) to int4 codes + fp32 group-16 scales;
+  2. srft_kv_dequantize : decode it back to fp16;
+  3. q4kv_decode_attention : one decode step of attention for all 512 query
+                          rows, reading the packed cache directly;
+  4. srft_kv_quantize   : append one new token per (sequence, kv head).
+`value` = KV head vectors pushed through the step per second (all ranks).
+Inputs are synthetic (seeded N(0,1) fp16), created on the device before the
+timed region; they are 8.6 GB, far larger than the 129 MB L2, so no flush is
+needed between steps.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs the same workload on its own GPU (weak scaling,
+no data exchange); rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KV vectors quantized/s and q4 decode-attn HBM GB/s (fraction of GB300 peak)"
+WORKLOAD = "packed-cache decode attention B=16 Hq=32 Hkv=8 d=128 T=131072, int4/int4 group 16"
+FALLBACK_HBM = 6800.0
+# algorithmic bytes per unit
+QUANT_BYTES_PER_VEC = 128 * 2 + 64 + 32      # read fp16 row, write int4 codes + 8 fp32 scales
+DEQ_BYTES_PER_VEC = QUANT_BYTES_PER_VEC
+ATTN_BYTES_PER_TOKEN_HEAD = 2 * (64 + 32)    # K and V: codes + scales per (b, t, kv head)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    return FALLBACK_HBM, "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for name in ("codec.cu", "srft_math.cuh", "ptx.cuh"):
+        with open(os.path.join(ROOT, "int8_kv_cache_srft_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(sha: str):
+    """dram bytes per quantize launch from the committed ncu summary, if it was taken on this source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        j = json.load(f)
+    ent = j.get("srft_quantize_kernel")
+    if not ent or ent.get("source_sha") != sha:
+        return None
+    return float(ent["bytes_per_launch_full_workload"])
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU side: the fp64 oracle on a bounded sample of the same workload
+# ---------------------------------------------------------------------------
+def oracle_sample(seconds: float):
+    """Time the oracle's quantize -> dequantize -> attention on slices of the workload (one sequence, one kv head,
+    4 query heads, 1024 tokens per slice) until about `seconds` of CPU time has been spent."""
+    import numpy as np
+    from oracle import srft_oracle as O
+
+    rng = np.random.default_rng(5)
+    d, T, rep = 128, 1024, 4
+    vecs, t0, slices = 0, time.perf_counter(), 0
+    while True:
+        k = rng.standard_normal((1, T, 1, d)).astype(np.float16).astype(np.float64)
+        v = rng.standard_normal((1, T, 1, d)).astype(np.float16).astype(np.float64)
+        q = rng.standard_normal((1, rep, d)).astype(np.float16).astype(np.float64)
+        ek = O.srft_kv_quantize(k, None, 4, 16, 5)
+        ev = O.srft_kv_quantize(v, None, 4, 16, 5)
+        O.srft_kv_dequantize(ek["codes"], ek["scales"], None, 4, 16, 5)
+        O.srft_kv_dequantize(ev["codes"], ev["scales"], None, 4, 16, 5)
+        O.packed_decode_attention(q, {"bits": 4, "codes": ek["codes"], "scales": ek["scales"], "lam": None, "group": 16},
+                                  {"bits": 4, "codes": ev["codes"], "scales": ev["scales"], "lam": None, "group": 16}, 5)
+        vecs += 2 * T
+        slices += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    cores = os.cpu_count()
+    return {"value": vecs / el, "unit": "KV vectors/s", "cores": cores, "kind": "oracle",
+            "sample": f"{slices} slices of 1 sequence x 1 kv head x 1024 tokens x d=128 (K and V quantised, "
+                      f"dequantised and attended by 4 query heads), {el:.1f} s; numpy fp64, BLAS default threads"}
+
+
+def run_reference(args, rank: int, world: int):
+    if rank != 0:
+        return
+    per_step = []
+    for _ in range(args.warmup):
+        oracle_sample(0.0)
+    for _ in range(args.steps):
+        r = oracle_sample(max(0.5, args.cpu_seconds / max(args.steps, 1)))
+        per_step.append(r["value"])
+    val = statistics.median(per_step)
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "KV vectors/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": "oracle slices (see cpu_baseline)"},
+            "cpu_baseline": {"value": val, "unit": "KV vectors/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": r["sample"]},
+            "e2e": {"value": val, "unit": "KV vectors/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU side
+# ---------------------------------------------------------------------------
+def run_ours(args, rank: int, world: int, local_rank: int):
+    import torch
+    import int8_kv_cache_srft_gb300 as K
+    from int8_kv_cache_srft_gb300 import inputs as I
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    K.library()
+    w = I.DECODE
+    B, Hkv, d, T, Hq, G = w.n_outer, w.kv_heads, w.d, w.tokens, w.q_heads, w.group
+    t_cap = T + 64
+    seed = w.sign_seed
+    wd = w.resized(data_seed=w.data_seed + 100 * rank)
+    xk, xv = I.kv_side(wd, "k", device=dev), I.kv_side(wd, "v", device=dev)
+    q = I.query(wd, device=dev)
+    sk, sv = K.alloc_side(B, t_cap, Hkv, d, 4, G, device=dev), K.alloc_side(B, t_cap, Hkv, d, 4, G, device=dev)
+    sk.x, sv.x = xk, xv
+    dk, dv = torch.empty_like(xk), torch.empty_like(xv)
+    deq_k, deq_v = K.Side(sk.codes, sk.scales, 4, x=dk), K.Side(sv.codes, sv.scales, 4, x=dv)
+    g = torch.Generator(device=dev).manual_seed(99 + rank)
+    nk = torch.randn((B, 1, Hkv, d), generator=g, device=dev).half()
+    nv = torch.randn((B, 1, Hkv, d), generator=g, device=dev).half()
+    app_k, app_v = K.Side(sk.codes, sk.scales, 4, x=nk), K.Side(sv.codes, sv.scales, 4, x=nv)
+    seq = torch.full((B,), T, dtype=torch.int32, device=dev)
+    out = torch.empty((B, Hq, d), dtype=torch.float32, device=dev)
+    ws = torch.empty(K.q4kv_decode_attention_workspace_size(B, Hq, Hkv, d, t_cap, 0), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    n_vec = 2 * B * T * Hkv
+    LAUNCHES = 6
+
+    ev = {k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for k in ("quant", "deq", "attn", "append")}
+    times = {k: [] for k in ev}
+
+    def step(timed_parts: bool):
+        if timed_parts:
+            ev["quant"][0].record(stream)
+        K.srft_kv_quantize(sk, sv, B, T, Hkv, d, G, t_cap, 0, seed, stream)
+        if timed_parts:
+            ev["quant"][1].record(stream)
+            ev["deq"][0].record(stream)
+        K.srft_kv_dequantize(deq_k, deq_v, B, T, Hkv, d, G, t_cap, 0, seed, stream)
+        if timed_parts:
+            ev["deq"][1].record(stream)
+            ev["attn"][0].record(stream)
+        K.q4kv_decode_attention(q, out, sk, sv, B, Hq, Hkv, d, G, t_cap, seq, 0.0, seed, 0, ws, stream)
+        if timed_parts:
+            ev["attn"][1].record(stream)
+            ev["append"][0].record(stream)
+        K.srft_kv_quantize(app_k, app_v, B, 1, Hkv, d, G, t_cap, T, seed, stream)
+        if timed_parts:
+            ev["append"][1].record(stream)
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(max(args.warmup, 3)):
+        step(False)
+    torch.cuda.synchronize()
+
+    # per-kernel durations (events on the launching stream), outside the main timed loop
+    for _ in range(10):
+        step(True)
+        torch.cuda.synchronize()
+        for k, (a, b) in ev.items():
+            times[k].append(a.elapsed_time(b))
+
+    clocks = ClockSampler(local_rank)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(False)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier()
+    ms_total = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    value = world * n_vec / (ms_step * 1e-3)
+
+    # fp16-cache comparator: the same attention kernel on the raw fp16 cache
+    raw_k, raw_v = K.Side(xk, None, 16), K.Side(xv, None, 16)
+    ws16 = torch.empty(K.q4kv_decode_attention_workspace_size(B, Hq, Hkv, d, T, 0), dtype=torch.uint8, device=dev)
+    t16 = []
+    for i in range(13):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        K.q4kv_decode_attention(q, out, raw_k, raw_v, B, Hq, Hkv, d, G, T, seq, 0.0, seed, 0, ws16, stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            t16.append(a.elapsed_time(b))
+
+    # end to end through the public API from pinned host memory
+    e2e = None
+    if args.e2e_steps > 0:
+        hk = xk.cpu().pin_memory()
+        hv = xv.cpu().pin_memory()
+        hq = q.cpu().pin_memory()
+        hout = torch.empty_like(out, device="cpu").pin_memory()
+        h2d = hk.numel() * 2 + hv.numel() * 2 + hq.numel() * 2
+        d2h = hout.numel() * 4
+        barrier()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.e2e_steps):
+            xk.copy_(hk, non_blocking=True)
+            xv.copy_(hv, non_blocking=True)
+            q.copy_(hq, non_blocking=True)
+            step(False)
+            hout.copy_(out, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = a.elapsed_time(b) / args.e2e_steps
+        e2e = {"value": world * n_vec / (ms_e2e * 1e-3), "unit": "KV vectors/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e}
+
+    if rank != 0:
+        return
+    med = {k: statistics.median(v) for k, v in times.items()}
+    peak, peak_kind = peaks()
+    quant_bytes = n_vec * QUANT_BYTES_PER_VEC
+    attn_bytes = B * T * Hkv * ATTN_BYTES_PER_TOKEN_HEAD
+    achieved = quant_bytes / (med["quant"] * 1e-3) / 1e9
+    sha = kernel_source_sha()
+    traffic = recorded_traffic(sha)
+    attn_gbs = attn_bytes / (med["attn"] * 1e-3) / 1e9
+    fp16_ms = statistics.median(t16)
+    cpu = None if args.no_cpu else oracle_sample(args.cpu_seconds)
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "KV vectors/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "q_heads": Hq, "kv_heads": Hkv, "head_dim": d, "context": T,
+                   "bits_k": 4, "bits_v": 4, "group": G, "scales": "fp32", "vectors_per_step": n_vec,
+                   "step": "quantize cache + dequantize cache + decode attention + 1-token append",
+                   "l2": "inputs 8.6 GB >> 129 MB L2, no flush needed"},
+        "roofline": {"bound": "hbm", "kernel": "srft_quantize_kernel", "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": quant_bytes},
+        "kernels_ms": med,
+        "quantize": {"vectors_per_s": n_vec / (med["quant"] * 1e-3), "gbs": achieved, "frac": achieved / peak},
+        "dequantize": {"vectors_per_s": n_vec / (med["deq"] * 1e-3),
+                       "gbs": n_vec * DEQ_BYTES_PER_VEC / (med["deq"] * 1e-3) / 1e9,
+                       "frac": n_vec * DEQ_BYTES_PER_VEC / (med["deq"] * 1e-3) / 1e9 / peak},
+        "attention": {"int4_ms": med["attn"], "hbm_gbs": attn_gbs, "frac": attn_gbs / peak,
+                      "frac_of_nominal_8000": attn_gbs / 8000.0, "decode_tokens_per_s": B / (med["attn"] * 1e-3),
+                      "kv_tokens_per_s": B * T / (med["attn"] * 1e-3), "fp16_cache_ms": fp16_ms,
+                      "fp16_cache_gbs": 2 * B * T * Hkv * d * 2 / (fp16_ms * 1e-3) / 1e9,
+                      "int4_speedup_vs_fp16_cache": fp16_ms / med["attn"]},
+        "append_us": med["append"] * 1e3,
+        "gpu_launches": LAUNCHES * args.steps,
+        "clocks": clk,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "kernel_source_sha": sha,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    run_ours(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

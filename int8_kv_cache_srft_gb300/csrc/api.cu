@@ -68,7 +68,7 @@ struct DevInfo {
 static DevInfo g_dev[64];
 static std::mutex g_dev_mu;
 
-static int current_device_ok() {
+int current_device_ok() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
         set_error("no current CUDA device");
@@ -118,6 +118,30 @@ static PFN_cuTensorMapEncodeTiled_v12000 encoder() {
             g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     });
     return g_encode;
+}
+
+bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, void* base, const unsigned long long* dims,
+                  const unsigned long long* strides_bytes, const unsigned* box, const char* what) {
+    auto enc = encoder();
+    if (!enc) {
+        set_error("cuTensorMapEncodeTiled is unavailable from the driver");
+        return false;
+    }
+    cuuint64_t d[5], s[4];
+    cuuint32_t b[5], e[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        e[i] = 1;
+        if (i + 1 < rank) s[i] = strides_bytes[i];
+    }
+    const CUresult r = enc(map, dt, rank, base, d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        set_error("cuTensorMapEncodeTiled failed (CUresult %d) for %s", (int)r, what);
+        return false;
+    }
+    return true;
 }
 
 bool encode_row_map(CUtensorMap* map, void* base, int d, long long rows_per_outer, int n_outer, int box_rows) {
@@ -257,6 +281,17 @@ int srft_transform(const void* x, float* y, int n, int d, uint64_t sign_seed, in
     return transform_launch(x, y, n, d, sign_seed, inverse != 0, static_cast<cudaStream_t>(stream));
 }
 
+int q4kv_decode_attention(const void* q, float* out, const srftkv_side* k, const srftkv_side* v, int B, int Hq, int Hkv,
+                          int d, int group, int t_cap, const int* seq_lens, float sm_scale, uint64_t sign_seed,
+                          int n_splits, void* workspace, size_t workspace_bytes, void* stream) {
+    return attention_entry(q, out, k, v, B, Hq, Hkv, d, group, t_cap, seq_lens, sm_scale, sign_seed, n_splits,
+                           workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+size_t q4kv_decode_attention_workspace_size(int B, int Hq, int Hkv, int d, int t_cap, int n_splits) {
+    return attention_workspace_size(B, Hq, Hkv, d, t_cap, n_splits);
+}
+
 const char* srftkv_last_error(void) { return t_err; }
 
 int srftkv_device_fault(unsigned int* fault) {
@@ -265,7 +300,7 @@ int srftkv_device_fault(unsigned int* fault) {
         set_error("cudaDeviceSynchronize failed");
         return SRFTKV_ERR_CUDA;
     }
-    *fault = codec_take_fault();
+    *fault = codec_take_fault() | (attn_take_fault() << 8);
     return SRFTKV_OK;
 }
 

@@ -1,11 +1,862 @@
-// attention.cu -- placeholder (decode attention is being written)
+// attention.cu -- decode attention that reads the packed SRFT cache directly.
+//
+// Method: "Gemini on-device quantization, KV cache, Apple Silicon", section
+// "Flash Attention and Metal kernel fusion": tiles of tokens with an online
+// softmax, so the T-long score vector never exists in memory.  "When
+// Quantization Is Free ...", Methodology 1: the SRFT R is orthogonal, so
+//   q . k_hat_t = (R q) . (R k_hat_t) = sum_i (R q)_i z_hat_{t,i} / lambda_i
+// and sum_t p_t v_hat_t = R^T (sum_t p_t z_hat^V_t / lambda^V).  The cache is
+// therefore read in its rotated, quantised form: q is rotated once, and the
+// output is rotated back once per (batch, query head), never per token.
+//
+// Three launches per call:
+//   1. prep: q_tilde = SRFT(q) / lambda_K * sm_scale * log2(e) (one thread per row);
+//   2. split: grid (n_splits, B*Hkv).  Each warp streams chunks of tokens of its
+//      split; a TMA copy per plane (codes and scales of K and V) lands each chunk
+//      in shared memory with 16 bytes of padding per row, so the ldmatrix reads
+//      that follow are bank-conflict free.  Codes are turned into exact fp16
+//      integers in registers and contracted on the tensor cores
+//      (mma.sync m16n8k16, fp32 accumulate): S = codes_K . q_tilde per 16-token
+//      tile, the per-group scale applied to the fp32 partial of each group,
+//      then acc += codes_V^T . (p * scale_V).  The GQA query heads of one kv
+//      head share every tile.  Per-warp online softmax states are merged in
+//      shared memory into one partial (m, l, acc) per (query head, split);
+//   3. combine: merge the splits, divide by l and lambda_V, inverse SRFT.
+//
+// The contractions are tiny (4 query heads per kv head), so the tensor cores
+// are used for what they are here: a way to do the 2 x 4 multiply-adds per
+// cached element in very few instructions, leaving the issue slots for the
+// dequantisation bit tricks and the softmax.  The codes are exact in fp16;
+// the other operand (q_tilde, or p * scale_V) is split into two fp16 halves
+// hi + lo and contracted twice, which keeps the products at ~22-bit accuracy.
+#include <cuda_fp16.h>
+
+#include <cmath>
+#include <cstring>
+
 #include "internal.h"
-using namespace srftkv;
-extern "C" {
-int q4kv_decode_attention(const void*, float*, const srftkv_side*, const srftkv_side*, int, int, int, int, int, int,
-                          const int*, float, uint64_t, int, void*, size_t, void*) {
-    set_error("decode attention not built yet");
+#include "ptx.cuh"
+#include "srft_math.cuh"
+
+namespace srftkv {
+
+static __device__ unsigned int g_attn_fault;
+
+constexpr int kAttnWarps = 4;
+
+struct AttnParams {
+    const uint16_t* q;     // fp16 [B][Hq][D]
+    float* qt;             // fp32 [B][Hq][D] prepared queries (workspace)
+    float* part_ml;        // [B*Hq][n_splits][2]  (m, l) in log2 units
+    float* part_acc;       // [B*Hq][n_splits][D]
+    float* out;            // fp32 [B][Hq][D]
+    const int* seq_lens;   // [B] or null
+    const float* lam_k;
+    long long lam_k_stride;
+    const float* lam_v;
+    long long lam_v_stride;
+    int B, Hq, Hkv, rep, t_cap, n_splits, group, log2_group;
+    int sp;                // padded scale row (floats) in shared memory
+    float qscale;          // sm_scale * log2(e)
+    uint32_t sign_mask[128];
+};
+
+// ---------------------------------------------------------------------------
+// Small PTX helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+// D = A . B + D, m16n8k16, fp16 inputs, fp32 accumulators
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t h2_sub(uint32_t x, uint32_t c) {  // exact for the integer values used here
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(c));
+    return r;
+}
+__device__ __forceinline__ uint32_t h2_fma(uint32_t x, uint32_t m, uint32_t c) {
+    uint32_t r;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(m), "r"(c));
+    return r;
+}
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+// (a, b) ~= hi + lo with both halves fp16: the MMA then sees a and b to about
+// 22 bits instead of 11 (codes are exact in fp16, so this is the only rounding
+// of the contraction inputs).
+__device__ __forceinline__ void split_h2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    const __half2 h = __floats2half2_rn(a, b);
+    const float2 f = __half22float2(h);
+    const __half2 l = __floats2half2_rn(a - f.x, b - f.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// Codes -> fp16 integer pairs.  Bits 0xF/0xF0000 (0xF0/0xF00000) hold two
+// two's-complement nibbles; XOR with 8 makes them offset binary, OR-ing the
+// fp16 exponent of 1024 makes the fp16 value 1024 + 8 + q (or 1024 + 16(8+q)),
+// and one f16x2 subtract (fma) gives q exactly.
+__device__ __forceinline__ uint32_t i4_lo(uint32_t w) {  // nibbles at bits 0 and 16
+    return h2_sub((w & 0x000F000Fu) ^ 0x64086408u, 0x64086408u);  // (1032, 1032)
+}
+__device__ __forceinline__ uint32_t i4_hi(uint32_t w) {  // nibbles at bits 4 and 20
+    return h2_fma((w & 0x00F000F0u) ^ 0x64806480u, 0x2C002C00u /* 1/16 */, 0xD480D480u /* -72 */);
+}
+__device__ __forceinline__ uint32_t i8_lo(uint32_t w) {  // bytes 0 and 2
+    return h2_sub((w & 0x00FF00FFu) ^ 0x64806480u, 0x64806480u);  // (1152, 1152)
+}
+__device__ __forceinline__ uint32_t i8_hi(uint32_t w) {  // bytes 1 and 3
+    return i8_lo(w >> 8);
+}
+
+template <int D, int BITS>
+struct PlaneT {
+    static constexpr int RB = D * BITS / 8;  // bytes per cached row
+    static constexpr int RP = RB + 16;       // padded shared-memory row
+};
+
+template <int D, int BK, int BV>
+struct AttnCfg {
+    static constexpr bool QK = BK != 16, QV = BV != 16;
+    static constexpr int SPMAX = D / 16 + 4;                       // padded scale row, floats
+    static constexpr int STAGE32 = 32 * (PlaneT<D, BK>::RP + PlaneT<D, BV>::RP + (QK ? SPMAX * 4 : 0) + (QV ? SPMAX * 4 : 0));
+    static constexpr int CH = STAGE32 <= 9216 ? 32 : 16;           // tokens per chunk
+    static constexpr int OFF_KC = 0;
+    static constexpr int OFF_KS = OFF_KC + CH * PlaneT<D, BK>::RP;
+    static constexpr int OFF_VC = OFF_KS + (QK ? CH * SPMAX * 4 : 0);
+    static constexpr int OFF_VS = OFF_VC + CH * PlaneT<D, BV>::RP;
+    static constexpr int STAGE = ((OFF_VS + (QV ? CH * SPMAX * 4 : 0)) + 127) / 128 * 128;
+    static constexpr int WARP_BYTES = 2 * STAGE;
+    static constexpr int MERGE_BYTES = kAttnWarps * (4 * D + 8) * 4;
+    static constexpr int BODY = kAttnWarps * WARP_BYTES > MERGE_BYTES ? kAttnWarps * WARP_BYTES : MERGE_BYTES;
+    static constexpr int SMEM = 128 + BODY;
+    static constexpr int QB = D / 8;    // K-side B-fragment registers
+    static constexpr int ACC = D / 4;   // V accumulators
+};
+
+// ---------------------------------------------------------------------------
+// 1. q preparation
+// ---------------------------------------------------------------------------
+template <int D, bool ROT>
+__global__ void __launch_bounds__(128) attn_prep_q_kernel(const __grid_constant__ AttnParams P) {
+    constexpr int N = D / 2;
+    const int row = blockIdx.x * 128 + threadIdx.x;
+    if (row >= P.B * P.Hq) return;
+    const int b = row / P.Hq, hq = row - b * P.Hq, hkv = hq / P.rep;
+    const uint4* xr = reinterpret_cast<const uint4*>(P.q + (long long)row * D);
+    float4* yr = reinterpret_cast<float4*>(P.qt + (long long)row * D);
+    float p[D];
+    if constexpr (ROT) {
+        float zr[N], zi[N];
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+            const uint4 v = __ldg(xr + c);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t s = w[e] ^ P.sign_mask[4 * c + e];
+                zr[4 * c + e] = __half2float(__ushort_as_half((unsigned short)(s & 0xFFFFu)));
+                zi[4 * c + e] = __half2float(__ushort_as_half((unsigned short)(s >> 16)));
+            }
+        }
+        fft<N, false>(zr, zi);
+        split_forward<D>(zr, zi, p);
+    } else {
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+            const uint4 v = __ldg(xr + c);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+                p[8 * c + 2 * e] = f.x;
+                p[8 * c + 2 * e + 1] = f.y;
+            }
+        }
+    }
+    if (ROT && P.lam_k != nullptr) {
+        const float4* lr = reinterpret_cast<const float4*>(P.lam_k + (long long)b * P.lam_k_stride + (long long)hkv * D);
+#pragma unroll
+        for (int c = 0; c < D / 4; ++c) {
+            const float4 l = __ldg(lr + c);
+            p[4 * c] *= P.qscale * __frcp_rn(l.x);
+            p[4 * c + 1] *= P.qscale * __frcp_rn(l.y);
+            p[4 * c + 2] *= P.qscale * __frcp_rn(l.z);
+            p[4 * c + 3] *= P.qscale * __frcp_rn(l.w);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < D; ++i) p[i] *= P.qscale;
+    }
+#pragma unroll
+    for (int c = 0; c < D / 4; ++c) yr[c] = make_float4(p[4 * c], p[4 * c + 1], p[4 * c + 2], p[4 * c + 3]);
+}
+
+// ---------------------------------------------------------------------------
+// 2. split kernel
+// ---------------------------------------------------------------------------
+// K-side B fragments (q_tilde in fp16) for this thread: column n = g of the
+// MMA is query head n % 4 of the group.  For 4-bit keys the columns 4..7
+// carry the same heads restricted to the second 16-dim group of each 32-dim
+// chunk (see the k-slot map below), so one MMA yields per-group partials.
+template <int D, int BK>
+__device__ __forceinline__ void build_qb(const float* __restrict__ qrow_base, int rep, int g, int c,
+                                         uint32_t (&qh)[D / 8], uint32_t (&ql)[D / 8]) {
+    const int h = g & 3;
+    const bool head_ok = h < rep;
+    const float* q = qrow_base + (long long)h * D;
+    auto val = [&](int dim, bool ok) -> float { return (ok && head_ok) ? q[dim] : 0.f; };
+    if constexpr (BK == 4) {
+        // chunk m (32 dims), thread c owns dims 8c..8c+7 of the chunk; columns
+        // n < 4 take dims of the first 16 (c < 2), columns n >= 4 the second.
+        const bool ok = (c >> 1) == (g >> 2);
+#pragma unroll
+        for (int m = 0; m < D / 32; ++m) {
+            const int base = 32 * m + 8 * c;
+            split_h2(val(base + 0, ok), val(base + 4, ok), qh[4 * m + 0], ql[4 * m + 0]);
+            split_h2(val(base + 1, ok), val(base + 5, ok), qh[4 * m + 1], ql[4 * m + 1]);
+            split_h2(val(base + 2, ok), val(base + 6, ok), qh[4 * m + 2], ql[4 * m + 2]);
+            split_h2(val(base + 3, ok), val(base + 7, ok), qh[4 * m + 3], ql[4 * m + 3]);
+        }
+    } else if constexpr (BK == 8) {
+        const bool ok = g < 4;
+#pragma unroll
+        for (int m = 0; m < D / 16; ++m) {
+            const int base = 16 * m + 4 * c;
+            split_h2(val(base + 0, ok), val(base + 2, ok), qh[2 * m + 0], ql[2 * m + 0]);
+            split_h2(val(base + 1, ok), val(base + 3, ok), qh[2 * m + 1], ql[2 * m + 1]);
+        }
+    } else {
+        const bool ok = g < 4;
+#pragma unroll
+        for (int j = 0; j < D / 16; ++j) {
+            split_h2(val(16 * j + 2 * c, ok), val(16 * j + 2 * c + 1, ok), qh[2 * j + 0], ql[2 * j + 0]);
+            split_h2(val(16 * j + 8 + 2 * c, ok), val(16 * j + 9 + 2 * c, ok), qh[2 * j + 1], ql[2 * j + 1]);
+        }
+    }
+}
+
+// ldmatrix row address for the 4 matrices (rows tr..tr+7 | tr+8..tr+15) x (seg | seg+1)
+__device__ __forceinline__ uint32_t ldsm_addr(uint32_t base, int rp, int tr, int seg, int lane) {
+    const int mi = lane >> 3;
+    return base + (uint32_t)((tr + (lane & 7) + (mi & 1) * 8) * rp + (seg + (mi >> 1)) * 16);
+}
+// fp16 V (trans): matrices (rows 0-7, seg), (rows 0-7, seg+1), (rows 8-15, seg), (rows 8-15, seg+1)
+__device__ __forceinline__ uint32_t ldsm_addr_v16(uint32_t base, int rp, int tr, int seg, int lane) {
+    const int mi = lane >> 3;
+    return base + (uint32_t)((tr + (lane & 7) + (mi >> 1) * 8) * rp + (seg + (mi & 1)) * 16);
+}
+
+template <int D, int BK, int BV>
+__device__ __forceinline__ void attn_tile(const AttnParams& P, const uint8_t* __restrict__ stage, int tr, int t0, int t_end,
+                                          int lane, const uint32_t (&qh)[D / 8], const uint32_t (&ql)[D / 8],
+                                          float (&acc)[D / 4], float (&m)[2],
+                                          float (&l)[2]) {
+    using C = AttnCfg<D, BK, BV>;
+    const int g = lane >> 2, c = lane & 3;
+    const uint32_t kc = ptx::smem_u32(stage + C::OFF_KC), vc = ptx::smem_u32(stage + C::OFF_VC);
+    const float* ks = reinterpret_cast<const float*>(stage + C::OFF_KS);
+    const float* vs = reinterpret_cast<const float*>(stage + C::OFF_VS);
+    const int sp = P.sp, lg = P.log2_group;
+    constexpr int RPK = PlaneT<D, BK>::RP, RPV = PlaneT<D, BV>::RP;
+
+    // ---- scores S[t][n] for the 16 tokens of the tile ----
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    if constexpr (BK == 4) {
+#pragma unroll
+        for (int m2 = 0; m2 < D / 64; ++m2) {
+            uint32_t r[4];
+            ldsm_x4(ldsm_addr(kc, RPK, tr, 2 * m2, lane), r);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int mm = 2 * m2 + hh;
+                const uint32_t rg = r[2 * hh], rg8 = r[2 * hh + 1];
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
+                const uint32_t x0 = i4_lo(rg), x1 = i4_lo(rg8), x2 = i4_hi(rg), x3 = i4_hi(rg8);
+                mma16816(d, x0, x1, x2, x3, qh[4 * mm], qh[4 * mm + 1]);
+                mma16816(d, x0, x1, x2, x3, ql[4 * mm], ql[4 * mm + 1]);
+                const uint32_t y0 = i4_lo(rg >> 8), y1 = i4_lo(rg8 >> 8), y2 = i4_hi(rg >> 8), y3 = i4_hi(rg8 >> 8);
+                mma16816(d, y0, y1, y2, y3, qh[4 * mm + 2], qh[4 * mm + 3]);
+                mma16816(d, y0, y1, y2, y3, ql[4 * mm + 2], ql[4 * mm + 3]);
+                const int gi = (32 * mm + 16 * (c >> 1)) >> lg;
+                const float s0 = ks[(tr + g) * sp + gi], s1 = ks[(tr + g + 8) * sp + gi];
+                s[0] = fmaf(s0, d[0], s[0]);
+                s[1] = fmaf(s0, d[1], s[1]);
+                s[2] = fmaf(s1, d[2], s[2]);
+                s[3] = fmaf(s1, d[3], s[3]);
+            }
+        }
+    } else if constexpr (BK == 8) {
+#pragma unroll
+        for (int m2 = 0; m2 < D / 32; ++m2) {
+            uint32_t r[4];
+            ldsm_x4(ldsm_addr(kc, RPK, tr, 2 * m2, lane), r);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int mm = 2 * m2 + hh;
+                const uint32_t rg = r[2 * hh], rg8 = r[2 * hh + 1];
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
+                const uint32_t x0 = i8_lo(rg), x1 = i8_lo(rg8), x2 = i8_hi(rg), x3 = i8_hi(rg8);
+                mma16816(d, x0, x1, x2, x3, qh[2 * mm], qh[2 * mm + 1]);
+                mma16816(d, x0, x1, x2, x3, ql[2 * mm], ql[2 * mm + 1]);
+                const int gi = (16 * mm) >> lg;
+                const float s0 = ks[(tr + g) * sp + gi], s1 = ks[(tr + g + 8) * sp + gi];
+                s[0] = fmaf(s0, d[0], s[0]);
+                s[1] = fmaf(s0, d[1], s[1]);
+                s[2] = fmaf(s1, d[2], s[2]);
+                s[3] = fmaf(s1, d[3], s[3]);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < D / 16; ++j) {
+            uint32_t r[4];
+            ldsm_x4(ldsm_addr(kc, RPK, tr, 2 * j, lane), r);
+            mma16816(s, r[0], r[1], r[2], r[3], qh[2 * j], qh[2 * j + 1]);
+            mma16816(s, r[0], r[1], r[2], r[3], ql[2 * j], ql[2 * j + 1]);
+        }
+    }
+    // the two column halves (groups of a chunk, or heads and zero padding) -> full scores
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s[i] += __shfl_xor_sync(0xffffffffu, s[i], 2);
+    const bool v0 = t0 + g < t_end, v1 = t0 + g + 8 < t_end;
+    if (!v0) s[0] = s[1] = -INFINITY;
+    if (!v1) s[2] = s[3] = -INFINITY;
+
+    // ---- online softmax for heads h0 = 2(c%2), h0+1 ----
+    float mt0 = fmaxf(s[0], s[2]), mt1 = fmaxf(s[1], s[3]);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        mt0 = fmaxf(mt0, __shfl_xor_sync(0xffffffffu, mt0, off));
+        mt1 = fmaxf(mt1, __shfl_xor_sync(0xffffffffu, mt1, off));
+    }
+    const float mn0 = fmaxf(m[0], mt0), mn1 = fmaxf(m[1], mt1);
+    if (__any_sync(0xffffffffu, (mn0 > m[0]) || (mn1 > m[1]))) {
+        const float f0 = (mn0 == -INFINITY) ? 1.f : exp2f(m[0] - mn0);
+        const float f1 = (mn1 == -INFINITY) ? 1.f : exp2f(m[1] - mn1);
+        l[0] *= f0;
+        l[1] *= f1;
+#pragma unroll
+        for (int i = 0; i < D / 4; i += 2) {
+            acc[i] *= f0;
+            acc[i + 1] *= f1;
+        }
+        m[0] = mn0;
+        m[1] = mn1;
+    }
+    // p in [0, 256]: the +8 keeps p * scale_V clear of fp16 subnormals; it cancels in acc / l
+    const float b0 = (m[0] == -INFINITY) ? 0.f : m[0] - 8.f, b1 = (m[1] == -INFINITY) ? 0.f : m[1] - 8.f;
+    const float p0 = exp2f(s[0] - b0), p1 = exp2f(s[1] - b1), p2 = exp2f(s[2] - b0), p3 = exp2f(s[3] - b1);
+    l[0] += p0 + p2;
+    l[1] += p1 + p3;
+
+    // ---- P into the B layout: thread (g, c) needs head g%4 for tokens 2c+e+8f ----
+    const float o0 = (c < 2) ? p0 : p1, o1 = (c < 2) ? p2 : p3;  // offered head: [0,2,1,3][c]
+    const int hd = g & 3;
+    const int src_c = ((hd & 1) << 1) | (hd >> 1);
+    const float P00 = __shfl_sync(0xffffffffu, o0, 4 * (2 * c) + src_c);
+    const float P10 = __shfl_sync(0xffffffffu, o0, 4 * (2 * c + 1) + src_c);
+    const float P01 = __shfl_sync(0xffffffffu, o1, 4 * (2 * c) + src_c);
+    const float P11 = __shfl_sync(0xffffffffu, o1, 4 * (2 * c + 1) + src_c);
+    const bool hok = hd < P.rep;
+    const bool w00 = hok && (t0 + 2 * c < t_end), w10 = hok && (t0 + 2 * c + 1 < t_end);
+    const bool w01 = hok && (t0 + 2 * c + 8 < t_end), w11 = hok && (t0 + 2 * c + 9 < t_end);
+
+    // ---- acc += V^T P (rotated domain) ----
+    if constexpr (BV == 4) {
+        const int side = g >> 2;
+#pragma unroll
+        for (int cb2 = 0; cb2 < D / 64; ++cb2) {
+            uint32_t r[4];
+            ldsm_x4_t(ldsm_addr(vc, RPV, tr, 2 * cb2, lane), r);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int cb = 2 * cb2 + hh;
+                const int gv = (32 * cb + 16 * side) >> lg;
+                const float* vsr = vs + (tr + 2 * c) * sp + gv;
+                uint32_t bh0, bl0, bh1, bl1;
+                split_h2(w00 ? P00 * vsr[0] : 0.f, w10 ? P10 * vsr[sp] : 0.f, bh0, bl0);
+                split_h2(w01 ? P01 * vsr[8 * sp] : 0.f, w11 ? P11 * vsr[9 * sp] : 0.f, bh1, bl1);
+                const uint32_t R0 = r[2 * hh], R1 = r[2 * hh + 1];
+                float(&a0)[4] = *reinterpret_cast<float(*)[4]>(&acc[8 * cb]);
+                float(&a1)[4] = *reinterpret_cast<float(*)[4]>(&acc[8 * cb + 4]);
+                const uint32_t x0 = i4_lo(R0), x1 = i4_hi(R0), x2 = i4_lo(R1), x3 = i4_hi(R1);
+                mma16816(a0, x0, x1, x2, x3, bh0, bh1);
+                mma16816(a0, x0, x1, x2, x3, bl0, bl1);
+                const uint32_t y0 = i4_lo(R0 >> 8), y1 = i4_hi(R0 >> 8), y2 = i4_lo(R1 >> 8), y3 = i4_hi(R1 >> 8);
+                mma16816(a1, y0, y1, y2, y3, bh0, bh1);
+                mma16816(a1, y0, y1, y2, y3, bl0, bl1);
+            }
+        }
+    } else if constexpr (BV == 8) {
+#pragma unroll
+        for (int s2 = 0; s2 < D / 32; ++s2) {
+            uint32_t r[4];
+            ldsm_x4_t(ldsm_addr(vc, RPV, tr, 2 * s2, lane), r);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int cb = 2 * s2 + hh;
+                const int gv = (16 * cb) >> lg;
+                const float* vsr = vs + (tr + 2 * c) * sp + gv;
+                const bool cok = g < 4;
+                uint32_t bh0, bl0, bh1, bl1;
+                split_h2((cok && w00) ? P00 * vsr[0] : 0.f, (cok && w10) ? P10 * vsr[sp] : 0.f, bh0, bl0);
+                split_h2((cok && w01) ? P01 * vsr[8 * sp] : 0.f, (cok && w11) ? P11 * vsr[9 * sp] : 0.f, bh1, bl1);
+                const uint32_t R0 = r[2 * hh], R1 = r[2 * hh + 1];
+                float(&a0)[4] = *reinterpret_cast<float(*)[4]>(&acc[4 * cb]);
+                const uint32_t x0 = i8_lo(R0), x1 = i8_hi(R0), x2 = i8_lo(R1), x3 = i8_hi(R1);
+                mma16816(a0, x0, x1, x2, x3, bh0, bh1);
+                mma16816(a0, x0, x1, x2, x3, bl0, bl1);
+            }
+        }
+    } else {
+        const bool cok = g < 4;
+        uint32_t bh0, bl0, bh1, bl1;
+        split_h2((cok && w00) ? P00 : 0.f, (cok && w10) ? P10 : 0.f, bh0, bl0);
+        split_h2((cok && w01) ? P01 : 0.f, (cok && w11) ? P11 : 0.f, bh1, bl1);
+        // raw fp16 rows past the sequence end may hold anything: zero them in the A operand
+        const bool tail = t0 + 16 > t_end;
+        const uint32_t mlo = (t0 + 2 * c < t_end ? 0x0000FFFFu : 0u) | (t0 + 2 * c + 1 < t_end ? 0xFFFF0000u : 0u);
+        const uint32_t mhi = (t0 + 2 * c + 8 < t_end ? 0x0000FFFFu : 0u) | (t0 + 2 * c + 9 < t_end ? 0xFFFF0000u : 0u);
+#pragma unroll
+        for (int j = 0; j < D / 16; ++j) {
+            uint32_t r[4];
+            ldsm_x4_t(ldsm_addr_v16(vc, RPV, tr, 2 * j, lane), r);
+            if (tail) {
+                r[0] &= mlo;
+                r[1] &= mlo;
+                r[2] &= mhi;
+                r[3] &= mhi;
+            }
+            float(&a0)[4] = *reinterpret_cast<float(*)[4]>(&acc[4 * j]);
+            mma16816(a0, r[0], r[1], r[2], r[3], bh0, bh1);
+            mma16816(a0, r[0], r[1], r[2], r[3], bl0, bl1);
+        }
+    }
+}
+
+// Where accumulator entry i of thread (g, c) lives: dim and head (column) and
+// whether it is meaningful.
+template <int D, int BV>
+__device__ __forceinline__ void acc_coord(int i, int g, int c, int& dim, int& head, bool& useful) {
+    const int e = i & 3;
+    const int col = 2 * c + (e & 1);
+    head = col & 3;
+    if constexpr (BV == 4) {
+        const int cb = i >> 3, j = (i >> 2) & 1;
+        dim = 32 * cb + 4 * g + 2 * j + (e >> 1);
+        useful = (g < 4) == (c < 2);
+    } else if constexpr (BV == 8) {
+        const int cb = i >> 2;
+        dim = 16 * cb + 2 * g + (e >> 1);
+        useful = c < 2;
+    } else {
+        const int j = i >> 2;
+        dim = 16 * j + g + 8 * (e >> 1);
+        useful = c < 2;
+    }
+}
+
+template <int D, int BK, int BV>
+__global__ void __launch_bounds__(kAttnWarps * 32, 3)
+    q4kv_attn_split_kernel(const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_ks,
+                           const __grid_constant__ CUtensorMap tm_vc, const __grid_constant__ CUtensorMap tm_vs,
+                           const __grid_constant__ AttnParams P) {
+    using C = AttnCfg<D, BK, BV>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+    const int bh = blockIdx.y, b = bh / P.Hkv, hkv = bh - b * P.Hkv;
+    const int split = blockIdx.x;
+    const int L = P.seq_lens ? min(max(P.seq_lens[b], 0), P.t_cap) : P.t_cap;
+    const int n_chunks = (L + C::CH - 1) / C::CH;
+    const int cps = (n_chunks + P.n_splits - 1) / P.n_splits;
+    const int c_begin = split * cps, c_end = min(c_begin + cps, n_chunks);
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+    uint8_t* wbase = smem + 128 + warp * C::WARP_BYTES;
+    const uint32_t bar0 = ptx::smem_u32(&bars[2 * warp]), bar1 = ptx::smem_u32(&bars[2 * warp + 1]);
+    if (lane == 0) {
+        ptx::mbar_init(bar0, 1);
+        ptx::mbar_init(bar1, 1);
+        ptx::fence_barrier_init();
+    }
+    __syncwarp();
+
+    uint32_t qh[C::QB], ql[C::QB];
+    build_qb<D, BK>(P.qt + ((long long)b * P.Hq + (long long)hkv * P.rep) * D, P.rep, g, c, qh, ql);
+    float acc[C::ACC];
+#pragma unroll
+    for (int i = 0; i < C::ACC; ++i) acc[i] = 0.f;
+    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+
+    const int row_base = b * P.t_cap;
+    const uint32_t kc_bytes = C::CH * PlaneT<D, BK>::RP, vc_bytes = C::CH * PlaneT<D, BV>::RP;
+    const uint32_t sc_bytes = C::CH * P.sp * 4;
+    const uint32_t tx = kc_bytes + vc_bytes + (C::QK ? sc_bytes : 0) + (C::QV ? sc_bytes : 0);
+    auto issue = [&](int chunk, int st) {
+        const uint32_t bar = st ? bar1 : bar0;
+        uint8_t* dst = wbase + st * C::STAGE;
+        const int row = row_base + chunk * C::CH;
+        ptx::mbar_arrive_expect_tx(bar, tx);
+        ptx::tma_load_3d(ptx::smem_u32(dst + C::OFF_KC), &tm_kc, bar, 0, hkv, row);
+        if constexpr (C::QK) ptx::tma_load_3d(ptx::smem_u32(dst + C::OFF_KS), &tm_ks, bar, 0, hkv, row);
+        ptx::tma_load_3d(ptx::smem_u32(dst + C::OFF_VC), &tm_vc, bar, 0, hkv, row);
+        if constexpr (C::QV) ptx::tma_load_3d(ptx::smem_u32(dst + C::OFF_VS), &tm_vs, bar, 0, hkv, row);
+    };
+
+    int chunk = c_begin + warp;
+    if (lane == 0 && chunk < c_end) issue(chunk, 0);
+    bool failed = false;
+    for (int it = 0; chunk < c_end; ++it, chunk += kAttnWarps) {
+        const int st = it & 1;
+        const bool has_next = chunk + kAttnWarps < c_end;
+        if (lane == 0 && has_next) issue(chunk + kAttnWarps, st ^ 1);
+        const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(st ? bar1 : bar0, (it >> 1) & 1));
+        if (!ok) {
+            if (lane == 0) {
+                atomicOr(&g_attn_fault, 1u);
+                if (has_next) ptx::mbar_wait_bounded(st ? bar0 : bar1, ((it + 1) >> 1) & 1, 1u << 16);
+            }
+            failed = true;
+            break;
+        }
+        const uint8_t* stage = wbase + st * C::STAGE;
+        const int tok0 = chunk * C::CH;
+#pragma unroll 1
+        for (int tr = 0; tr < C::CH; tr += 16) {
+            if (tok0 + tr >= L) break;
+            attn_tile<D, BK, BV>(P, stage, tr, tok0 + tr, L, lane, qh, ql, acc, m, l);
+        }
+        __syncwarp();
+    }
+    // the failure flag is per warp; every warp still joins the merge below
+    if (failed) {
+        m[0] = m[1] = -INFINITY;
+        l[0] = l[1] = 0.f;
+#pragma unroll
+        for (int i = 0; i < C::ACC; ++i) acc[i] = 0.f;
+    }
+
+    // ---- per-warp totals of l over the 8 token rows ----
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
+        l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
+    }
+    __syncthreads();  // all warps are done with their stage buffers
+    float* mw = reinterpret_cast<float*>(smem + 128);          // [warps][4][2]
+    float* aw = mw + kAttnWarps * 8;                            // [warps][4][D]
+    if (g == 0 && c < 2) {
+        mw[warp * 8 + (2 * c) * 2 + 0] = m[0];
+        mw[warp * 8 + (2 * c) * 2 + 1] = l[0];
+        mw[warp * 8 + (2 * c + 1) * 2 + 0] = m[1];
+        mw[warp * 8 + (2 * c + 1) * 2 + 1] = l[1];
+    }
+#pragma unroll
+    for (int i = 0; i < C::ACC; ++i) {
+        int dim, head;
+        bool useful;
+        acc_coord<D, BV>(i, g, c, dim, head, useful);
+        if (useful) aw[(warp * 4 + head) * D + dim] = acc[i];
+    }
+    __syncthreads();
+    const long long prow0 = ((long long)b * P.Hq + (long long)hkv * P.rep);
+    for (int idx = threadIdx.x; idx < P.rep * D; idx += blockDim.x) {
+        const int h = idx / D, dim = idx - h * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, mw[w * 8 + h * 2]);
+        float Lsum = 0.f, A = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kAttnWarps; ++w) {
+                const float f = exp2f(mw[w * 8 + h * 2] - M);
+                Lsum += f * mw[w * 8 + h * 2 + 1];
+                A += f * aw[(w * 4 + h) * D + dim];
+            }
+        }
+        const long long pidx = (prow0 + h) * P.n_splits + split;
+        P.part_acc[pidx * D + dim] = A;
+        if (dim == 0) {
+            P.part_ml[pidx * 2] = M;
+            P.part_ml[pidx * 2 + 1] = Lsum;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// 3. combine
+// ---------------------------------------------------------------------------
+template <int D, bool ROT>
+__global__ void __launch_bounds__(128) attn_combine_kernel(const __grid_constant__ AttnParams P) {
+    constexpr int N = D / 2, PER = D / 32;
+    __shared__ float rows[4][D];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row = blockIdx.x * 4 + warp;  // (b, hq)
+    const bool active = row < P.B * P.Hq;
+    if (active) {
+        const float* ml = P.part_ml + (long long)row * P.n_splits * 2;
+        const float* ac = P.part_acc + (long long)row * P.n_splits * D;
+        float M = -INFINITY;
+        for (int s = 0; s < P.n_splits; ++s) M = fmaxf(M, ml[2 * s]);
+        float Lsum = 0.f, o[PER];
+#pragma unroll
+        for (int j = 0; j < PER; ++j) o[j] = 0.f;
+        if (M != -INFINITY) {
+            for (int s = 0; s < P.n_splits; ++s) {
+                const float f = exp2f(ml[2 * s] - M);
+                Lsum += f * ml[2 * s + 1];
+#pragma unroll
+                for (int j = 0; j < PER; ++j) o[j] += f * ac[(long long)s * D + lane * PER + j];
+            }
+        }
+        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+        const int b = row / P.Hq, hkv = (row - b * P.Hq) / P.rep;
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+            float v = o[j] * inv;
+            if (ROT && P.lam_v != nullptr)
+                v *= __frcp_rn(P.lam_v[(long long)b * P.lam_v_stride + (long long)hkv * D + lane * PER + j]);
+            rows[warp][lane * PER + j] = v;
+        }
+    }
+    __syncwarp();
+    if (!active) return;
+    if constexpr (!ROT) {
+#pragma unroll
+        for (int j = 0; j < PER; ++j) P.out[(long long)row * D + lane * PER + j] = rows[warp][lane * PER + j];
+    } else {
+        if (lane != 0) return;
+        float p[D], zr[N], zi[N];
+#pragma unroll
+        for (int i = 0; i < D; ++i) p[i] = rows[warp][i];
+        split_inverse<D>(p, zr, zi);
+        fft<N, true>(zr, zi);
+        float4* yr = reinterpret_cast<float4*>(P.out + (long long)row * D);
+#pragma unroll
+        for (int c4 = 0; c4 < D / 4; ++c4) {
+            const int n0 = 2 * c4, n1 = 2 * c4 + 1;
+            const float a = u2f(f2u(zr[n0]) ^ ((P.sign_mask[n0] & 0x8000u) << 16));
+            const float bq = u2f(f2u(zi[n0]) ^ (P.sign_mask[n0] & 0x80000000u));
+            const float cc = u2f(f2u(zr[n1]) ^ ((P.sign_mask[n1] & 0x8000u) << 16));
+            const float dd = u2f(f2u(zi[n1]) ^ (P.sign_mask[n1] & 0x80000000u));
+            yr[c4] = make_float4(a, bq, cc, dd);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+static bool encode_plane(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int inner_elems, int elem_bytes,
+                         int box_inner, int Hkv, long long rows, int box_rows) {
+    const unsigned long long dims[3] = {(unsigned long long)inner_elems, (unsigned long long)Hkv,
+                                        (unsigned long long)rows};
+    const unsigned long long strides[2] = {(unsigned long long)inner_elems * elem_bytes,
+                                           (unsigned long long)inner_elems * elem_bytes * Hkv};
+    const unsigned box[3] = {(unsigned)box_inner, 1u, (unsigned)box_rows};
+    return encode_tiled(map, dt, 3, const_cast<void*>(base), dims, strides, box, "attention cache plane");
+}
+
+struct AttnLaunch {
+    AttnParams P;
+    const srftkv_side* k;
+    const srftkv_side* v;
+    int d;
+    cudaStream_t stream;
+};
+
+template <int D, int BK, int BV>
+static int launch_split(const AttnLaunch& A) {
+    using C = AttnCfg<D, BK, BV>;
+    const AttnParams& P = A.P;
+    const long long rows = (long long)P.B * P.t_cap;
+    CUtensorMap tkc, tks, tvc, tvs;
+    if (!encode_plane(&tkc, A.k->codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, PlaneT<D, BK>::RB / 4, 4,
+                      PlaneT<D, BK>::RB / 4 + 4, P.Hkv, rows, C::CH))
+        return SRFTKV_ERR_CUDA;
+    if (!encode_plane(&tvc, A.v->codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, PlaneT<D, BV>::RB / 4, 4,
+                      PlaneT<D, BV>::RB / 4 + 4, P.Hkv, rows, C::CH))
+        return SRFTKV_ERR_CUDA;
+    const int ng = D / P.group;
+    tks = tkc;
+    tvs = tvc;
+    if (C::QK && !encode_plane(&tks, A.k->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ng, 4, P.sp, P.Hkv, rows, C::CH))
+        return SRFTKV_ERR_CUDA;
+    if (C::QV && !encode_plane(&tvs, A.v->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ng, 4, P.sp, P.Hkv, rows, C::CH))
+        return SRFTKV_ERR_CUDA;
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(q4kv_attn_split_kernel<D, BK, BV>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        attr = true;
+    }
+    const dim3 grid(P.n_splits, P.B * P.Hkv);
+    q4kv_attn_split_kernel<D, BK, BV><<<grid, kAttnWarps * 32, C::SMEM, A.stream>>>(tkc, tks, tvc, tvs, P);
+    return 0;
+}
+
+template <int D>
+static int launch_all(const AttnLaunch& A) {
+    const AttnParams& P = A.P;
+    const int bk = A.k->bits, bv = A.v->bits;
+    const bool rot = bk != 16;
+    const int rows = P.B * P.Hq;
+    if (rot)
+        attn_prep_q_kernel<D, true><<<(rows + 127) / 128, 128, 0, A.stream>>>(P);
+    else
+        attn_prep_q_kernel<D, false><<<(rows + 127) / 128, 128, 0, A.stream>>>(P);
+    int rc;
+    if (bk == 4 && bv == 4) rc = launch_split<D, 4, 4>(A);
+    else if (bk == 8 && bv == 4) rc = launch_split<D, 8, 4>(A);
+    else if (bk == 4 && bv == 8) rc = launch_split<D, 4, 8>(A);
+    else if (bk == 8 && bv == 8) rc = launch_split<D, 8, 8>(A);
+    else rc = launch_split<D, 16, 16>(A);
+    if (rc) return rc;
+    if (rot)
+        attn_combine_kernel<D, true><<<(rows + 3) / 4, 128, 0, A.stream>>>(P);
+    else
+        attn_combine_kernel<D, false><<<(rows + 3) / 4, 128, 0, A.stream>>>(P);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("attention launch failed: %s", cudaGetErrorString(e));
+        return SRFTKV_ERR_CUDA;
+    }
+    return 0;
+}
+
+static int auto_splits(int B, int Hkv, int t_cap) {
+    const long long pairs = (long long)B * Hkv;
+    const long long target = 8ll * device_sm_count() * 3;  // about eight waves of resident CTAs
+    long long s = (target + pairs - 1) / pairs;
+    const long long max_s = (t_cap + 255) / 256;
+    if (s > max_s) s = max_s;
+    if (s < 1) s = 1;
+    return (int)s;
+}
+
+struct WsLayout {
+    size_t qt, ml, acc, total;
+};
+static WsLayout ws_layout(int B, int Hq, int d, int n_splits) {
+    auto up = [](size_t v) { return (v + 255) / 256 * 256; };
+    WsLayout w;
+    w.qt = 0;
+    w.ml = up((size_t)B * Hq * d * 4);
+    w.acc = w.ml + up((size_t)B * Hq * n_splits * 2 * 4);
+    w.total = w.acc + up((size_t)B * Hq * n_splits * d * 4);
+    return w;
+}
+
+static int invalid_attn(const char* msg) {
+    set_error("%s", msg);
     return SRFTKV_ERR_INVALID;
 }
-size_t q4kv_decode_attention_workspace_size(int, int, int, int, int, int) { return 0; }
+
+int attention_entry(const void* q, float* out, const srftkv_side* k, const srftkv_side* v, int B, int Hq, int Hkv,
+                    int d, int group, int t_cap, const int* seq_lens, float sm_scale, uint64_t seed, int n_splits,
+                    void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (d != 64 && d != 128 && d != 256) return invalid_attn("attention: d must be 64, 128 or 256");
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || t_cap <= 0) return invalid_attn("attention: need B >= 0, Hq, Hkv, t_cap > 0");
+    if (Hq % Hkv) return invalid_attn("attention: Hq must be a multiple of Hkv");
+    if (Hq / Hkv > 4) return invalid_attn("attention: at most 4 query heads per kv head are supported");
+    if (!k || !v || !q || !out) return invalid_attn("attention: q, out, k and v must not be NULL");
+    const bool raw = k->bits == 16 || v->bits == 16;
+    if (raw && (k->bits != 16 || v->bits != 16)) return invalid_attn("attention: bits 16 must be used on both sides");
+    if (!raw && ((k->bits != 4 && k->bits != 8) || (v->bits != 4 && v->bits != 8)))
+        return invalid_attn("attention: bits must be 4, 8 (or 16 on both sides)");
+    if (!raw) {
+        if (group < 16 || (group & (group - 1)) || group > d / 4)
+            return invalid_attn("attention: group must be a power of two with 16 <= group <= d/4");
+        if (!k->scales || !v->scales) return invalid_attn("attention: scales must not be NULL");
+        if ((reinterpret_cast<uintptr_t>(k->scales) | reinterpret_cast<uintptr_t>(v->scales)) & 15)
+            return invalid_attn("attention: scales must be 16-byte aligned");
+        const srftkv_side* sd[2] = {k, v};
+        for (auto s : sd)
+            if (s->lambda && ((reinterpret_cast<uintptr_t>(s->lambda) & 15) || s->lambda_outer_stride < 0 ||
+                              (s->lambda_outer_stride & 3)))
+                return invalid_attn("attention: lambda must be 16-byte aligned with a non-negative stride, multiple of 4");
+    }
+    if (!k->codes || !v->codes) return invalid_attn("attention: codes must not be NULL");
+    if ((reinterpret_cast<uintptr_t>(k->codes) | reinterpret_cast<uintptr_t>(v->codes) |
+         reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15)
+        return invalid_attn("attention: q, out and codes must be 16-byte aligned");
+    if ((long long)B * t_cap > (1ll << 31) - 1) return invalid_attn("attention: B * t_cap too large");
+    if (n_splits < 0) return invalid_attn("attention: n_splits must be >= 0");
+    if (B == 0) return SRFTKV_OK;
+    const int rc0 = current_device_ok();
+    if (rc0) return rc0;
+    const int ns = n_splits ? n_splits : auto_splits(B, Hkv, t_cap);
+    const WsLayout wl = ws_layout(B, Hq, d, ns);
+    if (!workspace || workspace_bytes < wl.total || (reinterpret_cast<uintptr_t>(workspace) & 15)) {
+        set_error("attention: workspace must be 16-byte aligned and hold %zu bytes (got %zu)", wl.total, workspace_bytes);
+        return SRFTKV_ERR_INVALID;
+    }
+    AttnLaunch A;
+    std::memset(&A.P, 0, sizeof(A.P));
+    AttnParams& P = A.P;
+    char* ws = static_cast<char*>(workspace);
+    P.q = static_cast<const uint16_t*>(q);
+    P.qt = reinterpret_cast<float*>(ws + wl.qt);
+    P.part_ml = reinterpret_cast<float*>(ws + wl.ml);
+    P.part_acc = reinterpret_cast<float*>(ws + wl.acc);
+    P.out = out;
+    P.seq_lens = seq_lens;
+    P.lam_k = raw ? nullptr : k->lambda;
+    P.lam_k_stride = k->lambda_outer_stride;
+    P.lam_v = raw ? nullptr : v->lambda;
+    P.lam_v_stride = v->lambda_outer_stride;
+    P.B = B;
+    P.Hq = Hq;
+    P.Hkv = Hkv;
+    P.rep = Hq / Hkv;
+    P.t_cap = t_cap;
+    P.n_splits = ns;
+    P.group = raw ? 16 : group;
+    P.log2_group = 0;
+    while ((1 << P.log2_group) < P.group) ++P.log2_group;
+    P.sp = raw ? 8 : d / P.group + 4;
+    const float sc = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt((float)d);
+    P.qscale = sc * 1.4426950408889634f;
+    sign_masks(d, seed, P.sign_mask);
+    A.k = k;
+    A.v = v;
+    A.d = d;
+    A.stream = stream;
+    switch (d) {
+        case 64: return launch_all<64>(A);
+        case 128: return launch_all<128>(A);
+        default: return launch_all<256>(A);
+    }
 }
+
+size_t attention_workspace_size(int B, int Hq, int Hkv, int d, int t_cap, int n_splits) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || t_cap <= 0 || n_splits < 0 || Hq % Hkv) return 0;
+    const int ns = n_splits ? n_splits : auto_splits(B, Hkv, t_cap);
+    return ws_layout(B, Hq, d, ns).total;
+}
+
+unsigned int attn_take_fault() {
+    unsigned int v = 0, z = 0;
+    cudaMemcpyFromSymbol(&v, g_attn_fault, sizeof(v));
+    cudaMemcpyToSymbol(g_attn_fault, &z, sizeof(z));
+    return v;
+}
+
+}  // namespace srftkv

@@ -47,5 +47,16 @@ unsigned int codec_take_fault();
 
 void set_error(const char* fmt, ...);
 int device_sm_count();
+int current_device_ok();  // SRFTKV_OK, or the error code with the message set
+
+// Generic tiled tensor map (element strides 1); false + message on failure.
+bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, void* base, const unsigned long long* dims,
+                  const unsigned long long* strides_bytes, const unsigned* box, const char* what);
+
+int attention_entry(const void* q, float* out, const srftkv_side* k, const srftkv_side* v, int B, int Hq, int Hkv,
+                    int d, int group, int t_cap, const int* seq_lens, float sm_scale, uint64_t seed, int n_splits,
+                    void* workspace, size_t workspace_bytes, cudaStream_t stream);
+size_t attention_workspace_size(int B, int Hq, int Hkv, int d, int t_cap, int n_splits);
+unsigned int attn_take_fault();
 
 }  // namespace srftkv

@@ -1,0 +1,119 @@
+"""CPU-side checks of the C ABI: the library loads, exports every function the
+header declares, computes the host-only sizes, and rejects bad arguments with
+SRFTKV_ERR_INVALID before touching the GPU (so these run without one)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import int8_kv_cache_srft_gb300 as K
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "srftkv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(K.LIB_PATH):
+        from int8_kv_cache_srft_gb300 import build
+
+        build.build()
+    return K.library()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s+\**([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = header_functions()
+    for n in ("srft_kv_quantize", "srft_kv_dequantize", "q4kv_decode_attention",
+              "q4kv_decode_attention_workspace_size", "srft_kv_vector_bytes", "srft_transform",
+              "srftkv_last_error", "srftkv_device_fault"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in header_functions():
+        assert hasattr(lib, n), f"libsrftkv.so does not export {n}"
+
+
+@pytest.mark.parametrize("d,bits,group,code,scale", [(128, 4, 16, 64, 32), (128, 8, 16, 128, 32), (256, 4, 32, 128, 32),
+                                                     (16, 4, 16, 8, 4), (64, 8, 64, 64, 4)])
+def test_vector_bytes(lib, d, bits, group, code, scale):
+    assert K.srft_kv_vector_bytes(d, bits, group) == (code, scale)
+
+
+@pytest.mark.parametrize("d,bits,group", [(48, 4, 16), (128, 3, 16), (128, 4, 8), (128, 4, 24), (64, 4, 128)])
+def test_vector_bytes_rejects(lib, d, bits, group):
+    with pytest.raises(K.SrftKvError) as e:
+        K.srft_kv_vector_bytes(d, bits, group)
+    assert e.value.code == K.SRFTKV_ERR_INVALID
+
+
+def _side(bits=4, x=16, codes=256, scales=256, lam=None, stride=0):
+    return K._Side(x, lam, stride, bits, codes, scales)
+
+
+def _q(lib, k, v, n_outer=1, n_tokens=4, H=2, d=128, group=16, t_cap=8, t_offset=0):
+    kp = None if k is None else ctypes.pointer(k)
+    vp = None if v is None else ctypes.pointer(v)
+    return lib.srft_kv_quantize(kp, vp, n_outer, n_tokens, H, d, group, t_cap, t_offset, 1, None)
+
+
+@pytest.mark.parametrize("case", [
+    dict(d=100), dict(d=512), dict(group=8), dict(group=48), dict(group=256),
+    dict(t_offset=5), dict(t_offset=-1), dict(n_tokens=-1), dict(H=0),
+])
+def test_quantize_rejects_bad_sizes(lib, case):
+    assert _q(lib, _side(), _side(), **case) == K.SRFTKV_ERR_INVALID
+    assert lib.srftkv_last_error()
+
+
+def test_quantize_rejects_bad_sides(lib):
+    assert _q(lib, None, None) == K.SRFTKV_ERR_INVALID
+    assert _q(lib, _side(bits=3), None) == K.SRFTKV_ERR_INVALID
+    assert _q(lib, _side(codes=0), None) == K.SRFTKV_ERR_INVALID
+    assert _q(lib, _side(codes=8), None) == K.SRFTKV_ERR_INVALID       # misaligned code plane
+    assert _q(lib, _side(scales=4), None) == K.SRFTKV_ERR_INVALID      # misaligned scale plane
+    assert _q(lib, _side(x=0), None) == K.SRFTKV_ERR_INVALID
+    assert _q(lib, _side(lam=4), None) == K.SRFTKV_ERR_INVALID         # misaligned lambda
+    assert _q(lib, _side(lam=16, stride=6), None) == K.SRFTKV_ERR_INVALID
+    # an empty call with valid arguments is a no-op and needs no GPU
+    assert _q(lib, _side(), _side(), n_tokens=0) == K.SRFTKV_OK
+    assert _q(lib, _side(), _side(), n_outer=0) == K.SRFTKV_OK
+
+
+def test_dequantize_rejects_bad_sizes(lib):
+    kp = ctypes.pointer(_side())
+    assert lib.srft_kv_dequantize(kp, None, 1, 9, 2, 128, 16, 8, 0, 1, None) == K.SRFTKV_ERR_INVALID
+
+
+def _attn(lib, k, v, B=2, Hq=8, Hkv=2, d=128, group=16, t_cap=64, ws=16, ws_bytes=1 << 20, q=16, out=16):
+    return lib.q4kv_decode_attention(q, out, ctypes.pointer(k), ctypes.pointer(v), B, Hq, Hkv, d, group, t_cap,
+                                     None, 0.0, 1, 0, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("case", [
+    dict(d=32), dict(Hq=6, Hkv=4), dict(Hq=16, Hkv=2), dict(group=64), dict(t_cap=0), dict(q=0), dict(out=8),
+])
+def test_attention_rejects_bad_arguments(lib, case):
+    assert _attn(lib, _side(), _side(), **case) == K.SRFTKV_ERR_INVALID
+
+
+def test_attention_rejects_mixed_raw_and_packed(lib):
+    assert _attn(lib, _side(bits=16), _side(bits=4)) == K.SRFTKV_ERR_INVALID
+    assert _attn(lib, _side(bits=4), _side(bits=2)) == K.SRFTKV_ERR_INVALID
+
+
+def test_workspace_size_is_monotone_in_splits(lib):
+    f = lib.q4kv_decode_attention_workspace_size
+    s1, s8 = f(16, 32, 8, 128, 131072, 1), f(16, 32, 8, 128, 131072, 8)
+    assert 0 < s1 < s8
+    assert s8 >= 16 * 32 * (128 + 8 * 130) * 4
+    assert f(16, 30, 8, 128, 1024, 1) == 0  # Hq not a multiple of Hkv
