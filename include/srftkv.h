@@ -145,6 +145,36 @@ int q4kv_decode_attention(const void* q, float* out, const srftkv_side* k, const
                           const int* seq_lens, float sm_scale, uint64_t sign_seed, int n_splits,
                           void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * q4kv_decode_attention_static -- q4kv_decode_attention for callers that
+ * cannot allocate device memory.  (The method's pages have no counterpart:
+ * this is a convenience of the library.)
+ *
+ * Some callers cannot allocate the workspace: a runtime that has handed all
+ * device memory to its own pool, a plugin behind a C ABI with no access to
+ * its host framework's allocator, code that cannot afford the implicit
+ * synchronisation of cudaMalloc.  This entry point takes the same arguments
+ * as q4kv_decode_attention without the workspace and uses instead a
+ * file-scope device array of SRFTKV_STATIC_SCRATCH_BYTES bytes that every GPU
+ * loading the library holds until the process exits.  It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *  - Sizes whose workspace (q4kv_decode_attention_workspace_size) exceeds
+ *    SRFTKV_STATIC_SCRATCH_BYTES are rejected with SRFTKV_ERR_INVALID;
+ *    fewer n_splits lowers the need (the automatic choice at B=16, Hq=32,
+ *    d=128 on a 152-SM GB300 needs about 8 MB).
+ *  - The first call on a device looks up the array's device address (once,
+ *    with that device current); make that first call before any stream
+ *    capture.
+ *  - All calls share the one array, which keeps the last call's contents;
+ *    calls whose work overlaps on the GPU (e.g. on two streams) race.
+ *    Nothing in it needs to start zeroed: each call writes all it reads.
+ */
+#define SRFTKV_STATIC_SCRATCH_BYTES (16u << 20)
+int q4kv_decode_attention_static(const void* q, float* out, const srftkv_side* k, const srftkv_side* v,
+                                 int B, int Hq, int Hkv, int d, int group, int t_cap,
+                                 const int* seq_lens, float sm_scale, uint64_t sign_seed, int n_splits,
+                                 void* stream);
+
 /* Bytes of workspace q4kv_decode_attention needs for these sizes (n_splits 0 = the
  * automatic choice on the current device).  Returns 0 for invalid sizes. */
 size_t q4kv_decode_attention_workspace_size(int B, int Hq, int Hkv, int d, int t_cap, int n_splits);

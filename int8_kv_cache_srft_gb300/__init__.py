@@ -59,13 +59,15 @@ def library() -> ctypes.CDLL:
     lib.srft_kv_quantize.argtypes = [sp, sp, i, i, i, i, i, i, i, u64, vp]
     lib.srft_kv_dequantize.argtypes = [sp, sp, i, i, i, i, i, i, i, u64, vp]
     lib.q4kv_decode_attention.argtypes = [vp, vp, sp, sp, i, i, i, i, i, i, vp, ctypes.c_float, u64, i, vp, sz, vp]
+    lib.q4kv_decode_attention_static.argtypes = [vp, vp, sp, sp, i, i, i, i, i, i, vp, ctypes.c_float, u64, i, vp]
     lib.q4kv_decode_attention_workspace_size.argtypes = [i, i, i, i, i, i]
     lib.q4kv_decode_attention_workspace_size.restype = sz
     lib.srft_kv_vector_bytes.argtypes = [i, i, i, ctypes.POINTER(sz), ctypes.POINTER(sz)]
     lib.srft_transform.argtypes = [vp, vp, i, i, u64, i, vp]
     lib.srftkv_last_error.restype = ctypes.c_char_p
     lib.srftkv_device_fault.argtypes = [ctypes.POINTER(ctypes.c_uint)]
-    for name in ("srft_kv_quantize", "srft_kv_dequantize", "q4kv_decode_attention", "srft_kv_vector_bytes",
+    for name in ("srft_kv_quantize", "srft_kv_dequantize", "q4kv_decode_attention", "q4kv_decode_attention_static",
+                 "srft_kv_vector_bytes",
                  "srft_transform", "srftkv_device_fault"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
@@ -144,6 +146,21 @@ def q4kv_decode_attention(q: torch.Tensor, out: torch.Tensor, k: Side, v: Side, 
                                          _ptr(seq_lens), sm_scale, sign_seed, n_splits, _ptr(workspace),
                                          workspace.numel() * workspace.element_size(), _stream(stream))
     _check("q4kv_decode_attention", rc)
+
+
+STATIC_SCRATCH_BYTES = 16 << 20  # SRFTKV_STATIC_SCRATCH_BYTES in include/srftkv.h
+
+
+def q4kv_decode_attention_static(q: torch.Tensor, out: torch.Tensor, k: Side, v: Side, B: int, Hq: int, Hkv: int,
+                                 d: int, group: int, t_cap: int, seq_lens: torch.Tensor | None, sm_scale: float,
+                                 sign_seed: int, n_splits: int, stream=None) -> None:
+    """Decode attention without a caller workspace, for callers that cannot allocate device memory: the
+    library's own fixed-size device array is the scratch (see include/srftkv.h for its size and the rules on
+    overlapping calls)."""
+    rc = library().q4kv_decode_attention_static(_ptr(q), _ptr(out), _sidep(k), _sidep(v), B, Hq, Hkv, d, group,
+                                                t_cap, _ptr(seq_lens), sm_scale, sign_seed, n_splits,
+                                                _stream(stream))
+    _check("q4kv_decode_attention_static", rc)
 
 
 def srft_kv_vector_bytes(d: int, bits: int, group: int) -> tuple[int, int]:
