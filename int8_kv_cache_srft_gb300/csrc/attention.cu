@@ -263,21 +263,21 @@ __device__ __forceinline__ uint32_t ldsm_addr_v16(uint32_t base, int rp, int tr,
     return base + (uint32_t)((tr + (lane & 7) + (mi >> 1) * 8) * rp + (seg + (mi & 1)) * 16);
 }
 
-template <int D, int BK, int BV>
-__device__ __forceinline__ void attn_tile(const AttnParams& P, const uint8_t* __restrict__ stage, int tr, int t0, int t_end,
-                                          int lane, const uint32_t (&qh)[D / 8], const uint32_t (&ql)[D / 8],
-                                          float (&acc)[D / 4], float (&m)[2],
-                                          float (&l)[2]) {
-    using C = AttnCfg<D, BK, BV>;
-    const int g = lane >> 2, c = lane & 3;
-    const uint32_t kc = ptx::smem_u32(stage + C::OFF_KC), vc = ptx::smem_u32(stage + C::OFF_VC);
-    const float* ks = reinterpret_cast<const float*>(stage + C::OFF_KS);
-    const float* vs = reinterpret_cast<const float*>(stage + C::OFF_VS);
-    const int sp = P.sp, lg = P.log2_group;
-    constexpr int RPK = PlaneT<D, BK>::RP, RPV = PlaneT<D, BV>::RP;
+__device__ __forceinline__ float ex2(float x) {  // 2^x; ex2.approx has a relative error of about 2^-22
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
-    // ---- scores S[t][n] for the 16 tokens of the tile ----
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
+// Scores of one 16-token sub-tile at row tr of the stage: s[0..3] for rows
+// (g, g+8) x columns (2c, 2c+1), before the two column halves are combined.
+template <int D, int BK>
+__device__ __forceinline__ void tile_scores(const uint8_t* __restrict__ stage, uint32_t kc, const float* __restrict__ ks,
+                                            int sp, int lg, int tr, int lane, const uint32_t (&qh)[D / 8],
+                                            const uint32_t (&ql)[D / 8], float (&s)[4]) {
+    constexpr int RPK = PlaneT<D, BK>::RP;
+    const int g = lane >> 2, c = lane & 3;
+    s[0] = s[1] = s[2] = s[3] = 0.f;
     if constexpr (BK == 4) {
 #pragma unroll
         for (int m2 = 0; m2 < D / 64; ++m2) {
@@ -332,53 +332,17 @@ __device__ __forceinline__ void attn_tile(const AttnParams& P, const uint8_t* __
             mma16816(s, r[0], r[1], r[2], r[3], ql[2 * j], ql[2 * j + 1]);
         }
     }
-    // the two column halves (groups of a chunk, or heads and zero padding) -> full scores
-#pragma unroll
-    for (int i = 0; i < 4; ++i) s[i] += __shfl_xor_sync(0xffffffffu, s[i], 2);
-    const bool v0 = t0 + g < t_end, v1 = t0 + g + 8 < t_end;
-    if (!v0) s[0] = s[1] = -INFINITY;
-    if (!v1) s[2] = s[3] = -INFINITY;
+}
 
-    // ---- online softmax for heads h0 = 2(c%2), h0+1 ----
-    float mt0 = fmaxf(s[0], s[2]), mt1 = fmaxf(s[1], s[3]);
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        mt0 = fmaxf(mt0, __shfl_xor_sync(0xffffffffu, mt0, off));
-        mt1 = fmaxf(mt1, __shfl_xor_sync(0xffffffffu, mt1, off));
-    }
-    const float mn0 = fmaxf(m[0], mt0), mn1 = fmaxf(m[1], mt1);
-    if (__any_sync(0xffffffffu, (mn0 > m[0]) || (mn1 > m[1]))) {
-        const float f0 = (mn0 == -INFINITY) ? 1.f : exp2f(m[0] - mn0);
-        const float f1 = (mn1 == -INFINITY) ? 1.f : exp2f(m[1] - mn1);
-        l[0] *= f0;
-        l[1] *= f1;
-#pragma unroll
-        for (int i = 0; i < D / 4; i += 2) {
-            acc[i] *= f0;
-            acc[i + 1] *= f1;
-        }
-        m[0] = mn0;
-        m[1] = mn1;
-    }
-    // p in [0, 256]: the +8 keeps p * scale_V clear of fp16 subnormals; it cancels in acc / l
-    const float b0 = (m[0] == -INFINITY) ? 0.f : m[0] - 8.f, b1 = (m[1] == -INFINITY) ? 0.f : m[1] - 8.f;
-    const float p0 = exp2f(s[0] - b0), p1 = exp2f(s[1] - b1), p2 = exp2f(s[2] - b0), p3 = exp2f(s[3] - b1);
-    l[0] += p0 + p2;
-    l[1] += p1 + p3;
-
-    // ---- P into the B layout: thread (g, c) needs head g%4 for tokens 2c+e+8f ----
-    const float o0 = (c < 2) ? p0 : p1, o1 = (c < 2) ? p2 : p3;  // offered head: [0,2,1,3][c]
-    const int hd = g & 3;
-    const int src_c = ((hd & 1) << 1) | (hd >> 1);
-    const float P00 = __shfl_sync(0xffffffffu, o0, 4 * (2 * c) + src_c);
-    const float P10 = __shfl_sync(0xffffffffu, o0, 4 * (2 * c + 1) + src_c);
-    const float P01 = __shfl_sync(0xffffffffu, o1, 4 * (2 * c) + src_c);
-    const float P11 = __shfl_sync(0xffffffffu, o1, 4 * (2 * c + 1) + src_c);
-    const bool hok = hd < P.rep;
-    const bool w00 = hok && (t0 + 2 * c < t_end), w10 = hok && (t0 + 2 * c + 1 < t_end);
-    const bool w01 = hok && (t0 + 2 * c + 8 < t_end), w11 = hok && (t0 + 2 * c + 9 < t_end);
-
-    // ---- acc += V^T P (rotated domain) ----
+// acc += V^T B for one 16-token sub-tile, B[k][n] = p(token k, head n%4) * scale_V.
+// p00..p11 are p for tokens 2c+e+8f of head g%4 (zero for padded heads and for
+// tokens past the end; their scale rows were zeroed in shared memory).
+template <int D, int BV>
+__device__ __forceinline__ void tile_pv(uint32_t vc, const float* __restrict__ vs, int sp, int lg, int tr, int lane,
+                                        float p00, float p10, float p01, float p11, uint32_t amask_lo,
+                                        uint32_t amask_hi, bool tail, float (&acc)[D / 4]) {
+    constexpr int RPV = PlaneT<D, BV>::RP;
+    const int g = lane >> 2, c = lane & 3;
     if constexpr (BV == 4) {
         const int side = g >> 2;
 #pragma unroll
@@ -391,8 +355,8 @@ __device__ __forceinline__ void attn_tile(const AttnParams& P, const uint8_t* __
                 const int gv = (32 * cb + 16 * side) >> lg;
                 const float* vsr = vs + (tr + 2 * c) * sp + gv;
                 uint32_t bh0, bl0, bh1, bl1;
-                split_h2(w00 ? P00 * vsr[0] : 0.f, w10 ? P10 * vsr[sp] : 0.f, bh0, bl0);
-                split_h2(w01 ? P01 * vsr[8 * sp] : 0.f, w11 ? P11 * vsr[9 * sp] : 0.f, bh1, bl1);
+                split_h2(p00 * vsr[0], p10 * vsr[sp], bh0, bl0);
+                split_h2(p01 * vsr[8 * sp], p11 * vsr[9 * sp], bh1, bl1);
                 const uint32_t R0 = r[2 * hh], R1 = r[2 * hh + 1];
                 float(&a0)[4] = *reinterpret_cast<float(*)[4]>(&acc[8 * cb]);
                 float(&a1)[4] = *reinterpret_cast<float(*)[4]>(&acc[8 * cb + 4]);
@@ -405,6 +369,12 @@ __device__ __forceinline__ void attn_tile(const AttnParams& P, const uint8_t* __
             }
         }
     } else if constexpr (BV == 8) {
+        // columns 4..7 carry no head for 8-bit values
+        const float cm = g < 4 ? 1.f : 0.f;
+        p00 *= cm;
+        p10 *= cm;
+        p01 *= cm;
+        p11 *= cm;
 #pragma unroll
         for (int s2 = 0; s2 < D / 32; ++s2) {
             uint32_t r[4];
@@ -414,10 +384,9 @@ __device__ __forceinline__ void attn_tile(const AttnParams& P, const uint8_t* __
                 const int cb = 2 * s2 + hh;
                 const int gv = (16 * cb) >> lg;
                 const float* vsr = vs + (tr + 2 * c) * sp + gv;
-                const bool cok = g < 4;
                 uint32_t bh0, bl0, bh1, bl1;
-                split_h2((cok && w00) ? P00 * vsr[0] : 0.f, (cok && w10) ? P10 * vsr[sp] : 0.f, bh0, bl0);
-                split_h2((cok && w01) ? P01 * vsr[8 * sp] : 0.f, (cok && w11) ? P11 * vsr[9 * sp] : 0.f, bh1, bl1);
+                split_h2(p00 * vsr[0], p10 * vsr[sp], bh0, bl0);
+                split_h2(p01 * vsr[8 * sp], p11 * vsr[9 * sp], bh1, bl1);
                 const uint32_t R0 = r[2 * hh], R1 = r[2 * hh + 1];
                 float(&a0)[4] = *reinterpret_cast<float(*)[4]>(&acc[4 * cb]);
                 const uint32_t x0 = i8_lo(R0), x1 = i8_hi(R0), x2 = i8_lo(R1), x3 = i8_hi(R1);
@@ -426,28 +395,113 @@ __device__ __forceinline__ void attn_tile(const AttnParams& P, const uint8_t* __
             }
         }
     } else {
-        const bool cok = g < 4;
+        const float cm = g < 4 ? 1.f : 0.f;
         uint32_t bh0, bl0, bh1, bl1;
-        split_h2((cok && w00) ? P00 : 0.f, (cok && w10) ? P10 : 0.f, bh0, bl0);
-        split_h2((cok && w01) ? P01 : 0.f, (cok && w11) ? P11 : 0.f, bh1, bl1);
-        // raw fp16 rows past the sequence end may hold anything: zero them in the A operand
-        const bool tail = t0 + 16 > t_end;
-        const uint32_t mlo = (t0 + 2 * c < t_end ? 0x0000FFFFu : 0u) | (t0 + 2 * c + 1 < t_end ? 0xFFFF0000u : 0u);
-        const uint32_t mhi = (t0 + 2 * c + 8 < t_end ? 0x0000FFFFu : 0u) | (t0 + 2 * c + 9 < t_end ? 0xFFFF0000u : 0u);
+        split_h2(p00 * cm, p10 * cm, bh0, bl0);
+        split_h2(p01 * cm, p11 * cm, bh1, bl1);
 #pragma unroll
         for (int j = 0; j < D / 16; ++j) {
             uint32_t r[4];
             ldsm_x4_t(ldsm_addr_v16(vc, RPV, tr, 2 * j, lane), r);
-            if (tail) {
-                r[0] &= mlo;
-                r[1] &= mlo;
-                r[2] &= mhi;
-                r[3] &= mhi;
+            if (tail) {  // raw fp16 rows past the end may hold anything: zero them in the A operand
+                r[0] &= amask_lo;
+                r[1] &= amask_lo;
+                r[2] &= amask_hi;
+                r[3] &= amask_hi;
             }
             float(&a0)[4] = *reinterpret_cast<float(*)[4]>(&acc[4 * j]);
             mma16816(a0, r[0], r[1], r[2], r[3], bh0, bh1);
             mma16816(a0, r[0], r[1], r[2], r[3], bl0, bl1);
         }
+    }
+}
+
+// One chunk of NT 16-token sub-tiles starting at token t0 of the sequence:
+// scores for all NT*16 tokens, one online-softmax update, then P.V.
+template <int D, int BK, int BV, int NT>
+__device__ __forceinline__ void attn_chunk(const AttnParams& P, uint8_t* __restrict__ stage, int t0, int t_end, int lane,
+                                           const uint32_t (&qh)[D / 8], const uint32_t (&ql)[D / 8],
+                                           float (&acc)[D / 4], float (&m)[2], float (&l)[2]) {
+    using C = AttnCfg<D, BK, BV>;
+    const int g = lane >> 2, c = lane & 3;
+    const uint32_t kc = ptx::smem_u32(stage + C::OFF_KC), vc = ptx::smem_u32(stage + C::OFF_VC);
+    float* ks = reinterpret_cast<float*>(stage + C::OFF_KS);
+    float* vs = reinterpret_cast<float*>(stage + C::OFF_VS);
+    const int sp = P.sp, lg = P.log2_group;
+    const int valid = t_end - t0;  // tokens of this chunk inside the sequence (> 0)
+    const bool tail = valid < 16 * NT;
+    if (tail && (C::QK || C::QV)) {
+        // scale rows past the end may hold anything: zero them so they contribute exact zeros
+        for (int i = valid * sp + lane; i < 16 * NT * sp; i += 32) {
+            if (C::QK) ks[i] = 0.f;
+            if (C::QV) vs[i] = 0.f;
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+    }
+
+    float s[NT][4];
+#pragma unroll
+    for (int st = 0; st < NT; ++st) {
+        if (16 * st < valid) tile_scores<D, BK>(stage, kc, ks, sp, lg, 16 * st, lane, qh, ql, s[st]);
+        else s[st][0] = s[st][1] = s[st][2] = s[st][3] = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s[st][i] += __shfl_xor_sync(0xffffffffu, s[st][i], 2);
+        if (16 * st + g >= valid) s[st][0] = s[st][1] = -INFINITY;
+        if (16 * st + g + 8 >= valid) s[st][2] = s[st][3] = -INFINITY;
+    }
+    // ---- online softmax for heads h0 = 2(c%2), h0+1 ----
+    float mt0 = -INFINITY, mt1 = -INFINITY;
+#pragma unroll
+    for (int st = 0; st < NT; ++st) {
+        mt0 = fmaxf(mt0, fmaxf(s[st][0], s[st][2]));
+        mt1 = fmaxf(mt1, fmaxf(s[st][1], s[st][3]));
+    }
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        mt0 = fmaxf(mt0, __shfl_xor_sync(0xffffffffu, mt0, off));
+        mt1 = fmaxf(mt1, __shfl_xor_sync(0xffffffffu, mt1, off));
+    }
+    const float mn0 = fmaxf(m[0], mt0), mn1 = fmaxf(m[1], mt1);
+    if (__any_sync(0xffffffffu, (mn0 > m[0]) || (mn1 > m[1]))) {
+        const float f0 = (mn0 == -INFINITY) ? 1.f : ex2(m[0] - mn0);
+        const float f1 = (mn1 == -INFINITY) ? 1.f : ex2(m[1] - mn1);
+        l[0] *= f0;
+        l[1] *= f1;
+#pragma unroll
+        for (int i = 0; i < D / 4; i += 2) {
+            acc[i] *= f0;
+            acc[i + 1] *= f1;
+        }
+        m[0] = mn0;
+        m[1] = mn1;
+    }
+    // p in [0, 256]: the +8 keeps p * scale_V clear of fp16 subnormals; it cancels in acc / l
+    const float b0 = (m[0] == -INFINITY) ? 0.f : m[0] - 8.f, b1 = (m[1] == -INFINITY) ? 0.f : m[1] - 8.f;
+    // this thread offers head [0,2,1,3][c] of its two token rows to the B layout; padded heads offer zero
+    const int hh = ((c & 1) << 1) | (c >> 1);
+    const bool offer = hh < P.rep;
+    const int hd = g & 3;
+    const int src_c = ((hd & 1) << 1) | (hd >> 1);
+    const uint32_t amask_lo = 0, amask_hi = 0;
+#pragma unroll
+    for (int st = 0; st < NT; ++st) {
+        if (16 * st >= valid) break;
+        const float p0 = ex2(s[st][0] - b0), p1 = ex2(s[st][1] - b1), p2 = ex2(s[st][2] - b0), p3 = ex2(s[st][3] - b1);
+        l[0] += p0 + p2;
+        l[1] += p1 + p3;
+        const float o0 = offer ? ((c < 2) ? p0 : p1) : 0.f, o1 = offer ? ((c < 2) ? p2 : p3) : 0.f;
+        const float P00 = __shfl_sync(0xffffffffu, o0, 4 * (2 * c) + src_c);
+        const float P10 = __shfl_sync(0xffffffffu, o0, 4 * (2 * c + 1) + src_c);
+        const float P01 = __shfl_sync(0xffffffffu, o1, 4 * (2 * c) + src_c);
+        const float P11 = __shfl_sync(0xffffffffu, o1, 4 * (2 * c + 1) + src_c);
+        const int vt = valid - 16 * st;
+        const bool sub_tail = vt < 16;
+        const uint32_t mlo = (2 * c < vt ? 0x0000FFFFu : 0u) | (2 * c + 1 < vt ? 0xFFFF0000u : 0u);
+        const uint32_t mhi = (2 * c + 8 < vt ? 0x0000FFFFu : 0u) | (2 * c + 9 < vt ? 0xFFFF0000u : 0u);
+        (void)amask_lo;
+        (void)amask_hi;
+        tile_pv<D, BV>(vc, vs, sp, lg, 16 * st, lane, P00, P10, P01, P11, mlo, mhi, sub_tail, acc);
     }
 }
 
@@ -537,13 +591,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 3)
             failed = true;
             break;
         }
-        const uint8_t* stage = wbase + st * C::STAGE;
-        const int tok0 = chunk * C::CH;
-#pragma unroll 1
-        for (int tr = 0; tr < C::CH; tr += 16) {
-            if (tok0 + tr >= L) break;
-            attn_tile<D, BK, BV>(P, stage, tr, tok0 + tr, L, lane, qh, ql, acc, m, l);
-        }
+        attn_chunk<D, BK, BV, C::CH / 16>(P, wbase + st * C::STAGE, chunk * C::CH, L, lane, qh, ql, acc, m, l);
         __syncwarp();
     }
     // the failure flag is per warp; every warp still joins the merge below
@@ -587,7 +635,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 3)
         if (M != -INFINITY) {
 #pragma unroll
             for (int w = 0; w < kAttnWarps; ++w) {
-                const float f = exp2f(mw[w * 8 + h * 2] - M);
+                const float f = ex2(mw[w * 8 + h * 2] - M);
                 Lsum += f * mw[w * 8 + h * 2 + 1];
                 A += f * aw[(w * 4 + h) * D + dim];
             }
@@ -621,7 +669,7 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const __grid_constant
         for (int j = 0; j < PER; ++j) o[j] = 0.f;
         if (M != -INFINITY) {
             for (int s = 0; s < P.n_splits; ++s) {
-                const float f = exp2f(ml[2 * s] - M);
+                const float f = ex2(ml[2 * s] - M);
                 Lsum += f * ml[2 * s + 1];
 #pragma unroll
                 for (int j = 0; j < PER; ++j) o[j] += f * ac[(long long)s * D + lane * PER + j];

@@ -1,350 +1,35 @@
-// codec.cu -- the fused SRFT quantize and dequantize kernels, and the bare
-// transform used for testing.
+// codec.cu -- host dispatch of the fused SRFT quantize / dequantize kernels
+// (codec_impl.cuh, instantiated per head dimension in codec_d*.cu), the bare
+// transform kernel used for testing, and the device fault word.
 //
 // Method: "When Quantization Is Free: An int4 KV Cache That Outruns fp16 on
-// Apple Silicon", Methodology 2: one fused kernel per direction doing the
-// sign multiply, the radix-2 Stockham FFT of length d/2, the Hermitian
-// packing, the per-channel lambda, the per-group absmax, the rounding to
-// signed int4/int8 and the nibble packing.  Methodology 3: lambda per
-// coordinate combined with one scale per group of `group` coordinates.
-//
-// GB300 mapping: one thread owns one head vector for the whole pipeline, so
-// the FFT, the group maxima and the packing never leave registers and need
-// no shuffles.  Each warp streams tiles of 32 vectors: a TMA tensor copy
-// brings the fp16 rows into shared memory padded by 16 bytes per row (the
-// box is 8 elements wider than the tensor; the extra columns are the zero
-// fill), which makes the row-per-thread 16-byte reads bank-conflict free.
-// Two buffers per warp overlap the next tile's copy with this tile's math.
-// The dequantize kernel runs the same pipeline backwards and writes its fp16
-// rows through shared memory with a TMA store.
+// Apple Silicon", Methodology 1 (SRFT) and 2 (the fused kernel's steps).
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "internal.h"
-#include "ptx.cuh"
 #include "srft_math.cuh"
 
 namespace srftkv {
 
 static __device__ unsigned int g_codec_fault;
-
-struct CodecSideK {
-    uint8_t* codes;
-    float* scales;
-    const float* lambda;
-    long long lambda_outer_stride;
-    int bits;
-    int pad_;
-};
-
-struct CodecParams {
-    CodecSideK side[2];
-    int n_outer, H, t_cap, t_offset, group;
-    int rows_per_outer;   // n_tokens * H
-    int tiles_per_outer;  // ceil(rows_per_outer / 32)
-    int tiles_per_side;   // n_outer * tiles_per_outer
-    int total_tiles;      // n_sides * tiles_per_side
-    uint32_t sign_mask[128];
-};
+static std::mutex g_fault_mu;
+static unsigned int* g_fault_ptr[64] = {};
 
 template <int D>
-struct Geo {
-    static constexpr int N = D / 2;
-    static constexpr int ROWS = 32;                                       // rows per warp tile
-    static constexpr int PAD = 8;                                         // fp16 elements of row padding
-    static constexpr int ROW_H = (D == 256) ? 2 * (128 + PAD) : D + PAD;  // elements per smem row
-    static constexpr int BUF_BYTES = ROWS * ROW_H * 2;
-    static constexpr int WARPS = 4;
-    static constexpr int SMEM = 128 + WARPS * 2 * BUF_BYTES;
-    static constexpr int MIN_BLOCKS = (D <= 128) ? 3 : 1;
-    // element offset of 16-byte chunk c inside a padded smem row
-    static __device__ __forceinline__ int chunk_off(int c) {
-        return (D == 256) ? (c / 16) * (128 + PAD) + (c % 16) * 8 : c * 8;
-    }
-};
-
-struct TileId {
-    int side, o, row0;
-};
-__device__ __forceinline__ TileId decode_tile(const CodecParams& P, int t) {
-    TileId id;
-    id.side = t / P.tiles_per_side;
-    const int rem = t - id.side * P.tiles_per_side;
-    id.o = rem / P.tiles_per_outer;
-    id.row0 = (rem - id.o * P.tiles_per_outer) * 32;
-    return id;
-}
-
-// ---------------------------------------------------------------------------
-// Quantise one row z (rotated, lambda applied) and store codes and scales.
-// The group maxima are built from 16-coordinate units, widened to the
-// runtime group size by a butterfly over units, so one code path serves
-// every group size; group == 16 (the default) keeps 16-byte scale stores.
-// ---------------------------------------------------------------------------
-template <int D, int BITS>
-__device__ __forceinline__ void quant_store_row(float (&z)[D], int group, uint8_t* __restrict__ crow,
-                                                float* __restrict__ srow) {
-    constexpr int U = D / 16;
-    constexpr float Q = (BITS == 4) ? 7.f : 127.f;
-    constexpr float MAG = kMagic + ((BITS == 4) ? 8.f : 128.f);
-    float m[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        float a = fabs_(z[16 * u]);
-#pragma unroll
-        for (int i = 1; i < 16; ++i) a = fmax_(a, fabs_(z[16 * u + i]));
-        m[u] = a;
-    }
-#pragma unroll
-    for (int s = 1; s < U; s <<= 1) {
-        if (group >= 32 * s) {
-#pragma unroll
-            for (int u = 0; u < U; ++u) m[u] = fmax_(m[u], m[u ^ s]);
-        }
-    }
-    float sc[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const float A = m[u];
-        sc[u] = fdiv_rn(A, Q);
-        const float inv = A > 0.f ? fdiv_rn(Q, A) : 0.f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) z[16 * u + i] = fmaf_(z[16 * u + i], inv, MAG);
-    }
-    constexpr int WORDS = D * BITS / 32;
-    uint32_t w[WORDS];
-#pragma unroll
-    for (int i = 0; i < WORDS; ++i) w[i] = (BITS == 4) ? pack8_int4(&z[8 * i]) : pack4_int8(&z[4 * i]);
-    if constexpr (WORDS >= 4) {
-#pragma unroll
-        for (int i = 0; i < WORDS / 4; ++i)
-            reinterpret_cast<uint4*>(crow)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-    } else {
-        reinterpret_cast<uint2*>(crow)[0] = make_uint2(w[0], w[1]);
-    }
-    if (group == 16) {
-        if constexpr (U >= 4) {
-#pragma unroll
-            for (int i = 0; i < U / 4; ++i)
-                reinterpret_cast<float4*>(srow)[i] = make_float4(sc[4 * i], sc[4 * i + 1], sc[4 * i + 2], sc[4 * i + 3]);
-        } else if constexpr (U == 2) {
-            reinterpret_cast<float2*>(srow)[0] = make_float2(sc[0], sc[1]);
-        } else {
-            srow[0] = sc[0];
-        }
-    } else {
-        const int gu = group >> 4, sh = __ffs(gu) - 1;
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-            if ((u & (gu - 1)) == 0) srow[u >> sh] = sc[u];
-    }
-}
-
-// ---------------------------------------------------------------------------
-// Decode one stored row to rotated coordinates q * scale (lambda not applied).
-// ---------------------------------------------------------------------------
-template <int D, int BITS>
-__device__ __forceinline__ void dequant_load_row(const uint8_t* __restrict__ crow, const float* __restrict__ srow,
-                                                 int group, float (&p)[D]) {
-    constexpr int WORDS = D * BITS / 32, PER = 32 / BITS, U = D / 16;
-    uint32_t w[WORDS];
-    if constexpr (WORDS >= 4) {
-#pragma unroll
-        for (int i = 0; i < WORDS / 4; ++i) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(crow) + i);
-            w[4 * i] = v.x;
-            w[4 * i + 1] = v.y;
-            w[4 * i + 2] = v.z;
-            w[4 * i + 3] = v.w;
-        }
-    } else {
-        const uint2 v = __ldg(reinterpret_cast<const uint2*>(crow));
-        w[0] = v.x;
-        w[1] = v.y;
-    }
-    const int sh = __ffs(group >> 4) - 1;
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const float sc = __ldg(srow + (u >> sh));
-#pragma unroll
-        for (int i = 16 * u; i < 16 * u + 16; ++i) {
-            const float c = (BITS == 4) ? code_int4(w[i / PER], i % PER) : code_int8(w[i / PER], i % PER);
-            p[i] = c * sc;
-        }
-    }
-}
+int launch_codec_d(const CodecCall& c, bool quantize);
+extern template int launch_codec_d<16>(const CodecCall&, bool);
+extern template int launch_codec_d<32>(const CodecCall&, bool);
+extern template int launch_codec_d<64>(const CodecCall&, bool);
+extern template int launch_codec_d<128>(const CodecCall&, bool);
+extern template int launch_codec_d<256>(const CodecCall&, bool);
 
 // fp16 pair (x_{2n}, x_{2n+1}) with the SRFT signs applied -> complex z_n
-__device__ __forceinline__ void signed_pair(uint32_t w, uint32_t mask, float& re, float& im) {
+__device__ __forceinline__ void signed_pair_t(uint32_t w, uint32_t mask, float& re, float& im) {
     const uint32_t s = w ^ mask;
     re = __half2float(__ushort_as_half((unsigned short)(s & 0xFFFFu)));
     im = __half2float(__ushort_as_half((unsigned short)(s >> 16)));
-}
-
-// ---------------------------------------------------------------------------
-// K1: fused quantize
-// ---------------------------------------------------------------------------
-template <int D>
-__device__ __forceinline__ void quantize_tile(const CodecParams& P, const TileId& id, const uint16_t* __restrict__ buf,
-                                              int lane) {
-    using Gm = Geo<D>;
-    constexpr int N = D / 2;
-    const CodecSideK& S = P.side[id.side];
-    const int r = id.row0 + lane;
-    const uint16_t* row = buf + lane * Gm::ROW_H;
-    float zr[N], zi[N];
-#pragma unroll
-    for (int c = 0; c < D / 8; ++c) {
-        const uint4 v = *reinterpret_cast<const uint4*>(row + Gm::chunk_off(c));
-        signed_pair(v.x, P.sign_mask[4 * c + 0], zr[4 * c + 0], zi[4 * c + 0]);
-        signed_pair(v.y, P.sign_mask[4 * c + 1], zr[4 * c + 1], zi[4 * c + 1]);
-        signed_pair(v.z, P.sign_mask[4 * c + 2], zr[4 * c + 2], zi[4 * c + 2]);
-        signed_pair(v.w, P.sign_mask[4 * c + 3], zr[4 * c + 3], zi[4 * c + 3]);
-    }
-    fft<N, false>(zr, zi);
-    float z[D];
-    split_forward<D>(zr, zi, z);
-    if (r >= P.rows_per_outer) return;
-    if (S.lambda != nullptr) {
-        const float4* lr =
-            reinterpret_cast<const float4*>(S.lambda + (long long)id.o * S.lambda_outer_stride + (long long)(r % P.H) * D);
-#pragma unroll
-        for (int c = 0; c < D / 4; ++c) {
-            const float4 l = __ldg(lr + c);
-            z[4 * c] *= l.x;
-            z[4 * c + 1] *= l.y;
-            z[4 * c + 2] *= l.z;
-            z[4 * c + 3] *= l.w;
-        }
-    }
-    const long long vrow = ((long long)id.o * P.t_cap + P.t_offset) * P.H + r;
-    if (S.bits == 4)
-        quant_store_row<D, 4>(z, P.group, S.codes + vrow * (D / 2), S.scales + vrow * (D / P.group));
-    else
-        quant_store_row<D, 8>(z, P.group, S.codes + vrow * D, S.scales + vrow * (D / P.group));
-}
-
-template <int D>
-__global__ void __launch_bounds__(128, Geo<D>::MIN_BLOCKS)
-    srft_quantize_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
-                         const __grid_constant__ CodecParams P) {
-    using Gm = Geo<D>;
-    extern __shared__ __align__(1024) uint8_t smem[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
-    uint8_t* bufs = smem + 128 + warp * 2 * Gm::BUF_BYTES;
-    const uint32_t bar0 = ptx::smem_u32(&bars[2 * warp]), bar1 = ptx::smem_u32(&bars[2 * warp + 1]);
-    if (lane == 0) {
-        ptx::mbar_init(bar0, 1);
-        ptx::mbar_init(bar1, 1);
-        ptx::fence_barrier_init();
-    }
-    __syncwarp();
-    const int stride = gridDim.x * Gm::WARPS;
-    int tile = blockIdx.x * Gm::WARPS + warp;
-    auto issue = [&](int t, int b) {
-        const TileId id = decode_tile(P, t);
-        const CUtensorMap* tm = id.side ? &tm1 : &tm0;
-        const uint32_t bar = b ? bar1 : bar0;
-        const uint32_t dst = ptx::smem_u32(bufs + b * Gm::BUF_BYTES);
-        ptx::mbar_arrive_expect_tx(bar, Gm::BUF_BYTES);
-        if constexpr (D == 256)
-            ptx::tma_load_4d(dst, tm, bar, 0, 0, id.row0, id.o);
-        else
-            ptx::tma_load_3d(dst, tm, bar, 0, id.row0, id.o);
-    };
-    if (lane == 0 && tile < P.total_tiles) issue(tile, 0);
-    for (int it = 0; tile < P.total_tiles; ++it, tile += stride) {
-        const int b = it & 1;
-        const bool has_next = tile + stride < P.total_tiles;
-        if (lane == 0 && has_next) issue(tile + stride, b ^ 1);
-        const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(b ? bar1 : bar0, (it >> 1) & 1));
-        if (!ok) {
-            if (lane == 0) {
-                atomicOr(&g_codec_fault, 1u);
-                if (has_next) ptx::mbar_wait_bounded(b ? bar0 : bar1, ((it + 1) >> 1) & 1, 1u << 16);
-            }
-            return;
-        }
-        quantize_tile<D>(P, decode_tile(P, tile), reinterpret_cast<const uint16_t*>(bufs + b * Gm::BUF_BYTES), lane);
-        __syncwarp();
-    }
-}
-
-// ---------------------------------------------------------------------------
-// K2: fused dequantize
-// ---------------------------------------------------------------------------
-template <int D>
-__global__ void __launch_bounds__(128, Geo<D>::MIN_BLOCKS)
-    srft_dequantize_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
-                           const __grid_constant__ CodecParams P) {
-    using Gm = Geo<D>;
-    constexpr int N = D / 2;
-    extern __shared__ __align__(1024) uint8_t smem[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    uint8_t* bufs = smem + 128 + warp * 2 * Gm::BUF_BYTES;
-    const int stride = gridDim.x * Gm::WARPS;
-    int it = 0;
-    for (int tile = blockIdx.x * Gm::WARPS + warp; tile < P.total_tiles; tile += stride, ++it) {
-        const TileId id = decode_tile(P, tile);
-        const CodecSideK& S = P.side[id.side];
-        const int r = id.row0 + lane;
-        const bool valid = r < P.rows_per_outer;
-        float p[D];
-        if (valid) {
-            const long long vrow = ((long long)id.o * P.t_cap + P.t_offset) * P.H + r;
-            const float* srow = S.scales + vrow * (D / P.group);
-            if (S.bits == 4)
-                dequant_load_row<D, 4>(S.codes + vrow * (D / 2), srow, P.group, p);
-            else
-                dequant_load_row<D, 8>(S.codes + vrow * D, srow, P.group, p);
-            if (S.lambda != nullptr) {
-                const float4* lr = reinterpret_cast<const float4*>(S.lambda + (long long)id.o * S.lambda_outer_stride +
-                                                                   (long long)(r % P.H) * D);
-#pragma unroll
-                for (int c = 0; c < D / 4; ++c) {
-                    const float4 l = __ldg(lr + c);
-                    p[4 * c] *= __frcp_rn(l.x);
-                    p[4 * c + 1] *= __frcp_rn(l.y);
-                    p[4 * c + 2] *= __frcp_rn(l.z);
-                    p[4 * c + 3] *= __frcp_rn(l.w);
-                }
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < D; ++i) p[i] = 0.f;
-        }
-        float zr[N], zi[N];
-        split_inverse<D>(p, zr, zi);
-        fft<N, true>(zr, zi);
-        const int b = it & 1;
-        uint16_t* buf = reinterpret_cast<uint16_t*>(bufs + b * Gm::BUF_BYTES);
-        // the store issued from this buffer two tiles ago must have read it
-        if (lane == 0) ptx::bulk_wait_read<1>();
-        __syncwarp();
-        uint16_t* row = buf + lane * Gm::ROW_H;
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int n = 4 * c + e;
-                __half2 h = __floats2half2_rn(zr[n], zi[n]);
-                w[e] = *reinterpret_cast<uint32_t*>(&h) ^ P.sign_mask[n];
-            }
-            *reinterpret_cast<uint4*>(row + Gm::chunk_off(c)) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-            const CUtensorMap* tm = id.side ? &tm1 : &tm0;
-            if constexpr (D == 256)
-                ptx::tma_store_4d(tm, ptx::smem_u32(buf), 0, 0, id.row0, id.o);
-            else
-                ptx::tma_store_3d(tm, ptx::smem_u32(buf), 0, id.row0, id.o);
-            ptx::bulk_commit();
-        }
-    }
-    if (lane == 0) ptx::bulk_wait<0>();
 }
 
 // ---------------------------------------------------------------------------
@@ -367,10 +52,10 @@ __global__ void __launch_bounds__(128) srft_transform_kernel(const uint16_t* __r
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) {
             const uint4 v = __ldg(xr + c);
-            signed_pair(v.x, S.w[4 * c + 0], zr[4 * c + 0], zi[4 * c + 0]);
-            signed_pair(v.y, S.w[4 * c + 1], zr[4 * c + 1], zi[4 * c + 1]);
-            signed_pair(v.z, S.w[4 * c + 2], zr[4 * c + 2], zi[4 * c + 2]);
-            signed_pair(v.w, S.w[4 * c + 3], zr[4 * c + 3], zi[4 * c + 3]);
+            signed_pair_t(v.x, S.w[4 * c + 0], zr[4 * c + 0], zi[4 * c + 0]);
+            signed_pair_t(v.y, S.w[4 * c + 1], zr[4 * c + 1], zi[4 * c + 1]);
+            signed_pair_t(v.z, S.w[4 * c + 2], zr[4 * c + 2], zi[4 * c + 2]);
+            signed_pair_t(v.w, S.w[4 * c + 3], zr[4 * c + 3], zi[4 * c + 3]);
         }
         fft<N, false>(zr, zi);
         float p[D];
@@ -404,69 +89,13 @@ __global__ void __launch_bounds__(128) srft_transform_kernel(const uint16_t* __r
     }
 }
 
-// ---------------------------------------------------------------------------
-// Host side
-// ---------------------------------------------------------------------------
-static void fill_params(const CodecCall& c, CodecParams& P) {
-    for (int s = 0; s < 2; ++s) {
-        const CodecSideDesc& d = c.side[s < c.n_sides ? s : 0];
-        P.side[s].codes = d.codes;
-        P.side[s].scales = d.scales;
-        P.side[s].lambda = d.lambda;
-        P.side[s].lambda_outer_stride = d.lambda_outer_stride;
-        P.side[s].bits = d.bits;
-        P.side[s].pad_ = 0;
-    }
-    P.n_outer = c.n_outer;
-    P.H = c.H;
-    P.t_cap = c.t_cap;
-    P.t_offset = c.t_offset;
-    P.group = c.group;
-    P.rows_per_outer = c.n_tokens * c.H;
-    P.tiles_per_outer = (P.rows_per_outer + 31) / 32;
-    P.tiles_per_side = c.n_outer * P.tiles_per_outer;
-    P.total_tiles = c.n_sides * P.tiles_per_side;
-    for (int i = 0; i < 128; ++i) P.sign_mask[i] = 0;
-    sign_masks(c.d, c.seed, P.sign_mask);
-}
-
-template <int D>
-static int launch_codec(const CodecCall& c, bool quantize) {
-    using Gm = Geo<D>;
-    CodecParams P;
-    fill_params(c, P);
-    if (P.total_tiles == 0) return 0;
-    CUtensorMap tm[2];
-    for (int s = 0; s < 2; ++s) {
-        const CodecSideDesc& d = c.side[s < c.n_sides ? s : 0];
-        if (!encode_row_map(&tm[s], d.x, D, (long long)c.n_tokens * c.H, c.n_outer, Gm::ROWS)) return SRFTKV_ERR_CUDA;
-    }
-    auto kern = quantize ? srft_quantize_kernel<D> : srft_dequantize_kernel<D>;
-    static bool attr_done[2] = {false, false};
-    if (!attr_done[quantize]) {
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
-        attr_done[quantize] = true;
-    }
-    const int warps_needed = P.total_tiles;
-    int blocks = (warps_needed + Gm::WARPS - 1) / Gm::WARPS;
-    const int cap = device_sm_count() * Gm::MIN_BLOCKS;
-    if (blocks > cap) blocks = cap;
-    kern<<<blocks, Gm::WARPS * 32, Gm::SMEM, c.stream>>>(tm[0], tm[1], P);
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) {
-        set_error("codec kernel launch failed: %s", cudaGetErrorString(e));
-        return SRFTKV_ERR_CUDA;
-    }
-    return 0;
-}
-
 static int dispatch_codec(const CodecCall& c, bool quantize) {
     switch (c.d) {
-        case 16: return launch_codec<16>(c, quantize);
-        case 32: return launch_codec<32>(c, quantize);
-        case 64: return launch_codec<64>(c, quantize);
-        case 128: return launch_codec<128>(c, quantize);
-        case 256: return launch_codec<256>(c, quantize);
+        case 16: return launch_codec_d<16>(c, quantize);
+        case 32: return launch_codec_d<32>(c, quantize);
+        case 64: return launch_codec_d<64>(c, quantize);
+        case 128: return launch_codec_d<128>(c, quantize);
+        case 256: return launch_codec_d<256>(c, quantize);
         default: set_error("unsupported d = %d", c.d); return -1;
     }
 }
@@ -502,6 +131,24 @@ int transform_launch(const void* x, float* y, int n, int d, uint64_t seed, bool 
         case 256: return launch_transform<256>(x, y, n, seed, inverse, s);
         default: set_error("unsupported d = %d", d); return -1;
     }
+}
+
+unsigned int* codec_fault_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        set_error("no current CUDA device");
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lk(g_fault_mu);
+    if (!g_fault_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_codec_fault) != cudaSuccess) {
+            set_error("cudaGetSymbolAddress failed for the codec fault word");
+            return nullptr;
+        }
+        g_fault_ptr[dev] = static_cast<unsigned int*>(p);
+    }
+    return g_fault_ptr[dev];
 }
 
 unsigned int codec_take_fault() {

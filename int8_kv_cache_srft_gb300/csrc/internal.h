@@ -44,6 +44,7 @@ int codec_quantize(const CodecCall& c);
 int codec_dequantize(const CodecCall& c);
 int transform_launch(const void* x, float* y, int n, int d, uint64_t seed, bool inverse, cudaStream_t s);
 unsigned int codec_take_fault();
+unsigned int* codec_fault_word();  // device address of the codec fault word (current device)
 
 void set_error(const char* fmt, ...);
 int device_sm_count();
