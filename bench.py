@@ -65,7 +65,7 @@ def peaks():
 
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
-    for name in ("codec.cu", "srft_math.cuh", "ptx.cuh"):
+    for name in ("codec_tc.cu", "codec_impl.cuh", "tcgen05.cuh", "srft_math.cuh", "ptx.cuh"):
         with open(os.path.join(ROOT, "int8_kv_cache_srft_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -78,7 +78,7 @@ def recorded_traffic(sha: str):
         return None
     with open(p) as f:
         j = json.load(f)
-    ent = j.get("srft_quantize_kernel")
+    ent = j.get("srft_quantize_tc_kernel")
     if not ent or ent.get("source_sha") != sha:
         return None
     return float(ent["bytes_per_launch_full_workload"])
@@ -342,7 +342,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                    "bits_k": 4, "bits_v": 4, "group": G, "scales": "fp32", "vectors_per_step": n_vec,
                    "step": "quantize cache + dequantize cache + decode attention + 1-token append",
                    "l2": "inputs 8.6 GB >> 129 MB L2, no flush needed"},
-        "roofline": {"bound": "hbm", "kernel": "srft_quantize_kernel", "achieved": achieved, "peak": peak,
+        "roofline": {"bound": "hbm", "kernel": "srft_quantize_tc_kernel", "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": quant_bytes},
         "kernels_ms": med,

@@ -122,6 +122,12 @@ static PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 
 bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, void* base, const unsigned long long* dims,
                   const unsigned long long* strides_bytes, const unsigned* box, const char* what) {
+    return encode_tiled_swz(map, dt, rank, base, dims, strides_bytes, box, CU_TENSOR_MAP_SWIZZLE_NONE, what);
+}
+
+bool encode_tiled_swz(CUtensorMap* map, CUtensorMapDataType dt, int rank, void* base, const unsigned long long* dims,
+                      const unsigned long long* strides_bytes, const unsigned* box, CUtensorMapSwizzle swz,
+                      const char* what) {
     auto enc = encoder();
     if (!enc) {
         set_error("cuTensorMapEncodeTiled is unavailable from the driver");
@@ -135,7 +141,7 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, void* base
         e[i] = 1;
         if (i + 1 < rank) s[i] = strides_bytes[i];
     }
-    const CUresult r = enc(map, dt, rank, base, d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+    const CUresult r = enc(map, dt, rank, base, d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         set_error("cuTensorMapEncodeTiled failed (CUresult %d) for %s", (int)r, what);

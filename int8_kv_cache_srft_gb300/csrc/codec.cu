@@ -6,6 +6,8 @@
 // Apple Silicon", Methodology 1 (SRFT) and 2 (the fused kernel's steps).
 #include <cuda_fp16.h>
 
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "internal.h"
@@ -100,7 +102,24 @@ static int dispatch_codec(const CodecCall& c, bool quantize) {
     }
 }
 
-int codec_quantize(const CodecCall& c) { return dispatch_codec(c, true); }
+// Quantize path: the tensor-core contraction (codec_tc.cu) for d = 128 with
+// groups of at most 64 when the call is large enough to amortise building R_s
+// in every CTA; the register FFT otherwise.  SRFTKV_QUANT_PATH=fft or =tc in
+// the environment forces one path (tc only where it applies).
+static int quant_path_override() {
+    const char* e = getenv("SRFTKV_QUANT_PATH");
+    return (e && !strcmp(e, "fft")) ? 1 : (e && !strcmp(e, "tc")) ? 2 : 0;
+}
+
+int codec_quantize(const CodecCall& c) {
+    const int ov = quant_path_override();
+    const long long rows = (long long)c.n_sides * c.n_outer * c.n_tokens * c.H;
+    if (ov == 2 || (ov == 0 && rows >= 64ll * 1024)) {
+        const int rc = codec_quantize_tc(c);
+        if (rc != 1) return rc;
+    }
+    return dispatch_codec(c, true);
+}
 int codec_dequantize(const CodecCall& c) { return dispatch_codec(c, false); }
 
 template <int D>

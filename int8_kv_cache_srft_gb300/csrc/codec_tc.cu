@@ -1,0 +1,265 @@
+// codec_tc.cu -- SRFT quantize with the transform done as a dense
+// contraction on the 5th-generation tensor cores (head dimension 128).
+//
+// Method: "When Quantization Is Free: An int4 KV Cache That Outruns fp16 on
+// Apple Silicon", Methodology 1 (SRFT(x) = pack(F diag(s) x) is a fixed real
+// d x d orthogonal map R_s) and Methodology 4 (the pages' CPU path batches
+// the DFT as dense matmuls; this is the GPU counterpart).  Methodology 2-3
+// (lambda, group absmax, rounding, packing) run unchanged in the epilogue.
+//
+// For a tile of 128 head vectors X (fp16, exact), P = X . R_s^T is one
+// M=128, N=128, K=128 contraction.  R_s is split into two fp16 matrices
+// R_hi + R_lo (about 21 significant bits together) and both are applied, so
+// each tile is 16 tcgen05.mma (K=16 each) accumulating in fp32 in tensor
+// memory.  Warp roles, one persistent CTA per SM:
+//   warp 0     TMA producer: x tiles (two 128-byte-swizzled k-blocks) into a
+//              3-stage ring;
+//   warp 1     allocates tensor memory and issues the MMAs (one thread) into
+//              two accumulator buffers;
+//   warps 2-9  epilogue: each reads 32 rows x 64 columns of an accumulator
+//              (warp w may only touch tensor-memory lanes 32(w%4)..+31),
+//              applies lambda, quantises its four 16-coordinate groups and
+//              stores codes and scales straight from registers.
+// R_hi / R_lo are built once per CTA in shared memory from the twiddle table
+// (entries of R are closed forms of cos and sin of 2 pi jk/d).
+#include "codec_impl.cuh"
+#include "tcgen05.cuh"
+
+namespace srftkv {
+
+namespace {
+constexpr int TD = 128;                       // head dimension
+constexpr int TM = 128;                       // rows per tile
+constexpr int TSTAGES = 3;
+constexpr int T_KB_BYTES = TM * 64 * 2;       // one 128-byte-wide k-block of a tile: 16 KB
+constexpr int T_A_BYTES = 2 * T_KB_BYTES;     // a full 128 x 128 fp16 tile
+constexpr int T_B_BYTES = TD * TD * 2;        // R_hi or R_lo
+constexpr int T_OFF_BLO = T_B_BYTES;
+constexpr int T_OFF_A = 2 * T_B_BYTES;
+constexpr int T_OFF_BAR = T_OFF_A + TSTAGES * T_A_BYTES;
+constexpr int T_SMEM = T_OFF_BAR + 128 + 1024;  // + barriers + alignment slack
+constexpr int T_WARPS = 10;
+constexpr uint32_t T_IDESC = tc::idesc_f16_f32(TM, TD);
+constexpr uint32_t T_TMEM_COLS = 256;         // two 128-column fp32 accumulators
+}  // namespace
+
+__device__ __forceinline__ TileId decode_tile128(const CodecParams& P, int t) {
+    TileId id;
+    id.side = t / P.tiles_per_side;
+    const int rem = t - id.side * P.tiles_per_side;
+    id.o = rem / P.tiles_per_outer;
+    id.row0 = (rem - id.o * P.tiles_per_outer) * TM;
+    return id;
+}
+
+// Byte offset of element (row n, column k) of a 128 x 128 fp16 operand stored
+// K-major in two 128-byte-swizzled k-blocks (the layout TMA's 128-byte swizzle
+// produces and the MMA descriptors below describe).
+__device__ __forceinline__ uint32_t sw128_offset(int n, int k) {
+    return (uint32_t)((k >> 6) * T_KB_BYTES + n * 128 + ((((k & 63) >> 3) ^ (n & 7)) << 4) + ((k & 7) << 1));
+}
+
+template <int BK, int BV>
+__global__ void __launch_bounds__(T_WARPS * 32, 1)
+    srft_quantize_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
+                            const __grid_constant__ CodecParams P) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = ptx::smem_u32(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T_OFF_BAR);
+    // barrier indices: full[0..2], empty[3..5], acc_full[6..7], acc_empty[8..9]; tensor-memory slot after them
+    auto bar = [&](int i) { return ptx::smem_u32(&bars[i]); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[10]);
+
+    // ---- R_s = R diag(s), split into fp16 hi + lo, in the MMA operand layout ----
+    {
+        constexpr float inv_sqrt_d = 0.08838834764831845f;  // 1/sqrt(128)
+        constexpr float c2 = 0.125f;                        // sqrt(2/128)
+        for (int idx = threadIdx.x; idx < TD * TD; idx += blockDim.x) {
+            const int n = idx >> 7, k = idx & 127;
+            float v;
+            if (n == 0) {
+                v = inv_sqrt_d;
+            } else if (n == 1) {
+                v = (k & 1) ? -inv_sqrt_d : inv_sqrt_d;
+            } else {
+                const int m = (((n >> 1) * k) & (TD - 1)) * (256 / TD);  // angle 2 pi (jk mod d)/d on the 256-point table
+                v = (n & 1) ? c2 * tw_im(m) : c2 * tw_re(m);             // tw_im holds -sin
+            }
+            const uint32_t sbit = (k & 1) ? 0x80000000u : 0x8000u;
+            if (P.sign_mask[k >> 1] & sbit) v = -v;
+            const __half hi = __float2half_rn(v);
+            const __half lo = __float2half_rn(v - __half2float(hi));
+            const uint32_t off = sw128_offset(n, k);
+            *reinterpret_cast<__half*>(smem + off) = hi;
+            *reinterpret_cast<__half*>(smem + T_OFF_BLO + off) = lo;
+        }
+        ptx::fence_proxy_async_smem();  // generic writes -> tensor-core (async proxy) reads
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < TSTAGES; ++s) {
+            ptx::mbar_init(bar(s), 1);
+            ptx::mbar_init(bar(3 + s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(bar(6 + a), 1);
+            ptx::mbar_init(bar(8 + a), 8);
+        }
+        ptx::fence_barrier_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(ptx::smem_u32(tmem_slot), T_TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const int stride = gridDim.x;
+    bool failed = false;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int t = blockIdx.x, i = 0; t < P.total_tiles; t += stride, ++i) {
+                const int s = i % TSTAGES, use = i / TSTAGES;
+                if (use > 0 && !ptx::mbar_wait_bounded(bar(3 + s), (use - 1) & 1)) {
+                    failed = true;
+                    break;
+                }
+                const TileId id = decode_tile128(P, t);
+                const CUtensorMap* tm = id.side ? &tm1 : &tm0;
+                const uint32_t dst = sbase + T_OFF_A + s * T_A_BYTES;
+                ptx::mbar_arrive_expect_tx(bar(s), T_A_BYTES);
+                ptx::tma_load_3d(dst, tm, bar(s), 0, id.row0, id.o);
+                ptx::tma_load_3d(dst + T_KB_BYTES, tm, bar(s), 64, id.row0, id.o);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            for (int t = blockIdx.x, i = 0; t < P.total_tiles; t += stride, ++i) {
+                const int s = i % TSTAGES, a = i & 1;
+                if (!ptx::mbar_wait_bounded(bar(s), (i / TSTAGES) & 1) ||
+                    (i >= 2 && !ptx::mbar_wait_bounded(bar(8 + a), ((i >> 1) - 1) & 1))) {
+                    failed = true;
+                    break;
+                }
+                tc::fence_after_sync();
+                const uint32_t d_tmem = tmem + a * TD;
+                const uint32_t a_base = sbase + T_OFF_A + s * T_A_BYTES;
+#pragma unroll
+                for (int ks = 0; ks < TD / 16; ++ks) {
+                    const uint32_t koff = (ks >> 2) * T_KB_BYTES + (ks & 3) * 32;
+                    const uint64_t ad = tc::sw128_desc(a_base + koff);
+                    tc::mma_f16(d_tmem, ad, tc::sw128_desc(sbase + koff), T_IDESC, ks > 0);
+                    tc::mma_f16(d_tmem, ad, tc::sw128_desc(sbase + T_OFF_BLO + koff), T_IDESC, 1);
+                }
+                tc::commit(bar(3 + s));  // the x stage can be refilled once these MMAs are done
+                tc::commit(bar(6 + a));  // accumulator a is ready for the epilogue
+            }
+        }
+    } else {
+        const int quarter = warp & 3, half = (warp - 2) >> 2;
+        for (int t = blockIdx.x, i = 0; t < P.total_tiles; t += stride, ++i) {
+            const int a = i & 1;
+            const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(bar(6 + a), (i >> 1) & 1));
+            if (!ok) {
+                failed = true;
+                break;
+            }
+            tc::fence_after_sync();
+            uint32_t r0[32], r1[32];
+            const uint32_t taddr = tmem + ((uint32_t)(32 * quarter) << 16) + a * TD + half * 64;
+            tc::ld_32x32b_x32(taddr, r0);
+            tc::ld_32x32b_x32(taddr + 32, r1);
+            tc::wait_ld(r0);
+            tc::wait_ld(r1);
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(8 + a));  // accumulator a may be overwritten
+
+            const TileId id = decode_tile128(P, t);
+            const CodecSideK& S = P.side[id.side];
+            const int r = id.row0 + 32 * quarter + lane;
+            if (r >= P.rows_per_outer) continue;
+            float z[64];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                z[j] = __uint_as_float(r0[j]);
+                z[32 + j] = __uint_as_float(r1[j]);
+            }
+            if (S.lambda != nullptr) {
+                const float4* lr = reinterpret_cast<const float4*>(
+                    S.lambda + (long long)id.o * S.lambda_outer_stride + (long long)(r % P.H) * TD + half * 64);
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const float4 l = __ldg(lr + c);
+                    z[4 * c] *= l.x;
+                    z[4 * c + 1] *= l.y;
+                    z[4 * c + 2] *= l.z;
+                    z[4 * c + 3] *= l.w;
+                }
+            }
+            const long long vrow = ((long long)id.o * P.t_cap + P.t_offset) * P.H + r;
+            const int ng = TD / P.group;
+            if (BK == BV || id.side == 0)
+                quant_store_row<64, BK>(z, P.group, S.codes + vrow * (TD * BK / 8) + half * (64 * BK / 8),
+                                        S.scales + vrow * ng + half * (ng / 2));
+            else
+                quant_store_row<64, BV>(z, P.group, S.codes + vrow * (TD * BV / 8) + half * (64 * BV / 8),
+                                        S.scales + vrow * ng + half * (ng / 2));
+        }
+    }
+    if (failed) atomicOr(P.fault, 1u);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (warp == 1) tc::tmem_dealloc(tmem, T_TMEM_COLS);
+}
+
+template <int BK, int BV>
+static int launch_tc(const CodecCall& c) {
+    CodecParams P;
+    fill_params(c, P);
+    P.tiles_per_outer = (P.rows_per_outer + TM - 1) / TM;
+    P.tiles_per_side = c.n_outer * P.tiles_per_outer;
+    P.total_tiles = c.n_sides * P.tiles_per_side;
+    P.fault = codec_fault_word();
+    if (!P.fault) return SRFTKV_ERR_CUDA;
+    CUtensorMap tm[2];
+    for (int s = 0; s < 2; ++s) {
+        const CodecSideDesc& d = c.side[s < c.n_sides ? s : 0];
+        const unsigned long long rows = (unsigned long long)c.n_tokens * c.H;
+        const unsigned long long dims[3] = {(unsigned long long)TD, rows, (unsigned long long)c.n_outer};
+        const unsigned long long strides[2] = {TD * 2ull, rows * TD * 2ull};
+        const unsigned box[3] = {64u, (unsigned)TM, 1u};
+        if (!encode_tiled_swz(&tm[s], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, d.x, dims, strides, box,
+                              CU_TENSOR_MAP_SWIZZLE_128B, "tensor-core quantize input"))
+            return SRFTKV_ERR_CUDA;
+    }
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(srft_quantize_tc_kernel<BK, BV>, cudaFuncAttributeMaxDynamicSharedMemorySize, T_SMEM);
+        attr = true;
+    }
+    int blocks = device_sm_count();
+    if (blocks > P.total_tiles) blocks = P.total_tiles;
+    srft_quantize_tc_kernel<BK, BV><<<blocks, T_WARPS * 32, T_SMEM, c.stream>>>(tm[0], tm[1], P);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("tensor-core quantize launch failed: %s", cudaGetErrorString(e));
+        return SRFTKV_ERR_CUDA;
+    }
+    return SRFTKV_OK;
+}
+
+int codec_quantize_tc(const CodecCall& c) {
+    if (c.d != TD || c.group > 64) return 1;
+    const int bk = c.side[0].bits, bv = c.n_sides > 1 ? c.side[1].bits : bk;
+    if (bk == 4 && bv == 4) return launch_tc<4, 4>(c);
+    if (bk == 8 && bv == 8) return launch_tc<8, 8>(c);
+    if (bk == 8 && bv == 4) return launch_tc<8, 4>(c);
+    return launch_tc<4, 8>(c);
+}
+
+}  // namespace srftkv

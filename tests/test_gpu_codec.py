@@ -129,6 +129,26 @@ def test_quantize_dequantize_ragged(d, bits, group, lam):
         assert_reconstruction_bound(_np(out), _np(x), enc["scales"], lam_full, group)
 
 
+TC_CASES = [(bk, bv, group, lam) for bk, bv in ((4, 4), (8, 8), (8, 4), (4, 8)) for group in (16, 32, 64)
+            for lam in (False, True)]
+
+
+@pytest.mark.parametrize("bk,bv,group,lam", TC_CASES)
+def test_tensor_core_quantize_path(monkeypatch, bk, bv, group, lam):
+    """d = 128 through the tensor-core contraction (forced on for a small, ragged call): 3 outer x 300 tokens x
+    3 heads = 900 rows per outer (7 tiles of 128 with a ragged last one), written at t_offset 3 of t_cap 310."""
+    monkeypatch.setenv("SRFTKV_QUANT_PATH", "tc")
+    w = I.Workload("tc", n_outer=3, tokens=300, kv_heads=3, d=128, lam=lam, data_seed=bk * 100 + bv * 10 + group,
+                   outlier_kind="scale", outlier_channels=4, outlier_factor=50.0)
+    xk, xv = I.kv_side(w, "k"), I.kv_side(w, "v")
+    lk, lv = I.lam_table(w, "k"), I.lam_table(w, "v")
+    sk, sv = _quantize_gpu(xk, xv, lk, lv, bk, bv, group, 13, t_cap=310, t_offset=3)
+    for side, x, lam_t, b in ((sk, xk, lk, bk), (sv, xv, lv, bv)):
+        _check_side(side, x, lam_t, b, group, 13, t_offset=3)
+        codes = _np(side.codes)
+        assert (codes[:, :3] == 0xAB).all() and (codes[:, 303:] == 0xAB).all()
+
+
 def test_zero_rows_and_empty_calls():
     x = torch.zeros((1, 40, 2, 128), dtype=torch.float16)
     sk, sv = _quantize_gpu(x, x, None, None, 4, 8, 16, 3)
@@ -163,9 +183,12 @@ def _sample_rows(n_rows, k, seed):
     return np.unique(np.concatenate([rng.integers(0, n_rows, k), [0, n_rows - 1]]))
 
 
-def test_qwen_shaped_full_size_sampled():
+@pytest.mark.parametrize("path", ("tc", "fft"))
+def test_qwen_shaped_full_size_sampled(monkeypatch, path):
     """The full 28 x 32768 x 2 x 128 cache with lambda, quantised in one launch; 3000 sampled rows per side
-    against the oracle, then the dequantised rows within one step and the reconstruction MSE reported."""
+    against the oracle, then the dequantised rows within one step and the reconstruction MSE reported.  Both
+    quantize paths (tensor-core contraction and register FFT) are checked."""
+    monkeypatch.setenv("SRFTKV_QUANT_PATH", path)
     w = I.QWEN
     xk, xv = I.kv_side(w, "k", device="cuda"), I.kv_side(w, "v", device="cuda")
     lk, lv = I.lam_table(w, "k", device="cuda"), I.lam_table(w, "v", device="cuda")
