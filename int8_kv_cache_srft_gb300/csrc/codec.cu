@@ -102,10 +102,11 @@ static int dispatch_codec(const CodecCall& c, bool quantize) {
     }
 }
 
-// Quantize path: the tensor-core contraction (codec_tc.cu) for d = 128 with
-// groups of at most 64 when the call is large enough to amortise building R_s
-// in every CTA; the register FFT otherwise.  SRFTKV_QUANT_PATH=fft or =tc in
-// the environment forces one path (tc only where it applies).
+// Codec path: the tensor-core contraction (codec_tc.cu) for d = 128 (and, to
+// quantize, groups of at most 64) when the call is large enough to amortise
+// building R_s in every CTA; the register FFT otherwise.  SRFTKV_QUANT_PATH=fft
+// or =tc in the environment forces one path for both directions (tc only
+// where it applies).
 static int quant_path_override() {
     const char* e = getenv("SRFTKV_QUANT_PATH");
     return (e && !strcmp(e, "fft")) ? 1 : (e && !strcmp(e, "tc")) ? 2 : 0;
@@ -120,7 +121,15 @@ int codec_quantize(const CodecCall& c) {
     }
     return dispatch_codec(c, true);
 }
-int codec_dequantize(const CodecCall& c) { return dispatch_codec(c, false); }
+int codec_dequantize(const CodecCall& c) {
+    const int ov = quant_path_override();
+    const long long rows = (long long)c.n_sides * c.n_outer * c.n_tokens * c.H;
+    if (ov == 2 || (ov == 0 && rows >= 64ll * 1024)) {
+        const int rc = codec_dequantize_tc(c);
+        if (rc != 1) return rc;
+    }
+    return dispatch_codec(c, false);
+}
 
 template <int D>
 static int launch_transform(const void* x, float* y, int n, uint64_t seed, bool inverse, cudaStream_t s) {

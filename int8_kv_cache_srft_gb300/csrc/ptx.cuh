@@ -99,3 +99,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 }  // namespace ptx
 }  // namespace srftkv
+
+namespace srftkv {
+namespace ptx {
+// Named barrier over `count` threads (a subset of the CTA).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+}  // namespace ptx
+}  // namespace srftkv

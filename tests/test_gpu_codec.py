@@ -144,9 +144,20 @@ def test_tensor_core_quantize_path(monkeypatch, bk, bv, group, lam):
     lk, lv = I.lam_table(w, "k"), I.lam_table(w, "v")
     sk, sv = _quantize_gpu(xk, xv, lk, lv, bk, bv, group, 13, t_cap=310, t_offset=3)
     for side, x, lam_t, b in ((sk, xk, lk, bk), (sv, xv, lv, bv)):
-        _check_side(side, x, lam_t, b, group, 13, t_offset=3)
+        enc, lam_b, _ = _check_side(side, x, lam_t, b, group, 13, t_offset=3)
         codes = _np(side.codes)
         assert (codes[:, :3] == 0xAB).all() and (codes[:, 303:] == 0xAB).all()
+        # and back through the tensor-core dequantize
+        out = torch.empty_like(side.x)
+        K.srft_kv_dequantize(K.Side(side.codes, side.scales, b, x=out, lam=side.lam), None, 3, 300, 3, 128, group,
+                             310, 3, 13)
+        torch.cuda.synchronize()
+        lam_full = None if lam_b is None else np.broadcast_to(lam_b, x.shape)
+        ref_hat = O.srft_kv_dequantize(enc["codes"], enc["scales"], lam_b, b, group, 13)
+        assert_dequant_within_step(_np(out), ref_hat, enc["scales"], lam_full, group)
+        assert_reconstruction_bound(_np(out), _np(x), enc["scales"], lam_full, group)
+        mine = O.srft_kv_dequantize(codes[:, 3:303], _np(side.scales)[:, 3:303].astype(np.float64), lam_b, b, group, 13)
+        assert np.abs(_np(out) - mine).max() <= np.abs(mine).max() * 2.0**-10 + 1e-5
 
 
 def test_zero_rows_and_empty_calls():
