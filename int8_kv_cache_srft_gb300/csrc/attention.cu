@@ -211,21 +211,21 @@ __global__ void __launch_bounds__(128) attn_prep_q_kernel(const __grid_constant_
 // ---------------------------------------------------------------------------
 // 2. split kernel
 // ---------------------------------------------------------------------------
-// K-side B fragments (q_tilde in fp16) for this thread: column n = g of the
-// MMA is query head n % 4 of the group.  For 4-bit keys the columns 4..7
-// carry the same heads restricted to the second 16-dim group of each 32-dim
-// chunk (see the k-slot map below), so one MMA yields per-group partials.
+// K-side B fragments (q_tilde as fp16 hi + lo) for this thread.  Column n of
+// every MMA is (query head n/2 of the group, half n%2): for 4-bit keys half 0
+// takes the dims of the first 16-dim group of each 32-dim chunk and half 1 the
+// second, so one MMA yields both groups' partials for a head in the two
+// columns one thread owns; for 8-bit and fp16 keys half 1 is zero.
 template <int D, int BK>
 __device__ __forceinline__ void build_qb(const float* __restrict__ qrow_base, int rep, int g, int c,
                                          uint32_t (&qh)[D / 8], uint32_t (&ql)[D / 8]) {
-    const int h = g & 3;
+    const int h = g >> 1, sigma = g & 1;
     const bool head_ok = h < rep;
     const float* q = qrow_base + (long long)h * D;
     auto val = [&](int dim, bool ok) -> float { return (ok && head_ok) ? q[dim] : 0.f; };
     if constexpr (BK == 4) {
-        // chunk m (32 dims), thread c owns dims 8c..8c+7 of the chunk; columns
-        // n < 4 take dims of the first 16 (c < 2), columns n >= 4 the second.
-        const bool ok = (c >> 1) == (g >> 2);
+        // chunk m (32 dims): thread c owns dims 8c..8c+7, which lie in half c/2
+        const bool ok = (c >> 1) == sigma;
 #pragma unroll
         for (int m = 0; m < D / 32; ++m) {
             const int base = 32 * m + 8 * c;
@@ -235,7 +235,7 @@ __device__ __forceinline__ void build_qb(const float* __restrict__ qrow_base, in
             split_h2(val(base + 3, ok), val(base + 7, ok), qh[4 * m + 3], ql[4 * m + 3]);
         }
     } else if constexpr (BK == 8) {
-        const bool ok = g < 4;
+        const bool ok = sigma == 0;
 #pragma unroll
         for (int m = 0; m < D / 16; ++m) {
             const int base = 16 * m + 4 * c;
@@ -243,7 +243,7 @@ __device__ __forceinline__ void build_qb(const float* __restrict__ qrow_base, in
             split_h2(val(base + 1, ok), val(base + 3, ok), qh[2 * m + 1], ql[2 * m + 1]);
         }
     } else {
-        const bool ok = g < 4;
+        const bool ok = sigma == 0;
 #pragma unroll
         for (int j = 0; j < D / 16; ++j) {
             split_h2(val(16 * j + 2 * c, ok), val(16 * j + 2 * c + 1, ok), qh[2 * j + 0], ql[2 * j + 0]);
@@ -269,16 +269,17 @@ __device__ __forceinline__ float ex2(float x) {  // 2^x; ex2.approx has a relati
     return y;
 }
 
-// Scores of one 16-token sub-tile at row tr of the stage: s[0..3] for rows
-// (g, g+8) x columns (2c, 2c+1), before the two column halves are combined.
+// Scores of one 16-token sub-tile at row tr of the stage for this thread's
+// head c: s[0] for token tr+g, s[1] for token tr+g+8.
 template <int D, int BK>
-__device__ __forceinline__ void tile_scores(const uint8_t* __restrict__ stage, uint32_t kc, const float* __restrict__ ks,
-                                            int sp, int lg, int tr, int lane, const uint32_t (&qh)[D / 8],
-                                            const uint32_t (&ql)[D / 8], float (&s)[4]) {
+__device__ __forceinline__ void tile_scores(uint32_t kc, const float* __restrict__ ks, int sp, int lg, int tr, int lane,
+                                            const uint32_t (&qh)[D / 8], const uint32_t (&ql)[D / 8], float (&s)[2]) {
     constexpr int RPK = PlaneT<D, BK>::RP;
-    const int g = lane >> 2, c = lane & 3;
-    s[0] = s[1] = s[2] = s[3] = 0.f;
+    const int g = lane >> 2;
+    const float* k0 = ks + (tr + g) * sp;
+    const float* k1 = ks + (tr + g + 8) * sp;
     if constexpr (BK == 4) {
+        float a0 = 0.f, a1 = 0.f;
 #pragma unroll
         for (int m2 = 0; m2 < D / 64; ++m2) {
             uint32_t r[4];
@@ -294,15 +295,16 @@ __device__ __forceinline__ void tile_scores(const uint8_t* __restrict__ stage, u
                 const uint32_t y0 = i4_lo(rg >> 8), y1 = i4_lo(rg8 >> 8), y2 = i4_hi(rg >> 8), y3 = i4_hi(rg8 >> 8);
                 mma16816(d, y0, y1, y2, y3, qh[4 * mm + 2], qh[4 * mm + 3]);
                 mma16816(d, y0, y1, y2, y3, ql[4 * mm + 2], ql[4 * mm + 3]);
-                const int gi = (32 * mm + 16 * (c >> 1)) >> lg;
-                const float s0 = ks[(tr + g) * sp + gi], s1 = ks[(tr + g + 8) * sp + gi];
-                s[0] = fmaf(s0, d[0], s[0]);
-                s[1] = fmaf(s0, d[1], s[1]);
-                s[2] = fmaf(s1, d[2], s[2]);
-                s[3] = fmaf(s1, d[3], s[3]);
+                // d = (token g: half 0, half 1, token g+8: half 0, half 1) for head c
+                const int ga = (32 * mm) >> lg, gb = (32 * mm + 16) >> lg;
+                a0 = fmaf(k0[ga], d[0], fmaf(k0[gb], d[1], a0));
+                a1 = fmaf(k1[ga], d[2], fmaf(k1[gb], d[3], a1));
             }
         }
+        s[0] = a0;
+        s[1] = a1;
     } else if constexpr (BK == 8) {
+        float a0 = 0.f, a1 = 0.f;
 #pragma unroll
         for (int m2 = 0; m2 < D / 32; ++m2) {
             uint32_t r[4];
@@ -316,27 +318,30 @@ __device__ __forceinline__ void tile_scores(const uint8_t* __restrict__ stage, u
                 mma16816(d, x0, x1, x2, x3, qh[2 * mm], qh[2 * mm + 1]);
                 mma16816(d, x0, x1, x2, x3, ql[2 * mm], ql[2 * mm + 1]);
                 const int gi = (16 * mm) >> lg;
-                const float s0 = ks[(tr + g) * sp + gi], s1 = ks[(tr + g + 8) * sp + gi];
-                s[0] = fmaf(s0, d[0], s[0]);
-                s[1] = fmaf(s0, d[1], s[1]);
-                s[2] = fmaf(s1, d[2], s[2]);
-                s[3] = fmaf(s1, d[3], s[3]);
+                a0 = fmaf(k0[gi], d[0], a0);
+                a1 = fmaf(k1[gi], d[2], a1);
             }
         }
+        s[0] = a0;
+        s[1] = a1;
     } else {
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int j = 0; j < D / 16; ++j) {
             uint32_t r[4];
             ldsm_x4(ldsm_addr(kc, RPK, tr, 2 * j, lane), r);
-            mma16816(s, r[0], r[1], r[2], r[3], qh[2 * j], qh[2 * j + 1]);
-            mma16816(s, r[0], r[1], r[2], r[3], ql[2 * j], ql[2 * j + 1]);
+            mma16816(d, r[0], r[1], r[2], r[3], qh[2 * j], qh[2 * j + 1]);
+            mma16816(d, r[0], r[1], r[2], r[3], ql[2 * j], ql[2 * j + 1]);
         }
+        s[0] = d[0];
+        s[1] = d[2];
     }
 }
 
-// acc += V^T B for one 16-token sub-tile, B[k][n] = p(token k, head n%4) * scale_V.
-// p00..p11 are p for tokens 2c+e+8f of head g%4 (zero for padded heads and for
-// tokens past the end; their scale rows were zeroed in shared memory).
+// acc += V^T B for one 16-token sub-tile, B[k][n] = p(token k, head n/2) *
+// scale_V(token k, group of half n%2).  p00..p11 are p for tokens 2c+e+8f of
+// head g/2 (zero for padded heads and for tokens past the end, whose scale
+// rows were zeroed in shared memory).
 template <int D, int BV>
 __device__ __forceinline__ void tile_pv(uint32_t vc, const float* __restrict__ vs, int sp, int lg, int tr, int lane,
                                         float p00, float p10, float p01, float p11, uint32_t amask_lo,
@@ -344,7 +349,7 @@ __device__ __forceinline__ void tile_pv(uint32_t vc, const float* __restrict__ v
     constexpr int RPV = PlaneT<D, BV>::RP;
     const int g = lane >> 2, c = lane & 3;
     if constexpr (BV == 4) {
-        const int side = g >> 2;
+        const int side = g & 1;
 #pragma unroll
         for (int cb2 = 0; cb2 < D / 64; ++cb2) {
             uint32_t r[4];
@@ -369,8 +374,8 @@ __device__ __forceinline__ void tile_pv(uint32_t vc, const float* __restrict__ v
             }
         }
     } else if constexpr (BV == 8) {
-        // columns 4..7 carry no head for 8-bit values
-        const float cm = g < 4 ? 1.f : 0.f;
+        // the half-1 columns carry nothing for 8-bit values
+        const float cm = (g & 1) ? 0.f : 1.f;
         p00 *= cm;
         p10 *= cm;
         p01 *= cm;
@@ -395,7 +400,7 @@ __device__ __forceinline__ void tile_pv(uint32_t vc, const float* __restrict__ v
             }
         }
     } else {
-        const float cm = g < 4 ? 1.f : 0.f;
+        const float cm = (g & 1) ? 0.f : 1.f;
         uint32_t bh0, bl0, bh1, bl1;
         split_h2(p00 * cm, p10 * cm, bh0, bl0);
         split_h2(p01 * cm, p11 * cm, bh1, bl1);
@@ -421,7 +426,7 @@ __device__ __forceinline__ void tile_pv(uint32_t vc, const float* __restrict__ v
 template <int D, int BK, int BV, int NT>
 __device__ __forceinline__ void attn_chunk(const AttnParams& P, uint8_t* __restrict__ stage, int t0, int t_end, int lane,
                                            const uint32_t (&qh)[D / 8], const uint32_t (&ql)[D / 8],
-                                           float (&acc)[D / 4], float (&m)[2], float (&l)[2]) {
+                                           float (&acc)[D / 4], float& m, float& l) {
     using C = AttnCfg<D, BK, BV>;
     const int g = lane >> 2, c = lane & 3;
     const uint32_t kc = ptx::smem_u32(stage + C::OFF_KC), vc = ptx::smem_u32(stage + C::OFF_VC);
@@ -440,67 +445,47 @@ __device__ __forceinline__ void attn_chunk(const AttnParams& P, uint8_t* __restr
         __syncwarp();
     }
 
-    float s[NT][4];
+    // this thread's head is c; s[st] holds tokens 16st+g and 16st+g+8
+    float s[NT][2];
 #pragma unroll
     for (int st = 0; st < NT; ++st) {
-        if (16 * st < valid) tile_scores<D, BK>(stage, kc, ks, sp, lg, 16 * st, lane, qh, ql, s[st]);
-        else s[st][0] = s[st][1] = s[st][2] = s[st][3] = 0.f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) s[st][i] += __shfl_xor_sync(0xffffffffu, s[st][i], 2);
-        if (16 * st + g >= valid) s[st][0] = s[st][1] = -INFINITY;
-        if (16 * st + g + 8 >= valid) s[st][2] = s[st][3] = -INFINITY;
+        if (16 * st < valid) tile_scores<D, BK>(kc, ks, sp, lg, 16 * st, lane, qh, ql, s[st]);
+        else s[st][0] = s[st][1] = 0.f;
+        if (16 * st + g >= valid) s[st][0] = -INFINITY;
+        if (16 * st + g + 8 >= valid) s[st][1] = -INFINITY;
     }
-    // ---- online softmax for heads h0 = 2(c%2), h0+1 ----
-    float mt0 = -INFINITY, mt1 = -INFINITY;
+    // ---- online softmax (log2 domain) ----
+    float mt = -INFINITY;
 #pragma unroll
-    for (int st = 0; st < NT; ++st) {
-        mt0 = fmaxf(mt0, fmaxf(s[st][0], s[st][2]));
-        mt1 = fmaxf(mt1, fmaxf(s[st][1], s[st][3]));
-    }
+    for (int st = 0; st < NT; ++st) mt = fmaxf(mt, fmaxf(s[st][0], s[st][1]));
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        mt0 = fmaxf(mt0, __shfl_xor_sync(0xffffffffu, mt0, off));
-        mt1 = fmaxf(mt1, __shfl_xor_sync(0xffffffffu, mt1, off));
-    }
-    const float mn0 = fmaxf(m[0], mt0), mn1 = fmaxf(m[1], mt1);
-    if (__any_sync(0xffffffffu, (mn0 > m[0]) || (mn1 > m[1]))) {
-        const float f0 = (mn0 == -INFINITY) ? 1.f : ex2(m[0] - mn0);
-        const float f1 = (mn1 == -INFINITY) ? 1.f : ex2(m[1] - mn1);
-        l[0] *= f0;
-        l[1] *= f1;
+    for (int off = 4; off < 32; off <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+    const float mn = fmaxf(m, mt);
+    if (__any_sync(0xffffffffu, mn > m)) {
+        const float f = (mn == -INFINITY) ? 1.f : ex2(m - mn);
+        l *= f;
 #pragma unroll
-        for (int i = 0; i < D / 4; i += 2) {
-            acc[i] *= f0;
-            acc[i + 1] *= f1;
-        }
-        m[0] = mn0;
-        m[1] = mn1;
+        for (int i = 0; i < D / 4; ++i) acc[i] *= f;
+        m = mn;
     }
     // p in [0, 256]: the +8 keeps p * scale_V clear of fp16 subnormals; it cancels in acc / l
-    const float b0 = (m[0] == -INFINITY) ? 0.f : m[0] - 8.f, b1 = (m[1] == -INFINITY) ? 0.f : m[1] - 8.f;
-    // this thread offers head [0,2,1,3][c] of its two token rows to the B layout; padded heads offer zero
-    const int hh = ((c & 1) << 1) | (c >> 1);
-    const bool offer = hh < P.rep;
-    const int hd = g & 3;
-    const int src_c = ((hd & 1) << 1) | (hd >> 1);
-    const uint32_t amask_lo = 0, amask_hi = 0;
+    const float bias = (m == -INFINITY) ? 0.f : m - 8.f;
+    const bool offer = c < P.rep;  // padded heads offer zero
+    const int hd = g >> 1;         // head of this thread's B columns
 #pragma unroll
     for (int st = 0; st < NT; ++st) {
         if (16 * st >= valid) break;
-        const float p0 = ex2(s[st][0] - b0), p1 = ex2(s[st][1] - b1), p2 = ex2(s[st][2] - b0), p3 = ex2(s[st][3] - b1);
-        l[0] += p0 + p2;
-        l[1] += p1 + p3;
-        const float o0 = offer ? ((c < 2) ? p0 : p1) : 0.f, o1 = offer ? ((c < 2) ? p2 : p3) : 0.f;
-        const float P00 = __shfl_sync(0xffffffffu, o0, 4 * (2 * c) + src_c);
-        const float P10 = __shfl_sync(0xffffffffu, o0, 4 * (2 * c + 1) + src_c);
-        const float P01 = __shfl_sync(0xffffffffu, o1, 4 * (2 * c) + src_c);
-        const float P11 = __shfl_sync(0xffffffffu, o1, 4 * (2 * c + 1) + src_c);
+        const float p0 = ex2(s[st][0] - bias), p1 = ex2(s[st][1] - bias);
+        l += p0 + p1;
+        const float o0 = offer ? p0 : 0.f, o1 = offer ? p1 : 0.f;
+        const float P00 = __shfl_sync(0xffffffffu, o0, 4 * (2 * c) + hd);
+        const float P10 = __shfl_sync(0xffffffffu, o0, 4 * (2 * c + 1) + hd);
+        const float P01 = __shfl_sync(0xffffffffu, o1, 4 * (2 * c) + hd);
+        const float P11 = __shfl_sync(0xffffffffu, o1, 4 * (2 * c + 1) + hd);
         const int vt = valid - 16 * st;
         const bool sub_tail = vt < 16;
         const uint32_t mlo = (2 * c < vt ? 0x0000FFFFu : 0u) | (2 * c + 1 < vt ? 0xFFFF0000u : 0u);
         const uint32_t mhi = (2 * c + 8 < vt ? 0x0000FFFFu : 0u) | (2 * c + 9 < vt ? 0xFFFF0000u : 0u);
-        (void)amask_lo;
-        (void)amask_hi;
         tile_pv<D, BV>(vc, vs, sp, lg, 16 * st, lane, P00, P10, P01, P11, mlo, mhi, sub_tail, acc);
     }
 }
@@ -510,20 +495,19 @@ __device__ __forceinline__ void attn_chunk(const AttnParams& P, uint8_t* __restr
 template <int D, int BV>
 __device__ __forceinline__ void acc_coord(int i, int g, int c, int& dim, int& head, bool& useful) {
     const int e = i & 3;
-    const int col = 2 * c + (e & 1);
-    head = col & 3;
+    head = c;  // columns 2c, 2c+1 are (head c, half 0), (head c, half 1)
     if constexpr (BV == 4) {
         const int cb = i >> 3, j = (i >> 2) & 1;
         dim = 32 * cb + 4 * g + 2 * j + (e >> 1);
-        useful = (g < 4) == (c < 2);
+        useful = (e & 1) == (g >= 4 ? 1 : 0);  // rows g < 4 are dims of half 0
     } else if constexpr (BV == 8) {
         const int cb = i >> 2;
         dim = 16 * cb + 2 * g + (e >> 1);
-        useful = c < 2;
+        useful = (e & 1) == 0;
     } else {
         const int j = i >> 2;
         dim = 16 * j + g + 8 * (e >> 1);
-        useful = c < 2;
+        useful = (e & 1) == 0;
     }
 }
 
@@ -558,7 +542,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 3)
     float acc[C::ACC];
 #pragma unroll
     for (int i = 0; i < C::ACC; ++i) acc[i] = 0.f;
-    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+    float m = -INFINITY, l = 0.f;  // online-softmax state for head c (log2 domain)
 
     const int row_base = b * P.t_cap;
     const uint32_t kc_bytes = C::CH * PlaneT<D, BK>::RP, vc_bytes = C::CH * PlaneT<D, BV>::RP;
@@ -596,26 +580,21 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 3)
     }
     // the failure flag is per warp; every warp still joins the merge below
     if (failed) {
-        m[0] = m[1] = -INFINITY;
-        l[0] = l[1] = 0.f;
+        m = -INFINITY;
+        l = 0.f;
 #pragma unroll
         for (int i = 0; i < C::ACC; ++i) acc[i] = 0.f;
     }
 
     // ---- per-warp totals of l over the 8 token rows ----
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
-        l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
-    }
+    for (int off = 4; off < 32; off <<= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
     __syncthreads();  // all warps are done with their stage buffers
     float* mw = reinterpret_cast<float*>(smem + 128);          // [warps][4][2]
     float* aw = mw + kAttnWarps * 8;                            // [warps][4][D]
-    if (g == 0 && c < 2) {
-        mw[warp * 8 + (2 * c) * 2 + 0] = m[0];
-        mw[warp * 8 + (2 * c) * 2 + 1] = l[0];
-        mw[warp * 8 + (2 * c + 1) * 2 + 0] = m[1];
-        mw[warp * 8 + (2 * c + 1) * 2 + 1] = l[1];
+    if (g == 0) {
+        mw[warp * 8 + c * 2 + 0] = m;
+        mw[warp * 8 + c * 2 + 1] = l;
     }
 #pragma unroll
     for (int i = 0; i < C::ACC; ++i) {

@@ -69,7 +69,8 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
     srft_quantize_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
                             const __grid_constant__ CodecParams P) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned, and still a __shared__ pointer so accesses compile to shared-memory instructions
+    uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = ptx::smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T_OFF_BAR);
@@ -269,14 +270,27 @@ __device__ __forceinline__ void dequant_row_smem(const uint8_t* __restrict__ cro
         w[4 * i + 2] = v.z;
         w[4 * i + 3] = v.w;
     }
-    const int sh = __ffs(group >> 4) - 1;
+    float sc[U];
+    if (group == 16) {  // one scale per 16-coordinate unit: vector loads of the (padded) scale row
+#pragma unroll
+        for (int i = 0; i < U / 4; ++i) {
+            const float4 v = reinterpret_cast<const float4*>(srow)[i];
+            sc[4 * i] = v.x;
+            sc[4 * i + 1] = v.y;
+            sc[4 * i + 2] = v.z;
+            sc[4 * i + 3] = v.w;
+        }
+    } else {
+        const int sh = __ffs(group >> 4) - 1;
+#pragma unroll
+        for (int u = 0; u < U; ++u) sc[u] = srow[u >> sh];
+    }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        const float sc = srow[u >> sh];
 #pragma unroll
         for (int i = 16 * u; i < 16 * u + 16; ++i) {
             const float c = (BITS == 4) ? code_int4(w[i / PER], i % PER) : code_int8(w[i / PER], i % PER);
-            p[i] = c * sc;
+            p[i] = c * sc[u];
         }
     }
 }
@@ -290,7 +304,8 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
     srft_dequantize_tc_kernel(const __grid_constant__ DqMaps M, const __grid_constant__ CodecParams P) {
     using C = DqCfg<BK, BV>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned, and still a __shared__ pointer so accesses compile to shared-memory instructions
+    uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = ptx::smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
