@@ -275,8 +275,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     ms_step = ms_total / args.steps
     value = world * n_vec / (ms_step * 1e-3)
 
-    # fp16-cache comparator: the same attention kernel on the raw fp16 cache
-    raw_k, raw_v = K.Side(xk, None, 16), K.Side(xv, None, 16)
+    # fp16-cache comparator: the same attention kernel on the raw fp16 cache (head-major like the packed planes)
+    raw_k = K.Side(xk.permute(0, 2, 1, 3).contiguous(), None, 16)
+    raw_v = K.Side(xv.permute(0, 2, 1, 3).contiguous(), None, 16)
     ws16 = torch.empty(K.q4kv_decode_attention_workspace_size(B, Hq, Hkv, d, T, 0), dtype=torch.uint8, device=dev)
     t16 = []
     for i in range(13):

@@ -69,17 +69,19 @@ extern "C" {
 #define SRFTKV_ERR_DEVICE (-3)  /* current device is not sm_103 */
 
 /*
- * One side (K or V) of a packed cache, stored as two planes ([AQT]):
- *   codes  : uint8 [n_outer][t_cap][H][d*bits/8]  (row start 16-byte aligned
+ * One side (K or V) of a packed cache, stored as two head-major planes ([AQT]):
+ *   codes  : uint8 [n_outer][H][t_cap][d*bits/8]  (row start 16-byte aligned
  *            when d*bits/8 >= 16, else d*bits/8-byte aligned)
- *   scales : fp32  [n_outer][t_cap][H][d/group]   (16-byte aligned when
+ *   scales : fp32  [n_outer][H][t_cap][d/group]   (16-byte aligned when
  *            d/group >= 4, else 4*d/group-byte aligned)
- * n_outer is the layer index for the codec calls and the batch index for
- * attention.  A side with bits == 16 (attention only) is a raw fp16 cache
- * [B][t_cap][Hkv][d] passed in `codes`, without rotation or scales.
+ * so the cached rows of one (outer, head) are contiguous.  n_outer is the
+ * layer index for the codec calls and the batch index for attention.  A side
+ * with bits == 16 (attention only) is a raw fp16 cache [B][Hkv][t_cap][d]
+ * passed in `codes`, without rotation or scales.  The fp16 rows a codec call
+ * reads or writes (`x`) keep the token-major layout [n_outer][n_tokens][H][d].
  */
 typedef struct srftkv_side {
-    void* x;                     /* quantize: fp16 input [n_outer][n_tokens][H][d] (read);
+    void* x;                     /* quantize: fp16 input [n_outer][n_tokens][H][d] (read, 16-byte aligned);
                                     dequantize: fp16 output, same layout (written);
                                     attention: unused */
     const float* lambda;         /* per-channel lambda, element (o, h, i) at
@@ -97,8 +99,8 @@ typedef struct srftkv_side {
  * per step is n_tokens = 1 at t_offset = current length [TQ]).
  * For each side that is not NULL and every (o, t, h) with t < n_tokens:
  *   p = SRFT(x[o][t][h]); z = lambda[o][h] * p; per group j of `group`
- *   coordinates: scales[o][t_offset+t][h][j] = max|z| / Q and
- *   codes[o][t_offset+t][h] = packed rint(z / scale).
+ *   coordinates: scales[o][h][t_offset+t][j] = max|z| / Q and
+ *   codes[o][h][t_offset+t] = packed rint(z / scale).
  * Both sides are encoded by one kernel launch.  Requires
  * 0 <= t_offset, t_offset + n_tokens <= t_cap, and x rows 16-byte aligned.
  * n_outer == 0 or n_tokens == 0 is a no-op that returns SRFTKV_OK.

@@ -94,8 +94,8 @@ class Side:
     """One side (K or V) of a packed cache: the code plane, the scale plane,
     an optional per-channel lambda and, for the codec calls, the fp16 rows."""
 
-    codes: torch.Tensor            # uint8 [n_outer][t_cap][H][d*bits/8] (or fp16 [B][t_cap][Hkv][d] for bits 16)
-    scales: torch.Tensor | None    # fp32 [n_outer][t_cap][H][d/group]
+    codes: torch.Tensor            # uint8 [n_outer][H][t_cap][d*bits/8] (or fp16 [B][Hkv][t_cap][d] for bits 16)
+    scales: torch.Tensor | None    # fp32 [n_outer][H][t_cap][d/group]
     bits: int
     x: torch.Tensor | None = None  # fp16 [n_outer][n_tokens][H][d]
     lam: torch.Tensor | None = None  # fp32 [n_lam][H][d]; n_lam == 1 broadcasts
@@ -109,11 +109,11 @@ class Side:
 
 
 def alloc_side(n_outer: int, t_cap: int, H: int, d: int, bits: int, group: int, device="cuda") -> Side:
-    """Allocate empty code and scale planes for one side."""
+    """Allocate empty (head-major) code and scale planes for one side."""
     if bits == 16:
-        return Side(torch.empty((n_outer, t_cap, H, d), dtype=torch.float16, device=device), None, 16)
-    codes = torch.empty((n_outer, t_cap, H, d * bits // 8), dtype=torch.uint8, device=device)
-    scales = torch.empty((n_outer, t_cap, H, d // group), dtype=torch.float32, device=device)
+        return Side(torch.empty((n_outer, H, t_cap, d), dtype=torch.float16, device=device), None, 16)
+    codes = torch.empty((n_outer, H, t_cap, d * bits // 8), dtype=torch.uint8, device=device)
+    scales = torch.empty((n_outer, H, t_cap, d // group), dtype=torch.float32, device=device)
     return Side(codes, scales, bits)
 
 

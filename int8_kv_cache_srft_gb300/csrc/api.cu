@@ -150,35 +150,31 @@ bool encode_tiled_swz(CUtensorMap* map, CUtensorMapDataType dt, int rank, void* 
     return true;
 }
 
-bool encode_row_map(CUtensorMap* map, void* base, int d, long long rows_per_outer, int n_outer, int box_rows) {
-    auto enc = encoder();
-    if (!enc) {
-        set_error("cuTensorMapEncodeTiled is unavailable from the driver");
-        return false;
+bool encode_x_map(CUtensorMap* map, void* base, int d, int H, int n_tokens, int n_outer, int box_rows, bool swz128) {
+    // fp16 rows x[n_outer][n_tokens][H][d]; one box = box_rows tokens of one (outer, head)
+    const unsigned long long e = 2;
+    if (swz128) {  // 128-byte swizzled k-blocks of 64 elements (d == 128)
+        const unsigned long long dims[4] = {(unsigned long long)d, (unsigned long long)H, (unsigned long long)n_tokens,
+                                            (unsigned long long)n_outer};
+        const unsigned long long str[3] = {d * e, (unsigned long long)H * d * e, (unsigned long long)n_tokens * H * d * e};
+        const unsigned box[4] = {64u, 1u, (unsigned)box_rows, 1u};
+        return encode_tiled_swz(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, base, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B,
+                                "x rows (swizzled)");
     }
-    CUresult r;
-    if (d <= 128) {
-        const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows_per_outer, (cuuint64_t)n_outer};
-        const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows_per_outer * d * 2};
-        const cuuint32_t box[3] = {(cuuint32_t)(d + 8), (cuuint32_t)box_rows, 1};
-        const cuuint32_t estr[3] = {1, 1, 1};
-        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    } else {
-        const int half = d / 2;
-        const cuuint64_t dims[4] = {(cuuint64_t)half, 2, (cuuint64_t)rows_per_outer, (cuuint64_t)n_outer};
-        const cuuint64_t strides[3] = {(cuuint64_t)half * 2, (cuuint64_t)d * 2, (cuuint64_t)rows_per_outer * d * 2};
-        const cuuint32_t box[4] = {(cuuint32_t)(half + 8), 2, (cuuint32_t)box_rows, 1};
-        const cuuint32_t estr[4] = {1, 1, 1, 1};
-        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (d <= 128) {  // rows land padded by 8 elements (the zero-filled columns past d)
+        const unsigned long long dims[4] = {(unsigned long long)d, (unsigned long long)H, (unsigned long long)n_tokens,
+                                            (unsigned long long)n_outer};
+        const unsigned long long str[3] = {d * e, (unsigned long long)H * d * e, (unsigned long long)n_tokens * H * d * e};
+        const unsigned box[4] = {(unsigned)(d + 8), 1u, (unsigned)box_rows, 1u};
+        return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, base, dims, str, box, "x rows");
     }
-    if (r != CUDA_SUCCESS) {
-        set_error("cuTensorMapEncodeTiled failed (CUresult %d) for d=%d rows=%lld outer=%d", (int)r, d, rows_per_outer,
-                  n_outer);
-        return false;
-    }
-    return true;
+    const int half = d / 2;  // d = 256: two halves of 128 (+8 padding) each
+    const unsigned long long dims[5] = {(unsigned long long)half, 2, (unsigned long long)H, (unsigned long long)n_tokens,
+                                        (unsigned long long)n_outer};
+    const unsigned long long str[4] = {half * e, d * e, (unsigned long long)H * d * e,
+                                       (unsigned long long)n_tokens * H * d * e};
+    const unsigned box[5] = {(unsigned)(half + 8), 2u, 1u, (unsigned)box_rows, 1u};
+    return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 5, base, dims, str, box, "x rows (d=256)");
 }
 
 // ---------------------------------------------------------------------------

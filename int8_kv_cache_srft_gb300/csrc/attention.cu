@@ -43,6 +43,12 @@ namespace srftkv {
 static __device__ unsigned int g_attn_fault;
 
 constexpr int kAttnWarps = 4;
+#ifndef SRFTKV_ATTN_STAGES
+#define SRFTKV_ATTN_STAGES 2  // TMA stages per warp (chunks in flight + 1)
+#endif
+#ifndef SRFTKV_ATTN_CH
+#define SRFTKV_ATTN_CH 0      // tokens per chunk; 0 = 32, or 16 when a 32-token stage would exceed 9 KB
+#endif
 
 struct AttnParams {
     const uint16_t* q;     // fp16 [B][Hq][D]
@@ -136,13 +142,14 @@ struct AttnCfg {
     static constexpr bool QK = BK != 16, QV = BV != 16;
     static constexpr int SPMAX = D / 16 + 4;                       // padded scale row, floats
     static constexpr int STAGE32 = 32 * (PlaneT<D, BK>::RP + PlaneT<D, BV>::RP + (QK ? SPMAX * 4 : 0) + (QV ? SPMAX * 4 : 0));
-    static constexpr int CH = STAGE32 <= 9216 ? 32 : 16;           // tokens per chunk
+    static constexpr int CH = SRFTKV_ATTN_CH ? SRFTKV_ATTN_CH : (STAGE32 <= 9216 ? 32 : 16);  // tokens per chunk
+    static constexpr int NS = SRFTKV_ATTN_STAGES;
     static constexpr int OFF_KC = 0;
     static constexpr int OFF_KS = OFF_KC + CH * PlaneT<D, BK>::RP;
     static constexpr int OFF_VC = OFF_KS + (QK ? CH * SPMAX * 4 : 0);
     static constexpr int OFF_VS = OFF_VC + CH * PlaneT<D, BV>::RP;
     static constexpr int STAGE = ((OFF_VS + (QV ? CH * SPMAX * 4 : 0)) + 127) / 128 * 128;
-    static constexpr int WARP_BYTES = 2 * STAGE;
+    static constexpr int WARP_BYTES = NS * STAGE;
     static constexpr int MERGE_BYTES = kAttnWarps * (4 * D + 8) * 4;
     static constexpr int BODY = kAttnWarps * WARP_BYTES > MERGE_BYTES ? kAttnWarps * WARP_BYTES : MERGE_BYTES;
     static constexpr int SMEM = 128 + BODY;
@@ -527,15 +534,17 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 3)
     const int cps = (n_chunks + P.n_splits - 1) / P.n_splits;
     const int c_begin = split * cps, c_end = min(c_begin + cps, n_chunks);
 
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // 4 per warp
     uint8_t* wbase = smem + 128 + warp * C::WARP_BYTES;
-    const uint32_t bar0 = ptx::smem_u32(&bars[2 * warp]), bar1 = ptx::smem_u32(&bars[2 * warp + 1]);
+    constexpr int NS = C::NS;
+    static_assert(NS >= 2 && NS <= 4, "stages per warp");
     if (lane == 0) {
-        ptx::mbar_init(bar0, 1);
-        ptx::mbar_init(bar1, 1);
+#pragma unroll
+        for (int s2 = 0; s2 < NS; ++s2) ptx::mbar_init(ptx::smem_u32(&bars[4 * warp + s2]), 1);
         ptx::fence_barrier_init();
     }
     __syncwarp();
+    auto barw = [&](int s2) { return ptx::smem_u32(&bars[4 * warp + s2]); };
 
     uint32_t qh[C::QB], ql[C::QB];
     build_qb<D, BK>(P.qt + ((long long)b * P.Hq + (long long)hkv * P.rep) * D, P.rep, g, c, qh, ql);
@@ -544,33 +553,40 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 3)
     for (int i = 0; i < C::ACC; ++i) acc[i] = 0.f;
     float m = -INFINITY, l = 0.f;  // online-softmax state for head c (log2 domain)
 
-    const int row_base = b * P.t_cap;
+    const int plane_row = b * P.Hkv + hkv;  // this (batch, kv head)'s rows in the head-major planes
     const uint32_t kc_bytes = C::CH * PlaneT<D, BK>::RP, vc_bytes = C::CH * PlaneT<D, BV>::RP;
     const uint32_t sc_bytes = C::CH * P.sp * 4;
     const uint32_t tx = kc_bytes + vc_bytes + (C::QK ? sc_bytes : 0) + (C::QV ? sc_bytes : 0);
     auto issue = [&](int chunk, int st) {
-        const uint32_t bar = st ? bar1 : bar0;
+        const uint32_t bar = barw(st);
         uint8_t* dst = wbase + st * C::STAGE;
-        const int row = row_base + chunk * C::CH;
+        const int tok = chunk * C::CH;
         ptx::mbar_arrive_expect_tx(bar, tx);
-        ptx::tma_load_3d(ptx::smem_u32(dst + C::OFF_KC), &tm_kc, bar, 0, hkv, row);
-        if constexpr (C::QK) ptx::tma_load_3d(ptx::smem_u32(dst + C::OFF_KS), &tm_ks, bar, 0, hkv, row);
-        ptx::tma_load_3d(ptx::smem_u32(dst + C::OFF_VC), &tm_vc, bar, 0, hkv, row);
-        if constexpr (C::QV) ptx::tma_load_3d(ptx::smem_u32(dst + C::OFF_VS), &tm_vs, bar, 0, hkv, row);
+        ptx::tma_load_3d(ptx::smem_u32(dst + C::OFF_KC), &tm_kc, bar, 0, tok, plane_row);
+        if constexpr (C::QK) ptx::tma_load_3d(ptx::smem_u32(dst + C::OFF_KS), &tm_ks, bar, 0, tok, plane_row);
+        ptx::tma_load_3d(ptx::smem_u32(dst + C::OFF_VC), &tm_vc, bar, 0, tok, plane_row);
+        if constexpr (C::QV) ptx::tma_load_3d(ptx::smem_u32(dst + C::OFF_VS), &tm_vs, bar, 0, tok, plane_row);
     };
 
+    // per-warp ring of NS stages: chunk j of this warp goes to stage j % NS, NS-1 chunks in flight
     int chunk = c_begin + warp;
-    if (lane == 0 && chunk < c_end) issue(chunk, 0);
+    if (lane == 0) {
+#pragma unroll
+        for (int j = 0; j < NS - 1; ++j)
+            if (chunk + j * kAttnWarps < c_end) issue(chunk + j * kAttnWarps, j);
+    }
     bool failed = false;
     for (int it = 0; chunk < c_end; ++it, chunk += kAttnWarps) {
-        const int st = it & 1;
-        const bool has_next = chunk + kAttnWarps < c_end;
-        if (lane == 0 && has_next) issue(chunk + kAttnWarps, st ^ 1);
-        const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(st ? bar1 : bar0, (it >> 1) & 1));
+        const int st = it % NS;
+        const int nxt = chunk + (NS - 1) * kAttnWarps;
+        if (lane == 0 && nxt < c_end) issue(nxt, (it + NS - 1) % NS);
+        const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(barw(st), (it / NS) & 1));
         if (!ok) {
             if (lane == 0) {
                 atomicOr(&g_attn_fault, 1u);
-                if (has_next) ptx::mbar_wait_bounded(st ? bar0 : bar1, ((it + 1) >> 1) & 1, 1u << 16);
+                for (int j = 1; j < NS; ++j)  // let the copies already in flight land before returning
+                    if (chunk + j * kAttnWarps < c_end)
+                        ptx::mbar_wait_bounded(barw((it + j) % NS), ((it + j) / NS) & 1, 1u << 16);
             }
             failed = true;
             break;
@@ -692,13 +708,16 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const __grid_constant
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
+// A plane [B*Hkv][t_cap][row] (head-major: the rows of one (batch, kv head)
+// are contiguous); a box is box_rows consecutive tokens, each row padded to
+// box_inner elements in shared memory.
 static bool encode_plane(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int inner_elems, int elem_bytes,
-                         int box_inner, int Hkv, long long rows, int box_rows) {
-    const unsigned long long dims[3] = {(unsigned long long)inner_elems, (unsigned long long)Hkv,
-                                        (unsigned long long)rows};
+                         int box_inner, long long bh, int t_cap, int box_rows) {
+    const unsigned long long dims[3] = {(unsigned long long)inner_elems, (unsigned long long)t_cap,
+                                        (unsigned long long)bh};
     const unsigned long long strides[2] = {(unsigned long long)inner_elems * elem_bytes,
-                                           (unsigned long long)inner_elems * elem_bytes * Hkv};
-    const unsigned box[3] = {(unsigned)box_inner, 1u, (unsigned)box_rows};
+                                           (unsigned long long)inner_elems * elem_bytes * t_cap};
+    const unsigned box[3] = {(unsigned)box_inner, (unsigned)box_rows, 1u};
     return encode_tiled(map, dt, 3, const_cast<void*>(base), dims, strides, box, "attention cache plane");
 }
 
@@ -714,20 +733,20 @@ template <int D, int BK, int BV>
 static int launch_split(const AttnLaunch& A) {
     using C = AttnCfg<D, BK, BV>;
     const AttnParams& P = A.P;
-    const long long rows = (long long)P.B * P.t_cap;
+    const long long bh = (long long)P.B * P.Hkv;
     CUtensorMap tkc, tks, tvc, tvs;
     if (!encode_plane(&tkc, A.k->codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, PlaneT<D, BK>::RB / 4, 4,
-                      PlaneT<D, BK>::RB / 4 + 4, P.Hkv, rows, C::CH))
+                      PlaneT<D, BK>::RB / 4 + 4, bh, P.t_cap, C::CH))
         return SRFTKV_ERR_CUDA;
     if (!encode_plane(&tvc, A.v->codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, PlaneT<D, BV>::RB / 4, 4,
-                      PlaneT<D, BV>::RB / 4 + 4, P.Hkv, rows, C::CH))
+                      PlaneT<D, BV>::RB / 4 + 4, bh, P.t_cap, C::CH))
         return SRFTKV_ERR_CUDA;
     const int ng = D / P.group;
     tks = tkc;
     tvs = tvc;
-    if (C::QK && !encode_plane(&tks, A.k->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ng, 4, P.sp, P.Hkv, rows, C::CH))
+    if (C::QK && !encode_plane(&tks, A.k->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ng, 4, P.sp, bh, P.t_cap, C::CH))
         return SRFTKV_ERR_CUDA;
-    if (C::QV && !encode_plane(&tvs, A.v->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ng, 4, P.sp, P.Hkv, rows, C::CH))
+    if (C::QV && !encode_plane(&tvs, A.v->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ng, 4, P.sp, bh, P.t_cap, C::CH))
         return SRFTKV_ERR_CUDA;
     static bool attr = false;
     if (!attr) {
@@ -824,7 +843,7 @@ int attention_entry(const void* q, float* out, const srftkv_side* k, const srftk
     if ((reinterpret_cast<uintptr_t>(k->codes) | reinterpret_cast<uintptr_t>(v->codes) |
          reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15)
         return invalid_attn("attention: q, out and codes must be 16-byte aligned");
-    if ((long long)B * t_cap > (1ll << 31) - 1) return invalid_attn("attention: B * t_cap too large");
+    if ((long long)B * Hkv > (1ll << 31) - 1) return invalid_attn("attention: B * Hkv too large");
     if (n_splits < 0) return invalid_attn("attention: n_splits must be >= 0");
     if (B == 0) return SRFTKV_OK;
     const int rc0 = current_device_ok();

@@ -10,7 +10,8 @@
 //
 // GB300 mapping: one thread owns one head vector for the whole pipeline, so
 // the FFT, the group maxima and the packing never leave registers and need
-// no shuffles.  Each warp streams tiles of 32 vectors: a TMA tensor copy
+// no shuffles.  Each warp streams tiles of 32 tokens of one (outer, head):
+// their packed rows are contiguous in the head-major planes.  A TMA tensor copy
 // brings the fp16 rows into shared memory padded by 16 bytes per row (the
 // box is 8 elements wider than the tensor; the extra columns are the zero
 // fill), which makes the row-per-thread 16-byte reads bank-conflict free.
@@ -38,9 +39,9 @@ struct CodecSideK {
 struct CodecParams {
     CodecSideK side[2];
     int n_outer, H, t_cap, t_offset, group;
-    int rows_per_outer;   // n_tokens * H
-    int tiles_per_outer;  // ceil(rows_per_outer / 32)
-    int tiles_per_side;   // n_outer * tiles_per_outer
+    int n_tokens;
+    int tiles_per_head;   // ceil(n_tokens / rows per tile)
+    int tiles_per_side;   // n_outer * H * tiles_per_head
     int total_tiles;      // n_sides * tiles_per_side
     unsigned int* fault;  // device fault word (bit 0: a bounded wait gave up)
     uint32_t sign_mask[128];
@@ -62,16 +63,26 @@ struct Geo {
     }
 };
 
+// A tile is a block of ROWS consecutive tokens of one (side, outer, head): its
+// fp16 rows are strided by H*d in x, its packed rows are contiguous in the
+// head-major planes.
 struct TileId {
-    int side, o, row0;
+    int side, o, h, t0;
 };
+template <int ROWS>
 __device__ __forceinline__ TileId decode_tile(const CodecParams& P, int t) {
     TileId id;
     id.side = t / P.tiles_per_side;
     const int rem = t - id.side * P.tiles_per_side;
-    id.o = rem / P.tiles_per_outer;
-    id.row0 = (rem - id.o * P.tiles_per_outer) * 32;
+    const int oh = rem / P.tiles_per_head;
+    id.t0 = (rem - oh * P.tiles_per_head) * ROWS;
+    id.o = oh / P.H;
+    id.h = oh - id.o * P.H;
     return id;
+}
+// packed row of token t of a tile: [outer][head][t_cap]
+__device__ __forceinline__ long long packed_row(const CodecParams& P, const TileId& id, int t) {
+    return ((long long)id.o * P.H + id.h) * P.t_cap + P.t_offset + t;
 }
 
 // ---------------------------------------------------------------------------
@@ -191,7 +202,7 @@ __device__ __forceinline__ void quantize_tile(const CodecParams& P, const TileId
     using Gm = Geo<D>;
     constexpr int N = D / 2;
     const CodecSideK& S = P.side[id.side];
-    const int r = id.row0 + lane;
+    const int t = id.t0 + lane;
     const uint16_t* row = buf + lane * Gm::ROW_H;
     float zr[N], zi[N];
 #pragma unroll
@@ -205,10 +216,10 @@ __device__ __forceinline__ void quantize_tile(const CodecParams& P, const TileId
     fft<N, false>(zr, zi);
     float z[D];
     split_forward<D>(zr, zi, z);
-    if (r >= P.rows_per_outer) return;
+    if (t >= P.n_tokens) return;
     if (S.lambda != nullptr) {
         const float4* lr =
-            reinterpret_cast<const float4*>(S.lambda + (long long)id.o * S.lambda_outer_stride + (long long)(r % P.H) * D);
+            reinterpret_cast<const float4*>(S.lambda + (long long)id.o * S.lambda_outer_stride + (long long)id.h * D);
 #pragma unroll
         for (int c = 0; c < D / 4; ++c) {
             const float4 l = __ldg(lr + c);
@@ -218,7 +229,7 @@ __device__ __forceinline__ void quantize_tile(const CodecParams& P, const TileId
             z[4 * c + 3] *= l.w;
         }
     }
-    const long long vrow = ((long long)id.o * P.t_cap + P.t_offset) * P.H + r;
+    const long long vrow = packed_row(P, id, t);
     // with equal widths on both sides only one epilogue is compiled
     if (BK == BV || id.side == 0)
         quant_store_row<D, BK>(z, P.group, S.codes + vrow * (D * BK / 8), S.scales + vrow * (D / P.group));
@@ -245,15 +256,15 @@ __global__ void __launch_bounds__(128, Geo<D>::MIN_BLOCKS)
     const int stride = gridDim.x * Gm::WARPS;
     int tile = blockIdx.x * Gm::WARPS + warp;
     auto issue = [&](int t, int b) {
-        const TileId id = decode_tile(P, t);
+        const TileId id = decode_tile<32>(P, t);
         const CUtensorMap* tm = id.side ? &tm1 : &tm0;
         const uint32_t bar = b ? bar1 : bar0;
         const uint32_t dst = ptx::smem_u32(bufs + b * Gm::BUF_BYTES);
         ptx::mbar_arrive_expect_tx(bar, Gm::BUF_BYTES);
         if constexpr (D == 256)
-            ptx::tma_load_4d(dst, tm, bar, 0, 0, id.row0, id.o);
+            ptx::tma_load_5d(dst, tm, bar, 0, 0, id.h, id.t0, id.o);
         else
-            ptx::tma_load_3d(dst, tm, bar, 0, id.row0, id.o);
+            ptx::tma_load_4d(dst, tm, bar, 0, id.h, id.t0, id.o);
     };
     if (lane == 0 && tile < P.total_tiles) issue(tile, 0);
     for (int it = 0; tile < P.total_tiles; ++it, tile += stride) {
@@ -268,7 +279,7 @@ __global__ void __launch_bounds__(128, Geo<D>::MIN_BLOCKS)
             }
             return;
         }
-        quantize_tile<D, BK, BV>(P, decode_tile(P, tile), reinterpret_cast<const uint16_t*>(bufs + b * Gm::BUF_BYTES), lane);
+        quantize_tile<D, BK, BV>(P, decode_tile<32>(P, tile), reinterpret_cast<const uint16_t*>(bufs + b * Gm::BUF_BYTES), lane);
         __syncwarp();
     }
 }
@@ -288,13 +299,13 @@ __global__ void __launch_bounds__(128, Geo<D>::MIN_BLOCKS)
     const int stride = gridDim.x * Gm::WARPS;
     int it = 0;
     for (int tile = blockIdx.x * Gm::WARPS + warp; tile < P.total_tiles; tile += stride, ++it) {
-        const TileId id = decode_tile(P, tile);
+        const TileId id = decode_tile<32>(P, tile);
         const CodecSideK& S = P.side[id.side];
-        const int r = id.row0 + lane;
-        const bool valid = r < P.rows_per_outer;
+        const int t = id.t0 + lane;
+        const bool valid = t < P.n_tokens;
         float p[D];
         if (valid) {
-            const long long vrow = ((long long)id.o * P.t_cap + P.t_offset) * P.H + r;
+            const long long vrow = packed_row(P, id, t);
             const float* srow = S.scales + vrow * (D / P.group);
             if (BK == BV || id.side == 0)
                 dequant_load_row<D, BK>(S.codes + vrow * (D * BK / 8), srow, P.group, p);
@@ -302,7 +313,7 @@ __global__ void __launch_bounds__(128, Geo<D>::MIN_BLOCKS)
                 dequant_load_row<D, BV>(S.codes + vrow * (D * BV / 8), srow, P.group, p);
             if (S.lambda != nullptr) {
                 const float4* lr = reinterpret_cast<const float4*>(S.lambda + (long long)id.o * S.lambda_outer_stride +
-                                                                   (long long)(r % P.H) * D);
+                                                                   (long long)id.h * D);
 #pragma unroll
                 for (int c = 0; c < D / 4; ++c) {
                     const float4 l = __ldg(lr + c);
@@ -341,9 +352,9 @@ __global__ void __launch_bounds__(128, Geo<D>::MIN_BLOCKS)
         if (lane == 0) {
             const CUtensorMap* tm = id.side ? &tm1 : &tm0;
             if constexpr (D == 256)
-                ptx::tma_store_4d(tm, ptx::smem_u32(buf), 0, 0, id.row0, id.o);
+                ptx::tma_store_5d(tm, ptx::smem_u32(buf), 0, 0, id.h, id.t0, id.o);
             else
-                ptx::tma_store_3d(tm, ptx::smem_u32(buf), 0, id.row0, id.o);
+                ptx::tma_store_4d(tm, ptx::smem_u32(buf), 0, id.h, id.t0, id.o);
             ptx::bulk_commit();
         }
     }
@@ -365,9 +376,9 @@ static inline void fill_params(const CodecCall& c, CodecParams& P) {
     P.t_cap = c.t_cap;
     P.t_offset = c.t_offset;
     P.group = c.group;
-    P.rows_per_outer = c.n_tokens * c.H;
-    P.tiles_per_outer = (P.rows_per_outer + 31) / 32;
-    P.tiles_per_side = c.n_outer * P.tiles_per_outer;
+    P.n_tokens = c.n_tokens;
+    P.tiles_per_head = (c.n_tokens + 31) / 32;
+    P.tiles_per_side = c.n_outer * c.H * P.tiles_per_head;
     P.total_tiles = c.n_sides * P.tiles_per_side;
     for (int i = 0; i < 128; ++i) P.sign_mask[i] = 0;
     sign_masks(c.d, c.seed, P.sign_mask);
@@ -382,7 +393,7 @@ static int launch_codec(const CodecCall& c, bool quantize) {
     CUtensorMap tm[2];
     for (int s = 0; s < 2; ++s) {
         const CodecSideDesc& d = c.side[s < c.n_sides ? s : 0];
-        if (!encode_row_map(&tm[s], d.x, D, (long long)c.n_tokens * c.H, c.n_outer, Gm::ROWS)) return SRFTKV_ERR_CUDA;
+        if (!encode_x_map(&tm[s], d.x, D, c.H, c.n_tokens, c.n_outer, Gm::ROWS, false)) return SRFTKV_ERR_CUDA;
     }
     P.fault = codec_fault_word();
     if (!P.fault) return SRFTKV_ERR_CUDA;

@@ -48,14 +48,7 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-__device__ __forceinline__ TileId decode_tile128(const CodecParams& P, int t) {
-    TileId id;
-    id.side = t / P.tiles_per_side;
-    const int rem = t - id.side * P.tiles_per_side;
-    id.o = rem / P.tiles_per_outer;
-    id.row0 = (rem - id.o * P.tiles_per_outer) * TM;
-    return id;
-}
+__device__ __forceinline__ TileId decode_tile128(const CodecParams& P, int t) { return decode_tile<TM>(P, t); }
 
 // Byte offset of element (row n, column k) of a 128 x 128 fp16 operand stored
 // K-major in two 128-byte-swizzled k-blocks (the layout TMA's 128-byte swizzle
@@ -137,8 +130,8 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
                 const CUtensorMap* tm = id.side ? &tm1 : &tm0;
                 const uint32_t dst = sbase + T_OFF_A + s * T_A_BYTES;
                 ptx::mbar_arrive_expect_tx(bar(s), T_A_BYTES);
-                ptx::tma_load_3d(dst, tm, bar(s), 0, id.row0, id.o);
-                ptx::tma_load_3d(dst + T_KB_BYTES, tm, bar(s), 64, id.row0, id.o);
+                ptx::tma_load_4d(dst, tm, bar(s), 0, id.h, id.t0, id.o);
+                ptx::tma_load_4d(dst + T_KB_BYTES, tm, bar(s), 64, id.h, id.t0, id.o);
             }
         }
     } else if (warp == 1) {
@@ -186,8 +179,8 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
 
             const TileId id = decode_tile128(P, t);
             const CodecSideK& S = P.side[id.side];
-            const int r = id.row0 + 32 * quarter + lane;
-            if (r >= P.rows_per_outer) continue;
+            const int t_tok = id.t0 + 32 * quarter + lane;
+            if (t_tok >= P.n_tokens) continue;
             float z[64];
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
@@ -196,7 +189,7 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
             }
             if (S.lambda != nullptr) {
                 const float4* lr = reinterpret_cast<const float4*>(
-                    S.lambda + (long long)id.o * S.lambda_outer_stride + (long long)(r % P.H) * TD + half * 64);
+                    S.lambda + (long long)id.o * S.lambda_outer_stride + (long long)id.h * TD + half * 64);
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     const float4 l = __ldg(lr + c);
@@ -206,7 +199,7 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
                     z[4 * c + 3] *= l.w;
                 }
             }
-            const long long vrow = ((long long)id.o * P.t_cap + P.t_offset) * P.H + r;
+            const long long vrow = packed_row(P, id, t_tok);
             const int ng = TD / P.group;
             if (BK == BV || id.side == 0)
                 quant_store_row<64, BK>(z, P.group, S.codes + vrow * (TD * BK / 8) + half * (64 * BK / 8),
@@ -394,10 +387,11 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
                 const TileId id = decode_tile128(P, t);
                 const int bits = (BK == BV || id.side == 0) ? BK : BV;
                 const uint32_t dst = sbase + DQ_OFF_IN + st * C::STAGE;
-                const int row = P.t_offset * P.H + id.row0;
+                const int row = P.t_offset + id.t0;   // packed planes: [outer*H][t_cap] rows
+                const int oh = id.o * P.H + id.h;
                 ptx::mbar_arrive_expect_tx(bar(8 + st), TM * (TD * bits / 8 + 16) + TM * (TD / P.group + 4) * 4);
-                ptx::tma_load_3d(dst, &M.codes[id.side], bar(8 + st), 0, row, id.o);
-                ptx::tma_load_3d(dst + C::OFF_SC, &M.scales[id.side], bar(8 + st), 0, row, id.o);
+                ptx::tma_load_3d(dst, &M.codes[id.side], bar(8 + st), 0, row, oh);
+                ptx::tma_load_3d(dst + C::OFF_SC, &M.scales[id.side], bar(8 + st), 0, row, oh);
             }
         }
     } else if (warp <= 5) {
@@ -406,7 +400,7 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
             const int s = i & 1, st = i % C::STAGES;
             const TileId id = decode_tile128(P, t);
             const CodecSideK& S = P.side[id.side];
-            const int r = id.row0 + m;
+            const int t_tok = id.t0 + m;
             const bool ok_in = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(bar(8 + st), (i / C::STAGES) & 1));
             if (!ok_in) {
                 failed = true;
@@ -421,9 +415,9 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
                 dequant_row_smem<TD, BV>(in + m * (TD * BV / 8 + 16), srow, P.group, p);
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(11 + st));  // input stage consumed
-            if (r < P.rows_per_outer && S.lambda != nullptr) {
+            if (t_tok < P.n_tokens && S.lambda != nullptr) {
                 const float4* lr = reinterpret_cast<const float4*>(S.lambda + (long long)id.o * S.lambda_outer_stride +
-                                                                   (long long)(r % P.H) * TD);
+                                                                   (long long)id.h * TD);
 #pragma unroll
                 for (int c = 0; c < TD / 4; ++c) {
                     const float4 l = __ldg(lr + c);
@@ -492,8 +486,8 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
             if (leader) {
                 const TileId id = decode_tile128(P, t);
                 const uint32_t src = sbase + DQ_OFF_O;
-                ptx::tma_store_3d(&M.out[id.side], src, 0, id.row0, id.o);
-                ptx::tma_store_3d(&M.out[id.side], src + T_KB_BYTES, 64, id.row0, id.o);
+                ptx::tma_store_4d(&M.out[id.side], src, 0, id.h, id.t0, id.o);
+                ptx::tma_store_4d(&M.out[id.side], src + T_KB_BYTES, 64, id.h, id.t0, id.o);
                 ptx::bulk_commit();
             }
         }
@@ -511,28 +505,25 @@ static int launch_dq_tc(const CodecCall& c) {
     using C = DqCfg<BK, BV>;
     CodecParams P;
     fill_params(c, P);
-    P.tiles_per_outer = (P.rows_per_outer + TM - 1) / TM;
-    P.tiles_per_side = c.n_outer * P.tiles_per_outer;
+    P.tiles_per_head = (c.n_tokens + TM - 1) / TM;
+    P.tiles_per_side = c.n_outer * c.H * P.tiles_per_head;
     P.total_tiles = c.n_sides * P.tiles_per_side;
     P.fault = codec_fault_word();
     if (!P.fault) return SRFTKV_ERR_CUDA;
     DqMaps M;
-    const unsigned long long rows = (unsigned long long)c.n_tokens * c.H, crows = (unsigned long long)c.t_cap * c.H;
+    const unsigned long long tcap = (unsigned long long)c.t_cap, nrow = (unsigned long long)c.n_outer * c.H;
     const int ng = TD / c.group;
     for (int s = 0; s < 2; ++s) {
         const CodecSideDesc& d = c.side[s < c.n_sides ? s : 0];
-        const unsigned long long odims[3] = {(unsigned long long)TD, rows, (unsigned long long)c.n_outer};
-        const unsigned long long ostr[2] = {TD * 2ull, rows * TD * 2ull};
-        const unsigned obox[3] = {64u, (unsigned)TM, 1u};
         const int rb = TD * d.bits / 8;
-        const unsigned long long cdims[3] = {(unsigned long long)rb / 4, crows, (unsigned long long)c.n_outer};
-        const unsigned long long cstr[2] = {(unsigned long long)rb, crows * rb};
+        // packed planes [n_outer*H][t_cap][row], row padded by 16 bytes in shared memory
+        const unsigned long long cdims[3] = {(unsigned long long)rb / 4, tcap, nrow};
+        const unsigned long long cstr[2] = {(unsigned long long)rb, tcap * rb};
         const unsigned cbox[3] = {(unsigned)(rb / 4 + 4), (unsigned)TM, 1u};
-        const unsigned long long sdims[3] = {(unsigned long long)ng, crows, (unsigned long long)c.n_outer};
-        const unsigned long long sstr[2] = {ng * 4ull, crows * ng * 4ull};
+        const unsigned long long sdims[3] = {(unsigned long long)ng, tcap, nrow};
+        const unsigned long long sstr[2] = {ng * 4ull, tcap * ng * 4ull};
         const unsigned sbox[3] = {(unsigned)(ng + 4), (unsigned)TM, 1u};
-        if (!encode_tiled_swz(&M.out[s], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, d.x, odims, ostr, obox,
-                              CU_TENSOR_MAP_SWIZZLE_128B, "tensor-core dequantize output") ||
+        if (!encode_x_map(&M.out[s], d.x, TD, c.H, c.n_tokens, c.n_outer, TM, true) ||
             !encode_tiled(&M.codes[s], CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, d.codes, cdims, cstr, cbox,
                           "tensor-core dequantize codes") ||
             !encode_tiled(&M.scales[s], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, d.scales, sdims, sstr, sbox,
@@ -559,21 +550,15 @@ template <int BK, int BV>
 static int launch_tc(const CodecCall& c) {
     CodecParams P;
     fill_params(c, P);
-    P.tiles_per_outer = (P.rows_per_outer + TM - 1) / TM;
-    P.tiles_per_side = c.n_outer * P.tiles_per_outer;
+    P.tiles_per_head = (c.n_tokens + TM - 1) / TM;
+    P.tiles_per_side = c.n_outer * c.H * P.tiles_per_head;
     P.total_tiles = c.n_sides * P.tiles_per_side;
     P.fault = codec_fault_word();
     if (!P.fault) return SRFTKV_ERR_CUDA;
     CUtensorMap tm[2];
     for (int s = 0; s < 2; ++s) {
         const CodecSideDesc& d = c.side[s < c.n_sides ? s : 0];
-        const unsigned long long rows = (unsigned long long)c.n_tokens * c.H;
-        const unsigned long long dims[3] = {(unsigned long long)TD, rows, (unsigned long long)c.n_outer};
-        const unsigned long long strides[2] = {TD * 2ull, rows * TD * 2ull};
-        const unsigned box[3] = {64u, (unsigned)TM, 1u};
-        if (!encode_tiled_swz(&tm[s], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, d.x, dims, strides, box,
-                              CU_TENSOR_MAP_SWIZZLE_128B, "tensor-core codec rows"))
-            return SRFTKV_ERR_CUDA;
+        if (!encode_x_map(&tm[s], d.x, TD, c.H, c.n_tokens, c.n_outer, TM, true)) return SRFTKV_ERR_CUDA;
     }
     static bool attr = false;
     if (!attr) {

@@ -15,8 +15,8 @@ namespace srftkv {
 // One side (K or V) of a codec call, after validation.
 struct CodecSideDesc {
     void* x;              // fp16 rows [n_outer][n_tokens][H][d]
-    uint8_t* codes;       // [n_outer][t_cap][H][d*bits/8]
-    float* scales;        // [n_outer][t_cap][H][d/group]
+    uint8_t* codes;       // [n_outer][H][t_cap][d*bits/8]
+    float* scales;        // [n_outer][H][t_cap][d/group]
     const float* lambda;  // [*][H][d] or null
     int64_t lambda_outer_stride;
     int bits;
@@ -34,11 +34,12 @@ struct CodecCall {
 // s_{2n} = -1 and bit 31 set when s_{2n+1} = -1 (d/2 words).
 void sign_masks(int d, uint64_t seed, uint32_t* words);
 
-// 3D (d <= 128) or 4D (d == 256) tensor map over fp16 rows
-// [n_outer][rows_per_outer][d] whose box is `box_rows` rows of d + 8
-// elements (256: two halves of 136), so that each row lands in shared memory
-// padded by 16 bytes.  Returns false and sets the error message on failure.
-bool encode_row_map(CUtensorMap* map, void* base, int d, long long rows_per_outer, int n_outer, int box_rows);
+// Tensor map over fp16 rows x[n_outer][n_tokens][H][d] whose box is
+// box_rows consecutive tokens of one (outer, head).  Plain: rows land in
+// shared memory padded by 8 elements (d <= 128; d = 256 as two padded
+// halves).  swz128 (d = 128): two 64-element k-blocks in the 128-byte
+// swizzle layout of the tensor-core operands.  False + message on failure.
+bool encode_x_map(CUtensorMap* map, void* base, int d, int H, int n_tokens, int n_outer, int box_rows, bool swz128);
 
 int codec_quantize(const CodecCall& c);
 int codec_dequantize(const CodecCall& c);

@@ -46,7 +46,7 @@ def build_cache(B, Hkv, d, t_cap, bits_k, bits_v, group, seed, lam=False, data_s
         x = I.kv_side(w, name, device="cuda")
         lt = I.lam_table(w, name, device="cuda")
         if bits == 16:
-            s = K.Side(x.contiguous(), None, 16)
+            s = K.Side(x.permute(0, 2, 1, 3).contiguous(), None, 16)  # head-major raw cache
         else:
             s = K.alloc_side(B, t_cap, Hkv, d, bits, group)
             s.x, s.lam = x, lt
@@ -66,10 +66,11 @@ def run_attention(q, sk, sv, B, Hq, Hkv, d, group, t_cap, seq_lens, seed, n_spli
 
 
 def oracle_side(s, group, rows=None):
+    """The oracle's token-major view [B][T][H][...] of a head-major side."""
     if s.bits == 16:
-        v = _np(s.codes)
+        v = _np(s.codes).transpose(0, 2, 1, 3)
         return {"bits": 16, "values": v if rows is None else v[rows]}
-    codes, scales = _np(s.codes), _np(s.scales).astype(np.float64)
+    codes, scales = _np(s.codes).transpose(0, 2, 1, 3), _np(s.scales).transpose(0, 2, 1, 3).astype(np.float64)
     lam = None if s.lam is None else _np(s.lam).astype(np.float64)
     if rows is not None:
         codes, scales = codes[rows], scales[rows]
@@ -145,8 +146,8 @@ def test_raw_fp16_cache_ignores_garbage_past_sequence_end():
     q = I.query(I.Workload("q", n_outer=B, tokens=1, kv_heads=Hkv, d=d, q_heads=Hkv * rep, data_seed=2), device="cuda")
     seq = torch.tensor([37, 100], dtype=torch.int32, device="cuda")
     ref = oracle_attention(q, sk, sv, 16, seed, seq)
-    sk.codes[0, 37:] = float("nan")
-    sv.codes[0, 37:] = float("inf")
+    sk.codes[0, :, 37:] = float("nan")
+    sv.codes[0, :, 37:] = float("inf")
     out = run_attention(q, sk, sv, B, Hkv * rep, Hkv, d, 16, t_cap, seq, seed)
     assert np.isfinite(out).all() and np.abs(out - ref).max() <= ATTN_ATOL
 
@@ -164,12 +165,14 @@ def test_decode_workload_full_size_sampled():
     K.srft_kv_quantize(sk, sv, B, T, Hkv, d, 16, T, 0, w.sign_seed)
     q = I.query(w, device="cuda")
     out = run_attention(q, sk, sv, B, Hq, Hkv, d, 16, T, None, w.sign_seed)
-    out16 = run_attention(q, K.Side(xk, None, 16), K.Side(xv, None, 16), B, Hq, Hkv, d, 16, T, None, w.sign_seed)
+    rk, rv = xk.permute(0, 2, 1, 3).contiguous(), xv.permute(0, 2, 1, 3).contiguous()
+    out16 = run_attention(q, K.Side(rk, None, 16), K.Side(rv, None, 16), B, Hq, Hkv, d, 16, T, None, w.sign_seed)
+    del rk, rv
     qn = _np(q).astype(np.float64)
     for b, h in ((0, 0), (B - 1, Hkv - 1), (7, 3)):
-        kh = O.srft_kv_dequantize(_np(sk.codes[b, :, h]), _np(sk.scales[b, :, h]).astype(np.float64), None, 4, 16,
+        kh = O.srft_kv_dequantize(_np(sk.codes[b, h]), _np(sk.scales[b, h]).astype(np.float64), None, 4, 16,
                                   w.sign_seed)
-        vh = O.srft_kv_dequantize(_np(sv.codes[b, :, h]), _np(sv.scales[b, :, h]).astype(np.float64), None, 4, 16,
+        vh = O.srft_kv_dequantize(_np(sv.codes[b, h]), _np(sv.scales[b, h]).astype(np.float64), None, 4, 16,
                                   w.sign_seed)
         k16, v16 = _np(xk[b, :, h]).astype(np.float64), _np(xv[b, :, h]).astype(np.float64)
         for r in range(rep):

@@ -37,6 +37,17 @@ def _np(t):
     return t.detach().cpu().numpy()
 
 
+def tm(t):
+    """Token-major view [outer][token][head][...] of a head-major plane [outer][head][token][...]."""
+    return t.permute(0, 2, 1, 3)
+
+
+def hm_rows(rows, T, H):
+    """Head-major row indices of token-major rows (o*T + t)*H + h of a [outer][T][H] array."""
+    o, rem = rows // (T * H), rows % (T * H)
+    return (o * H + rem % H) * T + rem // H
+
+
 def _quantize_gpu(x_k, x_v, lam_k, lam_v, bits_k, bits_v, group, seed, t_cap=None, t_offset=0, sentinel=0xAB):
     n_outer, T, H, d = x_k.shape
     t_cap = T if t_cap is None else t_cap
@@ -61,8 +72,8 @@ def _oracle(x, lam, bits, group, seed):
 def _check_side(side, x, lam, bits, group, seed, t_offset=0):
     T = x.shape[1]
     enc, lam_b = _oracle(x, lam, bits, group, seed)
-    codes = _np(side.codes)[:, t_offset : t_offset + T]
-    scales = _np(side.scales)[:, t_offset : t_offset + T]
+    codes = _np(tm(side.codes))[:, t_offset : t_offset + T]
+    scales = _np(tm(side.scales))[:, t_offset : t_offset + T]
     assert_scales(scales, enc["scales"])
     st = assert_codes(codes, enc["r"], bits)
     return enc, lam_b, st
@@ -98,7 +109,8 @@ def test_tiny_round_trip_workload():
         assert_dequant_within_step(xg, ref_hat, enc["scales"], None, w.group)
         assert_reconstruction_bound(xg, _np(x), enc["scales"], None, w.group)
         # tight: the GPU decode of the GPU codes against the oracle decode of the same codes
-        ref = O.srft_kv_dequantize(_np(side.codes), _np(side.scales).astype(np.float64), None, 4, w.group, w.sign_seed)
+        ref = O.srft_kv_dequantize(_np(tm(side.codes)), _np(tm(side.scales)).astype(np.float64), None, 4, w.group,
+                                   w.sign_seed)
         assert np.abs(xg - ref).max() <= np.abs(ref).max() * 2.0**-10 + 1e-5
 
 
@@ -117,7 +129,7 @@ def test_quantize_dequantize_ragged(d, bits, group, lam):
     sk, sv = _quantize_gpu(xk, xv, lk, lv, bits, bits_v, group, 11, t_cap=50, t_offset=5)
     for side, x, lam_t, b in ((sk, xk, lk, bits), (sv, xv, lv, bits_v)):
         enc, lam_b, _ = _check_side(side, x, lam_t, b, group, 11, t_offset=5)
-        codes = _np(side.codes)
+        codes = _np(tm(side.codes))
         assert (codes[:, :5] == 0xAB).all() and (codes[:, 42:] == 0xAB).all(), "rows outside the window were written"
         out = torch.empty_like(side.x)
         dq = K.Side(side.codes, side.scales, b, x=out, lam=side.lam)
@@ -145,7 +157,7 @@ def test_tensor_core_quantize_path(monkeypatch, bk, bv, group, lam):
     sk, sv = _quantize_gpu(xk, xv, lk, lv, bk, bv, group, 13, t_cap=310, t_offset=3)
     for side, x, lam_t, b in ((sk, xk, lk, bk), (sv, xv, lv, bv)):
         enc, lam_b, _ = _check_side(side, x, lam_t, b, group, 13, t_offset=3)
-        codes = _np(side.codes)
+        codes = _np(tm(side.codes))
         assert (codes[:, :3] == 0xAB).all() and (codes[:, 303:] == 0xAB).all()
         # and back through the tensor-core dequantize
         out = torch.empty_like(side.x)
@@ -156,7 +168,8 @@ def test_tensor_core_quantize_path(monkeypatch, bk, bv, group, lam):
         ref_hat = O.srft_kv_dequantize(enc["codes"], enc["scales"], lam_b, b, group, 13)
         assert_dequant_within_step(_np(out), ref_hat, enc["scales"], lam_full, group)
         assert_reconstruction_bound(_np(out), _np(x), enc["scales"], lam_full, group)
-        mine = O.srft_kv_dequantize(codes[:, 3:303], _np(side.scales)[:, 3:303].astype(np.float64), lam_b, b, group, 13)
+        mine = O.srft_kv_dequantize(codes[:, 3:303], _np(tm(side.scales))[:, 3:303].astype(np.float64), lam_b, b, group,
+                                    13)
         assert np.abs(_np(out) - mine).max() <= np.abs(mine).max() * 2.0**-10 + 1e-5
 
 
@@ -217,8 +230,9 @@ def test_qwen_shaped_full_size_sampled(monkeypatch, path):
         o_idx, h_idx = rows // (T * H), rows % H
         lam_rows = _np(lam)[o_idx, h_idx]
         enc = O.srft_kv_quantize(xs, lam_rows, 4, 16, w.sign_seed)
-        assert_scales(_np(side.scales.reshape(-1, d // 16)[rows]), enc["scales"])
-        assert_codes(_np(side.codes.reshape(-1, d // 2)[rows]), enc["r"], 4)
+        hrows = torch.as_tensor(hm_rows(rows, T, H), device="cuda")
+        assert_scales(_np(side.scales.reshape(-1, d // 16)[hrows]), enc["scales"])
+        assert_codes(_np(side.codes.reshape(-1, d // 2)[hrows]), enc["r"], 4)
         xg = _np(out.reshape(-1, d)[rows]).astype(np.float64)
         ref_hat = O.srft_kv_dequantize(enc["codes"], enc["scales"], lam_rows, 4, 16, w.sign_seed)
         assert_dequant_within_step(xg, ref_hat, enc["scales"], lam_rows, 16)
@@ -238,8 +252,8 @@ def test_k8v4_append_onto_prebuilt_cache():
     sk.x, sv.x = xk, xv
     K.srft_kv_quantize(sk, sv, n_outer, T, H, d, 16, t_cap, 0, w.sign_seed)
     torch.cuda.synchronize()
-    before_k = sk.codes[:, :T].clone()
-    before_v = sv.scales[:, :T].clone()
+    before_k = sk.codes[:, :, :T].clone()
+    before_v = sv.scales[:, :, :T].clone()
     g = torch.Generator(device="cuda").manual_seed(44)
     new = []
     for step in range(3):
@@ -249,18 +263,18 @@ def test_k8v4_append_onto_prebuilt_cache():
         K.srft_kv_quantize(ak, av, n_outer, 1, H, d, 16, t_cap, T + step, w.sign_seed)
         new.append((nk, nv))
     torch.cuda.synchronize()
-    assert torch.equal(before_k, sk.codes[:, :T]) and torch.equal(before_v, sv.scales[:, :T])
+    assert torch.equal(before_k, sk.codes[:, :, :T]) and torch.equal(before_v, sv.scales[:, :, :T])
     for step, (nk, nv) in enumerate(new):
         for side, x, bits in ((sk, nk, 8), (sv, nv, 4)):
             enc = O.srft_kv_quantize(_np(x).astype(np.float64), None, bits, 16, w.sign_seed)
-            assert_scales(_np(side.scales[:, T + step : T + step + 1]), enc["scales"])
-            assert_codes(_np(side.codes[:, T + step : T + step + 1]), enc["r"], bits)
+            assert_scales(_np(tm(side.scales)[:, T + step : T + step + 1]), enc["scales"])
+            assert_codes(_np(tm(side.codes)[:, T + step : T + step + 1]), enc["r"], bits)
     # sampled prefix rows against the oracle
     rows = _sample_rows(n_outer * T * H, 1000, 45)
     for side, x, bits in ((sk, xk, 8), (sv, xv, 4)):
         xs = _np(x.reshape(-1, d)[rows]).astype(np.float64)
         enc = O.srft_kv_quantize(xs, None, bits, 16, w.sign_seed)
         o_idx, rem = rows // (T * H), rows % (T * H)
-        crow = (o_idx * t_cap * H + rem)
+        crow = torch.as_tensor((o_idx * H + rem % H) * t_cap + rem // H, device="cuda")
         assert_codes(_np(side.codes.reshape(-1, d * bits // 8)[crow]), enc["r"], bits)
         assert_scales(_np(side.scales.reshape(-1, d // 16)[crow]), enc["scales"])
