@@ -83,25 +83,18 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
 // D = A . B + D, m16n8k16, fp16 inputs, fp32 accumulators
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
         "{%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ uint32_t h2_sub(uint32_t x, uint32_t c) {  // exact for the integer values used here
-    uint32_t r;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(c));
-    return r;
-}
-__device__ __forceinline__ uint32_t h2_fma(uint32_t x, uint32_t m, uint32_t c) {
-    uint32_t r;
-    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(m), "r"(c));
-    return r;
-}
-__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
-    __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&h);
+// D = A . B + (c0, c1, c0, c1): the accumulator starts from per-column values
+__device__ __forceinline__ void mma16816_c(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                           uint32_t b0, uint32_t b1, float c0, float c1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%10, %11, %10, %11};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1));
 }
 // (a, b) ~= hi + lo with both halves fp16: the MMA then sees a and b to about
 // 22 bits instead of 11 (codes are exact in fp16, so this is the only rounding
@@ -114,21 +107,21 @@ __device__ __forceinline__ void split_h2(float a, float b, uint32_t& hi, uint32_
     lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
-// Codes -> fp16 integer pairs.  Bits 0xF/0xF0000 (0xF0/0xF00000) hold two
-// two's-complement nibbles; XOR with 8 makes them offset binary, OR-ing the
-// fp16 exponent of 1024 makes the fp16 value 1024 + 8 + q (or 1024 + 16(8+q)),
-// and one f16x2 subtract (fma) gives q exactly.
-__device__ __forceinline__ uint32_t i4_lo(uint32_t w) {  // nibbles at bits 0 and 16
-    return h2_sub((w & 0x000F000Fu) ^ 0x64086408u, 0x64086408u);  // (1032, 1032)
-}
-__device__ __forceinline__ uint32_t i4_hi(uint32_t w) {  // nibbles at bits 4 and 20
-    return h2_fma((w & 0x00F000F0u) ^ 0x64806480u, 0x2C002C00u /* 1/16 */, 0xD480D480u /* -72 */);
-}
-__device__ __forceinline__ uint32_t i8_lo(uint32_t w) {  // bytes 0 and 2
-    return h2_sub((w & 0x00FF00FFu) ^ 0x64806480u, 0x64806480u);  // (1152, 1152)
-}
-__device__ __forceinline__ uint32_t i8_hi(uint32_t w) {  // bytes 1 and 3
-    return i8_lo(w >> 8);
+// Codes -> fp16 pairs in one logic op.  Bits 0xF/0xF0000 (0xF0/0xF00000)
+// hold two two's-complement nibbles; XOR with 8 makes them offset binary, and
+// with a zero exponent field the fp16 bit pattern is the subnormal
+// (q + 8) * 2^-24 (or (q + 8) * 2^-20 for the high nibbles), exactly.  Bytes
+// give (q + 128) * 2^-24.  The offset is removed after the contraction from the
+// column sums of the other operand (offset * sum of B), which is small enough
+// next to the signal that nothing is lost to cancellation; the unit 2^-24 is
+// folded into the score and output scaling.
+constexpr float kSub = 16777216.f;  // 2^24
+__device__ __forceinline__ uint32_t u4_lo(uint32_t w) { return (w & 0x000F000Fu) ^ 0x00080008u; }  // nibbles 0, 16
+__device__ __forceinline__ uint32_t u4_hi(uint32_t w) { return (w & 0x00F000F0u) ^ 0x00800080u; }  // nibbles 4, 20
+__device__ __forceinline__ uint32_t u8_lo(uint32_t w) { return (w & 0x00FF00FFu) ^ 0x00800080u; }  // bytes 0, 2
+__device__ __forceinline__ float h2_sum(uint32_t h) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+    return f.x + f.y;
 }
 
 template <int D, int BITS>
@@ -155,6 +148,7 @@ struct AttnCfg {
     static constexpr int SMEM = 128 + BODY;
     static constexpr int QB = D / 8;    // K-side B-fragment registers
     static constexpr int ACC = D / 4;   // V accumulators
+    static constexpr int NSV = BV == 4 ? D / 32 : BV == 8 ? D / 16 : 1;  // column sums of the V-side B
 };
 
 // ---------------------------------------------------------------------------
@@ -222,10 +216,15 @@ __global__ void __launch_bounds__(128) attn_prep_q_kernel(const __grid_constant_
 // every MMA is (query head n/2 of the group, half n%2): for 4-bit keys half 0
 // takes the dims of the first 16-dim group of each 32-dim chunk and half 1 the
 // second, so one MMA yields both groups' partials for a head in the two
-// columns one thread owns; for 8-bit and fp16 keys half 1 is zero.
+// columns one thread owns; for 8-bit and fp16 keys half 1 is zero.  The
+// high-nibble rows carry q / 16, matching their 16x larger code unit.
+//
+// nb[j] is minus the code offset times the column sum of B for the
+// accumulator columns this thread holds (4-bit: chunk j/2, column 2c + j%2;
+// 8-bit: chunk j, column 2c), in the 2^-24 unit of the codes.
 template <int D, int BK>
 __device__ __forceinline__ void build_qb(const float* __restrict__ qrow_base, int rep, int g, int c,
-                                         uint32_t (&qh)[D / 8], uint32_t (&ql)[D / 8]) {
+                                         uint32_t (&qh)[D / 8], uint32_t (&ql)[D / 8], float (&nb)[D / 16]) {
     const int h = g >> 1, sigma = g & 1;
     const bool head_ok = h < rep;
     const float* q = qrow_base + (long long)h * D;
@@ -233,13 +232,21 @@ __device__ __forceinline__ void build_qb(const float* __restrict__ qrow_base, in
     if constexpr (BK == 4) {
         // chunk m (32 dims): thread c owns dims 8c..8c+7, which lie in half c/2
         const bool ok = (c >> 1) == sigma;
+        constexpr float i16 = 0.0625f;
 #pragma unroll
         for (int m = 0; m < D / 32; ++m) {
             const int base = 32 * m + 8 * c;
             split_h2(val(base + 0, ok), val(base + 4, ok), qh[4 * m + 0], ql[4 * m + 0]);
-            split_h2(val(base + 1, ok), val(base + 5, ok), qh[4 * m + 1], ql[4 * m + 1]);
+            split_h2(val(base + 1, ok) * i16, val(base + 5, ok) * i16, qh[4 * m + 1], ql[4 * m + 1]);
             split_h2(val(base + 2, ok), val(base + 6, ok), qh[4 * m + 2], ql[4 * m + 2]);
-            split_h2(val(base + 3, ok), val(base + 7, ok), qh[4 * m + 3], ql[4 * m + 3]);
+            split_h2(val(base + 3, ok) * i16, val(base + 7, ok) * i16, qh[4 * m + 3], ql[4 * m + 3]);
+            // offset 8 per code; the high-nibble rows count 16x (their unit is 2^-20)
+            float part = h2_sum(qh[4 * m + 0]) + h2_sum(ql[4 * m + 0]) + h2_sum(qh[4 * m + 2]) + h2_sum(ql[4 * m + 2]);
+            part += 16.f * (h2_sum(qh[4 * m + 1]) + h2_sum(ql[4 * m + 1]) + h2_sum(qh[4 * m + 3]) + h2_sum(ql[4 * m + 3]));
+            part += __shfl_xor_sync(0xffffffffu, part, 1);
+            part += __shfl_xor_sync(0xffffffffu, part, 2);  // column g's total over its 16 k rows x 2 MMAs
+            nb[2 * m + 0] = (-8.f / kSub) * __shfl_sync(0xffffffffu, part, 4 * (2 * c));
+            nb[2 * m + 1] = (-8.f / kSub) * __shfl_sync(0xffffffffu, part, 4 * (2 * c + 1));
         }
     } else if constexpr (BK == 8) {
         const bool ok = sigma == 0;
@@ -248,6 +255,10 @@ __device__ __forceinline__ void build_qb(const float* __restrict__ qrow_base, in
             const int base = 16 * m + 4 * c;
             split_h2(val(base + 0, ok), val(base + 2, ok), qh[2 * m + 0], ql[2 * m + 0]);
             split_h2(val(base + 1, ok), val(base + 3, ok), qh[2 * m + 1], ql[2 * m + 1]);
+            float part = h2_sum(qh[2 * m]) + h2_sum(ql[2 * m]) + h2_sum(qh[2 * m + 1]) + h2_sum(ql[2 * m + 1]);
+            part += __shfl_xor_sync(0xffffffffu, part, 1);
+            part += __shfl_xor_sync(0xffffffffu, part, 2);
+            nb[m] = (-128.f / kSub) * __shfl_sync(0xffffffffu, part, 4 * (2 * c));
         }
     } else {
         const bool ok = sigma == 0;
@@ -255,6 +266,7 @@ __device__ __forceinline__ void build_qb(const float* __restrict__ qrow_base, in
         for (int j = 0; j < D / 16; ++j) {
             split_h2(val(16 * j + 2 * c, ok), val(16 * j + 2 * c + 1, ok), qh[2 * j + 0], ql[2 * j + 0]);
             split_h2(val(16 * j + 8 + 2 * c, ok), val(16 * j + 9 + 2 * c, ok), qh[2 * j + 1], ql[2 * j + 1]);
+            nb[j] = 0.f;
         }
     }
 }
@@ -277,10 +289,12 @@ __device__ __forceinline__ float ex2(float x) {  // 2^x; ex2.approx has a relati
 }
 
 // Scores of one 16-token sub-tile at row tr of the stage for this thread's
-// head c: s[0] for token tr+g, s[1] for token tr+g+8.
+// head c: s[0] for token tr+g, s[1] for token tr+g+8 (for packed keys in the
+// 2^-24 unit of the codes, for fp16 keys as is).
 template <int D, int BK>
 __device__ __forceinline__ void tile_scores(uint32_t kc, const float* __restrict__ ks, int sp, int lg, int tr, int lane,
-                                            const uint32_t (&qh)[D / 8], const uint32_t (&ql)[D / 8], float (&s)[2]) {
+                                            const uint32_t (&qh)[D / 8], const uint32_t (&ql)[D / 8],
+                                            const float (&nb)[D / 16], float (&s)[2]) {
     constexpr int RPK = PlaneT<D, BK>::RP;
     const int g = lane >> 2;
     const float* k0 = ks + (tr + g) * sp;
@@ -295,12 +309,13 @@ __device__ __forceinline__ void tile_scores(uint32_t kc, const float* __restrict
             for (int hh = 0; hh < 2; ++hh) {
                 const int mm = 2 * m2 + hh;
                 const uint32_t rg = r[2 * hh], rg8 = r[2 * hh + 1];
-                float d[4] = {0.f, 0.f, 0.f, 0.f};
-                const uint32_t x0 = i4_lo(rg), x1 = i4_lo(rg8), x2 = i4_hi(rg), x3 = i4_hi(rg8);
-                mma16816(d, x0, x1, x2, x3, qh[4 * mm], qh[4 * mm + 1]);
-                mma16816(d, x0, x1, x2, x3, ql[4 * mm], ql[4 * mm + 1]);
-                const uint32_t y0 = i4_lo(rg >> 8), y1 = i4_lo(rg8 >> 8), y2 = i4_hi(rg >> 8), y3 = i4_hi(rg8 >> 8);
+                const uint32_t rs = rg >> 8, rs8 = rg8 >> 8;
+                const uint32_t x0 = u4_lo(rg), x1 = u4_lo(rg8), x2 = u4_hi(rg), x3 = u4_hi(rg8);
+                const uint32_t y0 = u4_lo(rs), y1 = u4_lo(rs8), y2 = u4_hi(rs), y3 = u4_hi(rs8);
+                float d[4];
+                mma16816_c(d, x0, x1, x2, x3, qh[4 * mm], qh[4 * mm + 1], nb[2 * mm], nb[2 * mm + 1]);
                 mma16816(d, y0, y1, y2, y3, qh[4 * mm + 2], qh[4 * mm + 3]);
+                mma16816(d, x0, x1, x2, x3, ql[4 * mm], ql[4 * mm + 1]);
                 mma16816(d, y0, y1, y2, y3, ql[4 * mm + 2], ql[4 * mm + 3]);
                 // d = (token g: half 0, half 1, token g+8: half 0, half 1) for head c
                 const int ga = (32 * mm) >> lg, gb = (32 * mm + 16) >> lg;
@@ -320,9 +335,9 @@ __device__ __forceinline__ void tile_scores(uint32_t kc, const float* __restrict
             for (int hh = 0; hh < 2; ++hh) {
                 const int mm = 2 * m2 + hh;
                 const uint32_t rg = r[2 * hh], rg8 = r[2 * hh + 1];
-                float d[4] = {0.f, 0.f, 0.f, 0.f};
-                const uint32_t x0 = i8_lo(rg), x1 = i8_lo(rg8), x2 = i8_hi(rg), x3 = i8_hi(rg8);
-                mma16816(d, x0, x1, x2, x3, qh[2 * mm], qh[2 * mm + 1]);
+                const uint32_t x0 = u8_lo(rg), x1 = u8_lo(rg8), x2 = u8_lo(rg >> 8), x3 = u8_lo(rg8 >> 8);
+                float d[4];
+                mma16816_c(d, x0, x1, x2, x3, qh[2 * mm], qh[2 * mm + 1], nb[mm], 0.f);
                 mma16816(d, x0, x1, x2, x3, ql[2 * mm], ql[2 * mm + 1]);
                 const int gi = (16 * mm) >> lg;
                 a0 = fmaf(k0[gi], d[0], a0);
@@ -348,11 +363,14 @@ __device__ __forceinline__ void tile_scores(uint32_t kc, const float* __restrict
 // acc += V^T B for one 16-token sub-tile, B[k][n] = p(token k, head n/2) *
 // scale_V(token k, group of half n%2).  p00..p11 are p for tokens 2c+e+8f of
 // head g/2 (zero for padded heads and for tokens past the end, whose scale
-// rows were zeroed in shared memory).
+// rows were zeroed in shared memory).  Packed values enter as offset codes in
+// the 2^-24 unit (2^-20 for high nibbles); sv[] gathers this thread's share of
+// the column sums of B that remove the offset afterwards.
 template <int D, int BV>
 __device__ __forceinline__ void tile_pv(uint32_t vc, const float* __restrict__ vs, int sp, int lg, int tr, int lane,
                                         float p00, float p10, float p01, float p11, uint32_t amask_lo,
-                                        uint32_t amask_hi, bool tail, float (&acc)[D / 4]) {
+                                        uint32_t amask_hi, bool tail, float (&acc)[D / 4],
+                                        float (&sv)[AttnCfg<D, 4, BV>::NSV]) {
     constexpr int RPV = PlaneT<D, BV>::RP;
     const int g = lane >> 2, c = lane & 3;
     if constexpr (BV == 4) {
@@ -366,17 +384,19 @@ __device__ __forceinline__ void tile_pv(uint32_t vc, const float* __restrict__ v
                 const int cb = 2 * cb2 + hh;
                 const int gv = (32 * cb + 16 * side) >> lg;
                 const float* vsr = vs + (tr + 2 * c) * sp + gv;
+                const float b00 = p00 * vsr[0], b10 = p10 * vsr[sp], b01 = p01 * vsr[8 * sp], b11 = p11 * vsr[9 * sp];
+                sv[cb] += (b00 + b10) + (b01 + b11);
                 uint32_t bh0, bl0, bh1, bl1;
-                split_h2(p00 * vsr[0], p10 * vsr[sp], bh0, bl0);
-                split_h2(p01 * vsr[8 * sp], p11 * vsr[9 * sp], bh1, bl1);
-                const uint32_t R0 = r[2 * hh], R1 = r[2 * hh + 1];
+                split_h2(b00, b10, bh0, bl0);
+                split_h2(b01, b11, bh1, bl1);
+                const uint32_t R0 = r[2 * hh], R1 = r[2 * hh + 1], S0 = R0 >> 8, S1 = R1 >> 8;
                 float(&a0)[4] = *reinterpret_cast<float(*)[4]>(&acc[8 * cb]);
                 float(&a1)[4] = *reinterpret_cast<float(*)[4]>(&acc[8 * cb + 4]);
-                const uint32_t x0 = i4_lo(R0), x1 = i4_hi(R0), x2 = i4_lo(R1), x3 = i4_hi(R1);
+                const uint32_t x0 = u4_lo(R0), x1 = u4_hi(R0), x2 = u4_lo(R1), x3 = u4_hi(R1);
+                const uint32_t y0 = u4_lo(S0), y1 = u4_hi(S0), y2 = u4_lo(S1), y3 = u4_hi(S1);
                 mma16816(a0, x0, x1, x2, x3, bh0, bh1);
-                mma16816(a0, x0, x1, x2, x3, bl0, bl1);
-                const uint32_t y0 = i4_lo(R0 >> 8), y1 = i4_hi(R0 >> 8), y2 = i4_lo(R1 >> 8), y3 = i4_hi(R1 >> 8);
                 mma16816(a1, y0, y1, y2, y3, bh0, bh1);
+                mma16816(a0, x0, x1, x2, x3, bl0, bl1);
                 mma16816(a1, y0, y1, y2, y3, bl0, bl1);
             }
         }
@@ -396,12 +416,14 @@ __device__ __forceinline__ void tile_pv(uint32_t vc, const float* __restrict__ v
                 const int cb = 2 * s2 + hh;
                 const int gv = (16 * cb) >> lg;
                 const float* vsr = vs + (tr + 2 * c) * sp + gv;
+                const float b00 = p00 * vsr[0], b10 = p10 * vsr[sp], b01 = p01 * vsr[8 * sp], b11 = p11 * vsr[9 * sp];
+                sv[cb] += (b00 + b10) + (b01 + b11);
                 uint32_t bh0, bl0, bh1, bl1;
-                split_h2(p00 * vsr[0], p10 * vsr[sp], bh0, bl0);
-                split_h2(p01 * vsr[8 * sp], p11 * vsr[9 * sp], bh1, bl1);
+                split_h2(b00, b10, bh0, bl0);
+                split_h2(b01, b11, bh1, bl1);
                 const uint32_t R0 = r[2 * hh], R1 = r[2 * hh + 1];
                 float(&a0)[4] = *reinterpret_cast<float(*)[4]>(&acc[4 * cb]);
-                const uint32_t x0 = i8_lo(R0), x1 = i8_hi(R0), x2 = i8_lo(R1), x3 = i8_hi(R1);
+                const uint32_t x0 = u8_lo(R0), x1 = u8_lo(R0 >> 8), x2 = u8_lo(R1), x3 = u8_lo(R1 >> 8);
                 mma16816(a0, x0, x1, x2, x3, bh0, bh1);
                 mma16816(a0, x0, x1, x2, x3, bl0, bl1);
             }
@@ -430,16 +452,21 @@ __device__ __forceinline__ void tile_pv(uint32_t vc, const float* __restrict__ v
 
 // One chunk of NT 16-token sub-tiles starting at token t0 of the sequence:
 // scores for all NT*16 tokens, one online-softmax update, then P.V.
-template <int D, int BK, int BV, int NT>
+// G: the group size when known at compile time (16, the common case: all
+// scale-row indexing becomes immediate offsets), or 0 to read it from P.
+template <int D, int BK, int BV, int NT, int G>
 __device__ __forceinline__ void attn_chunk(const AttnParams& P, uint8_t* __restrict__ stage, int t0, int t_end, int lane,
                                            const uint32_t (&qh)[D / 8], const uint32_t (&ql)[D / 8],
-                                           float (&acc)[D / 4], float& m, float& l) {
+                                           const float (&nb)[D / 16], float (&acc)[D / 4],
+                                           float (&sv)[AttnCfg<D, BK, BV>::NSV], float& m, float& l) {
     using C = AttnCfg<D, BK, BV>;
+    constexpr float SU = C::QK ? kSub : 1.f;  // scores come in units of 1/SU
     const int g = lane >> 2, c = lane & 3;
     const uint32_t kc = ptx::smem_u32(stage + C::OFF_KC), vc = ptx::smem_u32(stage + C::OFF_VC);
     float* ks = reinterpret_cast<float*>(stage + C::OFF_KS);
     float* vs = reinterpret_cast<float*>(stage + C::OFF_VS);
-    const int sp = P.sp, lg = P.log2_group;
+    const int sp = G ? D / G + 4 : P.sp;
+    const int lg = G == 16 ? 4 : G == 32 ? 5 : G == 64 ? 6 : P.log2_group;
     const int valid = t_end - t0;  // tokens of this chunk inside the sequence (> 0)
     const bool tail = valid < 16 * NT;
     if (tail && (C::QK || C::QV)) {
@@ -456,23 +483,32 @@ __device__ __forceinline__ void attn_chunk(const AttnParams& P, uint8_t* __restr
     float s[NT][2];
 #pragma unroll
     for (int st = 0; st < NT; ++st) {
-        if (16 * st < valid) tile_scores<D, BK>(kc, ks, sp, lg, 16 * st, lane, qh, ql, s[st]);
+        if (16 * st < valid) tile_scores<D, BK>(kc, ks, sp, lg, 16 * st, lane, qh, ql, nb, s[st]);
         else s[st][0] = s[st][1] = 0.f;
-        if (16 * st + g >= valid) s[st][0] = -INFINITY;
-        if (16 * st + g + 8 >= valid) s[st][1] = -INFINITY;
+        if (tail) {
+            if (16 * st + g >= valid) s[st][0] = -INFINITY;
+            if (16 * st + g + 8 >= valid) s[st][1] = -INFINITY;
+        }
     }
     // ---- online softmax (log2 domain) ----
+    // The running max m only has to move when some score of the chunk exceeds
+    // it; that is tested per thread and voted, and only then is the head max
+    // reduced over the 8 token rows and the state rescaled.
     float mt = -INFINITY;
 #pragma unroll
     for (int st = 0; st < NT; ++st) mt = fmaxf(mt, fmaxf(s[st][0], s[st][1]));
+    mt *= SU;
+    if (__any_sync(0xffffffffu, mt > m)) {
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
-    const float mn = fmaxf(m, mt);
-    if (__any_sync(0xffffffffu, mn > m)) {
-        const float f = (mn == -INFINITY) ? 1.f : ex2(m - mn);
+        for (int off = 4; off < 32; off <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+        const float mn = fmaxf(m, mt);
+        const float f = (mn == -INFINITY) ? 1.f : ex2(m - mn);  // head c's factor
         l *= f;
 #pragma unroll
         for (int i = 0; i < D / 4; ++i) acc[i] *= f;
+        const float fs = __shfl_sync(0xffffffffu, f, g >> 1);  // head g/2's factor, for the column sums
+#pragma unroll
+        for (int i = 0; i < C::NSV; ++i) sv[i] *= fs;
         m = mn;
     }
     // p in [0, 256]: the +8 keeps p * scale_V clear of fp16 subnormals; it cancels in acc / l
@@ -482,7 +518,7 @@ __device__ __forceinline__ void attn_chunk(const AttnParams& P, uint8_t* __restr
 #pragma unroll
     for (int st = 0; st < NT; ++st) {
         if (16 * st >= valid) break;
-        const float p0 = ex2(s[st][0] - bias), p1 = ex2(s[st][1] - bias);
+        const float p0 = ex2(fmaf(s[st][0], SU, -bias)), p1 = ex2(fmaf(s[st][1], SU, -bias));
         l += p0 + p1;
         const float o0 = offer ? p0 : 0.f, o1 = offer ? p1 : 0.f;
         const float P00 = __shfl_sync(0xffffffffu, o0, 4 * (2 * c) + hd);
@@ -493,7 +529,7 @@ __device__ __forceinline__ void attn_chunk(const AttnParams& P, uint8_t* __restr
         const bool sub_tail = vt < 16;
         const uint32_t mlo = (2 * c < vt ? 0x0000FFFFu : 0u) | (2 * c + 1 < vt ? 0xFFFF0000u : 0u);
         const uint32_t mhi = (2 * c + 8 < vt ? 0x0000FFFFu : 0u) | (2 * c + 9 < vt ? 0xFFFF0000u : 0u);
-        tile_pv<D, BV>(vc, vs, sp, lg, 16 * st, lane, P00, P10, P01, P11, mlo, mhi, sub_tail, acc);
+        tile_pv<D, BV>(vc, vs, sp, lg, 16 * st, lane, P00, P10, P01, P11, mlo, mhi, sub_tail, acc, sv);
     }
 }
 
@@ -518,14 +554,17 @@ __device__ __forceinline__ void acc_coord(int i, int g, int c, int& dim, int& he
     }
 }
 
-template <int D, int BK, int BV>
-__global__ void __launch_bounds__(kAttnWarps * 32, 3)
+// d = 256 keeps 2 CTAs per SM: its fragments need more than a third of the register file
+template <int D, int BK, int BV, int G>
+__global__ void __launch_bounds__(kAttnWarps * 32, D >= 256 ? 2 : 3)
     q4kv_attn_split_kernel(const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_ks,
                            const __grid_constant__ CUtensorMap tm_vc, const __grid_constant__ CUtensorMap tm_vs,
                            const __grid_constant__ AttnParams P) {
     using C = AttnCfg<D, BK, BV>;
     extern __shared__ __align__(1024) uint8_t smem[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // the warp index through a shuffle, so the compiler knows it is warp-uniform
+    // (barrier and TMA operands then stay in uniform registers)
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0), lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
     const int bh = blockIdx.y, b = bh / P.Hkv, hkv = bh - b * P.Hkv;
     const int split = blockIdx.x;
@@ -547,10 +586,13 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 3)
     auto barw = [&](int s2) { return ptx::smem_u32(&bars[4 * warp + s2]); };
 
     uint32_t qh[C::QB], ql[C::QB];
-    build_qb<D, BK>(P.qt + ((long long)b * P.Hq + (long long)hkv * P.rep) * D, P.rep, g, c, qh, ql);
-    float acc[C::ACC];
+    float nb[D / 16];
+    build_qb<D, BK>(P.qt + ((long long)b * P.Hq + (long long)hkv * P.rep) * D, P.rep, g, c, qh, ql, nb);
+    float acc[C::ACC], sv[C::NSV];
 #pragma unroll
     for (int i = 0; i < C::ACC; ++i) acc[i] = 0.f;
+#pragma unroll
+    for (int i = 0; i < C::NSV; ++i) sv[i] = 0.f;
     float m = -INFINITY, l = 0.f;  // online-softmax state for head c (log2 domain)
 
     const int plane_row = b * P.Hkv + hkv;  // this (batch, kv head)'s rows in the head-major planes
@@ -591,7 +633,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 3)
             failed = true;
             break;
         }
-        attn_chunk<D, BK, BV, C::CH / 16>(P, wbase + st * C::STAGE, chunk * C::CH, L, lane, qh, ql, acc, m, l);
+        attn_chunk<D, BK, BV, C::CH / 16, G>(P, wbase + st * C::STAGE, chunk * C::CH, L, lane, qh, ql, nb, acc, sv, m,
+                                             l);
         __syncwarp();
     }
     // the failure flag is per warp; every warp still joins the merge below
@@ -600,6 +643,29 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 3)
         l = 0.f;
 #pragma unroll
         for (int i = 0; i < C::ACC; ++i) acc[i] = 0.f;
+#pragma unroll
+        for (int i = 0; i < C::NSV; ++i) sv[i] = 0.f;
+    }
+
+    // ---- remove the code offset: acc holds sums of (code + offset) * B in the
+    // code unit; the column sums of B (this thread's useful column) give the rest
+    float ssum[C::NSV];
+#pragma unroll
+    for (int i = 0; i < C::NSV; ++i) {
+        float t = sv[i];
+        t += __shfl_xor_sync(0xffffffffu, t, 1);
+        t += __shfl_xor_sync(0xffffffffu, t, 2);  // column g's sum over the 16 token slots
+        const int col = BV == 4 ? 2 * c + (g >= 4 ? 1 : 0) : 2 * c;
+        ssum[i] = __shfl_sync(0xffffffffu, t, 4 * col);
+    }
+#pragma unroll
+    for (int i = 0; i < C::ACC; ++i) {
+        if constexpr (BV == 4) {
+            const float unit = ((i >> 1) & 1) ? 1048576.f : kSub;  // high-nibble rows: 2^-20
+            acc[i] = fmaf(unit, acc[i], -8.f * ssum[i >> 3]);
+        } else if constexpr (BV == 8) {
+            acc[i] = fmaf(kSub, acc[i], -128.f * ssum[i >> 2]);
+        }
     }
 
     // ---- per-warp totals of l over the 8 token rows ----
@@ -748,13 +814,22 @@ static int launch_split(const AttnLaunch& A) {
         return SRFTKV_ERR_CUDA;
     if (C::QV && !encode_plane(&tvs, A.v->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ng, 4, P.sp, bh, P.t_cap, C::CH))
         return SRFTKV_ERR_CUDA;
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(q4kv_attn_split_kernel<D, BK, BV>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        attr = true;
+    static bool attr[2] = {false, false};
+    const bool g16 = P.group == 16;  // raw fp16 sides carry group 16
+    if (!attr[g16]) {
+        if (g16)
+            cudaFuncSetAttribute(q4kv_attn_split_kernel<D, BK, BV, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::SMEM);
+        else
+            cudaFuncSetAttribute(q4kv_attn_split_kernel<D, BK, BV, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::SMEM);
+        attr[g16] = true;
     }
     const dim3 grid(P.n_splits, P.B * P.Hkv);
-    q4kv_attn_split_kernel<D, BK, BV><<<grid, kAttnWarps * 32, C::SMEM, A.stream>>>(tkc, tks, tvc, tvs, P);
+    if (g16)
+        q4kv_attn_split_kernel<D, BK, BV, 16><<<grid, kAttnWarps * 32, C::SMEM, A.stream>>>(tkc, tks, tvc, tvs, P);
+    else
+        q4kv_attn_split_kernel<D, BK, BV, 0><<<grid, kAttnWarps * 32, C::SMEM, A.stream>>>(tkc, tks, tvc, tvs, P);
     return 0;
 }
 
