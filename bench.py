@@ -17,6 +17,12 @@ needed between steps.
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun each rank runs the same workload on its own GPU (weak scaling,
 no data exchange); rank 0 prints one JSON line.
+
+Profiling cases: python bench.py --kernel quantize|dequantize|attention [--steps K] [--warmup W]
+launches only that kernel on a cut-down decode workload (quantize/dequantize:
+B=2, the full 131072 tokens x 8 kv heads, 4.2 M vectors, about 1.6 GB held;
+attention: B=4, T=32768, a 201 MB packed cache) so that ncu captures stay
+small; it prints one JSON line with the median event time per launch.
 """
 
 from __future__ import annotations
@@ -51,6 +57,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--kernel", default=None, choices=("quantize", "dequantize", "attention"),
+                    help="profiling case: launch only this kernel on a small workload")
     return ap.parse_args()
 
 
@@ -63,25 +71,35 @@ def peaks():
     return FALLBACK_HBM, "fallback"
 
 
-def kernel_source_sha() -> str:
+# the sources each timed kernel is built from: a recorded ncu traffic figure
+# counts only while these are unchanged
+KERNEL_SOURCES = {
+    "srft_quantize_tc_kernel": ("codec_tc.cu", "codec_impl.cuh", "tcgen05.cuh", "srft_math.cuh", "ptx.cuh"),
+    "srft_dequantize_tc_kernel": ("codec_tc.cu", "codec_impl.cuh", "tcgen05.cuh", "srft_math.cuh", "ptx.cuh"),
+    "q4kv_attn_split_kernel": ("attention.cu", "ptx.cuh", "srft_math.cuh"),
+}
+
+
+def kernel_source_sha(kernel: str = "srft_quantize_tc_kernel") -> str:
     h = hashlib.sha256()
-    for name in ("codec_tc.cu", "codec_impl.cuh", "tcgen05.cuh", "srft_math.cuh", "ptx.cuh"):
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "int8_kv_cache_srft_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(sha: str):
-    """dram bytes per quantize launch from the committed ncu summary, if it was taken on this source."""
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` on the bench workload from the committed ncu record, if it was taken
+    on the current source of that kernel (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         j = json.load(f)
-    ent = j.get("srft_quantize_tc_kernel")
-    if not ent or ent.get("source_sha") != sha:
+    ent = j.get(kernel)
+    if not ent or ent.get("source_sha") != kernel_source_sha(kernel):
         return None
-    return float(ent["bytes_per_launch_full_workload"])
+    return float(ent["dram_bytes_per_launch"])
 
 
 class ClockSampler:
@@ -322,7 +340,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     attn_bytes = B * T * Hkv * ATTN_BYTES_PER_TOKEN_HEAD
     achieved = quant_bytes / (med["quant"] * 1e-3) / 1e9
     sha = kernel_source_sha()
-    traffic = recorded_traffic(sha)
+    traffic = recorded_traffic("srft_quantize_tc_kernel")
     attn_gbs = attn_bytes / (med["attn"] * 1e-3) / 1e9
     fp16_ms = statistics.median(t16)
     cpu = None if args.no_cpu else oracle_sample(args.cpu_seconds)
@@ -355,19 +373,74 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                       "frac_of_nominal_8000": attn_gbs / 8000.0, "decode_tokens_per_s": B / (med["attn"] * 1e-3),
                       "kv_tokens_per_s": B * T / (med["attn"] * 1e-3), "fp16_cache_ms": fp16_ms,
                       "fp16_cache_gbs": 2 * B * T * Hkv * d * 2 / (fp16_ms * 1e-3) / 1e9,
-                      "int4_speedup_vs_fp16_cache": fp16_ms / med["attn"]},
+                      "int4_speedup_vs_fp16_cache": fp16_ms / med["attn"],
+                      "algorithmic_bytes_per_launch": attn_bytes,
+                      "traffic": recorded_traffic("q4kv_attn_split_kernel")},
         "append_us": med["append"] * 1e3,
         "gpu_launches": LAUNCHES * args.steps,
         "clocks": clk,
         "e2e": e2e,
         "cpu_baseline": cpu,
-        "kernel_source_sha": sha,
+        "kernel_source_sha": {k: kernel_source_sha(k) for k in KERNEL_SOURCES},
     }
     print(json.dumps(line), flush=True)
 
 
+def run_case(args):
+    """One kernel of the path on a cut-down decode workload, for ncu captures."""
+    import torch
+    import int8_kv_cache_srft_gb300 as K
+    from int8_kv_cache_srft_gb300 import inputs as I
+
+    torch.cuda.set_device(0)
+    K.library()
+    attn = args.kernel == "attention"
+    w = I.DECODE.resized(n_outer=4, tokens=32768) if attn else I.DECODE.resized(n_outer=2)
+    B, Hkv, d, T, Hq, G, seed = w.n_outer, w.kv_heads, w.d, w.tokens, w.q_heads, w.group, w.sign_seed
+    xk, xv = I.kv_side(w, "k", device="cuda"), I.kv_side(w, "v", device="cuda")
+    sk, sv = K.alloc_side(B, T, Hkv, d, 4, G), K.alloc_side(B, T, Hkv, d, 4, G)
+    sk.x, sv.x = xk, xv
+    K.srft_kv_quantize(sk, sv, B, T, Hkv, d, G, T, 0, seed)
+    if args.kernel == "quantize":
+        def launch():
+            K.srft_kv_quantize(sk, sv, B, T, Hkv, d, G, T, 0, seed)
+    elif args.kernel == "dequantize":
+        dk, dv = torch.empty_like(xk), torch.empty_like(xv)
+        deq_k, deq_v = K.Side(sk.codes, sk.scales, 4, x=dk), K.Side(sv.codes, sv.scales, 4, x=dv)
+
+        def launch():
+            K.srft_kv_dequantize(deq_k, deq_v, B, T, Hkv, d, G, T, 0, seed)
+    else:
+        del xk, xv
+        sk.x = sv.x = None
+        q = I.query(w, device="cuda")
+        out = torch.empty((B, Hq, d), dtype=torch.float32, device="cuda")
+        ws = torch.empty(K.q4kv_decode_attention_workspace_size(B, Hq, Hkv, d, T, 0), dtype=torch.uint8,
+                         device="cuda")
+
+        def launch():
+            K.q4kv_decode_attention(q, out, sk, sv, B, Hq, Hkv, d, G, T, None, 0.0, seed, 0, ws)
+    for _ in range(args.warmup):
+        launch()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        launch()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    assert K.srftkv_device_fault() == 0
+    print(json.dumps({"profile_case": args.kernel, "B": B, "T": T, "kv_heads": Hkv, "d": d, "bits": 4, "group": G,
+                      "launches": args.steps, "median_ms": statistics.median(ts)}), flush=True)
+
+
 def main():
     args = parse()
+    if args.kernel is not None:
+        run_case(args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
