@@ -140,7 +140,10 @@ int srft_kv_dequantize(const srftkv_side* k, const srftkv_side* v, int n_outer, 
  *              q4kv_decode_attention_workspace_size(...) bytes (16-byte aligned)
  *              for the per-split partial results; contents need not be
  *              initialised and are overwritten.
- * Requires Hq % Hkv == 0 and Hq/Hkv <= 8.
+ * Requires d in {64, 128, 256}, Hq % Hkv == 0 and Hq/Hkv <= 4, and for
+ * packed sides a power-of-two group with 16 <= group <= d/4 (a scale row of
+ * at least 16 bytes, the smallest TMA row) and 16-byte aligned scales;
+ * anything else returns SRFTKV_ERR_INVALID before any launch.
  */
 int q4kv_decode_attention(const void* q, float* out, const srftkv_side* k, const srftkv_side* v,
                           int B, int Hq, int Hkv, int d, int group, int t_cap,
