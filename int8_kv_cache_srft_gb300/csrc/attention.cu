@@ -124,31 +124,56 @@ __device__ __forceinline__ float h2_sum(uint32_t h) {
     return f.x + f.y;
 }
 
+// Shared-memory images of the cache planes.  TMA copies whole rows (a box
+// exactly as wide as the row: a wider, zero-filled box turns each chunk into
+// one small request per row and cost about 9 % of the streaming rate).  Code
+// rows of at most 128 bytes land swizzled (TMA's 32/64/128-byte swizzle, the
+// mode equal to the row length), which keeps the ldmatrix reads free of bank
+// conflicts without padding; longer rows (fp16, or int8 at d=256) keep 16
+// bytes of padding per row.
 template <int D, int BITS>
 struct PlaneT {
-    static constexpr int RB = D * BITS / 8;  // bytes per cached row
-    static constexpr int RP = RB + 16;       // padded shared-memory row
+    static constexpr int RB = D * BITS / 8;                // bytes per cached row
+    static constexpr bool SWZ = BITS != 16 && RB <= 128;   // exact rows, swizzled
+    static constexpr int RP = SWZ ? RB : RB + 16;          // shared-memory row pitch
 };
+
+// Byte offset of 16-byte chunk `ch` of row `r` in a swizzled plane of RB-byte
+// rows (TMA swizzle: address bits [4, 4+b) XOR bits [7, 7+b), b = log2(RB/16)),
+// for a buffer that starts on a 1024-byte boundary.
+template <int RB>
+__host__ __device__ constexpr int swz_chunk(int r, int ch) {
+    return ch ^ (((r * RB) >> 7) & (RB / 16 - 1));
+}
+
+constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
 template <int D, int BK, int BV>
 struct AttnCfg {
     static constexpr bool QK = BK != 16, QV = BV != 16;
-    static constexpr int SPMAX = D / 16 + 4;                       // padded scale row, floats
-    static constexpr int STAGE32 = 32 * (PlaneT<D, BK>::RP + PlaneT<D, BV>::RP + (QK ? SPMAX * 4 : 0) + (QV ? SPMAX * 4 : 0));
+    static constexpr int SRB = D / 4;  // largest scale row in bytes (group 16); exact rows, no padding
+    static constexpr int STAGE32 = 32 * (PlaneT<D, BK>::RP + PlaneT<D, BV>::RP + (QK ? SRB : 0) + (QV ? SRB : 0));
     static constexpr int CH = SRFTKV_ATTN_CH ? SRFTKV_ATTN_CH : (STAGE32 <= 9216 ? 32 : 16);  // tokens per chunk
     static constexpr int NS = SRFTKV_ATTN_STAGES;
+    // swizzled sub-buffers (code rows of <= 128 bytes, group-16 scale rows of
+    // >= 32 bytes) start on a 1024-byte boundary, the others on 128 bytes
+    static constexpr int AK = PlaneT<D, BK>::SWZ ? 1024 : 128, AV = PlaneT<D, BV>::SWZ ? 1024 : 128;
+    static constexpr int AS = (QK || QV) && SRB >= 32 ? 1024 : 128;
+    static constexpr int A0 = AK > AV ? (AK > AS ? AK : AS) : (AV > AS ? AV : AS);  // stage alignment
     static constexpr int OFF_KC = 0;
-    static constexpr int OFF_KS = OFF_KC + CH * PlaneT<D, BK>::RP;
-    static constexpr int OFF_VC = OFF_KS + (QK ? CH * SPMAX * 4 : 0);
-    static constexpr int OFF_VS = OFF_VC + CH * PlaneT<D, BV>::RP;
-    static constexpr int STAGE = ((OFF_VS + (QV ? CH * SPMAX * 4 : 0)) + 127) / 128 * 128;
+    static constexpr int OFF_KS = align_up(OFF_KC + CH * PlaneT<D, BK>::RP, AS);
+    static constexpr int OFF_VC = align_up(OFF_KS + (QK ? CH * SRB : 0), AV);
+    static constexpr int OFF_VS = align_up(OFF_VC + CH * PlaneT<D, BV>::RP, AS);
+    static constexpr int STAGE = align_up(OFF_VS + (QV ? CH * SRB : 0), A0);
     static constexpr int WARP_BYTES = NS * STAGE;
     static constexpr int MERGE_BYTES = kAttnWarps * (4 * D + 8) * 4;
     static constexpr int BODY = kAttnWarps * WARP_BYTES > MERGE_BYTES ? kAttnWarps * WARP_BYTES : MERGE_BYTES;
-    static constexpr int SMEM = 128 + BODY;
+    static constexpr int BARS = BODY;                   // mbarriers after the body
+    static constexpr int SMEM = 1024 + BODY + 128;      // + slack to realign the base to 1024 bytes
     static constexpr int QB = D / 8;    // K-side B-fragment registers
     static constexpr int ACC = D / 4;   // V accumulators
     static constexpr int NSV = BV == 4 ? D / 32 : BV == 8 ? D / 16 : 1;  // column sums of the V-side B
+    static constexpr int NCH = SRB / 16;  // 16-byte chunks in a group-16 scale row
 };
 
 // ---------------------------------------------------------------------------
@@ -271,15 +296,58 @@ __device__ __forceinline__ void build_qb(const float* __restrict__ qrow_base, in
     }
 }
 
-// ldmatrix row address for the 4 matrices (rows tr..tr+7 | tr+8..tr+15) x (seg | seg+1)
-__device__ __forceinline__ uint32_t ldsm_addr(uint32_t base, int rp, int tr, int seg, int lane) {
-    const int mi = lane >> 3;
-    return base + (uint32_t)((tr + (lane & 7) + (mi & 1) * 8) * rp + (seg + (mi >> 1)) * 16);
+// Per-lane part of the ldmatrix row addresses into a plane image.  Lane l
+// supplies row rl of the 16-row sub-tile and reads dl chunks (0 or 1) past
+// the even chunk index being loaded.  off = rl times the row pitch (plus the
+// chunk step when unswizzled); x16 = (dl XOR the row's swizzle) * 16, which
+// for an even chunk index c gives the swizzled chunk of c + dl as c ^ x16/16.
+// A sub-tile starts on a multiple of 16 rows, which never changes the swizzle.
+struct LaneRow {
+    uint32_t off, x16;
+};
+template <int RB, bool SWZ, int RP>
+__device__ __forceinline__ LaneRow lane_row(int rl, int dl) {
+    LaneRow L;
+    if constexpr (SWZ) {
+        L.off = (uint32_t)(rl * RB);
+        L.x16 = (uint32_t)((dl ^ swz_chunk<RB>(rl, 0)) << 4);
+    } else {
+        L.off = (uint32_t)(rl * RP + dl * 16);
+        L.x16 = 0;
+    }
+    return L;
+}
+// codes, plain or transposed: matrices (rows 0-7 | 8-15) x (chunk seg | seg+1)
+template <int RB, bool SWZ, int RP>
+__device__ __forceinline__ LaneRow lane_row_codes(int lane) {
+    return lane_row<RB, SWZ, RP>((lane & 7) + ((lane >> 3) & 1) * 8, lane >> 4);
 }
 // fp16 V (trans): matrices (rows 0-7, seg), (rows 0-7, seg+1), (rows 8-15, seg), (rows 8-15, seg+1)
-__device__ __forceinline__ uint32_t ldsm_addr_v16(uint32_t base, int rp, int tr, int seg, int lane) {
-    const int mi = lane >> 3;
-    return base + (uint32_t)((tr + (lane & 7) + (mi >> 1) * 8) * rp + (seg + (mi & 1)) * 16);
+template <int RB, bool SWZ, int RP>
+__device__ __forceinline__ LaneRow lane_row_v16(int lane) {
+    return lane_row<RB, SWZ, RP>((lane & 7) + (lane >> 4) * 8, (lane >> 3) & 1);
+}
+// ldmatrix address of this lane for the sub-tile at row tr, even chunk seg
+template <int RB, bool SWZ, int RP>
+__device__ __forceinline__ uint32_t plane_addr(uint32_t base, const LaneRow& L, int tr, int seg) {
+    if constexpr (SWZ)
+        return base + L.off + (uint32_t)(tr * RB) + (((uint32_t)seg << 4) ^ L.x16);
+    else
+        return base + L.off + (uint32_t)(tr * RP + seg * 16);
+}
+
+// Per-thread scale addressing.  Group-16 scale rows are SRB = d/4 bytes,
+// swizzled like the codes (mode = row length); so[j] is the byte offset of
+// logical 16-byte chunk j of this thread's first row.  Other group sizes use
+// unswizzled rows of d/group floats.
+template <int D, int NCH>
+__device__ __forceinline__ void scale_offsets(int row, int extra, uint32_t (&so)[NCH]) {
+    constexpr int SRB = D / 4;
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) so[j] = (uint32_t)(row * SRB + (swz_chunk<SRB>(row, j) << 4) + extra);
+}
+__device__ __forceinline__ float lds_f32(const uint8_t* base, uint32_t off) {
+    return *reinterpret_cast<const float*>(base + off);
 }
 
 __device__ __forceinline__ float ex2(float x) {  // 2^x; ex2.approx has a relative error of about 2^-22
@@ -291,20 +359,27 @@ __device__ __forceinline__ float ex2(float x) {  // 2^x; ex2.approx has a relati
 // Scores of one 16-token sub-tile at row tr of the stage for this thread's
 // head c: s[0] for token tr+g, s[1] for token tr+g+8 (for packed keys in the
 // 2^-24 unit of the codes, for fp16 keys as is).
-template <int D, int BK>
-__device__ __forceinline__ void tile_scores(uint32_t kc, const float* __restrict__ ks, int sp, int lg, int tr, int lane,
-                                            const uint32_t (&qh)[D / 8], const uint32_t (&ql)[D / 8],
+template <int D, int BK, int G>
+__device__ __forceinline__ void tile_scores(uint32_t kc, const LaneRow& LK, const uint8_t* __restrict__ ksb,
+                                            const uint32_t (&kso)[D / 64], int sp, int lg, int tr,
+                                            int lane, const uint32_t (&qh)[D / 8], const uint32_t (&ql)[D / 8],
                                             const float (&nb)[D / 16], float (&s)[2]) {
-    constexpr int RPK = PlaneT<D, BK>::RP;
+    using PK = PlaneT<D, BK>;
+    constexpr int SRB = D / 4;
     const int g = lane >> 2;
-    const float* k0 = ks + (tr + g) * sp;
-    const float* k1 = ks + (tr + g + 8) * sp;
+    const float* k0 = reinterpret_cast<const float*>(ksb) + (tr + g) * sp;
+    const float* k1 = reinterpret_cast<const float*>(ksb) + (tr + g + 8) * sp;
+    // scale of group f for token rows tr+g (r = 0) and tr+g+8 (r = 1)
+    auto ksc = [&](int f, int r) -> float {
+        if constexpr (G == 16) return lds_f32(ksb, kso[f >> 2] + (tr + 8 * r) * SRB + (f & 3) * 4);
+        else return (r ? k1 : k0)[f];
+    };
     if constexpr (BK == 4) {
         float a0 = 0.f, a1 = 0.f;
 #pragma unroll
         for (int m2 = 0; m2 < D / 64; ++m2) {
             uint32_t r[4];
-            ldsm_x4(ldsm_addr(kc, RPK, tr, 2 * m2, lane), r);
+            ldsm_x4(plane_addr<PK::RB, PK::SWZ, PK::RP>(kc, LK, tr, 2 * m2), r);
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 const int mm = 2 * m2 + hh;
@@ -319,8 +394,8 @@ __device__ __forceinline__ void tile_scores(uint32_t kc, const float* __restrict
                 mma16816(d, y0, y1, y2, y3, ql[4 * mm + 2], ql[4 * mm + 3]);
                 // d = (token g: half 0, half 1, token g+8: half 0, half 1) for head c
                 const int ga = (32 * mm) >> lg, gb = (32 * mm + 16) >> lg;
-                a0 = fmaf(k0[ga], d[0], fmaf(k0[gb], d[1], a0));
-                a1 = fmaf(k1[ga], d[2], fmaf(k1[gb], d[3], a1));
+                a0 = fmaf(ksc(ga, 0), d[0], fmaf(ksc(gb, 0), d[1], a0));
+                a1 = fmaf(ksc(ga, 1), d[2], fmaf(ksc(gb, 1), d[3], a1));
             }
         }
         s[0] = a0;
@@ -330,7 +405,7 @@ __device__ __forceinline__ void tile_scores(uint32_t kc, const float* __restrict
 #pragma unroll
         for (int m2 = 0; m2 < D / 32; ++m2) {
             uint32_t r[4];
-            ldsm_x4(ldsm_addr(kc, RPK, tr, 2 * m2, lane), r);
+            ldsm_x4(plane_addr<PK::RB, PK::SWZ, PK::RP>(kc, LK, tr, 2 * m2), r);
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 const int mm = 2 * m2 + hh;
@@ -340,8 +415,8 @@ __device__ __forceinline__ void tile_scores(uint32_t kc, const float* __restrict
                 mma16816_c(d, x0, x1, x2, x3, qh[2 * mm], qh[2 * mm + 1], nb[mm], 0.f);
                 mma16816(d, x0, x1, x2, x3, ql[2 * mm], ql[2 * mm + 1]);
                 const int gi = (16 * mm) >> lg;
-                a0 = fmaf(k0[gi], d[0], a0);
-                a1 = fmaf(k1[gi], d[2], a1);
+                a0 = fmaf(ksc(gi, 0), d[0], a0);
+                a1 = fmaf(ksc(gi, 1), d[2], a1);
             }
         }
         s[0] = a0;
@@ -351,7 +426,7 @@ __device__ __forceinline__ void tile_scores(uint32_t kc, const float* __restrict
 #pragma unroll
         for (int j = 0; j < D / 16; ++j) {
             uint32_t r[4];
-            ldsm_x4(ldsm_addr(kc, RPK, tr, 2 * j, lane), r);
+            ldsm_x4(plane_addr<PK::RB, PK::SWZ, PK::RP>(kc, LK, tr, 2 * j), r);
             mma16816(d, r[0], r[1], r[2], r[3], qh[2 * j], qh[2 * j + 1]);
             mma16816(d, r[0], r[1], r[2], r[3], ql[2 * j], ql[2 * j + 1]);
         }
@@ -366,25 +441,36 @@ __device__ __forceinline__ void tile_scores(uint32_t kc, const float* __restrict
 // rows were zeroed in shared memory).  Packed values enter as offset codes in
 // the 2^-24 unit (2^-20 for high nibbles); sv[] gathers this thread's share of
 // the column sums of B that remove the offset afterwards.
-template <int D, int BV>
-__device__ __forceinline__ void tile_pv(uint32_t vc, const float* __restrict__ vs, int sp, int lg, int tr, int lane,
-                                        float p00, float p10, float p01, float p11, uint32_t amask_lo,
+template <int D, int BV, int G>
+__device__ __forceinline__ void tile_pv(uint32_t vc, const LaneRow& LV, const uint8_t* __restrict__ vsb,
+                                        const uint32_t (&vso)[D / 64], int sp, int lg, int tr,
+                                        int lane, float p00, float p10, float p01, float p11, uint32_t amask_lo,
                                         uint32_t amask_hi, bool tail, float (&acc)[D / 4],
                                         float (&sv)[AttnCfg<D, 4, BV>::NSV]) {
-    constexpr int RPV = PlaneT<D, BV>::RP;
+    using PV = PlaneT<D, BV>;
+    constexpr int SRB = D / 4;
     const int g = lane >> 2, c = lane & 3;
+    // scale of group f (group 16: chunk f/4 of the row, float f%4; vso already
+    // holds this thread's column offset for 4-bit values) for token rows
+    // tr+2c+e, e in {0, 1, 8, 9}
+    auto vsc = [&](int gv, int f_in_chunk, int e) -> float {
+        if constexpr (G == 16) return lds_f32(vsb, vso[gv] + (tr + e) * SRB + f_in_chunk * 4);
+        else return reinterpret_cast<const float*>(vsb)[(tr + 2 * c + e) * sp + gv];
+    };
     if constexpr (BV == 4) {
         const int side = g & 1;
 #pragma unroll
         for (int cb2 = 0; cb2 < D / 64; ++cb2) {
             uint32_t r[4];
-            ldsm_x4_t(ldsm_addr(vc, RPV, tr, 2 * cb2, lane), r);
+            ldsm_x4_t(plane_addr<PV::RB, PV::SWZ, PV::RP>(vc, LV, tr, 2 * cb2), r);
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 const int cb = 2 * cb2 + hh;
-                const int gv = (32 * cb + 16 * side) >> lg;
-                const float* vsr = vs + (tr + 2 * c) * sp + gv;
-                const float b00 = p00 * vsr[0], b10 = p10 * vsr[sp], b01 = p01 * vsr[8 * sp], b11 = p11 * vsr[9 * sp];
+                // group 16: group 2cb + side lies in chunk cb/2 at float 2(cb%2) + side (side folded into vso)
+                const int gv = G == 16 ? cb >> 1 : (32 * cb + 16 * side) >> lg;
+                const int fc = 2 * (cb & 1);
+                const float b00 = p00 * vsc(gv, fc, 0), b10 = p10 * vsc(gv, fc, 1), b01 = p01 * vsc(gv, fc, 8),
+                            b11 = p11 * vsc(gv, fc, 9);
                 sv[cb] += (b00 + b10) + (b01 + b11);
                 uint32_t bh0, bl0, bh1, bl1;
                 split_h2(b00, b10, bh0, bl0);
@@ -410,13 +496,14 @@ __device__ __forceinline__ void tile_pv(uint32_t vc, const float* __restrict__ v
 #pragma unroll
         for (int s2 = 0; s2 < D / 32; ++s2) {
             uint32_t r[4];
-            ldsm_x4_t(ldsm_addr(vc, RPV, tr, 2 * s2, lane), r);
+            ldsm_x4_t(plane_addr<PV::RB, PV::SWZ, PV::RP>(vc, LV, tr, 2 * s2), r);
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 const int cb = 2 * s2 + hh;
-                const int gv = (16 * cb) >> lg;
-                const float* vsr = vs + (tr + 2 * c) * sp + gv;
-                const float b00 = p00 * vsr[0], b10 = p10 * vsr[sp], b01 = p01 * vsr[8 * sp], b11 = p11 * vsr[9 * sp];
+                const int gv = G == 16 ? cb >> 2 : (16 * cb) >> lg;
+                const int fc = cb & 3;
+                const float b00 = p00 * vsc(gv, fc, 0), b10 = p10 * vsc(gv, fc, 1), b01 = p01 * vsc(gv, fc, 8),
+                            b11 = p11 * vsc(gv, fc, 9);
                 sv[cb] += (b00 + b10) + (b01 + b11);
                 uint32_t bh0, bl0, bh1, bl1;
                 split_h2(b00, b10, bh0, bl0);
@@ -436,7 +523,7 @@ __device__ __forceinline__ void tile_pv(uint32_t vc, const float* __restrict__ v
 #pragma unroll
         for (int j = 0; j < D / 16; ++j) {
             uint32_t r[4];
-            ldsm_x4_t(ldsm_addr_v16(vc, RPV, tr, 2 * j, lane), r);
+            ldsm_x4_t(plane_addr<PV::RB, PV::SWZ, PV::RP>(vc, LV, tr, 2 * j), r);
             if (tail) {  // raw fp16 rows past the end may hold anything: zero them in the A operand
                 r[0] &= amask_lo;
                 r[1] &= amask_lo;
@@ -456,7 +543,9 @@ __device__ __forceinline__ void tile_pv(uint32_t vc, const float* __restrict__ v
 // scale-row indexing becomes immediate offsets), or 0 to read it from P.
 template <int D, int BK, int BV, int NT, int G>
 __device__ __forceinline__ void attn_chunk(const AttnParams& P, uint8_t* __restrict__ stage, int t0, int t_end, int lane,
-                                           const uint32_t (&qh)[D / 8], const uint32_t (&ql)[D / 8],
+                                           const LaneRow& LK, const LaneRow& LV, const uint32_t (&kso)[D / 64],
+                                           const uint32_t (&vso)[D / 64], const uint32_t (&qh)[D / 8],
+                                           const uint32_t (&ql)[D / 8],
                                            const float (&nb)[D / 16], float (&acc)[D / 4],
                                            float (&sv)[AttnCfg<D, BK, BV>::NSV], float& m, float& l) {
     using C = AttnCfg<D, BK, BV>;
@@ -465,7 +554,7 @@ __device__ __forceinline__ void attn_chunk(const AttnParams& P, uint8_t* __restr
     const uint32_t kc = ptx::smem_u32(stage + C::OFF_KC), vc = ptx::smem_u32(stage + C::OFF_VC);
     float* ks = reinterpret_cast<float*>(stage + C::OFF_KS);
     float* vs = reinterpret_cast<float*>(stage + C::OFF_VS);
-    const int sp = G ? D / G + 4 : P.sp;
+    const int sp = G ? D / G : P.sp;  // floats per scale row
     const int lg = G == 16 ? 4 : G == 32 ? 5 : G == 64 ? 6 : P.log2_group;
     const int valid = t_end - t0;  // tokens of this chunk inside the sequence (> 0)
     const bool tail = valid < 16 * NT;
@@ -483,7 +572,8 @@ __device__ __forceinline__ void attn_chunk(const AttnParams& P, uint8_t* __restr
     float s[NT][2];
 #pragma unroll
     for (int st = 0; st < NT; ++st) {
-        if (16 * st < valid) tile_scores<D, BK>(kc, ks, sp, lg, 16 * st, lane, qh, ql, nb, s[st]);
+        if (16 * st < valid)
+            tile_scores<D, BK, G>(kc, LK, stage + C::OFF_KS, kso, sp, lg, 16 * st, lane, qh, ql, nb, s[st]);
         else s[st][0] = s[st][1] = 0.f;
         if (tail) {
             if (16 * st + g >= valid) s[st][0] = -INFINITY;
@@ -529,7 +619,8 @@ __device__ __forceinline__ void attn_chunk(const AttnParams& P, uint8_t* __restr
         const bool sub_tail = vt < 16;
         const uint32_t mlo = (2 * c < vt ? 0x0000FFFFu : 0u) | (2 * c + 1 < vt ? 0xFFFF0000u : 0u);
         const uint32_t mhi = (2 * c + 8 < vt ? 0x0000FFFFu : 0u) | (2 * c + 9 < vt ? 0xFFFF0000u : 0u);
-        tile_pv<D, BV>(vc, vs, sp, lg, 16 * st, lane, P00, P10, P01, P11, mlo, mhi, sub_tail, acc, sv);
+        tile_pv<D, BV, G>(vc, LV, stage + C::OFF_VS, vso, sp, lg, 16 * st, lane, P00, P10, P01, P11, mlo, mhi,
+                          sub_tail, acc, sv);
     }
 }
 
@@ -561,7 +652,10 @@ __global__ void __launch_bounds__(kAttnWarps * 32, D >= 256 ? 2 : 3)
                            const __grid_constant__ CUtensorMap tm_vc, const __grid_constant__ CUtensorMap tm_vs,
                            const __grid_constant__ AttnParams P) {
     using C = AttnCfg<D, BK, BV>;
-    extern __shared__ __align__(1024) uint8_t smem[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // swizzled TMA destinations need 1024-byte alignment: realign (offsetting
+    // the shared array keeps every access in the shared window)
+    uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
     // the warp index through a shuffle, so the compiler knows it is warp-uniform
     // (barrier and TMA operands then stay in uniform registers)
     const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0), lane = threadIdx.x & 31;
@@ -573,8 +667,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32, D >= 256 ? 2 : 3)
     const int cps = (n_chunks + P.n_splits - 1) / P.n_splits;
     const int c_begin = split * cps, c_end = min(c_begin + cps, n_chunks);
 
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // 4 per warp
-    uint8_t* wbase = smem + 128 + warp * C::WARP_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BARS);  // 4 per warp
+    uint8_t* wbase = smem + warp * C::WARP_BYTES;
     constexpr int NS = C::NS;
     static_assert(NS >= 2 && NS <= 4, "stages per warp");
     if (lane == 0) {
@@ -588,6 +682,14 @@ __global__ void __launch_bounds__(kAttnWarps * 32, D >= 256 ? 2 : 3)
     uint32_t qh[C::QB], ql[C::QB];
     float nb[D / 16];
     build_qb<D, BK>(P.qt + ((long long)b * P.Hq + (long long)hkv * P.rep) * D, P.rep, g, c, qh, ql, nb);
+    // per-lane shared-memory addressing of the plane images
+    using PK = PlaneT<D, BK>;
+    using PV = PlaneT<D, BV>;
+    const LaneRow LK = lane_row_codes<PK::RB, PK::SWZ, PK::RP>(lane);
+    const LaneRow LV = BV == 16 ? lane_row_v16<PV::RB, PV::SWZ, PV::RP>(lane) : lane_row_codes<PV::RB, PV::SWZ, PV::RP>(lane);
+    uint32_t kso[D / 64], vso[D / 64];
+    scale_offsets<D, D / 64>(g, 0, kso);                               // K: row g (and g + 8)
+    scale_offsets<D, D / 64>(2 * c, BV == 4 ? 4 * (g & 1) : 0, vso);  // V: rows 2c (+1, +8, +9), column half
     float acc[C::ACC], sv[C::NSV];
 #pragma unroll
     for (int i = 0; i < C::ACC; ++i) acc[i] = 0.f;
@@ -597,7 +699,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, D >= 256 ? 2 : 3)
 
     const int plane_row = b * P.Hkv + hkv;  // this (batch, kv head)'s rows in the head-major planes
     const uint32_t kc_bytes = C::CH * PlaneT<D, BK>::RP, vc_bytes = C::CH * PlaneT<D, BV>::RP;
-    const uint32_t sc_bytes = C::CH * P.sp * 4;
+    const uint32_t sc_bytes = C::CH * P.sp * 4;  // exact rows of d/group floats
     const uint32_t tx = kc_bytes + vc_bytes + (C::QK ? sc_bytes : 0) + (C::QV ? sc_bytes : 0);
     auto issue = [&](int chunk, int st) {
         const uint32_t bar = barw(st);
@@ -633,8 +735,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32, D >= 256 ? 2 : 3)
             failed = true;
             break;
         }
-        attn_chunk<D, BK, BV, C::CH / 16, G>(P, wbase + st * C::STAGE, chunk * C::CH, L, lane, qh, ql, nb, acc, sv, m,
-                                             l);
+        attn_chunk<D, BK, BV, C::CH / 16, G>(P, wbase + st * C::STAGE, chunk * C::CH, L, lane, LK, LV, kso, vso, qh,
+                                             ql, nb, acc, sv, m, l);
         __syncwarp();
     }
     // the failure flag is per warp; every warp still joins the merge below
@@ -672,7 +774,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, D >= 256 ? 2 : 3)
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
     __syncthreads();  // all warps are done with their stage buffers
-    float* mw = reinterpret_cast<float*>(smem + 128);          // [warps][4][2]
+    float* mw = reinterpret_cast<float*>(smem);                 // [warps][4][2]
     float* aw = mw + kAttnWarps * 8;                            // [warps][4][D]
     if (g == 0) {
         mw[warp * 8 + c * 2 + 0] = m;
@@ -775,16 +877,32 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const __grid_constant
 // Host side
 // ---------------------------------------------------------------------------
 // A plane [B*Hkv][t_cap][row] (head-major: the rows of one (batch, kv head)
-// are contiguous); a box is box_rows consecutive tokens, each row padded to
-// box_inner elements in shared memory.
+// are contiguous); a box is box_rows consecutive tokens of box_inner elements
+// (the whole row, or the row plus zero-filled padding for unswizzled code rows
+// longer than 128 bytes).
 static bool encode_plane(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int inner_elems, int elem_bytes,
-                         int box_inner, long long bh, int t_cap, int box_rows) {
+                         int box_inner, long long bh, int t_cap, int box_rows, CUtensorMapSwizzle swz) {
     const unsigned long long dims[3] = {(unsigned long long)inner_elems, (unsigned long long)t_cap,
                                         (unsigned long long)bh};
     const unsigned long long strides[2] = {(unsigned long long)inner_elems * elem_bytes,
                                            (unsigned long long)inner_elems * elem_bytes * t_cap};
     const unsigned box[3] = {(unsigned)box_inner, (unsigned)box_rows, 1u};
-    return encode_tiled(map, dt, 3, const_cast<void*>(base), dims, strides, box, "attention cache plane");
+    return encode_tiled_swz(map, dt, 3, const_cast<void*>(base), dims, strides, box, swz, "attention cache plane");
+}
+static CUtensorMapSwizzle swizzle_for(int row_bytes) {
+    return row_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+           : row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+           : row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                              : CU_TENSOR_MAP_SWIZZLE_NONE;
+}
+template <int D, int BITS>
+static bool encode_codes(CUtensorMap* map, const void* base, long long bh, int t_cap, int rows) {
+    using PT = PlaneT<D, BITS>;
+    if (PT::SWZ)
+        return encode_plane(map, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, PT::RB, 1, PT::RB, bh, t_cap, rows,
+                            swizzle_for(PT::RB));
+    return encode_plane(map, base, CU_TENSOR_MAP_DATA_TYPE_UINT32, PT::RB / 4, 4, PT::RB / 4 + 4, bh, t_cap, rows,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 struct AttnLaunch {
@@ -801,18 +919,16 @@ static int launch_split(const AttnLaunch& A) {
     const AttnParams& P = A.P;
     const long long bh = (long long)P.B * P.Hkv;
     CUtensorMap tkc, tks, tvc, tvs;
-    if (!encode_plane(&tkc, A.k->codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, PlaneT<D, BK>::RB / 4, 4,
-                      PlaneT<D, BK>::RB / 4 + 4, bh, P.t_cap, C::CH))
-        return SRFTKV_ERR_CUDA;
-    if (!encode_plane(&tvc, A.v->codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, PlaneT<D, BV>::RB / 4, 4,
-                      PlaneT<D, BV>::RB / 4 + 4, bh, P.t_cap, C::CH))
-        return SRFTKV_ERR_CUDA;
+    if (!encode_codes<D, BK>(&tkc, A.k->codes, bh, P.t_cap, C::CH)) return SRFTKV_ERR_CUDA;
+    if (!encode_codes<D, BV>(&tvc, A.v->codes, bh, P.t_cap, C::CH)) return SRFTKV_ERR_CUDA;
+    // scale rows: d/group floats; group-16 rows are swizzled like code rows of the same length
     const int ng = D / P.group;
+    const CUtensorMapSwizzle ssw = P.group == 16 ? swizzle_for(4 * ng) : CU_TENSOR_MAP_SWIZZLE_NONE;
     tks = tkc;
     tvs = tvc;
-    if (C::QK && !encode_plane(&tks, A.k->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ng, 4, P.sp, bh, P.t_cap, C::CH))
+    if (C::QK && !encode_plane(&tks, A.k->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ng, 4, ng, bh, P.t_cap, C::CH, ssw))
         return SRFTKV_ERR_CUDA;
-    if (C::QV && !encode_plane(&tvs, A.v->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ng, 4, P.sp, bh, P.t_cap, C::CH))
+    if (C::QV && !encode_plane(&tvs, A.v->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ng, 4, ng, bh, P.t_cap, C::CH, ssw))
         return SRFTKV_ERR_CUDA;
     static bool attr[2] = {false, false};
     const bool g16 = P.group == 16;  // raw fp16 sides carry group 16
@@ -952,7 +1068,7 @@ int attention_entry(const void* q, float* out, const srftkv_side* k, const srftk
     P.group = raw ? 16 : group;
     P.log2_group = 0;
     while ((1 << P.log2_group) < P.group) ++P.log2_group;
-    P.sp = raw ? 8 : d / P.group + 4;
+    P.sp = raw ? 0 : d / P.group;
     const float sc = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt((float)d);
     P.qscale = sc * 1.4426950408889634f;
     sign_masks(d, seed, P.sign_mask);
