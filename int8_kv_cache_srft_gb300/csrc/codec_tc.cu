@@ -16,10 +16,13 @@
 //              3-stage ring;
 //   warp 1     allocates tensor memory and issues the MMAs (one thread) into
 //              two accumulator buffers;
-//   warps 2-9  epilogue: each reads 32 rows x 64 columns of an accumulator
+//   warps 2-17 epilogue: each reads 32 rows x 32 columns of an accumulator
 //              (warp w may only touch tensor-memory lanes 32(w%4)..+31),
-//              applies lambda, quantises its four 16-coordinate groups and
-//              stores codes and scales straight from registers.
+//              applies lambda, quantises its two 16-coordinate groups and
+//              stores codes and scales straight from registers.  The
+//              quantisation is a chain of dependent steps per row (absmax,
+//              reciprocal, rounding, packing); sixteen warps with short rows
+//              keep enough of them in flight to match the load rate.
 // R_hi / R_lo are built once per CTA in shared memory from the twiddle table
 // (entries of R are closed forms of cos and sin of 2 pi jk/d).
 #include "codec_impl.cuh"
@@ -38,7 +41,8 @@ constexpr int T_OFF_BLO = T_B_BYTES;
 constexpr int T_OFF_A = 2 * T_B_BYTES;
 constexpr int T_OFF_BAR = T_OFF_A + TSTAGES * T_A_BYTES;
 constexpr int T_SMEM = T_OFF_BAR + 128 + 1024;  // + barriers + alignment slack
-constexpr int T_WARPS = 10;
+constexpr int T_EPI = 16;                     // epilogue warps of the quantize kernel
+constexpr int T_WARPS = 2 + T_EPI;
 constexpr uint32_t T_IDESC = tc::idesc_f16_f32(TM, TD);
 constexpr uint32_t T_TMEM_COLS = 256;         // two 128-column fp32 accumulators
 }  // namespace
@@ -103,7 +107,7 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(bar(6 + a), 1);
-            ptx::mbar_init(bar(8 + a), 8);
+            ptx::mbar_init(bar(8 + a), T_EPI);
         }
         ptx::fence_barrier_init();
     }
@@ -158,7 +162,8 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
             }
         }
     } else {
-        const int quarter = warp & 3, half = (warp - 2) >> 2;
+        // warp w reads tensor-memory lanes 32(w%4)..+31 (tile rows) and column quarter cq
+        const int quarter = warp & 3, cq = (warp - 2) >> 2;
         for (int t = blockIdx.x, i = 0; t < P.total_tiles; t += stride, ++i) {
             const int a = i & 1;
             const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(bar(6 + a), (i >> 1) & 1));
@@ -167,12 +172,10 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
                 break;
             }
             tc::fence_after_sync();
-            uint32_t r0[32], r1[32];
-            const uint32_t taddr = tmem + ((uint32_t)(32 * quarter) << 16) + a * TD + half * 64;
+            uint32_t r0[32];
+            const uint32_t taddr = tmem + ((uint32_t)(32 * quarter) << 16) + a * TD + cq * 32;
             tc::ld_32x32b_x32(taddr, r0);
-            tc::ld_32x32b_x32(taddr + 32, r1);
             tc::wait_ld(r0);
-            tc::wait_ld(r1);
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(8 + a));  // accumulator a may be overwritten
@@ -181,17 +184,14 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
             const CodecSideK& S = P.side[id.side];
             const int t_tok = id.t0 + 32 * quarter + lane;
             if (t_tok >= P.n_tokens) continue;
-            float z[64];
+            float z[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                z[j] = __uint_as_float(r0[j]);
-                z[32 + j] = __uint_as_float(r1[j]);
-            }
+            for (int j = 0; j < 32; ++j) z[j] = __uint_as_float(r0[j]);
             if (S.lambda != nullptr) {
                 const float4* lr = reinterpret_cast<const float4*>(
-                    S.lambda + (long long)id.o * S.lambda_outer_stride + (long long)id.h * TD + half * 64);
+                    S.lambda + (long long)id.o * S.lambda_outer_stride + (long long)id.h * TD + cq * 32);
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
+                for (int c = 0; c < 8; ++c) {
                     const float4 l = __ldg(lr + c);
                     z[4 * c] *= l.x;
                     z[4 * c + 1] *= l.y;
@@ -200,13 +200,13 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
                 }
             }
             const long long vrow = packed_row(P, id, t_tok);
-            const int ng = TD / P.group;
+            const int ng = TD / P.group;  // groups of at most 32: a column quarter holds whole groups
             if (BK == BV || id.side == 0)
-                quant_store_row<64, BK>(z, P.group, S.codes + vrow * (TD * BK / 8) + half * (64 * BK / 8),
-                                        S.scales + vrow * ng + half * (ng / 2));
+                quant_store_row<32, BK>(z, P.group, S.codes + vrow * (TD * BK / 8) + cq * (32 * BK / 8),
+                                        S.scales + vrow * ng + cq * (ng / 4));
             else
-                quant_store_row<64, BV>(z, P.group, S.codes + vrow * (TD * BV / 8) + half * (64 * BV / 8),
-                                        S.scales + vrow * ng + half * (ng / 2));
+                quant_store_row<32, BV>(z, P.group, S.codes + vrow * (TD * BV / 8) + cq * (32 * BV / 8),
+                                        S.scales + vrow * ng + cq * (ng / 4));
         }
     }
     if (failed) atomicOr(P.fault, 1u);
@@ -219,72 +219,178 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
 // ---------------------------------------------------------------------------
 // Dequantize: X_hat = P_hat . (R_s)^T, P_hat = codes * scale / lambda
 // ---------------------------------------------------------------------------
-// Warp roles (one persistent CTA per SM, 10 warps):
-//   warp 0     allocates tensor memory and issues the MMAs (one thread);
-//   warp 1     TMA producer: the tile's code rows and scale rows, each padded
-//              by 16 bytes in shared memory (conflict-free row reads), into a
-//              ring of input stages;
-//   warps 2-5  converters: thread = row of the tile; decode codes * scale,
-//              divide by lambda, write P_hat as fp16 into a 128-byte-swizzled
-//              A stage;
-//   warps 6-9  epilogue: tensor memory -> fp16 -> swizzled staging -> TMA store
-//              (warp w reads tensor-memory lanes 32(w%4)..+31).
-// B = diag(s) R (signs folded in), split hi + lo, so X_hat = s (R^T P_hat).
-// P_hat is rounded once to fp16 before the contraction; the result is rounded
-// to fp16 again on output.
+// Warp roles (one persistent CTA per SM, 18 warps):
+//   warp 0      allocates tensor memory and issues the MMAs (one thread);
+//   warp 1      TMA producer: the tile's code rows and scale rows, copied as
+//               exact rows (TMA swizzle equal to the row length keeps the
+//               row-per-thread reads free of bank conflicts), into a ring of
+//               input stages;
+//   warps 2-9   converters: thread = half a row of the tile; decode codes *
+//               scale, divide by lambda, write P_hat as fp16 straight into
+//               tensor memory (the MMA takes A from there: no shared-memory
+//               round trip, which with the B reads would otherwise exceed the
+//               SM's shared-memory bandwidth);
+//   warps 10-17 epilogue: tensor memory -> fp16 -> swizzled staging -> TMA
+//               store (warp w reads tensor-memory lanes 32(w%4)..+31, one
+//               column half).
+// Converting is a dependent chain per row; eight warps on half rows keep
+// enough of them in flight to match the load rate.
+// B = diag(s) R (signs folded in), so X_hat = s (R^T P_hat).  P_hat is
+// rounded once to fp16 before the contraction and the result is rounded to
+// fp16 again on output; R_s in fp16 (11 bits) matches that precision, so
+// unlike the quantize kernel (whose rounding decisions need R to about 21
+// bits, hence hi + lo) one contraction per tile suffices.
 namespace {
-constexpr int DQ_WARPS = 10;
-constexpr int DQ_SP = 12;                               // padded scale row (floats), groups of 16 or 32
-constexpr int DQ_OFF_A = 2 * T_B_BYTES;                 // two A stages of 32 KB
-constexpr int DQ_OFF_O = DQ_OFF_A + 2 * T_A_BYTES;      // one output staging buffer of 32 KB
-constexpr int DQ_OFF_IN = DQ_OFF_O + T_A_BYTES;         // input stages
+constexpr int DQ_CONV = 8, DQ_EPI = 8;                // converter and epilogue warps
+constexpr int DQ_WARPS = 2 + DQ_CONV + DQ_EPI;
+constexpr int DQ_OFF_O = T_B_BYTES;                     // two output staging buffers of 32 KB (after R_s)
+constexpr int DQ_OFF_IN = DQ_OFF_O + 2 * T_A_BYTES;     // input stages
+constexpr int DQ_NA = 3;                                // A buffers in tensor memory
+constexpr uint32_t DQ_TMEM_COLS = 512;                  // accumulators 0..255, A buffers 256..447
+constexpr uint32_t DQ_A_COL = 256;                      // A buffer b: 64 columns (128 fp16 per lane) at 256 + 64 b
 template <int BK, int BV>
 struct DqCfg {
-    static constexpr int RBMAX = TD * (BK > BV ? BK : BV) / 8;
-    static constexpr int CODE_RP = RBMAX + 16;                      // padded code row
-    static constexpr int OFF_SC = TM * CODE_RP;
-    static constexpr int STAGE = (OFF_SC + TM * DQ_SP * 4 + 1023) / 1024 * 1024;
-    static constexpr int STAGES = (BK == 4 && BV == 4) ? 3 : 2;
+    static constexpr int RBMAX = TD * (BK > BV ? BK : BV) / 8;     // exact code rows (64 or 128 bytes)
+    static constexpr int OFF_SC = TM * RBMAX;                       // 1024-aligned
+    static constexpr int STAGE = (OFF_SC + TM * 32 + 1023) / 1024 * 1024;  // scale rows of at most 32 bytes
+    static constexpr int STAGES = (BK == 4 && BV == 4) ? 4 : 3;
     static constexpr int OFF_BAR = DQ_OFF_IN + STAGES * STAGE;
     static constexpr int SMEM = OFF_BAR + 256 + 1024;
 };
+// 16-byte chunk c of row r of a buffer of RB-byte rows written by TMA with the
+// swizzle mode equal to RB (32, 64 or 128; 16 = no swizzle), 1024-aligned
+__device__ __forceinline__ int swz16(int rb, int r, int c) { return rb >= 32 ? c ^ (((r * rb) >> 7) & (rb / 16 - 1)) : c; }
+
+// K order of the dequantize contraction.  A column c = 4k + j (k: 8-element
+// code word, j = 0..3) holds the packed coordinates (8k + j, 8k + j + 4): those
+// two codes sit at bit offsets 16 apart in a 4-bit code word, so one logic op
+// and one f16x2 op turn them into an exact fp16 pair.  B is built in the same
+// K order, so the contraction is unchanged.
+__host__ __device__ constexpr int dq_kperm(int q) { return 8 * (q >> 3) + ((q >> 1) & 3) + 4 * (q & 1); }
+
+__device__ __forceinline__ uint32_t h2sub(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t h2mul(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t h2fma(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t r;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+    return r;
+}
+// Exact fp16 pairs of signed codes: XOR with 8 (128) makes a code offset
+// binary; under the exponent of 1024 its fp16 value is 1024 + 8 + q
+// (1024 + 16 (q + 8) for the high nibble, 1024 + 128 + q for bytes), and one
+// f16x2 subtract (or scaled fma) leaves q.
+__device__ __forceinline__ uint32_t codes_lo4(uint32_t w) {  // nibbles at bits 0 and 16
+    return h2sub((w & 0x000F000Fu) ^ 0x64086408u, 0x64086408u);
+}
+__device__ __forceinline__ uint32_t codes_hi4(uint32_t w) {  // nibbles at bits 4 and 20
+    return h2fma((w & 0x00F000F0u) ^ 0x64806480u, 0x2C002C00u /* 1/16 */, 0xD480D480u /* -72 */);
+}
+__device__ __forceinline__ uint32_t codes_b8(uint32_t w) {  // bytes 0 and 2
+    return h2sub((w & 0x00FF00FFu) ^ 0x64806480u, 0x64806480u);
+}
+__device__ __forceinline__ uint32_t half2_bcast(__half h) {
+    const uint32_t u = __half_as_ushort(h);
+    return u | (u << 16);
+}
 }  // namespace
 
-template <int D, int BITS>
-__device__ __forceinline__ void dequant_row_smem(const uint8_t* __restrict__ crow, const float* __restrict__ srow,
-                                                 int group, float (&p)[D]) {
-    constexpr int WORDS = D * BITS / 32, PER = 32 / BITS, U = D / 16;
-    uint32_t w[WORDS];
+// codes * scale for columns 64 hf .. 64 hf + 63 of tile row m, from the
+// stage's exact swizzled code rows (64 bytes for 4-bit, 128 for 8-bit) and
+// scale rows (TD / group floats: 32 bytes for group 16, 16 for group 32)
+template <int BITS>
+__device__ __forceinline__ void dequant_half_smem(const uint8_t* __restrict__ in, int off_sc, int m, int hf, int group,
+                                                  float (&p)[64]) {
+    constexpr int RB = TD * BITS / 8, NCH = 64 * BITS / 128, PER = 32 / BITS;  // chunks per half row
+    uint32_t w[4 * NCH];
 #pragma unroll
-    for (int i = 0; i < WORDS / 4; ++i) {
-        const uint4 v = reinterpret_cast<const uint4*>(crow)[i];
-        w[4 * i] = v.x;
-        w[4 * i + 1] = v.y;
-        w[4 * i + 2] = v.z;
-        w[4 * i + 3] = v.w;
+    for (int k = 0; k < NCH; ++k) {
+        const uint4 v = *reinterpret_cast<const uint4*>(in + m * RB + (swz16(RB, m, NCH * hf + k) << 4));
+        w[4 * k] = v.x;
+        w[4 * k + 1] = v.y;
+        w[4 * k + 2] = v.z;
+        w[4 * k + 3] = v.w;
     }
-    float sc[U];
-    if (group == 16) {  // one scale per 16-coordinate unit: vector loads of the (padded) scale row
+    float sc[4];
+    const int srb = 4 * (TD / group);
+    if (group == 16) {  // groups 4hf .. 4hf+3: chunk hf of the 32-byte row
+        const float4 v = *reinterpret_cast<const float4*>(in + off_sc + m * srb + (swz16(srb, m, hf) << 4));
+        sc[0] = v.x;
+        sc[1] = v.y;
+        sc[2] = v.z;
+        sc[3] = v.w;
+    } else {  // group 32: groups 2hf, 2hf+1 of the 16-byte row
+        const float2 v = *reinterpret_cast<const float2*>(in + off_sc + m * srb + 8 * hf);
+        sc[0] = sc[1] = v.x;
+        sc[2] = sc[3] = v.y;
+    }
 #pragma unroll
-        for (int i = 0; i < U / 4; ++i) {
-            const float4 v = reinterpret_cast<const float4*>(srow)[i];
-            sc[4 * i] = v.x;
-            sc[4 * i + 1] = v.y;
-            sc[4 * i + 2] = v.z;
-            sc[4 * i + 3] = v.w;
-        }
+    for (int i = 0; i < 64; ++i) {
+        const float c = (BITS == 4) ? code_int4(w[i / PER], i % PER) : code_int8(w[i / PER], i % PER);
+        p[i] = c * sc[i >> 4];
+    }
+}
+
+// P_hat for columns 64 hf .. +63 of tile row m directly as fp16 pairs in the
+// K order of dq_kperm (no lambda): codes -> exact fp16 pairs -> times the
+// group scale split into fp16 hi + lo, P_hat = fp16(q s_hi + fp16(q s_lo)), one
+// main rounding as when the fp32 product q s is rounded to fp16.
+template <int BITS>
+__device__ __forceinline__ void dequant_half_pairs(const uint8_t* __restrict__ in, int off_sc, int m, int hf, int group,
+                                                   uint32_t (&hp)[32]) {
+    constexpr int RB = TD * BITS / 8, NCH = 64 * BITS / 128;
+    uint32_t w[4 * NCH];
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) {
+        const uint4 v = *reinterpret_cast<const uint4*>(in + m * RB + (swz16(RB, m, NCH * hf + k) << 4));
+        w[4 * k] = v.x;
+        w[4 * k + 1] = v.y;
+        w[4 * k + 2] = v.z;
+        w[4 * k + 3] = v.w;
+    }
+    float sc[4];
+    const int srb = 4 * (TD / group);
+    if (group == 16) {
+        const float4 v = *reinterpret_cast<const float4*>(in + off_sc + m * srb + (swz16(srb, m, hf) << 4));
+        sc[0] = v.x;
+        sc[1] = v.y;
+        sc[2] = v.z;
+        sc[3] = v.w;
     } else {
-        const int sh = __ffs(group >> 4) - 1;
+        const float2 v = *reinterpret_cast<const float2*>(in + off_sc + m * srb + 8 * hf);
+        sc[0] = sc[1] = v.x;
+        sc[2] = sc[3] = v.y;
+    }
+    uint32_t sh[4], sl[4];
 #pragma unroll
-        for (int u = 0; u < U; ++u) sc[u] = srow[u >> sh];
+    for (int g = 0; g < 4; ++g) {
+        const __half h = __float2half_rn(sc[g]);
+        sh[g] = half2_bcast(h);
+        sl[g] = half2_bcast(__float2half_rn(sc[g] - __half2float(h)));
     }
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
+    for (int k = 0; k < 8; ++k) {  // 8-element word k of the half: coordinates 64 hf + 8k .. +7, group k/2
+        uint32_t c[4];
+        if constexpr (BITS == 4) {
+            const uint32_t x = w[k], xs = x >> 8;
+            c[0] = codes_lo4(x);
+            c[1] = codes_hi4(x);
+            c[2] = codes_lo4(xs);
+            c[3] = codes_hi4(xs);
+        } else {
 #pragma unroll
-        for (int i = 16 * u; i < 16 * u + 16; ++i) {
-            const float c = (BITS == 4) ? code_int4(w[i / PER], i % PER) : code_int8(w[i / PER], i % PER);
-            p[i] = c * sc[u];
+            for (int j = 0; j < 4; ++j)  // bytes j of the two words: coordinates 8k + j and 8k + j + 4
+                c[j] = codes_b8(__byte_perm(w[2 * k], w[2 * k + 1], j | (j << 4) | ((4 + j) << 8) | ((4 + j) << 12)));
         }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) hp[4 * k + j] = h2fma(c[j], sh[k >> 1], h2mul(c[j], sl[k >> 1]));
     }
 }
 
@@ -302,15 +408,19 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
     const uint32_t sbase = ptx::smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-    // a_full[0,1], a_empty[2,3], acc_full[4,5], acc_empty[6,7], in_full[8..10], in_empty[11..13]; tmem slot at 14
+    // a_full[0..2], a_empty[3..5], acc_full[6,7], acc_empty[8,9], in_full[10..13], in_empty[14..17];
+    // tensor-memory slot at 18
     auto bar = [&](int i) { return ptx::smem_u32(&bars[i]); };
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[14]);
+    constexpr int A_FULL = 0, A_EMPTY = 3, ACC_FULL = 6, ACC_EMPTY = 8, IN_FULL = 10, IN_EMPTY = 14;
+    static_assert(C::STAGES <= 4, "input stages");
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[18]);
 
     {  // B[k][n] = s_k R[n][k], hi and lo
         constexpr float inv_sqrt_d = 0.08838834764831845f;
         constexpr float c2 = 0.125f;
         for (int idx = threadIdx.x; idx < TD * TD; idx += blockDim.x) {
-            const int k = idx >> 7, n = idx & 127;  // B row k (output coordinate), column n (packed coordinate)
+            // B row k (output coordinate), K position q holding packed coordinate n
+            const int k = idx >> 7, q = idx & 127, n = dq_kperm(q);
             float v;
             if (n == 0) {
                 v = inv_sqrt_d;
@@ -321,29 +431,27 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
                 v = (n & 1) ? c2 * tw_im(m) : c2 * tw_re(m);
             }
             if (P.sign_mask[k >> 1] & ((k & 1) ? 0x80000000u : 0x8000u)) v = -v;
-            const __half hi = __float2half_rn(v);
-            const __half lo = __float2half_rn(v - __half2float(hi));
-            const uint32_t off = sw128_offset(k, n);
-            *reinterpret_cast<__half*>(smem + off) = hi;
-            *reinterpret_cast<__half*>(smem + T_OFF_BLO + off) = lo;
+            *reinterpret_cast<__half*>(smem + sw128_offset(k, q)) = __float2half_rn(v);
         }
         ptx::fence_proxy_async_smem();
     }
     if (threadIdx.x == 0) {
+        for (int b = 0; b < DQ_NA; ++b) {
+            ptx::mbar_init(bar(A_FULL + b), DQ_CONV);
+            ptx::mbar_init(bar(A_EMPTY + b), 1);
+        }
         for (int a = 0; a < 2; ++a) {
-            ptx::mbar_init(bar(0 + a), 4);
-            ptx::mbar_init(bar(2 + a), 1);
-            ptx::mbar_init(bar(4 + a), 1);
-            ptx::mbar_init(bar(6 + a), 4);
+            ptx::mbar_init(bar(ACC_FULL + a), 1);
+            ptx::mbar_init(bar(ACC_EMPTY + a), DQ_EPI);
         }
         for (int st = 0; st < C::STAGES; ++st) {
-            ptx::mbar_init(bar(8 + st), 1);
-            ptx::mbar_init(bar(11 + st), 4);
+            ptx::mbar_init(bar(IN_FULL + st), 1);
+            ptx::mbar_init(bar(IN_EMPTY + st), DQ_CONV);
         }
         ptx::fence_barrier_init();
     }
     if (warp == 0) {
-        tc::tmem_alloc(ptx::smem_u32(tmem_slot), T_TMEM_COLS);
+        tc::tmem_alloc(ptx::smem_u32(tmem_slot), DQ_TMEM_COLS);
         tc::tmem_relinquish();
     }
     tc::fence_before_sync();
@@ -356,31 +464,29 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
     if (warp == 0) {
         if (lane == 0) {
             for (int t = blockIdx.x, i = 0; t < P.total_tiles; t += stride, ++i) {
-                const int s = i & 1;
-                if (!ptx::mbar_wait_bounded(bar(0 + s), (i >> 1) & 1) ||
-                    (i >= 2 && !ptx::mbar_wait_bounded(bar(6 + s), ((i >> 1) - 1) & 1))) {
+                const int s = i & 1, b = i % DQ_NA;
+                if (!ptx::mbar_wait_bounded(bar(A_FULL + b), (i / DQ_NA) & 1) ||
+                    (i >= 2 && !ptx::mbar_wait_bounded(bar(ACC_EMPTY + s), ((i >> 1) - 1) & 1))) {
                     failed = true;
                     break;
                 }
                 tc::fence_after_sync();
                 const uint32_t d_tmem = tmem + s * TD;
-                const uint32_t a_base = sbase + DQ_OFF_A + s * T_A_BYTES;
+                const uint32_t a_tmem = tmem + DQ_A_COL + b * 64;
 #pragma unroll
                 for (int ks = 0; ks < TD / 16; ++ks) {
                     const uint32_t koff = (ks >> 2) * T_KB_BYTES + (ks & 3) * 32;
-                    const uint64_t ad = tc::sw128_desc(a_base + koff);
-                    tc::mma_f16(d_tmem, ad, tc::sw128_desc(sbase + koff), T_IDESC, ks > 0);
-                    tc::mma_f16(d_tmem, ad, tc::sw128_desc(sbase + T_OFF_BLO + koff), T_IDESC, 1);
+                    tc::mma_f16_ta(d_tmem, a_tmem + 8 * ks, tc::sw128_desc(sbase + koff), T_IDESC, ks > 0);
                 }
-                tc::commit(bar(2 + s));  // A stage s may be rewritten
-                tc::commit(bar(4 + s));  // accumulator s is ready
+                tc::commit(bar(A_EMPTY + b));  // A buffer b may be rewritten
+                tc::commit(bar(ACC_FULL + s));  // accumulator s is ready
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
             for (int t = blockIdx.x, i = 0; t < P.total_tiles; t += stride, ++i) {
                 const int st = i % C::STAGES, use = i / C::STAGES;
-                if (use > 0 && !ptx::mbar_wait_bounded(bar(11 + st), (use - 1) & 1)) {
+                if (use > 0 && !ptx::mbar_wait_bounded(bar(IN_EMPTY + st), (use - 1) & 1)) {
                     failed = true;
                     break;
                 }
@@ -389,103 +495,114 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
                 const uint32_t dst = sbase + DQ_OFF_IN + st * C::STAGE;
                 const int row = P.t_offset + id.t0;   // packed planes: [outer*H][t_cap] rows
                 const int oh = id.o * P.H + id.h;
-                ptx::mbar_arrive_expect_tx(bar(8 + st), TM * (TD * bits / 8 + 16) + TM * (TD / P.group + 4) * 4);
-                ptx::tma_load_3d(dst, &M.codes[id.side], bar(8 + st), 0, row, oh);
-                ptx::tma_load_3d(dst + C::OFF_SC, &M.scales[id.side], bar(8 + st), 0, row, oh);
+                ptx::mbar_arrive_expect_tx(bar(IN_FULL + st), TM * (TD * bits / 8) + TM * (TD / P.group) * 4);
+                ptx::tma_load_3d(dst, &M.codes[id.side], bar(IN_FULL + st), 0, row, oh);
+                ptx::tma_load_3d(dst + C::OFF_SC, &M.scales[id.side], bar(IN_FULL + st), 0, row, oh);
             }
         }
-    } else if (warp <= 5) {
-        const int m = threadIdx.x - 64;  // row of the tile, 0..127
+    } else if (warp < 2 + DQ_CONV) {
+        // converter warp w: tile rows = tensor-memory lanes 32(w%4)..+31 (the
+        // quarter a warp may write), column half (w-2)/4
+        const int quarter = warp & 3, m = 32 * quarter + lane, hf = (warp - 2) >> 2;
         for (int t = blockIdx.x, i = 0; t < P.total_tiles; t += stride, ++i) {
-            const int s = i & 1, st = i % C::STAGES;
+            const int b = i % DQ_NA, st = i % C::STAGES;
             const TileId id = decode_tile128(P, t);
             const CodecSideK& S = P.side[id.side];
             const int t_tok = id.t0 + m;
-            const bool ok_in = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(bar(8 + st), (i / C::STAGES) & 1));
+            const bool ok_in = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(bar(IN_FULL + st), (i / C::STAGES) & 1));
             if (!ok_in) {
                 failed = true;
                 break;
             }
             const uint8_t* in = smem + DQ_OFF_IN + st * C::STAGE;
-            const float* srow = reinterpret_cast<const float*>(in + C::OFF_SC) + m * (TD / P.group + 4);
-            float p[TD];
-            if (BK == BV || id.side == 0)
-                dequant_row_smem<TD, BK>(in + m * (TD * BK / 8 + 16), srow, P.group, p);
-            else
-                dequant_row_smem<TD, BV>(in + m * (TD * BV / 8 + 16), srow, P.group, p);
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(11 + st));  // input stage consumed
-            if (t_tok < P.n_tokens && S.lambda != nullptr) {
-                const float4* lr = reinterpret_cast<const float4*>(S.lambda + (long long)id.o * S.lambda_outer_stride +
-                                                                   (long long)id.h * TD);
+            uint32_t hp[32];  // fp16 pairs in the K order of dq_kperm: column 32 hf + c
+            const bool side_k = BK == BV || id.side == 0;
+            if (S.lambda == nullptr) {
+                if (side_k)
+                    dequant_half_pairs<BK>(in, C::OFF_SC, m, hf, P.group, hp);
+                else
+                    dequant_half_pairs<BV>(in, C::OFF_SC, m, hf, P.group, hp);
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(IN_EMPTY + st));  // input stage consumed
+            } else {
+                float p[64];
+                if (side_k)
+                    dequant_half_smem<BK>(in, C::OFF_SC, m, hf, P.group, p);
+                else
+                    dequant_half_smem<BV>(in, C::OFF_SC, m, hf, P.group, p);
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(IN_EMPTY + st));  // input stage consumed
+                if (t_tok < P.n_tokens) {
+                    const float4* lr = reinterpret_cast<const float4*>(
+                        S.lambda + (long long)id.o * S.lambda_outer_stride + (long long)id.h * TD + 64 * hf);
 #pragma unroll
-                for (int c = 0; c < TD / 4; ++c) {
-                    const float4 l = __ldg(lr + c);
-                    p[4 * c] = __fdividef(p[4 * c], l.x);
-                    p[4 * c + 1] = __fdividef(p[4 * c + 1], l.y);
-                    p[4 * c + 2] = __fdividef(p[4 * c + 2], l.z);
-                    p[4 * c + 3] = __fdividef(p[4 * c + 3], l.w);
+                    for (int c = 0; c < 16; ++c) {
+                        const float4 l = __ldg(lr + c);
+                        p[4 * c] = __fdividef(p[4 * c], l.x);
+                        p[4 * c + 1] = __fdividef(p[4 * c + 1], l.y);
+                        p[4 * c + 2] = __fdividef(p[4 * c + 2], l.z);
+                        p[4 * c + 3] = __fdividef(p[4 * c + 3], l.w);
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const int e = dq_kperm(2 * c);  // coordinates e, e + 4 of the half
+                    hp[c] = pack_half2(p[e], p[e + 4]);
                 }
             }
-            const bool ok = __all_sync(0xffffffffu, i < 2 || ptx::mbar_wait_bounded(bar(2 + s), ((i >> 1) - 1) & 1));
+            const bool ok = __all_sync(0xffffffffu,
+                                       i < DQ_NA || ptx::mbar_wait_bounded(bar(A_EMPTY + b), (i / DQ_NA - 1) & 1));
             if (!ok) {
                 failed = true;
                 break;
             }
-            uint8_t* A = smem + DQ_OFF_A + s * T_A_BYTES;
-#pragma unroll
-            for (int ch = 0; ch < TD / 8; ++ch) {  // 16-byte chunk ch holds columns 8ch..8ch+7
-                uint4 v;
-                v.x = pack_half2(p[8 * ch + 0], p[8 * ch + 1]);
-                v.y = pack_half2(p[8 * ch + 2], p[8 * ch + 3]);
-                v.z = pack_half2(p[8 * ch + 4], p[8 * ch + 5]);
-                v.w = pack_half2(p[8 * ch + 6], p[8 * ch + 7]);
-                *reinterpret_cast<uint4*>(A + sw128_offset(m, 8 * ch)) = v;
-            }
-            ptx::fence_proxy_async_smem();
+            tc::fence_after_sync();  // the MMAs that read A buffer b are complete
+            tc::st_32x32b_x32(tmem + ((uint32_t)(32 * quarter) << 16) + DQ_A_COL + b * 64 + 32 * hf, hp);
+            tc::wait_st();
+            tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(0 + s));
+            if (lane == 0) ptx::mbar_arrive(bar(A_FULL + b));
         }
     } else {
         const int quarter = warp & 3;   // tensor-memory lanes 32*quarter..+31 = tile rows
-        const int m = 32 * quarter + lane;
-        const bool leader = (warp == 6 && lane == 0);
+        const int m = 32 * quarter + lane, hf = (warp - 2 - DQ_CONV) >> 2;  // and column half hf
+        const bool leader = (warp == 2 + DQ_CONV && lane == 0);
         for (int t = blockIdx.x, i = 0; t < P.total_tiles; t += stride, ++i) {
             const int s = i & 1;
-            const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(bar(4 + s), (i >> 1) & 1));
+            const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(bar(ACC_FULL + s), (i >> 1) & 1));
             if (!ok) {
                 failed = true;
                 break;
             }
             tc::fence_after_sync();
-            uint32_t v[4][32];
-            const uint32_t taddr = tmem + ((uint32_t)(32 * quarter) << 16) + s * TD;
+            uint32_t v[2][32];
+            const uint32_t taddr = tmem + ((uint32_t)(32 * quarter) << 16) + s * TD + 64 * hf;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) tc::ld_32x32b_x32(taddr + 32 * j, v[j]);
+            for (int j = 0; j < 2; ++j) tc::ld_32x32b_x32(taddr + 32 * j, v[j]);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) tc::wait_ld(v[j]);
+            for (int j = 0; j < 2; ++j) tc::wait_ld(v[j]);
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(6 + s));
-            // the staging buffer: the TMA store of the previous tile must have read it
-            if (leader) ptx::bulk_wait_read<0>();
-            ptx::named_bar_sync(1, 128);
-            uint8_t* O = smem + DQ_OFF_O;
+            if (lane == 0) ptx::mbar_arrive(bar(ACC_EMPTY + s));
+            // staging buffer s: the TMA store issued from it two tiles ago must have read it
+            if (leader) ptx::bulk_wait_read<1>();
+            ptx::named_bar_sync(1, 32 * DQ_EPI);
+            uint8_t* O = smem + DQ_OFF_O + s * T_A_BYTES;
 #pragma unroll
-            for (int ch = 0; ch < TD / 8; ++ch) {
+            for (int ch = 0; ch < 8; ++ch) {
                 const int j = ch >> 2, c0 = (ch & 3) * 8;
                 uint4 w;
                 w.x = pack_half2(__uint_as_float(v[j][c0 + 0]), __uint_as_float(v[j][c0 + 1]));
                 w.y = pack_half2(__uint_as_float(v[j][c0 + 2]), __uint_as_float(v[j][c0 + 3]));
                 w.z = pack_half2(__uint_as_float(v[j][c0 + 4]), __uint_as_float(v[j][c0 + 5]));
                 w.w = pack_half2(__uint_as_float(v[j][c0 + 6]), __uint_as_float(v[j][c0 + 7]));
-                *reinterpret_cast<uint4*>(O + sw128_offset(m, 8 * ch)) = w;
+                *reinterpret_cast<uint4*>(O + sw128_offset(m, 64 * hf + 8 * ch)) = w;
             }
             ptx::fence_proxy_async_smem();
-            ptx::named_bar_sync(1, 128);
+            ptx::named_bar_sync(1, 32 * DQ_EPI);
             if (leader) {
                 const TileId id = decode_tile128(P, t);
-                const uint32_t src = sbase + DQ_OFF_O;
+                const uint32_t src = sbase + DQ_OFF_O + s * T_A_BYTES;
                 ptx::tma_store_4d(&M.out[id.side], src, 0, id.h, id.t0, id.o);
                 ptx::tma_store_4d(&M.out[id.side], src + T_KB_BYTES, 64, id.h, id.t0, id.o);
                 ptx::bulk_commit();
@@ -497,7 +614,7 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    if (warp == 0) tc::tmem_dealloc(tmem, T_TMEM_COLS);
+    if (warp == 0) tc::tmem_dealloc(tmem, DQ_TMEM_COLS);
 }
 
 template <int BK, int BV>
@@ -516,18 +633,26 @@ static int launch_dq_tc(const CodecCall& c) {
     for (int s = 0; s < 2; ++s) {
         const CodecSideDesc& d = c.side[s < c.n_sides ? s : 0];
         const int rb = TD * d.bits / 8;
-        // packed planes [n_outer*H][t_cap][row], row padded by 16 bytes in shared memory
-        const unsigned long long cdims[3] = {(unsigned long long)rb / 4, tcap, nrow};
+        // packed planes [n_outer*H][t_cap][row], copied as exact rows with the
+        // swizzle mode equal to the row length (64/128-byte code rows, 32-byte
+        // group-16 scale rows; 16-byte group-32 scale rows unswizzled)
+        auto swz = [](int bytes) {
+            return bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                   : bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                   : bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                 : CU_TENSOR_MAP_SWIZZLE_NONE;
+        };
+        const unsigned long long cdims[3] = {(unsigned long long)rb, tcap, nrow};
         const unsigned long long cstr[2] = {(unsigned long long)rb, tcap * rb};
-        const unsigned cbox[3] = {(unsigned)(rb / 4 + 4), (unsigned)TM, 1u};
+        const unsigned cbox[3] = {(unsigned)rb, (unsigned)TM, 1u};
         const unsigned long long sdims[3] = {(unsigned long long)ng, tcap, nrow};
         const unsigned long long sstr[2] = {ng * 4ull, tcap * ng * 4ull};
-        const unsigned sbox[3] = {(unsigned)(ng + 4), (unsigned)TM, 1u};
+        const unsigned sbox[3] = {(unsigned)ng, (unsigned)TM, 1u};
         if (!encode_x_map(&M.out[s], d.x, TD, c.H, c.n_tokens, c.n_outer, TM, true) ||
-            !encode_tiled(&M.codes[s], CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, d.codes, cdims, cstr, cbox,
-                          "tensor-core dequantize codes") ||
-            !encode_tiled(&M.scales[s], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, d.scales, sdims, sstr, sbox,
-                          "tensor-core dequantize scales"))
+            !encode_tiled_swz(&M.codes[s], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, d.codes, cdims, cstr, cbox, swz(rb),
+                              "tensor-core dequantize codes") ||
+            !encode_tiled_swz(&M.scales[s], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, d.scales, sdims, sstr, sbox,
+                              swz(4 * ng), "tensor-core dequantize scales"))
             return SRFTKV_ERR_CUDA;
     }
     static bool attr = false;
@@ -577,7 +702,7 @@ static int launch_tc(const CodecCall& c) {
 }
 
 int codec_quantize_tc(const CodecCall& c) {
-    if (c.d != TD || c.group > 64) return 1;
+    if (c.d != TD || c.group > 32) return 1;  // a group must fit in one epilogue thread's 32 columns
     const int bk = c.side[0].bits, bv = c.n_sides > 1 ? c.side[1].bits : bk;
     if (bk == 4 && bv == 4) return launch_tc<4, 4>(c);
     if (bk == 8 && bv == 8) return launch_tc<8, 8>(c);

@@ -352,7 +352,15 @@ SRFT_HD float fdiv_rn(float a, float b) {
     return a / b;
 #endif
 }
-SRFT_HD float fabs_(float a) { return a < 0.f ? -a : a; }
+// |a|: on the device the hardware absolute value (an operand modifier, free);
+// the host form is for host-side builds of the same helpers
+SRFT_HD float fabs_(float a) {
+#if defined(__CUDA_ARCH__)
+    return fabsf(a);
+#else
+    return a < 0.f ? -a : a;
+#endif
+}
 SRFT_HD float fmax_(float a, float b) {
 #if defined(__CUDA_ARCH__)
     return fmaxf(a, b);
