@@ -40,11 +40,12 @@ constexpr int T_B_BYTES = TD * TD * 2;        // R_hi or R_lo
 constexpr int T_OFF_BLO = T_B_BYTES;
 constexpr int T_OFF_A = 2 * T_B_BYTES;
 constexpr int T_OFF_BAR = T_OFF_A + TSTAGES * T_A_BYTES;
-constexpr int T_SMEM = T_OFF_BAR + 128 + 1024;  // + barriers + alignment slack
+constexpr int T_SMEM = T_OFF_BAR + 256 + 1024;  // + barriers + alignment slack
 constexpr int T_EPI = 16;                     // epilogue warps of the quantize kernel
 constexpr int T_WARPS = 2 + T_EPI;
 constexpr uint32_t T_IDESC = tc::idesc_f16_f32(TM, TD);
-constexpr uint32_t T_TMEM_COLS = 256;         // two 128-column fp32 accumulators
+constexpr int T_NACC = 4;                     // fp32 accumulators of 128 columns in tensor memory
+constexpr uint32_t T_TMEM_COLS = 128 * T_NACC;
 }  // namespace
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
@@ -71,9 +72,11 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
     const uint32_t sbase = ptx::smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T_OFF_BAR);
-    // barrier indices: full[0..2], empty[3..5], acc_full[6..7], acc_empty[8..9]; tensor-memory slot after them
+    // barriers: x stage full / empty, accumulator full / empty; tensor-memory slot after them
     auto bar = [&](int i) { return ptx::smem_u32(&bars[i]); };
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[10]);
+    constexpr int X_FULL = 0, X_EMPTY = TSTAGES, ACC_FULL = 2 * TSTAGES, ACC_EMPTY = 2 * TSTAGES + T_NACC;
+    static_assert((2 * TSTAGES + 2 * T_NACC) * 8 + 4 <= 256, "barrier area");
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[2 * TSTAGES + 2 * T_NACC]);
 
     // ---- R_s = R diag(s), split into fp16 hi + lo, in the MMA operand layout ----
     {
@@ -102,12 +105,12 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < TSTAGES; ++s) {
-            ptx::mbar_init(bar(s), 1);
-            ptx::mbar_init(bar(3 + s), 1);
+            ptx::mbar_init(bar(X_FULL + s), 1);
+            ptx::mbar_init(bar(X_EMPTY + s), 1);
         }
-        for (int a = 0; a < 2; ++a) {
-            ptx::mbar_init(bar(6 + a), 1);
-            ptx::mbar_init(bar(8 + a), T_EPI);
+        for (int a = 0; a < T_NACC; ++a) {
+            ptx::mbar_init(bar(ACC_FULL + a), 1);
+            ptx::mbar_init(bar(ACC_EMPTY + a), T_EPI);
         }
         ptx::fence_barrier_init();
     }
@@ -126,24 +129,24 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
         if (lane == 0) {
             for (int t = blockIdx.x, i = 0; t < P.total_tiles; t += stride, ++i) {
                 const int s = i % TSTAGES, use = i / TSTAGES;
-                if (use > 0 && !ptx::mbar_wait_bounded(bar(3 + s), (use - 1) & 1)) {
+                if (use > 0 && !ptx::mbar_wait_bounded(bar(X_EMPTY + s), (use - 1) & 1)) {
                     failed = true;
                     break;
                 }
                 const TileId id = decode_tile128(P, t);
                 const CUtensorMap* tm = id.side ? &tm1 : &tm0;
                 const uint32_t dst = sbase + T_OFF_A + s * T_A_BYTES;
-                ptx::mbar_arrive_expect_tx(bar(s), T_A_BYTES);
-                ptx::tma_load_4d(dst, tm, bar(s), 0, id.h, id.t0, id.o);
-                ptx::tma_load_4d(dst + T_KB_BYTES, tm, bar(s), 64, id.h, id.t0, id.o);
+                ptx::mbar_arrive_expect_tx(bar(X_FULL + s), T_A_BYTES);
+                ptx::tma_load_4d(dst, tm, bar(X_FULL + s), 0, id.h, id.t0, id.o);
+                ptx::tma_load_4d(dst + T_KB_BYTES, tm, bar(X_FULL + s), 64, id.h, id.t0, id.o);
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
             for (int t = blockIdx.x, i = 0; t < P.total_tiles; t += stride, ++i) {
-                const int s = i % TSTAGES, a = i & 1;
-                if (!ptx::mbar_wait_bounded(bar(s), (i / TSTAGES) & 1) ||
-                    (i >= 2 && !ptx::mbar_wait_bounded(bar(8 + a), ((i >> 1) - 1) & 1))) {
+                const int s = i % TSTAGES, a = i % T_NACC;
+                if (!ptx::mbar_wait_bounded(bar(X_FULL + s), (i / TSTAGES) & 1) ||
+                    (i >= T_NACC && !ptx::mbar_wait_bounded(bar(ACC_EMPTY + a), (i / T_NACC - 1) & 1))) {
                     failed = true;
                     break;
                 }
@@ -157,16 +160,16 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
                     tc::mma_f16(d_tmem, ad, tc::sw128_desc(sbase + koff), T_IDESC, ks > 0);
                     tc::mma_f16(d_tmem, ad, tc::sw128_desc(sbase + T_OFF_BLO + koff), T_IDESC, 1);
                 }
-                tc::commit(bar(3 + s));  // the x stage can be refilled once these MMAs are done
-                tc::commit(bar(6 + a));  // accumulator a is ready for the epilogue
+                tc::commit(bar(X_EMPTY + s));  // the x stage can be refilled once these MMAs are done
+                tc::commit(bar(ACC_FULL + a));  // accumulator a is ready for the epilogue
             }
         }
     } else {
         // warp w reads tensor-memory lanes 32(w%4)..+31 (tile rows) and column quarter cq
         const int quarter = warp & 3, cq = (warp - 2) >> 2;
         for (int t = blockIdx.x, i = 0; t < P.total_tiles; t += stride, ++i) {
-            const int a = i & 1;
-            const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(bar(6 + a), (i >> 1) & 1));
+            const int a = i % T_NACC;
+            const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(bar(ACC_FULL + a), (i / T_NACC) & 1));
             if (!ok) {
                 failed = true;
                 break;
@@ -178,7 +181,7 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
             tc::wait_ld(r0);
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(8 + a));  // accumulator a may be overwritten
+            if (lane == 0) ptx::mbar_arrive(bar(ACC_EMPTY + a));  // accumulator a may be overwritten
 
             const TileId id = decode_tile128(P, t);
             const CodecSideK& S = P.side[id.side];
