@@ -49,6 +49,13 @@ notes; the CUDA path implements the same readings independently):
    complement.  int8 codes are stored as two's-complement bytes.
 7. Attention softmax scale defaults to 1/sqrt(d); a query whose sequence
    length is 0 gets an all-zero output.
+8. The Hadamard variant ([WQF] Methodology 1 names SRHT as the common
+   alternative and Key results, quality, finds it indistinguishable from
+   SRFT; the pages do not write it out): SRHT(x) = d^(-1/2) H diag(s) x with
+   H the Sylvester Hadamard matrix in natural order, H_ij = (-1)^popcount(i & j),
+   the same sign vector s as the SRFT, no subsampling and no packing (the
+   output is already real).  Everything downstream (lambda, groups,
+   rounding, packing, attention) is unchanged.
 """
 
 from __future__ import annotations
@@ -170,6 +177,59 @@ def srft_matrix(d: int, seed: int) -> np.ndarray:
 
 
 # --------------------------------------------------------------------------
+# Hadamard variant (reading 8)
+# --------------------------------------------------------------------------
+
+def hadamard_matrix(d: int) -> np.ndarray:
+    """Sylvester Hadamard matrix of order d (a power of two), natural order:
+    H_ij = (-1)^popcount(i & j)."""
+    _check_d(d)
+    i = np.arange(d)
+    parity = np.array([[bin(a & b).count("1") & 1 for b in i] for a in i])
+    return np.where(parity == 1, -1.0, 1.0)
+
+
+def srht_forward(x: np.ndarray, seed: int) -> np.ndarray:
+    """SRHT(x) = d^(-1/2) H diag(s) x over the last axis, in fp64."""
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    return (x * sign_vector(d, seed)) @ hadamard_matrix(d).T / math.sqrt(d)
+
+
+def srht_inverse(y: np.ndarray, seed: int) -> np.ndarray:
+    """x = diag(s) H^T y / sqrt(d), the exact inverse (H H^T = d I)."""
+    y = np.asarray(y, dtype=np.float64)
+    d = y.shape[-1]
+    return (y @ hadamard_matrix(d)) / math.sqrt(d) * sign_vector(d, seed)
+
+
+def srht_matrix(d: int, seed: int) -> np.ndarray:
+    """The SRHT as a d x d matrix, built from ``srht_forward`` of the basis."""
+    return srht_forward(np.eye(d), seed).T
+
+
+TRANSFORMS = ("srft", "srht")
+
+
+def rotate(x, seed: int, transform: str = "srft") -> np.ndarray:
+    """The forward transform named by ``transform``."""
+    if transform == "srft":
+        return srft_forward(x, seed)
+    if transform == "srht":
+        return srht_forward(x, seed)
+    raise ValueError(f"unknown transform {transform!r}")
+
+
+def unrotate(p, seed: int, transform: str = "srft") -> np.ndarray:
+    """The inverse transform named by ``transform``."""
+    if transform == "srft":
+        return srft_inverse(p, seed)
+    if transform == "srht":
+        return srht_inverse(p, seed)
+    raise ValueError(f"unknown transform {transform!r}")
+
+
+# --------------------------------------------------------------------------
 # Group quantiser ([WQF] Methodology 2 and 3; readings 4-6)
 # --------------------------------------------------------------------------
 
@@ -232,15 +292,16 @@ def unpack_codes(codes: np.ndarray, bits: int) -> np.ndarray:
 # Codec: quantise / dequantise a K or V tensor
 # --------------------------------------------------------------------------
 
-def srft_kv_quantize(x, lam, bits: int, group: int, seed: int) -> dict:
+def srft_kv_quantize(x, lam, bits: int, group: int, seed: int, transform: str = "srft") -> dict:
     """Encode head vectors x[..., d] (fp16 values, any leading shape).
 
     lam is None (all ones) or broadcastable to x.  Returns a dict with the
     packed ``codes`` (uint8), fp64 ``scales`` [..., d/group], the integer
     codes ``q``, the pre-round values ``r`` and the rotated, rescaled ``z``.
+    ``transform`` selects the SRFT (default) or the SRHT (reading 8).
     """
     x = np.asarray(x, dtype=np.float64)
-    p = srft_forward(x, seed)
+    p = rotate(x, seed, transform)
     z = p if lam is None else p * np.asarray(lam, dtype=np.float64)
     q, scale, r = quantize_groups(z, bits, group)
     return {"codes": pack_codes(q, bits), "scales": scale, "q": q, "r": r, "z": z}
@@ -254,9 +315,9 @@ def dequantize_rotated(codes, scales, lam, bits: int, group: int) -> np.ndarray:
     return zhat if lam is None else zhat / np.asarray(lam, dtype=np.float64)
 
 
-def srft_kv_dequantize(codes, scales, lam, bits: int, group: int, seed: int) -> np.ndarray:
-    """x_hat = SRFT^{-1}((q * scale) / lambda), in fp64."""
-    return srft_inverse(dequantize_rotated(codes, scales, lam, bits, group), seed)
+def srft_kv_dequantize(codes, scales, lam, bits: int, group: int, seed: int, transform: str = "srft") -> np.ndarray:
+    """x_hat = T^{-1}((q * scale) / lambda) with T the SRFT (or the SRHT), in fp64."""
+    return unrotate(dequantize_rotated(codes, scales, lam, bits, group), seed, transform)
 
 
 # --------------------------------------------------------------------------
@@ -297,15 +358,17 @@ def dequantize_cache(side: dict, seed: int) -> np.ndarray:
     """Unrotated fp64 cache [B, T, H, d] from one side of a cache description.
 
     side = {"bits": 4|8, "codes", "scales", "lam" (None or [B|1, H, d]),
-    "group"} for a packed side, or {"bits": 16, "values": [B, T, H, d]} for a
-    raw fp16 side (no rotation, no scales).
+    "group", optional "transform" ("srft" when absent)} for a packed side, or
+    {"bits": 16, "values": [B, T, H, d]} for a raw fp16 side (no rotation, no
+    scales).
     """
     if side["bits"] == 16:
         return np.asarray(side["values"], dtype=np.float64)
     lam = side.get("lam")
     if lam is not None:
         lam = np.asarray(lam, dtype=np.float64)[:, None, :, :]
-    return srft_kv_dequantize(side["codes"], side["scales"], lam, side["bits"], side["group"], seed)
+    return srft_kv_dequantize(side["codes"], side["scales"], lam, side["bits"], side["group"], seed,
+                              side.get("transform", "srft"))
 
 
 def packed_decode_attention(q, k_side: dict, v_side: dict, seed: int, seq_lens=None, sm_scale=None):

@@ -338,6 +338,77 @@ def test_kvsplit_k8v4_formula_and_compression_ratio():
     assert round(ratio, 2) == gl["compression"]["max_ratio"]
 
 
+# ---------------------------------------------------------------- Hadamard variant (SRHT)
+
+def check_hadamard_matches_scipy(o, d):
+    # scipy builds H by the Sylvester recursion, independently of the popcount form
+    scipy_linalg = pytest.importorskip("scipy.linalg")
+    assert np.array_equal(o.hadamard_matrix(d), scipy_linalg.hadamard(d).astype(np.float64))
+
+
+@pytest.mark.parametrize("d", DIMS)
+def test_hadamard_matches_scipy(d):
+    check_hadamard_matches_scipy(O, d)
+
+
+def test_hadamard_d4_by_hand_and_sylvester_recursion():
+    h4 = np.array([[1, 1, 1, 1], [1, -1, 1, -1], [1, 1, -1, -1], [1, -1, -1, 1]], dtype=np.float64)
+    assert np.array_equal(O.hadamard_matrix(4), h4)
+    for d in (4, 8, 16, 32):
+        h = O.hadamard_matrix(d)
+        assert np.array_equal(O.hadamard_matrix(2 * d), np.block([[h, h], [h, -h]]))
+
+
+@pytest.mark.parametrize("d", DIMS)
+def test_srht_orthogonal_and_round_trip(d):
+    R = O.srht_matrix(d, 7)
+    assert np.abs(R.T @ R - np.eye(d)).max() < 1e-12
+    rng = np.random.default_rng(d)
+    x = rng.standard_normal((5, d))
+    assert np.abs(O.srht_inverse(O.srht_forward(x, 7), 7) - x).max() < 1e-12
+    assert np.abs(np.linalg.norm(O.srht_forward(x, 7), axis=-1) - np.linalg.norm(x, axis=-1)).max() < 1e-12
+
+
+def _fwht(u):
+    """Fast Walsh-Hadamard transform by in-place butterflies (O(d log d)), written here from the
+    definition of the Sylvester recursion; independent of the oracle's matrix."""
+    u = np.array(u, dtype=np.float64)
+    h = 1
+    while h < u.shape[-1]:
+        for i in range(0, u.shape[-1], 2 * h):
+            a = u[..., i:i + h].copy()
+            b = u[..., i + h:i + 2 * h].copy()
+            u[..., i:i + h], u[..., i + h:i + 2 * h] = a + b, a - b
+        h *= 2
+    return u
+
+
+@pytest.mark.parametrize("d", DIMS)
+def test_srht_equals_signed_fast_wht(d):
+    rng = np.random.default_rng(100 + d)
+    x = rng.standard_normal((3, d))
+    s = O.sign_vector(d, 11)
+    assert np.abs(O.srht_forward(x, 11) - _fwht(x * s) / math.sqrt(d)).max() < 1e-12
+
+
+def test_srht_quantiser_and_attention_identity():
+    rng = np.random.default_rng(5)
+    d, g = 16, 8
+    x = rng.standard_normal((4, d)).astype(np.float16).astype(np.float64)
+    enc = O.srft_kv_quantize(x, None, 4, g, 9, transform="srht")
+    assert np.abs(enc["z"] - _fwht(x * O.sign_vector(d, 9)) / math.sqrt(d)).max() < 1e-12
+    # brute force: every code is the nearest of the 2Q+1 levels of its group's scale
+    sc = np.repeat(enc["scales"], g, axis=-1)
+    levels = np.arange(-7, 8)
+    best = levels[np.argmin(np.abs(enc["z"][..., None] - levels * sc[..., None]), axis=-1)]
+    assert np.array_equal(enc["q"], best)
+    # the dequantised cache is the SRHT inverse of q * scale, and q . k_hat is preserved by the rotation
+    xhat = O.srft_kv_dequantize(enc["codes"], enc["scales"], None, 4, g, 9, transform="srht")
+    assert np.abs(_fwht(xhat * O.sign_vector(d, 9)) / math.sqrt(d) - enc["q"] * sc).max() < 1e-12
+    q = rng.standard_normal(d)
+    assert np.abs(xhat @ q - (enc["q"] * sc) @ O.srht_forward(q, 9)).max() < 1e-12
+
+
 # ---------------------------------------------------------------- mutation tests
 
 class _Mutant:
@@ -423,3 +494,13 @@ def test_mutant_wrong_splitmix_constant_is_caught():
 
     with pytest.raises(AssertionError):
         check_splitmix_vectors(_Mutant(splitmix64_stream=bad_stream))
+
+
+def test_mutant_hadamard_wrong_index_rule_is_caught():
+    def bad_hadamard(d):
+        i = np.arange(d)
+        parity = np.array([[bin(a | b).count("1") & 1 for b in i] for a in i])
+        return np.where(parity == 1, -1.0, 1.0)
+
+    with pytest.raises(AssertionError):
+        check_hadamard_matches_scipy(_Mutant(hadamard_matrix=bad_hadamard), 8)
