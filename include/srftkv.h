@@ -68,6 +68,14 @@ extern "C" {
 #define SRFTKV_ERR_CUDA (-2)    /* a CUDA call or launch failed */
 #define SRFTKV_ERR_DEVICE (-3)  /* current device is not sm_103 */
 
+/* The rotation applied before quantisation (per side, field `transform`). */
+#define SRFTKV_TRANSFORM_SRFT 0 /* SRFT(x) = pack(F diag(s) x), F the unitary DFT ([WQF] Methodology 1) */
+#define SRFTKV_TRANSFORM_SRHT 1 /* SRHT(x) = d^(-1/2) H diag(s) x, H the Sylvester Hadamard matrix in
+                                   natural order (H_ij = (-1)^popcount(i & j)); the alternative the same
+                                   section names, same sign vector s, no packing needed */
+/* The scale plane's number format (per side, field `scale_format`). */
+#define SRFTKV_SCALE_FP32 0     /* fp32 scales, d/group per row */
+
 /*
  * One side (K or V) of a packed cache, stored as two head-major planes ([AQT]):
  *   codes  : uint8 [n_outer][H][t_cap][d*bits/8]  (row start 16-byte aligned
@@ -91,6 +99,8 @@ typedef struct srftkv_side {
     int bits;                    /* 4 or 8 (16 = raw fp16 cache, attention only) */
     void* codes;                 /* code plane (see above) */
     float* scales;               /* scale plane (see above) */
+    int transform;               /* SRFTKV_TRANSFORM_SRFT (0) or SRFTKV_TRANSFORM_SRHT (1); ignored for bits 16 */
+    int scale_format;            /* SRFTKV_SCALE_FP32 (0); other values return SRFTKV_ERR_INVALID */
 } srftkv_side;
 
 /*
@@ -98,7 +108,8 @@ typedef struct srftkv_side {
  * ([WQF] Methodology 1-3; K8V4 via bits per side [KVS]; appending one token
  * per step is n_tokens = 1 at t_offset = current length [TQ]).
  * For each side that is not NULL and every (o, t, h) with t < n_tokens:
- *   p = SRFT(x[o][t][h]); z = lambda[o][h] * p; per group j of `group`
+ *   p = T(x[o][t][h]) with T the side's transform (SRFT, or SRHT);
+ *   z = lambda[o][h] * p; per group j of `group`
  *   coordinates: scales[o][h][t_offset+t][j] = max|z| / Q and
  *   codes[o][h][t_offset+t] = packed rint(z / scale).
  * Both sides are encoded by one kernel launch.  Requires
@@ -113,6 +124,7 @@ int srft_kv_quantize(const srftkv_side* k, const srftkv_side* v, int n_outer, in
  * srft_kv_dequantize -- decode tokens [t_offset, t_offset+n_tokens) of the
  * packed cache back to fp16 ([WQF] Methodology 2, run backwards):
  *   x_hat = diag(s) . F^{-1} . unpack((codes * scale) / lambda)
+ * (SRHT sides: x_hat = diag(s) . H . ((codes * scale) / lambda) / sqrt(d))
  * written to side->x as [n_outer][n_tokens][H][d].  Same size rules as
  * srft_kv_quantize.
  */
@@ -195,6 +207,14 @@ int srft_kv_vector_bytes(int d, int bits, int group, size_t* code_bytes, size_t*
  * inverse != 0: y = SRFT^{-1}(x) = diag(s) . F^{-1} . unpack(x).
  */
 int srft_transform(const void* x, float* y, int n, int d, uint64_t sign_seed, int inverse,
+                   void* stream);
+
+/*
+ * srht_transform -- the Hadamard variant of srft_transform, same arguments:
+ * inverse == 0: y = SRHT(x) = d^(-1/2) H diag(s) x;
+ * inverse != 0: y = diag(s) H x / sqrt(d).
+ */
+int srht_transform(const void* x, float* y, int n, int d, uint64_t sign_seed, int inverse,
                    void* stream);
 
 /* Message for the last non-zero return on this host thread ("" if none). */

@@ -40,7 +40,12 @@ class _Side(ctypes.Structure):
         ("bits", ctypes.c_int),
         ("codes", ctypes.c_void_p),
         ("scales", ctypes.c_void_p),
+        ("transform", ctypes.c_int),
+        ("scale_format", ctypes.c_int),
     ]
+
+
+TRANSFORMS = {"srft": 0, "srht": 1}  # SRFTKV_TRANSFORM_SRFT / _SRHT in include/srftkv.h
 
 
 _lib = None
@@ -64,11 +69,12 @@ def library() -> ctypes.CDLL:
     lib.q4kv_decode_attention_workspace_size.restype = sz
     lib.srft_kv_vector_bytes.argtypes = [i, i, i, ctypes.POINTER(sz), ctypes.POINTER(sz)]
     lib.srft_transform.argtypes = [vp, vp, i, i, u64, i, vp]
+    lib.srht_transform.argtypes = [vp, vp, i, i, u64, i, vp]
     lib.srftkv_last_error.restype = ctypes.c_char_p
     lib.srftkv_device_fault.argtypes = [ctypes.POINTER(ctypes.c_uint)]
     for name in ("srft_kv_quantize", "srft_kv_dequantize", "q4kv_decode_attention", "q4kv_decode_attention_static",
                  "srft_kv_vector_bytes",
-                 "srft_transform", "srftkv_device_fault"):
+                 "srft_transform", "srht_transform", "srftkv_device_fault"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -100,21 +106,25 @@ class Side:
     x: torch.Tensor | None = None  # fp16 [n_outer][n_tokens][H][d]
     lam: torch.Tensor | None = None  # fp32 [n_lam][H][d]; n_lam == 1 broadcasts
     lam_outer_stride: int | None = None
+    transform: str = "srft"        # "srft" or "srht"
+    scale_format: int = 0          # SRFTKV_SCALE_FP32
 
     def to_c(self) -> _Side:
         stride = self.lam_outer_stride
         if stride is None:
             stride = 0 if self.lam is None or self.lam.shape[0] == 1 else self.lam.shape[1] * self.lam.shape[2]
-        return _Side(_ptr(self.x), _ptr(self.lam), stride, self.bits, _ptr(self.codes), _ptr(self.scales))
+        return _Side(_ptr(self.x), _ptr(self.lam), stride, self.bits, _ptr(self.codes), _ptr(self.scales),
+                     TRANSFORMS[self.transform], self.scale_format)
 
 
-def alloc_side(n_outer: int, t_cap: int, H: int, d: int, bits: int, group: int, device="cuda") -> Side:
+def alloc_side(n_outer: int, t_cap: int, H: int, d: int, bits: int, group: int, device="cuda",
+               transform: str = "srft") -> Side:
     """Allocate empty (head-major) code and scale planes for one side."""
     if bits == 16:
         return Side(torch.empty((n_outer, H, t_cap, d), dtype=torch.float16, device=device), None, 16)
     codes = torch.empty((n_outer, H, t_cap, d * bits // 8), dtype=torch.uint8, device=device)
     scales = torch.empty((n_outer, H, t_cap, d // group), dtype=torch.float32, device=device)
-    return Side(codes, scales, bits)
+    return Side(codes, scales, bits, transform=transform)
 
 
 def _sidep(s: Side | None):
@@ -173,6 +183,12 @@ def srft_transform(x: torch.Tensor, y: torch.Tensor, n: int, d: int, sign_seed: 
                    stream=None) -> None:
     rc = library().srft_transform(_ptr(x), _ptr(y), n, d, sign_seed, int(bool(inverse)), _stream(stream))
     _check("srft_transform", rc)
+
+
+def srht_transform(x: torch.Tensor, y: torch.Tensor, n: int, d: int, sign_seed: int, inverse: bool,
+                   stream=None) -> None:
+    rc = library().srht_transform(_ptr(x), _ptr(y), n, d, sign_seed, int(bool(inverse)), _stream(stream))
+    _check("srht_transform", rc)
 
 
 def srftkv_device_fault() -> int:

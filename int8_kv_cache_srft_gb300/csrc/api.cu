@@ -199,6 +199,10 @@ static int check_codec_sizes(int n_outer, int n_tokens, int H, int d, int group,
 
 static int check_side(const srftkv_side* s, const char* name, int d, int group, bool need_x) {
     if (s->bits != 4 && s->bits != 8) return invalid("%s: bits must be 4 or 8 (got %d)", name, s->bits);
+    if (s->transform != SRFTKV_TRANSFORM_SRFT && s->transform != SRFTKV_TRANSFORM_SRHT)
+        return invalid("%s: transform must be SRFTKV_TRANSFORM_SRFT or SRFTKV_TRANSFORM_SRHT (got %d)", name, s->transform);
+    if (s->scale_format != SRFTKV_SCALE_FP32)
+        return invalid("%s: scale_format %d is not supported", name, s->scale_format);
     if (!s->codes || !s->scales) return invalid("%s: codes and scales must not be NULL", name);
     if (need_x && !s->x) return invalid("%s: x must not be NULL", name);
     const size_t crow = (size_t)d * s->bits / 8, srow = (size_t)(d / group) * 4;
@@ -231,6 +235,7 @@ static int codec_common(const srftkv_side* k, const srftkv_side* v, int n_outer,
         s.lambda = sides[i]->lambda;
         s.lambda_outer_stride = sides[i]->lambda_outer_stride;
         s.bits = sides[i]->bits;
+        s.transform = sides[i]->transform;
     }
     if (n_outer == 0 || n_tokens == 0) return SRFTKV_OK;
     rc = current_device_ok();
@@ -280,7 +285,18 @@ int srft_transform(const void* x, float* y, int n, int d, uint64_t sign_seed, in
     if (!aligned(x, 16) || !aligned(y, 16)) return invalid("x and y must be 16-byte aligned");
     const int rc = current_device_ok();
     if (rc) return rc;
-    return transform_launch(x, y, n, d, sign_seed, inverse != 0, static_cast<cudaStream_t>(stream));
+    return transform_launch(x, y, n, d, sign_seed, inverse != 0, false, static_cast<cudaStream_t>(stream));
+}
+
+int srht_transform(const void* x, float* y, int n, int d, uint64_t sign_seed, int inverse, void* stream) {
+    if (d != 16 && d != 32 && d != 64 && d != 128 && d != 256) return invalid("d must be one of 16, 32, 64, 128, 256");
+    if (n < 0) return invalid("n must be >= 0");
+    if (n == 0) return SRFTKV_OK;
+    if (!x || !y) return invalid("x and y must not be NULL");
+    if (!aligned(x, 16) || !aligned(y, 16)) return invalid("x and y must be 16-byte aligned");
+    const int rc = current_device_ok();
+    if (rc) return rc;
+    return transform_launch(x, y, n, d, sign_seed, inverse != 0, true, static_cast<cudaStream_t>(stream));
 }
 
 int q4kv_decode_attention(const void* q, float* out, const srftkv_side* k, const srftkv_side* v, int B, int Hq, int Hkv,

@@ -62,7 +62,8 @@ struct AttnParams {
     const float* lam_v;
     long long lam_v_stride;
     int B, Hq, Hkv, rep, t_cap, n_splits, group, log2_group;
-    int sp;                // padded scale row (floats) in shared memory
+    int sp;                // scale row (floats)
+    int tr_k, tr_v;        // transform of the K and V sides (SRFTKV_TRANSFORM_*)
     float qscale;          // sm_scale * log2(e)
     uint32_t sign_mask[128];
 };
@@ -201,8 +202,17 @@ __global__ void __launch_bounds__(128) attn_prep_q_kernel(const __grid_constant_
                 zi[4 * c + e] = __half2float(__ushort_as_half((unsigned short)(s >> 16)));
             }
         }
-        fft<N, false>(zr, zi);
-        split_forward<D>(zr, zi, p);
+        if (P.tr_k == SRFTKV_TRANSFORM_SRHT) {
+            wht_pairs<N>(zr, zi);
+#pragma unroll
+            for (int n = 0; n < N; ++n) {
+                p[2 * n] = zr[n] * SplitConst<D>::inv_sqrt_d;
+                p[2 * n + 1] = zi[n] * SplitConst<D>::inv_sqrt_d;
+            }
+        } else {
+            fft<N, false>(zr, zi);
+            split_forward<D>(zr, zi, p);
+        }
     } else {
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) {
@@ -858,8 +868,17 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const __grid_constant
         float p[D], zr[N], zi[N];
 #pragma unroll
         for (int i = 0; i < D; ++i) p[i] = rows[warp][i];
-        split_inverse<D>(p, zr, zi);
-        fft<N, true>(zr, zi);
+        if (P.tr_v == SRFTKV_TRANSFORM_SRHT) {
+#pragma unroll
+            for (int n = 0; n < N; ++n) {
+                zr[n] = p[2 * n] * SplitConst<D>::inv_sqrt_d;
+                zi[n] = p[2 * n + 1] * SplitConst<D>::inv_sqrt_d;
+            }
+            wht_pairs<N>(zr, zi);
+        } else {
+            split_inverse<D>(p, zr, zi);
+            fft<N, true>(zr, zi);
+        }
         float4* yr = reinterpret_cast<float4*>(P.out + (long long)row * D);
 #pragma unroll
         for (int c4 = 0; c4 < D / 4; ++c4) {
@@ -1022,6 +1041,12 @@ int attention_entry(const void* q, float* out, const srftkv_side* k, const srftk
         if (group < 16 || (group & (group - 1)) || group > d / 4)
             return invalid_attn("attention: group must be a power of two with 16 <= group <= d/4");
         if (!k->scales || !v->scales) return invalid_attn("attention: scales must not be NULL");
+        const srftkv_side* sv2[2] = {k, v};
+        for (auto sd : sv2) {
+            if (sd->transform != SRFTKV_TRANSFORM_SRFT && sd->transform != SRFTKV_TRANSFORM_SRHT)
+                return invalid_attn("attention: transform must be SRFTKV_TRANSFORM_SRFT or SRFTKV_TRANSFORM_SRHT");
+            if (sd->scale_format != SRFTKV_SCALE_FP32) return invalid_attn("attention: scale_format not supported");
+        }
         if ((reinterpret_cast<uintptr_t>(k->scales) | reinterpret_cast<uintptr_t>(v->scales)) & 15)
             return invalid_attn("attention: scales must be 16-byte aligned");
         const srftkv_side* sd[2] = {k, v};
@@ -1069,6 +1094,8 @@ int attention_entry(const void* q, float* out, const srftkv_side* k, const srftk
     P.log2_group = 0;
     while ((1 << P.log2_group) < P.group) ++P.log2_group;
     P.sp = raw ? 0 : d / P.group;
+    P.tr_k = raw ? 0 : k->transform;
+    P.tr_v = raw ? 0 : v->transform;
     const float sc = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt((float)d);
     P.qscale = sc * 1.4426950408889634f;
     sign_masks(d, seed, P.sign_mask);

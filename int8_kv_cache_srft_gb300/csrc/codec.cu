@@ -43,13 +43,40 @@ struct SignParams {
 
 template <int D, bool INV>
 __global__ void __launch_bounds__(128) srft_transform_kernel(const uint16_t* __restrict__ x, float* __restrict__ y, int n,
-                                                             const __grid_constant__ SignParams S) {
+                                                             const __grid_constant__ SignParams S, int srht) {
     constexpr int N = D / 2;
+    constexpr float isd = SplitConst<D>::inv_sqrt_d;
     const int r = blockIdx.x * blockDim.x + threadIdx.x;
     if (r >= n) return;
     const uint4* xr = reinterpret_cast<const uint4*>(x + (long long)r * D);
     float4* yr = reinterpret_cast<float4*>(y + (long long)r * D);
     float zr[N], zi[N];
+    if (srht) {  // y = d^-1/2 H diag(s) x, or its inverse diag(s) H x / sqrt(d)
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+            const uint4 v = __ldg(xr + c);
+            const uint32_t m0 = INV ? 0u : S.w[4 * c + 0], m1 = INV ? 0u : S.w[4 * c + 1];
+            const uint32_t m2 = INV ? 0u : S.w[4 * c + 2], m3 = INV ? 0u : S.w[4 * c + 3];
+            signed_pair_t(v.x, m0, zr[4 * c + 0], zi[4 * c + 0]);
+            signed_pair_t(v.y, m1, zr[4 * c + 1], zi[4 * c + 1]);
+            signed_pair_t(v.z, m2, zr[4 * c + 2], zi[4 * c + 2]);
+            signed_pair_t(v.w, m3, zr[4 * c + 3], zi[4 * c + 3]);
+        }
+        wht_pairs<N>(zr, zi);
+#pragma unroll
+        for (int c = 0; c < D / 4; ++c) {
+            const int n0 = 2 * c, n1 = 2 * c + 1;
+            float a = zr[n0] * isd, b = zi[n0] * isd, cc = zr[n1] * isd, dd = zi[n1] * isd;
+            if (INV) {
+                a = u2f(f2u(a) ^ ((S.w[n0] & 0x8000u) << 16));
+                b = u2f(f2u(b) ^ (S.w[n0] & 0x80000000u));
+                cc = u2f(f2u(cc) ^ ((S.w[n1] & 0x8000u) << 16));
+                dd = u2f(f2u(dd) ^ (S.w[n1] & 0x80000000u));
+            }
+            yr[c] = make_float4(a, b, cc, dd);
+        }
+        return;
+    }
     if constexpr (!INV) {
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) {
@@ -112,7 +139,22 @@ static int quant_path_override() {
     return (e && !strcmp(e, "fft")) ? 1 : (e && !strcmp(e, "tc")) ? 2 : 0;
 }
 
+// A call whose two sides use different transforms runs as two one-sided
+// calls (the tensor-core kernels hold one transform matrix per CTA).
+static bool split_mixed(const CodecCall& c, int (*fn)(const CodecCall&), int& rc) {
+    if (c.n_sides != 2 || c.side[0].transform == c.side[1].transform) return false;
+    CodecCall one = c;
+    one.n_sides = 1;
+    rc = fn(one);
+    if (rc) return true;
+    one.side[0] = c.side[1];
+    rc = fn(one);
+    return true;
+}
+
 int codec_quantize(const CodecCall& c) {
+    int split_rc = 0;
+    if (split_mixed(c, codec_quantize, split_rc)) return split_rc;
     const int ov = quant_path_override();
     const long long rows = (long long)c.n_sides * c.n_outer * c.n_tokens * c.H;
     if (ov == 2 || (ov == 0 && rows >= 64ll * 1024)) {
@@ -122,6 +164,8 @@ int codec_quantize(const CodecCall& c) {
     return dispatch_codec(c, true);
 }
 int codec_dequantize(const CodecCall& c) {
+    int split_rc = 0;
+    if (split_mixed(c, codec_dequantize, split_rc)) return split_rc;
     const int ov = quant_path_override();
     const long long rows = (long long)c.n_sides * c.n_outer * c.n_tokens * c.H;
     if (ov == 2 || (ov == 0 && rows >= 64ll * 1024)) {
@@ -132,15 +176,15 @@ int codec_dequantize(const CodecCall& c) {
 }
 
 template <int D>
-static int launch_transform(const void* x, float* y, int n, uint64_t seed, bool inverse, cudaStream_t s) {
+static int launch_transform(const void* x, float* y, int n, uint64_t seed, bool inverse, bool srht, cudaStream_t s) {
     SignParams S;
     for (int i = 0; i < 128; ++i) S.w[i] = 0;
     sign_masks(D, seed, S.w);
     const int blocks = (n + 127) / 128;
     if (inverse)
-        srft_transform_kernel<D, true><<<blocks, 128, 0, s>>>(static_cast<const uint16_t*>(x), y, n, S);
+        srft_transform_kernel<D, true><<<blocks, 128, 0, s>>>(static_cast<const uint16_t*>(x), y, n, S, srht ? 1 : 0);
     else
-        srft_transform_kernel<D, false><<<blocks, 128, 0, s>>>(static_cast<const uint16_t*>(x), y, n, S);
+        srft_transform_kernel<D, false><<<blocks, 128, 0, s>>>(static_cast<const uint16_t*>(x), y, n, S, srht ? 1 : 0);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("transform kernel launch failed: %s", cudaGetErrorString(e));
@@ -149,14 +193,14 @@ static int launch_transform(const void* x, float* y, int n, uint64_t seed, bool 
     return 0;
 }
 
-int transform_launch(const void* x, float* y, int n, int d, uint64_t seed, bool inverse, cudaStream_t s) {
+int transform_launch(const void* x, float* y, int n, int d, uint64_t seed, bool inverse, bool srht, cudaStream_t s) {
     if (n == 0) return 0;
     switch (d) {
-        case 16: return launch_transform<16>(x, y, n, seed, inverse, s);
-        case 32: return launch_transform<32>(x, y, n, seed, inverse, s);
-        case 64: return launch_transform<64>(x, y, n, seed, inverse, s);
-        case 128: return launch_transform<128>(x, y, n, seed, inverse, s);
-        case 256: return launch_transform<256>(x, y, n, seed, inverse, s);
+        case 16: return launch_transform<16>(x, y, n, seed, inverse, srht, s);
+        case 32: return launch_transform<32>(x, y, n, seed, inverse, srht, s);
+        case 64: return launch_transform<64>(x, y, n, seed, inverse, srht, s);
+        case 128: return launch_transform<128>(x, y, n, seed, inverse, srht, s);
+        case 256: return launch_transform<256>(x, y, n, seed, inverse, srht, s);
         default: set_error("unsupported d = %d", d); return -1;
     }
 }

@@ -33,7 +33,7 @@ struct CodecSideK {
     const float* lambda;
     long long lambda_outer_stride;
     int bits;
-    int pad_;
+    int transform;  // SRFTKV_TRANSFORM_SRFT or SRFTKV_TRANSFORM_SRHT
 };
 
 struct CodecParams {
@@ -213,9 +213,18 @@ __device__ __forceinline__ void quantize_tile(const CodecParams& P, const TileId
         signed_pair(v.z, P.sign_mask[4 * c + 2], zr[4 * c + 2], zi[4 * c + 2]);
         signed_pair(v.w, P.sign_mask[4 * c + 3], zr[4 * c + 3], zi[4 * c + 3]);
     }
-    fft<N, false>(zr, zi);
     float z[D];
-    split_forward<D>(zr, zi, z);
+    if (S.transform == SRFTKV_TRANSFORM_SRHT) {  // d^-1/2 H (signed x): no packing, the output is real
+        wht_pairs<N>(zr, zi);
+#pragma unroll
+        for (int n = 0; n < N; ++n) {
+            z[2 * n] = zr[n] * SplitConst<D>::inv_sqrt_d;
+            z[2 * n + 1] = zi[n] * SplitConst<D>::inv_sqrt_d;
+        }
+    } else {
+        fft<N, false>(zr, zi);
+        split_forward<D>(zr, zi, z);
+    }
     if (t >= P.n_tokens) return;
     if (S.lambda != nullptr) {
         const float4* lr =
@@ -328,8 +337,17 @@ __global__ void __launch_bounds__(128, Geo<D>::MIN_BLOCKS)
             for (int i = 0; i < D; ++i) p[i] = 0.f;
         }
         float zr[N], zi[N];
-        split_inverse<D>(p, zr, zi);
-        fft<N, true>(zr, zi);
+        if (S.transform == SRFTKV_TRANSFORM_SRHT) {  // H p / sqrt(d), signs applied on output
+#pragma unroll
+            for (int n = 0; n < N; ++n) {
+                zr[n] = p[2 * n] * SplitConst<D>::inv_sqrt_d;
+                zi[n] = p[2 * n + 1] * SplitConst<D>::inv_sqrt_d;
+            }
+            wht_pairs<N>(zr, zi);
+        } else {
+            split_inverse<D>(p, zr, zi);
+            fft<N, true>(zr, zi);
+        }
         const int b = it & 1;
         uint16_t* buf = reinterpret_cast<uint16_t*>(bufs + b * Gm::BUF_BYTES);
         // the store issued from this buffer two tiles ago must have read it
@@ -369,7 +387,7 @@ static inline void fill_params(const CodecCall& c, CodecParams& P) {
         P.side[s].lambda = d.lambda;
         P.side[s].lambda_outer_stride = d.lambda_outer_stride;
         P.side[s].bits = d.bits;
-        P.side[s].pad_ = 0;
+        P.side[s].transform = d.transform;
     }
     P.n_outer = c.n_outer;
     P.H = c.H;

@@ -79,13 +79,17 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[2 * TSTAGES + 2 * T_NACC]);
 
     // ---- R_s = R diag(s), split into fp16 hi + lo, in the MMA operand layout ----
+    // (both sides of a launch share the transform; mixed calls are split on the host)
     {
         constexpr float inv_sqrt_d = 0.08838834764831845f;  // 1/sqrt(128)
         constexpr float c2 = 0.125f;                        // sqrt(2/128)
+        const bool srht = P.side[0].transform == SRFTKV_TRANSFORM_SRHT;
         for (int idx = threadIdx.x; idx < TD * TD; idx += blockDim.x) {
             const int n = idx >> 7, k = idx & 127;
             float v;
-            if (n == 0) {
+            if (srht) {
+                v = (__popc(n & k) & 1) ? -inv_sqrt_d : inv_sqrt_d;  // Hadamard entry / sqrt(d)
+            } else if (n == 0) {
                 v = inv_sqrt_d;
             } else if (n == 1) {
                 v = (k & 1) ? -inv_sqrt_d : inv_sqrt_d;
@@ -421,11 +425,14 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
     {  // B[k][n] = s_k R[n][k], hi and lo
         constexpr float inv_sqrt_d = 0.08838834764831845f;
         constexpr float c2 = 0.125f;
+        const bool srht = P.side[0].transform == SRFTKV_TRANSFORM_SRHT;
         for (int idx = threadIdx.x; idx < TD * TD; idx += blockDim.x) {
             // B row k (output coordinate), K position q holding packed coordinate n
             const int k = idx >> 7, q = idx & 127, n = dq_kperm(q);
             float v;
-            if (n == 0) {
+            if (srht) {
+                v = (__popc(n & k) & 1) ? -inv_sqrt_d : inv_sqrt_d;
+            } else if (n == 0) {
                 v = inv_sqrt_d;
             } else if (n == 1) {
                 v = (k & 1) ? -inv_sqrt_d : inv_sqrt_d;

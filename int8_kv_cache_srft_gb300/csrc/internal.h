@@ -20,6 +20,7 @@ struct CodecSideDesc {
     const float* lambda;  // [*][H][d] or null
     int64_t lambda_outer_stride;
     int bits;
+    int transform;        // SRFTKV_TRANSFORM_SRFT or SRFTKV_TRANSFORM_SRHT
 };
 
 struct CodecCall {
@@ -43,7 +44,7 @@ bool encode_x_map(CUtensorMap* map, void* base, int d, int H, int n_tokens, int 
 
 int codec_quantize(const CodecCall& c);
 int codec_dequantize(const CodecCall& c);
-int transform_launch(const void* x, float* y, int n, int d, uint64_t seed, bool inverse, cudaStream_t s);
+int transform_launch(const void* x, float* y, int n, int d, uint64_t seed, bool inverse, bool srht, cudaStream_t s);
 unsigned int codec_take_fault();
 unsigned int* codec_fault_word();  // device address of the codec fault word (current device)
 

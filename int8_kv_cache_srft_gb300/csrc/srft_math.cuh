@@ -257,6 +257,37 @@ SRFT_HD void split_pair_fwd(float zkr, float zki, float zmr, float zmi, float a1
     pm1 = fmaf_(-h, s2, ti);
 }
 
+// Walsh-Hadamard transform, unnormalised, Sylvester natural order
+// (H_ij = (-1)^popcount(i & j)): in-place butterflies over strides 1..N/2.
+template <int N>
+SRFT_HD void wht(float (&a)[N]) {
+#pragma unroll
+    for (int h = 1; h < N; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            if (i & h) continue;
+            const float x = a[i], y = a[i + h];
+            a[i] = x + y;
+            a[i + h] = x - y;
+        }
+    }
+}
+// The same transform of the length-2N vector u with u_{2n} = re[n],
+// u_{2n+1} = im[n].  H_{2N} = H_N (x) H_2 with the H_2 factor on the low
+// index bit: one butterfly per pair, then a length-N transform of each half.
+// Its own inverse up to the factor 2N.
+template <int N>
+SRFT_HD void wht_pairs(float (&re)[N], float (&im)[N]) {
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+        const float x = re[n], y = im[n];
+        re[n] = x + y;
+        im[n] = x - y;
+    }
+    wht<N>(re);
+    wht<N>(im);
+}
+
 // Inverse of split_pair_fwd, including the 1/N of the inverse transform:
 // from packed (p_{2k}, p_{2k+1}), (p_{2m}, p_{2m+1}) to Z'_k, Z'_m such that
 // the unnormalised inverse N-point transform of Z' gives z_n = u_{2n} + i u_{2n+1}.

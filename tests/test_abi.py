@@ -117,3 +117,19 @@ def test_workspace_size_is_monotone_in_splits(lib):
     assert 0 < s1 < s8
     assert s8 >= 16 * 32 * (128 + 8 * 130) * 4
     assert f(16, 30, 8, 128, 1024, 1) == 0  # Hq not a multiple of Hkv
+
+
+def test_sides_reject_unknown_transform_and_scale_format(lib):
+    bad_t = _side()
+    bad_t.transform = 2
+    assert _q(lib, bad_t, None) == K.SRFTKV_ERR_INVALID
+    bad_f = _side()
+    bad_f.scale_format = 7
+    assert _q(lib, None, bad_f) == K.SRFTKV_ERR_INVALID
+    assert b"scale_format" in lib.srftkv_last_error()
+
+
+def test_srht_transform_rejects_bad_arguments(lib):
+    assert lib.srht_transform(16, 16, 4, 48, 1, 0, None) == K.SRFTKV_ERR_INVALID
+    assert lib.srht_transform(None, 16, 4, 64, 1, 0, None) == K.SRFTKV_ERR_INVALID
+    assert lib.srht_transform(16, 16, 0, 64, 1, 0, None) == K.SRFTKV_OK
