@@ -409,6 +409,81 @@ def test_srht_quantiser_and_attention_identity():
     assert np.abs(xhat @ q - (enc["q"] * sc) @ O.srht_forward(q, 9)).max() < 1e-12
 
 
+# ---------------------------------------------------------------- lighter scale planes (fp16, e8m0)
+
+def _all_fp16_values():
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    v = bits.view(np.float16).astype(np.float64)
+    ok = np.isfinite(v)
+    return v[ok], bits[ok]
+
+
+def check_fp16_scale_rounding(o):
+    """Brute force over every finite fp16: the stored scale is the nearest one to A/Q (ties to the even bit
+    pattern), saturating at 65504."""
+    vals, bits = _all_fp16_values()
+    rng = np.random.default_rng(3)
+    targets = np.concatenate([rng.lognormal(0.0, 4.0, 300), vals[(vals > 0) & (vals < 70000)][::997] *
+                              (1 + 2.0**-12), [1e6, 65504.0, 65519.0, 6e-8, 1e-9]])
+    got = o.fp16_round(targets)
+    for t, g in zip(targets, got):
+        dist = np.abs(vals - t)
+        near = np.flatnonzero(dist == dist.min())
+        if len(near) > 1:  # a tie: the even bit pattern wins
+            near = near[(bits[near] & 1) == 0]
+        want = min(vals[near[0]], 65504.0)
+        assert g == want, (t, g, want)
+
+
+def test_fp16_scale_is_nearest_fp16():
+    check_fp16_scale_rounding(O)
+
+
+def check_e8m0_scale(o):
+    rng = np.random.default_rng(4)
+    a = np.concatenate([rng.lognormal(0.0, 6.0, 500), np.ldexp(1.0, np.arange(-20, 21)).astype(np.float64)])
+    v, raw = o.store_scales(a, "e8m0")
+    assert np.all(v >= a) and np.all(v / 2 < a)  # the smallest power of two not below A/Q
+    assert np.array_equal(np.log2(v), raw.astype(np.int64) - 127)
+    assert np.array_equal(o.decode_scales(raw, "e8m0"), v)
+    p2 = np.ldexp(1.0, np.arange(-20, 21))
+    assert np.array_equal(o.store_scales(p2, "e8m0")[0], p2)  # exact powers of two map to themselves
+
+
+def test_e8m0_scale_is_smallest_power_of_two_above():
+    check_e8m0_scale(O)
+
+
+@pytest.mark.parametrize("fmt", ("fp16", "e8m0"))
+@pytest.mark.parametrize("bits", (4, 8))
+def test_codes_against_the_stored_scale(fmt, bits):
+    rng = np.random.default_rng(bits)
+    d, g = 32, 16
+    x = (rng.standard_normal((6, d)) * 3).astype(np.float16).astype(np.float64)
+    enc = O.srft_kv_quantize(x, None, bits, g, 5, scale_format=fmt)
+    Q = O.qmax(bits)
+    sc = np.repeat(enc["scales"], g, axis=-1)
+    levels = np.arange(-Q, Q + 1)
+    best = levels[np.argmin(np.abs(enc["z"][..., None] - levels * sc[..., None]), axis=-1)]
+    assert np.array_equal(enc["q"], best)
+    assert np.array_equal(O.decode_scales(enc["scales_raw"], fmt), enc["scales"])
+    if fmt == "e8m0":  # no code needs clamping: |z| / scale <= Q
+        assert np.all(np.abs(enc["r"]) <= Q)
+    # zero groups store 0 and codes 0
+    z0 = O.srft_kv_quantize(np.zeros((1, d)), None, bits, g, 5, scale_format=fmt)
+    assert not z0["scales"].any() and not z0["q"].any() and not np.asarray(z0["scales_raw"]).any()
+
+
+def test_lighter_scale_planes_give_the_pages_compression():
+    # [WQF] Key results, memory efficiency: 3.0x to 3.56x persistent compression (tests/golden/pages_memory.json)
+    with open(os.path.join(GOLDEN, "pages_memory.json")) as f:
+        gl = json.load(f)
+    fp16_vec = 2 * 128
+    assert round(fp16_vec / O.packed_vector_bytes(128, 4, 16, O.SCALE_BYTES["e8m0"]), 2) == gl["compression"]["max_ratio"]
+    assert fp16_vec / O.packed_vector_bytes(128, 4, 16, O.SCALE_BYTES["fp16"]) == pytest.approx(3.2)
+    assert fp16_vec / O.packed_vector_bytes(128, 4, 16, O.SCALE_BYTES["fp32"]) == pytest.approx(2.67, abs=0.005)
+
+
 # ---------------------------------------------------------------- mutation tests
 
 class _Mutant:
@@ -504,3 +579,28 @@ def test_mutant_hadamard_wrong_index_rule_is_caught():
 
     with pytest.raises(AssertionError):
         check_hadamard_matches_scipy(_Mutant(hadamard_matrix=bad_hadamard), 8)
+
+
+def test_mutant_truncating_fp16_scale_is_caught():
+    def bad_round(v):
+        v = np.asarray(v, dtype=np.float64)
+        h = np.clip(v, -O.FP16_MAX, O.FP16_MAX).astype(np.float16)
+        up = h.astype(np.float64) > v  # round toward zero instead of to nearest
+        h = np.where(up, np.nextafter(h, np.float16(0)), h)
+        return h.astype(np.float64)
+
+    with pytest.raises(AssertionError):
+        check_fp16_scale_rounding(_Mutant(fp16_round=bad_round))
+
+
+def test_mutant_floor_e8m0_exponent_is_caught():
+    def bad_exp(v):
+        v = np.asarray(v, dtype=np.float64)
+        return np.clip(np.floor(np.log2(np.where(v > 0, v, 1.0))), -126, 127).astype(np.int64)
+
+    def bad_store(a, fmt):
+        e = bad_exp(a)
+        return np.ldexp(1.0, e), (e + 127).astype(np.uint8)
+
+    with pytest.raises(AssertionError):
+        check_e8m0_scale(_Mutant(e8m0_exponent=bad_exp, store_scales=bad_store))
