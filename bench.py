@@ -293,6 +293,41 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     ms_step = ms_total / args.steps
     value = world * n_vec / (ms_step * 1e-3)
 
+    # variants of the cache format on the same workload and kernels (outside the timed step): the Hadamard
+    # rotation, and fp16 / e8m0 scale planes; each timed as the median of 10 launches with CUDA events on the
+    # launching stream.  Algorithmic bytes follow the plane sizes (scales of 4, 2 or 1 bytes).
+    def time_launch(fn, reps=10):
+        ts = []
+        for _ in range(reps + 2):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts[2:])
+
+    variants = {}
+    for name, tr, sf in (("srht", "srht", "fp32"), ("fp16_scales", "srft", "fp16"), ("e8m0_scales", "srft", "e8m0")):
+        sb = {"fp32": 4, "fp16": 2, "e8m0": 1}[sf]
+        vec_bytes = 2 * d + d // 2 + (d // G) * sb
+        tok_bytes = 2 * (d // 2 + (d // G) * sb)
+        vk = K.alloc_side(B, t_cap, Hkv, d, 4, G, device=dev, transform=tr, scale_format=sf)
+        vv = K.alloc_side(B, t_cap, Hkv, d, 4, G, device=dev, transform=tr, scale_format=sf)
+        vk.x, vv.x = xk, xv
+        qv = time_launch(lambda: K.srft_kv_quantize(vk, vv, B, T, Hkv, d, G, t_cap, 0, seed, stream))
+        dqk = K.Side(vk.codes, vk.scales, 4, x=dk, transform=tr, scale_format=sf)
+        dqv = K.Side(vv.codes, vv.scales, 4, x=dv, transform=tr, scale_format=sf)
+        dv_ms = time_launch(lambda: K.srft_kv_dequantize(dqk, dqv, B, T, Hkv, d, G, t_cap, 0, seed, stream))
+        av = time_launch(lambda: K.q4kv_decode_attention(q, out, vk, vv, B, Hq, Hkv, d, G, t_cap, seq, 0.0, seed, 0,
+                                                         ws, stream))
+        variants[name] = {"transform": tr, "scales": sf, "quant_ms": qv, "deq_ms": dv_ms, "attn_ms": av,
+                          "quant_gbs": n_vec * vec_bytes / (qv * 1e-3) / 1e9,
+                          "deq_gbs": n_vec * vec_bytes / (dv_ms * 1e-3) / 1e9,
+                          "attn_gbs": B * T * Hkv * tok_bytes / (av * 1e-3) / 1e9,
+                          "attn_bytes_per_token_head": tok_bytes}
+        del vk, vv, dqk, dqv
+
     # fp16-cache comparator: the same attention kernel on the raw fp16 cache (head-major like the packed planes)
     raw_k = K.Side(xk.permute(0, 2, 1, 3).contiguous(), None, 16)
     raw_v = K.Side(xv.permute(0, 2, 1, 3).contiguous(), None, 16)
@@ -343,6 +378,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     traffic = recorded_traffic("srft_quantize_tc_kernel")
     attn_gbs = attn_bytes / (med["attn"] * 1e-3) / 1e9
     fp16_ms = statistics.median(t16)
+    for vname in variants:
+        variants[vname]["attn_speedup_vs_fp16_cache"] = fp16_ms / variants[vname]["attn_ms"]
     cpu = None if args.no_cpu else oracle_sample(args.cpu_seconds)
     line = {
         "metric": METRIC,
@@ -377,6 +414,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                       "algorithmic_bytes_per_launch": attn_bytes,
                       "traffic": recorded_traffic("q4kv_attn_split_kernel")},
         "append_us": med["append"] * 1e3,
+        "variants": variants,
         "gpu_launches": LAUNCHES * args.steps,
         "clocks": clk,
         "e2e": e2e,

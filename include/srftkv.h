@@ -73,8 +73,12 @@ extern "C" {
 #define SRFTKV_TRANSFORM_SRHT 1 /* SRHT(x) = d^(-1/2) H diag(s) x, H the Sylvester Hadamard matrix in
                                    natural order (H_ij = (-1)^popcount(i & j)); the alternative the same
                                    section names, same sign vector s, no packing needed */
-/* The scale plane's number format (per side, field `scale_format`). */
-#define SRFTKV_SCALE_FP32 0     /* fp32 scales, d/group per row */
+/* The scale plane's number format (per side, field `scale_format`); the codes are
+ * rounded against the stored scale ([WQF] Key results, memory efficiency: 3.0-3.56x). */
+#define SRFTKV_SCALE_FP32 0     /* fp32 A/Q, d/group per row (4 bytes each) */
+#define SRFTKV_SCALE_FP16 1     /* fp16: A/Q rounded to nearest (ties even), saturating at 65504 (2 bytes) */
+#define SRFTKV_SCALE_E8M0 2     /* one byte e: scale 2^(e-127) = the smallest power of two not below A/Q,
+                                   e in [1, 254]; e = 0 stores an all-zero group (scale 0) */
 
 /*
  * One side (K or V) of a packed cache, stored as two head-major planes ([AQT]):
@@ -98,9 +102,9 @@ typedef struct srftkv_side {
     int64_t lambda_outer_stride; /* 0 broadcasts one [H][d] table over n_outer */
     int bits;                    /* 4 or 8 (16 = raw fp16 cache, attention only) */
     void* codes;                 /* code plane (see above) */
-    float* scales;               /* scale plane (see above) */
+    void* scales;                /* scale plane (see above): fp32, fp16 or e8m0 bytes per scale_format */
     int transform;               /* SRFTKV_TRANSFORM_SRFT (0) or SRFTKV_TRANSFORM_SRHT (1); ignored for bits 16 */
-    int scale_format;            /* SRFTKV_SCALE_FP32 (0); other values return SRFTKV_ERR_INVALID */
+    int scale_format;            /* SRFTKV_SCALE_FP32 (0), _FP16 (1) or _E8M0 (2): the element type of `scales` */
 } srftkv_side;
 
 /*

@@ -46,6 +46,8 @@ class _Side(ctypes.Structure):
 
 
 TRANSFORMS = {"srft": 0, "srht": 1}  # SRFTKV_TRANSFORM_SRFT / _SRHT in include/srftkv.h
+SCALE_FORMATS = {"fp32": 0, "fp16": 1, "e8m0": 2}  # SRFTKV_SCALE_FP32 / _FP16 / _E8M0
+SCALE_DTYPES = {"fp32": torch.float32, "fp16": torch.float16, "e8m0": torch.uint8}
 
 
 _lib = None
@@ -101,30 +103,30 @@ class Side:
     an optional per-channel lambda and, for the codec calls, the fp16 rows."""
 
     codes: torch.Tensor            # uint8 [n_outer][H][t_cap][d*bits/8] (or fp16 [B][Hkv][t_cap][d] for bits 16)
-    scales: torch.Tensor | None    # fp32 [n_outer][H][t_cap][d/group]
+    scales: torch.Tensor | None    # [n_outer][H][t_cap][d/group]: fp32, fp16 or uint8 (e8m0) per scale_format
     bits: int
     x: torch.Tensor | None = None  # fp16 [n_outer][n_tokens][H][d]
     lam: torch.Tensor | None = None  # fp32 [n_lam][H][d]; n_lam == 1 broadcasts
     lam_outer_stride: int | None = None
     transform: str = "srft"        # "srft" or "srht"
-    scale_format: int = 0          # SRFTKV_SCALE_FP32
+    scale_format: str = "fp32"     # "fp32", "fp16" or "e8m0"
 
     def to_c(self) -> _Side:
         stride = self.lam_outer_stride
         if stride is None:
             stride = 0 if self.lam is None or self.lam.shape[0] == 1 else self.lam.shape[1] * self.lam.shape[2]
         return _Side(_ptr(self.x), _ptr(self.lam), stride, self.bits, _ptr(self.codes), _ptr(self.scales),
-                     TRANSFORMS[self.transform], self.scale_format)
+                     TRANSFORMS[self.transform], SCALE_FORMATS[self.scale_format])
 
 
 def alloc_side(n_outer: int, t_cap: int, H: int, d: int, bits: int, group: int, device="cuda",
-               transform: str = "srft") -> Side:
+               transform: str = "srft", scale_format: str = "fp32") -> Side:
     """Allocate empty (head-major) code and scale planes for one side."""
     if bits == 16:
         return Side(torch.empty((n_outer, H, t_cap, d), dtype=torch.float16, device=device), None, 16)
     codes = torch.empty((n_outer, H, t_cap, d * bits // 8), dtype=torch.uint8, device=device)
-    scales = torch.empty((n_outer, H, t_cap, d // group), dtype=torch.float32, device=device)
-    return Side(codes, scales, bits, transform=transform)
+    scales = torch.empty((n_outer, H, t_cap, d // group), dtype=SCALE_DTYPES[scale_format], device=device)
+    return Side(codes, scales, bits, transform=transform, scale_format=scale_format)
 
 
 def _sidep(s: Side | None):

@@ -201,11 +201,12 @@ static int check_side(const srftkv_side* s, const char* name, int d, int group, 
     if (s->bits != 4 && s->bits != 8) return invalid("%s: bits must be 4 or 8 (got %d)", name, s->bits);
     if (s->transform != SRFTKV_TRANSFORM_SRFT && s->transform != SRFTKV_TRANSFORM_SRHT)
         return invalid("%s: transform must be SRFTKV_TRANSFORM_SRFT or SRFTKV_TRANSFORM_SRHT (got %d)", name, s->transform);
-    if (s->scale_format != SRFTKV_SCALE_FP32)
+    if (s->scale_format != SRFTKV_SCALE_FP32 && s->scale_format != SRFTKV_SCALE_FP16 &&
+        s->scale_format != SRFTKV_SCALE_E8M0)
         return invalid("%s: scale_format %d is not supported", name, s->scale_format);
     if (!s->codes || !s->scales) return invalid("%s: codes and scales must not be NULL", name);
     if (need_x && !s->x) return invalid("%s: x must not be NULL", name);
-    const size_t crow = (size_t)d * s->bits / 8, srow = (size_t)(d / group) * 4;
+    const size_t crow = (size_t)d * s->bits / 8, srow = (size_t)(d / group) * scale_bytes(s->scale_format);
     if (!aligned(s->codes, min_sz(16, crow))) return invalid("%s: codes must be %zu-byte aligned", name, min_sz(16, crow));
     if (!aligned(s->scales, min_sz(16, srow))) return invalid("%s: scales must be %zu-byte aligned", name, min_sz(16, srow));
     if (need_x && !aligned(s->x, 16)) return invalid("%s: x must be 16-byte aligned", name);
@@ -232,6 +233,7 @@ static int codec_common(const srftkv_side* k, const srftkv_side* v, int n_outer,
         s.x = sides[i]->x;
         s.codes = static_cast<uint8_t*>(sides[i]->codes);
         s.scales = sides[i]->scales;
+        s.scale_format = sides[i]->scale_format;
         s.lambda = sides[i]->lambda;
         s.lambda_outer_stride = sides[i]->lambda_outer_stride;
         s.bits = sides[i]->bits;

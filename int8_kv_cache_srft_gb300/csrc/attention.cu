@@ -64,6 +64,7 @@ struct AttnParams {
     int B, Hq, Hkv, rep, t_cap, n_splits, group, log2_group;
     int sp;                // scale row (floats)
     int tr_k, tr_v;        // transform of the K and V sides (SRFTKV_TRANSFORM_*)
+    int sf_k, sf_v;        // scale format of the K and V sides (SRFTKV_SCALE_*)
     float qscale;          // sm_scale * log2(e)
     uint32_t sign_mask[128];
 };
@@ -165,7 +166,11 @@ struct AttnCfg {
     static constexpr int OFF_KS = align_up(OFF_KC + CH * PlaneT<D, BK>::RP, AS);
     static constexpr int OFF_VC = align_up(OFF_KS + (QK ? CH * SRB : 0), AV);
     static constexpr int OFF_VS = align_up(OFF_VC + CH * PlaneT<D, BV>::RP, AS);
-    static constexpr int STAGE = align_up(OFF_VS + (QV ? CH * SRB : 0), A0);
+    // fp16 / e8m0 scale planes land raw (at most 2 bytes a scale) and are widened into the fp32 rows above
+    static constexpr int RAWB = CH * (D / 16) * 2;
+    static constexpr int OFF_KR = align_up(OFF_VS + (QV ? CH * SRB : 0), 128);
+    static constexpr int OFF_VR = OFF_KR + (QK ? RAWB : 0);
+    static constexpr int STAGE = align_up(OFF_VR + (QV ? RAWB : 0), A0);
     static constexpr int WARP_BYTES = NS * STAGE;
     static constexpr int MERGE_BYTES = kAttnWarps * (4 * D + 8) * 4;
     static constexpr int BODY = kAttnWarps * WARP_BYTES > MERGE_BYTES ? kAttnWarps * WARP_BYTES : MERGE_BYTES;
@@ -547,6 +552,28 @@ __device__ __forceinline__ void tile_pv(uint32_t vc, const LaneRow& LV, const ui
     }
 }
 
+// Widen the raw fp16 / e8m0 scales of a staged chunk (rows of ng scales of
+// sb bytes, contiguous) into the fp32 rows the compute reads: group 16 into
+// the swizzled rows of d/4 bytes, other groups into plain rows of ng floats.
+template <int D, int G>
+__device__ __forceinline__ void widen_scales(const uint8_t* __restrict__ raw, uint8_t* __restrict__ dst, int rows,
+                                             int ng, int sfmt, int lane) {
+    for (int i = lane; i < rows * ng; i += 32) {
+        const int r = i / ng, f = i - r * ng;
+        float v;
+        if (sfmt == SRFTKV_SCALE_FP16)
+            v = __half2float(__ushort_as_half(reinterpret_cast<const unsigned short*>(raw)[i]));
+        else
+            v = __uint_as_float((uint32_t)raw[i] << 23);  // e8m0: the byte is the fp32 exponent field
+        uint32_t off;
+        if constexpr (G == 16)
+            off = (uint32_t)(r * (D / 4) + (swz_chunk<D / 4>(r, f >> 2) << 4) + (f & 3) * 4);
+        else
+            off = (uint32_t)((r * ng + f) * 4);
+        *reinterpret_cast<float*>(dst + off) = v;
+    }
+}
+
 // One chunk of NT 16-token sub-tiles starting at token t0 of the sequence:
 // scores for all NT*16 tokens, one online-softmax update, then P.V.
 // G: the group size when known at compile time (16, the common case: all
@@ -565,6 +592,13 @@ __device__ __forceinline__ void attn_chunk(const AttnParams& P, uint8_t* __restr
     float* ks = reinterpret_cast<float*>(stage + C::OFF_KS);
     float* vs = reinterpret_cast<float*>(stage + C::OFF_VS);
     const int sp = G ? D / G : P.sp;  // floats per scale row
+    if ((C::QK && P.sf_k != SRFTKV_SCALE_FP32) || (C::QV && P.sf_v != SRFTKV_SCALE_FP32)) {
+        if (C::QK && P.sf_k != SRFTKV_SCALE_FP32)
+            widen_scales<D, G>(stage + C::OFF_KR, stage + C::OFF_KS, 16 * NT, sp, P.sf_k, lane);
+        if (C::QV && P.sf_v != SRFTKV_SCALE_FP32)
+            widen_scales<D, G>(stage + C::OFF_VR, stage + C::OFF_VS, 16 * NT, sp, P.sf_v, lane);
+        __syncwarp();
+    }
     const int lg = G == 16 ? 4 : G == 32 ? 5 : G == 64 ? 6 : P.log2_group;
     const int valid = t_end - t0;  // tokens of this chunk inside the sequence (> 0)
     const bool tail = valid < 16 * NT;
@@ -709,17 +743,28 @@ __global__ void __launch_bounds__(kAttnWarps * 32, D >= 256 ? 2 : 3)
 
     const int plane_row = b * P.Hkv + hkv;  // this (batch, kv head)'s rows in the head-major planes
     const uint32_t kc_bytes = C::CH * PlaneT<D, BK>::RP, vc_bytes = C::CH * PlaneT<D, BV>::RP;
-    const uint32_t sc_bytes = C::CH * P.sp * 4;  // exact rows of d/group floats
-    const uint32_t tx = kc_bytes + vc_bytes + (C::QK ? sc_bytes : 0) + (C::QV ? sc_bytes : 0);
+    // exact rows of d/group scales: fp32 into the compute rows, fp16 / e8m0 raw into their own area
+    const uint32_t ks_bytes = C::CH * P.sp * (P.sf_k == SRFTKV_SCALE_FP32 ? 4 : P.sf_k == SRFTKV_SCALE_FP16 ? 2 : 1);
+    const uint32_t vs_bytes = C::CH * P.sp * (P.sf_v == SRFTKV_SCALE_FP32 ? 4 : P.sf_v == SRFTKV_SCALE_FP16 ? 2 : 1);
+    const int ks_off = P.sf_k == SRFTKV_SCALE_FP32 ? C::OFF_KS : C::OFF_KR;
+    const int vs_off = P.sf_v == SRFTKV_SCALE_FP32 ? C::OFF_VS : C::OFF_VR;
+    // raw planes are addressed as rows of 16 bytes: the chunk's first one
+    const int ks_row = P.sf_k == SRFTKV_SCALE_FP32 ? 1 : (int)(ks_bytes / 16);
+    const int vs_row = P.sf_v == SRFTKV_SCALE_FP32 ? 1 : (int)(vs_bytes / 16);
+    const uint32_t tx = kc_bytes + vc_bytes + (C::QK ? ks_bytes : 0) + (C::QV ? vs_bytes : 0);
     auto issue = [&](int chunk, int st) {
         const uint32_t bar = barw(st);
         uint8_t* dst = wbase + st * C::STAGE;
         const int tok = chunk * C::CH;
         ptx::mbar_arrive_expect_tx(bar, tx);
         ptx::tma_load_3d(ptx::smem_u32(dst + C::OFF_KC), &tm_kc, bar, 0, tok, plane_row);
-        if constexpr (C::QK) ptx::tma_load_3d(ptx::smem_u32(dst + C::OFF_KS), &tm_ks, bar, 0, tok, plane_row);
+        if constexpr (C::QK)
+            ptx::tma_load_3d(ptx::smem_u32(dst + ks_off), &tm_ks, bar, 0,
+                             P.sf_k == SRFTKV_SCALE_FP32 ? tok : chunk * ks_row, plane_row);
         ptx::tma_load_3d(ptx::smem_u32(dst + C::OFF_VC), &tm_vc, bar, 0, tok, plane_row);
-        if constexpr (C::QV) ptx::tma_load_3d(ptx::smem_u32(dst + C::OFF_VS), &tm_vs, bar, 0, tok, plane_row);
+        if constexpr (C::QV)
+            ptx::tma_load_3d(ptx::smem_u32(dst + vs_off), &tm_vs, bar, 0,
+                             P.sf_v == SRFTKV_SCALE_FP32 ? tok : chunk * vs_row, plane_row);
     };
 
     // per-warp ring of NS stages: chunk j of this warp goes to stage j % NS, NS-1 chunks in flight
@@ -945,10 +990,26 @@ static int launch_split(const AttnLaunch& A) {
     const CUtensorMapSwizzle ssw = P.group == 16 ? swizzle_for(4 * ng) : CU_TENSOR_MAP_SWIZZLE_NONE;
     tks = tkc;
     tvs = tvc;
-    if (C::QK && !encode_plane(&tks, A.k->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ng, 4, ng, bh, P.t_cap, C::CH, ssw))
-        return SRFTKV_ERR_CUDA;
-    if (C::QV && !encode_plane(&tvs, A.v->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ng, 4, ng, bh, P.t_cap, C::CH, ssw))
-        return SRFTKV_ERR_CUDA;
+    // fp16 / e8m0 planes: the (batch, kv head)'s scale bytes as rows of 16 bytes; a box is one chunk's bytes
+    auto raw_plane = [&](CUtensorMap* map, const void* base, int sfmt) {
+        const int sb = sfmt == SRFTKV_SCALE_FP16 ? 2 : 1;
+        return encode_plane(map, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 16, 1, 16, bh, P.t_cap * ng * sb / 16,
+                            C::CH * ng * sb / 16, CU_TENSOR_MAP_SWIZZLE_NONE);
+    };
+    if (C::QK) {
+        const bool ok = P.sf_k == SRFTKV_SCALE_FP32
+                            ? encode_plane(&tks, A.k->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ng, 4, ng, bh, P.t_cap,
+                                           C::CH, ssw)
+                            : raw_plane(&tks, A.k->scales, P.sf_k);
+        if (!ok) return SRFTKV_ERR_CUDA;
+    }
+    if (C::QV) {
+        const bool ok = P.sf_v == SRFTKV_SCALE_FP32
+                            ? encode_plane(&tvs, A.v->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ng, 4, ng, bh, P.t_cap,
+                                           C::CH, ssw)
+                            : raw_plane(&tvs, A.v->scales, P.sf_v);
+        if (!ok) return SRFTKV_ERR_CUDA;
+    }
     static bool attr[2] = {false, false};
     const bool g16 = P.group == 16;  // raw fp16 sides carry group 16
     if (!attr[g16]) {
@@ -1045,7 +1106,13 @@ int attention_entry(const void* q, float* out, const srftkv_side* k, const srftk
         for (auto sd : sv2) {
             if (sd->transform != SRFTKV_TRANSFORM_SRFT && sd->transform != SRFTKV_TRANSFORM_SRHT)
                 return invalid_attn("attention: transform must be SRFTKV_TRANSFORM_SRFT or SRFTKV_TRANSFORM_SRHT");
-            if (sd->scale_format != SRFTKV_SCALE_FP32) return invalid_attn("attention: scale_format not supported");
+            if (sd->scale_format != SRFTKV_SCALE_FP32 && sd->scale_format != SRFTKV_SCALE_FP16 &&
+                sd->scale_format != SRFTKV_SCALE_E8M0)
+                return invalid_attn("attention: scale_format must be SRFTKV_SCALE_FP32, _FP16 or _E8M0");
+            // fp16 / e8m0 scale planes are copied as 16-byte rows: one (batch, kv head)'s scales fill whole rows
+            if (sd->scale_format != SRFTKV_SCALE_FP32 &&
+                ((long long)t_cap * (d / group) * scale_bytes(sd->scale_format)) % 16 != 0)
+                return invalid_attn("attention: t_cap * (d/group) * scale bytes must be a multiple of 16");
         }
         if ((reinterpret_cast<uintptr_t>(k->scales) | reinterpret_cast<uintptr_t>(v->scales)) & 15)
             return invalid_attn("attention: scales must be 16-byte aligned");
@@ -1096,6 +1163,8 @@ int attention_entry(const void* q, float* out, const srftkv_side* k, const srftk
     P.sp = raw ? 0 : d / P.group;
     P.tr_k = raw ? 0 : k->transform;
     P.tr_v = raw ? 0 : v->transform;
+    P.sf_k = raw ? 0 : k->scale_format;
+    P.sf_v = raw ? 0 : v->scale_format;
     const float sc = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt((float)d);
     P.qscale = sc * 1.4426950408889634f;
     sign_masks(d, seed, P.sign_mask);

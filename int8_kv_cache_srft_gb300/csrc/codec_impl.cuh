@@ -29,11 +29,13 @@ namespace srftkv {
 
 struct CodecSideK {
     uint8_t* codes;
-    float* scales;
+    uint8_t* scales;     // element type per sfmt
     const float* lambda;
     long long lambda_outer_stride;
     int bits;
     int transform;  // SRFTKV_TRANSFORM_SRFT or SRFTKV_TRANSFORM_SRHT
+    int sfmt;       // SRFTKV_SCALE_FP32 / _FP16 / _E8M0
+    int sbytes;     // bytes per stored scale
 };
 
 struct CodecParams {
@@ -92,8 +94,8 @@ __device__ __forceinline__ long long packed_row(const CodecParams& P, const Tile
 // every group size; group == 16 (the default) keeps 16-byte scale stores.
 // ---------------------------------------------------------------------------
 template <int D, int BITS>
-__device__ __forceinline__ void quant_store_row(float (&z)[D], int group, uint8_t* __restrict__ crow,
-                                                float* __restrict__ srow) {
+__device__ __forceinline__ void quant_store_row(float (&z)[D], int group, int sfmt, uint8_t* __restrict__ crow,
+                                                uint8_t* __restrict__ srow) {
     constexpr int U = D / 16;
     constexpr float Q = (BITS == 4) ? 7.f : 127.f;
     constexpr float MAG = kMagic + ((BITS == 4) ? 8.f : 128.f);
@@ -113,15 +115,40 @@ __device__ __forceinline__ void quant_store_row(float (&z)[D], int group, uint8_
         }
     }
     float sc[U];
+    uint32_t raw[U];  // fp16 bits or the e8m0 byte of the stored scale
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        // scale = A/Q to within an ulp; z * (Q * rcp(A)) rounds z/scale to within a few ulp, far inside the
-        // 1e-4 band around rounding boundaries
         const float A = m[u];
-        sc[u] = A * (1.0f / Q);
-        const float inv = A > 0.f ? Q * __frcp_rn(A) : 0.f;
+        float inv;
+        if (sfmt == SRFTKV_SCALE_FP32) {
+            // scale = A/Q to within an ulp; z * (Q * rcp(A)) rounds z/scale to within a few ulp, far inside the
+            // 1e-4 band around rounding boundaries
+            sc[u] = A * (1.0f / Q);
+            raw[u] = 0;
+            inv = A > 0.f ? Q * __frcp_rn(A) : 0.f;
+        } else if (sfmt == SRFTKV_SCALE_FP16) {
+            // A/Q correctly rounded in fp32, then to fp16: with 24 >= 2*11 + 2 bits the double rounding equals
+            // rounding A/Q to fp16 directly; saturate at the largest finite fp16
+            const __half h = __float2half_rn(fminf(__fdiv_rn(A, Q), 65504.f));
+            sc[u] = __half2float(h);
+            raw[u] = __half_as_ushort(h);
+            inv = sc[u] > 0.f ? __frcp_rn(sc[u]) : 0.f;
+        } else {
+            // e8m0: biased exponent of the smallest power of two not below A/Q (normal or subnormal v)
+            const float v = __fdiv_rn(A, Q);
+            const uint32_t b = __float_as_uint(v);
+            uint32_t e = (b >> 23) + ((b & 0x7FFFFFu) != 0u ? 1u : 0u);
+            e = v > 0.f ? min(max(e, 1u), 254u) : 0u;
+            raw[u] = e;
+            sc[u] = __uint_as_float(e << 23);
+            inv = e ? __frcp_rn(sc[u]) : 0.f;
+        }
 #pragma unroll
         for (int i = 0; i < 16; ++i) z[16 * u + i] = fmaf_(z[16 * u + i], inv, MAG);
+        if (sfmt == SRFTKV_SCALE_FP16) {  // a saturated scale can push |z/scale| past Q
+#pragma unroll
+            for (int i = 0; i < 16; ++i) z[16 * u + i] = fminf(fmaxf(z[16 * u + i], MAG - Q), MAG + Q);
+        }
     }
     constexpr int WORDS = D * BITS / 32;
     uint32_t w[WORDS];
@@ -134,30 +161,85 @@ __device__ __forceinline__ void quant_store_row(float (&z)[D], int group, uint8_
     } else {
         reinterpret_cast<uint2*>(crow)[0] = make_uint2(w[0], w[1]);
     }
-    if (group == 16) {
-        if constexpr (U >= 4) {
+    if (sfmt == SRFTKV_SCALE_FP32) {
+        float* sr = reinterpret_cast<float*>(srow);
+        if (group == 16) {
+            if constexpr (U >= 4) {
 #pragma unroll
-            for (int i = 0; i < U / 4; ++i)
-                reinterpret_cast<float4*>(srow)[i] = make_float4(sc[4 * i], sc[4 * i + 1], sc[4 * i + 2], sc[4 * i + 3]);
-        } else if constexpr (U == 2) {
-            reinterpret_cast<float2*>(srow)[0] = make_float2(sc[0], sc[1]);
+                for (int i = 0; i < U / 4; ++i)
+                    reinterpret_cast<float4*>(sr)[i] = make_float4(sc[4 * i], sc[4 * i + 1], sc[4 * i + 2], sc[4 * i + 3]);
+            } else if constexpr (U == 2) {
+                reinterpret_cast<float2*>(sr)[0] = make_float2(sc[0], sc[1]);
+            } else {
+                sr[0] = sc[0];
+            }
         } else {
-            srow[0] = sc[0];
+            const int gu = group >> 4, sh = __ffs(gu) - 1;
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if ((u & (gu - 1)) == 0) sr[u >> sh] = sc[u];
+        }
+    } else if (sfmt == SRFTKV_SCALE_FP16) {
+        uint16_t* sr = reinterpret_cast<uint16_t*>(srow);
+        if (group == 16) {
+            if constexpr (U >= 8) {
+#pragma unroll
+                for (int i = 0; i < U / 8; ++i)
+                    reinterpret_cast<uint4*>(sr)[i] =
+                        make_uint4(raw[8 * i] | (raw[8 * i + 1] << 16), raw[8 * i + 2] | (raw[8 * i + 3] << 16),
+                                   raw[8 * i + 4] | (raw[8 * i + 5] << 16), raw[8 * i + 6] | (raw[8 * i + 7] << 16));
+            } else if constexpr (U == 4) {
+                reinterpret_cast<uint2*>(sr)[0] = make_uint2(raw[0] | (raw[1] << 16), raw[2] | (raw[3] << 16));
+            } else if constexpr (U == 2) {
+                reinterpret_cast<uint32_t*>(sr)[0] = raw[0] | (raw[1] << 16);
+            } else {
+                sr[0] = (uint16_t)raw[0];
+            }
+        } else {
+            const int gu = group >> 4, sh = __ffs(gu) - 1;
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if ((u & (gu - 1)) == 0) sr[u >> sh] = (uint16_t)raw[u];
         }
     } else {
-        const int gu = group >> 4, sh = __ffs(gu) - 1;
+        if (group == 16) {
+            if constexpr (U >= 8) {
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-            if ((u & (gu - 1)) == 0) srow[u >> sh] = sc[u];
+                for (int i = 0; i < U / 8; ++i)
+                    reinterpret_cast<uint2*>(srow)[i] =
+                        make_uint2(raw[8 * i] | (raw[8 * i + 1] << 8) | (raw[8 * i + 2] << 16) | (raw[8 * i + 3] << 24),
+                                   raw[8 * i + 4] | (raw[8 * i + 5] << 8) | (raw[8 * i + 6] << 16) |
+                                       (raw[8 * i + 7] << 24));
+            } else if constexpr (U == 4) {
+                reinterpret_cast<uint32_t*>(srow)[0] = raw[0] | (raw[1] << 8) | (raw[2] << 16) | (raw[3] << 24);
+            } else if constexpr (U == 2) {
+                reinterpret_cast<uint16_t*>(srow)[0] = (uint16_t)(raw[0] | (raw[1] << 8));
+            } else {
+                srow[0] = (uint8_t)raw[0];
+            }
+        } else {
+            const int gu = group >> 4, sh = __ffs(gu) - 1;
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if ((u & (gu - 1)) == 0) srow[u >> sh] = (uint8_t)raw[u];
+        }
     }
+}
+
+// Value of stored scale i of a row in the given format (e8m0: the byte is the
+// fp32 exponent field, byte 0 reads as 0.0f)
+__device__ __forceinline__ float load_scale(const uint8_t* __restrict__ srow, int i, int sfmt) {
+    if (sfmt == SRFTKV_SCALE_FP32) return __ldg(reinterpret_cast<const float*>(srow) + i);
+    if (sfmt == SRFTKV_SCALE_FP16) return __half2float(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short*>(srow) + i)));
+    return __uint_as_float((uint32_t)__ldg(srow + i) << 23);
 }
 
 // ---------------------------------------------------------------------------
 // Decode one stored row to rotated coordinates q * scale (lambda not applied).
 // ---------------------------------------------------------------------------
 template <int D, int BITS>
-__device__ __forceinline__ void dequant_load_row(const uint8_t* __restrict__ crow, const float* __restrict__ srow,
-                                                 int group, float (&p)[D]) {
+__device__ __forceinline__ void dequant_load_row(const uint8_t* __restrict__ crow, const uint8_t* __restrict__ srow,
+                                                 int group, int sfmt, float (&p)[D]) {
     constexpr int WORDS = D * BITS / 32, PER = 32 / BITS, U = D / 16;
     uint32_t w[WORDS];
     if constexpr (WORDS >= 4) {
@@ -177,7 +259,7 @@ __device__ __forceinline__ void dequant_load_row(const uint8_t* __restrict__ cro
     const int sh = __ffs(group >> 4) - 1;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        const float sc = __ldg(srow + (u >> sh));
+        const float sc = load_scale(srow, u >> sh, sfmt);
 #pragma unroll
         for (int i = 16 * u; i < 16 * u + 16; ++i) {
             const float c = (BITS == 4) ? code_int4(w[i / PER], i % PER) : code_int8(w[i / PER], i % PER);
@@ -241,9 +323,11 @@ __device__ __forceinline__ void quantize_tile(const CodecParams& P, const TileId
     const long long vrow = packed_row(P, id, t);
     // with equal widths on both sides only one epilogue is compiled
     if (BK == BV || id.side == 0)
-        quant_store_row<D, BK>(z, P.group, S.codes + vrow * (D * BK / 8), S.scales + vrow * (D / P.group));
+        quant_store_row<D, BK>(z, P.group, S.sfmt, S.codes + vrow * (D * BK / 8),
+                               S.scales + vrow * (D / P.group) * S.sbytes);
     else
-        quant_store_row<D, BV>(z, P.group, S.codes + vrow * (D * BV / 8), S.scales + vrow * (D / P.group));
+        quant_store_row<D, BV>(z, P.group, S.sfmt, S.codes + vrow * (D * BV / 8),
+                               S.scales + vrow * (D / P.group) * S.sbytes);
 }
 
 template <int D, int BK, int BV>
@@ -315,11 +399,11 @@ __global__ void __launch_bounds__(128, Geo<D>::MIN_BLOCKS)
         float p[D];
         if (valid) {
             const long long vrow = packed_row(P, id, t);
-            const float* srow = S.scales + vrow * (D / P.group);
+            const uint8_t* srow = S.scales + vrow * (D / P.group) * S.sbytes;
             if (BK == BV || id.side == 0)
-                dequant_load_row<D, BK>(S.codes + vrow * (D * BK / 8), srow, P.group, p);
+                dequant_load_row<D, BK>(S.codes + vrow * (D * BK / 8), srow, P.group, S.sfmt, p);
             else
-                dequant_load_row<D, BV>(S.codes + vrow * (D * BV / 8), srow, P.group, p);
+                dequant_load_row<D, BV>(S.codes + vrow * (D * BV / 8), srow, P.group, S.sfmt, p);
             if (S.lambda != nullptr) {
                 const float4* lr = reinterpret_cast<const float4*>(S.lambda + (long long)id.o * S.lambda_outer_stride +
                                                                    (long long)id.h * D);
@@ -383,7 +467,9 @@ static inline void fill_params(const CodecCall& c, CodecParams& P) {
     for (int s = 0; s < 2; ++s) {
         const CodecSideDesc& d = c.side[s < c.n_sides ? s : 0];
         P.side[s].codes = d.codes;
-        P.side[s].scales = d.scales;
+        P.side[s].scales = static_cast<uint8_t*>(d.scales);
+        P.side[s].sfmt = d.scale_format;
+        P.side[s].sbytes = scale_bytes(d.scale_format);
         P.side[s].lambda = d.lambda;
         P.side[s].lambda_outer_stride = d.lambda_outer_stride;
         P.side[s].bits = d.bits;

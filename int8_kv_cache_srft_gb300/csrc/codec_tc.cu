@@ -209,11 +209,11 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
             const long long vrow = packed_row(P, id, t_tok);
             const int ng = TD / P.group;  // groups of at most 32: a column quarter holds whole groups
             if (BK == BV || id.side == 0)
-                quant_store_row<32, BK>(z, P.group, S.codes + vrow * (TD * BK / 8) + cq * (32 * BK / 8),
-                                        S.scales + vrow * ng + cq * (ng / 4));
+                quant_store_row<32, BK>(z, P.group, S.sfmt, S.codes + vrow * (TD * BK / 8) + cq * (32 * BK / 8),
+                                        S.scales + (vrow * ng + cq * (ng / 4)) * S.sbytes);
             else
-                quant_store_row<32, BV>(z, P.group, S.codes + vrow * (TD * BV / 8) + cq * (32 * BV / 8),
-                                        S.scales + vrow * ng + cq * (ng / 4));
+                quant_store_row<32, BV>(z, P.group, S.sfmt, S.codes + vrow * (TD * BV / 8) + cq * (32 * BV / 8),
+                                        S.scales + (vrow * ng + cq * (ng / 4)) * S.sbytes);
         }
     }
     if (failed) atomicOr(P.fault, 1u);
@@ -312,8 +312,38 @@ __device__ __forceinline__ uint32_t half2_bcast(__half h) {
 // codes * scale for columns 64 hf .. 64 hf + 63 of tile row m, from the
 // stage's exact swizzled code rows (64 bytes for 4-bit, 128 for 8-bit) and
 // scale rows (TD / group floats: 32 bytes for group 16, 16 for group 32)
+// The four 16-column unit scales of columns 64 hf .. +63 of tile row m: fp32
+// scale planes come through the stage in shared memory (exact swizzled rows:
+// 32 bytes for group 16, 16 for group 32); fp16 / e8m0 planes (at most 16
+// bytes a row) are read from global memory directly.
+__device__ __forceinline__ void half_row_scales(const uint8_t* __restrict__ in, int off_sc, int m, int hf, int group,
+                                                int sfmt, const uint8_t* __restrict__ grow, float (&sc)[4]) {
+    if (sfmt == SRFTKV_SCALE_FP32) {
+        const int srb = 4 * (TD / group);
+        if (group == 16) {  // groups 4hf .. 4hf+3: chunk hf of the 32-byte row
+            const float4 v = *reinterpret_cast<const float4*>(in + off_sc + m * srb + (swz16(srb, m, hf) << 4));
+            sc[0] = v.x;
+            sc[1] = v.y;
+            sc[2] = v.z;
+            sc[3] = v.w;
+        } else {  // group 32: groups 2hf, 2hf+1 of the 16-byte row
+            const float2 v = *reinterpret_cast<const float2*>(in + off_sc + m * srb + 8 * hf);
+            sc[0] = sc[1] = v.x;
+            sc[2] = sc[3] = v.y;
+        }
+        return;
+    }
+    if (group == 16) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) sc[u] = load_scale(grow, 4 * hf + u, sfmt);
+    } else {
+        sc[0] = sc[1] = load_scale(grow, 2 * hf, sfmt);
+        sc[2] = sc[3] = load_scale(grow, 2 * hf + 1, sfmt);
+    }
+}
+
 template <int BITS>
-__device__ __forceinline__ void dequant_half_smem(const uint8_t* __restrict__ in, int off_sc, int m, int hf, int group,
+__device__ __forceinline__ void dequant_half_smem(const uint8_t* __restrict__ in, int m, int hf, const float (&sc)[4],
                                                   float (&p)[64]) {
     constexpr int RB = TD * BITS / 8, NCH = 64 * BITS / 128, PER = 32 / BITS;  // chunks per half row
     uint32_t w[4 * NCH];
@@ -324,19 +354,6 @@ __device__ __forceinline__ void dequant_half_smem(const uint8_t* __restrict__ in
         w[4 * k + 1] = v.y;
         w[4 * k + 2] = v.z;
         w[4 * k + 3] = v.w;
-    }
-    float sc[4];
-    const int srb = 4 * (TD / group);
-    if (group == 16) {  // groups 4hf .. 4hf+3: chunk hf of the 32-byte row
-        const float4 v = *reinterpret_cast<const float4*>(in + off_sc + m * srb + (swz16(srb, m, hf) << 4));
-        sc[0] = v.x;
-        sc[1] = v.y;
-        sc[2] = v.z;
-        sc[3] = v.w;
-    } else {  // group 32: groups 2hf, 2hf+1 of the 16-byte row
-        const float2 v = *reinterpret_cast<const float2*>(in + off_sc + m * srb + 8 * hf);
-        sc[0] = sc[1] = v.x;
-        sc[2] = sc[3] = v.y;
     }
 #pragma unroll
     for (int i = 0; i < 64; ++i) {
@@ -350,7 +367,7 @@ __device__ __forceinline__ void dequant_half_smem(const uint8_t* __restrict__ in
 // group scale split into fp16 hi + lo, P_hat = fp16(q s_hi + fp16(q s_lo)), one
 // main rounding as when the fp32 product q s is rounded to fp16.
 template <int BITS>
-__device__ __forceinline__ void dequant_half_pairs(const uint8_t* __restrict__ in, int off_sc, int m, int hf, int group,
+__device__ __forceinline__ void dequant_half_pairs(const uint8_t* __restrict__ in, int m, int hf, const float (&sc)[4],
                                                    uint32_t (&hp)[32]) {
     constexpr int RB = TD * BITS / 8, NCH = 64 * BITS / 128;
     uint32_t w[4 * NCH];
@@ -361,19 +378,6 @@ __device__ __forceinline__ void dequant_half_pairs(const uint8_t* __restrict__ i
         w[4 * k + 1] = v.y;
         w[4 * k + 2] = v.z;
         w[4 * k + 3] = v.w;
-    }
-    float sc[4];
-    const int srb = 4 * (TD / group);
-    if (group == 16) {
-        const float4 v = *reinterpret_cast<const float4*>(in + off_sc + m * srb + (swz16(srb, m, hf) << 4));
-        sc[0] = v.x;
-        sc[1] = v.y;
-        sc[2] = v.z;
-        sc[3] = v.w;
-    } else {
-        const float2 v = *reinterpret_cast<const float2*>(in + off_sc + m * srb + 8 * hf);
-        sc[0] = sc[1] = v.x;
-        sc[2] = sc[3] = v.y;
     }
     uint32_t sh[4], sl[4];
 #pragma unroll
@@ -505,9 +509,11 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
                 const uint32_t dst = sbase + DQ_OFF_IN + st * C::STAGE;
                 const int row = P.t_offset + id.t0;   // packed planes: [outer*H][t_cap] rows
                 const int oh = id.o * P.H + id.h;
-                ptx::mbar_arrive_expect_tx(bar(IN_FULL + st), TM * (TD * bits / 8) + TM * (TD / P.group) * 4);
+                const bool sc_smem = P.side[id.side].sfmt == SRFTKV_SCALE_FP32;  // other formats: read from global
+                ptx::mbar_arrive_expect_tx(bar(IN_FULL + st),
+                                           TM * (TD * bits / 8) + (sc_smem ? TM * (TD / P.group) * 4 : 0));
                 ptx::tma_load_3d(dst, &M.codes[id.side], bar(IN_FULL + st), 0, row, oh);
-                ptx::tma_load_3d(dst + C::OFF_SC, &M.scales[id.side], bar(IN_FULL + st), 0, row, oh);
+                if (sc_smem) ptx::tma_load_3d(dst + C::OFF_SC, &M.scales[id.side], bar(IN_FULL + st), 0, row, oh);
             }
         }
     } else if (warp < 2 + DQ_CONV) {
@@ -527,19 +533,27 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
             const uint8_t* in = smem + DQ_OFF_IN + st * C::STAGE;
             uint32_t hp[32];  // fp16 pairs in the K order of dq_kperm: column 32 hf + c
             const bool side_k = BK == BV || id.side == 0;
+            float sc[4];
+            {
+                const int ng = TD / P.group, row_ok = t_tok < P.n_tokens;
+                const uint8_t* grow =
+                    S.scales + (((long long)id.o * P.H + id.h) * P.t_cap + P.t_offset + (row_ok ? t_tok : id.t0)) *
+                                   ng * S.sbytes;
+                half_row_scales(in, C::OFF_SC, m, hf, P.group, S.sfmt, grow, sc);
+            }
             if (S.lambda == nullptr) {
                 if (side_k)
-                    dequant_half_pairs<BK>(in, C::OFF_SC, m, hf, P.group, hp);
+                    dequant_half_pairs<BK>(in, m, hf, sc, hp);
                 else
-                    dequant_half_pairs<BV>(in, C::OFF_SC, m, hf, P.group, hp);
+                    dequant_half_pairs<BV>(in, m, hf, sc, hp);
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar(IN_EMPTY + st));  // input stage consumed
             } else {
                 float p[64];
                 if (side_k)
-                    dequant_half_smem<BK>(in, C::OFF_SC, m, hf, P.group, p);
+                    dequant_half_smem<BK>(in, m, hf, sc, p);
                 else
-                    dequant_half_smem<BV>(in, C::OFF_SC, m, hf, P.group, p);
+                    dequant_half_smem<BV>(in, m, hf, sc, p);
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar(IN_EMPTY + st));  // input stage consumed
                 if (t_tok < P.n_tokens) {
@@ -660,10 +674,14 @@ static int launch_dq_tc(const CodecCall& c) {
         const unsigned sbox[3] = {(unsigned)ng, (unsigned)TM, 1u};
         if (!encode_x_map(&M.out[s], d.x, TD, c.H, c.n_tokens, c.n_outer, TM, true) ||
             !encode_tiled_swz(&M.codes[s], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, d.codes, cdims, cstr, cbox, swz(rb),
-                              "tensor-core dequantize codes") ||
-            !encode_tiled_swz(&M.scales[s], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, d.scales, sdims, sstr, sbox,
-                              swz(4 * ng), "tensor-core dequantize scales"))
+                              "tensor-core dequantize codes"))
             return SRFTKV_ERR_CUDA;
+        if (d.scale_format != SRFTKV_SCALE_FP32) {
+            M.scales[s] = M.codes[s];  // unused: these scales are read from global memory
+        } else if (!encode_tiled_swz(&M.scales[s], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, d.scales, sdims, sstr, sbox,
+                                     swz(4 * ng), "tensor-core dequantize scales")) {
+            return SRFTKV_ERR_CUDA;
+        }
     }
     static bool attr = false;
     if (!attr) {

@@ -16,12 +16,16 @@ namespace srftkv {
 struct CodecSideDesc {
     void* x;              // fp16 rows [n_outer][n_tokens][H][d]
     uint8_t* codes;       // [n_outer][H][t_cap][d*bits/8]
-    float* scales;        // [n_outer][H][t_cap][d/group]
+    void* scales;         // [n_outer][H][t_cap][d/group], element type per scale_format
     const float* lambda;  // [*][H][d] or null
     int64_t lambda_outer_stride;
     int bits;
     int transform;        // SRFTKV_TRANSFORM_SRFT or SRFTKV_TRANSFORM_SRHT
+    int scale_format;     // SRFTKV_SCALE_FP32 / _FP16 / _E8M0
 };
+
+// bytes of one stored scale
+inline int scale_bytes(int scale_format) { return scale_format == SRFTKV_SCALE_FP32 ? 4 : scale_format == SRFTKV_SCALE_FP16 ? 2 : 1; }
 
 struct CodecCall {
     CodecSideDesc side[2];
