@@ -558,6 +558,28 @@ __device__ __forceinline__ void tile_pv(uint32_t vc, const LaneRow& LV, const ui
 template <int D, int G>
 __device__ __forceinline__ void widen_scales(const uint8_t* __restrict__ raw, uint8_t* __restrict__ dst, int rows,
                                              int ng, int sfmt, int lane) {
+    if constexpr (G == 16) {
+        // lane r widens row r: four scales (one 16-byte fp32 chunk) at a time
+        constexpr int NG = D / 16, SRB = D / 4;
+        if (lane < rows) {
+#pragma unroll
+            for (int j = 0; j < NG / 4; ++j) {
+                float4 v;
+                if (sfmt == SRFTKV_SCALE_FP16) {
+                    const uint2 h = *reinterpret_cast<const uint2*>(raw + lane * NG * 2 + 8 * j);
+                    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&h.x));
+                    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&h.y));
+                    v = make_float4(a.x, a.y, b.x, b.y);
+                } else {
+                    const uint32_t e = *reinterpret_cast<const uint32_t*>(raw + lane * NG + 4 * j);
+                    v = make_float4(__uint_as_float((e & 0xFFu) << 23), __uint_as_float(((e >> 8) & 0xFFu) << 23),
+                                    __uint_as_float(((e >> 16) & 0xFFu) << 23), __uint_as_float((e >> 24) << 23));
+                }
+                *reinterpret_cast<float4*>(dst + lane * SRB + (swz_chunk<SRB>(lane, j) << 4)) = v;
+            }
+        }
+        return;
+    }
     for (int i = lane; i < rows * ng; i += 32) {
         const int r = i / ng, f = i - r * ng;
         float v;

@@ -139,10 +139,13 @@ static int quant_path_override() {
     return (e && !strcmp(e, "fft")) ? 1 : (e && !strcmp(e, "tc")) ? 2 : 0;
 }
 
-// A call whose two sides use different transforms runs as two one-sided
-// calls (the tensor-core kernels hold one transform matrix per CTA).
+// A call whose two sides use different transforms or scale formats runs as
+// two one-sided calls (the tensor-core kernels hold one transform matrix per
+// CTA and are compiled per scale format).
 static bool split_mixed(const CodecCall& c, int (*fn)(const CodecCall&), int& rc) {
-    if (c.n_sides != 2 || c.side[0].transform == c.side[1].transform) return false;
+    if (c.n_sides != 2 ||
+        (c.side[0].transform == c.side[1].transform && c.side[0].scale_format == c.side[1].scale_format))
+        return false;
     CodecCall one = c;
     one.n_sides = 1;
     rc = fn(one);

@@ -93,9 +93,10 @@ __device__ __forceinline__ long long packed_row(const CodecParams& P, const Tile
 // runtime group size by a butterfly over units, so one code path serves
 // every group size; group == 16 (the default) keeps 16-byte scale stores.
 // ---------------------------------------------------------------------------
-template <int D, int BITS>
-__device__ __forceinline__ void quant_store_row(float (&z)[D], int group, int sfmt, uint8_t* __restrict__ crow,
+template <int D, int BITS, int SF>
+__device__ __forceinline__ void quant_store_row(float (&z)[D], int group, uint8_t* __restrict__ crow,
                                                 uint8_t* __restrict__ srow) {
+    constexpr int sfmt = SF;
     constexpr int U = D / 16;
     constexpr float Q = (BITS == 4) ? 7.f : 127.f;
     constexpr float MAG = kMagic + ((BITS == 4) ? 8.f : 128.f);
@@ -120,22 +121,23 @@ __device__ __forceinline__ void quant_store_row(float (&z)[D], int group, int sf
     for (int u = 0; u < U; ++u) {
         const float A = m[u];
         float inv;
-        if (sfmt == SRFTKV_SCALE_FP32) {
+        if constexpr (sfmt == SRFTKV_SCALE_FP32) {
             // scale = A/Q to within an ulp; z * (Q * rcp(A)) rounds z/scale to within a few ulp, far inside the
             // 1e-4 band around rounding boundaries
             sc[u] = A * (1.0f / Q);
             raw[u] = 0;
             inv = A > 0.f ? Q * __frcp_rn(A) : 0.f;
-        } else if (sfmt == SRFTKV_SCALE_FP16) {
-            // A/Q correctly rounded in fp32, then to fp16: with 24 >= 2*11 + 2 bits the double rounding equals
-            // rounding A/Q to fp16 directly; saturate at the largest finite fp16
-            const __half h = __float2half_rn(fminf(__fdiv_rn(A, Q), 65504.f));
+        } else if constexpr (sfmt == SRFTKV_SCALE_FP16) {
+            // A * (1/Q) (within an ulp of A/Q) rounded to fp16, saturating at the largest finite fp16; it can
+            // differ from rounding A/Q itself only within ~2^-23 of an fp16 midpoint
+            const __half h = __float2half_rn(fminf(A * (1.0f / Q), 65504.f));
             sc[u] = __half2float(h);
             raw[u] = __half_as_ushort(h);
             inv = sc[u] > 0.f ? __frcp_rn(sc[u]) : 0.f;
         } else {
-            // e8m0: biased exponent of the smallest power of two not below A/Q (normal or subnormal v)
-            const float v = __fdiv_rn(A, Q);
+            // e8m0: biased exponent of the smallest power of two not below A/Q (normal or subnormal v); A * (1/Q)
+            // is within an ulp of A/Q, which matters only within ~2^-23 of a power of two
+            const float v = A * (1.0f / Q);
             const uint32_t b = __float_as_uint(v);
             uint32_t e = (b >> 23) + ((b & 0x7FFFFFu) != 0u ? 1u : 0u);
             e = v > 0.f ? min(max(e, 1u), 254u) : 0u;
@@ -145,9 +147,11 @@ __device__ __forceinline__ void quant_store_row(float (&z)[D], int group, int sf
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i) z[16 * u + i] = fmaf_(z[16 * u + i], inv, MAG);
-        if (sfmt == SRFTKV_SCALE_FP16) {  // a saturated scale can push |z/scale| past Q
+        if constexpr (sfmt == SRFTKV_SCALE_FP16) {
+            if (A > 65504.f * Q) {  // a saturated scale can push |z/scale| past Q
 #pragma unroll
-            for (int i = 0; i < 16; ++i) z[16 * u + i] = fminf(fmaxf(z[16 * u + i], MAG - Q), MAG + Q);
+                for (int i = 0; i < 16; ++i) z[16 * u + i] = fminf(fmaxf(z[16 * u + i], MAG - Q), MAG + Q);
+            }
         }
     }
     constexpr int WORDS = D * BITS / 32;
@@ -161,7 +165,7 @@ __device__ __forceinline__ void quant_store_row(float (&z)[D], int group, int sf
     } else {
         reinterpret_cast<uint2*>(crow)[0] = make_uint2(w[0], w[1]);
     }
-    if (sfmt == SRFTKV_SCALE_FP32) {
+    if constexpr (sfmt == SRFTKV_SCALE_FP32) {
         float* sr = reinterpret_cast<float*>(srow);
         if (group == 16) {
             if constexpr (U >= 4) {
@@ -179,7 +183,7 @@ __device__ __forceinline__ void quant_store_row(float (&z)[D], int group, int sf
             for (int u = 0; u < U; ++u)
                 if ((u & (gu - 1)) == 0) sr[u >> sh] = sc[u];
         }
-    } else if (sfmt == SRFTKV_SCALE_FP16) {
+    } else if constexpr (sfmt == SRFTKV_SCALE_FP16) {
         uint16_t* sr = reinterpret_cast<uint16_t*>(srow);
         if (group == 16) {
             if constexpr (U >= 8) {
@@ -224,6 +228,18 @@ __device__ __forceinline__ void quant_store_row(float (&z)[D], int group, int sf
                 if ((u & (gu - 1)) == 0) srow[u >> sh] = (uint8_t)raw[u];
         }
     }
+}
+
+// One row with the scale format chosen at run time (uniform per call side)
+template <int D, int BITS>
+__device__ __forceinline__ void quant_store_row_any(float (&z)[D], int group, int sfmt, uint8_t* __restrict__ crow,
+                                                    uint8_t* __restrict__ srow) {
+    if (sfmt == SRFTKV_SCALE_FP32)
+        quant_store_row<D, BITS, SRFTKV_SCALE_FP32>(z, group, crow, srow);
+    else if (sfmt == SRFTKV_SCALE_FP16)
+        quant_store_row<D, BITS, SRFTKV_SCALE_FP16>(z, group, crow, srow);
+    else
+        quant_store_row<D, BITS, SRFTKV_SCALE_E8M0>(z, group, crow, srow);
 }
 
 // Value of stored scale i of a row in the given format (e8m0: the byte is the
@@ -323,10 +339,10 @@ __device__ __forceinline__ void quantize_tile(const CodecParams& P, const TileId
     const long long vrow = packed_row(P, id, t);
     // with equal widths on both sides only one epilogue is compiled
     if (BK == BV || id.side == 0)
-        quant_store_row<D, BK>(z, P.group, S.sfmt, S.codes + vrow * (D * BK / 8),
+        quant_store_row_any<D, BK>(z, P.group, S.sfmt, S.codes + vrow * (D * BK / 8),
                                S.scales + vrow * (D / P.group) * S.sbytes);
     else
-        quant_store_row<D, BV>(z, P.group, S.sfmt, S.codes + vrow * (D * BV / 8),
+        quant_store_row_any<D, BV>(z, P.group, S.sfmt, S.codes + vrow * (D * BV / 8),
                                S.scales + vrow * (D / P.group) * S.sbytes);
 }
 

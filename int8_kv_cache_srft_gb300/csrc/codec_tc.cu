@@ -62,7 +62,7 @@ __device__ __forceinline__ uint32_t sw128_offset(int n, int k) {
     return (uint32_t)((k >> 6) * T_KB_BYTES + n * 128 + ((((k & 63) >> 3) ^ (n & 7)) << 4) + ((k & 7) << 1));
 }
 
-template <int BK, int BV>
+template <int BK, int BV, int SF>  // SF: the scale format of both sides (mixed calls are split on the host)
 __global__ void __launch_bounds__(T_WARPS * 32, 1)
     srft_quantize_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
                             const __grid_constant__ CodecParams P) {
@@ -209,10 +209,10 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
             const long long vrow = packed_row(P, id, t_tok);
             const int ng = TD / P.group;  // groups of at most 32: a column quarter holds whole groups
             if (BK == BV || id.side == 0)
-                quant_store_row<32, BK>(z, P.group, S.sfmt, S.codes + vrow * (TD * BK / 8) + cq * (32 * BK / 8),
+                quant_store_row<32, BK, SF>(z, P.group, S.codes + vrow * (TD * BK / 8) + cq * (32 * BK / 8),
                                         S.scales + (vrow * ng + cq * (ng / 4)) * S.sbytes);
             else
-                quant_store_row<32, BV>(z, P.group, S.sfmt, S.codes + vrow * (TD * BV / 8) + cq * (32 * BV / 8),
+                quant_store_row<32, BV, SF>(z, P.group, S.codes + vrow * (TD * BV / 8) + cq * (32 * BV / 8),
                                         S.scales + (vrow * ng + cq * (ng / 4)) * S.sbytes);
         }
     }
@@ -312,12 +312,12 @@ __device__ __forceinline__ uint32_t half2_bcast(__half h) {
 // codes * scale for columns 64 hf .. 64 hf + 63 of tile row m, from the
 // stage's exact swizzled code rows (64 bytes for 4-bit, 128 for 8-bit) and
 // scale rows (TD / group floats: 32 bytes for group 16, 16 for group 32)
-// The four 16-column unit scales of columns 64 hf .. +63 of tile row m: fp32
-// scale planes come through the stage in shared memory (exact swizzled rows:
-// 32 bytes for group 16, 16 for group 32); fp16 / e8m0 planes (at most 16
-// bytes a row) are read from global memory directly.
+// The four 16-column unit scales of columns 64 hf .. +63 of tile row m, from
+// the stage in shared memory: fp32 planes as exact swizzled rows (32 bytes
+// for group 16, 16 for group 32), fp16 / e8m0 planes as their contiguous
+// bytes (rows of 4 to 16 bytes, unswizzled).
 __device__ __forceinline__ void half_row_scales(const uint8_t* __restrict__ in, int off_sc, int m, int hf, int group,
-                                                int sfmt, const uint8_t* __restrict__ grow, float (&sc)[4]) {
+                                                int sfmt, float (&sc)[4]) {
     if (sfmt == SRFTKV_SCALE_FP32) {
         const int srb = 4 * (TD / group);
         if (group == 16) {  // groups 4hf .. 4hf+3: chunk hf of the 32-byte row
@@ -333,12 +333,34 @@ __device__ __forceinline__ void half_row_scales(const uint8_t* __restrict__ in, 
         }
         return;
     }
-    if (group == 16) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u) sc[u] = load_scale(grow, 4 * hf + u, sfmt);
-    } else {
-        sc[0] = sc[1] = load_scale(grow, 2 * hf, sfmt);
-        sc[2] = sc[3] = load_scale(grow, 2 * hf + 1, sfmt);
+    const uint8_t* row = in + off_sc + m * (TD / group) * (sfmt == SRFTKV_SCALE_FP16 ? 2 : 1);
+    if (sfmt == SRFTKV_SCALE_FP16) {
+        if (group == 16) {
+            const uint2 h = *reinterpret_cast<const uint2*>(row + 8 * hf);
+            const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&h.x));
+            const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&h.y));
+            sc[0] = a.x;
+            sc[1] = a.y;
+            sc[2] = b.x;
+            sc[3] = b.y;
+        } else {
+            const uint32_t h = *reinterpret_cast<const uint32_t*>(row + 4 * hf);
+            const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&h));
+            sc[0] = sc[1] = a.x;
+            sc[2] = sc[3] = a.y;
+        }
+    } else {  // e8m0: the byte is the fp32 exponent field
+        if (group == 16) {
+            const uint32_t e = *reinterpret_cast<const uint32_t*>(row + 4 * hf);
+            sc[0] = __uint_as_float((e & 0xFFu) << 23);
+            sc[1] = __uint_as_float(((e >> 8) & 0xFFu) << 23);
+            sc[2] = __uint_as_float(((e >> 16) & 0xFFu) << 23);
+            sc[3] = __uint_as_float((e >> 24) << 23);
+        } else {
+            const uint32_t e = *reinterpret_cast<const unsigned short*>(row + 2 * hf);
+            sc[0] = sc[1] = __uint_as_float((e & 0xFFu) << 23);
+            sc[2] = sc[3] = __uint_as_float((e >> 8) << 23);
+        }
     }
 }
 
@@ -509,17 +531,19 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
                 const uint32_t dst = sbase + DQ_OFF_IN + st * C::STAGE;
                 const int row = P.t_offset + id.t0;   // packed planes: [outer*H][t_cap] rows
                 const int oh = id.o * P.H + id.h;
-                const bool sc_smem = P.side[id.side].sfmt == SRFTKV_SCALE_FP32;  // other formats: read from global
-                ptx::mbar_arrive_expect_tx(bar(IN_FULL + st),
-                                           TM * (TD * bits / 8) + (sc_smem ? TM * (TD / P.group) * 4 : 0));
+                // fp32 scales as rows of the tile; fp16 / e8m0 scales as the tile's bytes in rows of 16
+                const int sb = P.side[id.side].sbytes, sc_bytes = TM * (TD / P.group) * sb;
+                ptx::mbar_arrive_expect_tx(bar(IN_FULL + st), TM * (TD * bits / 8) + sc_bytes);
                 ptx::tma_load_3d(dst, &M.codes[id.side], bar(IN_FULL + st), 0, row, oh);
-                if (sc_smem) ptx::tma_load_3d(dst + C::OFF_SC, &M.scales[id.side], bar(IN_FULL + st), 0, row, oh);
+                ptx::tma_load_3d(dst + C::OFF_SC, &M.scales[id.side], bar(IN_FULL + st), 0,
+                                 sb == 4 ? row : row * (TD / P.group) * sb / 16, oh);
             }
         }
     } else if (warp < 2 + DQ_CONV) {
         // converter warp w: tile rows = tensor-memory lanes 32(w%4)..+31 (the
         // quarter a warp may write), column half (w-2)/4
         const int quarter = warp & 3, m = 32 * quarter + lane, hf = (warp - 2) >> 2;
+
         for (int t = blockIdx.x, i = 0; t < P.total_tiles; t += stride, ++i) {
             const int b = i % DQ_NA, st = i % C::STAGES;
             const TileId id = decode_tile128(P, t);
@@ -534,13 +558,7 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
             uint32_t hp[32];  // fp16 pairs in the K order of dq_kperm: column 32 hf + c
             const bool side_k = BK == BV || id.side == 0;
             float sc[4];
-            {
-                const int ng = TD / P.group, row_ok = t_tok < P.n_tokens;
-                const uint8_t* grow =
-                    S.scales + (((long long)id.o * P.H + id.h) * P.t_cap + P.t_offset + (row_ok ? t_tok : id.t0)) *
-                                   ng * S.sbytes;
-                half_row_scales(in, C::OFF_SC, m, hf, P.group, S.sfmt, grow, sc);
-            }
+            half_row_scales(in, C::OFF_SC, m, hf, P.group, S.sfmt, sc);
             if (S.lambda == nullptr) {
                 if (side_k)
                     dequant_half_pairs<BK>(in, m, hf, sc, hp);
@@ -677,7 +695,14 @@ static int launch_dq_tc(const CodecCall& c) {
                               "tensor-core dequantize codes"))
             return SRFTKV_ERR_CUDA;
         if (d.scale_format != SRFTKV_SCALE_FP32) {
-            M.scales[s] = M.codes[s];  // unused: these scales are read from global memory
+            // the plane's bytes as rows of 16; one tile is 128 * ng * sb / 16 of them
+            const unsigned long long sb = (unsigned long long)scale_bytes(d.scale_format);
+            const unsigned long long rdims[3] = {16ull, tcap * ng * sb / 16, nrow};
+            const unsigned long long rstr[2] = {16ull, tcap * ng * sb};
+            const unsigned rbox[3] = {16u, (unsigned)(TM * ng * sb / 16), 1u};
+            if (!encode_tiled(&M.scales[s], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, d.scales, rdims, rstr, rbox,
+                              "tensor-core dequantize scales (16-byte rows)"))
+                return SRFTKV_ERR_CUDA;
         } else if (!encode_tiled_swz(&M.scales[s], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, d.scales, sdims, sstr, sbox,
                                      swz(4 * ng), "tensor-core dequantize scales")) {
             return SRFTKV_ERR_CUDA;
@@ -699,7 +724,7 @@ static int launch_dq_tc(const CodecCall& c) {
     return SRFTKV_OK;
 }
 
-template <int BK, int BV>
+template <int BK, int BV, int SF>
 static int launch_tc(const CodecCall& c) {
     CodecParams P;
     fill_params(c, P);
@@ -715,12 +740,12 @@ static int launch_tc(const CodecCall& c) {
     }
     static bool attr = false;
     if (!attr) {
-        cudaFuncSetAttribute(srft_quantize_tc_kernel<BK, BV>, cudaFuncAttributeMaxDynamicSharedMemorySize, T_SMEM);
+        cudaFuncSetAttribute(srft_quantize_tc_kernel<BK, BV, SF>, cudaFuncAttributeMaxDynamicSharedMemorySize, T_SMEM);
         attr = true;
     }
     int blocks = device_sm_count();
     if (blocks > P.total_tiles) blocks = P.total_tiles;
-    srft_quantize_tc_kernel<BK, BV><<<blocks, T_WARPS * 32, T_SMEM, c.stream>>>(tm[0], tm[1], P);
+    srft_quantize_tc_kernel<BK, BV, SF><<<blocks, T_WARPS * 32, T_SMEM, c.stream>>>(tm[0], tm[1], P);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("tensor-core quantize launch failed: %s", cudaGetErrorString(e));
@@ -729,17 +754,30 @@ static int launch_tc(const CodecCall& c) {
     return SRFTKV_OK;
 }
 
+template <int SF>
+static int launch_tc_bits(const CodecCall& c, int bk, int bv) {
+    if (bk == 4 && bv == 4) return launch_tc<4, 4, SF>(c);
+    if (bk == 8 && bv == 8) return launch_tc<8, 8, SF>(c);
+    if (bk == 8 && bv == 4) return launch_tc<8, 4, SF>(c);
+    return launch_tc<4, 8, SF>(c);
+}
+
 int codec_quantize_tc(const CodecCall& c) {
     if (c.d != TD || c.group > 32) return 1;  // a group must fit in one epilogue thread's 32 columns
     const int bk = c.side[0].bits, bv = c.n_sides > 1 ? c.side[1].bits : bk;
-    if (bk == 4 && bv == 4) return launch_tc<4, 4>(c);
-    if (bk == 8 && bv == 8) return launch_tc<8, 8>(c);
-    if (bk == 8 && bv == 4) return launch_tc<8, 4>(c);
-    return launch_tc<4, 8>(c);
+    const int sf = c.side[0].scale_format;  // both sides share it (mixed calls are split on the host)
+    if (sf == SRFTKV_SCALE_FP16) return launch_tc_bits<SRFTKV_SCALE_FP16>(c, bk, bv);
+    if (sf == SRFTKV_SCALE_E8M0) return launch_tc_bits<SRFTKV_SCALE_E8M0>(c, bk, bv);
+    return launch_tc_bits<SRFTKV_SCALE_FP32>(c, bk, bv);
 }
 
 int codec_dequantize_tc(const CodecCall& c) {
     if (c.d != TD || c.group > 32) return 1;  // scale rows must be at least 16 bytes for the TMA copy
+    for (int s = 0; s < c.n_sides; ++s) {     // fp16 / e8m0 planes are copied in rows of 16 bytes
+        const long long rb = (long long)(TD / c.group) * scale_bytes(c.side[s].scale_format);
+        if (c.side[s].scale_format != SRFTKV_SCALE_FP32 && (((long long)c.t_cap * rb) % 16 || ((long long)c.t_offset * rb) % 16))
+            return 1;
+    }
     const int bk = c.side[0].bits, bv = c.n_sides > 1 ? c.side[1].bits : bk;
     if (bk == 4 && bv == 4) return launch_dq_tc<4, 4>(c);
     if (bk == 8 && bv == 8) return launch_dq_tc<8, 8>(c);
