@@ -102,6 +102,24 @@ def recorded_traffic(kernel: str):
     return float(ent["dram_bytes_per_launch"])
 
 
+def max_over_ranks(ms: float, device=None) -> float:
+    """The slowest rank's time: an all-reduce (MAX) over the default process group when one is initialised
+    (NCCL on the GPUs, or any backend for the given device), else ms itself."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world: int, units_per_rank: int, ms_per_step: float) -> float:
+    """Whole-job throughput under weak scaling: every rank processes units_per_rank per step."""
+    return world * units_per_rank / (ms_per_step * 1e-3)
+
+
 class ClockSampler:
     """nvidia-smi clock and throttle-reason samples during the timed region."""
 
@@ -286,12 +304,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     clk = clocks.stop()
     barrier()
     ms_total = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, dev)
     ms_step = ms_total / args.steps
-    value = world * n_vec / (ms_step * 1e-3)
+    value = job_value(world, n_vec, ms_step)
 
     # variants of the cache format on the same workload and kernels (outside the timed step): the Hadamard
     # rotation, and fp16 / e8m0 scale planes; each timed as the median of 10 launches with CUDA events on the
@@ -363,8 +378,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             hout.copy_(out, non_blocking=True)
         b.record(stream)
         torch.cuda.synchronize()
-        ms_e2e = a.elapsed_time(b) / args.e2e_steps
-        e2e = {"value": world * n_vec / (ms_e2e * 1e-3), "unit": "KV vectors/s", "h2d_bytes_per_step": h2d,
+        ms_e2e = max_over_ranks(a.elapsed_time(b) / args.e2e_steps, dev)
+        e2e = {"value": job_value(world, n_vec, ms_e2e), "unit": "KV vectors/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e}
 
     if rank != 0:
