@@ -159,7 +159,11 @@ int srft_kv_dequantize(const srftkv_side* k, const srftkv_side* v, int n_outer, 
  * Requires d in {64, 128, 256}, Hq % Hkv == 0 and Hq/Hkv <= 4, and for
  * packed sides a power-of-two group with 16 <= group <= d/4 (a scale row of
  * at least 16 bytes, the smallest TMA row) and 16-byte aligned scales;
- * anything else returns SRFTKV_ERR_INVALID before any launch.
+ * anything else returns SRFTKV_ERR_INVALID before any launch.  fp16 / e8m0
+ * scale planes also need t_cap * (d/group) * (2 or 1) to be a multiple of 16.
+ * Range: the kernel forms p * scale_V in fp16 with p in (0, 256], so value
+ * scales must stay below 255 (|z_V| < 1785 for 4-bit values, < 32385 for
+ * 8-bit); larger V scales overflow to inf.  Key scales have no such limit.
  */
 int q4kv_decode_attention(const void* q, float* out, const srftkv_side* k, const srftkv_side* v,
                           int B, int Hq, int Hkv, int d, int group, int t_cap,

@@ -133,3 +133,21 @@ def test_srht_transform_rejects_bad_arguments(lib):
     assert lib.srht_transform(16, 16, 4, 48, 1, 0, None) == K.SRFTKV_ERR_INVALID
     assert lib.srht_transform(None, 16, 4, 64, 1, 0, None) == K.SRFTKV_ERR_INVALID
     assert lib.srht_transform(16, 16, 0, 64, 1, 0, None) == K.SRFTKV_OK
+
+
+def test_attention_format_rules(lib):
+    e8 = _side()
+    e8.scale_format = 2  # e8m0: 8 bytes of scales a token at d=128, group 16 -> t_cap must be even
+    assert _attn(lib, e8, _side(), t_cap=63) == K.SRFTKV_ERR_INVALID
+    assert b"multiple of 16" in lib.srftkv_last_error()
+    bad = _side()
+    bad.scale_format = 3
+    assert _attn(lib, _side(), bad) == K.SRFTKV_ERR_INVALID
+    bad_t = _side()
+    bad_t.transform = 5
+    assert _attn(lib, bad_t, _side()) == K.SRFTKV_ERR_INVALID
+    assert _attn(lib, _side(scales=20), _side()) == K.SRFTKV_ERR_INVALID  # scales not 16-byte aligned
+
+
+def test_attention_empty_batch_is_a_no_op(lib):
+    assert _attn(lib, _side(), _side(), B=0) == K.SRFTKV_OK
