@@ -67,6 +67,10 @@ notes; the CUDA path implements the same readings independently):
    A zero group stores scale 0 (byte 0 for e8m0) and codes 0 in both.
    With int4 codes and groups of 16 this is 80 (fp16) and 72 (e8m0) bytes
    per d = 128 vector against 256 in fp16: 3.2x and 3.56x.
+10. Head dimensions that are not powers of two ([WQF] Methodology 1: the
+   SRFT's reason for being over the SRHT): the definitions above hold for
+   any even d (the DFT has no power-of-two requirement; Hermitian packing
+   needs d even).  The Hadamard variant stays power-of-two only.
 """
 
 from __future__ import annotations
@@ -111,8 +115,15 @@ def sign_vector(d: int, seed: int) -> np.ndarray:
 # --------------------------------------------------------------------------
 
 def _check_d(d: int) -> None:
+    """The SRFT needs an even d >= 4 (reading 10: [WQF] Methodology 1 credits the SRFT with handling
+    dimensions that are not powers of two); the Hadamard variant needs a power of two."""
+    if d < 4 or d % 2:
+        raise ValueError(f"d must be even and >= 4, got {d}")
+
+
+def _check_pow2(d: int) -> None:
     if d < 4 or d & (d - 1):
-        raise ValueError(f"d must be a power of two >= 4, got {d}")
+        raise ValueError(f"the Hadamard variant needs a power of two d >= 4, got {d}")
 
 
 def dft_half_matrix(d: int) -> np.ndarray:
@@ -194,7 +205,7 @@ def srft_matrix(d: int, seed: int) -> np.ndarray:
 def hadamard_matrix(d: int) -> np.ndarray:
     """Sylvester Hadamard matrix of order d (a power of two), natural order:
     H_ij = (-1)^popcount(i & j)."""
-    _check_d(d)
+    _check_pow2(d)
     i = np.arange(d)
     parity = np.array([[bin(a & b).count("1") & 1 for b in i] for a in i])
     return np.where(parity == 1, -1.0, 1.0)

@@ -21,6 +21,8 @@ from oracle import srft_oracle as O
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 DIMS = (4, 8, 16, 32, 64, 128, 256)
+ODD_DIMS = (6, 12, 80, 96, 192)  # even, not powers of two (reading 10)
+POW2 = DIMS
 
 
 # ---------------------------------------------------------------- sign vector
@@ -59,7 +61,7 @@ def check_unitarity(o, d, seed=7):
     assert abs(px @ py - x @ y) < 1e-12 * np.linalg.norm(x) * np.linalg.norm(y)
 
 
-@pytest.mark.parametrize("d", DIMS)
+@pytest.mark.parametrize("d", DIMS + ODD_DIMS)
 def test_unitarity(d):
     check_unitarity(O, d)
 
@@ -76,7 +78,7 @@ def check_basis_closed_form(o, d, seed=11):
         assert np.abs(R[:, j] - s[j] * np.array(col)).max() < 1e-13
 
 
-@pytest.mark.parametrize("d", (4, 8, 16, 64))
+@pytest.mark.parametrize("d", (4, 8, 16, 64, 6, 12, 96))
 def test_basis_vectors_closed_form(d):
     check_basis_closed_form(O, d)
 
@@ -120,12 +122,12 @@ def check_matches_numpy_fft(o, d, seed=3):
     assert np.abs(o.srft_forward(x, seed) - want).max() < 1e-12
 
 
-@pytest.mark.parametrize("d", DIMS)
+@pytest.mark.parametrize("d", DIMS + ODD_DIMS)
 def test_matches_numpy_fft(d):
     check_matches_numpy_fft(O, d)
 
 
-@pytest.mark.parametrize("d", DIMS)
+@pytest.mark.parametrize("d", DIMS + ODD_DIMS)
 def test_exact_round_trip_and_numpy_inverse(d):
     rng = np.random.default_rng(d)
     x = rng.standard_normal((5, d))
@@ -338,6 +340,23 @@ def test_kvsplit_k8v4_formula_and_compression_ratio():
     assert round(ratio, 2) == gl["compression"]["max_ratio"]
 
 
+def test_non_power_of_two_d6_by_hand():
+    """d = 6: the 3 + 1 bins of a real length-6 DFT, packed, from explicit complex sums."""
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal(6)
+    s = O.sign_vector(6, 2)
+    u = x * s
+    y = [sum(u[n] * cmath.exp(-2j * math.pi * n * k / 6) for n in range(6)) / math.sqrt(6) for k in range(4)]
+    want = [y[0].real, y[3].real, math.sqrt(2) * y[1].real, math.sqrt(2) * y[1].imag, math.sqrt(2) * y[2].real,
+            math.sqrt(2) * y[2].imag]
+    assert np.abs(O.srft_forward(x, 2) - np.array(want)).max() < 1e-13
+
+
+def test_hadamard_rejects_non_power_of_two():
+    with pytest.raises(ValueError):
+        O.hadamard_matrix(96)
+
+
 # ---------------------------------------------------------------- Hadamard variant (SRHT)
 
 def check_hadamard_matches_scipy(o, d):
@@ -346,7 +365,7 @@ def check_hadamard_matches_scipy(o, d):
     assert np.array_equal(o.hadamard_matrix(d), scipy_linalg.hadamard(d).astype(np.float64))
 
 
-@pytest.mark.parametrize("d", DIMS)
+@pytest.mark.parametrize("d", POW2)
 def test_hadamard_matches_scipy(d):
     check_hadamard_matches_scipy(O, d)
 
