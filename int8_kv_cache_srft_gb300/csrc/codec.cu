@@ -155,9 +155,23 @@ static bool split_mixed(const CodecCall& c, int (*fn)(const CodecCall&), int& rc
     return true;
 }
 
+// d = 96 runs only as the tensor-core contraction padded to 128 (the
+// register FFT is built for powers of two)
+static int tc_only(const CodecCall& c, int (*fn)(const CodecCall&), const char* what) {
+    const int rc = fn(c);
+    if (rc == 1) {
+        set_error("%s at d = %d needs groups of 16 or 32 and, for dequantize, t_cap and t_offset such that "
+                  "t_cap * (d / group) * scale bytes and t_offset * (d / group) * scale bytes are multiples of 16",
+                  what, c.d);
+        return SRFTKV_ERR_INVALID;
+    }
+    return rc;
+}
+
 int codec_quantize(const CodecCall& c) {
     int split_rc = 0;
     if (split_mixed(c, codec_quantize, split_rc)) return split_rc;
+    if (c.d == 96) return tc_only(c, codec_quantize_tc, "quantize");
     const int ov = quant_path_override();
     const long long rows = (long long)c.n_sides * c.n_outer * c.n_tokens * c.H;
     if (ov == 2 || (ov == 0 && rows >= 64ll * 1024)) {
@@ -169,6 +183,7 @@ int codec_quantize(const CodecCall& c) {
 int codec_dequantize(const CodecCall& c) {
     int split_rc = 0;
     if (split_mixed(c, codec_dequantize, split_rc)) return split_rc;
+    if (c.d == 96) return tc_only(c, codec_dequantize_tc, "dequantize");
     const int ov = quant_path_override();
     const long long rows = (long long)c.n_sides * c.n_outer * c.n_tokens * c.H;
     if (ov == 2 || (ov == 0 && rows >= 64ll * 1024)) {
@@ -196,8 +211,78 @@ static int launch_transform(const void* x, float* y, int n, uint64_t seed, bool 
     return 0;
 }
 
+// ---------------------------------------------------------------------------
+// The bare SRFT at a head dimension that is not a power of two (d = 96) as the
+// dense real map p = R diag(s) x of the packed unitary DFT: R[0][k] = d^-1/2,
+// R[1][k] = (-1)^k d^-1/2, and for 1 <= j < d/2 R[2j][k] = sqrt(2/d) cos(2 pi jk/d),
+// R[2j+1][k] = -sqrt(2/d) sin(2 pi jk/d); the inverse is diag(s) R^T.  A block
+// takes four rows at a time, one thread per output coordinate, with the
+// angles from a table of cos / sin(2 pi m/d) evaluated in double.
+// ---------------------------------------------------------------------------
+constexpr int DT_ROWS = 4, DT_MAXD = 128;
+
+__global__ void __launch_bounds__(128) srft_dense_transform_kernel(const __half* __restrict__ x, float* __restrict__ y,
+                                                                   int n, int d, const __grid_constant__ SignParams S,
+                                                                   int inverse) {
+    __shared__ float cs[DT_MAXD], sn[DT_MAXD], xs[DT_ROWS][DT_MAXD];
+    for (int m = threadIdx.x; m < d; m += blockDim.x) {
+        double sv, cv;
+        sincospi(2.0 * m / d, &sv, &cv);
+        cs[m] = (float)cv;
+        sn[m] = (float)sv;
+    }
+    const float isd = (float)(1.0 / sqrt((double)d)), r2 = (float)sqrt(2.0 / d);
+    auto neg = [&](int k) { return (S.w[k >> 1] & ((k & 1) ? 0x80000000u : 0x8000u)) != 0u; };
+    auto R = [&](int row, int k) {
+        if (row == 0) return isd;
+        if (row == 1) return (k & 1) ? -isd : isd;
+        const int m = ((row >> 1) * k) % d;
+        return (row & 1) ? -r2 * sn[m] : r2 * cs[m];
+    };
+    for (long long r0 = (long long)blockIdx.x * DT_ROWS; r0 < n; r0 += (long long)gridDim.x * DT_ROWS) {
+        __syncthreads();
+        for (int i = threadIdx.x; i < DT_ROWS * d; i += blockDim.x) {
+            const int v = i / d, k = i % d;
+            const long long r = r0 + v;
+            float val = r < n ? __half2float(x[r * d + k]) : 0.f;
+            if (!inverse && neg(k)) val = -val;
+            xs[v][k] = val;
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < DT_ROWS * d; i += blockDim.x) {
+            const int v = i / d, o = i % d;
+            const long long r = r0 + v;
+            if (r >= n) continue;
+            float acc = 0.f;
+            if (!inverse) {
+                for (int k = 0; k < d; ++k) acc = fmaf(R(o, k), xs[v][k], acc);
+            } else {
+                for (int k = 0; k < d; ++k) acc = fmaf(R(k, o), xs[v][k], acc);
+                if (neg(o)) acc = -acc;
+            }
+            y[r * d + o] = acc;
+        }
+    }
+}
+
+static int launch_dense_transform(const void* x, float* y, int n, int d, uint64_t seed, bool inverse, cudaStream_t s) {
+    SignParams S;
+    for (int i = 0; i < 128; ++i) S.w[i] = 0;
+    sign_masks(d, seed, S.w);
+    long long blocks = ((long long)n + DT_ROWS - 1) / DT_ROWS;
+    if (blocks > 152 * 8) blocks = 152 * 8;
+    srft_dense_transform_kernel<<<(int)blocks, 128, 0, s>>>(static_cast<const __half*>(x), y, n, d, S, inverse ? 1 : 0);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("transform kernel launch failed: %s", cudaGetErrorString(e));
+        return SRFTKV_ERR_CUDA;
+    }
+    return 0;
+}
+
 int transform_launch(const void* x, float* y, int n, int d, uint64_t seed, bool inverse, bool srht, cudaStream_t s) {
     if (n == 0) return 0;
+    if (d == 96 && !srht) return launch_dense_transform(x, y, n, d, seed, inverse, s);
     switch (d) {
         case 16: return launch_transform<16>(x, y, n, seed, inverse, srht, s);
         case 32: return launch_transform<32>(x, y, n, seed, inverse, srht, s);

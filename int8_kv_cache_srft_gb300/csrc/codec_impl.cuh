@@ -42,6 +42,7 @@ struct CodecParams {
     CodecSideK side[2];
     int n_outer, H, t_cap, t_offset, group;
     int n_tokens;
+    int d;                // head dimension (the tensor-core kernels pad d < 128 to their 128-wide tiles)
     int tiles_per_head;   // ceil(n_tokens / rows per tile)
     int tiles_per_side;   // n_outer * H * tiles_per_head
     int total_tiles;      // n_sides * tiles_per_side
@@ -497,6 +498,7 @@ static inline void fill_params(const CodecCall& c, CodecParams& P) {
     P.t_offset = c.t_offset;
     P.group = c.group;
     P.n_tokens = c.n_tokens;
+    P.d = c.d;
     P.tiles_per_head = (c.n_tokens + 31) / 32;
     P.tiles_per_side = c.n_outer * c.H * P.tiles_per_head;
     P.total_tiles = c.n_sides * P.tiles_per_side;

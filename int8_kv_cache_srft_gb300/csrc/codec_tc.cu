@@ -55,6 +55,31 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 
 __device__ __forceinline__ TileId decode_tile128(const CodecParams& P, int t) { return decode_tile<TM>(P, t); }
 
+// Entry (n, k) of the forward transform R for head dimension dv <= 128 (p = R x,
+// n the packed output coordinate, k the input coordinate), before the sign of
+// input k; zero outside dv x dv, so a smaller head dimension runs as the
+// 128-wide contraction padded with zeros.  dv = 128 takes the compile-time
+// twiddle table; other (even) dv the angle 2 pi (jk mod dv)/dv in double.
+__device__ float r_entry(int n, int k, int dv, bool srht) {
+    if (n >= dv || k >= dv) return 0.f;
+    if (dv == TD) {
+        constexpr float inv_sqrt_d = 0.08838834764831845f;  // 1/sqrt(128)
+        constexpr float c2 = 0.125f;                        // sqrt(2/128)
+        if (srht) return (__popc(n & k) & 1) ? -inv_sqrt_d : inv_sqrt_d;  // Hadamard entry / sqrt(d)
+        if (n == 0) return inv_sqrt_d;
+        if (n == 1) return (k & 1) ? -inv_sqrt_d : inv_sqrt_d;
+        const int m = (((n >> 1) * k) & (TD - 1)) * (256 / TD);  // angle 2 pi (jk mod d)/d on the 256-point table
+        return (n & 1) ? c2 * tw_im(m) : c2 * tw_re(m);             // tw_im holds -sin
+    }
+    const double isd = 1.0 / sqrt((double)dv);
+    if (n == 0) return (float)isd;
+    if (n == 1) return (float)((k & 1) ? -isd : isd);
+    const int m = ((n >> 1) * k) % dv;
+    double sn, cs;
+    sincospi(2.0 * m / dv, &sn, &cs);
+    return (float)((n & 1) ? -sqrt(2.0) * isd * sn : sqrt(2.0) * isd * cs);
+}
+
 // Byte offset of element (row n, column k) of a 128 x 128 fp16 operand stored
 // K-major in two 128-byte-swizzled k-blocks (the layout TMA's 128-byte swizzle
 // produces and the MMA descriptors below describe).
@@ -81,22 +106,10 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
     // ---- R_s = R diag(s), split into fp16 hi + lo, in the MMA operand layout ----
     // (both sides of a launch share the transform; mixed calls are split on the host)
     {
-        constexpr float inv_sqrt_d = 0.08838834764831845f;  // 1/sqrt(128)
-        constexpr float c2 = 0.125f;                        // sqrt(2/128)
         const bool srht = P.side[0].transform == SRFTKV_TRANSFORM_SRHT;
         for (int idx = threadIdx.x; idx < TD * TD; idx += blockDim.x) {
             const int n = idx >> 7, k = idx & 127;
-            float v;
-            if (srht) {
-                v = (__popc(n & k) & 1) ? -inv_sqrt_d : inv_sqrt_d;  // Hadamard entry / sqrt(d)
-            } else if (n == 0) {
-                v = inv_sqrt_d;
-            } else if (n == 1) {
-                v = (k & 1) ? -inv_sqrt_d : inv_sqrt_d;
-            } else {
-                const int m = (((n >> 1) * k) & (TD - 1)) * (256 / TD);  // angle 2 pi (jk mod d)/d on the 256-point table
-                v = (n & 1) ? c2 * tw_im(m) : c2 * tw_re(m);             // tw_im holds -sin
-            }
+            float v = r_entry(n, k, P.d, srht);
             const uint32_t sbit = (k & 1) ? 0x80000000u : 0x8000u;
             if (P.sign_mask[k >> 1] & sbit) v = -v;
             const __half hi = __float2half_rn(v);
@@ -190,13 +203,13 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
             const TileId id = decode_tile128(P, t);
             const CodecSideK& S = P.side[id.side];
             const int t_tok = id.t0 + 32 * quarter + lane;
-            if (t_tok >= P.n_tokens) continue;
+            if (t_tok >= P.n_tokens || 32 * cq >= P.d) continue;
             float z[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) z[j] = __uint_as_float(r0[j]);
             if (S.lambda != nullptr) {
                 const float4* lr = reinterpret_cast<const float4*>(
-                    S.lambda + (long long)id.o * S.lambda_outer_stride + (long long)id.h * TD + cq * 32);
+                    S.lambda + (long long)id.o * S.lambda_outer_stride + (long long)id.h * P.d + cq * 32);
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     const float4 l = __ldg(lr + c);
@@ -207,13 +220,14 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
                 }
             }
             const long long vrow = packed_row(P, id, t_tok);
-            const int ng = TD / P.group;  // groups of at most 32: a column quarter holds whole groups
+            // groups of at most 32: a column quarter holds whole groups; quarters past d hold padding
+            const int ng = P.d / P.group;
             if (BK == BV || id.side == 0)
-                quant_store_row<32, BK, SF>(z, P.group, S.codes + vrow * (TD * BK / 8) + cq * (32 * BK / 8),
-                                        S.scales + (vrow * ng + cq * (ng / 4)) * S.sbytes);
+                quant_store_row<32, BK, SF>(z, P.group, S.codes + vrow * (P.d * BK / 8) + cq * (32 * BK / 8),
+                                            S.scales + (vrow * ng + cq * (32 / P.group)) * S.sbytes);
             else
-                quant_store_row<32, BV, SF>(z, P.group, S.codes + vrow * (TD * BV / 8) + cq * (32 * BV / 8),
-                                        S.scales + (vrow * ng + cq * (ng / 4)) * S.sbytes);
+                quant_store_row<32, BV, SF>(z, P.group, S.codes + vrow * (P.d * BV / 8) + cq * (32 * BV / 8),
+                                            S.scales + (vrow * ng + cq * (32 / P.group)) * S.sbytes);
         }
     }
     if (failed) atomicOr(P.fault, 1u);
@@ -266,7 +280,9 @@ struct DqCfg {
 };
 // 16-byte chunk c of row r of a buffer of RB-byte rows written by TMA with the
 // swizzle mode equal to RB (32, 64 or 128; 16 = no swizzle), 1024-aligned
-__device__ __forceinline__ int swz16(int rb, int r, int c) { return rb >= 32 ? c ^ (((r * rb) >> 7) & (rb / 16 - 1)) : c; }
+__device__ __forceinline__ int swz16(int rb, int r, int c) {
+    return (rb == 32 || rb == 64 || rb == 128) ? c ^ (((r * rb) >> 7) & (rb / 16 - 1)) : c;
+}
 
 // K order of the dequantize contraction.  A column c = 4k + j (k: 8-element
 // code word, j = 0..3) holds the packed coordinates (8k + j, 8k + j + 4): those
@@ -317,7 +333,23 @@ __device__ __forceinline__ uint32_t half2_bcast(__half h) {
 // for group 16, 16 for group 32), fp16 / e8m0 planes as their contiguous
 // bytes (rows of 4 to 16 bytes, unswizzled).
 __device__ __forceinline__ void half_row_scales(const uint8_t* __restrict__ in, int off_sc, int m, int hf, int group,
-                                                int sfmt, float (&sc)[4]) {
+                                                int sfmt, int d, float (&sc)[4]) {
+    if (d != TD) {  // smaller head dimension: unswizzled rows of d/group scales; units past d read as 0
+        const int ng = d / group, sb = sfmt == SRFTKV_SCALE_FP32 ? 4 : sfmt == SRFTKV_SCALE_FP16 ? 2 : 1;
+        const uint8_t* row = in + off_sc + m * ng * sb;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int col = 64 * hf + 16 * u, gi = col / group;
+            float v = 0.f;
+            if (col < d) {
+                if (sfmt == SRFTKV_SCALE_FP32) v = *reinterpret_cast<const float*>(row + 4 * gi);
+                else if (sfmt == SRFTKV_SCALE_FP16) v = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(row + 2 * gi)));
+                else v = __uint_as_float((uint32_t)row[gi] << 23);
+            }
+            sc[u] = v;
+        }
+        return;
+    }
     if (sfmt == SRFTKV_SCALE_FP32) {
         const int srb = 4 * (TD / group);
         if (group == 16) {  // groups 4hf .. 4hf+3: chunk hf of the 32-byte row
@@ -364,19 +396,29 @@ __device__ __forceinline__ void half_row_scales(const uint8_t* __restrict__ in, 
     }
 }
 
-template <int BITS>
-__device__ __forceinline__ void dequant_half_smem(const uint8_t* __restrict__ in, int m, int hf, const float (&sc)[4],
-                                                  float (&p)[64]) {
-    constexpr int RB = TD * BITS / 8, NCH = 64 * BITS / 128, PER = 32 / BITS;  // chunks per half row
-    uint32_t w[4 * NCH];
+// The 16-byte code chunks of half hf of tile row m (rows of DV*BITS/8 bytes;
+// chunks past the row, the zero padding of DV < 128, read as zero codes)
+template <int BITS, int DV, int NCH>
+__device__ __forceinline__ void load_half_codes(const uint8_t* __restrict__ in, int m, int hf, uint32_t (&w)[4 * NCH]) {
+    constexpr int RB = DV * BITS / 8;
 #pragma unroll
     for (int k = 0; k < NCH; ++k) {
-        const uint4 v = *reinterpret_cast<const uint4*>(in + m * RB + (swz16(RB, m, NCH * hf + k) << 4));
+        const int c = NCH * hf + k;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (DV == TD || 16 * c < RB) v = *reinterpret_cast<const uint4*>(in + m * RB + (swz16(RB, m, c) << 4));
         w[4 * k] = v.x;
         w[4 * k + 1] = v.y;
         w[4 * k + 2] = v.z;
         w[4 * k + 3] = v.w;
     }
+}
+
+template <int BITS, int DV>
+__device__ __forceinline__ void dequant_half_smem(const uint8_t* __restrict__ in, int m, int hf, const float (&sc)[4],
+                                                  float (&p)[64]) {
+    constexpr int NCH = 64 * BITS / 128, PER = 32 / BITS;  // chunks per half row
+    uint32_t w[4 * NCH];
+    load_half_codes<BITS, DV, NCH>(in, m, hf, w);
 #pragma unroll
     for (int i = 0; i < 64; ++i) {
         const float c = (BITS == 4) ? code_int4(w[i / PER], i % PER) : code_int8(w[i / PER], i % PER);
@@ -388,19 +430,12 @@ __device__ __forceinline__ void dequant_half_smem(const uint8_t* __restrict__ in
 // K order of dq_kperm (no lambda): codes -> exact fp16 pairs -> times the
 // group scale split into fp16 hi + lo, P_hat = fp16(q s_hi + fp16(q s_lo)), one
 // main rounding as when the fp32 product q s is rounded to fp16.
-template <int BITS>
+template <int BITS, int DV>
 __device__ __forceinline__ void dequant_half_pairs(const uint8_t* __restrict__ in, int m, int hf, const float (&sc)[4],
                                                    uint32_t (&hp)[32]) {
-    constexpr int RB = TD * BITS / 8, NCH = 64 * BITS / 128;
+    constexpr int NCH = 64 * BITS / 128;
     uint32_t w[4 * NCH];
-#pragma unroll
-    for (int k = 0; k < NCH; ++k) {
-        const uint4 v = *reinterpret_cast<const uint4*>(in + m * RB + (swz16(RB, m, NCH * hf + k) << 4));
-        w[4 * k] = v.x;
-        w[4 * k + 1] = v.y;
-        w[4 * k + 2] = v.z;
-        w[4 * k + 3] = v.w;
-    }
+    load_half_codes<BITS, DV, NCH>(in, m, hf, w);
     uint32_t sh[4], sl[4];
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
@@ -431,7 +466,7 @@ struct DqMaps {
     CUtensorMap out[2], codes[2], scales[2];
 };
 
-template <int BK, int BV>
+template <int BK, int BV, int DV>  // DV: head dimension, 128 or a smaller one padded to the 128-wide tile
 __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
     srft_dequantize_tc_kernel(const __grid_constant__ DqMaps M, const __grid_constant__ CodecParams P) {
     using C = DqCfg<BK, BV>;
@@ -448,24 +483,12 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
     static_assert(C::STAGES <= 4, "input stages");
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[18]);
 
-    {  // B[k][n] = s_k R[n][k], hi and lo
-        constexpr float inv_sqrt_d = 0.08838834764831845f;
-        constexpr float c2 = 0.125f;
+    {  // B[k][q] = s_k R[n][k] with n = dq_kperm(q) (zero outside d x d)
         const bool srht = P.side[0].transform == SRFTKV_TRANSFORM_SRHT;
         for (int idx = threadIdx.x; idx < TD * TD; idx += blockDim.x) {
             // B row k (output coordinate), K position q holding packed coordinate n
             const int k = idx >> 7, q = idx & 127, n = dq_kperm(q);
-            float v;
-            if (srht) {
-                v = (__popc(n & k) & 1) ? -inv_sqrt_d : inv_sqrt_d;
-            } else if (n == 0) {
-                v = inv_sqrt_d;
-            } else if (n == 1) {
-                v = (k & 1) ? -inv_sqrt_d : inv_sqrt_d;
-            } else {
-                const int m = (((n >> 1) * k) & (TD - 1)) * (256 / TD);
-                v = (n & 1) ? c2 * tw_im(m) : c2 * tw_re(m);
-            }
+            float v = r_entry(n, k, DV, srht);
             if (P.sign_mask[k >> 1] & ((k & 1) ? 0x80000000u : 0x8000u)) v = -v;
             *reinterpret_cast<__half*>(smem + sw128_offset(k, q)) = __float2half_rn(v);
         }
@@ -532,11 +555,12 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
                 const int row = P.t_offset + id.t0;   // packed planes: [outer*H][t_cap] rows
                 const int oh = id.o * P.H + id.h;
                 // fp32 scales as rows of the tile; fp16 / e8m0 scales as the tile's bytes in rows of 16
-                const int sb = P.side[id.side].sbytes, sc_bytes = TM * (TD / P.group) * sb;
-                ptx::mbar_arrive_expect_tx(bar(IN_FULL + st), TM * (TD * bits / 8) + sc_bytes);
+                const int sb = P.side[id.side].sbytes, ng = DV / P.group, sc_bytes = TM * ng * sb;
+                const bool flat = !(sb == 4 && DV == TD);  // scale rows copied as 16-byte rows of bytes
+                ptx::mbar_arrive_expect_tx(bar(IN_FULL + st), TM * (DV * bits / 8) + sc_bytes);
                 ptx::tma_load_3d(dst, &M.codes[id.side], bar(IN_FULL + st), 0, row, oh);
                 ptx::tma_load_3d(dst + C::OFF_SC, &M.scales[id.side], bar(IN_FULL + st), 0,
-                                 sb == 4 ? row : row * (TD / P.group) * sb / 16, oh);
+                                 flat ? row * ng * sb / 16 : row, oh);
             }
         }
     } else if (warp < 2 + DQ_CONV) {
@@ -558,27 +582,28 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
             uint32_t hp[32];  // fp16 pairs in the K order of dq_kperm: column 32 hf + c
             const bool side_k = BK == BV || id.side == 0;
             float sc[4];
-            half_row_scales(in, C::OFF_SC, m, hf, P.group, S.sfmt, sc);
+            half_row_scales(in, C::OFF_SC, m, hf, P.group, S.sfmt, DV, sc);
             if (S.lambda == nullptr) {
                 if (side_k)
-                    dequant_half_pairs<BK>(in, m, hf, sc, hp);
+                    dequant_half_pairs<BK, DV>(in, m, hf, sc, hp);
                 else
-                    dequant_half_pairs<BV>(in, m, hf, sc, hp);
+                    dequant_half_pairs<BV, DV>(in, m, hf, sc, hp);
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar(IN_EMPTY + st));  // input stage consumed
             } else {
                 float p[64];
                 if (side_k)
-                    dequant_half_smem<BK>(in, m, hf, sc, p);
+                    dequant_half_smem<BK, DV>(in, m, hf, sc, p);
                 else
-                    dequant_half_smem<BV>(in, m, hf, sc, p);
+                    dequant_half_smem<BV, DV>(in, m, hf, sc, p);
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar(IN_EMPTY + st));  // input stage consumed
                 if (t_tok < P.n_tokens) {
                     const float4* lr = reinterpret_cast<const float4*>(
-                        S.lambda + (long long)id.o * S.lambda_outer_stride + (long long)id.h * TD + 64 * hf);
+                        S.lambda + (long long)id.o * S.lambda_outer_stride + (long long)id.h * DV + 64 * hf);
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
+                        if (DV != TD && 64 * hf + 4 * c >= DV) break;  // padding columns: p is already 0
                         const float4 l = __ldg(lr + c);
                         p[4 * c] = __fdividef(p[4 * c], l.x);
                         p[4 * c + 1] = __fdividef(p[4 * c + 1], l.y);
@@ -659,7 +684,7 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
     if (warp == 0) tc::tmem_dealloc(tmem, DQ_TMEM_COLS);
 }
 
-template <int BK, int BV>
+template <int BK, int BV, int DV>
 static int launch_dq_tc(const CodecCall& c) {
     using C = DqCfg<BK, BV>;
     CodecParams P;
@@ -671,13 +696,14 @@ static int launch_dq_tc(const CodecCall& c) {
     if (!P.fault) return SRFTKV_ERR_CUDA;
     DqMaps M;
     const unsigned long long tcap = (unsigned long long)c.t_cap, nrow = (unsigned long long)c.n_outer * c.H;
-    const int ng = TD / c.group;
+    const int ng = DV / c.group;
     for (int s = 0; s < 2; ++s) {
         const CodecSideDesc& d = c.side[s < c.n_sides ? s : 0];
-        const int rb = TD * d.bits / 8;
+        const int rb = DV * d.bits / 8;
         // packed planes [n_outer*H][t_cap][row], copied as exact rows with the
         // swizzle mode equal to the row length (64/128-byte code rows, 32-byte
-        // group-16 scale rows; 16-byte group-32 scale rows unswizzled)
+        // group-16 scale rows; 16-byte group-32 scale rows and the 48/96-byte
+        // code rows of d = 96 unswizzled)
         auto swz = [](int bytes) {
             return bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                    : bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
@@ -690,11 +716,11 @@ static int launch_dq_tc(const CodecCall& c) {
         const unsigned long long sdims[3] = {(unsigned long long)ng, tcap, nrow};
         const unsigned long long sstr[2] = {ng * 4ull, tcap * ng * 4ull};
         const unsigned sbox[3] = {(unsigned)ng, (unsigned)TM, 1u};
-        if (!encode_x_map(&M.out[s], d.x, TD, c.H, c.n_tokens, c.n_outer, TM, true) ||
+        if (!encode_x_map(&M.out[s], d.x, DV, c.H, c.n_tokens, c.n_outer, TM, true) ||
             !encode_tiled_swz(&M.codes[s], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, d.codes, cdims, cstr, cbox, swz(rb),
                               "tensor-core dequantize codes"))
             return SRFTKV_ERR_CUDA;
-        if (d.scale_format != SRFTKV_SCALE_FP32) {
+        if (d.scale_format != SRFTKV_SCALE_FP32 || DV != TD) {
             // the plane's bytes as rows of 16; one tile is 128 * ng * sb / 16 of them
             const unsigned long long sb = (unsigned long long)scale_bytes(d.scale_format);
             const unsigned long long rdims[3] = {16ull, tcap * ng * sb / 16, nrow};
@@ -710,12 +736,12 @@ static int launch_dq_tc(const CodecCall& c) {
     }
     static bool attr = false;
     if (!attr) {
-        cudaFuncSetAttribute(srft_dequantize_tc_kernel<BK, BV>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        cudaFuncSetAttribute(srft_dequantize_tc_kernel<BK, BV, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         attr = true;
     }
     int blocks = device_sm_count();
     if (blocks > P.total_tiles) blocks = P.total_tiles;
-    srft_dequantize_tc_kernel<BK, BV><<<blocks, DQ_WARPS * 32, C::SMEM, c.stream>>>(M, P);
+    srft_dequantize_tc_kernel<BK, BV, DV><<<blocks, DQ_WARPS * 32, C::SMEM, c.stream>>>(M, P);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("tensor-core dequantize launch failed: %s", cudaGetErrorString(e));
@@ -736,7 +762,7 @@ static int launch_tc(const CodecCall& c) {
     CUtensorMap tm[2];
     for (int s = 0; s < 2; ++s) {
         const CodecSideDesc& d = c.side[s < c.n_sides ? s : 0];
-        if (!encode_x_map(&tm[s], d.x, TD, c.H, c.n_tokens, c.n_outer, TM, true)) return SRFTKV_ERR_CUDA;
+        if (!encode_x_map(&tm[s], d.x, c.d, c.H, c.n_tokens, c.n_outer, TM, true)) return SRFTKV_ERR_CUDA;
     }
     static bool attr = false;
     if (!attr) {
@@ -763,7 +789,7 @@ static int launch_tc_bits(const CodecCall& c, int bk, int bv) {
 }
 
 int codec_quantize_tc(const CodecCall& c) {
-    if (c.d != TD || c.group > 32) return 1;  // a group must fit in one epilogue thread's 32 columns
+    if ((c.d != TD && c.d != 96) || c.group > 32) return 1;  // a group must fit in one epilogue thread's 32 columns
     const int bk = c.side[0].bits, bv = c.n_sides > 1 ? c.side[1].bits : bk;
     const int sf = c.side[0].scale_format;  // both sides share it (mixed calls are split on the host)
     if (sf == SRFTKV_SCALE_FP16) return launch_tc_bits<SRFTKV_SCALE_FP16>(c, bk, bv);
@@ -771,18 +797,31 @@ int codec_quantize_tc(const CodecCall& c) {
     return launch_tc_bits<SRFTKV_SCALE_FP32>(c, bk, bv);
 }
 
-int codec_dequantize_tc(const CodecCall& c) {
-    if (c.d != TD || c.group > 32) return 1;  // scale rows must be at least 16 bytes for the TMA copy
-    for (int s = 0; s < c.n_sides; ++s) {     // fp16 / e8m0 planes are copied in rows of 16 bytes
-        const long long rb = (long long)(TD / c.group) * scale_bytes(c.side[s].scale_format);
-        if (c.side[s].scale_format != SRFTKV_SCALE_FP32 && (((long long)c.t_cap * rb) % 16 || ((long long)c.t_offset * rb) % 16))
-            return 1;
+template <int DV>
+static int launch_dq_bits(const CodecCall& c, int bk, int bv) {
+    if (bk == 4 && bv == 4) return launch_dq_tc<4, 4, DV>(c);
+    if (bk == 8 && bv == 8) return launch_dq_tc<8, 8, DV>(c);
+    if (bk == 8 && bv == 4) return launch_dq_tc<8, 4, DV>(c);
+    return launch_dq_tc<4, 8, DV>(c);
+}
+
+int dq_tc_scale_rows_ok(const CodecCall& c) {
+    // fp16 / e8m0 planes (and every plane of d = 96) are copied in rows of 16
+    // bytes: a token's scale bytes times t_cap and t_offset must be whole rows
+    for (int s = 0; s < c.n_sides; ++s) {
+        const long long rb = (long long)(c.d / c.group) * scale_bytes(c.side[s].scale_format);
+        if ((c.side[s].scale_format != SRFTKV_SCALE_FP32 || c.d != TD) &&
+            (((long long)c.t_cap * rb) % 16 || ((long long)c.t_offset * rb) % 16))
+            return 0;
     }
+    return 1;
+}
+
+int codec_dequantize_tc(const CodecCall& c) {
+    if ((c.d != TD && c.d != 96) || c.group > 32) return 1;  // scale rows must be at least 16 bytes for the TMA copy
+    if (!dq_tc_scale_rows_ok(c)) return 1;
     const int bk = c.side[0].bits, bv = c.n_sides > 1 ? c.side[1].bits : bk;
-    if (bk == 4 && bv == 4) return launch_dq_tc<4, 4>(c);
-    if (bk == 8 && bv == 8) return launch_dq_tc<8, 8>(c);
-    if (bk == 8 && bv == 4) return launch_dq_tc<8, 4>(c);
-    return launch_dq_tc<4, 8>(c);
+    return c.d == 96 ? launch_dq_bits<96>(c, bk, bv) : launch_dq_bits<TD>(c, bk, bv);
 }
 
 }  // namespace srftkv

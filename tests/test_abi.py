@@ -151,3 +151,22 @@ def test_attention_format_rules(lib):
 
 def test_attention_empty_batch_is_a_no_op(lib):
     assert _attn(lib, _side(), _side(), B=0) == K.SRFTKV_OK
+
+
+@pytest.mark.parametrize("d,bits,group,code,scale", [(96, 4, 16, 48, 24), (96, 8, 32, 96, 12)])
+def test_vector_bytes_d96(lib, d, bits, group, code, scale):
+    assert K.srft_kv_vector_bytes(d, bits, group) == (code, scale)
+
+
+def test_d96_rules(lib):
+    """d = 96: groups must divide d (16 or 32), the Hadamard variant needs a power of two, and the planes are
+    copied by TMA so codes and scales must be 16-byte aligned."""
+    assert _q(lib, _side(), None, d=96, group=64) == K.SRFTKV_ERR_INVALID
+    srht = _side()
+    srht.transform = 1
+    assert _q(lib, srht, None, d=96) == K.SRFTKV_ERR_INVALID
+    assert b"power-of-two" in lib.srftkv_last_error()
+    assert _q(lib, _side(scales=264), None, d=96) == K.SRFTKV_ERR_INVALID   # 8-byte aligned only
+    assert lib.srht_transform(16, 16, 4, 96, 1, 0, None) == K.SRFTKV_ERR_INVALID
+    assert lib.srft_transform(16, 16, 0, 96, 1, 0, None) == K.SRFTKV_OK
+    assert _q(lib, _side(), None, d=96, n_tokens=0) == K.SRFTKV_OK

@@ -1,0 +1,143 @@
+"""GPU parity at a head dimension that is not a power of two (d = 96) against
+the fp64 oracle, through the C ABI.
+
+At d = 96 the SRFT is the packed unitary DFT of length 96 (the oracle's
+general even-d form); the library runs it as the tensor-core contraction
+padded to the 128-wide tile (codec) and as a dense map (bare transform).
+Sizes span several 128-row tiles with ragged tails and a window inside a
+larger cache (t_offset > 0), on both sides of one launch with mixed widths.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import srft_oracle as O
+from int8_kv_cache_srft_gb300 import inputs as I
+from tests.parity import assert_codes, assert_dequant_within_step, assert_reconstruction_bound, assert_scales
+from tests.test_gpu_scale_formats import check_side as check_side_fmt
+
+pytestmark = pytest.mark.gpu
+
+K = None
+D = 96
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    global K
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    import int8_kv_cache_srft_gb300 as mod
+
+    mod.library()
+    K = mod
+    yield
+    assert K.srftkv_device_fault() == 0
+
+
+def _np(t):
+    return t.detach().cpu().numpy()
+
+
+def tm(t):
+    return t.permute(0, 2, 1, 3)
+
+
+@pytest.mark.parametrize("inverse", (False, True))
+def test_transform_d96(inverse):
+    g = torch.Generator().manual_seed(96)
+    n = 1001  # ragged: not a multiple of the four rows a block takes
+    x = (torch.randn((n, D), generator=g) * 3).to(torch.float16)
+    y = torch.empty((n, D), dtype=torch.float32, device="cuda")
+    K.srft_transform(x.cuda(), y, n, D, 7, inverse)
+    torch.cuda.synchronize()
+    xd = _np(x).astype(np.float64)
+    ref = O.srft_inverse(xd, 7) if inverse else O.srft_forward(xd, 7)
+    err = np.abs(_np(y) - ref).max(axis=-1)
+    assert np.all(err <= 2e-6 * np.linalg.norm(xd, axis=-1) + 1e-7)
+
+
+@pytest.mark.parametrize("bits,group,lam", [(b, g, l) for b in (4, 8) for g in (16, 32) for l in (False, True)])
+def test_codec_d96_ragged(bits, group, lam):
+    """2 outer x 300 tokens x 3 heads (several 128-row tiles, ragged), written at t_offset 16 of t_cap 320;
+    K and V of one launch in different widths."""
+    n, T, H, t_cap, t_off, seed = 2, 300, 3, 320, 16, 11
+    w = I.Workload("d96", n_outer=n, tokens=T, kv_heads=H, d=D, lam=lam, data_seed=bits + group,
+                   outlier_kind="scale", outlier_channels=2, outlier_factor=30.0)
+    xk, xv = I.kv_side(w, "k"), I.kv_side(w, "v")
+    lk, lv = I.lam_table(w, "k"), I.lam_table(w, "v")
+    bits_v = 12 - bits
+    sides = []
+    for x, l, b in ((xk, lk, bits), (xv, lv, bits_v)):
+        s = K.alloc_side(n, t_cap, H, D, b, group)
+        s.codes.fill_(0xAB)
+        s.scales.fill_(-1.0)
+        s.x = x.cuda()
+        s.lam = None if l is None else l.cuda()
+        sides.append(s)
+    K.srft_kv_quantize(sides[0], sides[1], n, T, H, D, group, t_cap, t_off, seed)
+    torch.cuda.synchronize()
+    for s, x, l, b in ((sides[0], xk, lk, bits), (sides[1], xv, lv, bits_v)):
+        lam_b = None if l is None else _np(l)[:, None, :, :]
+        enc = O.srft_kv_quantize(_np(x).astype(np.float64), lam_b, b, group, seed)
+        codes = _np(tm(s.codes))
+        assert (codes[:, :t_off] == 0xAB).all() and (codes[:, t_off + T:] == 0xAB).all(), "rows outside the window"
+        assert_scales(_np(tm(s.scales))[:, t_off:t_off + T], enc["scales"])
+        assert_codes(codes[:, t_off:t_off + T], enc["r"], b)
+        out = torch.empty_like(s.x)
+        K.srft_kv_dequantize(K.Side(s.codes, s.scales, b, x=out, lam=s.lam), None, n, T, H, D, group, t_cap, t_off,
+                             seed)
+        torch.cuda.synchronize()
+        xg = _np(out).astype(np.float64)
+        lam_full = None if lam_b is None else np.broadcast_to(lam_b, x.shape)
+        ref_hat = O.srft_kv_dequantize(enc["codes"], enc["scales"], lam_b, b, group, seed)
+        assert_dequant_within_step(xg, ref_hat, enc["scales"], lam_full, group)
+        assert_reconstruction_bound(xg, _np(x), enc["scales"], lam_full, group)
+        mine = O.srft_kv_dequantize(codes[:, t_off:t_off + T], _np(tm(s.scales))[:, t_off:t_off + T].astype(np.float64),
+                                    lam_b, b, group, seed)
+        assert np.abs(xg - mine).max() <= np.abs(mine).max() * 2.0**-10 + 1e-5
+
+
+@pytest.mark.parametrize("fmt", ("fp16", "e8m0"))
+@pytest.mark.parametrize("bits,group", ((4, 16), (4, 32), (8, 16)))
+def test_codec_d96_scale_formats(fmt, bits, group):
+    n, T, H, seed = 2, 320, 3, 19
+    w = I.Workload("d96sf", n_outer=n, tokens=T, kv_heads=H, d=D, lam=(bits == 4), data_seed=3 * bits + group,
+                   outlier_kind="scale", outlier_channels=2, outlier_factor=30.0)
+    x, lam = I.kv_side(w, "k"), I.lam_table(w, "k")
+    s = K.alloc_side(n, T, H, D, bits, group, scale_format=fmt)
+    s.x = x.cuda()
+    s.lam = None if lam is None else lam.cuda()
+    K.srft_kv_quantize(s, None, n, T, H, D, group, T, 0, seed)
+    torch.cuda.synchronize()
+    enc, lam_b, raw = check_side_fmt(s, x, lam, bits, group, seed, fmt)
+    out = torch.empty_like(s.x)
+    K.srft_kv_dequantize(K.Side(s.codes, s.scales, bits, x=out, lam=s.lam, scale_format=fmt), None, n, T, H, D, group,
+                         T, 0, seed)
+    torch.cuda.synchronize()
+    mine = O.srft_kv_dequantize(_np(tm(s.codes)), O.decode_scales(raw, fmt), lam_b, bits, group, seed)
+    assert np.abs(_np(out) - mine).max() <= np.abs(mine).max() * 2.0**-10 + 1e-5
+
+
+def test_codec_d96_small_call():
+    """A call of a few rows (one partial tile) still takes the tensor-core path and matches."""
+    n, T, H, seed = 1, 5, 1, 3
+    w = I.Workload("d96small", n_outer=n, tokens=T, kv_heads=H, d=D, data_seed=5)
+    x = I.kv_side(w, "k")
+    s = K.alloc_side(n, 16, H, D, 4, 16)
+    s.x = x.cuda()
+    K.srft_kv_quantize(s, None, n, T, H, D, 16, 16, 0, seed)
+    torch.cuda.synchronize()
+    enc = O.srft_kv_quantize(_np(x).astype(np.float64), None, 4, 16, seed)
+    assert_scales(_np(tm(s.scales))[:, :T], enc["scales"])
+    assert_codes(_np(tm(s.codes))[:, :T], enc["r"], 4)
+
+
+def test_dequant_d96_unaligned_scale_rows_rejected():
+    """e8m0 groups of 32 at d = 96 are 3 bytes per token: a window whose scale bytes do not start on a 16-byte
+    row (t_offset 5) is rejected before any launch."""
+    s = K.alloc_side(1, 64, 1, D, 4, 32, scale_format="e8m0")
+    out = torch.empty((1, 8, 1, D), dtype=torch.float16, device="cuda")
+    with pytest.raises(RuntimeError, match="multiples of 16"):
+        K.srft_kv_dequantize(K.Side(s.codes, s.scales, 4, x=out, scale_format="e8m0"), None, 1, 8, 1, D, 32, 64, 5, 3)
