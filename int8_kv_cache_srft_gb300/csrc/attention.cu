@@ -77,6 +77,13 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(addr));
 }
+// two matrices (the addresses of lanes 0-15)
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t (&r)[2]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t (&r)[2]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(addr));
+}
 __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -136,9 +143,17 @@ __device__ __forceinline__ float h2_sum(uint32_t h) {
 template <int D, int BITS>
 struct PlaneT {
     static constexpr int RB = D * BITS / 8;                // bytes per cached row
-    static constexpr bool SWZ = BITS != 16 && RB <= 128;   // exact rows, swizzled
-    static constexpr int RP = SWZ ? RB : RB + 16;          // shared-memory row pitch
+    static constexpr bool SWZ = BITS != 16 && RB <= 128 && (RB & (RB - 1)) == 0;  // exact rows, swizzled
+    // unswizzled rows: an odd number of 16-byte chunks is already free of
+    // ldmatrix bank conflicts (48-byte int4 rows at d = 96); others get 16 bytes of padding
+    static constexpr int RP = SWZ || (RB / 16) % 2 == 1 ? RB : RB + 16;  // shared-memory row pitch
 };
+
+// 16-byte chunks of a group-16 fp32 scale row (d/4 bytes; 24 at d = 96 -> 2)
+template <int D>
+constexpr int scale_chunks() { return (D / 4 + 15) / 16; }
+template <int D>
+constexpr bool pow2_dim() { return (D & (D - 1)) == 0; }
 
 // Byte offset of 16-byte chunk `ch` of row `r` in a swizzled plane of RB-byte
 // rows (TMA swizzle: address bits [4, 4+b) XOR bits [7, 7+b), b = log2(RB/16)),
@@ -179,7 +194,6 @@ struct AttnCfg {
     static constexpr int QB = D / 8;    // K-side B-fragment registers
     static constexpr int ACC = D / 4;   // V accumulators
     static constexpr int NSV = BV == 4 ? D / 32 : BV == 8 ? D / 16 : 1;  // column sums of the V-side B
-    static constexpr int NCH = SRB / 16;  // 16-byte chunks in a group-16 scale row
 };
 
 // ---------------------------------------------------------------------------
@@ -247,6 +261,59 @@ __global__ void __launch_bounds__(128) attn_prep_q_kernel(const __grid_constant_
     }
 #pragma unroll
     for (int c = 0; c < D / 4; ++c) yr[c] = make_float4(p[4 * c], p[4 * c + 1], p[4 * c + 2], p[4 * c + 3]);
+}
+
+// Entry (n, k) of the packed unitary DFT R of length D (n the packed output
+// coordinate, k the input coordinate) from tables of cos / sin(2 pi m/D):
+// rows 0 and 1 are the real DC and Nyquist terms, rows 2j and 2j+1 the real
+// and imaginary parts of frequency j, times sqrt(2) for unitarity.
+template <int D>
+__device__ __forceinline__ float dense_r(const float* tcs, const float* tsn, int n, int k) {
+    const float isd = rsqrtf((float)D);
+    if (n == 0) return isd;
+    if (n == 1) return (k & 1) ? -isd : isd;
+    const int m = ((n >> 1) * k) % D;
+    const float r2 = 1.41421356237309515f * isd;
+    return (n & 1) ? -r2 * tsn[m] : r2 * tcs[m];
+}
+template <int D>
+__device__ __forceinline__ void dense_tables(float* tcs, float* tsn) {
+    for (int m = threadIdx.x; m < D; m += blockDim.x) {
+        double sv, cv;
+        sincospi(2.0 * m / D, &sv, &cv);
+        tcs[m] = (float)cv;
+        tsn[m] = (float)sv;
+    }
+}
+__device__ __forceinline__ bool sign_neg(const uint32_t* mask, int k) {
+    return (mask[k >> 1] & ((k & 1) ? 0x80000000u : 0x8000u)) != 0u;
+}
+
+// q preparation for a head dimension that is not a power of two (d = 96):
+// the SRFT as the dense map p = R diag(s) q, one warp per query row, then
+// 1/lambda_K and the softmax scale as above.
+template <int D>
+__global__ void __launch_bounds__(128) attn_prep_q_dense_kernel(const __grid_constant__ AttnParams P) {
+    __shared__ float tcs[D], tsn[D], xs[4][D];
+    dense_tables<D>(tcs, tsn);
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row = blockIdx.x * 4 + warp;
+    if (row >= P.B * P.Hq) return;
+    const int b = row / P.Hq, hq = row - b * P.Hq, hkv = hq / P.rep;
+    const __half* qr = reinterpret_cast<const __half*>(P.q) + (long long)row * D;
+    for (int k = lane; k < D; k += 32) {
+        const float v = __half2float(qr[k]);
+        xs[warp][k] = sign_neg(P.sign_mask, k) ? -v : v;
+    }
+    __syncwarp();
+    for (int o = lane; o < D; o += 32) {
+        float a = 0.f;
+        for (int k = 0; k < D; ++k) a = fmaf(dense_r<D>(tcs, tsn, o, k), xs[warp][k], a);
+        float sc = P.qscale;
+        if (P.lam_k != nullptr) sc *= __frcp_rn(P.lam_k[(long long)b * P.lam_k_stride + (long long)hkv * D + o]);
+        P.qt[(long long)row * D + o] = a * sc;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -376,7 +443,7 @@ __device__ __forceinline__ float ex2(float x) {  // 2^x; ex2.approx has a relati
 // 2^-24 unit of the codes, for fp16 keys as is).
 template <int D, int BK, int G>
 __device__ __forceinline__ void tile_scores(uint32_t kc, const LaneRow& LK, const uint8_t* __restrict__ ksb,
-                                            const uint32_t (&kso)[D / 64], int sp, int lg, int tr,
+                                            const uint32_t (&kso)[scale_chunks<D>()], int sp, int lg, int tr,
                                             int lane, const uint32_t (&qh)[D / 8], const uint32_t (&ql)[D / 8],
                                             const float (&nb)[D / 16], float (&s)[2]) {
     using PK = PlaneT<D, BK>;
@@ -391,27 +458,32 @@ __device__ __forceinline__ void tile_scores(uint32_t kc, const LaneRow& LK, cons
     };
     if constexpr (BK == 4) {
         float a0 = 0.f, a1 = 0.f;
+        // 32-dim chunk mm from its two 8-row matrices (rows 0-7, rows 8-15)
+        auto chunk = [&](int mm, uint32_t rg, uint32_t rg8) {
+            const uint32_t rs = rg >> 8, rs8 = rg8 >> 8;
+            const uint32_t x0 = u4_lo(rg), x1 = u4_lo(rg8), x2 = u4_hi(rg), x3 = u4_hi(rg8);
+            const uint32_t y0 = u4_lo(rs), y1 = u4_lo(rs8), y2 = u4_hi(rs), y3 = u4_hi(rs8);
+            float d[4];
+            mma16816_c(d, x0, x1, x2, x3, qh[4 * mm], qh[4 * mm + 1], nb[2 * mm], nb[2 * mm + 1]);
+            mma16816(d, y0, y1, y2, y3, qh[4 * mm + 2], qh[4 * mm + 3]);
+            mma16816(d, x0, x1, x2, x3, ql[4 * mm], ql[4 * mm + 1]);
+            mma16816(d, y0, y1, y2, y3, ql[4 * mm + 2], ql[4 * mm + 3]);
+            // d = (token g: half 0, half 1, token g+8: half 0, half 1) for head c
+            const int ga = (32 * mm) >> lg, gb = (32 * mm + 16) >> lg;
+            a0 = fmaf(ksc(ga, 0), d[0], fmaf(ksc(gb, 0), d[1], a0));
+            a1 = fmaf(ksc(ga, 1), d[2], fmaf(ksc(gb, 1), d[3], a1));
+        };
 #pragma unroll
         for (int m2 = 0; m2 < D / 64; ++m2) {
             uint32_t r[4];
             ldsm_x4(plane_addr<PK::RB, PK::SWZ, PK::RP>(kc, LK, tr, 2 * m2), r);
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int mm = 2 * m2 + hh;
-                const uint32_t rg = r[2 * hh], rg8 = r[2 * hh + 1];
-                const uint32_t rs = rg >> 8, rs8 = rg8 >> 8;
-                const uint32_t x0 = u4_lo(rg), x1 = u4_lo(rg8), x2 = u4_hi(rg), x3 = u4_hi(rg8);
-                const uint32_t y0 = u4_lo(rs), y1 = u4_lo(rs8), y2 = u4_hi(rs), y3 = u4_hi(rs8);
-                float d[4];
-                mma16816_c(d, x0, x1, x2, x3, qh[4 * mm], qh[4 * mm + 1], nb[2 * mm], nb[2 * mm + 1]);
-                mma16816(d, y0, y1, y2, y3, qh[4 * mm + 2], qh[4 * mm + 3]);
-                mma16816(d, x0, x1, x2, x3, ql[4 * mm], ql[4 * mm + 1]);
-                mma16816(d, y0, y1, y2, y3, ql[4 * mm + 2], ql[4 * mm + 3]);
-                // d = (token g: half 0, half 1, token g+8: half 0, half 1) for head c
-                const int ga = (32 * mm) >> lg, gb = (32 * mm + 16) >> lg;
-                a0 = fmaf(ksc(ga, 0), d[0], fmaf(ksc(gb, 0), d[1], a0));
-                a1 = fmaf(ksc(ga, 1), d[2], fmaf(ksc(gb, 1), d[3], a1));
-            }
+            chunk(2 * m2, r[0], r[1]);
+            chunk(2 * m2 + 1, r[2], r[3]);
+        }
+        if constexpr (D % 64 != 0) {  // an odd number of 32-dim chunks (d = 96): the last one alone
+            uint32_t r[2];
+            ldsm_x2(plane_addr<PK::RB, PK::SWZ, PK::RP>(kc, LK, tr, D / 32 - 1), r);
+            chunk(D / 32 - 1, r[0], r[1]);
         }
         s[0] = a0;
         s[1] = a1;
@@ -458,7 +530,7 @@ __device__ __forceinline__ void tile_scores(uint32_t kc, const LaneRow& LK, cons
 // the column sums of B that remove the offset afterwards.
 template <int D, int BV, int G>
 __device__ __forceinline__ void tile_pv(uint32_t vc, const LaneRow& LV, const uint8_t* __restrict__ vsb,
-                                        const uint32_t (&vso)[D / 64], int sp, int lg, int tr,
+                                        const uint32_t (&vso)[scale_chunks<D>()], int sp, int lg, int tr,
                                         int lane, float p00, float p10, float p01, float p11, uint32_t amask_lo,
                                         uint32_t amask_hi, bool tail, float (&acc)[D / 4],
                                         float (&sv)[AttnCfg<D, 4, BV>::NSV]) {
@@ -474,32 +546,38 @@ __device__ __forceinline__ void tile_pv(uint32_t vc, const LaneRow& LV, const ui
     };
     if constexpr (BV == 4) {
         const int side = g & 1;
+        // 32-dim chunk cb from its two transposed 8-row matrices (token rows 0-7, 8-15)
+        auto chunk = [&](int cb, uint32_t R0, uint32_t R1) {
+            // group 16: group 2cb + side lies in chunk cb/2 at float 2(cb%2) + side (side folded into vso)
+            const int gv = G == 16 ? cb >> 1 : (32 * cb + 16 * side) >> lg;
+            const int fc = 2 * (cb & 1);
+            const float b00 = p00 * vsc(gv, fc, 0), b10 = p10 * vsc(gv, fc, 1), b01 = p01 * vsc(gv, fc, 8),
+                        b11 = p11 * vsc(gv, fc, 9);
+            sv[cb] += (b00 + b10) + (b01 + b11);
+            uint32_t bh0, bl0, bh1, bl1;
+            split_h2(b00, b10, bh0, bl0);
+            split_h2(b01, b11, bh1, bl1);
+            const uint32_t S0 = R0 >> 8, S1 = R1 >> 8;
+            float(&a0)[4] = *reinterpret_cast<float(*)[4]>(&acc[8 * cb]);
+            float(&a1)[4] = *reinterpret_cast<float(*)[4]>(&acc[8 * cb + 4]);
+            const uint32_t x0 = u4_lo(R0), x1 = u4_hi(R0), x2 = u4_lo(R1), x3 = u4_hi(R1);
+            const uint32_t y0 = u4_lo(S0), y1 = u4_hi(S0), y2 = u4_lo(S1), y3 = u4_hi(S1);
+            mma16816(a0, x0, x1, x2, x3, bh0, bh1);
+            mma16816(a1, y0, y1, y2, y3, bh0, bh1);
+            mma16816(a0, x0, x1, x2, x3, bl0, bl1);
+            mma16816(a1, y0, y1, y2, y3, bl0, bl1);
+        };
 #pragma unroll
         for (int cb2 = 0; cb2 < D / 64; ++cb2) {
             uint32_t r[4];
             ldsm_x4_t(plane_addr<PV::RB, PV::SWZ, PV::RP>(vc, LV, tr, 2 * cb2), r);
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int cb = 2 * cb2 + hh;
-                // group 16: group 2cb + side lies in chunk cb/2 at float 2(cb%2) + side (side folded into vso)
-                const int gv = G == 16 ? cb >> 1 : (32 * cb + 16 * side) >> lg;
-                const int fc = 2 * (cb & 1);
-                const float b00 = p00 * vsc(gv, fc, 0), b10 = p10 * vsc(gv, fc, 1), b01 = p01 * vsc(gv, fc, 8),
-                            b11 = p11 * vsc(gv, fc, 9);
-                sv[cb] += (b00 + b10) + (b01 + b11);
-                uint32_t bh0, bl0, bh1, bl1;
-                split_h2(b00, b10, bh0, bl0);
-                split_h2(b01, b11, bh1, bl1);
-                const uint32_t R0 = r[2 * hh], R1 = r[2 * hh + 1], S0 = R0 >> 8, S1 = R1 >> 8;
-                float(&a0)[4] = *reinterpret_cast<float(*)[4]>(&acc[8 * cb]);
-                float(&a1)[4] = *reinterpret_cast<float(*)[4]>(&acc[8 * cb + 4]);
-                const uint32_t x0 = u4_lo(R0), x1 = u4_hi(R0), x2 = u4_lo(R1), x3 = u4_hi(R1);
-                const uint32_t y0 = u4_lo(S0), y1 = u4_hi(S0), y2 = u4_lo(S1), y3 = u4_hi(S1);
-                mma16816(a0, x0, x1, x2, x3, bh0, bh1);
-                mma16816(a1, y0, y1, y2, y3, bh0, bh1);
-                mma16816(a0, x0, x1, x2, x3, bl0, bl1);
-                mma16816(a1, y0, y1, y2, y3, bl0, bl1);
-            }
+            chunk(2 * cb2, r[0], r[1]);
+            chunk(2 * cb2 + 1, r[2], r[3]);
+        }
+        if constexpr (D % 64 != 0) {  // d = 96: the last 32-dim chunk alone
+            uint32_t r[2];
+            ldsm_x2_t(plane_addr<PV::RB, PV::SWZ, PV::RP>(vc, LV, tr, D / 32 - 1), r);
+            chunk(D / 32 - 1, r[0], r[1]);
         }
     } else if constexpr (BV == 8) {
         // the half-1 columns carry nothing for 8-bit values
@@ -558,7 +636,7 @@ __device__ __forceinline__ void tile_pv(uint32_t vc, const LaneRow& LV, const ui
 template <int D, int G>
 __device__ __forceinline__ void widen_scales(const uint8_t* __restrict__ raw, uint8_t* __restrict__ dst, int rows,
                                              int ng, int sfmt, int lane) {
-    if constexpr (G == 16) {
+    if constexpr (G == 16 && D % 64 == 0) {
         // lane r widens row r: four scales (one 16-byte fp32 chunk) at a time
         constexpr int NG = D / 16, SRB = D / 4;
         if (lane < rows) {
@@ -602,8 +680,9 @@ __device__ __forceinline__ void widen_scales(const uint8_t* __restrict__ raw, ui
 // scale-row indexing becomes immediate offsets), or 0 to read it from P.
 template <int D, int BK, int BV, int NT, int G>
 __device__ __forceinline__ void attn_chunk(const AttnParams& P, uint8_t* __restrict__ stage, int t0, int t_end, int lane,
-                                           const LaneRow& LK, const LaneRow& LV, const uint32_t (&kso)[D / 64],
-                                           const uint32_t (&vso)[D / 64], const uint32_t (&qh)[D / 8],
+                                           const LaneRow& LK, const LaneRow& LV,
+                                           const uint32_t (&kso)[scale_chunks<D>()],
+                                           const uint32_t (&vso)[scale_chunks<D>()], const uint32_t (&qh)[D / 8],
                                            const uint32_t (&ql)[D / 8],
                                            const float (&nb)[D / 16], float (&acc)[D / 4],
                                            float (&sv)[AttnCfg<D, BK, BV>::NSV], float& m, float& l) {
@@ -753,9 +832,10 @@ __global__ void __launch_bounds__(kAttnWarps * 32, D >= 256 ? 2 : 3)
     using PV = PlaneT<D, BV>;
     const LaneRow LK = lane_row_codes<PK::RB, PK::SWZ, PK::RP>(lane);
     const LaneRow LV = BV == 16 ? lane_row_v16<PV::RB, PV::SWZ, PV::RP>(lane) : lane_row_codes<PV::RB, PV::SWZ, PV::RP>(lane);
-    uint32_t kso[D / 64], vso[D / 64];
-    scale_offsets<D, D / 64>(g, 0, kso);                               // K: row g (and g + 8)
-    scale_offsets<D, D / 64>(2 * c, BV == 4 ? 4 * (g & 1) : 0, vso);  // V: rows 2c (+1, +8, +9), column half
+    constexpr int SCH = scale_chunks<D>();
+    uint32_t kso[SCH], vso[SCH];
+    scale_offsets<D, SCH>(g, 0, kso);                               // K: row g (and g + 8)
+    scale_offsets<D, SCH>(2 * c, BV == 4 ? 4 * (g & 1) : 0, vso);  // V: rows 2c (+1, +8, +9), column half
     float acc[C::ACC], sv[C::NSV];
 #pragma unroll
     for (int i = 0; i < C::ACC; ++i) acc[i] = 0.f;
@@ -770,9 +850,13 @@ __global__ void __launch_bounds__(kAttnWarps * 32, D >= 256 ? 2 : 3)
     const uint32_t vs_bytes = C::CH * P.sp * (P.sf_v == SRFTKV_SCALE_FP32 ? 4 : P.sf_v == SRFTKV_SCALE_FP16 ? 2 : 1);
     const int ks_off = P.sf_k == SRFTKV_SCALE_FP32 ? C::OFF_KS : C::OFF_KR;
     const int vs_off = P.sf_v == SRFTKV_SCALE_FP32 ? C::OFF_VS : C::OFF_VR;
-    // raw planes are addressed as rows of 16 bytes: the chunk's first one
-    const int ks_row = P.sf_k == SRFTKV_SCALE_FP32 ? 1 : (int)(ks_bytes / 16);
-    const int vs_row = P.sf_v == SRFTKV_SCALE_FP32 ? 1 : (int)(vs_bytes / 16);
+    // fp16 / e8m0 planes, and every plane of a d that is not a power of two (whose
+    // scale rows are not a multiple of 16 bytes), are addressed as rows of 16
+    // bytes: the chunk's first one; fp32 rows of a power-of-two d as rows
+    const bool kflat = !pow2_dim<D>() || P.sf_k != SRFTKV_SCALE_FP32;
+    const bool vflat = !pow2_dim<D>() || P.sf_v != SRFTKV_SCALE_FP32;
+    const int ks_row = kflat ? (int)(ks_bytes / 16) : 1;
+    const int vs_row = vflat ? (int)(vs_bytes / 16) : 1;
     const uint32_t tx = kc_bytes + vc_bytes + (C::QK ? ks_bytes : 0) + (C::QV ? vs_bytes : 0);
     auto issue = [&](int chunk, int st) {
         const uint32_t bar = barw(st);
@@ -781,12 +865,10 @@ __global__ void __launch_bounds__(kAttnWarps * 32, D >= 256 ? 2 : 3)
         ptx::mbar_arrive_expect_tx(bar, tx);
         ptx::tma_load_3d(ptx::smem_u32(dst + C::OFF_KC), &tm_kc, bar, 0, tok, plane_row);
         if constexpr (C::QK)
-            ptx::tma_load_3d(ptx::smem_u32(dst + ks_off), &tm_ks, bar, 0,
-                             P.sf_k == SRFTKV_SCALE_FP32 ? tok : chunk * ks_row, plane_row);
+            ptx::tma_load_3d(ptx::smem_u32(dst + ks_off), &tm_ks, bar, 0, kflat ? chunk * ks_row : tok, plane_row);
         ptx::tma_load_3d(ptx::smem_u32(dst + C::OFF_VC), &tm_vc, bar, 0, tok, plane_row);
         if constexpr (C::QV)
-            ptx::tma_load_3d(ptx::smem_u32(dst + vs_off), &tm_vs, bar, 0,
-                             P.sf_v == SRFTKV_SCALE_FP32 ? tok : chunk * vs_row, plane_row);
+            ptx::tma_load_3d(ptx::smem_u32(dst + vs_off), &tm_vs, bar, 0, vflat ? chunk * vs_row : tok, plane_row);
     };
 
     // per-warp ring of NS stages: chunk j of this warp goes to stage j % NS, NS-1 chunks in flight
@@ -930,6 +1012,21 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const __grid_constant
     if constexpr (!ROT) {
 #pragma unroll
         for (int j = 0; j < PER; ++j) P.out[(long long)row * D + lane * PER + j] = rows[warp][lane * PER + j];
+    } else if constexpr (!pow2_dim<D>()) {
+        // inverse SRFT as the dense map diag(s) R^T p, one output coordinate per lane at a time
+        __shared__ float tcs[4][D], tsn[4][D];  // per warp: warps past the last row have left the block
+        for (int m = lane; m < D; m += 32) {
+            double sv, cv;
+            sincospi(2.0 * m / D, &sv, &cv);
+            tcs[warp][m] = (float)cv;
+            tsn[warp][m] = (float)sv;
+        }
+        __syncwarp();
+        for (int k = lane; k < D; k += 32) {
+            float a = 0.f;
+            for (int n = 0; n < D; ++n) a = fmaf(dense_r<D>(tcs[warp], tsn[warp], n, k), rows[warp][n], a);
+            P.out[(long long)row * D + k] = sign_neg(P.sign_mask, k) ? -a : a;
+        }
     } else {
         if (lane != 0) return;
         float p[D], zr[N], zi[N];
@@ -987,7 +1084,7 @@ static bool encode_codes(CUtensorMap* map, const void* base, long long bh, int t
     if (PT::SWZ)
         return encode_plane(map, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, PT::RB, 1, PT::RB, bh, t_cap, rows,
                             swizzle_for(PT::RB));
-    return encode_plane(map, base, CU_TENSOR_MAP_DATA_TYPE_UINT32, PT::RB / 4, 4, PT::RB / 4 + 4, bh, t_cap, rows,
+    return encode_plane(map, base, CU_TENSOR_MAP_DATA_TYPE_UINT32, PT::RB / 4, 4, PT::RP / 4, bh, t_cap, rows,
                         CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
@@ -1014,19 +1111,19 @@ static int launch_split(const AttnLaunch& A) {
     tvs = tvc;
     // fp16 / e8m0 planes: the (batch, kv head)'s scale bytes as rows of 16 bytes; a box is one chunk's bytes
     auto raw_plane = [&](CUtensorMap* map, const void* base, int sfmt) {
-        const int sb = sfmt == SRFTKV_SCALE_FP16 ? 2 : 1;
+        const int sb = scale_bytes(sfmt);
         return encode_plane(map, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 16, 1, 16, bh, P.t_cap * ng * sb / 16,
                             C::CH * ng * sb / 16, CU_TENSOR_MAP_SWIZZLE_NONE);
     };
     if (C::QK) {
-        const bool ok = P.sf_k == SRFTKV_SCALE_FP32
+        const bool ok = P.sf_k == SRFTKV_SCALE_FP32 && pow2_dim<D>()
                             ? encode_plane(&tks, A.k->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ng, 4, ng, bh, P.t_cap,
                                            C::CH, ssw)
                             : raw_plane(&tks, A.k->scales, P.sf_k);
         if (!ok) return SRFTKV_ERR_CUDA;
     }
     if (C::QV) {
-        const bool ok = P.sf_v == SRFTKV_SCALE_FP32
+        const bool ok = P.sf_v == SRFTKV_SCALE_FP32 && pow2_dim<D>()
                             ? encode_plane(&tvs, A.v->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ng, 4, ng, bh, P.t_cap,
                                            C::CH, ssw)
                             : raw_plane(&tvs, A.v->scales, P.sf_v);
@@ -1057,10 +1154,12 @@ static int launch_all(const AttnLaunch& A) {
     const int bk = A.k->bits, bv = A.v->bits;
     const bool rot = bk != 16;
     const int rows = P.B * P.Hq;
-    if (rot)
+    if (!rot)
+        attn_prep_q_kernel<D, false><<<(rows + 127) / 128, 128, 0, A.stream>>>(P);
+    else if constexpr (pow2_dim<D>())
         attn_prep_q_kernel<D, true><<<(rows + 127) / 128, 128, 0, A.stream>>>(P);
     else
-        attn_prep_q_kernel<D, false><<<(rows + 127) / 128, 128, 0, A.stream>>>(P);
+        attn_prep_q_dense_kernel<D><<<(rows + 3) / 4, 128, 0, A.stream>>>(P);
     int rc;
     if (bk == 4 && bv == 4) rc = launch_split<D, 4, 4>(A);
     else if (bk == 8 && bv == 4) rc = launch_split<D, 8, 4>(A);
@@ -1111,7 +1210,7 @@ static int invalid_attn(const char* msg) {
 int attention_entry(const void* q, float* out, const srftkv_side* k, const srftkv_side* v, int B, int Hq, int Hkv,
                     int d, int group, int t_cap, const int* seq_lens, float sm_scale, uint64_t seed, int n_splits,
                     void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-    if (d != 64 && d != 128 && d != 256) return invalid_attn("attention: d must be 64, 128 or 256");
+    if (d != 64 && d != 96 && d != 128 && d != 256) return invalid_attn("attention: d must be 64, 96, 128 or 256");
     if (B < 0 || Hq <= 0 || Hkv <= 0 || t_cap <= 0) return invalid_attn("attention: need B >= 0, Hq, Hkv, t_cap > 0");
     if (Hq % Hkv) return invalid_attn("attention: Hq must be a multiple of Hkv");
     if (Hq / Hkv > 4) return invalid_attn("attention: at most 4 query heads per kv head are supported");
@@ -1121,8 +1220,10 @@ int attention_entry(const void* q, float* out, const srftkv_side* k, const srftk
     if (!raw && ((k->bits != 4 && k->bits != 8) || (v->bits != 4 && v->bits != 8)))
         return invalid_attn("attention: bits must be 4, 8 (or 16 on both sides)");
     if (!raw) {
-        if (group < 16 || (group & (group - 1)) || group > d / 4)
-            return invalid_attn("attention: group must be a power of two with 16 <= group <= d/4");
+        // a power-of-two d copies fp32 scale rows as rows (at least 16 bytes: group <= d/4); d = 96 copies
+        // every scale plane as 16-byte rows of bytes and takes groups of 16 or 32
+        if (group < 16 || (group & (group - 1)) || (d == 96 ? group > 32 : group > d / 4))
+            return invalid_attn("attention: group must be a power of two with 16 <= group <= d/4 (16 or 32 at d = 96)");
         if (!k->scales || !v->scales) return invalid_attn("attention: scales must not be NULL");
         const srftkv_side* sv2[2] = {k, v};
         for (auto sd : sv2) {
@@ -1132,9 +1233,11 @@ int attention_entry(const void* q, float* out, const srftkv_side* k, const srftk
                 sd->scale_format != SRFTKV_SCALE_E8M0)
                 return invalid_attn("attention: scale_format must be SRFTKV_SCALE_FP32, _FP16 or _E8M0");
             // fp16 / e8m0 scale planes are copied as 16-byte rows: one (batch, kv head)'s scales fill whole rows
-            if (sd->scale_format != SRFTKV_SCALE_FP32 &&
+            if ((sd->scale_format != SRFTKV_SCALE_FP32 || d == 96) &&
                 ((long long)t_cap * (d / group) * scale_bytes(sd->scale_format)) % 16 != 0)
                 return invalid_attn("attention: t_cap * (d/group) * scale bytes must be a multiple of 16");
+            if (d == 96 && sd->transform != SRFTKV_TRANSFORM_SRFT)
+                return invalid_attn("attention: the Hadamard transform needs a power-of-two d");
         }
         if ((reinterpret_cast<uintptr_t>(k->scales) | reinterpret_cast<uintptr_t>(v->scales)) & 15)
             return invalid_attn("attention: scales must be 16-byte aligned");
@@ -1196,6 +1299,7 @@ int attention_entry(const void* q, float* out, const srftkv_side* k, const srftk
     A.stream = stream;
     switch (d) {
         case 64: return launch_all<64>(A);
+        case 96: return launch_all<96>(A);
         case 128: return launch_all<128>(A);
         default: return launch_all<256>(A);
     }

@@ -141,3 +141,94 @@ def test_dequant_d96_unaligned_scale_rows_rejected():
     out = torch.empty((1, 8, 1, D), dtype=torch.float16, device="cuda")
     with pytest.raises(RuntimeError, match="multiples of 16"):
         K.srft_kv_dequantize(K.Side(s.codes, s.scales, 4, x=out, scale_format="e8m0"), None, 1, 8, 1, D, 32, 64, 5, 3)
+
+
+# ---------------------------------------------------------------------------
+# decode attention at d = 96
+# ---------------------------------------------------------------------------
+from tests.test_gpu_attention import build_cache, oracle_attention, run_attention  # noqa: E402
+from tests.test_gpu_scale_formats import raw_np  # noqa: E402
+from tests.parity import ATTN_ATOL  # noqa: E402
+
+
+ATTN96 = [(bk, bv, g) for bk, bv in ((4, 4), (8, 4), (4, 8), (8, 8), (16, 16)) for g in (16, 32)
+          if bk != 16 or g == 16]  # the raw fp16 cache has no groups
+
+
+@pytest.fixture()
+def attn_helpers():
+    """The attention tests' cache builder, bound to this module's library handle."""
+    import tests.test_gpu_attention as TA
+
+    TA.K = K
+    return TA
+
+
+@pytest.mark.parametrize("bk,bv,group", ATTN96)
+def test_attention_d96_matches_oracle(attn_helpers, bk, bv, group):
+    """Ragged lengths (300 = 9 chunks + 12, and 137) over t_cap 300, four query heads per kv head, lambda on."""
+    B, Hkv, rep, t_cap, seed = 2, 2, 4, 300, 21
+    Hq = Hkv * rep
+    sk, sv = build_cache(B, Hkv, D, t_cap, bk, bv, group, seed, lam=(bk != 16), data_seed=bk * 10 + bv + group)
+    q = I.query(I.Workload("q", n_outer=B, tokens=1, kv_heads=Hkv, d=D, q_heads=Hq, data_seed=96), device="cuda")
+    seq = torch.tensor([300, 137], dtype=torch.int32, device="cuda")
+    out = run_attention(q, sk, sv, B, Hq, Hkv, D, group, t_cap, seq, seed)
+    ref = oracle_attention(q, sk, sv, group, seed, seq)
+    err = np.abs(out - ref).max()
+    assert err <= ATTN_ATOL, f"max-abs error {err:.3g}"
+
+
+@pytest.mark.parametrize("rep,n_splits", ((1, 0), (2, 1), (3, 5), (4, 0)))
+def test_attention_d96_gqa_and_splits(attn_helpers, rep, n_splits):
+    B, Hkv, t_cap, seed = 3, 2, 1000, 8
+    Hq = Hkv * rep
+    sk, sv = build_cache(B, Hkv, D, t_cap, 4, 4, 16, seed, data_seed=rep)
+    q = I.query(I.Workload("q", n_outer=B, tokens=1, kv_heads=Hkv, d=D, q_heads=Hq, data_seed=rep + 50), device="cuda")
+    seq = torch.tensor([1000, 1, 517], dtype=torch.int32, device="cuda")
+    out = run_attention(q, sk, sv, B, Hq, Hkv, D, 16, t_cap, seq, seed, n_splits=n_splits, sm_scale=0.11)
+    ref = oracle_attention(q, sk, sv, 16, seed, seq, sm_scale=0.11)
+    assert np.abs(out - ref).max() <= ATTN_ATOL
+
+
+@pytest.mark.parametrize("fmt_k,fmt_v,group", (("fp16", "fp16", 16), ("e8m0", "e8m0", 16), ("fp32", "e8m0", 32),
+                                               ("fp16", "fp32", 32)))
+def test_attention_d96_scale_formats(fmt_k, fmt_v, group):
+    B, Hkv, rep, t_cap, seed = 2, 2, 4, 320, 31
+    w = I.Workload("attn96", n_outer=B, tokens=t_cap, kv_heads=Hkv, d=D, lam=True, data_seed=group,
+                   outlier_kind="scale", outlier_channels=2, outlier_factor=8.0)
+    sides = []
+    for name, fmt in (("k", fmt_k), ("v", fmt_v)):
+        x, lam = I.kv_side(w, name), I.lam_table(w, name)
+        s = K.alloc_side(B, t_cap, Hkv, D, 4, group, scale_format=fmt)
+        s.x, s.lam = x.cuda(), lam.cuda()
+        K.srft_kv_quantize(s, None, B, t_cap, Hkv, D, group, t_cap, 0, seed)
+        sides.append(s)
+    torch.cuda.synchronize()
+    q = I.query(I.Workload("q", n_outer=B, tokens=1, kv_heads=Hkv, d=D, q_heads=Hkv * rep, data_seed=7), device="cuda")
+    seq = torch.tensor([320, 97], dtype=torch.int32, device="cuda")
+    out = torch.empty((B, Hkv * rep, D), dtype=torch.float32, device="cuda")
+    ws = torch.empty(K.q4kv_decode_attention_workspace_size(B, Hkv * rep, Hkv, D, t_cap, 0), dtype=torch.uint8,
+                     device="cuda")
+    K.q4kv_decode_attention(q, out, sides[0], sides[1], B, Hkv * rep, Hkv, D, group, t_cap, seq, 0.0, seed, 0, ws)
+    torch.cuda.synchronize()
+
+    def oside(s, fmt):
+        return {"bits": 4, "codes": _np(tm(s.codes)), "scales": O.decode_scales(raw_np(s.scales, fmt), fmt),
+                "lam": _np(s.lam).astype(np.float64), "group": group}
+
+    ref = O.packed_decode_attention(_np(q).astype(np.float64), oside(sides[0], fmt_k), oside(sides[1], fmt_v), seed,
+                                    _np(seq))
+    assert np.abs(_np(out) - ref).max() <= ATTN_ATOL
+
+
+def test_attention_d96_rejects_unaligned_scale_rows():
+    """fp32 group-16 rows are 24 bytes at d = 96: an odd t_cap leaves a (batch, kv head)'s scales off the
+    16-byte rows the copy uses, and is rejected."""
+    B, Hkv, t_cap = 1, 1, 33
+    sk = K.alloc_side(B, t_cap, Hkv, D, 4, 16)
+    sv = K.alloc_side(B, t_cap, Hkv, D, 4, 16)
+    q = torch.zeros((B, 4, D), dtype=torch.float16, device="cuda")
+    out = torch.empty((B, 4, D), dtype=torch.float32, device="cuda")
+    ws = torch.empty(K.q4kv_decode_attention_workspace_size(B, 4, Hkv, D, t_cap, 0), dtype=torch.uint8, device="cuda")
+    with pytest.raises(RuntimeError, match="multiple of 16"):
+        K.q4kv_decode_attention(q, out, sk, sv, B, 4, Hkv, D, 16, t_cap, None, 0.0, 1, 0, ws)

@@ -86,12 +86,9 @@ def _check(side, x, lam, bits, group, seed, tr, t_offset):
     assert_reconstruction_bound(_np(out), _np(x), enc["scales"], lam_full, group)
 
 
-@pytest.mark.parametrize("d", (16, 32, 64, 128, 256))
-@pytest.mark.parametrize("bits", (4, 8))
-@pytest.mark.parametrize("path", ("fft", "tc"))
+@pytest.mark.parametrize("d,bits,path", [(d, b, p) for d in (16, 32, 64, 128, 256) for b in (4, 8) for p in ("fft", "tc")
+                                          if p == "fft" or d == 128])  # the tensor-core path is d = 128
 def test_srht_codec(monkeypatch, d, bits, path):
-    if path == "tc" and d != 128:
-        pytest.skip("the tensor-core path is d = 128")
     monkeypatch.setenv("SRFTKV_QUANT_PATH", path)
     w = I.Workload("srht", n_outer=2, tokens=261, kv_heads=3, d=d, lam=(bits == 4), data_seed=7 * d + bits,
                    outlier_kind="scale", outlier_channels=2, outlier_factor=30.0)
