@@ -37,7 +37,12 @@
  *  - int4: two's-complement nibbles, even coordinate in the low nibble;
  *    int8: two's-complement bytes;
  *  - scales are fp32; softmax scale defaults to 1/sqrt(d); a query with
- *    sequence length 0 gets a zero output.
+ *    sequence length 0 gets a zero output;
+ *  - a head dimension that is not a power of two (d = 96; Methodology 1
+ *    names SRFT's freedom from the power-of-two restriction of Hadamard
+ *    rotations): the same F, the unitary DFT of length d, with the same
+ *    packing; the library forms it as a dense d x d map instead of radix-2
+ *    FFT stages.
  *
  * General conventions
  *  - Every pointer argument that names tensor data is a DEVICE pointer
@@ -49,9 +54,11 @@
  *  - Return codes: SRFTKV_OK, or a negative SRFTKV_ERR_*; on any error no
  *    work has been enqueued and srftkv_last_error() describes it.
  *  - Inputs must be finite; NaN/Inf behaviour is unspecified.
- *  - Supported sizes: d in {16, 32, 64, 128, 256} for the codec and the
- *    transform, d in {64, 128, 256} for attention; group a power of two,
- *    16 <= group <= d; bits in {4, 8} for packed sides.
+ *  - Supported sizes: d in {16, 32, 64, 96, 128, 256} for the codec and
+ *    srft_transform, d in {64, 96, 128, 256} for attention; group a power
+ *    of two dividing d with 16 <= group <= d; bits in {4, 8} for packed
+ *    sides.  d = 96 takes the SRFT only (the Hadamard matrix needs a power
+ *    of two), groups of 16 or 32, and 16-byte aligned code and scale planes.
  */
 #ifndef SRFTKV_H
 #define SRFTKV_H
@@ -119,6 +126,8 @@ typedef struct srftkv_side {
  * Both sides are encoded by one kernel launch.  Requires
  * 0 <= t_offset, t_offset + n_tokens <= t_cap, and x rows 16-byte aligned.
  * n_outer == 0 or n_tokens == 0 is a no-op that returns SRFTKV_OK.
+ * d = 96 runs as the 128-wide tensor-core contraction with R zero outside
+ * its 96 x 96 block (any call size).
  */
 int srft_kv_quantize(const srftkv_side* k, const srftkv_side* v, int n_outer, int n_tokens,
                      int H, int d, int group, int t_cap, int t_offset, uint64_t sign_seed,
@@ -130,7 +139,11 @@ int srft_kv_quantize(const srftkv_side* k, const srftkv_side* v, int n_outer, in
  *   x_hat = diag(s) . F^{-1} . unpack((codes * scale) / lambda)
  * (SRHT sides: x_hat = diag(s) . H . ((codes * scale) / lambda) / sqrt(d))
  * written to side->x as [n_outer][n_tokens][H][d].  Same size rules as
- * srft_kv_quantize.
+ * srft_kv_quantize.  The tensor-core path copies fp16 / e8m0 scale planes
+ * (every scale plane at d = 96) as rows of 16 bytes, so there
+ * t_cap * (d/group) * scale bytes and t_offset * (d/group) * scale bytes must
+ * be multiples of 16: at d = 96 that is required (SRFTKV_ERR_INVALID
+ * otherwise); at d = 128 a call that misses it takes the FFT path.
  */
 int srft_kv_dequantize(const srftkv_side* k, const srftkv_side* v, int n_outer, int n_tokens,
                        int H, int d, int group, int t_cap, int t_offset, uint64_t sign_seed,
@@ -156,11 +169,14 @@ int srft_kv_dequantize(const srftkv_side* k, const srftkv_side* v, int n_outer, 
  *              q4kv_decode_attention_workspace_size(...) bytes (16-byte aligned)
  *              for the per-split partial results; contents need not be
  *              initialised and are overwritten.
- * Requires d in {64, 128, 256}, Hq % Hkv == 0 and Hq/Hkv <= 4, and for
+ * Requires d in {64, 96, 128, 256}, Hq % Hkv == 0 and Hq/Hkv <= 4, and for
  * packed sides a power-of-two group with 16 <= group <= d/4 (a scale row of
- * at least 16 bytes, the smallest TMA row) and 16-byte aligned scales;
- * anything else returns SRFTKV_ERR_INVALID before any launch.  fp16 / e8m0
- * scale planes also need t_cap * (d/group) * (2 or 1) to be a multiple of 16.
+ * at least 16 bytes, the smallest TMA row; 16 or 32 at d = 96) and 16-byte
+ * aligned scales; anything else returns SRFTKV_ERR_INVALID before any
+ * launch.  fp16 / e8m0 scale planes, and every scale plane at d = 96 (rows
+ * of 24 or 12 bytes), are copied as rows of 16 bytes and also need
+ * t_cap * (d/group) * scale bytes to be a multiple of 16; d = 96 sides use
+ * the SRFT.
  * Range: the kernel forms p * scale_V in fp16 with p in (0, 256], so value
  * scales must stay below 255 (|z_V| < 1785 for 4-bit values, < 32385 for
  * 8-bit); larger V scales overflow to inf.  Key scales have no such limit.
@@ -204,8 +220,8 @@ int q4kv_decode_attention_static(const void* q, float* out, const srftkv_side* k
  * automatic choice on the current device).  Returns 0 for invalid sizes. */
 size_t q4kv_decode_attention_workspace_size(int B, int Hq, int Hkv, int d, int t_cap, int n_splits);
 
-/* Bytes of one packed vector: code plane d*bits/8 and scale plane 4*d/group.
- * Host-only; returns SRFTKV_OK or SRFTKV_ERR_INVALID. */
+/* Bytes of one packed vector: code plane d*bits/8 and scale plane 4*d/group
+ * (fp32 scales).  Host-only; returns SRFTKV_OK or SRFTKV_ERR_INVALID. */
 int srft_kv_vector_bytes(int d, int bits, int group, size_t* code_bytes, size_t* scale_bytes);
 
 /*

@@ -25,6 +25,8 @@
 //              keep enough of them in flight to match the load rate.
 // R_hi / R_lo are built once per CTA in shared memory from the twiddle table
 // (entries of R are closed forms of cos and sin of 2 pi jk/d).
+#include <type_traits>
+
 #include "codec_impl.cuh"
 #include "tcgen05.cuh"
 
@@ -43,7 +45,6 @@ constexpr int T_OFF_BAR = T_OFF_A + TSTAGES * T_A_BYTES;
 constexpr int T_SMEM = T_OFF_BAR + 256 + 1024;  // + barriers + alignment slack
 constexpr int T_EPI = 16;                     // epilogue warps of the quantize kernel
 constexpr int T_WARPS = 2 + T_EPI;
-constexpr uint32_t T_IDESC = tc::idesc_f16_f32(TM, TD);
 constexpr int T_NACC = 4;                     // fp32 accumulators of 128 columns in tensor memory
 constexpr uint32_t T_TMEM_COLS = 128 * T_NACC;
 }  // namespace
@@ -87,7 +88,9 @@ __device__ __forceinline__ uint32_t sw128_offset(int n, int k) {
     return (uint32_t)((k >> 6) * T_KB_BYTES + n * 128 + ((((k & 63) >> 3) ^ (n & 7)) << 4) + ((k & 7) << 1));
 }
 
-template <int BK, int BV, int SF>  // SF: the scale format of both sides (mixed calls are split on the host)
+// SF: the scale format of both sides (mixed calls are split on the host);
+// DV: the head dimension, 128 or a smaller one padded to the 128-wide tile
+template <int BK, int BV, int SF, int DV>
 __global__ void __launch_bounds__(T_WARPS * 32, 1)
     srft_quantize_tc_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
                             const __grid_constant__ CodecParams P) {
@@ -109,7 +112,7 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
         const bool srht = P.side[0].transform == SRFTKV_TRANSFORM_SRHT;
         for (int idx = threadIdx.x; idx < TD * TD; idx += blockDim.x) {
             const int n = idx >> 7, k = idx & 127;
-            float v = r_entry(n, k, P.d, srht);
+            float v = r_entry(n, k, DV, srht);
             const uint32_t sbit = (k & 1) ? 0x80000000u : 0x8000u;
             if (P.sign_mask[k >> 1] & sbit) v = -v;
             const __half hi = __float2half_rn(v);
@@ -127,7 +130,7 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
         }
         for (int a = 0; a < T_NACC; ++a) {
             ptx::mbar_init(bar(ACC_FULL + a), 1);
-            ptx::mbar_init(bar(ACC_EMPTY + a), T_EPI);
+            ptx::mbar_init(bar(ACC_EMPTY + a), 4 * (DV / 32));  // one arrival per (lane quarter, column quarter)
         }
         ptx::fence_barrier_init();
     }
@@ -170,27 +173,28 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
                 tc::fence_after_sync();
                 const uint32_t d_tmem = tmem + a * TD;
                 const uint32_t a_base = sbase + T_OFF_A + s * T_A_BYTES;
+                // d < 128: K and N stop at d (the padding columns of x and rows of R_s are zero)
+                constexpr uint32_t IDESC = tc::idesc_f16_f32(TM, DV);
 #pragma unroll
-                for (int ks = 0; ks < TD / 16; ++ks) {
+                for (int ks = 0; ks < DV / 16; ++ks) {
                     const uint32_t koff = (ks >> 2) * T_KB_BYTES + (ks & 3) * 32;
                     const uint64_t ad = tc::sw128_desc(a_base + koff);
-                    tc::mma_f16(d_tmem, ad, tc::sw128_desc(sbase + koff), T_IDESC, ks > 0);
-                    tc::mma_f16(d_tmem, ad, tc::sw128_desc(sbase + T_OFF_BLO + koff), T_IDESC, 1);
+                    tc::mma_f16(d_tmem, ad, tc::sw128_desc(sbase + koff), IDESC, ks > 0);
+                    tc::mma_f16(d_tmem, ad, tc::sw128_desc(sbase + T_OFF_BLO + koff), IDESC, 1);
                 }
                 tc::commit(bar(X_EMPTY + s));  // the x stage can be refilled once these MMAs are done
                 tc::commit(bar(ACC_FULL + a));  // accumulator a is ready for the epilogue
             }
         }
     } else {
-        // warp w reads tensor-memory lanes 32(w%4)..+31 (tile rows) and column quarter cq
-        const int quarter = warp & 3, cq = (warp - 2) >> 2;
-        for (int t = blockIdx.x, i = 0; t < P.total_tiles; t += stride, ++i) {
-            const int a = i % T_NACC;
-            const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(bar(ACC_FULL + a), (i / T_NACC) & 1));
-            if (!ok) {
-                failed = true;
-                break;
-            }
+        // Work units: (lane quarter, 32-column quarter) of a tile; a warp may
+        // only read tensor-memory lanes 32(w%4)..+31.  unit(): wait for
+        // accumulator a, read the unit's 32 x 32 block, release the
+        // accumulator, then lambda, quantise and store the 32 rows.
+        const int quarter = warp & 3;
+        auto unit = [&](int t, int a, int cq, uint32_t parity) -> bool {
+            const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(bar(ACC_FULL + a), parity));
+            if (!ok) return false;
             tc::fence_after_sync();
             uint32_t r0[32];
             const uint32_t taddr = tmem + ((uint32_t)(32 * quarter) << 16) + a * TD + cq * 32;
@@ -203,13 +207,13 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
             const TileId id = decode_tile128(P, t);
             const CodecSideK& S = P.side[id.side];
             const int t_tok = id.t0 + 32 * quarter + lane;
-            if (t_tok >= P.n_tokens || 32 * cq >= P.d) continue;
+            if (t_tok >= P.n_tokens) return true;
             float z[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) z[j] = __uint_as_float(r0[j]);
             if (S.lambda != nullptr) {
                 const float4* lr = reinterpret_cast<const float4*>(
-                    S.lambda + (long long)id.o * S.lambda_outer_stride + (long long)id.h * P.d + cq * 32);
+                    S.lambda + (long long)id.o * S.lambda_outer_stride + (long long)id.h * DV + cq * 32);
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     const float4 l = __ldg(lr + c);
@@ -220,14 +224,44 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
                 }
             }
             const long long vrow = packed_row(P, id, t_tok);
-            // groups of at most 32: a column quarter holds whole groups; quarters past d hold padding
-            const int ng = P.d / P.group;
+            // groups of at most 32: a column quarter holds whole groups
+            const int ng = DV / P.group;
             if (BK == BV || id.side == 0)
-                quant_store_row<32, BK, SF>(z, P.group, S.codes + vrow * (P.d * BK / 8) + cq * (32 * BK / 8),
-                                            S.scales + (vrow * ng + cq * (32 / P.group)) * S.sbytes);
+                quant_store_row<32, BK, SF>(z, P.group, S.codes + vrow * (DV * BK / 8) + cq * (32 * BK / 8),
+                                            S.scales + (vrow * ng + cq * (ng / (DV / 32))) * S.sbytes);
             else
-                quant_store_row<32, BV, SF>(z, P.group, S.codes + vrow * (P.d * BV / 8) + cq * (32 * BV / 8),
-                                            S.scales + (vrow * ng + cq * (32 / P.group)) * S.sbytes);
+                quant_store_row<32, BV, SF>(z, P.group, S.codes + vrow * (DV * BV / 8) + cq * (32 * BV / 8),
+                                            S.scales + (vrow * ng + cq * (ng / (DV / 32))) * S.sbytes);
+            return true;
+        };
+        if constexpr (DV == TD) {
+            // warp w: the same column quarter (w-2)/4 of every tile
+            const int cq = (warp - 2) >> 2;
+            for (int t = blockIdx.x, i = 0; t < P.total_tiles; t += stride, ++i)
+                if (!unit(t, i % T_NACC, cq, (i / T_NACC) & 1)) {
+                    failed = true;
+                    break;
+                }
+        } else {
+            // NQ = DV/32 column quarters, 4 NQ units a tile, 16 NQ for the
+            // T_NACC = 4 tiles of one round of the accumulators: each of the 16
+            // warps takes NQ of them, units x, x+16, x+32, ... in tile order (x
+            // keeps the warp's lane quarter: unit u's is u % 4), so at d = 96
+            // the 12 units of a tile spread over all 16 warps.
+            static_assert(T_NACC == 4 && T_EPI == 16, "units per warp and round");
+            constexpr int NQ = DV / 32, U = 4 * NQ;
+            const int x = ((warp - 2) & ~3) | quarter;
+            for (int r = 0; blockIdx.x + T_NACC * r * stride < P.total_tiles && !failed; ++r)
+#pragma unroll 1
+                for (int uj = 0; uj < NQ; ++uj) {
+                    const int u = x + 16 * uj, tr = u / U;
+                    const int t = blockIdx.x + (T_NACC * r + tr) * stride;
+                    if (t >= P.total_tiles) break;  // later units belong to later tiles
+                    if (!unit(t, tr, (u % U) >> 2, r & 1)) {
+                        failed = true;
+                        break;
+                    }
+                }
         }
     }
     if (failed) atomicOr(P.fault, 1u);
@@ -430,7 +464,7 @@ __device__ __forceinline__ void dequant_half_smem(const uint8_t* __restrict__ in
 // K order of dq_kperm (no lambda): codes -> exact fp16 pairs -> times the
 // group scale split into fp16 hi + lo, P_hat = fp16(q s_hi + fp16(q s_lo)), one
 // main rounding as when the fp32 product q s is rounded to fp16.
-template <int BITS, int DV>
+template <int BITS, int DV, int NK = 8>  // NK: 8-element words of the half to convert (the rest is padding past d)
 __device__ __forceinline__ void dequant_half_pairs(const uint8_t* __restrict__ in, int m, int hf, const float (&sc)[4],
                                                    uint32_t (&hp)[32]) {
     constexpr int NCH = 64 * BITS / 128;
@@ -444,7 +478,11 @@ __device__ __forceinline__ void dequant_half_pairs(const uint8_t* __restrict__ i
         sl[g] = half2_bcast(__float2half_rn(sc[g] - __half2float(h)));
     }
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {  // 8-element word k of the half: coordinates 64 hf + 8k .. +7, group k/2
+    for (int k = NK; k < 8; ++k)  // padding past d: the contraction stops at d
+#pragma unroll
+        for (int j = 0; j < 4; ++j) hp[4 * k + j] = 0u;
+#pragma unroll
+    for (int k = 0; k < NK; ++k) {  // 8-element word k of the half: coordinates 64 hf + 8k .. +7, group k/2
         uint32_t c[4];
         if constexpr (BITS == 4) {
             const uint32_t x = w[k], xs = x >> 8;
@@ -532,10 +570,12 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
                 tc::fence_after_sync();
                 const uint32_t d_tmem = tmem + s * TD;
                 const uint32_t a_tmem = tmem + DQ_A_COL + b * 64;
+                // d < 128: K and N stop at d (accumulator columns past d are never stored)
+                constexpr uint32_t IDESC = tc::idesc_f16_f32(TM, DV);
 #pragma unroll
-                for (int ks = 0; ks < TD / 16; ++ks) {
+                for (int ks = 0; ks < DV / 16; ++ks) {
                     const uint32_t koff = (ks >> 2) * T_KB_BYTES + (ks & 3) * 32;
-                    tc::mma_f16_ta(d_tmem, a_tmem + 8 * ks, tc::sw128_desc(sbase + koff), T_IDESC, ks > 0);
+                    tc::mma_f16_ta(d_tmem, a_tmem + 8 * ks, tc::sw128_desc(sbase + koff), IDESC, ks > 0);
                 }
                 tc::commit(bar(A_EMPTY + b));  // A buffer b may be rewritten
                 tc::commit(bar(ACC_FULL + s));  // accumulator s is ready
@@ -584,10 +624,17 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
             float sc[4];
             half_row_scales(in, C::OFF_SC, m, hf, P.group, S.sfmt, DV, sc);
             if (S.lambda == nullptr) {
-                if (side_k)
+                constexpr int NK1 = DV == TD ? 8 : (DV - 64) / 8;  // words of the second half inside d
+                if (DV != TD && hf == 1) {
+                    if (side_k)
+                        dequant_half_pairs<BK, DV, NK1>(in, m, hf, sc, hp);
+                    else
+                        dequant_half_pairs<BV, DV, NK1>(in, m, hf, sc, hp);
+                } else if (side_k) {
                     dequant_half_pairs<BK, DV>(in, m, hf, sc, hp);
-                else
+                } else {
                     dequant_half_pairs<BV, DV>(in, m, hf, sc, hp);
+                }
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar(IN_EMPTY + st));  // input stage consumed
             } else {
@@ -644,10 +691,17 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
             tc::fence_after_sync();
             uint32_t v[2][32];
             const uint32_t taddr = tmem + ((uint32_t)(32 * quarter) << 16) + s * TD + 64 * hf;
+            // d = 96: the second half holds 32 columns of output (the store clips the rest)
+            const bool short_half = DV != TD && hf == 1;
+            if (short_half) {
+                tc::ld_32x32b_x32(taddr, v[0]);
+                tc::wait_ld(v[0]);
+            } else {
 #pragma unroll
-            for (int j = 0; j < 2; ++j) tc::ld_32x32b_x32(taddr + 32 * j, v[j]);
+                for (int j = 0; j < 2; ++j) tc::ld_32x32b_x32(taddr + 32 * j, v[j]);
 #pragma unroll
-            for (int j = 0; j < 2; ++j) tc::wait_ld(v[j]);
+                for (int j = 0; j < 2; ++j) tc::wait_ld(v[j]);
+            }
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(ACC_EMPTY + s));
@@ -655,16 +709,22 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
             if (leader) ptx::bulk_wait_read<1>();
             ptx::named_bar_sync(1, 32 * DQ_EPI);
             uint8_t* O = smem + DQ_OFF_O + s * T_A_BYTES;
+            auto stage_chunks = [&](auto nch) {
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                const int j = ch >> 2, c0 = (ch & 3) * 8;
-                uint4 w;
-                w.x = pack_half2(__uint_as_float(v[j][c0 + 0]), __uint_as_float(v[j][c0 + 1]));
-                w.y = pack_half2(__uint_as_float(v[j][c0 + 2]), __uint_as_float(v[j][c0 + 3]));
-                w.z = pack_half2(__uint_as_float(v[j][c0 + 4]), __uint_as_float(v[j][c0 + 5]));
-                w.w = pack_half2(__uint_as_float(v[j][c0 + 6]), __uint_as_float(v[j][c0 + 7]));
-                *reinterpret_cast<uint4*>(O + sw128_offset(m, 64 * hf + 8 * ch)) = w;
-            }
+                for (int ch = 0; ch < decltype(nch)::value; ++ch) {
+                    const int j = ch >> 2, c0 = (ch & 3) * 8;
+                    uint4 w;
+                    w.x = pack_half2(__uint_as_float(v[j][c0 + 0]), __uint_as_float(v[j][c0 + 1]));
+                    w.y = pack_half2(__uint_as_float(v[j][c0 + 2]), __uint_as_float(v[j][c0 + 3]));
+                    w.z = pack_half2(__uint_as_float(v[j][c0 + 4]), __uint_as_float(v[j][c0 + 5]));
+                    w.w = pack_half2(__uint_as_float(v[j][c0 + 6]), __uint_as_float(v[j][c0 + 7]));
+                    *reinterpret_cast<uint4*>(O + sw128_offset(m, 64 * hf + 8 * ch)) = w;
+                }
+            };
+            if (short_half)
+                stage_chunks(std::integral_constant<int, 4>{});
+            else
+                stage_chunks(std::integral_constant<int, 8>{});
             ptx::fence_proxy_async_smem();
             ptx::named_bar_sync(1, 32 * DQ_EPI);
             if (leader) {
@@ -750,7 +810,7 @@ static int launch_dq_tc(const CodecCall& c) {
     return SRFTKV_OK;
 }
 
-template <int BK, int BV, int SF>
+template <int BK, int BV, int SF, int DV>
 static int launch_tc(const CodecCall& c) {
     CodecParams P;
     fill_params(c, P);
@@ -766,12 +826,13 @@ static int launch_tc(const CodecCall& c) {
     }
     static bool attr = false;
     if (!attr) {
-        cudaFuncSetAttribute(srft_quantize_tc_kernel<BK, BV, SF>, cudaFuncAttributeMaxDynamicSharedMemorySize, T_SMEM);
+        cudaFuncSetAttribute(srft_quantize_tc_kernel<BK, BV, SF, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             T_SMEM);
         attr = true;
     }
     int blocks = device_sm_count();
     if (blocks > P.total_tiles) blocks = P.total_tiles;
-    srft_quantize_tc_kernel<BK, BV, SF><<<blocks, T_WARPS * 32, T_SMEM, c.stream>>>(tm[0], tm[1], P);
+    srft_quantize_tc_kernel<BK, BV, SF, DV><<<blocks, T_WARPS * 32, T_SMEM, c.stream>>>(tm[0], tm[1], P);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("tensor-core quantize launch failed: %s", cudaGetErrorString(e));
@@ -780,21 +841,25 @@ static int launch_tc(const CodecCall& c) {
     return SRFTKV_OK;
 }
 
-template <int SF>
+template <int SF, int DV>
 static int launch_tc_bits(const CodecCall& c, int bk, int bv) {
-    if (bk == 4 && bv == 4) return launch_tc<4, 4, SF>(c);
-    if (bk == 8 && bv == 8) return launch_tc<8, 8, SF>(c);
-    if (bk == 8 && bv == 4) return launch_tc<8, 4, SF>(c);
-    return launch_tc<4, 8, SF>(c);
+    if (bk == 4 && bv == 4) return launch_tc<4, 4, SF, DV>(c);
+    if (bk == 8 && bv == 8) return launch_tc<8, 8, SF, DV>(c);
+    if (bk == 8 && bv == 4) return launch_tc<8, 4, SF, DV>(c);
+    return launch_tc<4, 8, SF, DV>(c);
+}
+template <int SF>
+static int launch_tc_dim(const CodecCall& c, int bk, int bv) {
+    return c.d == 96 ? launch_tc_bits<SF, 96>(c, bk, bv) : launch_tc_bits<SF, TD>(c, bk, bv);
 }
 
 int codec_quantize_tc(const CodecCall& c) {
     if ((c.d != TD && c.d != 96) || c.group > 32) return 1;  // a group must fit in one epilogue thread's 32 columns
     const int bk = c.side[0].bits, bv = c.n_sides > 1 ? c.side[1].bits : bk;
     const int sf = c.side[0].scale_format;  // both sides share it (mixed calls are split on the host)
-    if (sf == SRFTKV_SCALE_FP16) return launch_tc_bits<SRFTKV_SCALE_FP16>(c, bk, bv);
-    if (sf == SRFTKV_SCALE_E8M0) return launch_tc_bits<SRFTKV_SCALE_E8M0>(c, bk, bv);
-    return launch_tc_bits<SRFTKV_SCALE_FP32>(c, bk, bv);
+    if (sf == SRFTKV_SCALE_FP16) return launch_tc_dim<SRFTKV_SCALE_FP16>(c, bk, bv);
+    if (sf == SRFTKV_SCALE_E8M0) return launch_tc_dim<SRFTKV_SCALE_E8M0>(c, bk, bv);
+    return launch_tc_dim<SRFTKV_SCALE_FP32>(c, bk, bv);
 }
 
 template <int DV>
