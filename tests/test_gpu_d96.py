@@ -232,3 +232,52 @@ def test_attention_d96_rejects_unaligned_scale_rows():
     ws = torch.empty(K.q4kv_decode_attention_workspace_size(B, 4, Hkv, D, t_cap, 0), dtype=torch.uint8, device="cuda")
     with pytest.raises(RuntimeError, match="multiple of 16"):
         K.q4kv_decode_attention(q, out, sk, sv, B, 4, Hkv, D, 16, t_cap, None, 0.0, 1, 0, ws)
+
+
+def test_d96_decode_shape_full_size_sampled():
+    """The decode workload's cache shape at d = 96 (B=16, Hkv=8, T=131072, Hq=32; the bench's d = 96 variant, in
+    the launch configuration it times): the whole cache quantised and dequantised in one launch each, attention
+    over all of it with the automatic split count; rows and (b, kv head) pairs sampled for the oracle."""
+    w = I.DECODE.resized(d=D)
+    B, Hkv, T, Hq, seed = w.n_outer, w.kv_heads, w.tokens, w.q_heads, w.sign_seed
+    rep = Hq // Hkv
+    xk, xv = I.kv_side(w, "k", device="cuda"), I.kv_side(w, "v", device="cuda")
+    sk, sv = K.alloc_side(B, T, Hkv, D, 4, 16), K.alloc_side(B, T, Hkv, D, 4, 16)
+    sk.x, sv.x = xk, xv
+    K.srft_kv_quantize(sk, sv, B, T, Hkv, D, 16, T, 0, seed)
+    ok_, ov_ = torch.empty_like(xk), torch.empty_like(xv)
+    K.srft_kv_dequantize(K.Side(sk.codes, sk.scales, 4, x=ok_), K.Side(sv.codes, sv.scales, 4, x=ov_), B, T, Hkv, D,
+                         16, T, 0, seed)
+    q = I.query(w, device="cuda")
+    out = run_attention_d96(q, sk, sv, B, Hq, Hkv, T, seed)
+    torch.cuda.synchronize()
+    gen = np.random.default_rng(96)
+    qn = _np(q).astype(np.float64)
+    for b, h in ((0, 0), (B - 1, Hkv - 1), (7, 3)):
+        rows = np.sort(gen.choice(T, 256, replace=False))
+        for side, x, xhat in ((sk, xk, ok_), (sv, xv, ov_)):
+            xs = _np(x[b, rows, h]).astype(np.float64)[None, :, None, :]
+            enc = O.srft_kv_quantize(xs, None, 4, 16, seed)
+            codes = _np(side.codes[b, h, rows])[None, :, None, :]
+            scales = _np(side.scales[b, h, rows])[None, :, None, :]
+            assert_scales(scales, enc["scales"])
+            assert_codes(codes, enc["r"], 4)
+            mine = O.srft_kv_dequantize(codes, scales.astype(np.float64), None, 4, 16, seed)
+            got = _np(xhat[b, rows, h]).astype(np.float64)[None, :, None, :]
+            assert np.abs(got - mine).max() <= np.abs(mine).max() * 2.0**-10 + 1e-5
+        kh = O.srft_kv_dequantize(_np(sk.codes[b, h]), _np(sk.scales[b, h]).astype(np.float64), None, 4, 16, seed)
+        vh = O.srft_kv_dequantize(_np(sv.codes[b, h]), _np(sv.scales[b, h]).astype(np.float64), None, 4, 16, seed)
+        for r in range(rep):
+            hq = h * rep + r
+            s = kh @ qn[b, hq] / np.sqrt(D)
+            pw = np.exp(s - s.max())
+            ref = (pw @ vh) / pw.sum()
+            assert np.abs(out[b, hq] - ref).max() <= ATTN_ATOL
+
+
+def run_attention_d96(q, sk, sv, B, Hq, Hkv, T, seed):
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device="cuda")
+    ws = torch.empty(K.q4kv_decode_attention_workspace_size(B, Hq, Hkv, D, T, 0), dtype=torch.uint8, device="cuda")
+    K.q4kv_decode_attention(q, out, sk, sv, B, Hq, Hkv, D, 16, T, None, 0.0, seed, 0, ws)
+    torch.cuda.synchronize()
+    return _np(out)
