@@ -374,6 +374,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                        "fp16_cache_ms": f96, "attn_speedup_vs_fp16_cache": f96 / av}
     del rk96, rv96, xk96, xv96, q96, out96, ws96, ws96r
 
+    other = other_workloads(K, I, torch, dev, stream, time_launch) if rank == 0 else None
+
     # fp16-cache comparator: the same attention kernel on the raw fp16 cache (head-major like the packed planes)
     raw_k = K.Side(xk.permute(0, 2, 1, 3).contiguous(), None, 16)
     raw_v = K.Side(xv.permute(0, 2, 1, 3).contiguous(), None, 16)
@@ -461,6 +463,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                       "traffic": recorded_traffic("q4kv_attn_split_kernel")},
         "append_us": med["append"] * 1e3,
         "variants": variants,
+        "other_workloads": other,
         "gpu_launches": LAUNCHES * args.steps,
         "clocks": clk,
         "e2e": e2e,
@@ -468,6 +471,79 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "kernel_source_sha": {k: kernel_source_sha(k) for k in KERNEL_SOURCES},
     }
     print(json.dumps(line), flush=True)
+
+
+def other_workloads(K, I, torch, dev, stream, time_launch):
+    """The codec workloads besides the decode cache, each launch timed alone (median of 10, CUDA events on the
+    launching stream): the Gemma-3-1B-shaped cache (d = 256, 0.21 M vectors, 150 MB: L2 flushed before every
+    launch by writing 256 MB), the Qwen2.5-1.5B-shaped cache with per-channel lambda (3.67 M vectors, 1.29 GB)
+    and the K8V4 one-token append onto a prebuilt 7B-like cache (K int8 / V int4, 256 + 256 vectors a step)."""
+    out = {}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def timed(fn, l2_flush):
+        def run():
+            fn()
+        if not l2_flush:
+            return time_launch(run)
+        ts = []
+        for _ in range(12):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts[2:])
+
+    for key, w, l2_flush in (("gemma_d256", I.GEMMA, True), ("qwen_d128_lambda", I.QWEN, False)):
+        n, T, H, d, G, seed = w.n_outer, w.tokens, w.kv_heads, w.d, w.group, w.sign_seed
+        xk, xv = I.kv_side(w, "k", device=dev), I.kv_side(w, "v", device=dev)
+        lk, lv = I.lam_table(w, "k", device=dev), I.lam_table(w, "v", device=dev)
+        sk, sv = K.alloc_side(n, T, H, d, 4, G, device=dev), K.alloc_side(n, T, H, d, 4, G, device=dev)
+        sk.x, sv.x, sk.lam, sv.lam = xk, xv, lk, lv
+        qms = timed(lambda: K.srft_kv_quantize(sk, sv, n, T, H, d, G, T, 0, seed, stream), l2_flush)
+        ok, ov = torch.empty_like(xk), torch.empty_like(xv)
+        dk, dv = K.Side(sk.codes, sk.scales, 4, x=ok, lam=lk), K.Side(sv.codes, sv.scales, 4, x=ov, lam=lv)
+        dms = timed(lambda: K.srft_kv_dequantize(dk, dv, n, T, H, d, G, T, 0, seed, stream), l2_flush)
+        vec = 2 * n * T * H
+        vb = 2 * d + d // 2 + 4 * (d // G)
+        rel = [float(((o.float() - x.float()) ** 2).sum() / (x.float() ** 2).sum()) for o, x in ((ok, xk), (ov, xv))]
+        out[key] = {"workload": w.name, "vectors": vec, "bytes_per_vector": vb,
+                    "quant_ms": qms, "quant_vectors_per_s": vec / (qms * 1e-3), "quant_gbs": vec * vb / (qms * 1e-3) / 1e9,
+                    "deq_ms": dms, "deq_gbs": vec * vb / (dms * 1e-3) / 1e9,
+                    "relative_mse_k_v": rel, "l2_flushed": l2_flush}
+        del xk, xv, sk, sv, ok, ov, dk, dv
+
+    w = I.K8V4
+    n, T, H, d, G, seed, t_cap = w.n_outer, w.tokens, w.kv_heads, w.d, w.group, w.sign_seed, w.t_cap
+    xk, xv = I.kv_side(w, "k", device=dev), I.kv_side(w, "v", device=dev)
+    sk = K.alloc_side(n, t_cap, H, d, w.bits_k, G, device=dev)
+    sv = K.alloc_side(n, t_cap, H, d, w.bits_v, G, device=dev)
+    sk.x, sv.x = xk, xv
+    K.srft_kv_quantize(sk, sv, n, T, H, d, G, t_cap, 0, seed, stream)  # the prebuilt cache
+    del xk, xv
+    g = torch.Generator(device=dev).manual_seed(404)
+    nk = torch.randn((n, 1, H, d), generator=g, device=dev).half()
+    nv = torch.randn((n, 1, H, d), generator=g, device=dev).half()
+    ak = K.Side(sk.codes, sk.scales, w.bits_k, x=nk)
+    av = K.Side(sv.codes, sv.scales, w.bits_v, x=nv)
+    ts = []
+    for step in range(102):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        K.srft_kv_quantize(ak, av, n, 1, H, d, G, t_cap, T + step % (t_cap - T), seed, stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    vb_k, vb_v = 2 * d + d * w.bits_k // 8 + 4 * (d // G), 2 * d + d * w.bits_v // 8 + 4 * (d // G)
+    out["k8v4_append"] = {"workload": w.name, "vectors_per_step": 2 * n * H,
+                          "bytes_per_step": n * H * (vb_k + vb_v), "append_us_median": statistics.median(ts[2:]) * 1e3,
+                          "append_us_min": min(ts[2:]) * 1e3}
+    del sk, sv, flush
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_case(args):

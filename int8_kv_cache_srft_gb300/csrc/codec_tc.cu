@@ -25,8 +25,6 @@
 //              keep enough of them in flight to match the load rate.
 // R_hi / R_lo are built once per CTA in shared memory from the twiddle table
 // (entries of R are closed forms of cos and sin of 2 pi jk/d).
-#include <type_traits>
-
 #include "codec_impl.cuh"
 #include "tcgen05.cuh"
 
@@ -464,7 +462,7 @@ __device__ __forceinline__ void dequant_half_smem(const uint8_t* __restrict__ in
 // K order of dq_kperm (no lambda): codes -> exact fp16 pairs -> times the
 // group scale split into fp16 hi + lo, P_hat = fp16(q s_hi + fp16(q s_lo)), one
 // main rounding as when the fp32 product q s is rounded to fp16.
-template <int BITS, int DV, int NK = 8>  // NK: 8-element words of the half to convert (the rest is padding past d)
+template <int BITS, int DV>
 __device__ __forceinline__ void dequant_half_pairs(const uint8_t* __restrict__ in, int m, int hf, const float (&sc)[4],
                                                    uint32_t (&hp)[32]) {
     constexpr int NCH = 64 * BITS / 128;
@@ -478,11 +476,7 @@ __device__ __forceinline__ void dequant_half_pairs(const uint8_t* __restrict__ i
         sl[g] = half2_bcast(__float2half_rn(sc[g] - __half2float(h)));
     }
 #pragma unroll
-    for (int k = NK; k < 8; ++k)  // padding past d: the contraction stops at d
-#pragma unroll
-        for (int j = 0; j < 4; ++j) hp[4 * k + j] = 0u;
-#pragma unroll
-    for (int k = 0; k < NK; ++k) {  // 8-element word k of the half: coordinates 64 hf + 8k .. +7, group k/2
+    for (int k = 0; k < 8; ++k) {  // 8-element word k of the half: coordinates 64 hf + 8k .. +7, group k/2
         uint32_t c[4];
         if constexpr (BITS == 4) {
             const uint32_t x = w[k], xs = x >> 8;
@@ -497,6 +491,101 @@ __device__ __forceinline__ void dequant_half_pairs(const uint8_t* __restrict__ i
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) hp[4 * k + j] = h2fma(c[j], sh[k >> 1], h2mul(c[j], sl[k >> 1]));
+    }
+}
+
+// d = 96: the two halves of a row are six 8-coordinate words each, words
+// 4h..4h+3 (coordinates 32h..32h+31) and 8+2h, 9+2h (coordinates 64+16h..+15)
+// for half h, so both do equal work and every tensor-memory access stays
+// naturally aligned: A columns 16h..+15 and 32+8h..+7 (column c holds word
+// c/4), accumulator columns 32h..+31 and 64+16h..+15 (one per coordinate).
+__device__ __forceinline__ int d96_word(int hf, int k) { return k < 4 ? 4 * hf + k : 8 + 2 * hf + (k - 4); }
+
+// The code words of half hf of tile row m (48- or 96-byte unswizzled rows):
+// int4 word k is w[k], int8 word k is w[2k], w[2k+1].
+template <int BITS>
+__device__ __forceinline__ void d96_half_words(const uint8_t* __restrict__ in, int m, int hf,
+                                               uint32_t (&w)[6 * BITS / 4]) {
+    const uint8_t* row = in + m * (96 * BITS / 8);
+    if constexpr (BITS == 4) {
+        const uint4 a = *reinterpret_cast<const uint4*>(row + 16 * hf);
+        const uint2 c = *reinterpret_cast<const uint2*>(row + 32 + 8 * hf);
+        w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = c.x; w[5] = c.y;
+    } else {
+        const uint4 a = *reinterpret_cast<const uint4*>(row + 32 * hf);
+        const uint4 b = *reinterpret_cast<const uint4*>(row + 32 * hf + 16);
+        const uint4 c = *reinterpret_cast<const uint4*>(row + 64 + 16 * hf);
+        w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+        w[8] = c.x; w[9] = c.y; w[10] = c.z; w[11] = c.w;
+    }
+}
+
+// The scales of half hf's three 16-coordinate units 2hf, 2hf+1, 4+hf (flat rows of 96/group scales)
+__device__ __forceinline__ void d96_half_scales(const uint8_t* __restrict__ in, int off_sc, int m, int hf, int group,
+                                                int sfmt, float (&sc)[3]) {
+    const int ng = 96 / group, sb = sfmt == SRFTKV_SCALE_FP32 ? 4 : sfmt == SRFTKV_SCALE_FP16 ? 2 : 1;
+    const uint8_t* row = in + off_sc + m * ng * sb;
+    const int units[3] = {2 * hf, 2 * hf + 1, 4 + hf};
+#pragma unroll
+    for (int u = 0; u < 3; ++u) {
+        const int gi = 16 * units[u] / group;
+        if (sfmt == SRFTKV_SCALE_FP32) sc[u] = *reinterpret_cast<const float*>(row + 4 * gi);
+        else if (sfmt == SRFTKV_SCALE_FP16) sc[u] = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(row + 2 * gi)));
+        else sc[u] = __uint_as_float((uint32_t)row[gi] << 23);
+    }
+}
+
+// fp16 pairs (coordinates 8w+j, 8w+j+4; j = 0..3) of half hf of a d = 96 row,
+// codes * scale (then / lambda when lam is given), in the order of the A columns
+template <int BITS>
+__device__ __forceinline__ void d96_half_pairs(const uint8_t* __restrict__ in, int off_sc, int m, int hf, int group,
+                                               int sfmt, const float* __restrict__ lam, uint32_t (&hp)[24]) {
+    uint32_t w[6 * BITS / 4];
+    d96_half_words<BITS>(in, m, hf, w);
+    float sc[3];
+    d96_half_scales(in, off_sc, m, hf, group, sfmt, sc);
+    if (lam == nullptr) {  // exact code pairs times the scale split into fp16 hi + lo
+        uint32_t sh[3], sl[3];
+#pragma unroll
+        for (int u = 0; u < 3; ++u) {
+            const __half h = __float2half_rn(sc[u]);
+            sh[u] = half2_bcast(h);
+            sl[u] = half2_bcast(__float2half_rn(sc[u] - __half2float(h)));
+        }
+#pragma unroll
+        for (int k = 0; k < 6; ++k) {
+            const int u = k < 4 ? k >> 1 : 2;
+            uint32_t c[4];
+            if constexpr (BITS == 4) {
+                const uint32_t x = w[k], xs = x >> 8;
+                c[0] = codes_lo4(x);
+                c[1] = codes_hi4(x);
+                c[2] = codes_lo4(xs);
+                c[3] = codes_hi4(xs);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    c[j] = codes_b8(__byte_perm(w[2 * k], w[2 * k + 1], j | (j << 4) | ((4 + j) << 8) | ((4 + j) << 12)));
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) hp[4 * k + j] = h2fma(c[j], sh[u], h2mul(c[j], sl[u]));
+        }
+        return;
+    }
+#pragma unroll
+    for (int k = 0; k < 6; ++k) {
+        const int u = k < 4 ? k >> 1 : 2, e0 = 8 * d96_word(hf, k);
+        const float4 l0 = __ldg(reinterpret_cast<const float4*>(lam + e0));
+        const float4 l1 = __ldg(reinterpret_cast<const float4*>(lam + e0 + 4));
+        const float li[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+        float p[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+            const float c = (BITS == 4) ? code_int4(w[k], jj) : code_int8(w[2 * k + (jj >> 2)], jj & 3);
+            p[jj] = __fdividef(c * sc[u], li[jj]);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) hp[4 * k + j] = pack_half2(p[j], p[j + 4]);
     }
 }
 
@@ -621,20 +710,40 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
             const uint8_t* in = smem + DQ_OFF_IN + st * C::STAGE;
             uint32_t hp[32];  // fp16 pairs in the K order of dq_kperm: column 32 hf + c
             const bool side_k = BK == BV || id.side == 0;
+            if constexpr (DV != TD) {  // d = 96: balanced halves of six words (d96_word)
+                const float* lam = (S.lambda != nullptr && t_tok < P.n_tokens)
+                                       ? S.lambda + (long long)id.o * S.lambda_outer_stride + (long long)id.h * DV
+                                       : nullptr;
+                uint32_t (&h24)[24] = *reinterpret_cast<uint32_t(*)[24]>(hp);
+                if (side_k)
+                    d96_half_pairs<BK>(in, C::OFF_SC, m, hf, P.group, S.sfmt, lam, h24);
+                else
+                    d96_half_pairs<BV>(in, C::OFF_SC, m, hf, P.group, S.sfmt, lam, h24);
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(IN_EMPTY + st));  // input stage consumed
+                const bool ok = __all_sync(0xffffffffu,
+                                           i < DQ_NA || ptx::mbar_wait_bounded(bar(A_EMPTY + b), (i / DQ_NA - 1) & 1));
+                if (!ok) {
+                    failed = true;
+                    break;
+                }
+                tc::fence_after_sync();  // the MMAs that read A buffer b are complete
+                const uint32_t acol = tmem + ((uint32_t)(32 * quarter) << 16) + DQ_A_COL + b * 64;
+                tc::st_32x32b_x16(acol + 16 * hf, hp);
+                tc::st_32x32b_x8(acol + 32 + 8 * hf, hp + 16);
+                tc::wait_st();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(A_FULL + b));
+                continue;
+            }
             float sc[4];
             half_row_scales(in, C::OFF_SC, m, hf, P.group, S.sfmt, DV, sc);
             if (S.lambda == nullptr) {
-                constexpr int NK1 = DV == TD ? 8 : (DV - 64) / 8;  // words of the second half inside d
-                if (DV != TD && hf == 1) {
-                    if (side_k)
-                        dequant_half_pairs<BK, DV, NK1>(in, m, hf, sc, hp);
-                    else
-                        dequant_half_pairs<BV, DV, NK1>(in, m, hf, sc, hp);
-                } else if (side_k) {
+                if (side_k)
                     dequant_half_pairs<BK, DV>(in, m, hf, sc, hp);
-                } else {
+                else
                     dequant_half_pairs<BV, DV>(in, m, hf, sc, hp);
-                }
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar(IN_EMPTY + st));  // input stage consumed
             } else {
@@ -690,17 +799,18 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
             }
             tc::fence_after_sync();
             uint32_t v[2][32];
-            const uint32_t taddr = tmem + ((uint32_t)(32 * quarter) << 16) + s * TD + 64 * hf;
-            // d = 96: the second half holds 32 columns of output (the store clips the rest)
-            const bool short_half = DV != TD && hf == 1;
-            if (short_half) {
-                tc::ld_32x32b_x32(taddr, v[0]);
-                tc::wait_ld(v[0]);
-            } else {
+            const uint32_t lanes = tmem + ((uint32_t)(32 * quarter) << 16) + s * TD;
+            if constexpr (DV == TD) {
 #pragma unroll
-                for (int j = 0; j < 2; ++j) tc::ld_32x32b_x32(taddr + 32 * j, v[j]);
+                for (int j = 0; j < 2; ++j) tc::ld_32x32b_x32(lanes + 64 * hf + 32 * j, v[j]);
 #pragma unroll
                 for (int j = 0; j < 2; ++j) tc::wait_ld(v[j]);
+            } else {  // d = 96: columns 32hf..+31 and 64+16hf..+15 (d96_word)
+                uint32_t (&v16)[16] = *reinterpret_cast<uint32_t(*)[16]>(v[1]);
+                tc::ld_32x32b_x32(lanes + 32 * hf, v[0]);
+                tc::ld_32x32b_x16(lanes + 64 + 16 * hf, v16);
+                tc::wait_ld(v[0]);
+                tc::wait_ld(v16);
             }
             tc::fence_before_sync();
             __syncwarp();
@@ -709,22 +819,19 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
             if (leader) ptx::bulk_wait_read<1>();
             ptx::named_bar_sync(1, 32 * DQ_EPI);
             uint8_t* O = smem + DQ_OFF_O + s * T_A_BYTES;
-            auto stage_chunks = [&](auto nch) {
+            // 8-column chunk ch (of 8 here, 6 at d = 96) -> its output column
+            constexpr int NCHK = DV == TD ? 8 : 6;
 #pragma unroll
-                for (int ch = 0; ch < decltype(nch)::value; ++ch) {
-                    const int j = ch >> 2, c0 = (ch & 3) * 8;
-                    uint4 w;
-                    w.x = pack_half2(__uint_as_float(v[j][c0 + 0]), __uint_as_float(v[j][c0 + 1]));
-                    w.y = pack_half2(__uint_as_float(v[j][c0 + 2]), __uint_as_float(v[j][c0 + 3]));
-                    w.z = pack_half2(__uint_as_float(v[j][c0 + 4]), __uint_as_float(v[j][c0 + 5]));
-                    w.w = pack_half2(__uint_as_float(v[j][c0 + 6]), __uint_as_float(v[j][c0 + 7]));
-                    *reinterpret_cast<uint4*>(O + sw128_offset(m, 64 * hf + 8 * ch)) = w;
-                }
-            };
-            if (short_half)
-                stage_chunks(std::integral_constant<int, 4>{});
-            else
-                stage_chunks(std::integral_constant<int, 8>{});
+            for (int ch = 0; ch < NCHK; ++ch) {
+                const int j = ch >> 2, c0 = (ch & 3) * 8;
+                const int col = DV == TD ? 64 * hf + 8 * ch : (ch < 4 ? 32 * hf + 8 * ch : 64 + 16 * hf + 8 * (ch - 4));
+                uint4 w;
+                w.x = pack_half2(__uint_as_float(v[j][c0 + 0]), __uint_as_float(v[j][c0 + 1]));
+                w.y = pack_half2(__uint_as_float(v[j][c0 + 2]), __uint_as_float(v[j][c0 + 3]));
+                w.z = pack_half2(__uint_as_float(v[j][c0 + 4]), __uint_as_float(v[j][c0 + 5]));
+                w.w = pack_half2(__uint_as_float(v[j][c0 + 6]), __uint_as_float(v[j][c0 + 7]));
+                *reinterpret_cast<uint4*>(O + sw128_offset(m, col)) = w;
+            }
             ptx::fence_proxy_async_smem();
             ptx::named_bar_sync(1, 32 * DQ_EPI);
             if (leader) {
