@@ -1,5 +1,6 @@
 // codec_tc.cu -- SRFT quantize and dequantize with the transform done as a
-// dense contraction on the 5th-generation tensor cores (head dimension 128).
+// dense contraction on the 5th-generation tensor cores (head dimension 128,
+// and 96 inside the same 128-wide tiles with R zero outside its 96 x 96 block).
 //
 // Method: "When Quantization Is Free: An int4 KV Cache That Outruns fp16 on
 // Apple Silicon", Methodology 1 (SRFT(x) = pack(F diag(s) x) is a fixed real
@@ -285,7 +286,7 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
 //               SM's shared-memory bandwidth);
 //   warps 10-17 epilogue: tensor memory -> fp16 -> swizzled staging -> TMA
 //               store (warp w reads tensor-memory lanes 32(w%4)..+31, one
-//               column half).
+//               column half; at d = 96 the six-word halves of d96_word).
 // Converting is a dependent chain per row; eight warps on half rows keep
 // enough of them in flight to match the load rate.
 // B = diag(s) R (signs folded in), so X_hat = s (R^T P_hat).  P_hat is
@@ -357,31 +358,12 @@ __device__ __forceinline__ uint32_t half2_bcast(__half h) {
 }
 }  // namespace
 
-// codes * scale for columns 64 hf .. 64 hf + 63 of tile row m, from the
-// stage's exact swizzled code rows (64 bytes for 4-bit, 128 for 8-bit) and
-// scale rows (TD / group floats: 32 bytes for group 16, 16 for group 32)
 // The four 16-column unit scales of columns 64 hf .. +63 of tile row m, from
 // the stage in shared memory: fp32 planes as exact swizzled rows (32 bytes
 // for group 16, 16 for group 32), fp16 / e8m0 planes as their contiguous
 // bytes (rows of 4 to 16 bytes, unswizzled).
 __device__ __forceinline__ void half_row_scales(const uint8_t* __restrict__ in, int off_sc, int m, int hf, int group,
-                                                int sfmt, int d, float (&sc)[4]) {
-    if (d != TD) {  // smaller head dimension: unswizzled rows of d/group scales; units past d read as 0
-        const int ng = d / group, sb = sfmt == SRFTKV_SCALE_FP32 ? 4 : sfmt == SRFTKV_SCALE_FP16 ? 2 : 1;
-        const uint8_t* row = in + off_sc + m * ng * sb;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int col = 64 * hf + 16 * u, gi = col / group;
-            float v = 0.f;
-            if (col < d) {
-                if (sfmt == SRFTKV_SCALE_FP32) v = *reinterpret_cast<const float*>(row + 4 * gi);
-                else if (sfmt == SRFTKV_SCALE_FP16) v = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(row + 2 * gi)));
-                else v = __uint_as_float((uint32_t)row[gi] << 23);
-            }
-            sc[u] = v;
-        }
-        return;
-    }
+                                                int sfmt, float (&sc)[4]) {
     if (sfmt == SRFTKV_SCALE_FP32) {
         const int srb = 4 * (TD / group);
         if (group == 16) {  // groups 4hf .. 4hf+3: chunk hf of the 32-byte row
@@ -428,16 +410,14 @@ __device__ __forceinline__ void half_row_scales(const uint8_t* __restrict__ in, 
     }
 }
 
-// The 16-byte code chunks of half hf of tile row m (rows of DV*BITS/8 bytes;
-// chunks past the row, the zero padding of DV < 128, read as zero codes)
-template <int BITS, int DV, int NCH>
+// The 16-byte code chunks of half hf of tile row m (swizzled rows of 128*BITS/8 bytes)
+template <int BITS, int NCH>
 __device__ __forceinline__ void load_half_codes(const uint8_t* __restrict__ in, int m, int hf, uint32_t (&w)[4 * NCH]) {
-    constexpr int RB = DV * BITS / 8;
+    constexpr int RB = TD * BITS / 8;
 #pragma unroll
     for (int k = 0; k < NCH; ++k) {
         const int c = NCH * hf + k;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (DV == TD || 16 * c < RB) v = *reinterpret_cast<const uint4*>(in + m * RB + (swz16(RB, m, c) << 4));
+        const uint4 v = *reinterpret_cast<const uint4*>(in + m * RB + (swz16(RB, m, c) << 4));
         w[4 * k] = v.x;
         w[4 * k + 1] = v.y;
         w[4 * k + 2] = v.z;
@@ -445,12 +425,14 @@ __device__ __forceinline__ void load_half_codes(const uint8_t* __restrict__ in, 
     }
 }
 
-template <int BITS, int DV>
+// codes * scale for columns 64 hf .. 64 hf + 63 of tile row m, from the
+// stage's exact swizzled code rows (64 bytes for 4-bit, 128 for 8-bit)
+template <int BITS>
 __device__ __forceinline__ void dequant_half_smem(const uint8_t* __restrict__ in, int m, int hf, const float (&sc)[4],
                                                   float (&p)[64]) {
     constexpr int NCH = 64 * BITS / 128, PER = 32 / BITS;  // chunks per half row
     uint32_t w[4 * NCH];
-    load_half_codes<BITS, DV, NCH>(in, m, hf, w);
+    load_half_codes<BITS, NCH>(in, m, hf, w);
 #pragma unroll
     for (int i = 0; i < 64; ++i) {
         const float c = (BITS == 4) ? code_int4(w[i / PER], i % PER) : code_int8(w[i / PER], i % PER);
@@ -462,12 +444,12 @@ __device__ __forceinline__ void dequant_half_smem(const uint8_t* __restrict__ in
 // K order of dq_kperm (no lambda): codes -> exact fp16 pairs -> times the
 // group scale split into fp16 hi + lo, P_hat = fp16(q s_hi + fp16(q s_lo)), one
 // main rounding as when the fp32 product q s is rounded to fp16.
-template <int BITS, int DV>
+template <int BITS>
 __device__ __forceinline__ void dequant_half_pairs(const uint8_t* __restrict__ in, int m, int hf, const float (&sc)[4],
                                                    uint32_t (&hp)[32]) {
     constexpr int NCH = 64 * BITS / 128;
     uint32_t w[4 * NCH];
-    load_half_codes<BITS, DV, NCH>(in, m, hf, w);
+    load_half_codes<BITS, NCH>(in, m, hf, w);
     uint32_t sh[4], sl[4];
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
@@ -738,28 +720,27 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
                 continue;
             }
             float sc[4];
-            half_row_scales(in, C::OFF_SC, m, hf, P.group, S.sfmt, DV, sc);
+            half_row_scales(in, C::OFF_SC, m, hf, P.group, S.sfmt, sc);
             if (S.lambda == nullptr) {
                 if (side_k)
-                    dequant_half_pairs<BK, DV>(in, m, hf, sc, hp);
+                    dequant_half_pairs<BK>(in, m, hf, sc, hp);
                 else
-                    dequant_half_pairs<BV, DV>(in, m, hf, sc, hp);
+                    dequant_half_pairs<BV>(in, m, hf, sc, hp);
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar(IN_EMPTY + st));  // input stage consumed
             } else {
                 float p[64];
                 if (side_k)
-                    dequant_half_smem<BK, DV>(in, m, hf, sc, p);
+                    dequant_half_smem<BK>(in, m, hf, sc, p);
                 else
-                    dequant_half_smem<BV, DV>(in, m, hf, sc, p);
+                    dequant_half_smem<BV>(in, m, hf, sc, p);
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar(IN_EMPTY + st));  // input stage consumed
                 if (t_tok < P.n_tokens) {
                     const float4* lr = reinterpret_cast<const float4*>(
-                        S.lambda + (long long)id.o * S.lambda_outer_stride + (long long)id.h * DV + 64 * hf);
+                        S.lambda + (long long)id.o * S.lambda_outer_stride + (long long)id.h * TD + 64 * hf);
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
-                        if (DV != TD && 64 * hf + 4 * c >= DV) break;  // padding columns: p is already 0
                         const float4 l = __ldg(lr + c);
                         p[4 * c] = __fdividef(p[4 * c], l.x);
                         p[4 * c + 1] = __fdividef(p[4 * c + 1], l.y);
