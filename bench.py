@@ -390,7 +390,11 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         if i >= 3:
             t16.append(a.elapsed_time(b))
 
-    # end to end through the public API from pinned host memory
+    # end to end through the public API from pinned host memory: every step copies its inputs (K, V, q) host ->
+    # device, runs the step and reads the attention output back, all on one stream.  The host link carries
+    # about 211 GB/s with the GPU otherwise idle but drops to about 23 GB/s while a kernel saturates HBM with
+    # reads, so copies overlapped with the step (a second stream and a second set of input buffers) made a step
+    # take 85 ms instead of 46: they stay serialised.
     e2e = None
     if args.e2e_steps > 0:
         hk = xk.cpu().pin_memory()
