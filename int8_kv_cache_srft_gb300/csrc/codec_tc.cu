@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
 //               row-per-thread reads free of bank conflicts), into a ring of
 //               input stages;
 //   warps 2-9   converters: thread = half a row of the tile; decode codes *
-//               scale, divide by lambda, write P_hat as fp16 straight into
+//               scale, write P_hat as fp16 straight into
 //               tensor memory (the MMA takes A from there: no shared-memory
 //               round trip, which with the B reads would otherwise exceed the
 //               SM's shared-memory bandwidth);
@@ -289,6 +289,12 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
 //               column half; at d = 96 the six-word halves of d96_word).
 // Converting is a dependent chain per row; eight warps on half rows keep
 // enough of them in flight to match the load rate.
+// 1/lambda scales the contraction's K index (the packed coordinate), so it is
+// folded into B: B[k][q] = R_s[k][q] / lambda_n(q), rebuilt (by the MMA warp,
+// from an fp32 copy of R_s, once the MMAs that read B have completed)
+// whenever the tile's lambda row changes.  With lambda a CTA takes a
+// contiguous range of tiles, so a rebuild comes once per (side, outer, head)
+// run rather than per tile, and the converters keep the code-pair path.
 // B = diag(s) R (signs folded in), so X_hat = s (R^T P_hat).  P_hat is
 // rounded once to fp16 before the contraction and the result is rounded to
 // fp16 again on output; R_s in fp16 (11 bits) matches that precision, so
@@ -308,7 +314,9 @@ struct DqCfg {
     static constexpr int OFF_SC = TM * RBMAX;                       // 1024-aligned
     static constexpr int STAGE = (OFF_SC + TM * 32 + 1023) / 1024 * 1024;  // scale rows of at most 32 bytes
     static constexpr int STAGES = (BK == 4 && BV == 4) ? 4 : 3;
-    static constexpr int OFF_BAR = DQ_OFF_IN + STAGES * STAGE;
+    static constexpr int OFF_BASE = DQ_OFF_IN + STAGES * STAGE;  // R_s in fp32, [k][q] rows of 128 (64 KB)
+    static constexpr int OFF_IL = OFF_BASE + TD * TD * 4;        // 1/lambda of the current run, 128 floats
+    static constexpr int OFF_BAR = OFF_IL + TD * 4;
     static constexpr int SMEM = OFF_BAR + 256 + 1024;
 };
 // 16-byte chunk c of row r of a buffer of RB-byte rows written by TMA with the
@@ -425,21 +433,6 @@ __device__ __forceinline__ void load_half_codes(const uint8_t* __restrict__ in, 
     }
 }
 
-// codes * scale for columns 64 hf .. 64 hf + 63 of tile row m, from the
-// stage's exact swizzled code rows (64 bytes for 4-bit, 128 for 8-bit)
-template <int BITS>
-__device__ __forceinline__ void dequant_half_smem(const uint8_t* __restrict__ in, int m, int hf, const float (&sc)[4],
-                                                  float (&p)[64]) {
-    constexpr int NCH = 64 * BITS / 128, PER = 32 / BITS;  // chunks per half row
-    uint32_t w[4 * NCH];
-    load_half_codes<BITS, NCH>(in, m, hf, w);
-#pragma unroll
-    for (int i = 0; i < 64; ++i) {
-        const float c = (BITS == 4) ? code_int4(w[i / PER], i % PER) : code_int8(w[i / PER], i % PER);
-        p[i] = c * sc[i >> 4];
-    }
-}
-
 // P_hat for columns 64 hf .. +63 of tile row m directly as fp16 pairs in the
 // K order of dq_kperm (no lambda): codes -> exact fp16 pairs -> times the
 // group scale split into fp16 hi + lo, P_hat = fp16(q s_hi + fp16(q s_lo)), one
@@ -518,56 +511,38 @@ __device__ __forceinline__ void d96_half_scales(const uint8_t* __restrict__ in, 
 }
 
 // fp16 pairs (coordinates 8w+j, 8w+j+4; j = 0..3) of half hf of a d = 96 row,
-// codes * scale (then / lambda when lam is given), in the order of the A columns
+// codes * scale with the scale split into fp16 hi + lo, in the order of the A columns
 template <int BITS>
 __device__ __forceinline__ void d96_half_pairs(const uint8_t* __restrict__ in, int off_sc, int m, int hf, int group,
-                                               int sfmt, const float* __restrict__ lam, uint32_t (&hp)[24]) {
+                                               int sfmt, uint32_t (&hp)[24]) {
     uint32_t w[6 * BITS / 4];
     d96_half_words<BITS>(in, m, hf, w);
     float sc[3];
     d96_half_scales(in, off_sc, m, hf, group, sfmt, sc);
-    if (lam == nullptr) {  // exact code pairs times the scale split into fp16 hi + lo
-        uint32_t sh[3], sl[3];
+    uint32_t sh[3], sl[3];
 #pragma unroll
-        for (int u = 0; u < 3; ++u) {
-            const __half h = __float2half_rn(sc[u]);
-            sh[u] = half2_bcast(h);
-            sl[u] = half2_bcast(__float2half_rn(sc[u] - __half2float(h)));
-        }
-#pragma unroll
-        for (int k = 0; k < 6; ++k) {
-            const int u = k < 4 ? k >> 1 : 2;
-            uint32_t c[4];
-            if constexpr (BITS == 4) {
-                const uint32_t x = w[k], xs = x >> 8;
-                c[0] = codes_lo4(x);
-                c[1] = codes_hi4(x);
-                c[2] = codes_lo4(xs);
-                c[3] = codes_hi4(xs);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    c[j] = codes_b8(__byte_perm(w[2 * k], w[2 * k + 1], j | (j << 4) | ((4 + j) << 8) | ((4 + j) << 12)));
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) hp[4 * k + j] = h2fma(c[j], sh[u], h2mul(c[j], sl[u]));
-        }
-        return;
+    for (int u = 0; u < 3; ++u) {
+        const __half h = __float2half_rn(sc[u]);
+        sh[u] = half2_bcast(h);
+        sl[u] = half2_bcast(__float2half_rn(sc[u] - __half2float(h)));
     }
 #pragma unroll
     for (int k = 0; k < 6; ++k) {
-        const int u = k < 4 ? k >> 1 : 2, e0 = 8 * d96_word(hf, k);
-        const float4 l0 = __ldg(reinterpret_cast<const float4*>(lam + e0));
-        const float4 l1 = __ldg(reinterpret_cast<const float4*>(lam + e0 + 4));
-        const float li[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
-        float p[8];
+        const int u = k < 4 ? k >> 1 : 2;
+        uint32_t c[4];
+        if constexpr (BITS == 4) {
+            const uint32_t x = w[k], xs = x >> 8;
+            c[0] = codes_lo4(x);
+            c[1] = codes_hi4(x);
+            c[2] = codes_lo4(xs);
+            c[3] = codes_hi4(xs);
+        } else {
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-            const float c = (BITS == 4) ? code_int4(w[k], jj) : code_int8(w[2 * k + (jj >> 2)], jj & 3);
-            p[jj] = __fdividef(c * sc[u], li[jj]);
+            for (int j = 0; j < 4; ++j)
+                c[j] = codes_b8(__byte_perm(w[2 * k], w[2 * k + 1], j | (j << 4) | ((4 + j) << 8) | ((4 + j) << 12)));
         }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) hp[4 * k + j] = pack_half2(p[j], p[j + 4]);
+        for (int j = 0; j < 4; ++j) hp[4 * k + j] = h2fma(c[j], sh[u], h2mul(c[j], sl[u]));
     }
 }
 
@@ -585,20 +560,22 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
     const uint32_t sbase = ptx::smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-    // a_full[0..2], a_empty[3..5], acc_full[6,7], acc_empty[8,9], in_full[10..13], in_empty[14..17];
-    // tensor-memory slot at 18
+    // a_full[0..2], a_empty[3..5], acc_full[6,7], acc_empty[8,9], in_full[10..13], in_empty[14..17],
+    // b_free at 18; tensor-memory slot at 19
     auto bar = [&](int i) { return ptx::smem_u32(&bars[i]); };
-    constexpr int A_FULL = 0, A_EMPTY = 3, ACC_FULL = 6, ACC_EMPTY = 8, IN_FULL = 10, IN_EMPTY = 14;
+    constexpr int A_FULL = 0, A_EMPTY = 3, ACC_FULL = 6, ACC_EMPTY = 8, IN_FULL = 10, IN_EMPTY = 14, B_FREE = 18;
     static_assert(C::STAGES <= 4, "input stages");
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[18]);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[19]);
+    float* rbase = reinterpret_cast<float*>(smem + C::OFF_BASE);
 
-    {  // B[k][q] = s_k R[n][k] with n = dq_kperm(q) (zero outside d x d)
+    {  // B[k][q] = s_k R[n][k] with n = dq_kperm(q) (zero outside d x d), in fp16; and in fp32 for the rebuilds
         const bool srht = P.side[0].transform == SRFTKV_TRANSFORM_SRHT;
         for (int idx = threadIdx.x; idx < TD * TD; idx += blockDim.x) {
             // B row k (output coordinate), K position q holding packed coordinate n
             const int k = idx >> 7, q = idx & 127, n = dq_kperm(q);
             float v = r_entry(n, k, DV, srht);
             if (P.sign_mask[k >> 1] & ((k & 1) ? 0x80000000u : 0x8000u)) v = -v;
+            rbase[idx] = v;
             *reinterpret_cast<__half*>(smem + sw128_offset(k, q)) = __float2half_rn(v);
         }
         ptx::fence_proxy_async_smem();
@@ -616,6 +593,7 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
             ptx::mbar_init(bar(IN_FULL + st), 1);
             ptx::mbar_init(bar(IN_EMPTY + st), DQ_CONV);
         }
+        ptx::mbar_init(bar(B_FREE), 1);
         ptx::fence_barrier_init();
     }
     if (warp == 0) {
@@ -626,35 +604,84 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const int stride = gridDim.x;
+    // this CTA's tiles: a contiguous range when a side has lambda (runs of one lambda row), else round-robin
+    const bool contig = P.side[0].lambda != nullptr || P.side[1].lambda != nullptr;
+    const int per = (P.total_tiles + gridDim.x - 1) / gridDim.x;
+    const int first = contig ? blockIdx.x * per : blockIdx.x, step = contig ? 1 : gridDim.x;
+    const int count = contig ? max(0, min(per, P.total_tiles - first))
+                             : (P.total_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
     bool failed = false;
 
     if (warp == 0) {
-        if (lane == 0) {
-            for (int t = blockIdx.x, i = 0; t < P.total_tiles; t += stride, ++i) {
-                const int s = i & 1, b = i % DQ_NA;
-                if (!ptx::mbar_wait_bounded(bar(A_FULL + b), (i / DQ_NA) & 1) ||
-                    (i >= 2 && !ptx::mbar_wait_bounded(bar(ACC_EMPTY + s), ((i >> 1) - 1) & 1))) {
+        const float* cur = nullptr;  // the lambda row B is divided by (nullptr: none)
+        uint32_t bfree_parity = 0;
+        for (int i = 0; i < count; ++i) {
+            const int t = first + i * step;
+            const TileId id = decode_tile128(P, t);
+            const CodecSideK& S = P.side[id.side];
+            const float* key = S.lambda == nullptr
+                                   ? nullptr
+                                   : S.lambda + (long long)id.o * S.lambda_outer_stride + (long long)id.h * DV;
+            if (key != cur) {
+                // the MMAs issued so far read B: wait for them, then rebuild B = R_s / lambda from the fp32 copy
+                bool ok = true;
+                if (lane == 0) {
+                    tc::commit(bar(B_FREE));
+                    ok = ptx::mbar_wait_bounded(bar(B_FREE), bfree_parity);
+                }
+                bfree_parity ^= 1u;
+                if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
                     failed = true;
                     break;
                 }
                 tc::fence_after_sync();
-                const uint32_t d_tmem = tmem + s * TD;
-                const uint32_t a_tmem = tmem + DQ_A_COL + b * 64;
-                // d < 128: K and N stop at d (accumulator columns past d are never stored)
-                constexpr uint32_t IDESC = tc::idesc_f16_f32(TM, DV);
+                float* il = reinterpret_cast<float*>(smem + C::OFF_IL);
+                for (int c = lane; c < TD; c += 32) il[c] = (key != nullptr && c < DV) ? __frcp_rn(__ldg(key + c)) : 1.f;
+                __syncwarp();
+                for (int j = lane; j < TD * TD / 8; j += 32) {  // row k, K positions 8c .. 8c+7
+                    const int k = j >> 4, q0 = (j & 15) * 8;
+                    const float4 lo = *reinterpret_cast<const float4*>(rbase + k * TD + q0);
+                    const float4 hi = *reinterpret_cast<const float4*>(rbase + k * TD + q0 + 4);
+                    const float v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+                    uint32_t h[4];
 #pragma unroll
-                for (int ks = 0; ks < DV / 16; ++ks) {
-                    const uint32_t koff = (ks >> 2) * T_KB_BYTES + (ks & 3) * 32;
-                    tc::mma_f16_ta(d_tmem, a_tmem + 8 * ks, tc::sw128_desc(sbase + koff), IDESC, ks > 0);
+                    for (int e = 0; e < 4; ++e)
+                        h[e] = pack_half2(v[2 * e] * il[dq_kperm(q0 + 2 * e)], v[2 * e + 1] * il[dq_kperm(q0 + 2 * e + 1)]);
+                    *reinterpret_cast<uint4*>(smem + sw128_offset(k, q0)) = make_uint4(h[0], h[1], h[2], h[3]);
                 }
-                tc::commit(bar(A_EMPTY + b));  // A buffer b may be rewritten
-                tc::commit(bar(ACC_FULL + s));  // accumulator s is ready
+                ptx::fence_proxy_async_smem();  // generic writes -> tensor-core reads
+                __syncwarp();
+                cur = key;
+            }
+            bool ok = true;
+            if (lane == 0) {
+                const int s = i & 1, b = i % DQ_NA;
+                ok = ptx::mbar_wait_bounded(bar(A_FULL + b), (i / DQ_NA) & 1) &&
+                     (i < 2 || ptx::mbar_wait_bounded(bar(ACC_EMPTY + s), ((i >> 1) - 1) & 1));
+                if (ok) {
+                    tc::fence_after_sync();
+                    const uint32_t d_tmem = tmem + s * TD;
+                    const uint32_t a_tmem = tmem + DQ_A_COL + b * 64;
+                    // d < 128: K and N stop at d (accumulator columns past d are never stored)
+                    constexpr uint32_t IDESC = tc::idesc_f16_f32(TM, DV);
+#pragma unroll
+                    for (int ks = 0; ks < DV / 16; ++ks) {
+                        const uint32_t koff = (ks >> 2) * T_KB_BYTES + (ks & 3) * 32;
+                        tc::mma_f16_ta(d_tmem, a_tmem + 8 * ks, tc::sw128_desc(sbase + koff), IDESC, ks > 0);
+                    }
+                    tc::commit(bar(A_EMPTY + b));  // A buffer b may be rewritten
+                    tc::commit(bar(ACC_FULL + s));  // accumulator s is ready
+                }
+            }
+            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
+                failed = true;
+                break;
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            for (int t = blockIdx.x, i = 0; t < P.total_tiles; t += stride, ++i) {
+            for (int i = 0; i < count; ++i) {
+                const int t = first + i * step;
                 const int st = i % C::STAGES, use = i / C::STAGES;
                 if (use > 0 && !ptx::mbar_wait_bounded(bar(IN_EMPTY + st), (use - 1) & 1)) {
                     failed = true;
@@ -679,11 +706,11 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
         // quarter a warp may write), column half (w-2)/4
         const int quarter = warp & 3, m = 32 * quarter + lane, hf = (warp - 2) >> 2;
 
-        for (int t = blockIdx.x, i = 0; t < P.total_tiles; t += stride, ++i) {
+        for (int i = 0; i < count; ++i) {
+            const int t = first + i * step;
             const int b = i % DQ_NA, st = i % C::STAGES;
             const TileId id = decode_tile128(P, t);
             const CodecSideK& S = P.side[id.side];
-            const int t_tok = id.t0 + m;
             const bool ok_in = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(bar(IN_FULL + st), (i / C::STAGES) & 1));
             if (!ok_in) {
                 failed = true;
@@ -692,15 +719,13 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
             const uint8_t* in = smem + DQ_OFF_IN + st * C::STAGE;
             uint32_t hp[32];  // fp16 pairs in the K order of dq_kperm: column 32 hf + c
             const bool side_k = BK == BV || id.side == 0;
+            // lambda is folded into B: the converters take codes * scale only
             if constexpr (DV != TD) {  // d = 96: balanced halves of six words (d96_word)
-                const float* lam = (S.lambda != nullptr && t_tok < P.n_tokens)
-                                       ? S.lambda + (long long)id.o * S.lambda_outer_stride + (long long)id.h * DV
-                                       : nullptr;
                 uint32_t (&h24)[24] = *reinterpret_cast<uint32_t(*)[24]>(hp);
                 if (side_k)
-                    d96_half_pairs<BK>(in, C::OFF_SC, m, hf, P.group, S.sfmt, lam, h24);
+                    d96_half_pairs<BK>(in, C::OFF_SC, m, hf, P.group, S.sfmt, h24);
                 else
-                    d96_half_pairs<BV>(in, C::OFF_SC, m, hf, P.group, S.sfmt, lam, h24);
+                    d96_half_pairs<BV>(in, C::OFF_SC, m, hf, P.group, S.sfmt, h24);
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar(IN_EMPTY + st));  // input stage consumed
                 const bool ok = __all_sync(0xffffffffu,
@@ -721,39 +746,12 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
             }
             float sc[4];
             half_row_scales(in, C::OFF_SC, m, hf, P.group, S.sfmt, sc);
-            if (S.lambda == nullptr) {
-                if (side_k)
-                    dequant_half_pairs<BK>(in, m, hf, sc, hp);
-                else
-                    dequant_half_pairs<BV>(in, m, hf, sc, hp);
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar(IN_EMPTY + st));  // input stage consumed
-            } else {
-                float p[64];
-                if (side_k)
-                    dequant_half_smem<BK>(in, m, hf, sc, p);
-                else
-                    dequant_half_smem<BV>(in, m, hf, sc, p);
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar(IN_EMPTY + st));  // input stage consumed
-                if (t_tok < P.n_tokens) {
-                    const float4* lr = reinterpret_cast<const float4*>(
-                        S.lambda + (long long)id.o * S.lambda_outer_stride + (long long)id.h * TD + 64 * hf);
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const float4 l = __ldg(lr + c);
-                        p[4 * c] = __fdividef(p[4 * c], l.x);
-                        p[4 * c + 1] = __fdividef(p[4 * c + 1], l.y);
-                        p[4 * c + 2] = __fdividef(p[4 * c + 2], l.z);
-                        p[4 * c + 3] = __fdividef(p[4 * c + 3], l.w);
-                    }
-                }
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    const int e = dq_kperm(2 * c);  // coordinates e, e + 4 of the half
-                    hp[c] = pack_half2(p[e], p[e + 4]);
-                }
-            }
+            if (side_k)
+                dequant_half_pairs<BK>(in, m, hf, sc, hp);
+            else
+                dequant_half_pairs<BV>(in, m, hf, sc, hp);
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(IN_EMPTY + st));  // input stage consumed
             const bool ok = __all_sync(0xffffffffu,
                                        i < DQ_NA || ptx::mbar_wait_bounded(bar(A_EMPTY + b), (i / DQ_NA - 1) & 1));
             if (!ok) {
@@ -771,7 +769,8 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
         const int quarter = warp & 3;   // tensor-memory lanes 32*quarter..+31 = tile rows
         const int m = 32 * quarter + lane, hf = (warp - 2 - DQ_CONV) >> 2;  // and column half hf
         const bool leader = (warp == 2 + DQ_CONV && lane == 0);
-        for (int t = blockIdx.x, i = 0; t < P.total_tiles; t += stride, ++i) {
+        for (int i = 0; i < count; ++i) {
+            const int t = first + i * step;
             const int s = i & 1;
             const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(bar(ACC_FULL + s), (i >> 1) & 1));
             if (!ok) {
