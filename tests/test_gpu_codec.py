@@ -173,6 +173,29 @@ def test_tensor_core_quantize_path(monkeypatch, bk, bv, group, lam):
         assert np.abs(_np(out) - mine).max() <= np.abs(mine).max() * 2.0**-10 + 1e-5
 
 
+def test_lambda_fold_mixed_sides_and_broadcast(monkeypatch):
+    """The tensor-core dequantize folds 1/lambda into its B operand and rebuilds it whenever the lambda row of
+    its tiles changes.  K with one lambda table broadcast over the outer index (outer stride 0) and V without
+    lambda go through one launch; 3 outer x 1100 tokens x 4 heads (9 tiles of 128 a head, 216 tiles) so the
+    contiguous tile range of a CTA straddles heads and the K/V boundary."""
+    monkeypatch.setenv("SRFTKV_QUANT_PATH", "tc")
+    n, T, H, d, g, seed = 3, 1100, 4, 128, 16, 29
+    w = I.Workload("fold", n_outer=n, tokens=T, kv_heads=H, d=d, lam=True, data_seed=29,
+                   outlier_kind="scale", outlier_channels=4, outlier_factor=50.0)
+    xk, xv = I.kv_side(w, "k"), I.kv_side(w, "v")
+    lk = I.lam_table(w, "k", n_outer=1)  # [1][H][d]: one table for every outer index
+    sk, sv = _quantize_gpu(xk, xv, lk, None, 4, 4, g, seed)
+    enc_k, lam_b, _ = _check_side(sk, xk, lk, 4, g, seed)
+    enc_v, _, _ = _check_side(sv, xv, None, 4, g, seed)
+    outk, outv = torch.empty_like(sk.x), torch.empty_like(sv.x)
+    K.srft_kv_dequantize(K.Side(sk.codes, sk.scales, 4, x=outk, lam=sk.lam), K.Side(sv.codes, sv.scales, 4, x=outv),
+                         n, T, H, d, g, T, 0, seed)
+    torch.cuda.synchronize()
+    for side, out, lam_side in ((sk, outk, lam_b), (sv, outv, None)):
+        mine = O.srft_kv_dequantize(_np(tm(side.codes)), _np(tm(side.scales)).astype(np.float64), lam_side, 4, g, seed)
+        assert np.abs(_np(out) - mine).max() <= np.abs(mine).max() * 2.0**-10 + 1e-5
+
+
 def test_zero_rows_and_empty_calls():
     x = torch.zeros((1, 40, 2, 128), dtype=torch.float16)
     sk, sv = _quantize_gpu(x, x, None, None, 4, 8, 16, 3)
