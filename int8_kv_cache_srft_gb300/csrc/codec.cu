@@ -129,15 +129,18 @@ static int dispatch_codec(const CodecCall& c, bool quantize) {
     }
 }
 
-// Codec path: the tensor-core contraction (codec_tc.cu) for d = 128 (and, to
-// quantize, groups of at most 64) when the call is large enough to amortise
-// building R_s in every CTA; the register FFT otherwise.  SRFTKV_QUANT_PATH=fft
-// or =tc in the environment forces one path for both directions (tc only
-// where it applies).
+// Codec path: the tensor-core contraction (codec_tc.cu) for d = 128 when the
+// call is large enough to amortise building R_s in every CTA; to quantize a
+// small d = 128 call (a token append), one warp per vector (codec_small.cu),
+// where the latency of a vector's dependent chain is what counts; the
+// register FFT otherwise.  SRFTKV_QUANT_PATH=fft, =tc or =warp in the
+// environment forces one path (tc and warp only where they apply).
 static int quant_path_override() {
     const char* e = getenv("SRFTKV_QUANT_PATH");
-    return (e && !strcmp(e, "fft")) ? 1 : (e && !strcmp(e, "tc")) ? 2 : 0;
+    if (!e) return 0;
+    return !strcmp(e, "fft") ? 1 : !strcmp(e, "tc") ? 2 : !strcmp(e, "warp") ? 3 : 0;
 }
+constexpr long long kWarpPathMaxRows = 8192;
 
 // A call whose two sides use different transforms or scale formats runs as
 // two one-sided calls (the tensor-core kernels hold one transform matrix per
@@ -176,6 +179,10 @@ int codec_quantize(const CodecCall& c) {
     const long long rows = (long long)c.n_sides * c.n_outer * c.n_tokens * c.H;
     if (ov == 2 || (ov == 0 && rows >= 64ll * 1024)) {
         const int rc = codec_quantize_tc(c);
+        if (rc != 1) return rc;
+    }
+    if (ov == 3 || (ov == 0 && rows <= kWarpPathMaxRows)) {
+        const int rc = codec_quantize_warp(c);
         if (rc != 1) return rc;
     }
     return dispatch_codec(c, true);

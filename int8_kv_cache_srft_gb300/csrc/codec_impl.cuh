@@ -94,6 +94,38 @@ __device__ __forceinline__ long long packed_row(const CodecParams& P, const Tile
 // runtime group size by a butterfly over units, so one code path serves
 // every group size; group == 16 (the default) keeps 16-byte scale stores.
 // ---------------------------------------------------------------------------
+// The stored scale of a group with absmax A, in the side's format, the value
+// its codes are rounded against (sc), its stored bits (raw: fp16 bits or the
+// e8m0 byte) and the multiplier inv that turns z into z / sc.
+template <int BITS, int SF>
+__device__ __forceinline__ void group_scale(float A, float& sc, uint32_t& raw, float& inv) {
+    constexpr float Q = (BITS == 4) ? 7.f : 127.f;
+    if constexpr (SF == SRFTKV_SCALE_FP32) {
+        // scale = A/Q to within an ulp; z * (Q * rcp(A)) rounds z/scale to within a few ulp, far inside the
+        // 1e-4 band around rounding boundaries
+        sc = A * (1.0f / Q);
+        raw = 0;
+        inv = A > 0.f ? Q * __frcp_rn(A) : 0.f;
+    } else if constexpr (SF == SRFTKV_SCALE_FP16) {
+        // A * (1/Q) (within an ulp of A/Q) rounded to fp16, saturating at the largest finite fp16; it can
+        // differ from rounding A/Q itself only within ~2^-23 of an fp16 midpoint
+        const __half h = __float2half_rn(fminf(A * (1.0f / Q), 65504.f));
+        sc = __half2float(h);
+        raw = __half_as_ushort(h);
+        inv = sc > 0.f ? __frcp_rn(sc) : 0.f;
+    } else {
+        // e8m0: biased exponent of the smallest power of two not below A/Q (normal or subnormal v); A * (1/Q)
+        // is within an ulp of A/Q, which matters only within ~2^-23 of a power of two
+        const float v = A * (1.0f / Q);
+        const uint32_t b = __float_as_uint(v);
+        uint32_t e = (b >> 23) + ((b & 0x7FFFFFu) != 0u ? 1u : 0u);
+        e = v > 0.f ? min(max(e, 1u), 254u) : 0u;
+        raw = e;
+        sc = __uint_as_float(e << 23);
+        inv = e ? __frcp_rn(sc) : 0.f;
+    }
+}
+
 template <int D, int BITS, int SF>
 __device__ __forceinline__ void quant_store_row(float (&z)[D], int group, uint8_t* __restrict__ crow,
                                                 uint8_t* __restrict__ srow) {
@@ -122,30 +154,7 @@ __device__ __forceinline__ void quant_store_row(float (&z)[D], int group, uint8_
     for (int u = 0; u < U; ++u) {
         const float A = m[u];
         float inv;
-        if constexpr (sfmt == SRFTKV_SCALE_FP32) {
-            // scale = A/Q to within an ulp; z * (Q * rcp(A)) rounds z/scale to within a few ulp, far inside the
-            // 1e-4 band around rounding boundaries
-            sc[u] = A * (1.0f / Q);
-            raw[u] = 0;
-            inv = A > 0.f ? Q * __frcp_rn(A) : 0.f;
-        } else if constexpr (sfmt == SRFTKV_SCALE_FP16) {
-            // A * (1/Q) (within an ulp of A/Q) rounded to fp16, saturating at the largest finite fp16; it can
-            // differ from rounding A/Q itself only within ~2^-23 of an fp16 midpoint
-            const __half h = __float2half_rn(fminf(A * (1.0f / Q), 65504.f));
-            sc[u] = __half2float(h);
-            raw[u] = __half_as_ushort(h);
-            inv = sc[u] > 0.f ? __frcp_rn(sc[u]) : 0.f;
-        } else {
-            // e8m0: biased exponent of the smallest power of two not below A/Q (normal or subnormal v); A * (1/Q)
-            // is within an ulp of A/Q, which matters only within ~2^-23 of a power of two
-            const float v = A * (1.0f / Q);
-            const uint32_t b = __float_as_uint(v);
-            uint32_t e = (b >> 23) + ((b & 0x7FFFFFu) != 0u ? 1u : 0u);
-            e = v > 0.f ? min(max(e, 1u), 254u) : 0u;
-            raw[u] = e;
-            sc[u] = __uint_as_float(e << 23);
-            inv = e ? __frcp_rn(sc[u]) : 0.f;
-        }
+        group_scale<BITS, SF>(A, sc[u], raw[u], inv);
 #pragma unroll
         for (int i = 0; i < 16; ++i) z[16 * u + i] = fmaf_(z[16 * u + i], inv, MAG);
         if constexpr (sfmt == SRFTKV_SCALE_FP16) {

@@ -67,6 +67,8 @@ bool encode_tiled_swz(CUtensorMap* map, CUtensorMapDataType dt, int rank, void* 
 // Tensor-core quantize path (d = 128, group <= 64); returns 1 when the call
 // is not one it handles, else SRFTKV_OK or an error code.
 int codec_quantize_tc(const CodecCall& c);
+// One warp per vector (d = 128, groups of at most 32): returns 1 when the call does not fit it.
+int codec_quantize_warp(const CodecCall& c);
 int codec_dequantize_tc(const CodecCall& c);
 
 int attention_entry(const void* q, float* out, const srftkv_side* k, const srftkv_side* v, int B, int Hq, int Hkv,

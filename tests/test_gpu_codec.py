@@ -301,3 +301,74 @@ def test_k8v4_append_onto_prebuilt_cache():
         crow = torch.as_tensor((o_idx * H + rem % H) * t_cap + rem // H, device="cuda")
         assert_codes(_np(side.codes.reshape(-1, d * bits // 8)[crow]), enc["r"], bits)
         assert_scales(_np(side.scales.reshape(-1, d // 16)[crow]), enc["scales"])
+
+
+# ---------------------------------------------------------------------------
+# the warp-per-vector quantize (d = 128 small calls, e.g. token appends)
+# ---------------------------------------------------------------------------
+WARP_CASES = [(bk, bv, g, lam) for bk, bv in ((4, 4), (8, 4), (4, 8), (8, 8)) for g in (16, 32) for lam in (False, True)]
+
+
+@pytest.mark.parametrize("bk,bv,group,lam", WARP_CASES)
+def test_warp_quantize_path(monkeypatch, bk, bv, group, lam):
+    """One warp per vector (forced): 2 outer x 37 tokens x 3 heads written at t_offset 5 of t_cap 50, K and V of
+    different widths in one launch, rows outside the window untouched."""
+    monkeypatch.setenv("SRFTKV_QUANT_PATH", "warp")
+    w = I.Workload("warp", n_outer=2, tokens=37, kv_heads=3, d=128, lam=lam, data_seed=bk * 10 + bv + group,
+                   outlier_kind="scale", outlier_channels=4, outlier_factor=50.0)
+    xk, xv = I.kv_side(w, "k"), I.kv_side(w, "v")
+    lk, lv = I.lam_table(w, "k"), I.lam_table(w, "v")
+    sk, sv = _quantize_gpu(xk, xv, lk, lv, bk, bv, group, 17, t_cap=50, t_offset=5)
+    for side, x, lam_t, b in ((sk, xk, lk, bk), (sv, xv, lv, bv)):
+        _check_side(side, x, lam_t, b, group, 17, t_offset=5)
+        codes = _np(tm(side.codes))
+        assert (codes[:, :5] == 0xAB).all() and (codes[:, 42:] == 0xAB).all(), "rows outside the window were written"
+
+
+@pytest.mark.parametrize("transform,fmt", (("srht", "fp32"), ("srht", "e8m0"), ("srft", "fp16"), ("srft", "e8m0")))
+@pytest.mark.parametrize("bits", (4, 8))
+def test_warp_quantize_transforms_and_formats(monkeypatch, transform, fmt, bits):
+    """The warp path with the Hadamard transform and the fp16 / e8m0 scale planes (stored scales bit-exact away
+    from a rounding boundary of the format, codes against the stored scale)."""
+    from tests.test_gpu_scale_formats import near_boundary, raw_np
+
+    monkeypatch.setenv("SRFTKV_QUANT_PATH", "warp")
+    n, T, H, g, seed = 2, 64, 4, 16, 23
+    w = I.Workload("warpf", n_outer=n, tokens=T, kv_heads=H, d=128, lam=True, data_seed=bits + len(fmt),
+                   outlier_kind="scale", outlier_channels=2, outlier_factor=30.0)
+    x, lam = I.kv_side(w, "k"), I.lam_table(w, "k")
+    s = K.alloc_side(n, T, H, 128, bits, g, transform=transform, scale_format=fmt)
+    s.x, s.lam = x.cuda(), lam.cuda()
+    K.srft_kv_quantize(s, None, n, T, H, 128, g, T, 0, seed)
+    torch.cuda.synchronize()
+    enc = O.srft_kv_quantize(_np(x).astype(np.float64), _np(lam)[:, None, :, :], bits, g, seed, transform=transform,
+                             scale_format=fmt)
+    raw = raw_np(s.scales, fmt) if fmt != "fp32" else _np(tm(s.scales))
+    if fmt == "fp32":
+        assert_scales(raw, enc["scales"])
+        assert_codes(_np(tm(s.codes)), enc["r"], bits)
+    else:
+        want = np.asarray(enc["scales_raw"])
+        diff = raw != want
+        assert not (diff & ~near_boundary(enc["a_over_q"], fmt)).any()
+        sc = np.repeat(O.decode_scales(raw, fmt), g, axis=-1)
+        assert_codes(_np(tm(s.codes)), np.where(sc > 0, enc["z"] / np.where(sc > 0, sc, 1.0), 0.0), bits)
+
+
+def test_warp_path_matches_tensor_core_path(monkeypatch):
+    """The same 1000 vectors through the warp kernel and the tensor-core kernel: scales agree to 1e-5 and codes
+    agree except at rounding ties (both are checked against the oracle elsewhere)."""
+    n, T, H, g = 1, 250, 4, 16
+    w = I.Workload("cmp", n_outer=n, tokens=T, kv_heads=H, d=128, data_seed=77)
+    x = I.kv_side(w, "k")
+    outs = {}
+    for path in ("warp", "tc"):
+        monkeypatch.setenv("SRFTKV_QUANT_PATH", path)
+        s = K.alloc_side(n, T, H, 128, 4, g)
+        s.x = x.cuda()
+        K.srft_kv_quantize(s, None, n, T, H, 128, g, T, 0, 5)
+        torch.cuda.synchronize()
+        outs[path] = (_np(s.codes), _np(s.scales))
+    assert np.allclose(outs["warp"][1], outs["tc"][1], rtol=1e-5, atol=0)
+    qa, qb = O.unpack_codes(outs["warp"][0], 4), O.unpack_codes(outs["tc"][0], 4)
+    assert (np.abs(qa - qb) <= 1).all() and (qa != qb).mean() < 1e-3
