@@ -91,8 +91,13 @@ def _ptr(t: torch.Tensor | None) -> int | None:
     return None if t is None else t.data_ptr()
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream) -> int | None:
-    if stream is None:
+    if stream is None:  # torch's current stream on the current device
+        if _raw_stream is not None:
+            return _raw_stream(torch.cuda.current_device())
         return torch.cuda.current_stream().cuda_stream
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
@@ -110,6 +115,20 @@ class Side:
     lam_outer_stride: int | None = None
     transform: str = "srft"        # "srft" or "srht"
     scale_format: str = "fp32"     # "fp32", "fp16" or "e8m0"
+
+    # The marshalled struct is built once and reused until a field is assigned again (a tensor changed in
+    # place keeps its address; one resized or replaced must be assigned anew).
+    def __setattr__(self, name, value):
+        object.__setattr__(self, name, value)
+        if name != "_c":
+            object.__setattr__(self, "_c", None)
+
+    def c_pointer(self):
+        c = getattr(self, "_c", None)
+        if c is None:
+            c = ctypes.pointer(self.to_c())
+            object.__setattr__(self, "_c", c)
+        return c
 
     def to_c(self) -> _Side:
         stride = self.lam_outer_stride
@@ -130,7 +149,7 @@ def alloc_side(n_outer: int, t_cap: int, H: int, d: int, bits: int, group: int, 
 
 
 def _sidep(s: Side | None):
-    return None if s is None else ctypes.pointer(s.to_c())
+    return None if s is None else s.c_pointer()
 
 
 def srft_kv_quantize(k: Side | None, v: Side | None, n_outer: int, n_tokens: int, H: int, d: int, group: int,

@@ -48,12 +48,25 @@ static uint64_t splitmix64_output(uint64_t state) {
 }
 
 void sign_masks(int d, uint64_t seed, uint32_t* words) {
+    // the last (d, seed) of this host thread is kept: a decode loop asks for the same one every call
+    thread_local int last_d = -1;
+    thread_local uint64_t last_seed = 0;
+    thread_local uint32_t last_words[128];
+    if (d == last_d && seed == last_seed && d <= 256) {
+        for (int i = 0; i < d / 2; ++i) words[i] = (words[i] & 0x7FFF7FFFu) | last_words[i];
+        return;
+    }
     uint64_t state = seed;
     for (int i = 0; i < d; ++i) {
         state += 0x9E3779B97F4A7C15ull;
         const bool neg = (splitmix64_output(state) >> 63) != 0;
         if (neg) words[i / 2] |= (i & 1) ? 0x80000000u : 0x00008000u;
         else words[i / 2] &= (i & 1) ? ~0x80000000u : ~0x00008000u;
+    }
+    if (d <= 256) {
+        for (int i = 0; i < d / 2; ++i) last_words[i] = words[i] & 0x80008000u;
+        last_d = d;
+        last_seed = seed;
     }
 }
 
