@@ -170,3 +170,24 @@ def test_d96_rules(lib):
     assert lib.srht_transform(16, 16, 4, 96, 1, 0, None) == K.SRFTKV_ERR_INVALID
     assert lib.srft_transform(16, 16, 0, 96, 1, 0, None) == K.SRFTKV_OK
     assert _q(lib, _side(), None, d=96, n_tokens=0) == K.SRFTKV_OK
+
+
+def test_side_marshalling_is_cached_until_a_field_changes():
+    """The binding builds a side's C struct once; assigning any field rebuilds it with the new pointers."""
+    import torch
+
+    codes, scales = torch.zeros(64, dtype=torch.uint8), torch.zeros(8)
+    s = K.Side(codes, scales, 4)
+    p = s.c_pointer()
+    assert s.c_pointer() is p
+    assert p.contents.codes == codes.data_ptr() and p.contents.x is None
+    x = torch.zeros(128, dtype=torch.float16)
+    s.x = x
+    q = s.c_pointer()
+    assert q is not p and q.contents.x == x.data_ptr()
+    lam = torch.ones((1, 2, 64))
+    s.lam = lam
+    r = s.c_pointer()
+    assert r.contents.lambda_ == lam.data_ptr() and r.contents.lambda_outer_stride == 0
+    s.scale_format = "e8m0"
+    assert s.c_pointer().contents.scale_format == 2
