@@ -130,17 +130,20 @@ static int dispatch_codec(const CodecCall& c, bool quantize) {
 }
 
 // Codec path: the tensor-core contraction (codec_tc.cu) for d = 128 when the
-// call is large enough to amortise building R_s in every CTA; to quantize a
-// small d = 128 call (a token append), one warp per vector (codec_small.cu),
-// where the latency of a vector's dependent chain is what counts; the
-// register FFT otherwise.  SRFTKV_QUANT_PATH=fft, =tc or =warp in the
-// environment forces one path (tc and warp only where they apply).
+// call is large enough to amortise building R_s in every CTA (measured on
+// GB300: from about 192 K vectors a call it beats the register FFT in both
+// directions, and is 1.5-1.8x faster at millions); to quantize a small d = 128
+// call (a token append), one warp per vector (codec_small.cu), faster than
+// one thread per vector up to about 4 K vectors; the register FFT otherwise.
+// SRFTKV_QUANT_PATH=fft, =tc or =warp in the environment forces one path (tc
+// and warp only where they apply).
 static int quant_path_override() {
     const char* e = getenv("SRFTKV_QUANT_PATH");
     if (!e) return 0;
     return !strcmp(e, "fft") ? 1 : !strcmp(e, "tc") ? 2 : !strcmp(e, "warp") ? 3 : 0;
 }
-constexpr long long kWarpPathMaxRows = 8192;
+constexpr long long kWarpPathMaxRows = 4096;
+constexpr long long kTensorCorePathMinRows = 3ll << 16;
 
 // A call whose two sides use different transforms or scale formats runs as
 // two one-sided calls (the tensor-core kernels hold one transform matrix per
@@ -177,7 +180,7 @@ int codec_quantize(const CodecCall& c) {
     if (c.d == 96) return tc_only(c, codec_quantize_tc, "quantize");
     const int ov = quant_path_override();
     const long long rows = (long long)c.n_sides * c.n_outer * c.n_tokens * c.H;
-    if (ov == 2 || (ov == 0 && rows >= 64ll * 1024)) {
+    if (ov == 2 || (ov == 0 && rows >= kTensorCorePathMinRows)) {
         const int rc = codec_quantize_tc(c);
         if (rc != 1) return rc;
     }
@@ -193,7 +196,7 @@ int codec_dequantize(const CodecCall& c) {
     if (c.d == 96) return tc_only(c, codec_dequantize_tc, "dequantize");
     const int ov = quant_path_override();
     const long long rows = (long long)c.n_sides * c.n_outer * c.n_tokens * c.H;
-    if (ov == 2 || (ov == 0 && rows >= 64ll * 1024)) {
+    if (ov == 2 || (ov == 0 && rows >= kTensorCorePathMinRows)) {
         const int rc = codec_dequantize_tc(c);
         if (rc != 1) return rc;
     }

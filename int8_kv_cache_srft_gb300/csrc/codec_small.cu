@@ -30,10 +30,8 @@ namespace {
 constexpr int WQ_D = 128;
 constexpr int WQ_WARPS = 4;  // vectors per block
 
-// e^{-2 pi i m / 256} in global memory: per-lane twiddle indices differ, which
-// the constant bank would serialise; through L1 a warp's loads are a few lines
-__device__ const TwiddleTable g_tw256 = make_twiddles();
-__device__ __forceinline__ float2 twid(int m) { return make_float2(__ldg(&g_tw256.re[m]), __ldg(&g_tw256.im[m])); }
+// e^{-2 pi i m / 256}; per-lane indices, so from the L1-served copy of the table
+__device__ __forceinline__ float2 twid(int m) { return make_float2(tw_re_lane(m), tw_im_lane(m)); }
 
 __device__ __forceinline__ float shfl_x(float v, int m) { return __shfl_xor_sync(0xffffffffu, v, m); }
 __device__ __forceinline__ float shfl_i(float v, int src) { return __shfl_sync(0xffffffffu, v, src); }

@@ -69,7 +69,7 @@ __device__ float r_entry(int n, int k, int dv, bool srht) {
         if (n == 0) return inv_sqrt_d;
         if (n == 1) return (k & 1) ? -inv_sqrt_d : inv_sqrt_d;
         const int m = (((n >> 1) * k) & (TD - 1)) * (256 / TD);  // angle 2 pi (jk mod d)/d on the 256-point table
-        return (n & 1) ? c2 * tw_im(m) : c2 * tw_re(m);             // tw_im holds -sin
+        return (n & 1) ? c2 * tw_im_lane(m) : c2 * tw_re_lane(m);   // the imaginary part holds -sin
     }
     const double isd = 1.0 / sqrt((double)dv);
     if (n == 0) return (float)isd;

@@ -124,6 +124,11 @@ constexpr SplitTable make_split_twiddles() {
 #if defined(__CUDACC__)
 static __constant__ TwiddleTable c_tw = make_twiddles();
 static __constant__ SplitTable c_split = make_split_twiddles();
+// The same table in global memory, for indices that differ between the lanes
+// of a warp: the constant bank serialises those, L1 serves them in a few lines.
+static __device__ const TwiddleTable g_tw = make_twiddles();
+__device__ __forceinline__ float tw_re_lane(int m) { return __ldg(&g_tw.re[m]); }
+__device__ __forceinline__ float tw_im_lane(int m) { return __ldg(&g_tw.im[m]); }
 #endif
 static constexpr TwiddleTable h_tw = make_twiddles();
 static constexpr SplitTable h_split = make_split_twiddles();
