@@ -25,7 +25,6 @@ extern template int launch_codec_d<16>(const CodecCall&, bool);
 extern template int launch_codec_d<32>(const CodecCall&, bool);
 extern template int launch_codec_d<64>(const CodecCall&, bool);
 extern template int launch_codec_d<128>(const CodecCall&, bool);
-extern template int launch_codec_d<256>(const CodecCall&, bool);
 
 // fp16 pair (x_{2n}, x_{2n+1}) with the SRFT signs applied -> complex z_n
 __device__ __forceinline__ void signed_pair_t(uint32_t w, uint32_t mask, float& re, float& im) {
@@ -124,7 +123,7 @@ static int dispatch_codec(const CodecCall& c, bool quantize) {
         case 32: return launch_codec_d<32>(c, quantize);
         case 64: return launch_codec_d<64>(c, quantize);
         case 128: return launch_codec_d<128>(c, quantize);
-        case 256: return launch_codec_d<256>(c, quantize);
+        case 256: return launch_codec_d256(c, quantize);
         default: set_error("unsupported d = %d", c.d); return -1;
     }
 }

@@ -216,6 +216,71 @@ def test_gemma_shaped_reduced():
         _check_side(side, x, None, 4, 16, w.sign_seed)
 
 
+PAIR_CASES = [(group, bits, lam, tr) for group in (32, 64, 128) for bits in (4, 8) for lam in (False, True)
+              for tr in ("srft", "srht")]
+
+
+@pytest.mark.parametrize("group,bits,lam,tr", PAIR_CASES)
+def test_d256_groups_between_16_and_d(group, bits, lam, tr):
+    """d = 256 (two lanes per vector, each group's coordinates split between them) at the group sizes between
+    16 and d: 2 outer x 75 tokens x 2 heads (16-row tiles with a ragged last one) at t_offset 3 of t_cap 80,
+    the other width on V, then the GPU decode of the GPU codes against the oracle's decode of the same codes."""
+    w = I.Workload("pair", n_outer=2, tokens=75, kv_heads=2, d=256, lam=lam, data_seed=group + bits,
+                   outlier_kind="scale", outlier_channels=3, outlier_factor=40.0)
+    xk, xv = I.kv_side(w, "k"), I.kv_side(w, "v")
+    lk, lv = I.lam_table(w, "k"), I.lam_table(w, "v")
+    bits_v = 12 - bits
+    sides = []
+    for x, lam_t, b in ((xk, lk, bits), (xv, lv, bits_v)):
+        s = K.alloc_side(2, 80, 2, 256, b, group, transform=tr)
+        s.codes.fill_(0xAB)
+        s.scales.fill_(-1.0)
+        s.x, s.lam = x.cuda(), None if lam_t is None else lam_t.cuda()
+        sides.append(s)
+    K.srft_kv_quantize(sides[0], sides[1], 2, 75, 2, 256, group, 80, 3, 19)
+    torch.cuda.synchronize()
+    for side, x, lam_t, b in ((sides[0], xk, lk, bits), (sides[1], xv, lv, bits_v)):
+        lam_b = None if lam_t is None else _np(lam_t)[:, None, :, :]
+        enc = O.srft_kv_quantize(_np(x).astype(np.float64), lam_b, b, group, 19, transform=tr)
+        codes = _np(tm(side.codes))
+        assert_scales(_np(tm(side.scales))[:, 3:78], enc["scales"])
+        assert_codes(codes[:, 3:78], enc["r"], b)
+        assert (codes[:, :3] == 0xAB).all() and (codes[:, 78:] == 0xAB).all(), "rows outside the window were written"
+        out = torch.empty_like(side.x)
+        K.srft_kv_dequantize(K.Side(side.codes, side.scales, b, x=out, lam=side.lam, transform=tr), None, 2, 75, 2,
+                             256, group, 80, 3, 19)
+        torch.cuda.synchronize()
+        mine = O.srft_kv_dequantize(codes[:, 3:78], _np(tm(side.scales))[:, 3:78].astype(np.float64), lam_b, b, group,
+                                    19, transform=tr)
+        assert np.abs(_np(out) - mine).max() <= np.abs(mine).max() * 2.0**-10 + 1e-5
+
+
+def test_gemma_shaped_full_size_sampled():
+    """The full Gemma-3-1B-shaped cache (26 x 4096 x 1 x 256), K and V quantised in one launch and dequantised
+    in one launch, as the benchmark times them; 2000 sampled rows per side against the oracle."""
+    w = I.GEMMA
+    xk, xv = I.kv_side(w, "k", device="cuda"), I.kv_side(w, "v", device="cuda")
+    n_outer, T, H, d = xk.shape
+    sk, sv = K.alloc_side(n_outer, T, H, d, 4, 16), K.alloc_side(n_outer, T, H, d, 4, 16)
+    sk.x, sv.x = xk, xv
+    K.srft_kv_quantize(sk, sv, n_outer, T, H, d, 16, T, 0, w.sign_seed)
+    outk, outv = torch.empty_like(xk), torch.empty_like(xv)
+    K.srft_kv_dequantize(K.Side(sk.codes, sk.scales, 4, x=outk), K.Side(sv.codes, sv.scales, 4, x=outv), n_outer, T, H,
+                         d, 16, T, 0, w.sign_seed)
+    torch.cuda.synchronize()
+    rows = _sample_rows(n_outer * T * H, 2000, 47)
+    hrows = torch.as_tensor(hm_rows(rows, T, H), device="cuda")
+    for side, x, out in ((sk, xk, outk), (sv, xv, outv)):
+        xs = _np(x.reshape(-1, d)[rows]).astype(np.float64)
+        enc = O.srft_kv_quantize(xs, None, 4, 16, w.sign_seed)
+        assert_scales(_np(side.scales.reshape(-1, d // 16)[hrows]), enc["scales"])
+        assert_codes(_np(side.codes.reshape(-1, d // 2)[hrows]), enc["r"], 4)
+        xg = _np(out.reshape(-1, d)[rows]).astype(np.float64)
+        ref_hat = O.srft_kv_dequantize(enc["codes"], enc["scales"], None, 4, 16, w.sign_seed)
+        assert_dequant_within_step(xg, ref_hat, enc["scales"], None, 16)
+        assert_reconstruction_bound(xg, xs, enc["scales"], None, 16)
+
+
 def test_qwen_shaped_reduced_with_lambda():
     w = I.QWEN
     xk, xv = I.kv_side(w, "k", n_outer=2, tokens=700), I.kv_side(w, "v", n_outer=2, tokens=700)
