@@ -23,6 +23,8 @@ launches only that kernel on a cut-down decode workload (quantize/dequantize:
 B=2, the full 131072 tokens x 8 kv heads, 4.2 M vectors, about 1.6 GB held;
 attention: B=4, T=32768, a 201 MB packed cache) so that ncu captures stay
 small; it prints one JSON line with the median event time per launch.
+--kernel gemma_quantize|gemma_dequantize does the same for the d = 256 codec
+on the full Gemma-3-1B-shaped cache (0.21 M vectors, 150 MB).
 """
 
 from __future__ import annotations
@@ -57,7 +59,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--kernel", default=None, choices=("quantize", "dequantize", "attention"),
+    ap.add_argument("--kernel", default=None,
+                    choices=("quantize", "dequantize", "attention", "gemma_quantize", "gemma_dequantize"),
                     help="profiling case: launch only this kernel on a small workload")
     return ap.parse_args()
 
@@ -577,16 +580,20 @@ def run_case(args):
     torch.cuda.set_device(0)
     K.library()
     attn = args.kernel == "attention"
-    w = I.DECODE.resized(n_outer=4, tokens=32768) if attn else I.DECODE.resized(n_outer=2)
+    kind = args.kernel.split("_")[-1]
+    if args.kernel.startswith("gemma_"):
+        w = I.GEMMA
+    else:
+        w = I.DECODE.resized(n_outer=4, tokens=32768) if attn else I.DECODE.resized(n_outer=2)
     B, Hkv, d, T, Hq, G, seed = w.n_outer, w.kv_heads, w.d, w.tokens, w.q_heads, w.group, w.sign_seed
     xk, xv = I.kv_side(w, "k", device="cuda"), I.kv_side(w, "v", device="cuda")
     sk, sv = K.alloc_side(B, T, Hkv, d, 4, G), K.alloc_side(B, T, Hkv, d, 4, G)
     sk.x, sv.x = xk, xv
     K.srft_kv_quantize(sk, sv, B, T, Hkv, d, G, T, 0, seed)
-    if args.kernel == "quantize":
+    if kind == "quantize":
         def launch():
             K.srft_kv_quantize(sk, sv, B, T, Hkv, d, G, T, 0, seed)
-    elif args.kernel == "dequantize":
+    elif kind == "dequantize":
         dk, dv = torch.empty_like(xk), torch.empty_like(xv)
         deq_k, deq_v = K.Side(sk.codes, sk.scales, 4, x=dk), K.Side(sv.codes, sv.scales, 4, x=dv)
 
