@@ -346,36 +346,44 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                           "attn_bytes_per_token_head": tok_bytes}
         del vk, vv, dqk, dqv
 
-    # head dimension 96 (not a power of two): the same cache shape at d = 96 (the first 96 coordinates of the
-    # inputs), int4/int4, group 16, fp32 scales; attention also on the raw fp16 cache of the same inputs
-    d96 = 96
-    xk96, xv96, q96 = xk[..., :d96].contiguous(), xv[..., :d96].contiguous(), q[..., :d96].contiguous()
-    vk = K.alloc_side(B, t_cap, Hkv, d96, 4, G, device=dev)
-    vv = K.alloc_side(B, t_cap, Hkv, d96, 4, G, device=dev)
-    vk.x, vv.x = xk96, xv96
-    qv = time_launch(lambda: K.srft_kv_quantize(vk, vv, B, T, Hkv, d96, G, t_cap, 0, seed, stream))
-    ok96, ov96 = torch.empty_like(xk96), torch.empty_like(xv96)
-    dqk, dqv = K.Side(vk.codes, vk.scales, 4, x=ok96), K.Side(vv.codes, vv.scales, 4, x=ov96)
-    dv_ms = time_launch(lambda: K.srft_kv_dequantize(dqk, dqv, B, T, Hkv, d96, G, t_cap, 0, seed, stream))
-    out96 = torch.empty((B, Hq, d96), dtype=torch.float32, device=dev)
-    ws96 = torch.empty(K.q4kv_decode_attention_workspace_size(B, Hq, Hkv, d96, t_cap, 0), dtype=torch.uint8,
-                       device=dev)
-    av = time_launch(lambda: K.q4kv_decode_attention(q96, out96, vk, vv, B, Hq, Hkv, d96, G, t_cap, seq, 0.0, seed, 0,
-                                                     ws96, stream))
-    del ok96, ov96, dqk, dqv, vk, vv
-    rk96 = K.Side(xk96.permute(0, 2, 1, 3).contiguous(), None, 16)
-    rv96 = K.Side(xv96.permute(0, 2, 1, 3).contiguous(), None, 16)
-    ws96r = torch.empty(K.q4kv_decode_attention_workspace_size(B, Hq, Hkv, d96, T, 0), dtype=torch.uint8, device=dev)
-    f96 = time_launch(lambda: K.q4kv_decode_attention(q96, out96, rk96, rv96, B, Hq, Hkv, d96, G, T, seq, 0.0, seed,
-                                                      0, ws96r, stream))
-    vec96 = 2 * d96 + d96 // 2 + (d96 // G) * 4
-    tok96 = 2 * (d96 // 2 + (d96 // G) * 4)
-    variants["d96"] = {"head_dim": d96, "transform": "srft", "scales": "fp32", "quant_ms": qv, "deq_ms": dv_ms,
-                       "attn_ms": av, "quant_gbs": n_vec * vec96 / (qv * 1e-3) / 1e9,
-                       "deq_gbs": n_vec * vec96 / (dv_ms * 1e-3) / 1e9,
-                       "attn_gbs": B * T * Hkv * tok96 / (av * 1e-3) / 1e9, "attn_bytes_per_token_head": tok96,
-                       "fp16_cache_ms": f96, "attn_speedup_vs_fp16_cache": f96 / av}
-    del rk96, rv96, xk96, xv96, q96, out96, ws96, ws96r
+    # head dimensions that are not powers of two, on the same cache shape: d = 96 (the first 96 coordinates of
+    # the inputs; the tensor-core contraction) and d = 192 (the decode workload's generator at d = 192; the
+    # two-lane mixed-radix register transform), int4/int4, group 16, fp32 scales; attention also on the raw fp16
+    # cache of the same inputs
+    def nonpow2_variant(dn, xkn, xvn, qn):
+        vk = K.alloc_side(B, t_cap, Hkv, dn, 4, G, device=dev)
+        vv = K.alloc_side(B, t_cap, Hkv, dn, 4, G, device=dev)
+        vk.x, vv.x = xkn, xvn
+        qv = time_launch(lambda: K.srft_kv_quantize(vk, vv, B, T, Hkv, dn, G, t_cap, 0, seed, stream))
+        okn, ovn = torch.empty_like(xkn), torch.empty_like(xvn)
+        dqk, dqv = K.Side(vk.codes, vk.scales, 4, x=okn), K.Side(vv.codes, vv.scales, 4, x=ovn)
+        dv_ms = time_launch(lambda: K.srft_kv_dequantize(dqk, dqv, B, T, Hkv, dn, G, t_cap, 0, seed, stream))
+        outn = torch.empty((B, Hq, dn), dtype=torch.float32, device=dev)
+        wsn = torch.empty(K.q4kv_decode_attention_workspace_size(B, Hq, Hkv, dn, t_cap, 0), dtype=torch.uint8,
+                          device=dev)
+        av = time_launch(lambda: K.q4kv_decode_attention(qn, outn, vk, vv, B, Hq, Hkv, dn, G, t_cap, seq, 0.0, seed,
+                                                         0, wsn, stream))
+        del okn, ovn, dqk, dqv, vk, vv
+        rkn = K.Side(xkn.permute(0, 2, 1, 3).contiguous(), None, 16)
+        rvn = K.Side(xvn.permute(0, 2, 1, 3).contiguous(), None, 16)
+        wsr = torch.empty(K.q4kv_decode_attention_workspace_size(B, Hq, Hkv, dn, T, 0), dtype=torch.uint8, device=dev)
+        fn = time_launch(lambda: K.q4kv_decode_attention(qn, outn, rkn, rvn, B, Hq, Hkv, dn, G, T, seq, 0.0, seed,
+                                                         0, wsr, stream))
+        del rkn, rvn
+        vecn = 2 * dn + dn // 2 + (dn // G) * 4
+        tokn = 2 * (dn // 2 + (dn // G) * 4)
+        return {"head_dim": dn, "transform": "srft", "scales": "fp32", "quant_ms": qv, "deq_ms": dv_ms,
+                "attn_ms": av, "quant_gbs": n_vec * vecn / (qv * 1e-3) / 1e9,
+                "deq_gbs": n_vec * vecn / (dv_ms * 1e-3) / 1e9,
+                "attn_gbs": B * T * Hkv * tokn / (av * 1e-3) / 1e9, "attn_bytes_per_token_head": tokn,
+                "fp16_cache_ms": fn, "attn_speedup_vs_fp16_cache": fn / av}
+
+    variants["d96"] = nonpow2_variant(96, xk[..., :96].contiguous(), xv[..., :96].contiguous(),
+                                      q[..., :96].contiguous())
+    w192 = wd.resized(d=192)
+    variants["d192"] = nonpow2_variant(192, I.kv_side(w192, "k", device=dev), I.kv_side(w192, "v", device=dev),
+                                       I.query(w192, device=dev))
+    torch.cuda.empty_cache()
 
     other = other_workloads(K, I, torch, dev, stream, time_launch) if rank == 0 else None
 

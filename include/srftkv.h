@@ -38,11 +38,12 @@
  *    int8: two's-complement bytes;
  *  - scales are fp32; softmax scale defaults to 1/sqrt(d); a query with
  *    sequence length 0 gets a zero output;
- *  - a head dimension that is not a power of two (d = 96; Methodology 1
- *    names SRFT's freedom from the power-of-two restriction of Hadamard
- *    rotations): the same F, the unitary DFT of length d, with the same
- *    packing; the library forms it as a dense d x d map instead of radix-2
- *    FFT stages.
+ *  - a head dimension that is not a power of two (d = 96 or 192;
+ *    Methodology 1 names SRFT's freedom from the power-of-two restriction
+ *    of Hadamard rotations): the same F, the unitary DFT of length d, with
+ *    the same packing; the library forms it as a dense d x d map (d = 96)
+ *    or as a mixed-radix FFT (d = 192: 96 = 2 x 3 x 16 points) instead of
+ *    radix-2 stages only.
  *
  * General conventions
  *  - Every pointer argument that names tensor data is a DEVICE pointer
@@ -54,11 +55,12 @@
  *  - Return codes: SRFTKV_OK, or a negative SRFTKV_ERR_*; on any error no
  *    work has been enqueued and srftkv_last_error() describes it.
  *  - Inputs must be finite; NaN/Inf behaviour is unspecified.
- *  - Supported sizes: d in {16, 32, 64, 96, 128, 256} for the codec and
- *    srft_transform, d in {64, 96, 128, 256} for attention; group a power
- *    of two dividing d with 16 <= group <= d; bits in {4, 8} for packed
- *    sides.  d = 96 takes the SRFT only (the Hadamard matrix needs a power
- *    of two), groups of 16 or 32, and 16-byte aligned code and scale planes.
+ *  - Supported sizes: d in {16, 32, 64, 96, 128, 192, 256} for the codec
+ *    and srft_transform, d in {64, 96, 128, 192, 256} for attention; group
+ *    a power of two dividing d with 16 <= group <= d; bits in {4, 8} for
+ *    packed sides.  d = 96 and 192 take the SRFT only (the Hadamard matrix
+ *    needs a power of two) and 16-byte aligned code and scale planes; d =
+ *    96 takes groups of 16 or 32, d = 192 groups of 16, 32 or 64.
  */
 #ifndef SRFTKV_H
 #define SRFTKV_H
@@ -127,7 +129,8 @@ typedef struct srftkv_side {
  * 0 <= t_offset, t_offset + n_tokens <= t_cap, and x rows 16-byte aligned.
  * n_outer == 0 or n_tokens == 0 is a no-op that returns SRFTKV_OK.
  * d = 96 runs as the 128-wide tensor-core contraction with R zero outside
- * its 96 x 96 block (any call size).
+ * its 96 x 96 block (any call size); d = 192 as the register transform, two
+ * threads per vector.
  */
 int srft_kv_quantize(const srftkv_side* k, const srftkv_side* v, int n_outer, int n_tokens,
                      int H, int d, int group, int t_cap, int t_offset, uint64_t sign_seed,
@@ -169,14 +172,14 @@ int srft_kv_dequantize(const srftkv_side* k, const srftkv_side* v, int n_outer, 
  *              q4kv_decode_attention_workspace_size(...) bytes (16-byte aligned)
  *              for the per-split partial results; contents need not be
  *              initialised and are overwritten.
- * Requires d in {64, 96, 128, 256}, Hq % Hkv == 0 and Hq/Hkv <= 4, and for
- * packed sides a power-of-two group with 16 <= group <= d/4 (a scale row of
- * at least 16 bytes, the smallest TMA row; 16 or 32 at d = 96) and 16-byte
- * aligned scales; anything else returns SRFTKV_ERR_INVALID before any
- * launch.  fp16 / e8m0 scale planes, and every scale plane at d = 96 (rows
- * of 24 or 12 bytes), are copied as rows of 16 bytes and also need
- * t_cap * (d/group) * scale bytes to be a multiple of 16; d = 96 sides use
- * the SRFT.
+ * Requires d in {64, 96, 128, 192, 256}, Hq % Hkv == 0 and Hq/Hkv <= 4, and
+ * for packed sides a power-of-two group with 16 <= group <= d/4 (a scale
+ * row of at least 16 bytes, the smallest TMA row; 16 or 32 at d = 96 and
+ * 192) and 16-byte aligned scales; anything else returns SRFTKV_ERR_INVALID
+ * before any launch.  fp16 / e8m0 scale planes, and every scale plane at
+ * d = 96 and 192 (rows that are not a power of two), are copied as rows of
+ * 16 bytes and also need t_cap * (d/group) * scale bytes to be a multiple
+ * of 16; d = 96 and 192 sides use the SRFT.
  * Range: the kernel forms p * scale_V in fp16 with p in (0, 256], so value
  * scales must stay below 255 (|z_V| < 1785 for 4-bit values, < 32385 for
  * 8-bit); larger V scales overflow to inf.  Key scales have no such limit.

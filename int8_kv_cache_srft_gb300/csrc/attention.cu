@@ -160,6 +160,7 @@ constexpr bool pow2_dim() { return (D & (D - 1)) == 0; }
 // for a buffer that starts on a 1024-byte boundary.
 template <int RB>
 __host__ __device__ constexpr int swz_chunk(int r, int ch) {
+    if constexpr ((RB & (RB - 1)) != 0) return ch;  // rows that are not a power of two are never swizzled
     return ch ^ (((r * RB) >> 7) & (RB / 16 - 1));
 }
 
@@ -1210,7 +1211,9 @@ static int invalid_attn(const char* msg) {
 int attention_entry(const void* q, float* out, const srftkv_side* k, const srftkv_side* v, int B, int Hq, int Hkv,
                     int d, int group, int t_cap, const int* seq_lens, float sm_scale, uint64_t seed, int n_splits,
                     void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-    if (d != 64 && d != 96 && d != 128 && d != 256) return invalid_attn("attention: d must be 64, 96, 128 or 256");
+    if (d != 64 && d != 96 && d != 128 && d != 192 && d != 256)
+        return invalid_attn("attention: d must be 64, 96, 128, 192 or 256");
+    const bool pow2d = (d & (d - 1)) == 0;
     if (B < 0 || Hq <= 0 || Hkv <= 0 || t_cap <= 0) return invalid_attn("attention: need B >= 0, Hq, Hkv, t_cap > 0");
     if (Hq % Hkv) return invalid_attn("attention: Hq must be a multiple of Hkv");
     if (Hq / Hkv > 4) return invalid_attn("attention: at most 4 query heads per kv head are supported");
@@ -1220,8 +1223,8 @@ int attention_entry(const void* q, float* out, const srftkv_side* k, const srftk
     if (!raw && ((k->bits != 4 && k->bits != 8) || (v->bits != 4 && v->bits != 8)))
         return invalid_attn("attention: bits must be 4, 8 (or 16 on both sides)");
     if (!raw) {
-        // a power-of-two d copies fp32 scale rows as rows (at least 16 bytes: group <= d/4); d = 96 copies
-        // every scale plane as 16-byte rows of bytes and takes groups of 16 or 32
+        // a power-of-two d copies fp32 scale rows as rows (at least 16 bytes: group <= d/4); d = 96 and 192
+        // copy every scale plane as 16-byte rows of bytes and take groups of 16 or 32
         if (group < 16 || (group & (group - 1)) || (d == 96 ? group > 32 : group > d / 4))
             return invalid_attn("attention: group must be a power of two with 16 <= group <= d/4 (16 or 32 at d = 96)");
         if (!k->scales || !v->scales) return invalid_attn("attention: scales must not be NULL");
@@ -1233,10 +1236,10 @@ int attention_entry(const void* q, float* out, const srftkv_side* k, const srftk
                 sd->scale_format != SRFTKV_SCALE_E8M0)
                 return invalid_attn("attention: scale_format must be SRFTKV_SCALE_FP32, _FP16 or _E8M0");
             // fp16 / e8m0 scale planes are copied as 16-byte rows: one (batch, kv head)'s scales fill whole rows
-            if ((sd->scale_format != SRFTKV_SCALE_FP32 || d == 96) &&
+            if ((sd->scale_format != SRFTKV_SCALE_FP32 || !pow2d) &&
                 ((long long)t_cap * (d / group) * scale_bytes(sd->scale_format)) % 16 != 0)
                 return invalid_attn("attention: t_cap * (d/group) * scale bytes must be a multiple of 16");
-            if (d == 96 && sd->transform != SRFTKV_TRANSFORM_SRFT)
+            if (!pow2d && sd->transform != SRFTKV_TRANSFORM_SRFT)
                 return invalid_attn("attention: the Hadamard transform needs a power-of-two d");
         }
         if ((reinterpret_cast<uintptr_t>(k->scales) | reinterpret_cast<uintptr_t>(v->scales)) & 15)
@@ -1300,6 +1303,7 @@ int attention_entry(const void* q, float* out, const srftkv_side* k, const srftk
     switch (d) {
         case 64: return launch_all<64>(A);
         case 96: return launch_all<96>(A);
+        case 192: return launch_all<192>(A);
         case 128: return launch_all<128>(A);
         default: return launch_all<256>(A);
     }

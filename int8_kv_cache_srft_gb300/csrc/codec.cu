@@ -123,6 +123,7 @@ static int dispatch_codec(const CodecCall& c, bool quantize) {
         case 32: return launch_codec_d<32>(c, quantize);
         case 64: return launch_codec_d<64>(c, quantize);
         case 128: return launch_codec_d<128>(c, quantize);
+        case 192: return launch_codec_d192(c, quantize);
         case 256: return launch_codec_d256(c, quantize);
         default: set_error("unsupported d = %d", c.d); return -1;
     }
@@ -221,14 +222,14 @@ static int launch_transform(const void* x, float* y, int n, uint64_t seed, bool 
 }
 
 // ---------------------------------------------------------------------------
-// The bare SRFT at a head dimension that is not a power of two (d = 96) as the
+// The bare SRFT at a head dimension that is not a power of two (d = 96, 192) as the
 // dense real map p = R diag(s) x of the packed unitary DFT: R[0][k] = d^-1/2,
 // R[1][k] = (-1)^k d^-1/2, and for 1 <= j < d/2 R[2j][k] = sqrt(2/d) cos(2 pi jk/d),
 // R[2j+1][k] = -sqrt(2/d) sin(2 pi jk/d); the inverse is diag(s) R^T.  A block
 // takes four rows at a time, one thread per output coordinate, with the
 // angles from a table of cos / sin(2 pi m/d) evaluated in double.
 // ---------------------------------------------------------------------------
-constexpr int DT_ROWS = 4, DT_MAXD = 128;
+constexpr int DT_ROWS = 4, DT_MAXD = 256;
 
 __global__ void __launch_bounds__(128) srft_dense_transform_kernel(const __half* __restrict__ x, float* __restrict__ y,
                                                                    int n, int d, const __grid_constant__ SignParams S,
@@ -291,7 +292,7 @@ static int launch_dense_transform(const void* x, float* y, int n, int d, uint64_
 
 int transform_launch(const void* x, float* y, int n, int d, uint64_t seed, bool inverse, bool srht, cudaStream_t s) {
     if (n == 0) return 0;
-    if (d == 96 && !srht) return launch_dense_transform(x, y, n, d, seed, inverse, s);
+    if ((d == 96 || d == 192) && !srht) return launch_dense_transform(x, y, n, d, seed, inverse, s);
     switch (d) {
         case 16: return launch_transform<16>(x, y, n, seed, inverse, srht, s);
         case 32: return launch_transform<32>(x, y, n, seed, inverse, srht, s);

@@ -6,7 +6,7 @@
 namespace srftkv {
 
 int launch_codec_d256(const CodecCall& c, bool quantize) {
-    return quantize ? launch_pair_all<true>(c) : pair_dequantize_d256(c);
+    return quantize ? launch_pair_all<256, true>(c) : pair_dequantize_d256(c);
 }
 
 }  // namespace srftkv

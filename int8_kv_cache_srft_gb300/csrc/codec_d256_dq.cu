@@ -4,6 +4,6 @@
 
 namespace srftkv {
 
-int pair_dequantize_d256(const CodecCall& c) { return launch_pair_all<false>(c); }
+int pair_dequantize_d256(const CodecCall& c) { return launch_pair_all<256, false>(c); }
 
 }  // namespace srftkv

@@ -48,7 +48,8 @@ bool encode_x_map(CUtensorMap* map, void* base, int d, int H, int n_tokens, int 
 
 int codec_quantize(const CodecCall& c);
 int codec_dequantize(const CodecCall& c);
-// The register-transform codec at d = 256 (two threads per vector, codec_d256.cu).
+// The register-transform codec at d = 192 and 256 (two threads per vector, codec_d192.cu, codec_d256.cu).
+int launch_codec_d192(const CodecCall& c, bool quantize);
 int launch_codec_d256(const CodecCall& c, bool quantize);
 int transform_launch(const void* x, float* y, int n, int d, uint64_t seed, bool inverse, bool srht, cudaStream_t s);
 unsigned int codec_take_fault();

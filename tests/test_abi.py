@@ -172,6 +172,26 @@ def test_d96_rules(lib):
     assert _q(lib, _side(), None, d=96, n_tokens=0) == K.SRFTKV_OK
 
 
+@pytest.mark.parametrize("d,bits,group,code,scale", [(192, 4, 16, 96, 48), (192, 8, 64, 192, 12)])
+def test_vector_bytes_d192(lib, d, bits, group, code, scale):
+    assert K.srft_kv_vector_bytes(d, bits, group) == (code, scale)
+
+
+def test_d192_rules(lib):
+    """d = 192: groups must divide d (16, 32 or 64; not 128), the Hadamard variant needs a power of two, codes
+    and scales must be 16-byte aligned, and attention takes groups of 16 or 32 (at most d/4)."""
+    assert _q(lib, _side(), None, d=192, group=128) == K.SRFTKV_ERR_INVALID
+    srht = _side()
+    srht.transform = 1
+    assert _q(lib, srht, None, d=192) == K.SRFTKV_ERR_INVALID
+    assert b"power-of-two" in lib.srftkv_last_error()
+    assert _q(lib, _side(scales=264), None, d=192) == K.SRFTKV_ERR_INVALID   # 8-byte aligned only
+    assert lib.srht_transform(16, 16, 4, 192, 1, 0, None) == K.SRFTKV_ERR_INVALID
+    assert lib.srft_transform(16, 16, 0, 192, 1, 0, None) == K.SRFTKV_OK
+    assert _q(lib, _side(), None, d=192, n_tokens=0) == K.SRFTKV_OK
+    assert _attn(lib, _side(), _side(), d=192, group=64) == K.SRFTKV_ERR_INVALID
+
+
 def test_side_marshalling_is_cached_until_a_field_changes():
     """The binding builds a side's C struct once; assigning any field rebuilds it with the new pointers."""
     import torch

@@ -78,7 +78,7 @@ def check_basis_closed_form(o, d, seed=11):
         assert np.abs(R[:, j] - s[j] * np.array(col)).max() < 1e-13
 
 
-@pytest.mark.parametrize("d", (4, 8, 16, 64, 6, 12, 96))
+@pytest.mark.parametrize("d", (4, 8, 16, 64, 6, 12, 96, 192))
 def test_basis_vectors_closed_form(d):
     check_basis_closed_form(O, d)
 
