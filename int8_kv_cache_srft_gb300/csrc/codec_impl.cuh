@@ -1,5 +1,8 @@
-// codec_impl.cuh -- the fused SRFT quantize and dequantize kernels.  Each
-// head dimension is instantiated in its own translation unit (codec_d*.cu).
+// codec_impl.cuh -- the fused SRFT quantize and dequantize kernels for the
+// power-of-two head dimensions up to 128, one thread per head vector; each d is
+// instantiated in its own translation unit (codec_d16.cu ... codec_d128.cu).
+// d = 192 and 256 use two threads per vector (codec_pair.cuh).  The helpers
+// shared with the other codec kernels (group scales, packing, tiles) live here.
 //
 // Method: "When Quantization Is Free: An int4 KV Cache That Outruns fp16 on
 // Apple Silicon", Methodology 2: one fused kernel per direction doing the
@@ -42,7 +45,6 @@ struct CodecParams {
     CodecSideK side[2];
     int n_outer, H, t_cap, t_offset, group;
     int n_tokens;
-    int d;                // head dimension (the tensor-core kernels pad d < 128 to their 128-wide tiles)
     int tiles_per_head;   // ceil(n_tokens / rows per tile)
     int tiles_per_side;   // n_outer * H * tiles_per_head
     int total_tiles;      // n_sides * tiles_per_side
@@ -55,15 +57,14 @@ struct Geo {
     static constexpr int N = D / 2;
     static constexpr int ROWS = 32;                                       // rows per warp tile
     static constexpr int PAD = 8;                                         // fp16 elements of row padding
-    static constexpr int ROW_H = (D == 256) ? 2 * (128 + PAD) : D + PAD;  // elements per smem row
+    static constexpr int ROW_H = D + PAD;                                 // elements per smem row
     static constexpr int BUF_BYTES = ROWS * ROW_H * 2;
     static constexpr int WARPS = 4;
     static constexpr int SMEM = 128 + WARPS * 2 * BUF_BYTES;
-    static constexpr int MIN_BLOCKS = (D <= 128) ? 3 : 1;
+    static constexpr int MIN_BLOCKS = 3;
+    static_assert(D <= 128, "one thread per vector covers d <= 128");
     // element offset of 16-byte chunk c inside a padded smem row
-    static __device__ __forceinline__ int chunk_off(int c) {
-        return (D == 256) ? (c / 16) * (128 + PAD) + (c % 16) * 8 : c * 8;
-    }
+    static __device__ __forceinline__ int chunk_off(int c) { return c * 8; }
 };
 
 // A tile is a block of ROWS consecutive tokens of one (side, outer, head): its
@@ -380,10 +381,7 @@ __global__ void __launch_bounds__(128, Geo<D>::MIN_BLOCKS)
         const uint32_t bar = b ? bar1 : bar0;
         const uint32_t dst = ptx::smem_u32(bufs + b * Gm::BUF_BYTES);
         ptx::mbar_arrive_expect_tx(bar, Gm::BUF_BYTES);
-        if constexpr (D == 256)
-            ptx::tma_load_5d(dst, tm, bar, 0, 0, id.h, id.t0, id.o);
-        else
-            ptx::tma_load_4d(dst, tm, bar, 0, id.h, id.t0, id.o);
+        ptx::tma_load_4d(dst, tm, bar, 0, id.h, id.t0, id.o);
     };
     if (lane == 0 && tile < P.total_tiles) issue(tile, 0);
     for (int it = 0; tile < P.total_tiles; ++it, tile += stride) {
@@ -479,10 +477,7 @@ __global__ void __launch_bounds__(128, Geo<D>::MIN_BLOCKS)
         __syncwarp();
         if (lane == 0) {
             const CUtensorMap* tm = id.side ? &tm1 : &tm0;
-            if constexpr (D == 256)
-                ptx::tma_store_5d(tm, ptx::smem_u32(buf), 0, 0, id.h, id.t0, id.o);
-            else
-                ptx::tma_store_4d(tm, ptx::smem_u32(buf), 0, id.h, id.t0, id.o);
+            ptx::tma_store_4d(tm, ptx::smem_u32(buf), 0, id.h, id.t0, id.o);
             ptx::bulk_commit();
         }
     }
@@ -507,7 +502,6 @@ static inline void fill_params(const CodecCall& c, CodecParams& P) {
     P.t_offset = c.t_offset;
     P.group = c.group;
     P.n_tokens = c.n_tokens;
-    P.d = c.d;
     P.tiles_per_head = (c.n_tokens + 31) / 32;
     P.tiles_per_side = c.n_outer * c.H * P.tiles_per_head;
     P.total_tiles = c.n_sides * P.tiles_per_side;
