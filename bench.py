@@ -171,34 +171,150 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # CPU side: the fp64 oracle on a bounded sample of the same workload
 # ---------------------------------------------------------------------------
+def host_cores() -> dict:
+    """Host cores this process may run on, and the thread count of the BLAS numpy calls (queried from the loaded
+    OpenBLAS when threadpoolctl is absent)."""
+    info = {"affinity_cores": len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count(),
+            "cpu_count": os.cpu_count(), "blas_threads": None, "blas": None}
+    try:
+        from threadpoolctl import threadpool_info
+
+        pools = [p for p in threadpool_info() if p.get("user_api") == "blas"]
+        if pools:
+            info["blas_threads"] = pools[0].get("num_threads")
+            info["blas"] = pools[0].get("internal_api")
+            return info
+    except ImportError:
+        pass
+    import ctypes
+
+    import numpy  # noqa: F401  (loads numpy's BLAS)
+
+    try:
+        with open("/proc/self/maps") as f:
+            libs = sorted({ln.split()[-1] for ln in f if "openblas" in ln.lower() and ln.strip().endswith(".so")
+                           or "openblas" in ln.lower() and ".so" in ln.split()[-1]})
+    except OSError:
+        libs = []
+    for path in libs:
+        try:
+            lib = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for sym in ("openblas_get_num_threads64_", "scipy_openblas_get_num_threads64_", "openblas_get_num_threads"):
+            fn = getattr(lib, sym, None)
+            if fn is not None:
+                fn.restype = ctypes.c_int
+                info["blas_threads"] = int(fn())
+                info["blas"] = os.path.basename(path)
+                return info
+    return info
+
+
+class _CpuClock:
+    """Wall and process CPU time of a region: cpu/wall is the number of cores the region kept busy."""
+
+    def __enter__(self):
+        self.w0, self.c0 = time.perf_counter(), time.process_time()
+        return self
+
+    def __exit__(self, *exc):
+        self.wall = time.perf_counter() - self.w0
+        self.cpu = time.process_time() - self.c0
+        self.busy_cores = self.cpu / self.wall if self.wall > 0 else None
+
+
 def oracle_sample(seconds: float):
-    """Time the oracle's quantize -> dequantize -> attention on slices of the workload (one sequence, one kv head,
-    4 query heads, 1024 tokens per slice) until about `seconds` of CPU time has been spent."""
+    """Time the oracle's quantize -> dequantize -> attention on slices of the decode workload (one sequence, one
+    kv head, 4 query heads, 1024 tokens per slice) until about `seconds` of wall time has been spent."""
     import numpy as np
     from oracle import srft_oracle as O
 
     rng = np.random.default_rng(5)
     d, T, rep = 128, 1024, 4
-    vecs, t0, slices = 0, time.perf_counter(), 0
-    while True:
-        k = rng.standard_normal((1, T, 1, d)).astype(np.float16).astype(np.float64)
-        v = rng.standard_normal((1, T, 1, d)).astype(np.float16).astype(np.float64)
-        q = rng.standard_normal((1, rep, d)).astype(np.float16).astype(np.float64)
-        ek = O.srft_kv_quantize(k, None, 4, 16, 5)
-        ev = O.srft_kv_quantize(v, None, 4, 16, 5)
-        O.srft_kv_dequantize(ek["codes"], ek["scales"], None, 4, 16, 5)
-        O.srft_kv_dequantize(ev["codes"], ev["scales"], None, 4, 16, 5)
-        O.packed_decode_attention(q, {"bits": 4, "codes": ek["codes"], "scales": ek["scales"], "lam": None, "group": 16},
-                                  {"bits": 4, "codes": ev["codes"], "scales": ev["scales"], "lam": None, "group": 16}, 5)
-        vecs += 2 * T
-        slices += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
-    cores = os.cpu_count()
-    return {"value": vecs / el, "unit": "KV vectors/s", "cores": cores, "kind": "oracle",
+    vecs, slices = 0, 0
+    with _CpuClock() as clk:
+        while True:
+            k = rng.standard_normal((1, T, 1, d)).astype(np.float16).astype(np.float64)
+            v = rng.standard_normal((1, T, 1, d)).astype(np.float16).astype(np.float64)
+            q = rng.standard_normal((1, rep, d)).astype(np.float16).astype(np.float64)
+            ek = O.srft_kv_quantize(k, None, 4, 16, 5)
+            ev = O.srft_kv_quantize(v, None, 4, 16, 5)
+            O.srft_kv_dequantize(ek["codes"], ek["scales"], None, 4, 16, 5)
+            O.srft_kv_dequantize(ev["codes"], ev["scales"], None, 4, 16, 5)
+            O.packed_decode_attention(q, {"bits": 4, "codes": ek["codes"], "scales": ek["scales"], "lam": None,
+                                          "group": 16},
+                                      {"bits": 4, "codes": ev["codes"], "scales": ev["scales"], "lam": None,
+                                       "group": 16}, 5)
+            vecs += 2 * T
+            slices += 1
+            if time.perf_counter() - clk.w0 >= seconds:
+                break
+    el = clk.wall
+    hc = host_cores()
+    return {"value": vecs / el, "unit": "KV vectors/s", "cores": hc["affinity_cores"], "kind": "oracle",
+            "busy_cores": clk.busy_cores, "blas_threads": hc["blas_threads"], "blas": hc["blas"],
             "sample": f"{slices} slices of 1 sequence x 1 kv head x 1024 tokens x d=128 (K and V quantised, "
-                      f"dequantised and attended by 4 query heads), {el:.1f} s; numpy fp64, BLAS default threads"}
+                      f"dequantised and attended by 4 query heads), {el:.1f} s; numpy fp64"}
+
+
+def oracle_per_config(seconds_each: float):
+    """The oracle on bounded samples of each workload, one figure per (workload, direction), plus a "fast CPU"
+    line: the same fp64 arithmetic with the d x d SRFT matrix R formed once and applied as a matrix product
+    (still O(d^2) a vector, no FFT).  Each sample is a whole number of (layer, token range) slices of the
+    workload's own seeded input, grown until about `seconds_each` of wall time."""
+    import numpy as np
+    import torch
+    from oracle import srft_oracle as O
+    from int8_kv_cache_srft_gb300 import inputs as I
+
+    out = {}
+
+    def run(key, w, direction, fast):
+        d, G, seed = w.d, w.group, w.sign_seed
+        R = O.srft_matrix(d, seed) if fast else None
+        toks = min(w.tokens, 512)
+        n_vec, n_slices, mse_num, mse_den, wall, cpu = 0, 0, 0.0, 0.0, 0.0, 0.0
+        while wall < seconds_each and n_vec < w.vectors_per_side:
+            # one slice: 1 layer x toks tokens x all kv heads of the workload's distribution (inputs generated
+            # outside the timed region)
+            ws = w.resized(n_outer=1, tokens=toks, data_seed=w.data_seed * 1000 + n_slices)
+            x = I.kv_side(ws, "k").to(torch.float64).numpy()
+            lam = I.lam_table(ws, "k")
+            lam = None if lam is None else lam[:, None].to(torch.float64).numpy()
+            with _CpuClock() as clk:
+                if fast:
+                    z = x @ R.T
+                    z = z if lam is None else z * lam
+                    qv, sc, _ = O.quantize_groups(z, 4, G)
+                    if direction == "dequantize":
+                        zh = np.repeat(sc, G, axis=-1) * qv
+                        xh = (zh if lam is None else zh / lam) @ R
+                else:
+                    enc = O.srft_kv_quantize(x, lam, 4, G, seed)
+                    if direction == "dequantize":
+                        xh = O.srft_kv_dequantize(enc["codes"], enc["scales"], lam, 4, G, seed)
+            wall += clk.wall
+            cpu += clk.cpu
+            if direction == "dequantize":
+                mse_num += float(((xh - x) ** 2).sum())
+                mse_den += float((x ** 2).sum())
+            n_vec += x.shape[1] * x.shape[2]
+            n_slices += 1
+        ent = {"vectors_per_s": n_vec / wall, "vectors": n_vec, "of_workload": n_vec / w.vectors_per_side,
+               "seconds": wall, "busy_cores": cpu / wall if wall > 0 else None,
+               "sample": f"{n_slices} slices of 1 layer x {toks} tokens x {w.kv_heads} kv heads (K side), d={d}"}
+        if direction == "dequantize":
+            ent["relative_mse"] = mse_num / mse_den
+            ent["note"] = "quantize of the sample included (the dequantize input is the oracle's own codes)"
+        out[key] = ent
+
+    for name, w in (("tiny", I.TINY), ("gemma_d256", I.GEMMA), ("qwen_d128_lambda", I.QWEN)):
+        for fast in (False, True):
+            run(f"{name}_quantize" + ("_fast" if fast else ""), w, "quantize", fast)
+    for fast in (False, True):
+        run("gemma_d256_dequantize" + ("_fast" if fast else ""), I.GEMMA, "dequantize", fast)
+    return out
 
 
 def run_reference(args, rank: int, world: int):
@@ -215,7 +331,8 @@ def run_reference(args, rank: int, world: int):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD, "sample": "oracle slices (see cpu_baseline)"},
-            "cpu_baseline": {"value": val, "unit": "KV vectors/s", "cores": os.cpu_count(), "kind": "oracle",
+            "cpu_baseline": {"value": val, "unit": "KV vectors/s", "cores": r["cores"], "kind": "oracle",
+                             "busy_cores": r["busy_cores"], "blas_threads": r["blas_threads"],
                              "sample": r["sample"]},
             "e2e": {"value": val, "unit": "KV vectors/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -430,8 +547,20 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         b.record(stream)
         torch.cuda.synchronize()
         ms_e2e = max_over_ranks(a.elapsed_time(b) / args.e2e_steps, dev)
+        # the same copies alone (no kernels): the host link's rate, which bounds the end-to-end figure
+        a.record(stream)
+        for _ in range(args.e2e_steps):
+            xk.copy_(hk, non_blocking=True)
+            xv.copy_(hv, non_blocking=True)
+            q.copy_(hq, non_blocking=True)
+            hout.copy_(out, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms_copy = a.elapsed_time(b) / args.e2e_steps
         e2e = {"value": job_value(world, n_vec, ms_e2e), "unit": "KV vectors/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e}
+               "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e, "copy_only_ms_per_step": ms_copy,
+               "host_link_gbs_copy_only": (h2d + d2h) / (ms_copy * 1e-3) / 1e9,
+               "bound": "host link: the step's copies alone take copy_only_ms_per_step of ms_per_step"}
 
     if rank != 0:
         return
@@ -440,13 +569,27 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     quant_bytes = n_vec * QUANT_BYTES_PER_VEC
     attn_bytes = B * T * Hkv * ATTN_BYTES_PER_TOKEN_HEAD
     achieved = quant_bytes / (med["quant"] * 1e-3) / 1e9
-    sha = kernel_source_sha()
-    traffic = recorded_traffic("srft_quantize_tc_kernel")
     attn_gbs = attn_bytes / (med["attn"] * 1e-3) / 1e9
+    # one roofline entry per HBM-bound kernel of the step (algorithmic bytes per launch / median event time);
+    # the line's "roofline" is the entry of the longest one
+    rooflines = {}
+    for part, kern, nbytes in (("quant", "srft_quantize_tc_kernel", quant_bytes),
+                               ("deq", "srft_dequantize_tc_kernel", n_vec * DEQ_BYTES_PER_VEC),
+                               ("attn", "q4kv_attn_split_kernel", attn_bytes)):
+        gbs = nbytes / (med[part] * 1e-3) / 1e9
+        tr = recorded_traffic(kern)
+        rooflines[kern] = {"bound": "hbm", "kernel": kern, "ms": med[part], "achieved": gbs, "peak": peak,
+                           "peak_kind": peak_kind, "unit": "GB/s", "frac": gbs / peak, "traffic": tr,
+                           "traffic_over_algorithmic": None if tr is None else tr / nbytes,
+                           "algorithmic_bytes_per_launch": nbytes}
+    dominant = max(rooflines.values(), key=lambda r: r["ms"])
     fp16_ms = statistics.median(t16)
     for vname in variants:  # against the d = 128 fp16 cache unless the variant timed its own
         variants[vname].setdefault("attn_speedup_vs_fp16_cache", fp16_ms / variants[vname]["attn_ms"])
-    cpu = None if args.no_cpu else oracle_sample(args.cpu_seconds)
+    cpu = None
+    if not args.no_cpu:
+        cpu = oracle_sample(args.cpu_seconds)
+        cpu["per_workload"] = oracle_per_config(args.cpu_seconds / 8)
     line = {
         "metric": METRIC,
         "value": value,
@@ -464,9 +607,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                    "bits_k": 4, "bits_v": 4, "group": G, "scales": "fp32", "vectors_per_step": n_vec,
                    "step": "quantize cache + dequantize cache + decode attention + 1-token append",
                    "l2": "inputs 8.6 GB >> 129 MB L2, no flush needed"},
-        "roofline": {"bound": "hbm", "kernel": "srft_quantize_tc_kernel", "achieved": achieved, "peak": peak,
-                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
-                     "algorithmic_bytes_per_launch": quant_bytes},
+        "roofline": dominant,
+        "rooflines": rooflines,
         "kernels_ms": med,
         "quantize": {"vectors_per_s": n_vec / (med["quant"] * 1e-3), "gbs": achieved, "frac": achieved / peak},
         "dequantize": {"vectors_per_s": n_vec / (med["deq"] * 1e-3),

@@ -47,8 +47,13 @@
  *
  * General conventions
  *  - Every pointer argument that names tensor data is a DEVICE pointer
- *    owned by the caller; the library allocates no device memory and keeps
- *    no state between calls except per-device capability checks.
+ *    owned by the caller; the library allocates no device memory.  State it
+ *    keeps between calls: per-device capability checks, a per-host-thread
+ *    copy of the last sign vector and error message, constant twiddle tables
+ *    compiled into the kernels, two device fault words (one per kernel
+ *    family) and the fixed-size scratch array of
+ *    q4kv_decode_attention_static (all file-scope __device__ data, held by
+ *    every GPU that loads the library).
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Work is enqueued without host synchronisation; device-side
  *    faults surface on the caller's next synchronisation.
@@ -202,13 +207,17 @@ int q4kv_decode_attention(const void* q, float* out, const srftkv_side* k, const
  * file-scope device array of SRFTKV_STATIC_SCRATCH_BYTES bytes that every GPU
  * loading the library holds until the process exits.  It calls no
  * cudaMalloc, cudaFree or other allocating routine.
- *  - Sizes whose workspace (q4kv_decode_attention_workspace_size) exceeds
- *    SRFTKV_STATIC_SCRATCH_BYTES are rejected with SRFTKV_ERR_INVALID;
- *    fewer n_splits lowers the need (the automatic choice at B=16, Hq=32,
- *    d=128 on a 152-SM GB300 needs about 8 MB).
- *  - The first call on a device looks up the array's device address (once,
- *    with that device current); make that first call before any stream
- *    capture.
+ *  - The arguments are checked first, exactly as q4kv_decode_attention
+ *    checks them.  With n_splits == 0 the automatic split count is lowered
+ *    until the workspace (q4kv_decode_attention_workspace_size) fits in
+ *    SRFTKV_STATIC_SCRATCH_BYTES; sizes whose workspace exceeds it even so
+ *    (or with the n_splits given) are rejected with SRFTKV_ERR_INVALID.  The
+ *    automatic choice at B=16, Hq=32, d=128 on a 152-SM GB300 needs about
+ *    8 MB and is not lowered.
+ *  - The first call in a CUDA context (for the runtime's primary context:
+ *    the first call on a device) looks up the array's device address with
+ *    that device current and caches it under the context's ID; make that
+ *    first call before any stream capture.
  *  - All calls share the one array, which keeps the last call's contents;
  *    calls whose work overlaps on the GPU (e.g. on two streams) race.
  *    Nothing in it needs to start zeroed: each call writes all it reads.
@@ -223,9 +232,11 @@ int q4kv_decode_attention_static(const void* q, float* out, const srftkv_side* k
  * automatic choice on the current device).  Returns 0 for invalid sizes. */
 size_t q4kv_decode_attention_workspace_size(int B, int Hq, int Hkv, int d, int t_cap, int n_splits);
 
-/* Bytes of one packed vector: code plane d*bits/8 and scale plane 4*d/group
- * (fp32 scales).  Host-only; returns SRFTKV_OK or SRFTKV_ERR_INVALID. */
-int srft_kv_vector_bytes(int d, int bits, int group, size_t* code_bytes, size_t* scale_bytes);
+/* Bytes of one packed vector: code plane d*bits/8 and scale plane
+ * (d/group) * b with b = 4, 2 or 1 for scale_format SRFTKV_SCALE_FP32, _FP16
+ * or _E8M0.  Host-only; returns SRFTKV_OK or SRFTKV_ERR_INVALID (sizes the
+ * codec does not take, or an unknown scale_format). */
+int srft_kv_vector_bytes(int d, int bits, int group, int scale_format, size_t* code_bytes, size_t* scale_bytes);
 
 /*
  * srft_transform -- the bare transform, for testing ([WQF] Methodology 1).

@@ -69,7 +69,7 @@ def library() -> ctypes.CDLL:
     lib.q4kv_decode_attention_static.argtypes = [vp, vp, sp, sp, i, i, i, i, i, i, vp, ctypes.c_float, u64, i, vp]
     lib.q4kv_decode_attention_workspace_size.argtypes = [i, i, i, i, i, i]
     lib.q4kv_decode_attention_workspace_size.restype = sz
-    lib.srft_kv_vector_bytes.argtypes = [i, i, i, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+    lib.srft_kv_vector_bytes.argtypes = [i, i, i, i, ctypes.POINTER(sz), ctypes.POINTER(sz)]
     lib.srft_transform.argtypes = [vp, vp, i, i, u64, i, vp]
     lib.srht_transform.argtypes = [vp, vp, i, i, u64, i, vp]
     lib.srftkv_last_error.restype = ctypes.c_char_p
@@ -194,9 +194,12 @@ def q4kv_decode_attention_static(q: torch.Tensor, out: torch.Tensor, k: Side, v:
     _check("q4kv_decode_attention_static", rc)
 
 
-def srft_kv_vector_bytes(d: int, bits: int, group: int) -> tuple[int, int]:
+def srft_kv_vector_bytes(d: int, bits: int, group: int, scale_format: str = "fp32") -> tuple[int, int]:
+    """(code bytes, scale bytes) of one packed vector."""
     cb, sb = ctypes.c_size_t(0), ctypes.c_size_t(0)
-    _check("srft_kv_vector_bytes", library().srft_kv_vector_bytes(d, bits, group, ctypes.byref(cb), ctypes.byref(sb)))
+    fmt = SCALE_FORMATS[scale_format] if isinstance(scale_format, str) else int(scale_format)
+    _check("srft_kv_vector_bytes", library().srft_kv_vector_bytes(d, bits, group, fmt, ctypes.byref(cb),
+                                                                  ctypes.byref(sb)))
     return cb.value, sb.value
 
 

@@ -117,6 +117,62 @@ int device_sm_count() {
 }
 
 // ---------------------------------------------------------------------------
+// Device addresses of the library's __device__ variables, per CUDA context
+// ---------------------------------------------------------------------------
+// The address of a __device__ variable belongs to the context that loaded the
+// module: it differs between contexts of one device (the primary context and a
+// driver-API context, or the primary context before and after a device reset).
+// So lookups are cached under the current context's ID, which CUDA never
+// reuses within a process.
+static PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+static PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+static std::once_flag g_ctx_once;
+
+static bool current_context_id(unsigned long long* id) {
+    std::call_once(g_ctx_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+    });
+    if (!g_ctx_current || !g_ctx_id) return false;
+    CUcontext ctx = nullptr;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+    return g_ctx_id(ctx, id) == CUDA_SUCCESS;
+}
+
+int symbol_address(SymbolCache& cache, const void* symbol, void** out, const char* what) {
+    unsigned long long id = 0;
+    const bool have_id = current_context_id(&id);  // false before the runtime has made a context current
+    std::lock_guard<std::mutex> lk(cache.mu);
+    if (have_id)
+        for (int i = 0; i < SymbolCache::kSlots; ++i)
+            if (cache.id[i] == id && cache.ptr[i]) {
+                *out = cache.ptr[i];
+                return SRFTKV_OK;
+            }
+    void* p = nullptr;  // the lookup allocates nothing; it makes the device's primary context current if none is
+    const cudaError_t e = cudaGetSymbolAddress(&p, symbol);
+    if (e != cudaSuccess || !p) {
+        set_error("cudaGetSymbolAddress failed for %s: %s", what, cudaGetErrorString(e));
+        return SRFTKV_ERR_CUDA;
+    }
+    if (have_id || current_context_id(&id)) {
+        const int slot = cache.next;
+        cache.next = (cache.next + 1) % SymbolCache::kSlots;
+        cache.id[slot] = id;
+        cache.ptr[slot] = p;
+    }
+    *out = p;
+    return SRFTKV_OK;
+}
+
+// ---------------------------------------------------------------------------
 // TMA tensor maps
 // ---------------------------------------------------------------------------
 static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -294,13 +350,15 @@ int srft_kv_dequantize(const srftkv_side* k, const srftkv_side* v, int n_outer, 
     return codec_common(k, v, n_outer, n_tokens, H, d, group, t_cap, t_offset, sign_seed, stream, false);
 }
 
-int srft_kv_vector_bytes(int d, int bits, int group, size_t* code_bytes, size_t* scale_bytes) {
+int srft_kv_vector_bytes(int d, int bits, int group, int scale_format, size_t* code_bytes, size_t* scale_bytes_out) {
     if (!codec_d(d)) return invalid("d must be one of 16, 32, 64, 96, 128, 192, 256");
     if (bits != 4 && bits != 8) return invalid("bits must be 4 or 8");
     if (!pow2(group) || group < 16 || group > d || d % group)
         return invalid("group must be a power of two dividing d with 16 <= group <= d");
+    if (scale_format != SRFTKV_SCALE_FP32 && scale_format != SRFTKV_SCALE_FP16 && scale_format != SRFTKV_SCALE_E8M0)
+        return invalid("scale_format %d is not supported", scale_format);
     if (code_bytes) *code_bytes = (size_t)d * bits / 8;
-    if (scale_bytes) *scale_bytes = (size_t)(d / group) * 4;
+    if (scale_bytes_out) *scale_bytes_out = (size_t)(d / group) * scale_bytes(scale_format);
     return SRFTKV_OK;
 }
 

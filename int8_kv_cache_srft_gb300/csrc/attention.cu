@@ -1208,9 +1208,8 @@ static int invalid_attn(const char* msg) {
     return SRFTKV_ERR_INVALID;
 }
 
-int attention_entry(const void* q, float* out, const srftkv_side* k, const srftkv_side* v, int B, int Hq, int Hkv,
-                    int d, int group, int t_cap, const int* seq_lens, float sm_scale, uint64_t seed, int n_splits,
-                    void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+int attention_check(const void* q, const float* out, const srftkv_side* k, const srftkv_side* v, int B, int Hq,
+                    int Hkv, int d, int group, int t_cap, int n_splits) {
     if (d != 64 && d != 96 && d != 128 && d != 192 && d != 256)
         return invalid_attn("attention: d must be 64, 96, 128, 192 or 256");
     const bool pow2d = (d & (d - 1)) == 0;
@@ -1256,9 +1255,20 @@ int attention_entry(const void* q, float* out, const srftkv_side* k, const srftk
         return invalid_attn("attention: q, out and codes must be 16-byte aligned");
     if ((long long)B * Hkv > (1ll << 31) - 1) return invalid_attn("attention: B * Hkv too large");
     if (n_splits < 0) return invalid_attn("attention: n_splits must be >= 0");
+    return SRFTKV_OK;
+}
+
+int attention_auto_splits(int B, int Hkv, int t_cap) { return auto_splits(B, Hkv, t_cap); }
+
+int attention_entry(const void* q, float* out, const srftkv_side* k, const srftkv_side* v, int B, int Hq, int Hkv,
+                    int d, int group, int t_cap, const int* seq_lens, float sm_scale, uint64_t seed, int n_splits,
+                    void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    const int rc = attention_check(q, out, k, v, B, Hq, Hkv, d, group, t_cap, n_splits);
+    if (rc) return rc;
     if (B == 0) return SRFTKV_OK;
     const int rc0 = current_device_ok();
     if (rc0) return rc0;
+    const bool raw = k->bits == 16;
     const int ns = n_splits ? n_splits : auto_splits(B, Hkv, t_cap);
     const WsLayout wl = ws_layout(B, Hq, d, ns);
     if (!workspace || workspace_bytes < wl.total || (reinterpret_cast<uintptr_t>(workspace) & 15)) {

@@ -13,15 +13,14 @@
 //
 // Host code cannot use the array's name as a device address (on the host it
 // is only a stand-in symbol), so the address is looked up with
-// cudaGetSymbolAddress once per device, with that device current, on the
-// first call made on that device; that first call should therefore come
+// cudaGetSymbolAddress, with the device current, on the first call made in a
+// CUDA context (for the runtime's usual primary context: once per device) and
+// cached under that context's ID; that first call should therefore come
 // before any stream capture.  All calls share the one array and it keeps the
 // contents of the last call: two calls whose work overlaps on the GPU (for
 // example on two streams) race on it.  Nothing in it needs to start at zero:
 // every call writes all the scratch it reads.
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "internal.h"
 
@@ -29,31 +28,10 @@ namespace srftkv {
 
 static __device__ __align__(256) unsigned char g_attention_scratch[SRFTKV_STATIC_SCRATCH_BYTES];
 
-namespace {
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-}  // namespace
-
-// Device address of the scratch array on the current device (looked up once).
-static int scratch_for_current_device(void** out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-        set_error("q4kv_decode_attention_static: no usable current CUDA device");
-        return SRFTKV_ERR_CUDA;
-    }
-    std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
-        void* p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_attention_scratch);
-        if (e != cudaSuccess || !p) {
-            set_error("q4kv_decode_attention_static: cudaGetSymbolAddress failed: %s", cudaGetErrorString(e));
-            return SRFTKV_ERR_CUDA;
-        }
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
-    return SRFTKV_OK;
+// Device address of the scratch array in the current context (looked up once per context).
+static int scratch_for_current_context(void** out) {
+    static SymbolCache cache;
+    return symbol_address(cache, g_attention_scratch, out, "the static attention scratch array");
 }
 
 }  // namespace srftkv
@@ -63,19 +41,29 @@ using namespace srftkv;
 extern "C" int q4kv_decode_attention_static(const void* q, float* out, const srftkv_side* k, const srftkv_side* v,
                                             int B, int Hq, int Hkv, int d, int group, int t_cap, const int* seq_lens,
                                             float sm_scale, uint64_t sign_seed, int n_splits, void* stream) {
-    const size_t need = attention_workspace_size(B, Hq, Hkv, d, t_cap, n_splits);
-    if (need == 0)  // invalid sizes (or nothing to do): the shared validation reports which
-        return attention_entry(q, out, k, v, B, Hq, Hkv, d, group, t_cap, seq_lens, sm_scale, sign_seed, n_splits,
-                               nullptr, 0, static_cast<cudaStream_t>(stream));
-    if (need > (size_t)SRFTKV_STATIC_SCRATCH_BYTES) {
-        set_error("q4kv_decode_attention_static: these sizes need %zu bytes of scratch but the static array holds %zu; "
-                  "pass fewer n_splits or use q4kv_decode_attention with a caller workspace",
-                  need, (size_t)SRFTKV_STATIC_SCRATCH_BYTES);
+    // the arguments first, so that a bad call reports its own error rather than the array's size
+    int rc = attention_check(q, out, k, v, B, Hq, Hkv, d, group, t_cap, n_splits);
+    if (rc) return rc;
+    if (B == 0) return SRFTKV_OK;
+    rc = current_device_ok();
+    if (rc) return rc;
+    const size_t cap = (size_t)SRFTKV_STATIC_SCRATCH_BYTES;
+    int ns = n_splits;
+    if (ns == 0) {  // the automatic count, lowered until the workspace fits the array
+        ns = attention_auto_splits(B, Hkv, t_cap);
+        while (ns > 1 && attention_workspace_size(B, Hq, Hkv, d, t_cap, ns) > cap) --ns;
+    }
+    const size_t need = attention_workspace_size(B, Hq, Hkv, d, t_cap, ns);
+    if (need > cap) {
+        set_error("q4kv_decode_attention_static: these sizes need %zu bytes of scratch with %d split(s) but the static "
+                  "array holds %zu; pass fewer n_splits, a smaller batch, or use q4kv_decode_attention with a caller "
+                  "workspace",
+                  need, ns, cap);
         return SRFTKV_ERR_INVALID;
     }
     void* scratch = nullptr;
-    const int rc = scratch_for_current_device(&scratch);
+    rc = scratch_for_current_context(&scratch);
     if (rc) return rc;
-    return attention_entry(q, out, k, v, B, Hq, Hkv, d, group, t_cap, seq_lens, sm_scale, sign_seed, n_splits,
-                           scratch, (size_t)SRFTKV_STATIC_SCRATCH_BYTES, static_cast<cudaStream_t>(stream));
+    return attention_entry(q, out, k, v, B, Hq, Hkv, d, group, t_cap, seq_lens, sm_scale, sign_seed, ns, scratch, cap,
+                           static_cast<cudaStream_t>(stream));
 }

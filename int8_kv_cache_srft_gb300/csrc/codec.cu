@@ -16,8 +16,6 @@
 namespace srftkv {
 
 static __device__ unsigned int g_codec_fault;
-static std::mutex g_fault_mu;
-static unsigned int* g_fault_ptr[64] = {};
 
 template <int D>
 int launch_codec_d(const CodecCall& c, bool quantize);
@@ -304,21 +302,11 @@ int transform_launch(const void* x, float* y, int n, int d, uint64_t seed, bool 
 }
 
 unsigned int* codec_fault_word() {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
-        set_error("no current CUDA device");
-        return nullptr;
-    }
-    std::lock_guard<std::mutex> lk(g_fault_mu);
-    if (!g_fault_ptr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_codec_fault) != cudaSuccess) {
-            set_error("cudaGetSymbolAddress failed for the codec fault word");
-            return nullptr;
-        }
-        g_fault_ptr[dev] = static_cast<unsigned int*>(p);
-    }
-    return g_fault_ptr[dev];
+    static SymbolCache cache;
+    void* p = nullptr;
+    return symbol_address(cache, &g_codec_fault, &p, "the codec fault word") == SRFTKV_OK
+               ? static_cast<unsigned int*>(p)
+               : nullptr;
 }
 
 unsigned int codec_take_fault() {

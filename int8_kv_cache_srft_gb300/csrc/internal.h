@@ -7,6 +7,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 
 #include "srftkv.h"
 
@@ -56,6 +57,18 @@ unsigned int codec_take_fault();
 unsigned int* codec_fault_word();  // device address of the codec fault word (current device)
 
 void set_error(const char* fmt, ...);
+
+// Device address of a __device__ variable in the CUDA context current on this
+// thread, looked up once per context (cudaGetSymbolAddress, which allocates
+// nothing) and cached under the context's ID.  SRFTKV_OK or SRFTKV_ERR_CUDA.
+struct SymbolCache {
+    static constexpr int kSlots = 16;
+    std::mutex mu;
+    unsigned long long id[kSlots] = {};
+    void* ptr[kSlots] = {};
+    int next = 0;
+};
+int symbol_address(SymbolCache& cache, const void* symbol, void** out, const char* what);
 int device_sm_count();
 int current_device_ok();  // SRFTKV_OK, or the error code with the message set
 
@@ -78,6 +91,11 @@ int attention_entry(const void* q, float* out, const srftkv_side* k, const srftk
                     int d, int group, int t_cap, const int* seq_lens, float sm_scale, uint64_t seed, int n_splits,
                     void* workspace, size_t workspace_bytes, cudaStream_t stream);
 size_t attention_workspace_size(int B, int Hq, int Hkv, int d, int t_cap, int n_splits);
+// Argument checks of attention_entry that do not involve the workspace (SRFTKV_OK or the error, message set).
+int attention_check(const void* q, const float* out, const srftkv_side* k, const srftkv_side* v, int B, int Hq,
+                    int Hkv, int d, int group, int t_cap, int n_splits);
+// The split count attention_entry picks for n_splits == 0 on the current device.
+int attention_auto_splits(int B, int Hkv, int t_cap);
 unsigned int attn_take_fault();
 
 }  // namespace srftkv

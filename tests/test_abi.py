@@ -33,8 +33,8 @@ def header_functions():
 def test_header_declares_the_entry_points():
     names = header_functions()
     for n in ("srft_kv_quantize", "srft_kv_dequantize", "q4kv_decode_attention",
-              "q4kv_decode_attention_workspace_size", "srft_kv_vector_bytes", "srft_transform",
-              "srftkv_last_error", "srftkv_device_fault"):
+              "q4kv_decode_attention_workspace_size", "q4kv_decode_attention_static", "srft_kv_vector_bytes",
+              "srft_transform", "srht_transform", "srftkv_last_error", "srftkv_device_fault"):
         assert n in names
 
 
@@ -54,6 +54,21 @@ def test_vector_bytes_rejects(lib, d, bits, group):
     with pytest.raises(K.SrftKvError) as e:
         K.srft_kv_vector_bytes(d, bits, group)
     assert e.value.code == K.SRFTKV_ERR_INVALID
+
+
+@pytest.mark.parametrize("d,bits,group,fmt,code,scale", [
+    (128, 4, 16, "fp16", 64, 16), (128, 4, 16, "e8m0", 64, 8), (128, 8, 32, "fp16", 128, 8),
+    (256, 4, 32, "e8m0", 128, 8), (96, 4, 16, "fp16", 48, 12), (192, 4, 16, "e8m0", 96, 12)])
+def test_vector_bytes_scale_formats(lib, d, bits, group, fmt, code, scale):
+    """The scale plane's bytes follow the scale format (4, 2 or 1 bytes a group): d=128, int4, group 16 gives
+    64 + 16 = 80 bytes with fp16 scales and 64 + 8 = 72 with e8m0 (3.2x and 3.56x against 256 bytes of fp16)."""
+    assert K.srft_kv_vector_bytes(d, bits, group, fmt) == (code, scale)
+
+
+def test_vector_bytes_rejects_unknown_scale_format(lib):
+    cb, sb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert lib.srft_kv_vector_bytes(128, 4, 16, 3, ctypes.byref(cb), ctypes.byref(sb)) == K.SRFTKV_ERR_INVALID
+    assert b"scale_format" in lib.srftkv_last_error()
 
 
 def _side(bits=4, x=16, codes=256, scales=256, lam=None, stride=0):
@@ -211,3 +226,26 @@ def test_side_marshalling_is_cached_until_a_field_changes():
     assert r.contents.lambda_ == lam.data_ptr() and r.contents.lambda_outer_stride == 0
     s.scale_format = "e8m0"
     assert s.c_pointer().contents.scale_format == 2
+
+
+def _attn_static(lib, k, v, B=2, Hq=8, Hkv=2, d=128, group=16, t_cap=64, n_splits=0, q=16, out=16):
+    return lib.q4kv_decode_attention_static(q, out, ctypes.pointer(k), ctypes.pointer(v), B, Hq, Hkv, d, group,
+                                            t_cap, None, 0.0, 1, n_splits, None)
+
+
+def test_static_attention_checks_arguments_before_the_array_size(lib):
+    """A bad argument is reported as itself even when the sizes would also overflow the static array, and the
+    checks run before any device work (so this needs no GPU)."""
+    assert _attn_static(lib, _side(), _side(), d=100, t_cap=1 << 24, n_splits=4096) == K.SRFTKV_ERR_INVALID
+    assert b"d must be" in lib.srftkv_last_error()
+    assert _attn_static(lib, _side(bits=3), _side(), t_cap=1 << 24, n_splits=4096) == K.SRFTKV_ERR_INVALID
+    assert b"bits" in lib.srftkv_last_error()
+    assert _attn_static(lib, _side(), _side(), B=0) == K.SRFTKV_OK
+
+
+def test_static_scratch_size_matches_the_header():
+    """The binding's copy of SRFTKV_STATIC_SCRATCH_BYTES is the header's value."""
+    text = open(HEADER).read()
+    m = re.search(r"#define\s+SRFTKV_STATIC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", text)
+    assert m, "SRFTKV_STATIC_SCRATCH_BYTES not found in the header"
+    assert K.STATIC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))

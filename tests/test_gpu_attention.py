@@ -5,8 +5,6 @@ dequantises exactly those codes and scales and runs plain softmax attention,
 so the comparison isolates the attention kernel (tolerance: 2e-3 max-abs).
 """
 
-import math
-
 import numpy as np
 import pytest
 import torch
@@ -150,35 +148,3 @@ def test_raw_fp16_cache_ignores_garbage_past_sequence_end():
     sv.codes[0, :, 37:] = float("inf")
     out = run_attention(q, sk, sv, B, Hkv * rep, Hkv, d, 16, t_cap, seq, seed)
     assert np.isfinite(out).all() and np.abs(out - ref).max() <= ATTN_ATOL
-
-
-def test_decode_workload_full_size_sampled():
-    """B=16, Hq=32, Hkv=8, d=128, T=131072: the full int4 cache quantised by the library, attention over all of
-    it with the automatic split count; (b, kv head) pairs sampled for the oracle.  The same kernel on the raw
-    fp16 cache is checked on the same samples."""
-    w = I.DECODE
-    B, Hkv, d, T, Hq = w.n_outer, w.kv_heads, w.d, w.tokens, w.q_heads
-    rep = Hq // Hkv
-    xk, xv = I.kv_side(w, "k", device="cuda"), I.kv_side(w, "v", device="cuda")
-    sk, sv = K.alloc_side(B, T, Hkv, d, 4, 16), K.alloc_side(B, T, Hkv, d, 4, 16)
-    sk.x, sv.x = xk, xv
-    K.srft_kv_quantize(sk, sv, B, T, Hkv, d, 16, T, 0, w.sign_seed)
-    q = I.query(w, device="cuda")
-    out = run_attention(q, sk, sv, B, Hq, Hkv, d, 16, T, None, w.sign_seed)
-    rk, rv = xk.permute(0, 2, 1, 3).contiguous(), xv.permute(0, 2, 1, 3).contiguous()
-    out16 = run_attention(q, K.Side(rk, None, 16), K.Side(rv, None, 16), B, Hq, Hkv, d, 16, T, None, w.sign_seed)
-    del rk, rv
-    qn = _np(q).astype(np.float64)
-    for b, h in ((0, 0), (B - 1, Hkv - 1), (7, 3)):
-        kh = O.srft_kv_dequantize(_np(sk.codes[b, h]), _np(sk.scales[b, h]).astype(np.float64), None, 4, 16,
-                                  w.sign_seed)
-        vh = O.srft_kv_dequantize(_np(sv.codes[b, h]), _np(sv.scales[b, h]).astype(np.float64), None, 4, 16,
-                                  w.sign_seed)
-        k16, v16 = _np(xk[b, :, h]).astype(np.float64), _np(xv[b, :, h]).astype(np.float64)
-        for r in range(rep):
-            hq = h * rep + r
-            for kk, vv, o in ((kh, vh, out), (k16, v16, out16)):
-                s = kk @ qn[b, hq] / math.sqrt(d)
-                pw = np.exp(s - s.max())
-                ref = (pw @ vv) / pw.sum()
-                assert np.abs(o[b, hq] - ref).max() <= ATTN_ATOL
