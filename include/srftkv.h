@@ -177,7 +177,9 @@ int srft_kv_dequantize(const srftkv_side* k, const srftkv_side* v, int n_outer, 
  *              q4kv_decode_attention_workspace_size(...) bytes (16-byte aligned)
  *              for the per-split partial results; contents need not be
  *              initialised and are overwritten.
- * Requires d in {64, 96, 128, 192, 256}, Hq % Hkv == 0 and Hq/Hkv <= 4, and
+ * Requires d in {64, 96, 128, 192, 256}, Hq % Hkv == 0 (any GQA ratio:
+ * ratios above 4 run as head groups of at most four query heads, so
+ * B * Hkv * ceil(Hq/Hkv/4) <= 65535), and
  * for packed sides a power-of-two group with 16 <= group <= d/4 (a scale
  * row of at least 16 bytes, the smallest TMA row; 16 or 32 at d = 96 and
  * 192) and 16-byte aligned scales; anything else returns SRFTKV_ERR_INVALID
@@ -185,9 +187,12 @@ int srft_kv_dequantize(const srftkv_side* k, const srftkv_side* v, int n_outer, 
  * d = 96 and 192 (rows that are not a power of two), are copied as rows of
  * 16 bytes and also need t_cap * (d/group) * scale bytes to be a multiple
  * of 16; d = 96 and 192 sides use the SRFT.
- * Range: the kernel forms p * scale_V in fp16 with p in (0, 256], so value
- * scales must stay below 255 (|z_V| < 1785 for 4-bit values, < 32385 for
- * 8-bit); larger V scales overflow to inf.  Key scales have no such limit.
+ * Range: the kernel forms p * scale_V in fp16.  A stretch of tokens whose
+ * V scales overflow that (scales of 128 and more) or sit far below it
+ * (p-weighted mean scale under 2^-14) is run a second time with the values
+ * rescaled by a power of two taken from its largest V scale, so any finite
+ * scale works; only such caches pay for the second pass.  Key scales are
+ * applied in fp32 and have no range limit.
  */
 int q4kv_decode_attention(const void* q, float* out, const srftkv_side* k, const srftkv_side* v,
                           int B, int Hq, int Hkv, int d, int group, int t_cap,

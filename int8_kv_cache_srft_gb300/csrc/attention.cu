@@ -61,7 +61,9 @@ struct AttnParams {
     long long lam_k_stride;
     const float* lam_v;
     long long lam_v_stride;
+    const uint8_t* vscale; // V scale plane (bytes), read directly only to size the V unit (see the split kernel)
     int B, Hq, Hkv, rep, t_cap, n_splits, group, log2_group;
+    int hpg, n_hg;         // query heads per head group (<= 4) and head groups per kv head
     int sp;                // scale row (floats)
     int tr_k, tr_v;        // transform of the K and V sides (SRFTKV_TRANSFORM_*)
     int sf_k, sf_v;        // scale format of the K and V sides (SRFTKV_SCALE_*)
@@ -685,8 +687,8 @@ __device__ __forceinline__ void attn_chunk(const AttnParams& P, uint8_t* __restr
                                            const uint32_t (&kso)[scale_chunks<D>()],
                                            const uint32_t (&vso)[scale_chunks<D>()], const uint32_t (&qh)[D / 8],
                                            const uint32_t (&ql)[D / 8],
-                                           const float (&nb)[D / 16], float (&acc)[D / 4],
-                                           float (&sv)[AttnCfg<D, BK, BV>::NSV], float& m, float& l) {
+                                           const float (&nb)[D / 16], int nh, float (&acc)[D / 4],
+                                           float (&sv)[AttnCfg<D, BK, BV>::NSV], float& m, float& l, float mu) {
     using C = AttnCfg<D, BK, BV>;
     constexpr float SU = C::QK ? kSub : 1.f;  // scores come in units of 1/SU
     const int g = lane >> 2, c = lane & 3;
@@ -747,9 +749,10 @@ __device__ __forceinline__ void attn_chunk(const AttnParams& P, uint8_t* __restr
         for (int i = 0; i < C::NSV; ++i) sv[i] *= fs;
         m = mn;
     }
-    // p in [0, 256]: the +8 keeps p * scale_V clear of fp16 subnormals; it cancels in acc / l
-    const float bias = (m == -INFINITY) ? 0.f : m - 8.f;
-    const bool offer = c < P.rep;  // padded heads offer zero
+    // p in [0, 256 * 2^-mu] (mu: the warp's V unit, 0 unless the V scales are far from 1): the +8 keeps
+    // p * scale_V clear of fp16 subnormals; it cancels in acc / l
+    const float bias = (m == -INFINITY) ? 0.f : m - 8.f + mu;
+    const bool offer = c < nh;  // padded heads offer zero
     const int hd = g >> 1;         // head of this thread's B columns
 #pragma unroll
     for (int st = 0; st < NT; ++st) {
@@ -791,6 +794,11 @@ __device__ __forceinline__ void acc_coord(int i, int g, int c, int& dim, int& he
     }
 }
 
+// Grid (n_splits, B * Hkv * n_hg): CTA (split, (b, kv head, head group)).
+// A head group is up to four query heads of one kv head (the MMA columns
+// carry four heads); GQA ratios above four run as several head groups, whose
+// CTAs sit next to each other in the launch order so that the second one's
+// reads of the same cache rows are mostly L2 hits.
 // d = 256 keeps 2 CTAs per SM: its fragments need more than a third of the register file
 template <int D, int BK, int BV, int G>
 __global__ void __launch_bounds__(kAttnWarps * 32, D >= 256 ? 2 : 3)
@@ -806,7 +814,9 @@ __global__ void __launch_bounds__(kAttnWarps * 32, D >= 256 ? 2 : 3)
     // (barrier and TMA operands then stay in uniform registers)
     const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0), lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
-    const int bh = blockIdx.y, b = bh / P.Hkv, hkv = bh - b * P.Hkv;
+    const int bhg = blockIdx.y, hg = bhg % P.n_hg, bh = bhg / P.n_hg;
+    const int b = bh / P.Hkv, hkv = bh - b * P.Hkv;
+    const int h0 = hg * P.hpg, nh = min(P.hpg, P.rep - h0);  // this CTA's query heads: h0 .. h0 + nh - 1
     const int split = blockIdx.x;
     const int L = P.seq_lens ? min(max(P.seq_lens[b], 0), P.t_cap) : P.t_cap;
     const int n_chunks = (L + C::CH - 1) / C::CH;
@@ -827,7 +837,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, D >= 256 ? 2 : 3)
 
     uint32_t qh[C::QB], ql[C::QB];
     float nb[D / 16];
-    build_qb<D, BK>(P.qt + ((long long)b * P.Hq + (long long)hkv * P.rep) * D, P.rep, g, c, qh, ql, nb);
+    build_qb<D, BK>(P.qt + ((long long)b * P.Hq + (long long)hkv * P.rep + h0) * D, nh, g, c, qh, ql, nb);
     // per-lane shared-memory addressing of the plane images
     using PK = PlaneT<D, BK>;
     using PV = PlaneT<D, BV>;
@@ -838,10 +848,6 @@ __global__ void __launch_bounds__(kAttnWarps * 32, D >= 256 ? 2 : 3)
     scale_offsets<D, SCH>(g, 0, kso);                               // K: row g (and g + 8)
     scale_offsets<D, SCH>(2 * c, BV == 4 ? 4 * (g & 1) : 0, vso);  // V: rows 2c (+1, +8, +9), column half
     float acc[C::ACC], sv[C::NSV];
-#pragma unroll
-    for (int i = 0; i < C::ACC; ++i) acc[i] = 0.f;
-#pragma unroll
-    for (int i = 0; i < C::NSV; ++i) sv[i] = 0.f;
     float m = -INFINITY, l = 0.f;  // online-softmax state for head c (log2 domain)
 
     const int plane_row = b * P.Hkv + hkv;  // this (batch, kv head)'s rows in the head-major planes
@@ -872,32 +878,116 @@ __global__ void __launch_bounds__(kAttnWarps * 32, D >= 256 ? 2 : 3)
             ptx::tma_load_3d(ptx::smem_u32(dst + vs_off), &tm_vs, bar, 0, vflat ? chunk * vs_row : tok, plane_row);
     };
 
-    // per-warp ring of NS stages: chunk j of this warp goes to stage j % NS, NS-1 chunks in flight
-    int chunk = c_begin + warp;
-    if (lane == 0) {
+    // per-warp ring of NS stages: iteration it (counted over both passes below)
+    // uses stage it % NS; NS-1 chunks are in flight
+    auto prologue = [&](int it0) {
+        if (lane == 0) {
 #pragma unroll
-        for (int j = 0; j < NS - 1; ++j)
-            if (chunk + j * kAttnWarps < c_end) issue(chunk + j * kAttnWarps, j);
-    }
-    bool failed = false;
-    for (int it = 0; chunk < c_end; ++it, chunk += kAttnWarps) {
-        const int st = it % NS;
-        const int nxt = chunk + (NS - 1) * kAttnWarps;
-        if (lane == 0 && nxt < c_end) issue(nxt, (it + NS - 1) % NS);
-        const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(barw(st), (it / NS) & 1));
-        if (!ok) {
-            if (lane == 0) {
-                atomicOr(&g_attn_fault, 1u);
-                for (int j = 1; j < NS; ++j)  // let the copies already in flight land before returning
-                    if (chunk + j * kAttnWarps < c_end)
-                        ptx::mbar_wait_bounded(barw((it + j) % NS), ((it + j) / NS) & 1, 1u << 16);
-            }
-            failed = true;
-            break;
+            for (int j = 0; j < NS - 1; ++j)
+                if (c_begin + warp + j * kAttnWarps < c_end) issue(c_begin + warp + j * kAttnWarps, (it0 + j) % NS);
         }
-        attn_chunk<D, BK, BV, C::CH / 16, G>(P, wbase + st * C::STAGE, chunk * C::CH, L, lane, LK, LV, kso, vso, qh,
-                                             ql, nb, acc, sv, m, l);
-        __syncwarp();
+    };
+    prologue(0);
+
+    // V unit.  P.V takes B = p * scale_V in fp16 with p <= 256 * 2^-mu, l and acc
+    // accumulating in that unit, and the (m, l) the warp exports carry m + mu.
+    // The first pass takes mu = 0, right for V scales of ordinary size.  A warp
+    // whose pass overflowed (a non-finite accumulator: some scale_V * p at or
+    // above 65520) or whose p-weighted mean V scale is below 2^-14 in every
+    // head (the low fp16 halves of B would fall into subnormals) runs its
+    // chunks once more with mu = (exponent of its largest V scale) - 6, read
+    // from the scale plane, so that every B is below 2^15.
+    float mu = 0.f;
+    bool failed = false, undrained = false;
+    int it = 0;
+    // one pass over this warp's chunks with V unit 2^mu_p (the first pass is called with a literal 0, so its
+    // loop is the plain one; the rare second pass is a separate copy)
+    auto run_pass = [&](float mu_p) {
+#pragma unroll
+        for (int i = 0; i < C::ACC; ++i) acc[i] = 0.f;
+#pragma unroll
+        for (int i = 0; i < C::NSV; ++i) sv[i] = 0.f;
+        m = -INFINITY;
+        l = 0.f;
+        for (int chunk = c_begin + warp; chunk < c_end; ++it, chunk += kAttnWarps) {
+            const int st = it % NS;
+            const int nxt = chunk + (NS - 1) * kAttnWarps;
+            if (lane == 0 && nxt < c_end) issue(nxt, (it + NS - 1) % NS);
+            const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(barw(st), (it / NS) & 1));
+            if (!ok) {
+                if (lane == 0) {
+                    atomicOr(&g_attn_fault, 1u);
+                    // let this warp's copies in flight land (this stage's included) before giving up; a copy
+                    // that still has not landed keeps the CTA away from its shared memory below
+                    bool all = true;
+                    for (int j = 0; j < NS; ++j)
+                        if (chunk + j * kAttnWarps < c_end)
+                            all &= ptx::mbar_wait_bounded(barw((it + j) % NS), ((it + j) / NS) & 1, 1u << 16);
+                    undrained = !all;
+                }
+                undrained = __shfl_sync(0xffffffffu, undrained, 0);
+                failed = true;
+                break;
+            }
+            attn_chunk<D, BK, BV, C::CH / 16, G>(P, wbase + st * C::STAGE, chunk * C::CH, L, lane, LK, LV, kso, vso,
+                                                 qh, ql, nb, nh, acc, sv, m, l, mu_p);
+            __syncwarp();
+        }
+    };
+    run_pass(0.f);
+    if (C::QV && !failed) {
+        bool redo;
+        {
+            bool bad = !isfinite(l);
+#pragma unroll
+            for (int i = 0; i < C::ACC; ++i) bad |= !isfinite(acc[i]);
+#pragma unroll
+            for (int i = 0; i < C::NSV; ++i) bad |= !isfinite(sv[i]);
+            redo = __any_sync(0xffffffffu, bad);
+            if (!redo) {
+                // p-weighted mean V scale of this thread's column (head c, its half) against 2^-14
+                float lt = l, smax = 0.f;
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
+#pragma unroll
+                for (int i = 0; i < C::NSV; ++i) {
+                    float t = sv[i];
+                    t += __shfl_xor_sync(0xffffffffu, t, 1);
+                    t += __shfl_xor_sync(0xffffffffu, t, 2);
+                    const int col = BV == 4 ? 2 * c + (g >= 4 ? 1 : 0) : 2 * c;
+                    smax = fmaxf(smax, __shfl_sync(0xffffffffu, t, 4 * col));
+                }
+                const bool counts = c < nh && lt > 0.f;
+                redo = __any_sync(0xffffffffu, counts) && __all_sync(0xffffffffu, !counts || smax < lt * 6.103515625e-05f);
+            }
+        }
+        if (redo) {
+            // the largest V scale of this warp's chunks, from the scale plane
+            const int sbv = P.sf_v == SRFTKV_SCALE_FP32 ? 4 : P.sf_v == SRFTKV_SCALE_FP16 ? 2 : 1;
+            const uint8_t* vsrc = P.vscale + (size_t)plane_row * P.t_cap * P.sp * sbv;
+            uint32_t vmax = 0u;
+            for (int ch = c_begin + warp; ch < c_end; ch += kAttnWarps) {
+                const int t = ch * C::CH + lane;
+                if (lane < C::CH && t < L) {
+                    const uint8_t* row = vsrc + (size_t)t * P.sp * sbv;
+                    for (int f = 0; f < P.sp; ++f) {
+                        float v;
+                        if (P.sf_v == SRFTKV_SCALE_FP32) v = __ldg(reinterpret_cast<const float*>(row) + f);
+                        else if (P.sf_v == SRFTKV_SCALE_FP16) v = __half2float(__ldg(reinterpret_cast<const __half*>(row) + f));
+                        else v = __uint_as_float((uint32_t)__ldg(row + f) << 23);
+                        vmax = max(vmax, __float_as_uint(fabsf(v)));
+                    }
+                }
+            }
+            vmax = __reduce_max_sync(0xffffffffu, vmax);
+            int un = vmax ? (int)(vmax >> 23) - 127 - 6 : 0;
+            un = min(max(un, -110), 120);  // p = 2^(8 - mu) .. stays a finite fp32 number
+            if (un != 0) {
+                mu = (float)un;
+                prologue(it);
+                run_pass(mu);
+            }
+        }
     }
     // the failure flag is per warp; every warp still joins the merge below
     if (failed) {
@@ -933,11 +1023,24 @@ __global__ void __launch_bounds__(kAttnWarps * 32, D >= 256 ? 2 : 3)
     // ---- per-warp totals of l over the 8 token rows ----
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-    __syncthreads();  // all warps are done with their stage buffers
+    const long long prow0 = (long long)b * P.Hq + (long long)hkv * P.rep + h0;
+    // all warps are done with their stage buffers; a copy that never landed keeps them all out of shared memory
+    if (__syncthreads_or(undrained ? 1 : 0)) {
+        for (int idx = threadIdx.x; idx < nh * D; idx += blockDim.x) {
+            const int h = idx / D, dim = idx - h * D;
+            const long long pidx = (prow0 + h) * P.n_splits + split;
+            P.part_acc[pidx * D + dim] = 0.f;
+            if (dim == 0) {
+                P.part_ml[pidx * 2] = -INFINITY;
+                P.part_ml[pidx * 2 + 1] = 0.f;
+            }
+        }
+        return;
+    }
     float* mw = reinterpret_cast<float*>(smem);                 // [warps][4][2]
     float* aw = mw + kAttnWarps * 8;                            // [warps][4][D]
     if (g == 0) {
-        mw[warp * 8 + c * 2 + 0] = m;
+        mw[warp * 8 + c * 2 + 0] = m == -INFINITY ? m : m + mu;  // the state is in the unit 2^-(m + mu - 8)
         mw[warp * 8 + c * 2 + 1] = l;
     }
 #pragma unroll
@@ -948,8 +1051,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, D >= 256 ? 2 : 3)
         if (useful) aw[(warp * 4 + head) * D + dim] = acc[i];
     }
     __syncthreads();
-    const long long prow0 = ((long long)b * P.Hq + (long long)hkv * P.rep);
-    for (int idx = threadIdx.x; idx < P.rep * D; idx += blockDim.x) {
+    for (int idx = threadIdx.x; idx < nh * D; idx += blockDim.x) {
         const int h = idx / D, dim = idx - h * D;
         float M = -INFINITY;
 #pragma unroll
@@ -1141,7 +1243,7 @@ static int launch_split(const AttnLaunch& A) {
                                  C::SMEM);
         attr[g16] = true;
     }
-    const dim3 grid(P.n_splits, P.B * P.Hkv);
+    const dim3 grid(P.n_splits, P.B * P.Hkv * P.n_hg);
     if (g16)
         q4kv_attn_split_kernel<D, BK, BV, 16><<<grid, kAttnWarps * 32, C::SMEM, A.stream>>>(tkc, tks, tvc, tvs, P);
     else
@@ -1180,8 +1282,12 @@ static int launch_all(const AttnLaunch& A) {
     return 0;
 }
 
-static int auto_splits(int B, int Hkv, int t_cap) {
-    const long long pairs = (long long)B * Hkv;
+// head groups of at most four query heads per kv head (the MMA columns carry four heads), as even as possible
+static int head_groups(int rep) { return (rep + 3) / 4; }
+static int heads_per_group(int rep) { return (rep + head_groups(rep) - 1) / head_groups(rep); }
+
+static int auto_splits(int B, int Hq, int Hkv, int t_cap) {
+    const long long pairs = (long long)B * Hkv * head_groups(Hq / Hkv);
     const long long target = 8ll * device_sm_count() * 3;  // about eight waves of resident CTAs
     long long s = (target + pairs - 1) / pairs;
     const long long max_s = (t_cap + 255) / 256;
@@ -1215,7 +1321,6 @@ int attention_check(const void* q, const float* out, const srftkv_side* k, const
     const bool pow2d = (d & (d - 1)) == 0;
     if (B < 0 || Hq <= 0 || Hkv <= 0 || t_cap <= 0) return invalid_attn("attention: need B >= 0, Hq, Hkv, t_cap > 0");
     if (Hq % Hkv) return invalid_attn("attention: Hq must be a multiple of Hkv");
-    if (Hq / Hkv > 4) return invalid_attn("attention: at most 4 query heads per kv head are supported");
     if (!k || !v || !q || !out) return invalid_attn("attention: q, out, k and v must not be NULL");
     const bool raw = k->bits == 16 || v->bits == 16;
     if (raw && (k->bits != 16 || v->bits != 16)) return invalid_attn("attention: bits 16 must be used on both sides");
@@ -1253,12 +1358,14 @@ int attention_check(const void* q, const float* out, const srftkv_side* k, const
     if ((reinterpret_cast<uintptr_t>(k->codes) | reinterpret_cast<uintptr_t>(v->codes) |
          reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15)
         return invalid_attn("attention: q, out and codes must be 16-byte aligned");
-    if ((long long)B * Hkv > (1ll << 31) - 1) return invalid_attn("attention: B * Hkv too large");
+    if ((long long)B * Hkv * head_groups(Hq / Hkv) > 65535)
+        return invalid_attn("attention: B * Hkv * ceil(Hq / Hkv / 4) must be at most 65535 (the grid's second dimension)");
+    if ((long long)B * Hq > (1ll << 31) - 1) return invalid_attn("attention: B * Hq too large");
     if (n_splits < 0) return invalid_attn("attention: n_splits must be >= 0");
     return SRFTKV_OK;
 }
 
-int attention_auto_splits(int B, int Hkv, int t_cap) { return auto_splits(B, Hkv, t_cap); }
+int attention_auto_splits(int B, int Hq, int Hkv, int t_cap) { return auto_splits(B, Hq, Hkv, t_cap); }
 
 int attention_entry(const void* q, float* out, const srftkv_side* k, const srftkv_side* v, int B, int Hq, int Hkv,
                     int d, int group, int t_cap, const int* seq_lens, float sm_scale, uint64_t seed, int n_splits,
@@ -1269,7 +1376,7 @@ int attention_entry(const void* q, float* out, const srftkv_side* k, const srftk
     const int rc0 = current_device_ok();
     if (rc0) return rc0;
     const bool raw = k->bits == 16;
-    const int ns = n_splits ? n_splits : auto_splits(B, Hkv, t_cap);
+    const int ns = n_splits ? n_splits : auto_splits(B, Hq, Hkv, t_cap);
     const WsLayout wl = ws_layout(B, Hq, d, ns);
     if (!workspace || workspace_bytes < wl.total || (reinterpret_cast<uintptr_t>(workspace) & 15)) {
         set_error("attention: workspace must be 16-byte aligned and hold %zu bytes (got %zu)", wl.total, workspace_bytes);
@@ -1293,6 +1400,9 @@ int attention_entry(const void* q, float* out, const srftkv_side* k, const srftk
     P.Hq = Hq;
     P.Hkv = Hkv;
     P.rep = Hq / Hkv;
+    P.n_hg = head_groups(P.rep);
+    P.hpg = heads_per_group(P.rep);
+    P.vscale = raw ? nullptr : static_cast<const uint8_t*>(v->scales);
     P.t_cap = t_cap;
     P.n_splits = ns;
     P.group = raw ? 16 : group;
@@ -1321,7 +1431,7 @@ int attention_entry(const void* q, float* out, const srftkv_side* k, const srftk
 
 size_t attention_workspace_size(int B, int Hq, int Hkv, int d, int t_cap, int n_splits) {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || t_cap <= 0 || n_splits < 0 || Hq % Hkv) return 0;
-    const int ns = n_splits ? n_splits : auto_splits(B, Hkv, t_cap);
+    const int ns = n_splits ? n_splits : auto_splits(B, Hq, Hkv, t_cap);
     return ws_layout(B, Hq, d, ns).total;
 }
 

@@ -50,7 +50,7 @@ extern "C" int q4kv_decode_attention_static(const void* q, float* out, const srf
     const size_t cap = (size_t)SRFTKV_STATIC_SCRATCH_BYTES;
     int ns = n_splits;
     if (ns == 0) {  // the automatic count, lowered until the workspace fits the array
-        ns = attention_auto_splits(B, Hkv, t_cap);
+        ns = attention_auto_splits(B, Hq, Hkv, t_cap);
         while (ns > 1 && attention_workspace_size(B, Hq, Hkv, d, t_cap, ns) > cap) --ns;
     }
     const size_t need = attention_workspace_size(B, Hq, Hkv, d, t_cap, ns);

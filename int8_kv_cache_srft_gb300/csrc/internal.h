@@ -95,7 +95,7 @@ size_t attention_workspace_size(int B, int Hq, int Hkv, int d, int t_cap, int n_
 int attention_check(const void* q, const float* out, const srftkv_side* k, const srftkv_side* v, int B, int Hq,
                     int Hkv, int d, int group, int t_cap, int n_splits);
 // The split count attention_entry picks for n_splits == 0 on the current device.
-int attention_auto_splits(int B, int Hkv, int t_cap);
+int attention_auto_splits(int B, int Hq, int Hkv, int t_cap);
 unsigned int attn_take_fault();
 
 }  // namespace srftkv

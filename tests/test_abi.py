@@ -115,7 +115,7 @@ def _attn(lib, k, v, B=2, Hq=8, Hkv=2, d=128, group=16, t_cap=64, ws=16, ws_byte
 
 
 @pytest.mark.parametrize("case", [
-    dict(d=32), dict(Hq=6, Hkv=4), dict(Hq=16, Hkv=2), dict(group=64), dict(t_cap=0), dict(q=0), dict(out=8),
+    dict(d=32), dict(Hq=6, Hkv=4), dict(B=70000, Hq=1, Hkv=1), dict(group=64), dict(t_cap=0), dict(q=0), dict(out=8),
 ])
 def test_attention_rejects_bad_arguments(lib, case):
     assert _attn(lib, _side(), _side(), **case) == K.SRFTKV_ERR_INVALID

@@ -148,3 +148,114 @@ def test_raw_fp16_cache_ignores_garbage_past_sequence_end():
     sv.codes[0, :, 37:] = float("inf")
     out = run_attention(q, sk, sv, B, Hkv * rep, Hkv, d, 16, t_cap, seq, seed)
     assert np.isfinite(out).all() and np.abs(out - ref).max() <= ATTN_ATOL
+
+
+@pytest.mark.parametrize("rep", (5, 6, 8, 16))
+@pytest.mark.parametrize("bk,bv", ((4, 4), (8, 4), (16, 16)))
+@pytest.mark.parametrize("n_splits", (0, 3))
+def test_attention_gqa_head_groups(rep, bk, bv, n_splits):
+    """GQA ratios above four run as head groups of at most four query heads (5 -> 3 + 2, 6 -> 3 + 3, 8 -> 4 + 4,
+    16 -> 4 x 4): every query head against the oracle, ragged sequence lengths."""
+    B, Hkv, d, t_cap, seed = 2, 2, 128, 700, 12
+    Hq = Hkv * rep
+    sk, sv = build_cache(B, Hkv, d, t_cap, bk, bv, 16, seed, lam=(bk != 16), data_seed=rep * 7 + bk)
+    q = I.query(I.Workload("q", n_outer=B, tokens=1, kv_heads=Hkv, d=d, q_heads=Hq, data_seed=rep + 90), device="cuda")
+    seq = torch.tensor([700, 333], dtype=torch.int32, device="cuda")
+    out = run_attention(q, sk, sv, B, Hq, Hkv, d, 16, t_cap, seq, seed, n_splits=n_splits)
+    ref = oracle_attention(q, sk, sv, 16, seed, seq)
+    assert np.abs(out - ref).max() <= ATTN_ATOL
+
+
+@pytest.mark.parametrize("d", (64, 96, 192, 256))
+def test_attention_gqa8_other_head_dims(d):
+    B, Hkv, rep, t_cap, seed = 2, 1, 8, 320, 13
+    Hq = Hkv * rep
+    sk, sv = build_cache(B, Hkv, d, t_cap, 4, 4, 16, seed, data_seed=d + 3)
+    q = I.query(I.Workload("q", n_outer=B, tokens=1, kv_heads=Hkv, d=d, q_heads=Hq, data_seed=d + 4), device="cuda")
+    seq = torch.tensor([320, 45], dtype=torch.int32, device="cuda")
+    out = run_attention(q, sk, sv, B, Hq, Hkv, d, 16, t_cap, seq, seed)
+    ref = oracle_attention(q, sk, sv, 16, seed, seq)
+    assert np.abs(out - ref).max() <= ATTN_ATOL
+
+
+def _quantize(x, bits, group, seed, lam=None, scale_format="fp32"):
+    B, T, H, d = x.shape
+    s = K.alloc_side(B, T, H, d, bits, group, scale_format=scale_format)
+    s.x, s.lam = x, lam
+    K.srft_kv_quantize(s, None, B, T, H, d, group, T, 0, seed)
+    torch.cuda.synchronize()
+    return s
+
+
+@pytest.mark.parametrize("k", (10, 14, -20))
+@pytest.mark.parametrize("bits_v,fmt", ((4, "fp32"), (8, "fp32"), (4, "e8m0")))
+def test_value_scales_far_from_one(k, bits_v, fmt):
+    """V scales far outside [2^-13, 2^7): a per-channel lambda_V = 2^k multiplies every rotated V coordinate
+    (k = 10 gives |z_V| near 5000 and 4-bit scales near 700, past the 255 at which p * scale_V would overflow
+    fp16; k = -20 gives scales near 1e-6).  The codes are those of lambda = 1 and the scales 2^k times larger
+    (an exact power-of-two scaling), and attention divides by lambda_V, so the output must be that of the
+    lambda = 1 cache, and within the tolerance of the oracle on the same cache."""
+    B, Hkv, rep, d, T, seed = 2, 2, 4, 128, 600, 17
+    Hq = Hkv * rep
+    w = I.Workload("vrange", n_outer=B, tokens=T, kv_heads=Hkv, d=d, data_seed=41)
+    xk, xv = I.kv_side(w, "k", device="cuda"), I.kv_side(w, "v", device="cuda")
+    sk = _quantize(xk, 4, 16, seed)
+    sv1 = _quantize(xv, bits_v, 16, seed, scale_format=fmt)
+    lam = torch.full((1, Hkv, d), 2.0**k, dtype=torch.float32, device="cuda")
+    svk = _quantize(xv, bits_v, 16, seed, lam=lam, scale_format=fmt)
+    assert torch.equal(svk.codes, sv1.codes)
+    if fmt == "fp32":
+        assert torch.equal(svk.scales, sv1.scales * 2.0**k)
+    q = I.query(I.Workload("q", n_outer=B, tokens=1, kv_heads=Hkv, d=d, q_heads=Hq, data_seed=42), device="cuda")
+    seq = torch.tensor([600, 211], dtype=torch.int32, device="cuda")
+    o1 = run_attention(q, sk, sv1, B, Hq, Hkv, d, 16, T, seq, seed)
+    ok = run_attention(q, sk, svk, B, Hq, Hkv, d, 16, T, seq, seed)
+    assert np.isfinite(ok).all()
+    assert np.abs(ok - o1).max() <= 1e-5 * max(1.0, float(np.abs(o1).max()))
+    if fmt == "fp32":
+        ref = oracle_attention(q, sk, svk, 16, seed, seq)
+        assert np.abs(ok - ref).max() <= ATTN_ATOL
+
+
+def test_value_magnitudes_scaled_by_1024():
+    """V inputs times 2^10 (fp16 holds them exactly, |v| up to about 5000): codes unchanged, scales 2^10 times
+    larger (near 700, past the old fp16 limit of 255), outputs 2^10 times the unscaled ones; against the oracle
+    the 2e-3 rule is applied to the output divided by 2^10."""
+    B, Hkv, rep, d, T, seed = 2, 2, 4, 128, 600, 18
+    Hq = Hkv * rep
+    w = I.Workload("vbig", n_outer=B, tokens=T, kv_heads=Hkv, d=d, data_seed=43)
+    xk, xv = I.kv_side(w, "k", device="cuda"), I.kv_side(w, "v", device="cuda")
+    sk = _quantize(xk, 4, 16, seed)
+    sv1 = _quantize(xv, 4, 16, seed)
+    svb = _quantize(xv * 1024.0, 4, 16, seed)
+    assert torch.equal(svb.codes, sv1.codes) and torch.equal(svb.scales, sv1.scales * 1024.0)
+    assert float(svb.scales.max()) > 255.0
+    q = I.query(I.Workload("q", n_outer=B, tokens=1, kv_heads=Hkv, d=d, q_heads=Hq, data_seed=44), device="cuda")
+    o1 = run_attention(q, sk, sv1, B, Hq, Hkv, d, 16, T, None, seed)
+    ob = run_attention(q, sk, svb, B, Hq, Hkv, d, 16, T, None, seed)
+    assert np.isfinite(ob).all()
+    assert np.abs(ob / 1024.0 - o1).max() <= 1e-5 * max(1.0, float(np.abs(o1).max()))
+    ref = oracle_attention(q, sk, svb, 16, seed, None)
+    assert np.abs(ob - ref).max() / 1024.0 <= ATTN_ATOL
+
+
+def test_value_scales_spanning_many_binades_across_chunks():
+    """One cache whose V rows alternate, 64 tokens at a time, between magnitudes 2^13 and 2^-12 (fp16 inputs,
+    a range of 2^25 in the scales): the V unit moves up and down between chunks.  Keys make the large rows'
+    scores very low, so the small rows carry the output; checked against the oracle relative to the output's
+    size."""
+    B, Hkv, d, T, seed = 1, 1, 128, 512, 19
+    w = I.Workload("vspan", n_outer=B, tokens=T, kv_heads=Hkv, d=d, data_seed=45)
+    xk, xv = I.kv_side(w, "k", device="cuda"), I.kv_side(w, "v", device="cuda")
+    q = I.query(I.Workload("q", n_outer=B, tokens=1, kv_heads=Hkv, d=d, q_heads=1, data_seed=46), device="cuda")
+    big = ((torch.arange(T, device="cuda") // 64) % 2 == 0)
+    xv = torch.where(big[None, :, None, None], xv.float() * 2.0**13, xv.float() * 2.0**-12).half()
+    qk = q.float()[:, None, :, :].expand(B, T, Hkv, d)
+    xk = torch.where(big[None, :, None, None], -3.0 * qk, xk.float()).half()
+    sk = _quantize(xk, 8, 16, seed)
+    sv = _quantize(xv, 4, 16, seed)
+    for n_splits in (1, 0):
+        out = run_attention(q, sk, sv, B, 1, Hkv, d, 16, T, None, seed, n_splits=n_splits)
+        ref = oracle_attention(q, sk, sv, 16, seed, None)
+        assert np.isfinite(out).all()
+        assert np.abs(out - ref).max() <= 1e-4 * float(np.abs(ref).max())
