@@ -25,8 +25,9 @@ attention: B=4, T=32768, a 201 MB packed cache) so that ncu captures stay
 small; it prints one JSON line with the median event time per launch.
 --kernel gemma_quantize|gemma_dequantize does the same for the d = 256 codec
 on the full Gemma-3-1B-shaped cache (0.21 M vectors, 150 MB), and
---kernel d192_quantize|d192_dequantize for the d = 192 codec on the decode
-cache shape at d = 192 cut to B=2 (4.2 M vectors, about 2.2 GB held).
+--kernel d192_quantize|d192_dequantize (and d256_...) for the d = 192 (256)
+codec on the decode cache shape at that d cut to B=2 (4.2 M vectors, about
+2.2 GB (2.9 GB) held).
 """
 
 from __future__ import annotations
@@ -63,7 +64,7 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--kernel", default=None,
                     choices=("quantize", "dequantize", "attention", "gemma_quantize", "gemma_dequantize",
-                             "d192_quantize", "d192_dequantize"),
+                             "d192_quantize", "d192_dequantize", "d256_quantize", "d256_dequantize"),
                     help="profiling case: launch only this kernel on a small workload")
     return ap.parse_args()
 
@@ -738,6 +739,8 @@ def run_case(args):
         w = I.GEMMA
     elif args.kernel.startswith("d192_"):
         w = I.DECODE.resized(n_outer=2, d=192)
+    elif args.kernel.startswith("d256_"):
+        w = I.DECODE.resized(n_outer=2, d=256)
     else:
         w = I.DECODE.resized(n_outer=4, tokens=32768) if attn else I.DECODE.resized(n_outer=2)
     B, Hkv, d, T, Hq, G, seed = w.n_outer, w.kv_heads, w.d, w.tokens, w.q_heads, w.group, w.sign_seed

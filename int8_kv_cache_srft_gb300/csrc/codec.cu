@@ -142,6 +142,10 @@ static int quant_path_override() {
 }
 constexpr long long kWarpPathMaxRows = 4096;
 constexpr long long kTensorCorePathMinRows = 3ll << 16;
+// d = 192 / 256: building R_s in every CTA costs more (N x d entries); the
+// Gemma-shaped cache (0.21 M vectors of d = 256) still quantizes faster on the
+// two-lane register path (measured 0.075 against 0.080 ms)
+constexpr long long kWideTensorCorePathMinRows = 1ll << 19;
 
 // A call whose two sides use different transforms or scale formats runs as
 // two one-sided calls (the tensor-core kernels hold one transform matrix per
@@ -178,6 +182,9 @@ int codec_quantize(const CodecCall& c) {
     if (c.d == 96) return tc_only(c, codec_quantize_tc, "quantize");
     const int ov = quant_path_override();
     const long long rows = (long long)c.n_sides * c.n_outer * c.n_tokens * c.H;
+    if ((c.d == 192 || c.d == 256) && c.group <= 32 &&  // a group must fit in one epilogue thread's 32 columns
+        (ov == 2 || (ov == 0 && rows >= kWideTensorCorePathMinRows)))
+        return c.d == 192 ? codec_quantize_tc_wide192(c) : codec_quantize_tc_wide256(c);
     if (ov == 2 || (ov == 0 && rows >= kTensorCorePathMinRows)) {
         const int rc = codec_quantize_tc(c);
         if (rc != 1) return rc;

@@ -127,10 +127,15 @@ __device__ __forceinline__ void group_scale(float A, float& sc, uint32_t& raw, f
     }
 }
 
-template <int D, int BITS, int SF>
+// ZLOG2: z holds the coordinates times 2^ZLOG2 (a contraction whose operand
+// was scaled by a power of two); the scales stored are those of the true
+// coordinates, the codes are unchanged.
+template <int D, int BITS, int SF, int ZLOG2 = 0>
 __device__ __forceinline__ void quant_store_row(float (&z)[D], int group, uint8_t* __restrict__ crow,
                                                 uint8_t* __restrict__ srow) {
     constexpr int sfmt = SF;
+    static_assert(ZLOG2 >= 0 && ZLOG2 < 30, "z unit");
+    constexpr float ZUNIT = 1.f / (float)(1 << ZLOG2);
     constexpr int U = D / 16;
     constexpr float Q = (BITS == 4) ? 7.f : 127.f;
     constexpr float MAG = kMagic + ((BITS == 4) ? 8.f : 128.f);
@@ -153,9 +158,11 @@ __device__ __forceinline__ void quant_store_row(float (&z)[D], int group, uint8_
     uint32_t raw[U];  // fp16 bits or the e8m0 byte of the stored scale
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        const float A = m[u];
+        float A = m[u];
+        if constexpr (ZLOG2 != 0) A *= ZUNIT;  // the true group absmax (exact: a power of two)
         float inv;
         group_scale<BITS, SF>(A, sc[u], raw[u], inv);
+        if constexpr (ZLOG2 != 0) inv *= ZUNIT;  // z / scale for z in units of 2^-ZLOG2
 #pragma unroll
         for (int i = 0; i < 16; ++i) z[16 * u + i] = fmaf_(z[16 * u + i], inv, MAG);
         if constexpr (sfmt == SRFTKV_SCALE_FP16) {

@@ -83,6 +83,9 @@ bool encode_tiled_swz(CUtensorMap* map, CUtensorMapDataType dt, int rank, void* 
 // Tensor-core quantize path (d = 128, group <= 64); returns 1 when the call
 // is not one it handles, else SRFTKV_OK or an error code.
 int codec_quantize_tc(const CodecCall& c);
+// Tensor-core quantize at d = 192 and d = 256 (codec_tc_wide.cuh; groups of at most 32).
+int codec_quantize_tc_wide192(const CodecCall& c);
+int codec_quantize_tc_wide256(const CodecCall& c);
 // One warp per vector (d = 128, groups of at most 32): returns 1 when the call does not fit it.
 int codec_quantize_warp(const CodecCall& c);
 int codec_dequantize_tc(const CodecCall& c);
