@@ -201,6 +201,10 @@ int codec_dequantize(const CodecCall& c) {
     if (c.d == 96) return tc_only(c, codec_dequantize_tc, "dequantize");
     const int ov = quant_path_override();
     const long long rows = (long long)c.n_sides * c.n_outer * c.n_tokens * c.H;
+    if ((c.d == 192 || c.d == 256) && (ov == 2 || (ov == 0 && rows >= kWideTensorCorePathMinRows))) {
+        const int rc = c.d == 192 ? codec_dequantize_tc_wide192(c) : codec_dequantize_tc_wide256(c);
+        if (rc != 1) return rc;  // 1: a call the tensor-core kernel does not take (lambda, groups > 32, scale rows)
+    }
     if (ov == 2 || (ov == 0 && rows >= kTensorCorePathMinRows)) {
         const int rc = codec_dequantize_tc(c);
         if (rc != 1) return rc;

@@ -31,6 +31,7 @@
 namespace srftkv {
 
 struct CodecSideK {
+    void* x;             // fp16 rows [n_outer][n_tokens][H][d] (written directly only by the wide tensor-core dequantize)
     uint8_t* codes;
     uint8_t* scales;     // element type per sfmt
     const float* lambda;
@@ -494,6 +495,7 @@ __global__ void __launch_bounds__(128, Geo<D>::MIN_BLOCKS)
 static inline void fill_params(const CodecCall& c, CodecParams& P) {
     for (int s = 0; s < 2; ++s) {
         const CodecSideDesc& d = c.side[s < c.n_sides ? s : 0];
+        P.side[s].x = d.x;
         P.side[s].codes = d.codes;
         P.side[s].scales = static_cast<uint8_t*>(d.scales);
         P.side[s].sfmt = d.scale_format;

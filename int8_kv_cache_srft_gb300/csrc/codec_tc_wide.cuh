@@ -37,6 +37,7 @@
 #pragma once
 
 #include "codec_impl.cuh"
+#include "codec_tc_common.cuh"
 #include "tcgen05.cuh"
 
 namespace srftkv {
@@ -314,6 +315,430 @@ static int launch_tc_wide(const CodecCall& c) {
         return SRFTKV_ERR_CUDA;
     }
     return SRFTKV_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Dequantize at d = 192 and 256: X_hat = s (R^T P_hat), P_hat = codes * scale
+// ---------------------------------------------------------------------------
+// The d = 128 design (codec_tc.cu) widened:
+//   warp 0      owns tensor memory and issues the MMAs (one thread): per tile
+//               two contractions of N = d/2 output coordinates each, into two
+//               accumulators, so the epilogue drains one half while the
+//               other is computed;
+//   warp 1      TMA producer: each tile's code rows and scale rows into a ring
+//               of input stages.  A code row is copied as segments of 128, 64
+//               or 32 bytes (96 = 64 + 32, 192 = 128 + 64, 256 = 128 + 128),
+//               each with the TMA swizzle equal to its width, which keeps the
+//               row-per-thread reads free of bank conflicts;
+//   warps 2-9   converters: thread = half a row; codes * scale as exact fp16
+//               pairs (the K order of dq_kperm), written into tensor memory
+//               as the MMA's A operand, in pieces of 8 or 4 code words;
+//   warps 10-17 epilogue: tensor memory -> fp16 -> global, each thread
+//               storing its row's half (d bytes) straight from registers (no
+//               staging buffer: the shared memory goes to R_s, 72 or 128 KB).
+// B = diag(s) R in fp16 (P_hat and the output are fp16).  A side with lambda
+// takes the register path (there is no room for the fp32 copy of R_s that
+// the d = 128 kernel rebuilds B from).
+namespace wide {
+constexpr int DQ_CONV = 8, DQ_EPI = 8, DQ_WARPS = 2 + DQ_CONV + DQ_EPI;
+constexpr int DQ_NA = 2;          // A buffers in tensor memory
+constexpr uint32_t DQ_A_COL = 256, DQ_A_STRIDE = 128;  // accumulator halves at columns 0 and 128
+
+// Segments of a code row of rb bytes: powers of two of at most 128 bytes, largest first.
+__host__ __device__ constexpr int seg_width(int rb, int s) {
+    return rb == 96 ? (s == 0 ? 64 : 32) : rb == 128 ? 128 : rb == 192 ? (s == 0 ? 128 : 64) : 128;
+}
+__host__ __device__ constexpr int seg_count(int rb) { return rb == 128 ? 1 : 2; }
+__host__ __device__ constexpr int seg_off(int rb, int s) { return s == 0 ? 0 : seg_width(rb, 0); }
+
+template <int DV, int BK, int BV>
+struct DqCfg {
+    static constexpr int RBMAX = DV * (BK > BV ? BK : BV) / 8;   // code bytes a row
+    static constexpr int OFF_SC = M * RBMAX;                       // 1024-aligned
+    static constexpr int STAGE = (OFF_SC + M * (DV / 4) + 1023) / 1024 * 1024;  // scale rows of at most d/4 bytes
+    static constexpr int B_BYTES = DV * DV * 2;                    // R_s in fp16, k-blocks of DV rows
+    static constexpr int OFF_IN = B_BYTES;
+    static constexpr int STAGES = (SMEM_CAP - 1024 - 256 - OFF_IN) / STAGE > 4 ? 4 : (SMEM_CAP - 1024 - 256 - OFF_IN) / STAGE;
+    static constexpr int OFF_BAR = OFF_IN + STAGES * STAGE;
+    static constexpr int SMEM = OFF_BAR + 256 + 1024;
+    static_assert(STAGES >= 2, "input stages");
+    static_assert(SMEM <= SMEM_CAP, "shared memory");
+};
+
+// Byte offset, in an input stage, of 16-byte chunk c of code row m (rows of rb bytes in swizzled segments)
+__device__ __forceinline__ uint32_t code_chunk(int rb, int m, int c) {
+    const int p = 16 * c;
+    const int s = p >= seg_width(rb, 0) ? 1 : 0;
+    const int w = seg_width(rb, s), cc = (p - seg_off(rb, s)) >> 4;
+    return (uint32_t)(M * seg_off(rb, s) + m * w + (swz16(w, m, cc) << 4));
+}
+
+// Scale of 16-coordinate unit u of tile row m: fp32 planes of d = 256 as swizzled rows (64 bytes for
+// group 16, 32 for group 32), every other plane as its contiguous bytes (rows of ng * sb bytes)
+template <int DV>
+__device__ __forceinline__ float unit_scale(const uint8_t* __restrict__ in, int m, int u, int group, int sfmt) {
+    const int gi = (16 * u) / group, ng = DV / group;
+    if (sfmt == SRFTKV_SCALE_FP32) {
+        if constexpr (DV == 256) {
+            const int srb = 4 * ng, b = 4 * gi;
+            return *reinterpret_cast<const float*>(in + m * srb + (swz16(srb, m, b >> 4) << 4) + (b & 15));
+        } else {
+            return *reinterpret_cast<const float*>(in + (m * ng + gi) * 4);
+        }
+    }
+    if (sfmt == SRFTKV_SCALE_FP16)
+        return __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(in + (m * ng + gi) * 2)));
+    return __uint_as_float((uint32_t)in[m * ng + gi] << 23);  // e8m0: the byte is the fp32 exponent field
+}
+
+// fp16 pairs of NW consecutive 8-coordinate code words starting at word w0 of tile row m: codes * scale
+// with the scale split into fp16 hi + lo (one main rounding), in the K order of dq_kperm
+template <int DV, int BITS, int NW>
+__device__ __forceinline__ void word_pairs(const uint8_t* __restrict__ in, int off_sc, int m, int w0, int group,
+                                           int sfmt, uint32_t (&hp)[4 * NW]) {
+    constexpr int RB = DV * BITS / 8;
+    constexpr int NCH = NW * BITS / 16;  // 16-byte chunks of the NW words (8 coordinates = BITS bytes)
+    uint32_t w[4 * NCH];
+    const int c0 = w0 * BITS / 16;
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) {
+        const uint4 v = *reinterpret_cast<const uint4*>(in + code_chunk(RB, m, c0 + k));
+        w[4 * k] = v.x;
+        w[4 * k + 1] = v.y;
+        w[4 * k + 2] = v.z;
+        w[4 * k + 3] = v.w;
+    }
+#pragma unroll
+    for (int u = 0; u < NW / 2; ++u) {  // unit u: words 2u, 2u+1 (16 coordinates)
+        const float sc = unit_scale<DV>(in + off_sc, m, w0 / 2 + u, group, sfmt);
+        const __half h = __float2half_rn(sc);
+        const uint32_t sh = half2_bcast(h), sl = half2_bcast(__float2half_rn(sc - __half2float(h)));
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int k = 2 * u + e;
+            uint32_t c[4];
+            if constexpr (BITS == 4) {
+                const uint32_t x = w[k], xs = x >> 8;
+                c[0] = codes_lo4(x);
+                c[1] = codes_hi4(x);
+                c[2] = codes_lo4(xs);
+                c[3] = codes_hi4(xs);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)  // bytes j of the two words: coordinates 8k + j and 8k + j + 4
+                    c[j] = codes_b8(__byte_perm(w[2 * k], w[2 * k + 1], j | (j << 4) | ((4 + j) << 8) | ((4 + j) << 12)));
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) hp[4 * k + j] = h2fma(c[j], sh, h2mul(c[j], sl));
+        }
+    }
+}
+}  // namespace wide
+
+struct WideDqMaps {
+    CUtensorMap codes[2][2];  // [side][segment]
+    CUtensorMap scales[2];
+};
+
+template <int BK, int BV, int DV>
+__global__ void __launch_bounds__(wide::DQ_WARPS * 32, 1)
+    srft_dequantize_tc_wide_kernel(const __grid_constant__ WideDqMaps Mp, const __grid_constant__ CodecParams P) {
+    using C = wide::DqCfg<DV, BK, BV>;
+    constexpr int M = wide::M, NH = DV / 2;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sbase = ptx::smem_u32(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    auto bar = [&](int i) { return ptx::smem_u32(&bars[i]); };
+    constexpr int IN_FULL = 0, IN_EMPTY = C::STAGES, A_FULL = 2 * C::STAGES, A_EMPTY = A_FULL + wide::DQ_NA,
+                  ACC_FULL = A_EMPTY + wide::DQ_NA, ACC_EMPTY = ACC_FULL + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[ACC_EMPTY + 2]);
+
+    {  // B[k][q] = s_k R[n][k] with n = dq_kperm(q), fp16, in the MMA operand layout (k-blocks of DV rows)
+        float* cs = reinterpret_cast<float*>(smem + C::OFF_IN);  // cos / sin (2 pi m/d) in the (unused) input stages
+        float* sn = cs + DV;
+        for (int m = threadIdx.x; m < DV; m += blockDim.x) {
+            double sv, cv;
+            sincospi(2.0 * m / DV, &sv, &cv);
+            cs[m] = (float)cv;
+            sn[m] = (float)sv;
+        }
+        __syncthreads();
+        const bool srht = P.side[0].transform == SRFTKV_TRANSFORM_SRHT;
+        const float isd = (float)(1.0 / sqrt((double)DV)), r2 = (float)sqrt(2.0 / DV);
+        for (int idx = threadIdx.x; idx < DV * DV; idx += blockDim.x) {
+            const int k = idx / DV, q = idx - k * DV, n = dq_kperm(q);  // B row k (output), K position q
+            float v;
+            if (srht) v = (__popc(n & k) & 1) ? -isd : isd;
+            else if (n == 0) v = isd;
+            else if (n == 1) v = (k & 1) ? -isd : isd;
+            else {
+                const int mm = ((n >> 1) * k) % DV;
+                v = (n & 1) ? -r2 * sn[mm] : r2 * cs[mm];
+            }
+            if (P.sign_mask[k >> 1] & ((k & 1) ? 0x80000000u : 0x8000u)) v = -v;
+            *reinterpret_cast<__half*>(smem + wide::kb_offset<DV>(k, q)) = __float2half_rn(v);
+        }
+        ptx::fence_proxy_async_smem();
+    }
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < C::STAGES; ++st) {
+            ptx::mbar_init(bar(IN_FULL + st), 1);
+            ptx::mbar_init(bar(IN_EMPTY + st), wide::DQ_CONV);
+        }
+        for (int b = 0; b < wide::DQ_NA; ++b) {
+            ptx::mbar_init(bar(A_FULL + b), wide::DQ_CONV);
+            ptx::mbar_init(bar(A_EMPTY + b), 1);
+        }
+        for (int h = 0; h < 2; ++h) {
+            ptx::mbar_init(bar(ACC_FULL + h), 1);
+            ptx::mbar_init(bar(ACC_EMPTY + h), wide::DQ_EPI / 2);
+        }
+        ptx::fence_barrier_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(ptx::smem_u32(tmem_slot), 512);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const int count = (P.total_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+    bool failed = false;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            constexpr uint32_t IDESC = tc::idesc_f16_f32(M, NH);
+            for (int i = 0; i < count && !failed; ++i) {
+                const int b = i % wide::DQ_NA;
+                if (!ptx::mbar_wait_bounded(bar(A_FULL + b), (i / wide::DQ_NA) & 1)) {
+                    failed = true;
+                    break;
+                }
+                const uint32_t a_tmem = tmem + wide::DQ_A_COL + b * wide::DQ_A_STRIDE;
+#pragma unroll 1
+                for (int hf = 0; hf < 2; ++hf) {
+                    if (i > 0 && !ptx::mbar_wait_bounded(bar(ACC_EMPTY + hf), (i - 1) & 1)) {
+                        failed = true;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                    const uint32_t d_tmem = tmem + hf * 128;
+#pragma unroll
+                    for (int ks = 0; ks < DV / 16; ++ks) {
+                        const uint32_t boff = (ks >> 2) * (DV * 128) + hf * NH * 128 + (ks & 3) * 32;
+                        tc::mma_f16_ta(d_tmem, a_tmem + 8 * ks, tc::sw128_desc(sbase + boff), IDESC, ks > 0);
+                    }
+                    tc::commit(bar(ACC_FULL + hf));  // output half hf of this tile is ready
+                }
+                if (failed) break;
+                tc::commit(bar(A_EMPTY + b));  // A buffer b may be rewritten once these MMAs are done
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            for (int i = 0; i < count; ++i) {
+                const int t = blockIdx.x + i * gridDim.x;
+                const int st = i % C::STAGES, use = i / C::STAGES;
+                if (use > 0 && !ptx::mbar_wait_bounded(bar(IN_EMPTY + st), (use - 1) & 1)) {
+                    failed = true;
+                    break;
+                }
+                const TileId id = decode_tile<M>(P, t);
+                const int bits = (BK == BV || id.side == 0) ? BK : BV, rb = DV * bits / 8;
+                const uint32_t dst = sbase + C::OFF_IN + st * C::STAGE;
+                const int row = P.t_offset + id.t0;  // packed planes: [outer*H][t_cap] rows
+                const int oh = id.o * P.H + id.h;
+                const int sb = P.side[id.side].sbytes, ng = DV / P.group;
+                // fp32 scale rows of d = 256 through the tensor map (swizzled rows); every other plane as the
+                // tile's contiguous bytes by a plain bulk copy that stops at the end of this (outer, head)
+                const bool flat = !(sb == 4 && DV == 256);
+                const uint32_t sc_bytes = flat ? (uint32_t)(min(M, P.t_cap - row) * ng * sb) : (uint32_t)(M * ng * sb);
+                ptx::mbar_arrive_expect_tx(bar(IN_FULL + st), M * rb + sc_bytes);
+                for (int sg = 0; sg < wide::seg_count(rb); ++sg)
+                    ptx::tma_load_3d(dst + M * wide::seg_off(rb, sg), &Mp.codes[id.side][sg], bar(IN_FULL + st),
+                                     wide::seg_off(rb, sg), row, oh);
+                if (flat)
+                    ptx::bulk_load(dst + C::OFF_SC, P.side[id.side].scales + ((long long)oh * P.t_cap + row) * ng * sb,
+                                   sc_bytes, bar(IN_FULL + st));
+                else
+                    ptx::tma_load_3d(dst + C::OFF_SC, &Mp.scales[id.side], bar(IN_FULL + st), 0, row, oh);
+            }
+        }
+    } else if (warp < 2 + wide::DQ_CONV) {
+        // converter warp w: tile rows = tensor-memory lanes 32(w%4)..+31, row half (w-2)/4
+        const int quarter = warp & 3, m = 32 * quarter + lane, hf = (warp - 2) >> 2;
+        const uint32_t lanes = tmem + ((uint32_t)(32 * quarter) << 16);
+        for (int i = 0; i < count; ++i) {
+            const int t = blockIdx.x + i * gridDim.x;
+            const int b = i % wide::DQ_NA, st = i % C::STAGES;
+            const TileId id = decode_tile<M>(P, t);
+            const CodecSideK& S = P.side[id.side];
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait_bounded(bar(IN_FULL + st), (i / C::STAGES) & 1))) {
+                failed = true;
+                break;
+            }
+            const uint8_t* in = smem + C::OFF_IN + st * C::STAGE;
+            if (!__all_sync(0xffffffffu,
+                            i < wide::DQ_NA || ptx::mbar_wait_bounded(bar(A_EMPTY + b), (i / wide::DQ_NA - 1) & 1))) {
+                failed = true;
+                break;
+            }
+            tc::fence_after_sync();  // the MMAs that read A buffer b are complete
+            const uint32_t acol = lanes + wide::DQ_A_COL + b * wide::DQ_A_STRIDE;
+            const bool side_k = BK == BV || id.side == 0;
+            // half hf = code words hf*DV/16 .. +DV/16-1 = A columns hf*DV/4 .. +DV/4-1 (column c holds word c/4),
+            // written in pieces of 8 words (32 columns) and, at d = 192, one of 4 words (16 columns), each at a
+            // column offset that is a multiple of its width
+            auto piece = [&](auto nwc, int w0) {
+                constexpr int NW = decltype(nwc)::value;
+                uint32_t hp[4 * NW];
+                if (side_k) wide::word_pairs<DV, BK, NW>(in, C::OFF_SC, m, w0, P.group, S.sfmt, hp);
+                else wide::word_pairs<DV, BV, NW>(in, C::OFF_SC, m, w0, P.group, S.sfmt, hp);
+                if constexpr (NW == 8) tc::st_32x32b_x32(acol + 4 * w0, hp);
+                else tc::st_32x32b_x16(acol + 4 * w0, hp);
+            };
+            using W8 = std::integral_constant<int, 8>;
+            using W4 = std::integral_constant<int, 4>;
+            if constexpr (DV == 256) {
+                piece(W8{}, 16 * hf);
+                piece(W8{}, 16 * hf + 8);
+            } else if (hf == 0) {  // words 0-7 (columns 0-31), 8-11 (32-47)
+                piece(W8{}, 0);
+                piece(W4{}, 8);
+            } else {               // words 12-15 (columns 48-63), 16-23 (64-95)
+                piece(W4{}, 12);
+                piece(W8{}, 16);
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(IN_EMPTY + st));  // input stage consumed
+            tc::wait_st();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(A_FULL + b));
+        }
+    } else {
+        // epilogue warp w: tensor-memory lanes 32(w%4)..+31 = tile rows, output half (w-10)/4
+        const int quarter = warp & 3, hf = (warp - 2 - wide::DQ_CONV) >> 2;
+        const uint32_t lanes = tmem + ((uint32_t)(32 * quarter) << 16) + hf * 128;
+        for (int i = 0; i < count; ++i) {
+            const int t = blockIdx.x + i * gridDim.x;
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait_bounded(bar(ACC_FULL + hf), i & 1))) {
+                failed = true;
+                break;
+            }
+            tc::fence_after_sync();
+            const TileId id = decode_tile<M>(P, t);
+            const int t_tok = id.t0 + 32 * quarter + lane;
+            const bool live = t_tok < P.n_tokens;
+            uint4* dst = reinterpret_cast<uint4*>(
+                reinterpret_cast<__half*>(P.side[id.side].x) +
+                ((((long long)id.o * P.n_tokens + t_tok) * P.H + id.h) * DV + hf * NH));
+#pragma unroll 1
+            for (int j = 0; j < NH / 32; ++j) {
+                uint32_t v[32];
+                tc::ld_32x32b_x32(lanes + 32 * j, v);
+                tc::wait_ld(v);
+                if (live) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        dst[4 * j + q] = make_uint4(pack_half2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                                                    pack_half2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                                                    pack_half2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                                                    pack_half2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+                }
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(ACC_EMPTY + hf));  // accumulator half hf may be overwritten
+        }
+    }
+    if (failed) atomicOr(P.fault, 1u);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (warp == 0) tc::tmem_dealloc(tmem, 512);
+}
+
+template <int BK, int BV, int DV>
+static int launch_dq_tc_wide(const CodecCall& c) {
+    using C = wide::DqCfg<DV, BK, BV>;
+    CodecParams P;
+    fill_params(c, P);
+    P.tiles_per_head = (c.n_tokens + wide::M - 1) / wide::M;
+    P.tiles_per_side = c.n_outer * c.H * P.tiles_per_head;
+    P.total_tiles = c.n_sides * P.tiles_per_side;
+    P.fault = codec_fault_word();
+    if (!P.fault) return SRFTKV_ERR_CUDA;
+    WideDqMaps Mp;
+    const unsigned long long tcap = (unsigned long long)c.t_cap, nrow = (unsigned long long)c.n_outer * c.H;
+    const int ng = DV / c.group;
+    auto swz = [](int bytes) {
+        return bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+               : bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+               : bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                             : CU_TENSOR_MAP_SWIZZLE_NONE;
+    };
+    for (int s = 0; s < 2; ++s) {
+        const CodecSideDesc& d = c.side[s < c.n_sides ? s : 0];
+        const int rb = DV * d.bits / 8;
+        // code plane [n_outer*H][t_cap][rb] as segments of the row, each with its own swizzle
+        for (int sg = 0; sg < 2; ++sg) {
+            const int g = sg < wide::seg_count(rb) ? sg : 0;
+            const unsigned long long cdims[3] = {(unsigned long long)rb, tcap, nrow};
+            const unsigned long long cstr[2] = {(unsigned long long)rb, tcap * rb};
+            const unsigned cbox[3] = {(unsigned)wide::seg_width(rb, g), (unsigned)wide::M, 1u};
+            if (!encode_tiled_swz(&Mp.codes[s][sg], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, d.codes, cdims, cstr, cbox,
+                                  swz(wide::seg_width(rb, g)), "wide tensor-core dequantize codes"))
+                return SRFTKV_ERR_CUDA;
+        }
+        if (d.scale_format != SRFTKV_SCALE_FP32 || DV != 256) {
+            Mp.scales[s] = Mp.codes[s][0];  // read by plain bulk copies (no tensor map)
+        } else {
+            const unsigned long long sdims[3] = {(unsigned long long)ng, tcap, nrow};
+            const unsigned long long sstr[2] = {ng * 4ull, tcap * ng * 4ull};
+            const unsigned sbox[3] = {(unsigned)ng, (unsigned)wide::M, 1u};
+            if (!encode_tiled_swz(&Mp.scales[s], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, d.scales, sdims, sstr, sbox,
+                                  swz(4 * ng), "wide tensor-core dequantize scales"))
+                return SRFTKV_ERR_CUDA;
+        }
+    }
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(srft_dequantize_tc_wide_kernel<BK, BV, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM);
+        attr = true;
+    }
+    int blocks = device_sm_count();
+    if (blocks > P.total_tiles) blocks = P.total_tiles;
+    srft_dequantize_tc_wide_kernel<BK, BV, DV><<<blocks, wide::DQ_WARPS * 32, C::SMEM, c.stream>>>(Mp, P);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("wide tensor-core dequantize launch failed: %s", cudaGetErrorString(e));
+        return SRFTKV_ERR_CUDA;
+    }
+    return SRFTKV_OK;
+}
+
+// The wide tensor-core dequantize for one head dimension: 1 when the call does not fit it (a side with
+// lambda, groups above 32, or scale rows that are not whole 16-byte rows of the plane).
+template <int DV>
+int codec_dequantize_tc_wide_d(const CodecCall& c) {
+    if (c.group > 32) return 1;
+    for (int s = 0; s < c.n_sides; ++s) {
+        if (c.side[s].lambda) return 1;
+        const long long rb = (long long)(DV / c.group) * scale_bytes(c.side[s].scale_format);
+        if ((c.side[s].scale_format != SRFTKV_SCALE_FP32 || DV != 256) &&
+            (((long long)c.t_cap * rb) % 16 || ((long long)c.t_offset * rb) % 16))
+            return 1;
+    }
+    const int bk = c.side[0].bits, bv = c.n_sides > 1 ? c.side[1].bits : bk;
+    if (bk == 4 && bv == 4) return launch_dq_tc_wide<4, 4, DV>(c);
+    if (bk == 8 && bv == 8) return launch_dq_tc_wide<8, 8, DV>(c);
+    if (bk == 8 && bv == 4) return launch_dq_tc_wide<8, 4, DV>(c);
+    return launch_dq_tc_wide<4, 8, DV>(c);
 }
 
 // Every (K, V) width pair and scale format of one wide head dimension.

@@ -86,6 +86,9 @@ int codec_quantize_tc(const CodecCall& c);
 // Tensor-core quantize at d = 192 and d = 256 (codec_tc_wide.cuh; groups of at most 32).
 int codec_quantize_tc_wide192(const CodecCall& c);
 int codec_quantize_tc_wide256(const CodecCall& c);
+// Tensor-core dequantize at d = 192 and 256: 1 when the call does not fit it (lambda, groups above 32, scale rows).
+int codec_dequantize_tc_wide192(const CodecCall& c);
+int codec_dequantize_tc_wide256(const CodecCall& c);
 // One warp per vector (d = 128, groups of at most 32): returns 1 when the call does not fit it.
 int codec_quantize_warp(const CodecCall& c);
 int codec_dequantize_tc(const CodecCall& c);

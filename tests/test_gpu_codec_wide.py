@@ -172,3 +172,32 @@ def test_wide_tensor_core_many_tiles(d):
         assert_scales(_np(side.scales[oi, hi, ti])[:, None, :], enc["scales"])
         assert_codes(_np(side.codes[oi, hi, ti])[:, None, :], enc["r"], 4)
         assert bool((side.scales > 0).all()), "unwritten scale rows"
+
+
+DQ_CASES = [(d, bk, bv, group, fmt) for d in (192, 256) for bk, bv in ((4, 4), (8, 8), (8, 4), (4, 8))
+            for group in (16, 32) for fmt in ("fp32", "fp16", "e8m0")]
+
+
+@pytest.mark.parametrize("d,bk,bv,group,fmt", DQ_CASES)
+def test_wide_tensor_core_dequantize(monkeypatch, d, bk, bv, group, fmt):
+    """The tensor-core dequantize at d = 192 / 256 (forced on): codes written at t_offset 16 of t_cap 416 (so
+    fp16 / e8m0 scale rows start on whole 16-byte rows), 2 outer x 300 tokens x 3 heads (ragged last tile),
+    against the oracle's decode of the GPU's codes and within one quantisation step of the oracle's own."""
+    w = I.Workload("widedq", n_outer=2, tokens=300, kv_heads=3, d=d, data_seed=d + 3 * bk + bv + group + len(fmt),
+                   outlier_kind="scale", outlier_channels=4, outlier_factor=50.0)
+    xk, xv = I.kv_side(w, "k"), I.kv_side(w, "v")
+    monkeypatch.setenv("SRFTKV_QUANT_PATH", "tc")
+    sk, sv = _quantize(xk, xv, None, None, bk, bv, group, 39, 416, 16, fmt=fmt)
+    ok_, ov_ = torch.empty((2, 300, 3, d), dtype=torch.float16, device="cuda"), torch.empty(
+        (2, 300, 3, d), dtype=torch.float16, device="cuda")
+    ok_.fill_(float("nan"))
+    ov_.fill_(float("nan"))
+    K.srft_kv_dequantize(K.Side(sk.codes, sk.scales, bk, x=ok_, scale_format=fmt),
+                         K.Side(sv.codes, sv.scales, bv, x=ov_, scale_format=fmt), 2, 300, 3, d, group, 416, 16, 39)
+    torch.cuda.synchronize()
+    for side, out, x, b in ((sk, ok_, xk, bk), (sv, ov_, xv, bv)):
+        codes, scales, _ = _check(side, x, None, b, group, 39, 16, fmt=fmt)
+        got = _np(out).astype(np.float64)
+        assert np.isfinite(got).all()
+        mine = O.srft_kv_dequantize(codes, scales, None, b, group, 39)
+        assert np.abs(got - mine).max() <= np.abs(mine).max() * 2.0**-10 + 1e-5
