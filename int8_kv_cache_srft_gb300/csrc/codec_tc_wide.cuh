@@ -341,8 +341,11 @@ static int launch_tc_wide(const CodecCall& c) {
 // the d = 128 kernel rebuilds B from).
 namespace wide {
 constexpr int DQ_CONV = 8, DQ_EPI = 8, DQ_WARPS = 2 + DQ_CONV + DQ_EPI;
-constexpr int DQ_NA = 2;          // A buffers in tensor memory
-constexpr uint32_t DQ_A_COL = 256, DQ_A_STRIDE = 128;  // accumulator halves at columns 0 and 128
+// tensor memory: a ring of three accumulator slots of 128 columns (one output half of a tile each, so
+// the epilogue has a tile and a half of slack) and one A buffer at column 384; the converters convert
+// the next tile into registers before they wait for the A buffer, so one suffices
+constexpr int DQ_NA = 1, DQ_SLOTS = 3;
+constexpr uint32_t DQ_A_COL = 384, DQ_A_STRIDE = 128;
 
 // Segments of a code row of rb bytes: powers of two of at most 128 bytes, largest first.
 __host__ __device__ constexpr int seg_width(int rb, int s) {
@@ -391,6 +394,35 @@ __device__ __forceinline__ float unit_scale(const uint8_t* __restrict__ in, int 
     return __uint_as_float((uint32_t)in[m * ng + gi] << 23);  // e8m0: the byte is the fp32 exponent field
 }
 
+// Scales of the NU 16-coordinate units u0 .. u0+NU-1 of tile row m (u0 even), with vector loads where the
+// row layout allows: fp32 rows of d = 256 are swizzled 16-byte chunks, fp32 rows of d = 192 contiguous and
+// 8-byte aligned at even groups; fp16 / e8m0 rows contiguous
+template <int DV, int NU>
+__device__ __forceinline__ void unit_scales(const uint8_t* __restrict__ in, int m, int u0, int group, int sfmt,
+                                            float (&sc)[NU]) {
+    const int ng = DV / group;
+    if (sfmt == SRFTKV_SCALE_FP32 && group == 16) {
+        if constexpr (DV == 256) {  // 64-byte rows, 64-byte swizzle; u0 a multiple of 4
+            const int srb = 64;
+#pragma unroll
+            for (int q = 0; q < NU / 4; ++q) {
+                const float4 v = *reinterpret_cast<const float4*>(in + m * srb + (swz16(srb, m, u0 / 4 + q) << 4));
+                sc[4 * q] = v.x, sc[4 * q + 1] = v.y, sc[4 * q + 2] = v.z, sc[4 * q + 3] = v.w;
+            }
+            if constexpr (NU % 4 == 0) return;
+        } else {  // 48-byte rows; unit = group, 8-byte aligned pairs
+#pragma unroll
+            for (int q = 0; q < NU / 2; ++q) {
+                const float2 v = *reinterpret_cast<const float2*>(in + (m * ng + u0 + 2 * q) * 4);
+                sc[2 * q] = v.x, sc[2 * q + 1] = v.y;
+            }
+            return;
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < NU; ++u) sc[u] = unit_scale<DV>(in, m, u0 + u, group, sfmt);
+}
+
 // fp16 pairs of NW consecutive 8-coordinate code words starting at word w0 of tile row m: codes * scale
 // with the scale split into fp16 hi + lo (one main rounding), in the K order of dq_kperm
 template <int DV, int BITS, int NW>
@@ -408,9 +440,11 @@ __device__ __forceinline__ void word_pairs(const uint8_t* __restrict__ in, int o
         w[4 * k + 2] = v.z;
         w[4 * k + 3] = v.w;
     }
+    float scu[NW / 2];
+    unit_scales<DV, NW / 2>(in + off_sc, m, w0 / 2, group, sfmt, scu);
 #pragma unroll
     for (int u = 0; u < NW / 2; ++u) {  // unit u: words 2u, 2u+1 (16 coordinates)
-        const float sc = unit_scale<DV>(in + off_sc, m, w0 / 2 + u, group, sfmt);
+        const float sc = scu[u];
         const __half h = __float2half_rn(sc);
         const uint32_t sh = half2_bcast(h), sl = half2_bcast(__float2half_rn(sc - __half2float(h)));
 #pragma unroll
@@ -452,8 +486,8 @@ __global__ void __launch_bounds__(wide::DQ_WARPS * 32, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     auto bar = [&](int i) { return ptx::smem_u32(&bars[i]); };
     constexpr int IN_FULL = 0, IN_EMPTY = C::STAGES, A_FULL = 2 * C::STAGES, A_EMPTY = A_FULL + wide::DQ_NA,
-                  ACC_FULL = A_EMPTY + wide::DQ_NA, ACC_EMPTY = ACC_FULL + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[ACC_EMPTY + 2]);
+                  ACC_FULL = A_EMPTY + wide::DQ_NA, ACC_EMPTY = ACC_FULL + wide::DQ_SLOTS;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[ACC_EMPTY + wide::DQ_SLOTS]);
 
     {  // B[k][q] = s_k R[n][k] with n = dq_kperm(q), fp16, in the MMA operand layout (k-blocks of DV rows)
         float* cs = reinterpret_cast<float*>(smem + C::OFF_IN);  // cos / sin (2 pi m/d) in the (unused) input stages
@@ -491,9 +525,9 @@ __global__ void __launch_bounds__(wide::DQ_WARPS * 32, 1)
             ptx::mbar_init(bar(A_FULL + b), wide::DQ_CONV);
             ptx::mbar_init(bar(A_EMPTY + b), 1);
         }
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < wide::DQ_SLOTS; ++h) {
             ptx::mbar_init(bar(ACC_FULL + h), 1);
-            ptx::mbar_init(bar(ACC_EMPTY + h), wide::DQ_EPI / 2);
+            ptx::mbar_init(bar(ACC_EMPTY + h), wide::DQ_EPI / 2);  // the four epilogue warps of one output half
         }
         ptx::fence_barrier_init();
     }
@@ -520,18 +554,20 @@ __global__ void __launch_bounds__(wide::DQ_WARPS * 32, 1)
                 const uint32_t a_tmem = tmem + wide::DQ_A_COL + b * wide::DQ_A_STRIDE;
 #pragma unroll 1
                 for (int hf = 0; hf < 2; ++hf) {
-                    if (i > 0 && !ptx::mbar_wait_bounded(bar(ACC_EMPTY + hf), (i - 1) & 1)) {
+                    const int j = 2 * i + hf, sl = j % wide::DQ_SLOTS;  // half j of the call -> slot j % 3
+                    if (j >= wide::DQ_SLOTS &&
+                        !ptx::mbar_wait_bounded(bar(ACC_EMPTY + sl), (j / wide::DQ_SLOTS - 1) & 1)) {
                         failed = true;
                         break;
                     }
                     tc::fence_after_sync();
-                    const uint32_t d_tmem = tmem + hf * 128;
+                    const uint32_t d_tmem = tmem + sl * 128;
 #pragma unroll
                     for (int ks = 0; ks < DV / 16; ++ks) {
                         const uint32_t boff = (ks >> 2) * (DV * 128) + hf * NH * 128 + (ks & 3) * 32;
                         tc::mma_f16_ta(d_tmem, a_tmem + 8 * ks, tc::sw128_desc(sbase + boff), IDESC, ks > 0);
                     }
-                    tc::commit(bar(ACC_FULL + hf));  // output half hf of this tile is ready
+                    tc::commit(bar(ACC_FULL + sl));  // output half hf of this tile is ready
                 }
                 if (failed) break;
                 tc::commit(bar(A_EMPTY + b));  // A buffer b may be rewritten once these MMAs are done
@@ -581,6 +617,22 @@ __global__ void __launch_bounds__(wide::DQ_WARPS * 32, 1)
                 break;
             }
             const uint8_t* in = smem + C::OFF_IN + st * C::STAGE;
+            const bool side_k = BK == BV || id.side == 0;
+            // half hf = code words hf*DV/16 .. +DV/16-1 = A columns hf*DV/4 .. +DV/4-1 (column c holds word c/4),
+            // converted into registers first, then written in pieces of 8 words (32 columns) and, at d = 192,
+            // one of 4 words (16 columns), each at a column offset that is a multiple of its width
+            constexpr int NWA = DV == 256 ? 8 : 8, NWB = DV == 256 ? 8 : 4;
+            const int wa = DV == 256 ? 16 * hf : (hf == 0 ? 0 : 16), wb = DV == 256 ? 16 * hf + 8 : (hf == 0 ? 8 : 12);
+            uint32_t ha[4 * NWA], hb[4 * NWB];
+            if (side_k) {
+                wide::word_pairs<DV, BK, NWA>(in, C::OFF_SC, m, wa, P.group, S.sfmt, ha);
+                wide::word_pairs<DV, BK, NWB>(in, C::OFF_SC, m, wb, P.group, S.sfmt, hb);
+            } else {
+                wide::word_pairs<DV, BV, NWA>(in, C::OFF_SC, m, wa, P.group, S.sfmt, ha);
+                wide::word_pairs<DV, BV, NWB>(in, C::OFF_SC, m, wb, P.group, S.sfmt, hb);
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(IN_EMPTY + st));  // input stage consumed
             if (!__all_sync(0xffffffffu,
                             i < wide::DQ_NA || ptx::mbar_wait_bounded(bar(A_EMPTY + b), (i / wide::DQ_NA - 1) & 1))) {
                 failed = true;
@@ -588,32 +640,9 @@ __global__ void __launch_bounds__(wide::DQ_WARPS * 32, 1)
             }
             tc::fence_after_sync();  // the MMAs that read A buffer b are complete
             const uint32_t acol = lanes + wide::DQ_A_COL + b * wide::DQ_A_STRIDE;
-            const bool side_k = BK == BV || id.side == 0;
-            // half hf = code words hf*DV/16 .. +DV/16-1 = A columns hf*DV/4 .. +DV/4-1 (column c holds word c/4),
-            // written in pieces of 8 words (32 columns) and, at d = 192, one of 4 words (16 columns), each at a
-            // column offset that is a multiple of its width
-            auto piece = [&](auto nwc, int w0) {
-                constexpr int NW = decltype(nwc)::value;
-                uint32_t hp[4 * NW];
-                if (side_k) wide::word_pairs<DV, BK, NW>(in, C::OFF_SC, m, w0, P.group, S.sfmt, hp);
-                else wide::word_pairs<DV, BV, NW>(in, C::OFF_SC, m, w0, P.group, S.sfmt, hp);
-                if constexpr (NW == 8) tc::st_32x32b_x32(acol + 4 * w0, hp);
-                else tc::st_32x32b_x16(acol + 4 * w0, hp);
-            };
-            using W8 = std::integral_constant<int, 8>;
-            using W4 = std::integral_constant<int, 4>;
-            if constexpr (DV == 256) {
-                piece(W8{}, 16 * hf);
-                piece(W8{}, 16 * hf + 8);
-            } else if (hf == 0) {  // words 0-7 (columns 0-31), 8-11 (32-47)
-                piece(W8{}, 0);
-                piece(W4{}, 8);
-            } else {               // words 12-15 (columns 48-63), 16-23 (64-95)
-                piece(W4{}, 12);
-                piece(W8{}, 16);
-            }
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(IN_EMPTY + st));  // input stage consumed
+            tc::st_32x32b_x32(acol + 4 * wa, ha);
+            if constexpr (NWB == 8) tc::st_32x32b_x32(acol + 4 * wb, hb);
+            else tc::st_32x32b_x16(acol + 4 * wb, hb);
             tc::wait_st();
             tc::fence_before_sync();
             __syncwarp();
@@ -622,10 +651,11 @@ __global__ void __launch_bounds__(wide::DQ_WARPS * 32, 1)
     } else {
         // epilogue warp w: tensor-memory lanes 32(w%4)..+31 = tile rows, output half (w-10)/4
         const int quarter = warp & 3, hf = (warp - 2 - wide::DQ_CONV) >> 2;
-        const uint32_t lanes = tmem + ((uint32_t)(32 * quarter) << 16) + hf * 128;
         for (int i = 0; i < count; ++i) {
             const int t = blockIdx.x + i * gridDim.x;
-            if (!__all_sync(0xffffffffu, ptx::mbar_wait_bounded(bar(ACC_FULL + hf), i & 1))) {
+            const int j = 2 * i + hf, sl = j % wide::DQ_SLOTS;
+            const uint32_t lanes = tmem + ((uint32_t)(32 * quarter) << 16) + sl * 128;
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait_bounded(bar(ACC_FULL + sl), (j / wide::DQ_SLOTS) & 1))) {
                 failed = true;
                 break;
             }
@@ -636,23 +666,49 @@ __global__ void __launch_bounds__(wide::DQ_WARPS * 32, 1)
             uint4* dst = reinterpret_cast<uint4*>(
                 reinterpret_cast<__half*>(P.side[id.side].x) +
                 ((((long long)id.o * P.n_tokens + t_tok) * P.H + id.h) * DV + hf * NH));
-#pragma unroll 1
-            for (int j = 0; j < NH / 32; ++j) {
-                uint32_t v[32];
-                tc::ld_32x32b_x32(lanes + 32 * j, v);
-                tc::wait_ld(v);
-                if (live) {
+            // the row's segment starts on 32 bytes when x does (rows of 2d bytes, halves of d bytes)
+            const bool v8 = (reinterpret_cast<uintptr_t>(P.side[id.side].x) & 31u) == 0u;
+            auto store32 = [&](int j, const uint32_t (&v)[32]) {  // fp32 columns 32j .. +31 -> fp16 -> global
+                if (!live) return;
+                uint32_t h[16];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        dst[4 * j + q] = make_uint4(pack_half2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
-                                                    pack_half2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
-                                                    pack_half2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
-                                                    pack_half2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+                for (int q = 0; q < 16; ++q) h[q] = pack_half2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
+                if (v8) {
+                    ptx::st_global_v8(dst + 4 * j, h[0], h[1], h[2], h[3], h[4], h[5], h[6], h[7]);
+                    ptx::st_global_v8(dst + 4 * j + 2, h[8], h[9], h[10], h[11], h[12], h[13], h[14], h[15]);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) dst[4 * j + q] = make_uint4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
                 }
+            };
+            // two 32-column loads in flight at a time; the accumulator half is released right after the last one
+            uint32_t va[32], vb[32];
+            tc::ld_32x32b_x32(lanes, va);
+            tc::ld_32x32b_x32(lanes + 32, vb);
+            tc::wait_ld(va);
+            tc::wait_ld(vb);
+            if constexpr (NH == 96) {
+                store32(0, va);
+                tc::ld_32x32b_x32(lanes + 64, va);
+                tc::wait_ld(va);
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(ACC_EMPTY + sl));  // the slot may be overwritten
+                store32(1, vb);
+                store32(2, va);
+            } else {
+                store32(0, va);
+                store32(1, vb);
+                tc::ld_32x32b_x32(lanes + 64, va);
+                tc::ld_32x32b_x32(lanes + 96, vb);
+                tc::wait_ld(va);
+                tc::wait_ld(vb);
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(ACC_EMPTY + sl));
+                store32(2, va);
+                store32(3, vb);
             }
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(ACC_EMPTY + hf));  // accumulator half hf may be overwritten
         }
     }
     if (failed) atomicOr(P.fault, 1u);
