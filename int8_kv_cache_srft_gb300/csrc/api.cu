@@ -252,14 +252,16 @@ bool encode_x_map(CUtensorMap* map, void* base, int d, int H, int n_tokens, int 
 static bool pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
 static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 static size_t min_sz(size_t a, size_t b) { return a < b ? a : b; }
-// head dimensions of the codec and the SRFT: the powers of two 16..256, 96 and 192
-// (a non-power-of-two d runs the SRFT only: d = 96 as the tensor-core contraction,
-// d = 192 as the mixed-radix register transform)
-static bool codec_d(int d) { return d == 16 || d == 32 || d == 64 || d == 96 || d == 128 || d == 192 || d == 256; }
+// head dimensions of the codec and the SRFT: the powers of two 16..256, 80, 96 and 192
+// (a non-power-of-two d runs the SRFT only: d = 80 and 96 as the 128-wide tensor-core
+// contraction, d = 192 as the wide tensor-core contraction or the mixed-radix register transform)
+static bool codec_d(int d) {
+    return d == 16 || d == 32 || d == 64 || d == 80 || d == 96 || d == 128 || d == 192 || d == 256;
+}
 static bool pow2_d(int d) { return d == 16 || d == 32 || d == 64 || d == 128 || d == 256; }
 
 static int check_codec_sizes(int n_outer, int n_tokens, int H, int d, int group, int t_cap, int t_offset) {
-    if (!codec_d(d)) return invalid("d must be one of 16, 32, 64, 96, 128, 192, 256 (got %d)", d);
+    if (!codec_d(d)) return invalid("d must be one of 16, 32, 64, 80, 96, 128, 192, 256 (got %d)", d);
     if (!pow2(group) || group < 16 || group > d || d % group)
         return invalid("group must be a power of two dividing d with 16 <= group <= d (got %d)", group);
     if (n_outer < 0 || n_tokens < 0 || H <= 0) return invalid("n_outer, n_tokens must be >= 0 and H > 0");
@@ -283,8 +285,8 @@ static int check_side(const srftkv_side* s, const char* name, int d, int group, 
         return invalid("%s: the Hadamard transform needs a power-of-two d (got %d)", name, d);
     if (!s->codes || !s->scales) return invalid("%s: codes and scales must not be NULL", name);
     if (need_x && !s->x) return invalid("%s: x must not be NULL", name);
-    // rows of a power-of-two d are powers of two: align to the row up to 16 bytes; d = 96 and 192 planes are
-    // copied by TMA
+    // rows of a power-of-two d are powers of two: align to the row up to 16 bytes; the planes of d = 80, 96 and
+    // 192 are copied by TMA or plain bulk copies
     const size_t crow = (size_t)d * s->bits / 8, srow = (size_t)(d / group) * scale_bytes(s->scale_format);
     const size_t ca = pow2(d) ? min_sz(16, crow) : 16, sa = pow2(d) ? min_sz(16, srow) : 16;
     if (!aligned(s->codes, ca)) return invalid("%s: codes must be %zu-byte aligned", name, ca);
@@ -351,7 +353,7 @@ int srft_kv_dequantize(const srftkv_side* k, const srftkv_side* v, int n_outer, 
 }
 
 int srft_kv_vector_bytes(int d, int bits, int group, int scale_format, size_t* code_bytes, size_t* scale_bytes_out) {
-    if (!codec_d(d)) return invalid("d must be one of 16, 32, 64, 96, 128, 192, 256");
+    if (!codec_d(d)) return invalid("d must be one of 16, 32, 64, 80, 96, 128, 192, 256");
     if (bits != 4 && bits != 8) return invalid("bits must be 4 or 8");
     if (!pow2(group) || group < 16 || group > d || d % group)
         return invalid("group must be a power of two dividing d with 16 <= group <= d");
@@ -363,7 +365,7 @@ int srft_kv_vector_bytes(int d, int bits, int group, int scale_format, size_t* c
 }
 
 int srft_transform(const void* x, float* y, int n, int d, uint64_t sign_seed, int inverse, void* stream) {
-    if (!codec_d(d)) return invalid("d must be one of 16, 32, 64, 96, 128, 192, 256");
+    if (!codec_d(d)) return invalid("d must be one of 16, 32, 64, 80, 96, 128, 192, 256");
     if (n < 0) return invalid("n must be >= 0");
     if (n == 0) return SRFTKV_OK;
     if (!x || !y) return invalid("x and y must not be NULL");

@@ -163,13 +163,14 @@ static bool split_mixed(const CodecCall& c, int (*fn)(const CodecCall&), int& rc
     return true;
 }
 
-// d = 96 runs only as the tensor-core contraction padded to 128 (the
+// d = 80 and 96 run only as the tensor-core contraction padded to 128 (the
 // register FFT is built for powers of two)
 static int tc_only(const CodecCall& c, int (*fn)(const CodecCall&), const char* what) {
     const int rc = fn(c);
     if (rc == 1) {
         set_error("%s at d = %d needs groups of 16 or 32 and, for dequantize, t_cap and t_offset such that "
-                  "t_cap * (d / group) * scale bytes and t_offset * (d / group) * scale bytes are multiples of 16",
+                  "t_cap * (d / group) * scale bytes and t_offset * (d / group) * scale bytes (at d = 80 also "
+                  "t_cap and t_offset * d * bits / 8) are multiples of 16",
                   what, c.d);
         return SRFTKV_ERR_INVALID;
     }
@@ -179,7 +180,7 @@ static int tc_only(const CodecCall& c, int (*fn)(const CodecCall&), const char* 
 int codec_quantize(const CodecCall& c) {
     int split_rc = 0;
     if (split_mixed(c, codec_quantize, split_rc)) return split_rc;
-    if (c.d == 96) return tc_only(c, codec_quantize_tc, "quantize");
+    if (c.d == 96 || c.d == 80) return tc_only(c, codec_quantize_tc, "quantize");
     const int ov = quant_path_override();
     const long long rows = (long long)c.n_sides * c.n_outer * c.n_tokens * c.H;
     if ((c.d == 192 || c.d == 256) && c.group <= 32 &&  // a group must fit in one epilogue thread's 32 columns
@@ -198,7 +199,7 @@ int codec_quantize(const CodecCall& c) {
 int codec_dequantize(const CodecCall& c) {
     int split_rc = 0;
     if (split_mixed(c, codec_dequantize, split_rc)) return split_rc;
-    if (c.d == 96) return tc_only(c, codec_dequantize_tc, "dequantize");
+    if (c.d == 96 || c.d == 80) return tc_only(c, codec_dequantize_tc, "dequantize");
     const int ov = quant_path_override();
     const long long rows = (long long)c.n_sides * c.n_outer * c.n_tokens * c.H;
     if ((c.d == 192 || c.d == 256) && (ov == 2 || (ov == 0 && rows >= kWideTensorCorePathMinRows))) {
@@ -231,7 +232,7 @@ static int launch_transform(const void* x, float* y, int n, uint64_t seed, bool 
 }
 
 // ---------------------------------------------------------------------------
-// The bare SRFT at a head dimension that is not a power of two (d = 96, 192) as the
+// The bare SRFT at a head dimension that is not a power of two (d = 80, 96, 192) as the
 // dense real map p = R diag(s) x of the packed unitary DFT: R[0][k] = d^-1/2,
 // R[1][k] = (-1)^k d^-1/2, and for 1 <= j < d/2 R[2j][k] = sqrt(2/d) cos(2 pi jk/d),
 // R[2j+1][k] = -sqrt(2/d) sin(2 pi jk/d); the inverse is diag(s) R^T.  A block
@@ -301,7 +302,7 @@ static int launch_dense_transform(const void* x, float* y, int n, int d, uint64_
 
 int transform_launch(const void* x, float* y, int n, int d, uint64_t seed, bool inverse, bool srht, cudaStream_t s) {
     if (n == 0) return 0;
-    if ((d == 96 || d == 192) && !srht) return launch_dense_transform(x, y, n, d, seed, inverse, s);
+    if ((d == 80 || d == 96 || d == 192) && !srht) return launch_dense_transform(x, y, n, d, seed, inverse, s);
     switch (d) {
         case 16: return launch_transform<16>(x, y, n, seed, inverse, srht, s);
         case 32: return launch_transform<32>(x, y, n, seed, inverse, srht, s);

@@ -130,8 +130,11 @@ __device__ __forceinline__ void group_scale(float A, float& sc, uint32_t& raw, f
 
 // ZLOG2: z holds the coordinates times 2^ZLOG2 (a contraction whose operand
 // was scaled by a power of two); the scales stored are those of the true
-// coordinates, the codes are unchanged.
-template <int D, int BITS, int SF, int ZLOG2 = 0>
+// coordinates, the codes are unchanged.  NARROW: the code row is only 8-byte
+// aligned and the scale row only aligned to one scale (rows of d = 80: 40
+// bytes of int4 codes, 5 scales), so codes go out as 8-byte stores and scales
+// one at a time.
+template <int D, int BITS, int SF, int ZLOG2 = 0, bool NARROW = false>
 __device__ __forceinline__ void quant_store_row(float (&z)[D], int group, uint8_t* __restrict__ crow,
                                                 uint8_t* __restrict__ srow) {
     constexpr int sfmt = SF;
@@ -177,6 +180,20 @@ __device__ __forceinline__ void quant_store_row(float (&z)[D], int group, uint8_
     uint32_t w[WORDS];
 #pragma unroll
     for (int i = 0; i < WORDS; ++i) w[i] = (BITS == 4) ? pack8_int4(&z[8 * i]) : pack4_int8(&z[4 * i]);
+    if constexpr (NARROW) {
+        static_assert(WORDS % 2 == 0, "8-byte code stores");
+#pragma unroll
+        for (int i = 0; i < WORDS / 2; ++i) reinterpret_cast<uint2*>(crow)[i] = make_uint2(w[2 * i], w[2 * i + 1]);
+        const int gu = group >> 4, sh = __ffs(gu) - 1;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if ((u & (gu - 1)) != 0) continue;
+            if constexpr (sfmt == SRFTKV_SCALE_FP32) reinterpret_cast<float*>(srow)[u >> sh] = sc[u];
+            else if constexpr (sfmt == SRFTKV_SCALE_FP16) reinterpret_cast<uint16_t*>(srow)[u >> sh] = (uint16_t)raw[u];
+            else srow[u >> sh] = (uint8_t)raw[u];
+        }
+        return;
+    }
     if constexpr (WORDS >= 4) {
 #pragma unroll
         for (int i = 0; i < WORDS / 4; ++i)

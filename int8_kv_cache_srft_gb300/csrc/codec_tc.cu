@@ -26,6 +26,8 @@
 //              keep enough of them in flight to match the load rate.
 // R_hi / R_lo are built once per CTA in shared memory from the twiddle table
 // (entries of R are closed forms of cos and sin of 2 pi jk/d).
+#include <type_traits>
+
 #include "codec_impl.cuh"
 #include "codec_tc_common.cuh"
 #include "tcgen05.cuh"
@@ -125,7 +127,7 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
         }
         for (int a = 0; a < T_NACC; ++a) {
             ptx::mbar_init(bar(ACC_FULL + a), 1);
-            ptx::mbar_init(bar(ACC_EMPTY + a), 4 * (DV / 32));  // one arrival per (lane quarter, column quarter)
+            ptx::mbar_init(bar(ACC_EMPTY + a), 4 * ((DV + 31) / 32));  // one arrival per (lane quarter, column quarter)
         }
         ptx::fence_barrier_init();
     }
@@ -203,30 +205,42 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
             const CodecSideK& S = P.side[id.side];
             const int t_tok = id.t0 + 32 * quarter + lane;
             if (t_tok >= P.n_tokens) return true;
-            float z[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) z[j] = __uint_as_float(r0[j]);
-            if (S.lambda != nullptr) {
-                const float4* lr = reinterpret_cast<const float4*>(
-                    S.lambda + (long long)id.o * S.lambda_outer_stride + (long long)id.h * DV + cq * 32);
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const float4 l = __ldg(lr + c);
-                    z[4 * c] *= l.x;
-                    z[4 * c + 1] *= l.y;
-                    z[4 * c + 2] *= l.z;
-                    z[4 * c + 3] *= l.w;
-                }
-            }
             const long long vrow = packed_row(P, id, t_tok);
-            // groups of at most 32: a column quarter holds whole groups
             const int ng = DV / P.group;
-            if (BK == BV || id.side == 0)
-                quant_store_row<32, BK, SF>(z, P.group, S.codes + vrow * (DV * BK / 8) + cq * (32 * BK / 8),
-                                            S.scales + (vrow * ng + cq * (ng / (DV / 32))) * S.sbytes);
-            else
-                quant_store_row<32, BV, SF>(z, P.group, S.codes + vrow * (DV * BV / 8) + cq * (32 * BV / 8),
-                                            S.scales + (vrow * ng + cq * (ng / (DV / 32))) * S.sbytes);
+            // the unit's columns 32 cq .. +W-1 (W = 32, or 16 for the last quarter at d = 80); at d = 80 the
+            // code rows (40 or 80 bytes) and scale rows (5 scales) allow only narrow stores
+            auto finish = [&](auto wc) {
+                constexpr int W = decltype(wc)::value;
+                constexpr bool NARROW = DV == 80;
+                float z[W];
+#pragma unroll
+                for (int j = 0; j < W; ++j) z[j] = __uint_as_float(r0[j]);
+                if (S.lambda != nullptr) {
+                    const float4* lr = reinterpret_cast<const float4*>(
+                        S.lambda + (long long)id.o * S.lambda_outer_stride + (long long)id.h * DV + cq * 32);
+#pragma unroll
+                    for (int c = 0; c < W / 4; ++c) {
+                        const float4 l = __ldg(lr + c);
+                        z[4 * c] *= l.x;
+                        z[4 * c + 1] *= l.y;
+                        z[4 * c + 2] *= l.z;
+                        z[4 * c + 3] *= l.w;
+                    }
+                }
+                uint8_t* srow = S.scales + (vrow * ng + (32 * cq) / P.group) * S.sbytes;
+                if (BK == BV || id.side == 0)
+                    quant_store_row<W, BK, SF, 0, NARROW>(z, P.group, S.codes + vrow * (DV * BK / 8) + cq * (32 * BK / 8),
+                                                          srow);
+                else
+                    quant_store_row<W, BV, SF, 0, NARROW>(z, P.group, S.codes + vrow * (DV * BV / 8) + cq * (32 * BV / 8),
+                                                          srow);
+            };
+            if constexpr (DV % 32 != 0) {
+                if (cq == DV / 32) finish(std::integral_constant<int, DV % 32>{});
+                else finish(std::integral_constant<int, 32>{});
+            } else {
+                finish(std::integral_constant<int, 32>{});
+            }
             return true;
         };
         if constexpr (DV == TD) {
@@ -244,7 +258,7 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
             // keeps the warp's lane quarter: unit u's is u % 4), so at d = 96
             // the 12 units of a tile spread over all 16 warps.
             static_assert(T_NACC == 4 && T_EPI == 16, "units per warp and round");
-            constexpr int NQ = DV / 32, U = 4 * NQ;
+            constexpr int NQ = (DV + 31) / 32, U = 4 * NQ;  // the last quarter is 16 columns wide at d = 80
             const int x = ((warp - 2) & ~3) | quarter;
             for (int r = 0; blockIdx.x + T_NACC * r * stride < P.total_tiles && !failed; ++r)
 #pragma unroll 1
@@ -497,6 +511,71 @@ __device__ __forceinline__ void d96_half_pairs(const uint8_t* __restrict__ in, i
     }
 }
 
+// d = 80: ten 8-coordinate words a row, five a half: words 4h..4h+3
+// (coordinates 32h..32h+31, A columns 16h..+15) and 8+h (coordinates
+// 64+8h..+7, A columns 32+4h..+3), so both halves do equal work and each
+// tensor-memory store (16 + 4 columns) is aligned to its width.  Rows are
+// 40 (int4) or 80 (int8) bytes, copied flat, so only 8-byte alignment holds.
+template <int BITS>
+__device__ __forceinline__ void d80_half_words(const uint8_t* __restrict__ in, int m, int hf,
+                                               uint32_t (&w)[5 * BITS / 4]) {
+    const uint8_t* row = in + m * (80 * BITS / 8);
+    if constexpr (BITS == 4) {
+        const uint2 a = *reinterpret_cast<const uint2*>(row + 16 * hf);
+        const uint2 b = *reinterpret_cast<const uint2*>(row + 16 * hf + 8);
+        w[0] = a.x; w[1] = a.y; w[2] = b.x; w[3] = b.y;
+        w[4] = *reinterpret_cast<const uint32_t*>(row + 32 + 4 * hf);
+    } else {
+        const uint4 a = *reinterpret_cast<const uint4*>(row + 32 * hf);
+        const uint4 b = *reinterpret_cast<const uint4*>(row + 32 * hf + 16);
+        const uint2 c = *reinterpret_cast<const uint2*>(row + 64 + 8 * hf);
+        w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+        w[8] = c.x; w[9] = c.y;
+    }
+}
+
+// fp16 pairs of half hf of a d = 80 row (units 2hf, 2hf+1 and 4; groups of 16), codes * scale with the
+// scale split into fp16 hi + lo, in the order of the A columns
+template <int BITS>
+__device__ __forceinline__ void d80_half_pairs(const uint8_t* __restrict__ in, int off_sc, int m, int hf, int sfmt,
+                                               uint32_t (&hp)[20]) {
+    uint32_t w[5 * BITS / 4];
+    d80_half_words<BITS>(in, m, hf, w);
+    const int sb = sfmt == SRFTKV_SCALE_FP32 ? 4 : sfmt == SRFTKV_SCALE_FP16 ? 2 : 1;
+    const uint8_t* srow = in + off_sc + m * 5 * sb;
+    const int units[3] = {2 * hf, 2 * hf + 1, 4};
+    uint32_t sh[3], sl[3];
+#pragma unroll
+    for (int u = 0; u < 3; ++u) {
+        const int gi = units[u];
+        float sc;
+        if (sfmt == SRFTKV_SCALE_FP32) sc = *reinterpret_cast<const float*>(srow + 4 * gi);
+        else if (sfmt == SRFTKV_SCALE_FP16) sc = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(srow + 2 * gi)));
+        else sc = __uint_as_float((uint32_t)srow[gi] << 23);
+        const __half h = __float2half_rn(sc);
+        sh[u] = half2_bcast(h);
+        sl[u] = half2_bcast(__float2half_rn(sc - __half2float(h)));
+    }
+#pragma unroll
+    for (int k = 0; k < 5; ++k) {
+        const int u = k < 4 ? k >> 1 : 2;
+        uint32_t c[4];
+        if constexpr (BITS == 4) {
+            const uint32_t x = w[k], xs = x >> 8;
+            c[0] = codes_lo4(x);
+            c[1] = codes_hi4(x);
+            c[2] = codes_lo4(xs);
+            c[3] = codes_hi4(xs);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                c[j] = codes_b8(__byte_perm(w[2 * k], w[2 * k + 1], j | (j << 4) | ((4 + j) << 8) | ((4 + j) << 12)));
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) hp[4 * k + j] = h2fma(c[j], sh[u], h2mul(c[j], sl[u]));
+    }
+}
+
 struct DqMaps {
     CUtensorMap out[2], codes[2], scales[2];
 };
@@ -643,6 +722,18 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
                 const uint32_t dst = sbase + DQ_OFF_IN + st * C::STAGE;
                 const int row = P.t_offset + id.t0;   // packed planes: [outer*H][t_cap] rows
                 const int oh = id.o * P.H + id.h;
+                if constexpr (DV == 80) {
+                    // rows of 40 / 80 code bytes and 5 scales are no TMA rows: the tile's bytes of both planes as
+                    // plain bulk copies, stopping at the end of this (outer, head)
+                    const CodecSideK& S = P.side[id.side];
+                    const int rows = min(TM, P.t_cap - row), rb = 80 * bits / 8, srb = 5 * S.sbytes;
+                    ptx::mbar_arrive_expect_tx(bar(IN_FULL + st), (uint32_t)(rows * (rb + srb)));
+                    ptx::bulk_load(dst, S.codes + ((long long)oh * P.t_cap + row) * rb, (uint32_t)(rows * rb),
+                                   bar(IN_FULL + st));
+                    ptx::bulk_load(dst + C::OFF_SC, S.scales + ((long long)oh * P.t_cap + row) * srb,
+                                   (uint32_t)(rows * srb), bar(IN_FULL + st));
+                    continue;
+                }
                 // fp32 scales as rows of the tile; fp16 / e8m0 scales as the tile's bytes in rows of 16
                 const int sb = P.side[id.side].sbytes, ng = DV / P.group, sc_bytes = TM * ng * sb;
                 const bool flat = !(sb == 4 && DV == TD);  // scale rows copied as 16-byte rows of bytes
@@ -671,7 +762,30 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
             uint32_t hp[32];  // fp16 pairs in the K order of dq_kperm: column 32 hf + c
             const bool side_k = BK == BV || id.side == 0;
             // lambda is folded into B: the converters take codes * scale only
-            if constexpr (DV != TD) {  // d = 96: balanced halves of six words (d96_word)
+            if constexpr (DV == 80) {  // d = 80: balanced halves of five words
+                uint32_t (&h20)[20] = *reinterpret_cast<uint32_t(*)[20]>(hp);
+                if (side_k)
+                    d80_half_pairs<BK>(in, C::OFF_SC, m, hf, S.sfmt, h20);
+                else
+                    d80_half_pairs<BV>(in, C::OFF_SC, m, hf, S.sfmt, h20);
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(IN_EMPTY + st));  // input stage consumed
+                const bool ok = __all_sync(0xffffffffu,
+                                           i < DQ_NA || ptx::mbar_wait_bounded(bar(A_EMPTY + b), (i / DQ_NA - 1) & 1));
+                if (!ok) {
+                    failed = true;
+                    break;
+                }
+                tc::fence_after_sync();  // the MMAs that read A buffer b are complete
+                const uint32_t acol = tmem + ((uint32_t)(32 * quarter) << 16) + DQ_A_COL + b * 64;
+                tc::st_32x32b_x16(acol + 16 * hf, hp);
+                tc::st_32x32b_x4(acol + 32 + 4 * hf, hp + 16);
+                tc::wait_st();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(A_FULL + b));
+                continue;
+            } else if constexpr (DV != TD) {  // d = 96: balanced halves of six words (d96_word)
                 uint32_t (&h24)[24] = *reinterpret_cast<uint32_t(*)[24]>(hp);
                 if (side_k)
                     d96_half_pairs<BK>(in, C::OFF_SC, m, hf, P.group, S.sfmt, h24);
@@ -736,6 +850,12 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
                 for (int j = 0; j < 2; ++j) tc::ld_32x32b_x32(lanes + 64 * hf + 32 * j, v[j]);
 #pragma unroll
                 for (int j = 0; j < 2; ++j) tc::wait_ld(v[j]);
+            } else if constexpr (DV == 80) {  // d = 80: columns 32hf..+31 and 64+8hf..+7
+                uint32_t (&v8)[8] = *reinterpret_cast<uint32_t(*)[8]>(v[1]);
+                tc::ld_32x32b_x32(lanes + 32 * hf, v[0]);
+                tc::ld_32x32b_x8(lanes + 64 + 8 * hf, v8);
+                tc::wait_ld(v[0]);
+                tc::wait_ld(v8);
             } else {  // d = 96: columns 32hf..+31 and 64+16hf..+15 (d96_word)
                 uint32_t (&v16)[16] = *reinterpret_cast<uint32_t(*)[16]>(v[1]);
                 tc::ld_32x32b_x32(lanes + 32 * hf, v[0]);
@@ -750,12 +870,14 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
             if (leader) ptx::bulk_wait_read<1>();
             ptx::named_bar_sync(1, 32 * DQ_EPI);
             uint8_t* O = smem + DQ_OFF_O + s * T_A_BYTES;
-            // 8-column chunk ch (of 8 here, 6 at d = 96) -> its output column
-            constexpr int NCHK = DV == TD ? 8 : 6;
+            // 8-column chunk ch (of 8 here, 6 at d = 96, 5 at d = 80) -> its output column
+            constexpr int NCHK = DV == TD ? 8 : DV == 96 ? 6 : 5;
 #pragma unroll
             for (int ch = 0; ch < NCHK; ++ch) {
                 const int j = ch >> 2, c0 = (ch & 3) * 8;
-                const int col = DV == TD ? 64 * hf + 8 * ch : (ch < 4 ? 32 * hf + 8 * ch : 64 + 16 * hf + 8 * (ch - 4));
+                const int col = DV == TD ? 64 * hf + 8 * ch
+                                : DV == 96 ? (ch < 4 ? 32 * hf + 8 * ch : 64 + 16 * hf + 8 * (ch - 4))
+                                           : (ch < 4 ? 32 * hf + 8 * ch : 64 + 8 * hf);
                 uint4 w;
                 w.x = pack_half2(__uint_as_float(v[j][c0 + 0]), __uint_as_float(v[j][c0 + 1]));
                 w.y = pack_half2(__uint_as_float(v[j][c0 + 2]), __uint_as_float(v[j][c0 + 3]));
@@ -814,8 +936,12 @@ static int launch_dq_tc(const CodecCall& c) {
         const unsigned long long sdims[3] = {(unsigned long long)ng, tcap, nrow};
         const unsigned long long sstr[2] = {ng * 4ull, tcap * ng * 4ull};
         const unsigned sbox[3] = {(unsigned)ng, (unsigned)TM, 1u};
-        if (!encode_x_map(&M.out[s], d.x, DV, c.H, c.n_tokens, c.n_outer, TM, true) ||
-            !encode_tiled_swz(&M.codes[s], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, d.codes, cdims, cstr, cbox, swz(rb),
+        if (!encode_x_map(&M.out[s], d.x, DV, c.H, c.n_tokens, c.n_outer, TM, true)) return SRFTKV_ERR_CUDA;
+        if (DV == 80) {  // code and scale rows read by plain bulk copies
+            M.codes[s] = M.scales[s] = M.out[s];
+            continue;
+        }
+        if (!encode_tiled_swz(&M.codes[s], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, d.codes, cdims, cstr, cbox, swz(rb),
                               "tensor-core dequantize codes"))
             return SRFTKV_ERR_CUDA;
         if (d.scale_format != SRFTKV_SCALE_FP32 || DV != TD) {
@@ -888,11 +1014,13 @@ static int launch_tc_bits(const CodecCall& c, int bk, int bv) {
 }
 template <int SF>
 static int launch_tc_dim(const CodecCall& c, int bk, int bv) {
-    return c.d == 96 ? launch_tc_bits<SF, 96>(c, bk, bv) : launch_tc_bits<SF, TD>(c, bk, bv);
+    return c.d == 96 ? launch_tc_bits<SF, 96>(c, bk, bv)
+           : c.d == 80 ? launch_tc_bits<SF, 80>(c, bk, bv)
+                       : launch_tc_bits<SF, TD>(c, bk, bv);
 }
 
 int codec_quantize_tc(const CodecCall& c) {
-    if ((c.d != TD && c.d != 96) || c.group > 32) return 1;  // a group must fit in one epilogue thread's 32 columns
+    if ((c.d != TD && c.d != 96 && c.d != 80) || c.group > 32) return 1;  // a group must fit in one epilogue thread's 32 columns
     const int bk = c.side[0].bits, bv = c.n_sides > 1 ? c.side[1].bits : bk;
     const int sf = c.side[0].scale_format;  // both sides share it (mixed calls are split on the host)
     if (sf == SRFTKV_SCALE_FP16) return launch_tc_dim<SRFTKV_SCALE_FP16>(c, bk, bv);
@@ -909,9 +1037,12 @@ static int launch_dq_bits(const CodecCall& c, int bk, int bv) {
 }
 
 int dq_tc_scale_rows_ok(const CodecCall& c) {
-    // fp16 / e8m0 planes (and every plane of d = 96) are copied in rows of 16
-    // bytes: a token's scale bytes times t_cap and t_offset must be whole rows
+    // fp16 / e8m0 planes (and every plane of d = 96 and 80) are copied in rows of 16
+    // bytes: a token's scale bytes times t_cap and t_offset must be whole rows;
+    // at d = 80 the code planes as well
     for (int s = 0; s < c.n_sides; ++s) {
+        const long long cb = (long long)c.d * c.side[s].bits / 8;
+        if (c.d == 80 && (((long long)c.t_cap * cb) % 16 || ((long long)c.t_offset * cb) % 16)) return 0;
         const long long rb = (long long)(c.d / c.group) * scale_bytes(c.side[s].scale_format);
         if ((c.side[s].scale_format != SRFTKV_SCALE_FP32 || c.d != TD) &&
             (((long long)c.t_cap * rb) % 16 || ((long long)c.t_offset * rb) % 16))
@@ -921,10 +1052,12 @@ int dq_tc_scale_rows_ok(const CodecCall& c) {
 }
 
 int codec_dequantize_tc(const CodecCall& c) {
-    if ((c.d != TD && c.d != 96) || c.group > 32) return 1;  // scale rows must be at least 16 bytes for the TMA copy
+    if ((c.d != TD && c.d != 96 && c.d != 80) || c.group > 32) return 1;  // scale rows of at least 16 bytes (TMA)
     if (!dq_tc_scale_rows_ok(c)) return 1;
     const int bk = c.side[0].bits, bv = c.n_sides > 1 ? c.side[1].bits : bk;
-    return c.d == 96 ? launch_dq_bits<96>(c, bk, bv) : launch_dq_bits<TD>(c, bk, bv);
+    return c.d == 96 ? launch_dq_bits<96>(c, bk, bv)
+           : c.d == 80 ? launch_dq_bits<80>(c, bk, bv)
+                       : launch_dq_bits<TD>(c, bk, bv);
 }
 
 }  // namespace srftkv
