@@ -467,10 +467,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                           "attn_bytes_per_token_head": tok_bytes}
         del vk, vv, dqk, dqv
 
-    # head dimensions that are not powers of two, on the same cache shape: d = 96 (the first 96 coordinates of
-    # the inputs; the tensor-core contraction) and d = 192 (the decode workload's generator at d = 192; the
-    # two-lane mixed-radix register transform), int4/int4, group 16, fp32 scales; attention also on the raw fp16
-    # cache of the same inputs
+    # other head dimensions on the same cache shape: d = 96 (the first 96 coordinates of the inputs), d = 192
+    # and d = 256 (the decode workload's generator at that d), all through the tensor-core codec, int4/int4,
+    # group 16, fp32 scales; attention also on the raw fp16 cache of the same inputs
     def nonpow2_variant(dn, xkn, xvn, qn):
         vk = K.alloc_side(B, t_cap, Hkv, dn, 4, G, device=dev)
         vv = K.alloc_side(B, t_cap, Hkv, dn, 4, G, device=dev)
@@ -501,9 +500,15 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     variants["d96"] = nonpow2_variant(96, xk[..., :96].contiguous(), xv[..., :96].contiguous(),
                                       q[..., :96].contiguous())
+    torch.cuda.empty_cache()
     w192 = wd.resized(d=192)
     variants["d192"] = nonpow2_variant(192, I.kv_side(w192, "k", device=dev), I.kv_side(w192, "v", device=dev),
                                        I.query(w192, device=dev))
+    torch.cuda.empty_cache()
+    # the same cache shape at d = 256 (33.5 M vectors, 704 B each: 23.6 GB through each codec launch)
+    w256 = wd.resized(d=256)
+    variants["d256"] = nonpow2_variant(256, I.kv_side(w256, "k", device=dev), I.kv_side(w256, "v", device=dev),
+                                       I.query(w256, device=dev))
     torch.cuda.empty_cache()
 
     other = other_workloads(K, I, torch, dev, stream, time_launch) if rank == 0 else None
