@@ -27,7 +27,8 @@ small; it prints one JSON line with the median event time per launch.
 on the full Gemma-3-1B-shaped cache (0.21 M vectors, 150 MB), and
 --kernel d192_quantize|d192_dequantize (and d256_...) for the d = 192 (256)
 codec on the decode cache shape at that d cut to B=2 (4.2 M vectors, about
-2.2 GB (2.9 GB) held).
+2.2 GB (2.9 GB) held), and d80_quantize|d80_dequantize|d80_attention for
+d = 80 on the cuts above.
 """
 
 from __future__ import annotations
@@ -64,7 +65,8 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--kernel", default=None,
                     choices=("quantize", "dequantize", "attention", "gemma_quantize", "gemma_dequantize",
-                             "d192_quantize", "d192_dequantize", "d256_quantize", "d256_dequantize"),
+                             "d80_quantize", "d80_dequantize", "d80_attention", "d192_quantize", "d192_dequantize",
+                             "d256_quantize", "d256_dequantize"),
                     help="profiling case: launch only this kernel on a small workload")
     return ap.parse_args()
 
@@ -467,8 +469,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                           "attn_bytes_per_token_head": tok_bytes}
         del vk, vv, dqk, dqv
 
-    # other head dimensions on the same cache shape: d = 96 (the first 96 coordinates of the inputs), d = 192
-    # and d = 256 (the decode workload's generator at that d), all through the tensor-core codec, int4/int4,
+    # other head dimensions on the same cache shape: d = 96 (the first 96 coordinates of the inputs), d = 80, 192
+    # and 256 (the decode workload's generator at that d), all through the tensor-core codec, int4/int4,
     # group 16, fp32 scales; attention also on the raw fp16 cache of the same inputs
     def nonpow2_variant(dn, xkn, xvn, qn):
         vk = K.alloc_side(B, t_cap, Hkv, dn, 4, G, device=dev)
@@ -500,6 +502,12 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     variants["d96"] = nonpow2_variant(96, xk[..., :96].contiguous(), xv[..., :96].contiguous(),
                                       q[..., :96].contiguous())
+    torch.cuda.empty_cache()
+    # d = 80: the decode workload's generator at that d (int4 rows of 40 bytes: the attention reads them as rows
+    # of token pairs)
+    w80 = wd.resized(d=80)
+    variants["d80"] = nonpow2_variant(80, I.kv_side(w80, "k", device=dev), I.kv_side(w80, "v", device=dev),
+                                      I.query(w80, device=dev))
     torch.cuda.empty_cache()
     w192 = wd.resized(d=192)
     variants["d192"] = nonpow2_variant(192, I.kv_side(w192, "k", device=dev), I.kv_side(w192, "v", device=dev),
@@ -738,10 +746,12 @@ def run_case(args):
 
     torch.cuda.set_device(0)
     K.library()
-    attn = args.kernel == "attention"
+    attn = args.kernel.endswith("attention")
     kind = args.kernel.split("_")[-1]
     if args.kernel.startswith("gemma_"):
         w = I.GEMMA
+    elif args.kernel.startswith("d80_"):
+        w = I.DECODE.resized(n_outer=4, tokens=32768, d=80) if attn else I.DECODE.resized(n_outer=2, d=80)
     elif args.kernel.startswith("d192_"):
         w = I.DECODE.resized(n_outer=2, d=192)
     elif args.kernel.startswith("d256_"):

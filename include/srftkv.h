@@ -38,12 +38,12 @@
  *    int8: two's-complement bytes;
  *  - scales are fp32; softmax scale defaults to 1/sqrt(d); a query with
  *    sequence length 0 gets a zero output;
- *  - a head dimension that is not a power of two (d = 96 or 192;
+ *  - a head dimension that is not a power of two (d = 80, 96 or 192;
  *    Methodology 1 names SRFT's freedom from the power-of-two restriction
  *    of Hadamard rotations): the same F, the unitary DFT of length d, with
- *    the same packing; the library forms it as a dense d x d map (d = 96)
- *    or as a mixed-radix FFT (d = 192: 96 = 2 x 3 x 16 points) instead of
- *    radix-2 stages only.
+ *    the same packing; the library forms it as a dense d x d map (d = 80,
+ *    96, and d = 192 on the tensor cores) or as a mixed-radix FFT (d = 192:
+ *    96 = 2 x 3 x 16 points) instead of radix-2 stages only.
  *
  * General conventions
  *  - Every pointer argument that names tensor data is a DEVICE pointer
@@ -60,12 +60,14 @@
  *  - Return codes: SRFTKV_OK, or a negative SRFTKV_ERR_*; on any error no
  *    work has been enqueued and srftkv_last_error() describes it.
  *  - Inputs must be finite; NaN/Inf behaviour is unspecified.
- *  - Supported sizes: d in {16, 32, 64, 96, 128, 192, 256} for the codec
- *    and srft_transform, d in {64, 96, 128, 192, 256} for attention; group
- *    a power of two dividing d with 16 <= group <= d; bits in {4, 8} for
- *    packed sides.  d = 96 and 192 take the SRFT only (the Hadamard matrix
- *    needs a power of two) and 16-byte aligned code and scale planes; d =
- *    96 takes groups of 16 or 32, d = 192 groups of 16, 32 or 64.
+ *  - Supported sizes: d in {16, 32, 64, 80, 96, 128, 192, 256} for the
+ *    codec and srft_transform, d in {64, 80, 96, 128, 192, 256} for
+ *    attention; group a power of two dividing d with 16 <= group <= d; bits
+ *    in {4, 8} for packed sides.  d = 80, 96 and 192 take the SRFT only (the
+ *    Hadamard matrix needs a power of two) and 16-byte aligned code and
+ *    scale planes; d = 80 takes groups of 16 (the only power of two >= 16
+ *    dividing 80), d = 96 groups of 16 or 32, d = 192 groups of 16, 32 or
+ *    64.
  */
 #ifndef SRFTKV_H
 #define SRFTKV_H
@@ -133,9 +135,10 @@ typedef struct srftkv_side {
  * Both sides are encoded by one kernel launch.  Requires
  * 0 <= t_offset, t_offset + n_tokens <= t_cap, and x rows 16-byte aligned.
  * n_outer == 0 or n_tokens == 0 is a no-op that returns SRFTKV_OK.
- * d = 96 runs as the 128-wide tensor-core contraction with R zero outside
- * its 96 x 96 block (any call size); d = 192 as the register transform, two
- * threads per vector.
+ * d = 80 and 96 run as the 128-wide tensor-core contraction with R zero
+ * outside its d x d block (any call size); d = 192 and 256 as the wide
+ * tensor-core contraction for calls of 2^19 vectors and more, else as the
+ * register transform (two threads per vector at d = 192).
  */
 int srft_kv_quantize(const srftkv_side* k, const srftkv_side* v, int n_outer, int n_tokens,
                      int H, int d, int group, int t_cap, int t_offset, uint64_t sign_seed,
@@ -148,10 +151,12 @@ int srft_kv_quantize(const srftkv_side* k, const srftkv_side* v, int n_outer, in
  * (SRHT sides: x_hat = diag(s) . H . ((codes * scale) / lambda) / sqrt(d))
  * written to side->x as [n_outer][n_tokens][H][d].  Same size rules as
  * srft_kv_quantize.  The tensor-core path copies fp16 / e8m0 scale planes
- * (every scale plane at d = 96) as rows of 16 bytes, so there
+ * (every scale plane at d = 80 and 96) as rows of 16 bytes, so there
  * t_cap * (d/group) * scale bytes and t_offset * (d/group) * scale bytes must
- * be multiples of 16: at d = 96 that is required (SRFTKV_ERR_INVALID
- * otherwise); at d = 128 a call that misses it takes the FFT path.
+ * be multiples of 16, and at d = 80 (code rows of 40 or 80 bytes, copied
+ * flat) also t_cap * d * bits / 8 and t_offset * d * bits / 8: at d = 80
+ * and 96 that is required (SRFTKV_ERR_INVALID otherwise); at d = 128 a call
+ * that misses it takes the FFT path.
  */
 int srft_kv_dequantize(const srftkv_side* k, const srftkv_side* v, int n_outer, int n_tokens,
                        int H, int d, int group, int t_cap, int t_offset, uint64_t sign_seed,
@@ -177,16 +182,18 @@ int srft_kv_dequantize(const srftkv_side* k, const srftkv_side* v, int n_outer, 
  *              q4kv_decode_attention_workspace_size(...) bytes (16-byte aligned)
  *              for the per-split partial results; contents need not be
  *              initialised and are overwritten.
- * Requires d in {64, 96, 128, 192, 256}, Hq % Hkv == 0 (any GQA ratio:
+ * Requires d in {64, 80, 96, 128, 192, 256}, Hq % Hkv == 0 (any GQA ratio:
  * ratios above 4 run as head groups of at most four query heads, so
  * B * Hkv * ceil(Hq/Hkv/4) <= 65535), and
  * for packed sides a power-of-two group with 16 <= group <= d/4 (a scale
- * row of at least 16 bytes, the smallest TMA row; 16 or 32 at d = 96 and
- * 192) and 16-byte aligned scales; anything else returns SRFTKV_ERR_INVALID
- * before any launch.  fp16 / e8m0 scale planes, and every scale plane at
- * d = 96 and 192 (rows that are not a power of two), are copied as rows of
- * 16 bytes and also need t_cap * (d/group) * scale bytes to be a multiple
- * of 16; d = 96 and 192 sides use the SRFT.
+ * row of at least 16 bytes, the smallest TMA row; 16 at d = 80, 16 or 32
+ * at d = 96 and 192) and 16-byte aligned scales; anything else returns
+ * SRFTKV_ERR_INVALID before any launch.  fp16 / e8m0 scale planes, and
+ * every scale plane at d = 80, 96 and 192 (rows that are not a power of
+ * two), are copied as rows of 16 bytes and also need t_cap * (d/group) *
+ * scale bytes to be a multiple of 16; int4 rows at d = 80 (40 bytes) are
+ * read as rows of token pairs and need an even t_cap; d = 80, 96 and 192
+ * sides use the SRFT.
  * Range: the kernel forms p * scale_V in fp16.  A stretch of tokens whose
  * V scales overflow that (scales of 128 and more) or sit far below it
  * (p-weighted mean scale under 2^-14) is run a second time with the values

@@ -142,13 +142,23 @@ __device__ __forceinline__ float h2_sum(uint32_t h) {
 // mode equal to the row length), which keeps the ldmatrix reads free of bank
 // conflicts without padding; longer rows (fp16, or int8 at d=256) keep 16
 // bytes of padding per row.
+//
+// Rows that are not a whole number of 16-byte chunks (int4 at d = 80: 40
+// bytes) can be neither a TMA row (strides are multiples of 16 bytes) nor an
+// ldmatrix row (16-byte aligned addresses).  Such planes are read as rows of
+// token PAIRS (80 bytes: five 16-byte segments, the middle one holding the
+// even token's last 8 bytes and the odd token's first 8), and the MMAs take
+// pairs as their rows (see tile_scores_pair / tile_pv_pair).
 template <int D, int BITS>
 struct PlaneT {
     static constexpr int RB = D * BITS / 8;                // bytes per cached row
-    static constexpr bool SWZ = BITS != 16 && RB <= 128 && (RB & (RB - 1)) == 0;  // exact rows, swizzled
+    static constexpr bool PAIR = RB % 16 == 8;             // read as rows of token pairs
+    static constexpr bool SWZ = !PAIR && BITS != 16 && RB <= 128 && (RB & (RB - 1)) == 0;  // exact rows, swizzled
     // unswizzled rows: an odd number of 16-byte chunks is already free of
-    // ldmatrix bank conflicts (48-byte int4 rows at d = 96); others get 16 bytes of padding
-    static constexpr int RP = SWZ || (RB / 16) % 2 == 1 ? RB : RB + 16;  // shared-memory row pitch
+    // ldmatrix bank conflicts (48-byte int4 rows at d = 96, 80-byte int8 rows and
+    // int4 pairs at d = 80); others get 16 bytes of padding
+    static constexpr int RP = SWZ || PAIR || (RB / 16) % 2 == 1 ? RB : RB + 16;  // shared-memory pitch per token
+    static constexpr int NSEG = 2 * RB / 16;               // 16-byte segments of a pair row (PAIR only)
 };
 
 // 16-byte chunks of a group-16 fp32 scale row (d/4 bytes; 24 at d = 96 -> 2)
@@ -187,16 +197,25 @@ struct AttnCfg {
     // fp16 / e8m0 scale planes land raw (at most 2 bytes a scale) and are widened into the fp32 rows above
     static constexpr int RAWB = CH * (D / 16) * 2;
     static constexpr int OFF_KR = align_up(OFF_VS + (QV ? CH * SRB : 0), 128);
-    static constexpr int OFF_VR = OFF_KR + (QK ? RAWB : 0);
+    static constexpr int OFF_VR = align_up(OFF_KR + (QK ? RAWB : 0), 128);  // a TMA destination (320 bytes of K at d = 80)
     static constexpr int STAGE = align_up(OFF_VR + (QV ? RAWB : 0), A0);
     static constexpr int WARP_BYTES = NS * STAGE;
     static constexpr int MERGE_BYTES = kAttnWarps * (4 * D + 8) * 4;
     static constexpr int BODY = kAttnWarps * WARP_BYTES > MERGE_BYTES ? kAttnWarps * WARP_BYTES : MERGE_BYTES;
     static constexpr int BARS = BODY;                   // mbarriers after the body
     static constexpr int SMEM = 1024 + BODY + 128;      // + slack to realign the base to 1024 bytes
-    static constexpr int QB = D / 8;    // K-side B-fragment registers
-    static constexpr int ACC = D / 4;   // V accumulators
-    static constexpr int NSV = BV == 4 ? D / 32 : BV == 8 ? D / 16 : 1;  // column sums of the V-side B
+    static_assert(OFF_KC % 128 == 0 && OFF_KS % 128 == 0 && OFF_VC % 128 == 0 && OFF_VS % 128 == 0 &&
+                      OFF_KR % 128 == 0 && OFF_VR % 128 == 0 && STAGE % 128 == 0,
+                  "TMA destinations on 128-byte boundaries");
+    static constexpr bool PK = PlaneT<D, BK>::PAIR, PV = PlaneT<D, BV>::PAIR;
+    static_assert(!(PK || PV) || CH == 32, "a chunk of token pairs is one 16-row MMA tile");
+    // K-side B-fragment registers and code-offset terms: four and two per 32-dim chunk (int4), per 16-byte
+    // segment of a pair row (int4 pairs), two and one per 16 dims (int8 / fp16)
+    static constexpr int QB = PK ? 4 * PlaneT<D, BK>::NSEG : D / 8;
+    static constexpr int NB = PK ? 2 * PlaneT<D, BK>::NSEG : D / 16;
+    // V accumulators: eight per 32-dim chunk or pair segment (half of them useful for int4), four per 16 dims
+    static constexpr int ACC = PV ? 8 * PlaneT<D, BV>::NSEG : D / 4;
+    static constexpr int NSV = PV ? PlaneT<D, BV>::NSEG : BV == 4 ? D / 32 : BV == 8 ? D / 16 : 1;  // column sums of the V-side B
 };
 
 // ---------------------------------------------------------------------------
@@ -381,6 +400,40 @@ __device__ __forceinline__ void build_qb(const float* __restrict__ qrow_base, in
     }
 }
 
+// K-side B fragments for int4 keys read as token pairs (d = 80).  Segment sg
+// of a pair row is bytes 16 sg .. +15 of the pair; thread c's 4-byte word of
+// it is pair byte 16 sg + 4c, i.e. token (16 sg + 4c) / RB's dims 2 b .. 2 b + 7
+// with b = (16 sg + 4c) mod RB, laid out exactly as a 32-dim chunk of build_qb
+// (bytes 0-7 of a segment feed column half 0, bytes 8-15 half 1; the
+// straddling segment's halves belong to different tokens, which is why they
+// must be separate columns).
+template <int D>
+__device__ __forceinline__ void build_qb_pair(const float* __restrict__ qrow_base, int rep, int g, int c,
+                                              uint32_t (&qh)[4 * PlaneT<D, 4>::NSEG],
+                                              uint32_t (&ql)[4 * PlaneT<D, 4>::NSEG],
+                                              float (&nb)[2 * PlaneT<D, 4>::NSEG]) {
+    constexpr int RB = PlaneT<D, 4>::RB, NSEG = PlaneT<D, 4>::NSEG;
+    const int h = g >> 1, sigma = g & 1;
+    const bool ok = h < rep && (c >> 1) == sigma;
+    const float* q = qrow_base + (long long)h * D;
+    auto val = [&](int dim) -> float { return ok ? q[dim] : 0.f; };
+    constexpr float i16 = 0.0625f;
+#pragma unroll
+    for (int sg = 0; sg < NSEG; ++sg) {
+        const int base = 2 * ((16 * sg + 4 * c) % RB);
+        split_h2(val(base + 0), val(base + 4), qh[4 * sg + 0], ql[4 * sg + 0]);
+        split_h2(val(base + 1) * i16, val(base + 5) * i16, qh[4 * sg + 1], ql[4 * sg + 1]);
+        split_h2(val(base + 2), val(base + 6), qh[4 * sg + 2], ql[4 * sg + 2]);
+        split_h2(val(base + 3) * i16, val(base + 7) * i16, qh[4 * sg + 3], ql[4 * sg + 3]);
+        float part = h2_sum(qh[4 * sg + 0]) + h2_sum(ql[4 * sg + 0]) + h2_sum(qh[4 * sg + 2]) + h2_sum(ql[4 * sg + 2]);
+        part += 16.f * (h2_sum(qh[4 * sg + 1]) + h2_sum(ql[4 * sg + 1]) + h2_sum(qh[4 * sg + 3]) + h2_sum(ql[4 * sg + 3]));
+        part += __shfl_xor_sync(0xffffffffu, part, 1);
+        part += __shfl_xor_sync(0xffffffffu, part, 2);
+        nb[2 * sg + 0] = (-8.f / kSub) * __shfl_sync(0xffffffffu, part, 4 * (2 * c));
+        nb[2 * sg + 1] = (-8.f / kSub) * __shfl_sync(0xffffffffu, part, 4 * (2 * c + 1));
+    }
+}
+
 // Per-lane part of the ldmatrix row addresses into a plane image.  Lane l
 // supplies row rl of the 16-row sub-tile and reads dl chunks (0 or 1) past
 // the even chunk index being loaded.  off = rl times the row pitch (plus the
@@ -509,6 +562,18 @@ __device__ __forceinline__ void tile_scores(uint32_t kc, const LaneRow& LK, cons
                 a1 = fmaf(ksc(gi, 1), d[2], a1);
             }
         }
+        if constexpr (D % 32 != 0) {  // an odd number of 16-dim chunks (d = 80): the last one alone
+            constexpr int mm = D / 16 - 1;
+            uint32_t r[2];
+            ldsm_x2(plane_addr<PK::RB, PK::SWZ, PK::RP>(kc, LK, tr, mm), r);
+            const uint32_t x0 = u8_lo(r[0]), x1 = u8_lo(r[1]), x2 = u8_lo(r[0] >> 8), x3 = u8_lo(r[1] >> 8);
+            float d[4];
+            mma16816_c(d, x0, x1, x2, x3, qh[2 * mm], qh[2 * mm + 1], nb[mm], 0.f);
+            mma16816(d, x0, x1, x2, x3, ql[2 * mm], ql[2 * mm + 1]);
+            const int gi = (16 * mm) >> lg;
+            a0 = fmaf(ksc(gi, 0), d[0], a0);
+            a1 = fmaf(ksc(gi, 1), d[2], a1);
+        }
         s[0] = a0;
         s[1] = a1;
     } else {
@@ -522,6 +587,58 @@ __device__ __forceinline__ void tile_scores(uint32_t kc, const LaneRow& LK, cons
         }
         s[0] = d[0];
         s[1] = d[2];
+    }
+}
+
+// Scores of a 32-token chunk of int4 keys read as 16 token pairs (d = 80):
+// one MMA tile whose rows are pairs.  Per 16-byte segment the two column
+// halves of a head are (token parity, group) pieces of the pair: half h of
+// segment sg is pair byte 16 sg + 8h, token parity (16 sg + 8h) / RB, group
+// 2 ((16 sg + 8h) mod RB) / G.  s[a][b] is token 16a + 2g + b.
+template <int D, int G>
+__device__ __forceinline__ void tile_scores_pair(uint32_t kc, const LaneRow& LK, const uint8_t* __restrict__ ksb,
+                                                 int sp, int lg, int lane, const uint32_t (&qh)[4 * PlaneT<D, 4>::NSEG],
+                                                 const uint32_t (&ql)[4 * PlaneT<D, 4>::NSEG],
+                                                 const float (&nb)[2 * PlaneT<D, 4>::NSEG], float (&s)[2][2]) {
+    using PK = PlaneT<D, 4>;
+    constexpr int RB = PK::RB, NSEG = PK::NSEG, PB = 2 * RB;
+    const int g = lane >> 2;
+    const float* ks = reinterpret_cast<const float*>(ksb);
+    float a[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // [pair g | g + 8][token parity]
+    auto seg = [&](int sg, uint32_t rg, uint32_t rg8) {
+        const uint32_t rs = rg >> 8, rs8 = rg8 >> 8;
+        const uint32_t x0 = u4_lo(rg), x1 = u4_lo(rg8), x2 = u4_hi(rg), x3 = u4_hi(rg8);
+        const uint32_t y0 = u4_lo(rs), y1 = u4_lo(rs8), y2 = u4_hi(rs), y3 = u4_hi(rs8);
+        float d[4];
+        mma16816_c(d, x0, x1, x2, x3, qh[4 * sg], qh[4 * sg + 1], nb[2 * sg], nb[2 * sg + 1]);
+        mma16816(d, y0, y1, y2, y3, qh[4 * sg + 2], qh[4 * sg + 3]);
+        mma16816(d, x0, x1, x2, x3, ql[4 * sg], ql[4 * sg + 1]);
+        mma16816(d, y0, y1, y2, y3, ql[4 * sg + 2], ql[4 * sg + 3]);
+        // d = (pair g: half 0, half 1, pair g + 8: half 0, half 1) for head c
+        const int b0 = 16 * sg, b1 = 16 * sg + 8;
+        const int t0 = b0 / RB, t1 = b1 / RB;  // token parity of each half
+        const int f0 = (2 * (b0 % RB)) >> lg, f1 = (2 * (b1 % RB)) >> lg;
+        a[0][t0] = fmaf(ks[(2 * g + t0) * sp + f0], d[0], a[0][t0]);
+        a[0][t1] = fmaf(ks[(2 * g + t1) * sp + f1], d[1], a[0][t1]);
+        a[1][t0] = fmaf(ks[(16 + 2 * g + t0) * sp + f0], d[2], a[1][t0]);
+        a[1][t1] = fmaf(ks[(16 + 2 * g + t1) * sp + f1], d[3], a[1][t1]);
+    };
+#pragma unroll
+    for (int m2 = 0; m2 < NSEG / 2; ++m2) {
+        uint32_t r[4];
+        ldsm_x4(plane_addr<PB, false, PB>(kc, LK, 0, 2 * m2), r);
+        seg(2 * m2, r[0], r[1]);
+        seg(2 * m2 + 1, r[2], r[3]);
+    }
+    if constexpr (NSEG % 2 != 0) {
+        uint32_t r[2];
+        ldsm_x2(plane_addr<PB, false, PB>(kc, LK, 0, NSEG - 1), r);
+        seg(NSEG - 1, r[0], r[1]);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        s[i][0] = a[i][0];
+        s[i][1] = a[i][1];
     }
 }
 
@@ -611,6 +728,23 @@ __device__ __forceinline__ void tile_pv(uint32_t vc, const LaneRow& LV, const ui
                 mma16816(a0, x0, x1, x2, x3, bl0, bl1);
             }
         }
+        if constexpr (D % 32 != 0) {  // d = 80: the last 16-dim chunk alone
+            constexpr int cb = D / 16 - 1;
+            uint32_t r[2];
+            ldsm_x2_t(plane_addr<PV::RB, PV::SWZ, PV::RP>(vc, LV, tr, cb), r);
+            const int gv = G == 16 ? cb >> 2 : (16 * cb) >> lg;
+            const int fc = cb & 3;
+            const float b00 = p00 * vsc(gv, fc, 0), b10 = p10 * vsc(gv, fc, 1), b01 = p01 * vsc(gv, fc, 8),
+                        b11 = p11 * vsc(gv, fc, 9);
+            sv[cb] += (b00 + b10) + (b01 + b11);
+            uint32_t bh0, bl0, bh1, bl1;
+            split_h2(b00, b10, bh0, bl0);
+            split_h2(b01, b11, bh1, bl1);
+            float(&a0)[4] = *reinterpret_cast<float(*)[4]>(&acc[4 * cb]);
+            const uint32_t x0 = u8_lo(r[0]), x1 = u8_lo(r[0] >> 8), x2 = u8_lo(r[1]), x3 = u8_lo(r[1] >> 8);
+            mma16816(a0, x0, x1, x2, x3, bh0, bh1);
+            mma16816(a0, x0, x1, x2, x3, bl0, bl1);
+        }
     } else {
         const float cm = (g & 1) ? 0.f : 1.f;
         uint32_t bh0, bl0, bh1, bl1;
@@ -630,6 +764,59 @@ __device__ __forceinline__ void tile_pv(uint32_t vc, const LaneRow& LV, const ui
             mma16816(a0, r[0], r[1], r[2], r[3], bh0, bh1);
             mma16816(a0, r[0], r[1], r[2], r[3], bl0, bl1);
         }
+    }
+}
+
+// acc += V^T B for a 32-token chunk of int4 values read as 16 token pairs
+// (d = 80).  The MMA's K index is the pair; per 16-byte segment sg the A rows
+// of column half h (thread rows g < 4: h = 0) are dims of token parity
+// (16 sg + 8h) / RB, so B[pair][n] = p(2 pair + parity, head n/2) *
+// scale_V(that token, its group).  q[f][e][t] is p of token 2 (2c + e + 8f) + t
+// for head g/2 (pairs 2c + e + 8f are this thread's K slots).  Segment sg
+// accumulates into acc[8 sg .. 8 sg + 7] (acc_coord_pair maps them back).
+template <int D, int G>
+__device__ __forceinline__ void tile_pv_pair(uint32_t vc, const LaneRow& LV, const uint8_t* __restrict__ vsb, int sp,
+                                             int lg, int lane, const float (&q)[2][2][2],
+                                             float (&acc)[8 * PlaneT<D, 4>::NSEG], float (&sv)[PlaneT<D, 4>::NSEG]) {
+    using PV = PlaneT<D, 4>;
+    constexpr int RB = PV::RB, NSEG = PV::NSEG, PB = 2 * RB;
+    const int g = lane >> 2, c = lane & 3, side = g & 1;
+    const float* vs = reinterpret_cast<const float*>(vsb);
+    auto seg = [&](int sg, uint32_t R0, uint32_t R1) {
+        // this thread's column half is `side`: pair byte 16 sg + 8 side
+        const int pb = 16 * sg + 8 * side;
+        const int t = 16 * sg + 16 <= RB ? 0 : 16 * sg >= RB ? 1 : pb / RB;  // token parity (constant but for the straddling segment)
+        const int f = (2 * (pb % RB)) >> lg;
+        const float q00 = t ? q[0][0][1] : q[0][0][0], q10 = t ? q[0][1][1] : q[0][1][0];
+        const float q01 = t ? q[1][0][1] : q[1][0][0], q11 = t ? q[1][1][1] : q[1][1][0];
+        const int r0 = 4 * c + t;  // token of pair 2c
+        const float b00 = q00 * vs[r0 * sp + f], b10 = q10 * vs[(r0 + 2) * sp + f];
+        const float b01 = q01 * vs[(r0 + 16) * sp + f], b11 = q11 * vs[(r0 + 18) * sp + f];
+        sv[sg] += (b00 + b10) + (b01 + b11);
+        uint32_t bh0, bl0, bh1, bl1;
+        split_h2(b00, b10, bh0, bl0);
+        split_h2(b01, b11, bh1, bl1);
+        const uint32_t S0 = R0 >> 8, S1 = R1 >> 8;
+        float(&a0)[4] = *reinterpret_cast<float(*)[4]>(&acc[8 * sg]);
+        float(&a1)[4] = *reinterpret_cast<float(*)[4]>(&acc[8 * sg + 4]);
+        const uint32_t x0 = u4_lo(R0), x1 = u4_hi(R0), x2 = u4_lo(R1), x3 = u4_hi(R1);
+        const uint32_t y0 = u4_lo(S0), y1 = u4_hi(S0), y2 = u4_lo(S1), y3 = u4_hi(S1);
+        mma16816(a0, x0, x1, x2, x3, bh0, bh1);
+        mma16816(a1, y0, y1, y2, y3, bh0, bh1);
+        mma16816(a0, x0, x1, x2, x3, bl0, bl1);
+        mma16816(a1, y0, y1, y2, y3, bl0, bl1);
+    };
+#pragma unroll
+    for (int m2 = 0; m2 < NSEG / 2; ++m2) {
+        uint32_t r[4];
+        ldsm_x4_t(plane_addr<PB, false, PB>(vc, LV, 0, 2 * m2), r);
+        seg(2 * m2, r[0], r[1]);
+        seg(2 * m2 + 1, r[2], r[3]);
+    }
+    if constexpr (NSEG % 2 != 0) {
+        uint32_t r[2];
+        ldsm_x2_t(plane_addr<PB, false, PB>(vc, LV, 0, NSEG - 1), r);
+        seg(NSEG - 1, r[0], r[1]);
     }
 }
 
@@ -685,9 +872,11 @@ template <int D, int BK, int BV, int NT, int G>
 __device__ __forceinline__ void attn_chunk(const AttnParams& P, uint8_t* __restrict__ stage, int t0, int t_end, int lane,
                                            const LaneRow& LK, const LaneRow& LV,
                                            const uint32_t (&kso)[scale_chunks<D>()],
-                                           const uint32_t (&vso)[scale_chunks<D>()], const uint32_t (&qh)[D / 8],
-                                           const uint32_t (&ql)[D / 8],
-                                           const float (&nb)[D / 16], int nh, float (&acc)[D / 4],
+                                           const uint32_t (&vso)[scale_chunks<D>()],
+                                           const uint32_t (&qh)[AttnCfg<D, BK, BV>::QB],
+                                           const uint32_t (&ql)[AttnCfg<D, BK, BV>::QB],
+                                           const float (&nb)[AttnCfg<D, BK, BV>::NB], int nh,
+                                           float (&acc)[AttnCfg<D, BK, BV>::ACC],
                                            float (&sv)[AttnCfg<D, BK, BV>::NSV], float& m, float& l, float mu) {
     using C = AttnCfg<D, BK, BV>;
     constexpr float SU = C::QK ? kSub : 1.f;  // scores come in units of 1/SU
@@ -716,16 +905,28 @@ __device__ __forceinline__ void attn_chunk(const AttnParams& P, uint8_t* __restr
         __syncwarp();
     }
 
-    // this thread's head is c; s[st] holds tokens 16st+g and 16st+g+8
+    // this thread's head is c; s[st][r] holds token 16st + g + 8r (rows of tokens), or token 16st + 2g + r
+    // (rows of token pairs)
     float s[NT][2];
-#pragma unroll
-    for (int st = 0; st < NT; ++st) {
-        if (16 * st < valid)
-            tile_scores<D, BK, G>(kc, LK, stage + C::OFF_KS, kso, sp, lg, 16 * st, lane, qh, ql, nb, s[st]);
-        else s[st][0] = s[st][1] = 0.f;
+    if constexpr (C::PK) {
+        tile_scores_pair<D, G>(kc, LK, stage + C::OFF_KS, sp, lg, lane, qh, ql, nb, s);
         if (tail) {
-            if (16 * st + g >= valid) s[st][0] = -INFINITY;
-            if (16 * st + g + 8 >= valid) s[st][1] = -INFINITY;
+#pragma unroll
+            for (int st = 0; st < NT; ++st)
+#pragma unroll
+                for (int r = 0; r < 2; ++r)
+                    if (16 * st + 2 * g + r >= valid) s[st][r] = -INFINITY;
+        }
+    } else {
+#pragma unroll
+        for (int st = 0; st < NT; ++st) {
+            if (16 * st < valid)
+                tile_scores<D, BK, G>(kc, LK, stage + C::OFF_KS, kso, sp, lg, 16 * st, lane, qh, ql, nb, s[st]);
+            else s[st][0] = s[st][1] = 0.f;
+            if (tail) {
+                if (16 * st + g >= valid) s[st][0] = -INFINITY;
+                if (16 * st + g + 8 >= valid) s[st][1] = -INFINITY;
+            }
         }
     }
     // ---- online softmax (log2 domain) ----
@@ -743,7 +944,7 @@ __device__ __forceinline__ void attn_chunk(const AttnParams& P, uint8_t* __restr
         const float f = (mn == -INFINITY) ? 1.f : ex2(m - mn);  // head c's factor
         l *= f;
 #pragma unroll
-        for (int i = 0; i < D / 4; ++i) acc[i] *= f;
+        for (int i = 0; i < C::ACC; ++i) acc[i] *= f;
         const float fs = __shfl_sync(0xffffffffu, f, g >> 1);  // head g/2's factor, for the column sums
 #pragma unroll
         for (int i = 0; i < C::NSV; ++i) sv[i] *= fs;
@@ -754,22 +955,60 @@ __device__ __forceinline__ void attn_chunk(const AttnParams& P, uint8_t* __restr
     const float bias = (m == -INFINITY) ? 0.f : m - 8.f + mu;
     const bool offer = c < nh;  // padded heads offer zero
     const int hd = g >> 1;         // head of this thread's B columns
+    if constexpr (C::PV) {
+        // all p of the chunk first; q[f][e][t]: token 4c + 2e + 16f + t for head hd
+        float o[NT][2];
+#pragma unroll
+        for (int st = 0; st < NT; ++st)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const float pv = ex2(fmaf(s[st][r], SU, -bias));  // 0 for masked tokens
+                l += pv;
+                o[st][r] = offer ? pv : 0.f;
+            }
+        float q[2][2][2];
+#pragma unroll
+        for (int f = 0; f < 2; ++f)
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    if constexpr (C::PK) {  // token 16f + 2(2c + e) + t sits in pair row 2c + e, register [f][t]
+                        q[f][e][t] = __shfl_sync(0xffffffffu, o[f][t], 4 * (2 * c + e) + hd);
+                    } else {  // token 16f + u, u = 4c + 2e + t: row u % 8, register [f][u / 8] with u / 8 = c / 2
+                        const int src = 4 * ((4 * c + 2 * e + t) & 7) + hd;
+                        const float lo = __shfl_sync(0xffffffffu, o[f][0], src);
+                        const float hi = __shfl_sync(0xffffffffu, o[f][1], src);
+                        q[f][e][t] = (c >> 1) ? hi : lo;
+                    }
+                }
+        tile_pv_pair<D, G>(vc, LV, stage + C::OFF_VS, sp, lg, lane, q, acc, sv);
+    } else {
 #pragma unroll
     for (int st = 0; st < NT; ++st) {
         if (16 * st >= valid) break;
         const float p0 = ex2(fmaf(s[st][0], SU, -bias)), p1 = ex2(fmaf(s[st][1], SU, -bias));
         l += p0 + p1;
         const float o0 = offer ? p0 : 0.f, o1 = offer ? p1 : 0.f;
-        const float P00 = __shfl_sync(0xffffffffu, o0, 4 * (2 * c) + hd);
-        const float P10 = __shfl_sync(0xffffffffu, o0, 4 * (2 * c + 1) + hd);
-        const float P01 = __shfl_sync(0xffffffffu, o1, 4 * (2 * c) + hd);
-        const float P11 = __shfl_sync(0xffffffffu, o1, 4 * (2 * c + 1) + hd);
+        float P00, P10, P01, P11;
+        if constexpr (C::PK) {  // token 16st + 2c + e + 8f sits in pair row c + 4f, register [st][e]
+            P00 = __shfl_sync(0xffffffffu, o0, 4 * c + hd);
+            P10 = __shfl_sync(0xffffffffu, o1, 4 * c + hd);
+            P01 = __shfl_sync(0xffffffffu, o0, 4 * (c + 4) + hd);
+            P11 = __shfl_sync(0xffffffffu, o1, 4 * (c + 4) + hd);
+        } else {
+            P00 = __shfl_sync(0xffffffffu, o0, 4 * (2 * c) + hd);
+            P10 = __shfl_sync(0xffffffffu, o0, 4 * (2 * c + 1) + hd);
+            P01 = __shfl_sync(0xffffffffu, o1, 4 * (2 * c) + hd);
+            P11 = __shfl_sync(0xffffffffu, o1, 4 * (2 * c + 1) + hd);
+        }
         const int vt = valid - 16 * st;
         const bool sub_tail = vt < 16;
         const uint32_t mlo = (2 * c < vt ? 0x0000FFFFu : 0u) | (2 * c + 1 < vt ? 0xFFFF0000u : 0u);
         const uint32_t mhi = (2 * c + 8 < vt ? 0x0000FFFFu : 0u) | (2 * c + 9 < vt ? 0xFFFF0000u : 0u);
         tile_pv<D, BV, G>(vc, LV, stage + C::OFF_VS, vso, sp, lg, 16 * st, lane, P00, P10, P01, P11, mlo, mhi,
                           sub_tail, acc, sv);
+    }
     }
 }
 
@@ -792,6 +1031,21 @@ __device__ __forceinline__ void acc_coord(int i, int g, int c, int& dim, int& he
         dim = 16 * j + g + 8 * (e >> 1);
         useful = (e & 1) == 0;
     }
+}
+
+// The same for int4 values read as token pairs: accumulator i = 8 sg + 4j + e
+// of thread (g, c) is head c, column half e % 2, A row g (+ 8 for e >= 2) of
+// segment sg's x (j = 0) or y (j = 1) MMA: nibble e / 2 of pair byte
+// 16 sg + 2g + j, i.e. token parity par and dim 2 (byte mod RB) + e / 2.
+template <int D>
+__device__ __forceinline__ void acc_coord_pair(int i, int g, int c, int& dim, int& head, bool& useful, int& par) {
+    constexpr int RB = PlaneT<D, 4>::RB;
+    const int sg = i >> 3, j = (i >> 2) & 1, e = i & 3;
+    const int pb = 16 * sg + 2 * g + j;
+    head = c;
+    par = pb >= RB ? 1 : 0;
+    dim = 2 * (pb - par * RB) + (e >> 1);
+    useful = (e & 1) == (g >= 4 ? 1 : 0);  // rows g < 4 are bytes 0-7 of the segment: column half 0
 }
 
 // Grid (n_splits, B * Hkv * n_hg): CTA (split, (b, kv head, head group)).
@@ -836,13 +1090,20 @@ __global__ void __launch_bounds__(kAttnWarps * 32, D >= 256 ? 2 : 3)
     auto barw = [&](int s2) { return ptx::smem_u32(&bars[4 * warp + s2]); };
 
     uint32_t qh[C::QB], ql[C::QB];
-    float nb[D / 16];
-    build_qb<D, BK>(P.qt + ((long long)b * P.Hq + (long long)hkv * P.rep + h0) * D, nh, g, c, qh, ql, nb);
+    float nb[C::NB];
+    if constexpr (C::PK)
+        build_qb_pair<D>(P.qt + ((long long)b * P.Hq + (long long)hkv * P.rep + h0) * D, nh, g, c, qh, ql, nb);
+    else
+        build_qb<D, BK>(P.qt + ((long long)b * P.Hq + (long long)hkv * P.rep + h0) * D, nh, g, c, qh, ql, nb);
     // per-lane shared-memory addressing of the plane images
     using PK = PlaneT<D, BK>;
     using PV = PlaneT<D, BV>;
-    const LaneRow LK = lane_row_codes<PK::RB, PK::SWZ, PK::RP>(lane);
-    const LaneRow LV = BV == 16 ? lane_row_v16<PV::RB, PV::SWZ, PV::RP>(lane) : lane_row_codes<PV::RB, PV::SWZ, PV::RP>(lane);
+    // (pair planes: rows of 2 RB bytes)
+    const LaneRow LK = PK::PAIR ? lane_row_codes<2 * PK::RB, false, 2 * PK::RB>(lane)
+                                : lane_row_codes<PK::RB, PK::SWZ, PK::RP>(lane);
+    const LaneRow LV = PV::PAIR   ? lane_row_codes<2 * PV::RB, false, 2 * PV::RB>(lane)
+                       : BV == 16 ? lane_row_v16<PV::RB, PV::SWZ, PV::RP>(lane)
+                                  : lane_row_codes<PV::RB, PV::SWZ, PV::RP>(lane);
     constexpr int SCH = scale_chunks<D>();
     uint32_t kso[SCH], vso[SCH];
     scale_offsets<D, SCH>(g, 0, kso);                               // K: row g (and g + 8)
@@ -870,10 +1131,11 @@ __global__ void __launch_bounds__(kAttnWarps * 32, D >= 256 ? 2 : 3)
         uint8_t* dst = wbase + st * C::STAGE;
         const int tok = chunk * C::CH;
         ptx::mbar_arrive_expect_tx(bar, tx);
-        ptx::tma_load_3d(ptx::smem_u32(dst + C::OFF_KC), &tm_kc, bar, 0, tok, plane_row);
+        // (pair planes: rows of two tokens)
+        ptx::tma_load_3d(ptx::smem_u32(dst + C::OFF_KC), &tm_kc, bar, 0, C::PK ? tok / 2 : tok, plane_row);
         if constexpr (C::QK)
             ptx::tma_load_3d(ptx::smem_u32(dst + ks_off), &tm_ks, bar, 0, kflat ? chunk * ks_row : tok, plane_row);
-        ptx::tma_load_3d(ptx::smem_u32(dst + C::OFF_VC), &tm_vc, bar, 0, tok, plane_row);
+        ptx::tma_load_3d(ptx::smem_u32(dst + C::OFF_VC), &tm_vc, bar, 0, C::PV ? tok / 2 : tok, plane_row);
         if constexpr (C::QV)
             ptx::tma_load_3d(ptx::smem_u32(dst + vs_off), &tm_vs, bar, 0, vflat ? chunk * vs_row : tok, plane_row);
     };
@@ -1047,8 +1309,24 @@ __global__ void __launch_bounds__(kAttnWarps * 32, D >= 256 ? 2 : 3)
     for (int i = 0; i < C::ACC; ++i) {
         int dim, head;
         bool useful;
-        acc_coord<D, BV>(i, g, c, dim, head, useful);
-        if (useful) aw[(warp * 4 + head) * D + dim] = acc[i];
+        if constexpr (C::PV) {  // the even tokens' entries (one per dim and head) first, the odd ones added below
+            int par;
+            acc_coord_pair<D>(i, g, c, dim, head, useful, par);
+            if (useful && par == 0) aw[(warp * 4 + head) * D + dim] = acc[i];
+        } else {
+            acc_coord<D, BV>(i, g, c, dim, head, useful);
+            if (useful) aw[(warp * 4 + head) * D + dim] = acc[i];
+        }
+    }
+    if constexpr (C::PV) {
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < C::ACC; ++i) {
+            int dim, head, par;
+            bool useful;
+            acc_coord_pair<D>(i, g, c, dim, head, useful, par);
+            if (useful && par == 1) aw[(warp * 4 + head) * D + dim] += acc[i];
+        }
     }
     __syncthreads();
     for (int idx = threadIdx.x; idx < nh * D; idx += blockDim.x) {
@@ -1079,7 +1357,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, D >= 256 ? 2 : 3)
 // ---------------------------------------------------------------------------
 template <int D, bool ROT>
 __global__ void __launch_bounds__(128) attn_combine_kernel(const __grid_constant__ AttnParams P) {
-    constexpr int N = D / 2, PER = D / 32;
+    constexpr int N = D / 2, PER = (D + 31) / 32;  // dims lane + 32 j (the last j partial at d = 80)
     __shared__ float rows[4][D];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row = blockIdx.x * 4 + warp;  // (b, hq)
@@ -1097,24 +1375,28 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const __grid_constant
                 const float f = ex2(ml[2 * s] - M);
                 Lsum += f * ml[2 * s + 1];
 #pragma unroll
-                for (int j = 0; j < PER; ++j) o[j] += f * ac[(long long)s * D + lane * PER + j];
+                for (int j = 0; j < PER; ++j)
+                    if (lane + 32 * j < D) o[j] += f * ac[(long long)s * D + lane + 32 * j];
             }
         }
         const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
         const int b = row / P.Hq, hkv = (row - b * P.Hq) / P.rep;
 #pragma unroll
         for (int j = 0; j < PER; ++j) {
+            const int dim = lane + 32 * j;
+            if (dim >= D) break;
             float v = o[j] * inv;
             if (ROT && P.lam_v != nullptr)
-                v *= __frcp_rn(P.lam_v[(long long)b * P.lam_v_stride + (long long)hkv * D + lane * PER + j]);
-            rows[warp][lane * PER + j] = v;
+                v *= __frcp_rn(P.lam_v[(long long)b * P.lam_v_stride + (long long)hkv * D + dim]);
+            rows[warp][dim] = v;
         }
     }
     __syncwarp();
     if (!active) return;
     if constexpr (!ROT) {
 #pragma unroll
-        for (int j = 0; j < PER; ++j) P.out[(long long)row * D + lane * PER + j] = rows[warp][lane * PER + j];
+        for (int j = 0; j < PER; ++j)
+            if (lane + 32 * j < D) P.out[(long long)row * D + lane + 32 * j] = rows[warp][lane + 32 * j];
     } else if constexpr (!pow2_dim<D>()) {
         // inverse SRFT as the dense map diag(s) R^T p, one output coordinate per lane at a time
         __shared__ float tcs[4][D], tsn[4][D];  // per warp: warps past the last row have left the block
@@ -1184,6 +1466,9 @@ static CUtensorMapSwizzle swizzle_for(int row_bytes) {
 template <int D, int BITS>
 static bool encode_codes(CUtensorMap* map, const void* base, long long bh, int t_cap, int rows) {
     using PT = PlaneT<D, BITS>;
+    if (PT::PAIR)  // rows of two tokens (t_cap even, checked by attention_check)
+        return encode_plane(map, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2 * PT::RB, 1, 2 * PT::RB, bh, t_cap / 2,
+                            rows / 2, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (PT::SWZ)
         return encode_plane(map, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, PT::RB, 1, PT::RB, bh, t_cap, rows,
                             swizzle_for(PT::RB));
@@ -1316,8 +1601,8 @@ static int invalid_attn(const char* msg) {
 
 int attention_check(const void* q, const float* out, const srftkv_side* k, const srftkv_side* v, int B, int Hq,
                     int Hkv, int d, int group, int t_cap, int n_splits) {
-    if (d != 64 && d != 96 && d != 128 && d != 192 && d != 256)
-        return invalid_attn("attention: d must be 64, 96, 128, 192 or 256");
+    if (d != 64 && d != 80 && d != 96 && d != 128 && d != 192 && d != 256)
+        return invalid_attn("attention: d must be 64, 80, 96, 128, 192 or 256");
     const bool pow2d = (d & (d - 1)) == 0;
     if (B < 0 || Hq <= 0 || Hkv <= 0 || t_cap <= 0) return invalid_attn("attention: need B >= 0, Hq, Hkv, t_cap > 0");
     if (Hq % Hkv) return invalid_attn("attention: Hq must be a multiple of Hkv");
@@ -1327,8 +1612,8 @@ int attention_check(const void* q, const float* out, const srftkv_side* k, const
     if (!raw && ((k->bits != 4 && k->bits != 8) || (v->bits != 4 && v->bits != 8)))
         return invalid_attn("attention: bits must be 4, 8 (or 16 on both sides)");
     if (!raw) {
-        // a power-of-two d copies fp32 scale rows as rows (at least 16 bytes: group <= d/4); d = 96 and 192
-        // copy every scale plane as 16-byte rows of bytes and take groups of 16 or 32
+        // a power-of-two d copies fp32 scale rows as rows (at least 16 bytes: group <= d/4); d = 80, 96 and 192
+        // copy every scale plane as 16-byte rows of bytes and take groups of 16 (d = 80) or 16 and 32
         if (group < 16 || (group & (group - 1)) || (d == 96 ? group > 32 : group > d / 4))
             return invalid_attn("attention: group must be a power of two with 16 <= group <= d/4 (16 or 32 at d = 96)");
         if (!k->scales || !v->scales) return invalid_attn("attention: scales must not be NULL");
@@ -1346,6 +1631,9 @@ int attention_check(const void* q, const float* out, const srftkv_side* k, const
             if (!pow2d && sd->transform != SRFTKV_TRANSFORM_SRFT)
                 return invalid_attn("attention: the Hadamard transform needs a power-of-two d");
         }
+        // int4 rows of 40 bytes (d = 80) are copied as rows of token pairs
+        if (d == 80 && (k->bits == 4 || v->bits == 4) && (t_cap & 1))
+            return invalid_attn("attention: int4 rows at d = 80 need an even t_cap");
         if ((reinterpret_cast<uintptr_t>(k->scales) | reinterpret_cast<uintptr_t>(v->scales)) & 15)
             return invalid_attn("attention: scales must be 16-byte aligned");
         const srftkv_side* sd[2] = {k, v};
@@ -1422,6 +1710,7 @@ int attention_entry(const void* q, float* out, const srftkv_side* k, const srftk
     A.stream = stream;
     switch (d) {
         case 64: return launch_all<64>(A);
+        case 80: return launch_all<80>(A);
         case 96: return launch_all<96>(A);
         case 192: return launch_all<192>(A);
         case 128: return launch_all<128>(A);

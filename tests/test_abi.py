@@ -44,12 +44,14 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 @pytest.mark.parametrize("d,bits,group,code,scale", [(128, 4, 16, 64, 32), (128, 8, 16, 128, 32), (256, 4, 32, 128, 32),
-                                                     (16, 4, 16, 8, 4), (64, 8, 64, 64, 4)])
+                                                     (16, 4, 16, 8, 4), (64, 8, 64, 64, 4), (80, 4, 16, 40, 20),
+                                                     (80, 8, 16, 80, 20), (96, 4, 32, 48, 12)])
 def test_vector_bytes(lib, d, bits, group, code, scale):
     assert K.srft_kv_vector_bytes(d, bits, group) == (code, scale)
 
 
-@pytest.mark.parametrize("d,bits,group", [(48, 4, 16), (128, 3, 16), (128, 4, 8), (128, 4, 24), (64, 4, 128)])
+@pytest.mark.parametrize("d,bits,group", [(48, 4, 16), (128, 3, 16), (128, 4, 8), (128, 4, 24), (64, 4, 128),
+                                          (80, 4, 32)])
 def test_vector_bytes_rejects(lib, d, bits, group):
     with pytest.raises(K.SrftKvError) as e:
         K.srft_kv_vector_bytes(d, bits, group)
@@ -82,7 +84,7 @@ def _q(lib, k, v, n_outer=1, n_tokens=4, H=2, d=128, group=16, t_cap=8, t_offset
 
 
 @pytest.mark.parametrize("case", [
-    dict(d=100), dict(d=512), dict(group=8), dict(group=48), dict(group=256),
+    dict(d=100), dict(d=512), dict(d=72), dict(group=8), dict(group=48), dict(group=256), dict(d=80, group=32),
     dict(t_offset=5), dict(t_offset=-1), dict(n_tokens=-1), dict(H=0),
 ])
 def test_quantize_rejects_bad_sizes(lib, case):
@@ -115,7 +117,8 @@ def _attn(lib, k, v, B=2, Hq=8, Hkv=2, d=128, group=16, t_cap=64, ws=16, ws_byte
 
 
 @pytest.mark.parametrize("case", [
-    dict(d=32), dict(Hq=6, Hkv=4), dict(B=70000, Hq=1, Hkv=1), dict(group=64), dict(t_cap=0), dict(q=0), dict(out=8),
+    dict(d=32), dict(d=72), dict(Hq=6, Hkv=4), dict(B=70000, Hq=1, Hkv=1), dict(group=64), dict(t_cap=0), dict(q=0),
+    dict(out=8), dict(d=80, group=32), dict(d=80, t_cap=66),
 ])
 def test_attention_rejects_bad_arguments(lib, case):
     assert _attn(lib, _side(), _side(), **case) == K.SRFTKV_ERR_INVALID

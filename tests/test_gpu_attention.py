@@ -166,7 +166,7 @@ def test_attention_gqa_head_groups(rep, bk, bv, n_splits):
     assert np.abs(out - ref).max() <= ATTN_ATOL
 
 
-@pytest.mark.parametrize("d", (64, 96, 192, 256))
+@pytest.mark.parametrize("d", (64, 80, 96, 192, 256))
 def test_attention_gqa8_other_head_dims(d):
     B, Hkv, rep, t_cap, seed = 2, 1, 8, 320, 13
     Hq = Hkv * rep
