@@ -278,6 +278,21 @@ const char* srftkv_last_error(void);
  */
 int srftkv_device_fault(unsigned int* fault);
 
+/*
+ * srftkv_set_attention_poll_limit_for_testing -- TEST HOOK, not for use in
+ * production.  Sets how many times (each poll may suspend for up to about
+ * 1 us) a warp of the attention split kernel polls for its next chunk of the
+ * cache before it gives up; a negative value restores the default (2^20
+ * polls, about a second) and 0 makes every warp give up at its first chunk.
+ * A warp that gives up sets bit 8 of the fault word, waits with the default
+ * bound for its own copies in flight and contributes nothing, so a call on
+ * which every warp gives up leaves the fault word set and writes zero
+ * outputs.  Applies to every later attention call of the process (a
+ * process-wide setting, both attention entry points); the codec kernels
+ * keep their bound.  Always returns SRFTKV_OK.
+ */
+int srftkv_set_attention_poll_limit_for_testing(int polls);
+
 #ifdef __cplusplus
 }
 #endif

@@ -399,6 +399,11 @@ size_t q4kv_decode_attention_workspace_size(int B, int Hq, int Hkv, int d, int t
 
 const char* srftkv_last_error(void) { return t_err; }
 
+int srftkv_set_attention_poll_limit_for_testing(int polls) {
+    attention_set_poll_limit(polls);
+    return SRFTKV_OK;
+}
+
 int srftkv_device_fault(unsigned int* fault) {
     if (!fault) return invalid("fault must not be NULL");
     if (cudaDeviceSynchronize() != cudaSuccess) {

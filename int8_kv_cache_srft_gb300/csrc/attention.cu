@@ -31,6 +31,7 @@
 // hi + lo and contracted twice, which keeps the products at ~22-bit accuracy.
 #include <cuda_fp16.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstring>
 
@@ -41,6 +42,12 @@
 namespace srftkv {
 
 static __device__ unsigned int g_attn_fault;
+
+// Polls of the split kernel's wait for a chunk before the warp gives up; a
+// negative value selects the default (2^20 polls, about a second).  Set only
+// by srftkv_set_attention_poll_limit_for_testing.
+static std::atomic<int> g_poll_limit{-1};
+void attention_set_poll_limit(int polls) { g_poll_limit.store(polls < 0 ? -1 : polls); }
 
 constexpr int kAttnWarps = 4;
 #ifndef SRFTKV_ATTN_STAGES
@@ -68,6 +75,7 @@ struct AttnParams {
     int tr_k, tr_v;        // transform of the K and V sides (SRFTKV_TRANSFORM_*)
     int sf_k, sf_v;        // scale format of the K and V sides (SRFTKV_SCALE_*)
     float qscale;          // sm_scale * log2(e)
+    uint32_t poll_limit;   // polls of a warp's wait for its next chunk before it gives up
     uint32_t sign_mask[128];
 };
 
@@ -1175,7 +1183,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, D >= 256 ? 2 : 3)
             const int st = it % NS;
             const int nxt = chunk + (NS - 1) * kAttnWarps;
             if (lane == 0 && nxt < c_end) issue(nxt, (it + NS - 1) % NS);
-            const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(barw(st), (it / NS) & 1));
+            const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(barw(st), (it / NS) & 1, P.poll_limit));
             if (!ok) {
                 if (lane == 0) {
                     atomicOr(&g_attn_fault, 1u);
@@ -1703,6 +1711,8 @@ int attention_entry(const void* q, float* out, const srftkv_side* k, const srftk
     P.sf_v = raw ? 0 : v->scale_format;
     const float sc = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt((float)d);
     P.qscale = sc * 1.4426950408889634f;
+    const int lim = g_poll_limit.load();
+    P.poll_limit = lim < 0 ? (1u << 20) : (uint32_t)lim;
     sign_masks(d, seed, P.sign_mask);
     A.k = k;
     A.v = v;

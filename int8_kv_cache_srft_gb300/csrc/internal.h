@@ -103,5 +103,7 @@ int attention_check(const void* q, const float* out, const srftkv_side* k, const
 // The split count attention_entry picks for n_splits == 0 on the current device.
 int attention_auto_splits(int B, int Hq, int Hkv, int t_cap);
 unsigned int attn_take_fault();
+// Test hook behind srftkv_set_attention_poll_limit_for_testing (negative = the default limit).
+void attention_set_poll_limit(int polls);
 
 }  // namespace srftkv
