@@ -600,6 +600,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     fp16_ms = statistics.median(t16)
     for vname in variants:  # against the d = 128 fp16 cache unless the variant timed its own
         variants[vname].setdefault("attn_speedup_vs_fp16_cache", fp16_ms / variants[vname]["attn_ms"])
+        # each kernel of the variant against the same measured HBM peak (algorithmic bytes / event time)
+        for kk in ("quant", "deq", "attn"):
+            variants[vname][kk + "_frac"] = variants[vname][kk + "_gbs"] / peak
     cpu = None
     if not args.no_cpu:
         cpu = oracle_sample(args.cpu_seconds)
