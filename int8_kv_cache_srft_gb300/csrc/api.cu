@@ -196,7 +196,7 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, void* base
 
 bool encode_tiled_swz(CUtensorMap* map, CUtensorMapDataType dt, int rank, void* base, const unsigned long long* dims,
                       const unsigned long long* strides_bytes, const unsigned* box, CUtensorMapSwizzle swz,
-                      const char* what) {
+                      const char* what, CUtensorMapL2promotion promo) {
     auto enc = encoder();
     if (!enc) {
         set_error("cuTensorMapEncodeTiled is unavailable from the driver");
@@ -210,8 +210,8 @@ bool encode_tiled_swz(CUtensorMap* map, CUtensorMapDataType dt, int rank, void* 
         e[i] = 1;
         if (i + 1 < rank) s[i] = strides_bytes[i];
     }
-    const CUresult r = enc(map, dt, rank, base, d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const CUresult r = enc(map, dt, rank, base, d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, promo,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         set_error("cuTensorMapEncodeTiled failed (CUresult %d) for %s", (int)r, what);
         return false;
@@ -227,8 +227,13 @@ bool encode_x_map(CUtensorMap* map, void* base, int d, int H, int n_tokens, int 
                                             (unsigned long long)n_outer};
         const unsigned long long str[3] = {d * e, (unsigned long long)H * d * e, (unsigned long long)n_tokens * H * d * e};
         const unsigned box[4] = {64u, 1u, (unsigned)box_rows, 1u};
+        // rows that are not a multiple of 256 bytes (d = 80, 96, 192): an L2 promotion wider than the row's
+        // alignment would fetch part of the neighbouring head's row, read much later by another tile
+        const CUtensorMapL2promotion promo = (d * e) % 256 == 0   ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                                             : (d * e) % 128 == 0 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                                                                  : CU_TENSOR_MAP_L2_PROMOTION_NONE;
         return encode_tiled_swz(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, base, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B,
-                                "x rows (swizzled)");
+                                "x rows (swizzled)", promo);
     }
     if (d <= 128) {  // rows land padded by 8 elements (the zero-filled columns past d)
         const unsigned long long dims[4] = {(unsigned long long)d, (unsigned long long)H, (unsigned long long)n_tokens,

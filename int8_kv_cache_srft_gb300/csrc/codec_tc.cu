@@ -57,8 +57,9 @@ __device__ __forceinline__ TileId decode_tile128(const CodecParams& P, int t) { 
 // n the packed output coordinate, k the input coordinate), before the sign of
 // input k; zero outside dv x dv, so a smaller head dimension runs as the
 // 128-wide contraction padded with zeros.  dv = 128 takes the compile-time
-// twiddle table; other (even) dv the angle 2 pi (jk mod dv)/dv in double.
-__device__ float r_entry(int n, int k, int dv, bool srht) {
+// twiddle table; other (even) dv take cs[m], sn[m] = cos, sin(2 pi m / dv),
+// tabulated once per CTA (in double, rounded to float) by r_tables.
+__device__ float r_entry(int n, int k, int dv, bool srht, const float* __restrict__ cs, const float* __restrict__ sn) {
     if (n >= dv || k >= dv) return 0.f;
     if (dv == TD) {
         constexpr float inv_sqrt_d = 0.08838834764831845f;  // 1/sqrt(128)
@@ -69,13 +70,24 @@ __device__ float r_entry(int n, int k, int dv, bool srht) {
         const int m = (((n >> 1) * k) & (TD - 1)) * (256 / TD);  // angle 2 pi (jk mod d)/d on the 256-point table
         return (n & 1) ? c2 * tw_im_lane(m) : c2 * tw_re_lane(m);   // the imaginary part holds -sin
     }
-    const double isd = 1.0 / sqrt((double)dv);
-    if (n == 0) return (float)isd;
-    if (n == 1) return (float)((k & 1) ? -isd : isd);
+    const float isd = (float)(1.0 / sqrt((double)dv)), r2 = (float)sqrt(2.0 / dv);
+    if (n == 0) return isd;
+    if (n == 1) return (k & 1) ? -isd : isd;
     const int m = ((n >> 1) * k) % dv;
-    double sn, cs;
-    sincospi(2.0 * m / dv, &sn, &cs);
-    return (float)((n & 1) ? -sqrt(2.0) * isd * sn : sqrt(2.0) * isd * cs);
+    return (n & 1) ? -r2 * sn[m] : r2 * cs[m];
+}
+
+// cos, sin (2 pi m / dv) for m < dv into cs, sn (shared memory not yet in use);
+// the caller synchronises the block before r_entry reads them.  A table of dv
+// entries instead of an angle per entry of R: 16 K double-precision sincos per
+// CTA had cost about 80 us a launch (FP64 is slow on this GPU).
+__device__ __forceinline__ void r_tables(int dv, float* cs, float* sn) {
+    for (int m = threadIdx.x; m < dv; m += blockDim.x) {
+        double sv, cv;
+        sincospi(2.0 * m / dv, &sv, &cv);
+        cs[m] = (float)cv;
+        sn[m] = (float)sv;
+    }
 }
 
 // Byte offset of element (row n, column k) of a 128 x 128 fp16 operand stored
@@ -107,9 +119,16 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
     // (both sides of a launch share the transform; mixed calls are split on the host)
     {
         const bool srht = P.side[0].transform == SRFTKV_TRANSFORM_SRHT;
+        // angle tables (d < 128) in the x stages, which no copy has reached yet
+        float* cs = reinterpret_cast<float*>(smem + T_OFF_A);
+        float* sn = cs + TD;
+        if constexpr (DV != TD) {
+            r_tables(DV, cs, sn);
+            __syncthreads();
+        }
         for (int idx = threadIdx.x; idx < TD * TD; idx += blockDim.x) {
             const int n = idx >> 7, k = idx & 127;
-            float v = r_entry(n, k, DV, srht);
+            float v = r_entry(n, k, DV, srht, cs, sn);
             const uint32_t sbit = (k & 1) ? 0x80000000u : 0x8000u;
             if (P.sign_mask[k >> 1] & sbit) v = -v;
             const __half hi = __float2half_rn(v);
@@ -600,10 +619,17 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
 
     {  // B[k][q] = s_k R[n][k] with n = dq_kperm(q) (zero outside d x d), in fp16; and in fp32 for the rebuilds
         const bool srht = P.side[0].transform == SRFTKV_TRANSFORM_SRHT;
+        // angle tables (d < 128) in the output staging buffers, which no epilogue has reached yet
+        float* cs = reinterpret_cast<float*>(smem + DQ_OFF_O);
+        float* sn = cs + TD;
+        if constexpr (DV != TD) {
+            r_tables(DV, cs, sn);
+            __syncthreads();
+        }
         for (int idx = threadIdx.x; idx < TD * TD; idx += blockDim.x) {
             // B row k (output coordinate), K position q holding packed coordinate n
             const int k = idx >> 7, q = idx & 127, n = dq_kperm(q);
-            float v = r_entry(n, k, DV, srht);
+            float v = r_entry(n, k, DV, srht, cs, sn);
             if (P.sign_mask[k >> 1] & ((k & 1) ? 0x80000000u : 0x8000u)) v = -v;
             rbase[idx] = v;
             *reinterpret_cast<__half*>(smem + sw128_offset(k, q)) = __float2half_rn(v);

@@ -78,7 +78,7 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, void* base
 
 bool encode_tiled_swz(CUtensorMap* map, CUtensorMapDataType dt, int rank, void* base, const unsigned long long* dims,
                       const unsigned long long* strides_bytes, const unsigned* box, CUtensorMapSwizzle swz,
-                      const char* what);
+                      const char* what, CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 
 // Tensor-core quantize path (d = 128, group <= 64); returns 1 when the call
 // is not one it handles, else SRFTKV_OK or an error code.
