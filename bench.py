@@ -27,8 +27,8 @@ small; it prints one JSON line with the median event time per launch.
 on the full Gemma-3-1B-shaped cache (0.21 M vectors, 150 MB), and
 --kernel d192_quantize|d192_dequantize (and d256_...) for the d = 192 (256)
 codec on the decode cache shape at that d cut to B=2 (4.2 M vectors, about
-2.2 GB (2.9 GB) held), d80_quantize|d80_dequantize|d80_attention for
-d = 80 and d96_quantize|d96_dequantize for d = 96 on the cuts above.
+2.2 GB (2.9 GB) held); d80_, d96_, d192_ and d256_ cases of quantize,
+dequantize and attention run the same cuts at that head dimension.
 """
 
 from __future__ import annotations
@@ -66,7 +66,7 @@ def parse():
     ap.add_argument("--kernel", default=None,
                     choices=("quantize", "dequantize", "attention", "gemma_quantize", "gemma_dequantize",
                              "d80_quantize", "d80_dequantize", "d80_attention", "d96_quantize", "d96_dequantize",
-                             "d192_quantize", "d192_dequantize",
+                             "d96_attention", "d192_quantize", "d192_dequantize", "d192_attention", "d256_attention",
                              "d256_quantize", "d256_dequantize"),
                     help="profiling case: launch only this kernel on a small workload")
     return ap.parse_args()
@@ -754,14 +754,9 @@ def run_case(args):
     kind = args.kernel.split("_")[-1]
     if args.kernel.startswith("gemma_"):
         w = I.GEMMA
-    elif args.kernel.startswith("d80_"):
-        w = I.DECODE.resized(n_outer=4, tokens=32768, d=80) if attn else I.DECODE.resized(n_outer=2, d=80)
-    elif args.kernel.startswith("d96_"):
-        w = I.DECODE.resized(n_outer=2, d=96)
-    elif args.kernel.startswith("d192_"):
-        w = I.DECODE.resized(n_outer=2, d=192)
-    elif args.kernel.startswith("d256_"):
-        w = I.DECODE.resized(n_outer=2, d=256)
+    elif args.kernel[0] == "d" and args.kernel[1].isdigit():  # d80_, d96_, d192_, d256_ cases
+        dk = int(args.kernel[1:].split("_")[0])
+        w = I.DECODE.resized(n_outer=4, tokens=32768, d=dk) if attn else I.DECODE.resized(n_outer=2, d=dk)
     else:
         w = I.DECODE.resized(n_outer=4, tokens=32768) if attn else I.DECODE.resized(n_outer=2)
     B, Hkv, d, T, Hq, G, seed = w.n_outer, w.kv_heads, w.d, w.tokens, w.q_heads, w.group, w.sign_seed

@@ -146,10 +146,13 @@ __device__ __forceinline__ void quant_store_row(float (&z)[D], int group, uint8_
     float m[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        float a = fabs_(z[16 * u]);
+        // a tree (depth 4, max is exact in any order) rather than a chain of 15 dependent maxima
+        float t[8];
 #pragma unroll
-        for (int i = 1; i < 16; ++i) a = fmax_(a, fabs_(z[16 * u + i]));
-        m[u] = a;
+        for (int i = 0; i < 8; ++i) t[i] = fmax_(fabs_(z[16 * u + i]), fabs_(z[16 * u + i + 8]));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) t[i] = fmax_(t[i], t[i + 4]);
+        m[u] = fmax_(fmax_(t[0], t[2]), fmax_(t[1], t[3]));
     }
 #pragma unroll
     for (int s = 1; s < U; s <<= 1) {
