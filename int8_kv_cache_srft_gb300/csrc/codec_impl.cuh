@@ -42,13 +42,36 @@ struct CodecSideK {
     int sbytes;     // bytes per stored scale
 };
 
+// Division by a divisor fixed for a launch, as a multiply and a shift
+// (Granlund & Montgomery, "Division by invariant integers using
+// multiplication", 1994: the round-up multiplier m = floor(2^32 (2^s - d) / d)
+// + 1 with s = ceil(log2 d), q = (mulhi(n, m) + n) >> s), exact for
+// 0 <= n < 2^31.  The tile index decode runs in every epilogue unit and
+// converter warp; a runtime integer division there is a sequence of some
+// twenty instructions.
+struct FastDiv {
+    uint32_t mul;
+    int shift;
+};
+static inline FastDiv make_fastdiv(uint32_t d) {  // d >= 1
+    int s = 0;
+    while ((1ull << s) < d) ++s;
+    FastDiv f;
+    f.mul = (uint32_t)(((1ull << 32) * ((1ull << s) - d)) / d + 1);
+    f.shift = s;
+    return f;
+}
+__device__ __forceinline__ uint32_t fastdiv(uint32_t n, FastDiv f) { return (__umulhi(n, f.mul) + n) >> f.shift; }
+
 struct CodecParams {
     CodecSideK side[2];
     int n_outer, H, t_cap, t_offset, group;
+    int lg_group;         // log2(group)
     int n_tokens;
     int tiles_per_head;   // ceil(n_tokens / rows per tile)
     int tiles_per_side;   // n_outer * H * tiles_per_head
     int total_tiles;      // n_sides * tiles_per_side
+    FastDiv div_side, div_head, div_H;  // by tiles_per_side, tiles_per_head, H
     unsigned int* fault;  // device fault word (bit 0: a bounded wait gave up)
     uint32_t sign_mask[128];
 };
@@ -77,11 +100,11 @@ struct TileId {
 template <int ROWS>
 __device__ __forceinline__ TileId decode_tile(const CodecParams& P, int t) {
     TileId id;
-    id.side = t / P.tiles_per_side;
+    id.side = (int)fastdiv((uint32_t)t, P.div_side);
     const int rem = t - id.side * P.tiles_per_side;
-    const int oh = rem / P.tiles_per_head;
+    const int oh = (int)fastdiv((uint32_t)rem, P.div_head);
     id.t0 = (rem - oh * P.tiles_per_head) * ROWS;
-    id.o = oh / P.H;
+    id.o = (int)fastdiv((uint32_t)oh, P.div_H);
     id.h = oh - id.o * P.H;
     return id;
 }
@@ -512,6 +535,16 @@ __global__ void __launch_bounds__(128, Geo<D>::MIN_BLOCKS)
     if (lane == 0) ptx::bulk_wait<0>();
 }
 
+// Tiles of `rows` tokens: counts per head, side and call, and their divisors.
+static inline void set_tile_grid(const CodecCall& c, CodecParams& P, int rows) {
+    P.tiles_per_head = (c.n_tokens + rows - 1) / rows;
+    P.tiles_per_side = c.n_outer * c.H * P.tiles_per_head;
+    P.total_tiles = c.n_sides * P.tiles_per_side;
+    P.div_side = make_fastdiv(P.tiles_per_side > 0 ? (uint32_t)P.tiles_per_side : 1u);
+    P.div_head = make_fastdiv(P.tiles_per_head > 0 ? (uint32_t)P.tiles_per_head : 1u);
+    P.div_H = make_fastdiv((uint32_t)c.H);
+}
+
 static inline void fill_params(const CodecCall& c, CodecParams& P) {
     for (int s = 0; s < 2; ++s) {
         const CodecSideDesc& d = c.side[s < c.n_sides ? s : 0];
@@ -531,9 +564,9 @@ static inline void fill_params(const CodecCall& c, CodecParams& P) {
     P.t_offset = c.t_offset;
     P.group = c.group;
     P.n_tokens = c.n_tokens;
-    P.tiles_per_head = (c.n_tokens + 31) / 32;
-    P.tiles_per_side = c.n_outer * c.H * P.tiles_per_head;
-    P.total_tiles = c.n_sides * P.tiles_per_side;
+    P.lg_group = 0;
+    while ((1 << P.lg_group) < c.group) ++P.lg_group;
+    set_tile_grid(c, P, 32);
     for (int i = 0; i < 128; ++i) P.sign_mask[i] = 0;
     sign_masks(c.d, c.seed, P.sign_mask);
 }

@@ -696,9 +696,7 @@ int launch_pair(const CodecCall& c) {
     }
     CodecParams P;
     fill_params(c, P);
-    P.tiles_per_head = (c.n_tokens + PR_ROWS - 1) / PR_ROWS;
-    P.tiles_per_side = c.n_outer * c.H * P.tiles_per_head;
-    P.total_tiles = c.n_sides * P.tiles_per_side;
+    set_tile_grid(c, P, PR_ROWS);
     if (P.total_tiles == 0) return 0;
     CUtensorMap tm[2];
     for (int s = 0; s < 2; ++s) {

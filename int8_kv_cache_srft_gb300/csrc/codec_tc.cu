@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
             const int t_tok = id.t0 + 32 * quarter + lane;
             if (t_tok >= P.n_tokens) return true;
             const long long vrow = packed_row(P, id, t_tok);
-            const int ng = DV / P.group;
+            const int ng = DV >> P.lg_group;
             // the unit's columns 32 cq .. +W-1 (W = 32, or 16 for the last quarter at d = 80); at d = 80 the
             // code rows (40 or 80 bytes) and scale rows (5 scales) allow only narrow stores
             auto finish = [&](auto wc) {
@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
                         z[4 * c + 3] *= l.w;
                     }
                 }
-                uint8_t* srow = S.scales + (vrow * ng + (32 * cq) / P.group) * S.sbytes;
+                uint8_t* srow = S.scales + (vrow * ng + ((32 * cq) >> P.lg_group)) * S.sbytes;
                 if (BK == BV || id.side == 0)
                     quant_store_row<W, BK, SF, 0, NARROW>(z, P.group, S.codes + vrow * (DV * BK / 8) + cq * (32 * BK / 8),
                                                           srow);
@@ -935,9 +935,7 @@ static int launch_dq_tc(const CodecCall& c) {
     using C = DqCfg<BK, BV>;
     CodecParams P;
     fill_params(c, P);
-    P.tiles_per_head = (c.n_tokens + TM - 1) / TM;
-    P.tiles_per_side = c.n_outer * c.H * P.tiles_per_head;
-    P.total_tiles = c.n_sides * P.tiles_per_side;
+    set_tile_grid(c, P, TM);
     P.fault = codec_fault_word();
     if (!P.fault) return SRFTKV_ERR_CUDA;
     DqMaps M;
@@ -1004,9 +1002,7 @@ template <int BK, int BV, int SF, int DV>
 static int launch_tc(const CodecCall& c) {
     CodecParams P;
     fill_params(c, P);
-    P.tiles_per_head = (c.n_tokens + TM - 1) / TM;
-    P.tiles_per_side = c.n_outer * c.H * P.tiles_per_head;
-    P.total_tiles = c.n_sides * P.tiles_per_side;
+    set_tile_grid(c, P, TM);
     P.fault = codec_fault_word();
     if (!P.fault) return SRFTKV_ERR_CUDA;
     CUtensorMap tm[2];

@@ -264,8 +264,8 @@ __global__ void __launch_bounds__(wide::WARPS * 32, 1)
                     }
                 }
                 const long long vrow = packed_row(P, id, t_tok);
-                const int ng = DV / P.group;
-                uint8_t* srow = S.scales + (vrow * ng + c0 / P.group) * S.sbytes;
+                const int ng = DV >> P.lg_group;
+                uint8_t* srow = S.scales + (vrow * ng + (c0 >> P.lg_group)) * S.sbytes;
                 if (BK == BV || id.side == 0)
                     quant_store_row<32, BK, SF, wide::RLOG2>(z, P.group, S.codes + vrow * (DV * BK / 8) + c0 * BK / 8,
                                                              srow);
@@ -287,9 +287,7 @@ static int launch_tc_wide(const CodecCall& c) {
     using C = wide::Cfg<DV, NSPLIT>;
     CodecParams P;
     fill_params(c, P);
-    P.tiles_per_head = (c.n_tokens + wide::M - 1) / wide::M;
-    P.tiles_per_side = c.n_outer * c.H * P.tiles_per_head;
-    P.total_tiles = c.n_sides * P.tiles_per_side;
+    set_tile_grid(c, P, wide::M);
     P.fault = codec_fault_word();
     if (!P.fault) return SRFTKV_ERR_CUDA;
     CUtensorMap tm[2];
@@ -723,9 +721,7 @@ static int launch_dq_tc_wide(const CodecCall& c) {
     using C = wide::DqCfg<DV, BK, BV>;
     CodecParams P;
     fill_params(c, P);
-    P.tiles_per_head = (c.n_tokens + wide::M - 1) / wide::M;
-    P.tiles_per_side = c.n_outer * c.H * P.tiles_per_head;
-    P.total_tiles = c.n_sides * P.tiles_per_side;
+    set_tile_grid(c, P, wide::M);
     P.fault = codec_fault_word();
     if (!P.fault) return SRFTKV_ERR_CUDA;
     WideDqMaps Mp;
