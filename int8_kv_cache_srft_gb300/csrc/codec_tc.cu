@@ -357,7 +357,7 @@ struct DqCfg {
 __device__ __forceinline__ void half_row_scales(const uint8_t* __restrict__ in, int off_sc, int m, int hf, int group,
                                                 int sfmt, float (&sc)[4]) {
     if (sfmt == SRFTKV_SCALE_FP32) {
-        const int srb = 4 * (TD / group);
+        const int srb = 4 * (TD >> (__ffs(group) - 1));  // group: a power of two (a shift, not a division)
         if (group == 16) {  // groups 4hf .. 4hf+3: chunk hf of the 32-byte row
             const float4 v = *reinterpret_cast<const float4*>(in + off_sc + m * srb + (swz16(srb, m, hf) << 4));
             sc[0] = v.x;
@@ -371,7 +371,7 @@ __device__ __forceinline__ void half_row_scales(const uint8_t* __restrict__ in, 
         }
         return;
     }
-    const uint8_t* row = in + off_sc + m * (TD / group) * (sfmt == SRFTKV_SCALE_FP16 ? 2 : 1);
+    const uint8_t* row = in + off_sc + m * (TD >> (__ffs(group) - 1)) * (sfmt == SRFTKV_SCALE_FP16 ? 2 : 1);
     if (sfmt == SRFTKV_SCALE_FP16) {
         if (group == 16) {
             const uint2 h = *reinterpret_cast<const uint2*>(row + 8 * hf);
@@ -482,12 +482,13 @@ __device__ __forceinline__ void d96_half_words(const uint8_t* __restrict__ in, i
 // The scales of half hf's three 16-coordinate units 2hf, 2hf+1, 4+hf (flat rows of 96/group scales)
 __device__ __forceinline__ void d96_half_scales(const uint8_t* __restrict__ in, int off_sc, int m, int hf, int group,
                                                 int sfmt, float (&sc)[3]) {
-    const int ng = 96 / group, sb = sfmt == SRFTKV_SCALE_FP32 ? 4 : sfmt == SRFTKV_SCALE_FP16 ? 2 : 1;
+    const int lg = __ffs(group) - 1;  // group: a power of two
+    const int ng = 96 >> lg, sb = sfmt == SRFTKV_SCALE_FP32 ? 4 : sfmt == SRFTKV_SCALE_FP16 ? 2 : 1;
     const uint8_t* row = in + off_sc + m * ng * sb;
     const int units[3] = {2 * hf, 2 * hf + 1, 4 + hf};
 #pragma unroll
     for (int u = 0; u < 3; ++u) {
-        const int gi = 16 * units[u] / group;
+        const int gi = (16 * units[u]) >> lg;
         if (sfmt == SRFTKV_SCALE_FP32) sc[u] = *reinterpret_cast<const float*>(row + 4 * gi);
         else if (sfmt == SRFTKV_SCALE_FP16) sc[u] = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(row + 2 * gi)));
         else sc[u] = __uint_as_float((uint32_t)row[gi] << 23);
@@ -761,7 +762,7 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
                     continue;
                 }
                 // fp32 scales as rows of the tile; fp16 / e8m0 scales as the tile's bytes in rows of 16
-                const int sb = P.side[id.side].sbytes, ng = DV / P.group, sc_bytes = TM * ng * sb;
+                const int sb = P.side[id.side].sbytes, ng = DV >> P.lg_group, sc_bytes = TM * ng * sb;
                 const bool flat = !(sb == 4 && DV == TD);  // scale rows copied as 16-byte rows of bytes
                 ptx::mbar_arrive_expect_tx(bar(IN_FULL + st), TM * (DV * bits / 8) + sc_bytes);
                 ptx::tma_load_3d(dst, &M.codes[id.side], bar(IN_FULL + st), 0, row, oh);

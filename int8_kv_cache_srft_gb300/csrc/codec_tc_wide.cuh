@@ -378,7 +378,8 @@ __device__ __forceinline__ uint32_t code_chunk(int rb, int m, int c) {
 // group 16, 32 for group 32), every other plane as its contiguous bytes (rows of ng * sb bytes)
 template <int DV>
 __device__ __forceinline__ float unit_scale(const uint8_t* __restrict__ in, int m, int u, int group, int sfmt) {
-    const int gi = (16 * u) / group, ng = DV / group;
+    const int lg = __ffs(group) - 1;  // group: a power of two
+    const int gi = (16 * u) >> lg, ng = DV >> lg;
     if (sfmt == SRFTKV_SCALE_FP32) {
         if constexpr (DV == 256) {
             const int srb = 4 * ng, b = 4 * gi;
@@ -398,7 +399,7 @@ __device__ __forceinline__ float unit_scale(const uint8_t* __restrict__ in, int 
 template <int DV, int NU>
 __device__ __forceinline__ void unit_scales(const uint8_t* __restrict__ in, int m, int u0, int group, int sfmt,
                                             float (&sc)[NU]) {
-    const int ng = DV / group;
+    const int ng = DV >> (__ffs(group) - 1);  // group: a power of two
     if (sfmt == SRFTKV_SCALE_FP32 && group == 16) {
         if constexpr (DV == 256) {  // 64-byte rows, 64-byte swizzle; u0 a multiple of 4
             const int srb = 64;
@@ -585,7 +586,7 @@ __global__ void __launch_bounds__(wide::DQ_WARPS * 32, 1)
                 const uint32_t dst = sbase + C::OFF_IN + st * C::STAGE;
                 const int row = P.t_offset + id.t0;  // packed planes: [outer*H][t_cap] rows
                 const int oh = id.o * P.H + id.h;
-                const int sb = P.side[id.side].sbytes, ng = DV / P.group;
+                const int sb = P.side[id.side].sbytes, ng = DV >> P.lg_group;
                 // fp32 scale rows of d = 256 through the tensor map (swizzled rows); every other plane as the
                 // tile's contiguous bytes by a plain bulk copy that stops at the end of this (outer, head)
                 const bool flat = !(sb == 4 && DV == 256);
