@@ -443,6 +443,9 @@ __global__ void __launch_bounds__(128, Geo<D>::MIN_BLOCKS)
         if (!ok) {
             if (lane == 0) {
                 atomicOr(P.fault, 1u);
+                // let this warp's copies in flight land before it leaves: the stage whose wait gave up and the
+                // one issued after it (each wait bounded, so the warp still returns)
+                ptx::mbar_wait_bounded(b ? bar1 : bar0, (it >> 1) & 1, 1u << 16);
                 if (has_next) ptx::mbar_wait_bounded(b ? bar0 : bar1, ((it + 1) >> 1) & 1, 1u << 16);
             }
             return;
