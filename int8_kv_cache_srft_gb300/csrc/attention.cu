@@ -191,7 +191,11 @@ struct AttnCfg {
     static constexpr bool QK = BK != 16, QV = BV != 16;
     static constexpr int SRB = D / 4;  // largest scale row in bytes (group 16); exact rows, no padding
     static constexpr int STAGE32 = 32 * (PlaneT<D, BK>::RP + PlaneT<D, BV>::RP + (QK ? SRB : 0) + (QV ? SRB : 0));
-    static constexpr int CH = SRFTKV_ATTN_CH ? SRFTKV_ATTN_CH : (STAGE32 <= 9216 ? 32 : 16);  // tokens per chunk
+    // d = 192 with stages of at most 13.5 KB: 32-token chunks at 2 CTAs an SM (no register spills either)
+    // beat 16-token chunks at 3 (1.04 against 1.13 ms on the decode shape); d = 256 keeps 16 (1.48 against 1.79)
+    static constexpr bool WIDE32 = D == 192 && STAGE32 <= 13824;
+    static constexpr int CH = SRFTKV_ATTN_CH ? SRFTKV_ATTN_CH : (STAGE32 <= 9216 || WIDE32 ? 32 : 16);  // tokens per chunk
+    static constexpr int MINB = D >= 256 || WIDE32 ? 2 : 3;  // CTAs an SM the kernel is compiled for
     static constexpr int NS = SRFTKV_ATTN_STAGES;
     // swizzled sub-buffers (code rows of <= 128 bytes, group-16 scale rows of
     // >= 32 bytes) start on a 1024-byte boundary, the others on 128 bytes
@@ -1061,9 +1065,10 @@ __device__ __forceinline__ void acc_coord_pair(int i, int g, int c, int& dim, in
 // carry four heads); GQA ratios above four run as several head groups, whose
 // CTAs sit next to each other in the launch order so that the second one's
 // reads of the same cache rows are mostly L2 hits.
-// d = 256 keeps 2 CTAs per SM: its fragments need more than a third of the register file
+// d = 256 keeps 2 CTAs per SM (its fragments need more than a third of the register file), and so does
+// d = 192 with 32-token chunks (their stages fit two CTAs' shared memory); every other instance 3
 template <int D, int BK, int BV, int G>
-__global__ void __launch_bounds__(kAttnWarps * 32, D >= 256 ? 2 : 3)
+__global__ void __launch_bounds__(kAttnWarps * 32, AttnCfg<D, BK, BV>::MINB)
     q4kv_attn_split_kernel(const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_ks,
                            const __grid_constant__ CUtensorMap tm_vc, const __grid_constant__ CUtensorMap tm_vs,
                            const __grid_constant__ AttnParams P) {
