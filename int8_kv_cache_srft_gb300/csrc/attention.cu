@@ -195,7 +195,7 @@ struct AttnCfg {
     // beat 16-token chunks at 3 (1.04 against 1.13 ms on the decode shape); d = 256 keeps 16 (1.48 against 1.79)
     static constexpr bool WIDE32 = D == 192 && STAGE32 <= 13824;
     static constexpr int CH = SRFTKV_ATTN_CH ? SRFTKV_ATTN_CH : (STAGE32 <= 9216 || WIDE32 ? 32 : 16);  // tokens per chunk
-    static constexpr int MINB = D >= 256 || WIDE32 ? 2 : 3;  // CTAs an SM the kernel is compiled for
+    static constexpr int MINB = D >= 256 || WIDE32 ? 2 : (D == 96 && BK == 4 && BV == 4) ? 4 : 3;  // CTAs an SM the kernel is compiled for
     static constexpr int NS = SRFTKV_ATTN_STAGES;
     // swizzled sub-buffers (code rows of <= 128 bytes, group-16 scale rows of
     // >= 32 bytes) start on a 1024-byte boundary, the others on 128 bytes
