@@ -28,7 +28,10 @@ on the full Gemma-3-1B-shaped cache (0.21 M vectors, 150 MB), and
 --kernel d192_quantize|d192_dequantize (and d256_...) for the d = 192 (256)
 codec on the decode cache shape at that d cut to B=2 (4.2 M vectors, about
 2.2 GB (2.9 GB) held); d80_, d96_, d192_ and d256_ cases of quantize,
-dequantize and attention run the same cuts at that head dimension.
+dequantize and attention run the same cuts at that head dimension;
+long_attention runs attention on B=4 at the full T=131072 with 8 splits (512
+chunks a split, so the per-split work weighs as little as on the full
+decode workload; an 805 MB packed cache).
 """
 
 from __future__ import annotations
@@ -67,6 +70,7 @@ def parse():
                     choices=("quantize", "dequantize", "attention", "gemma_quantize", "gemma_dequantize",
                              "d80_quantize", "d80_dequantize", "d80_attention", "d96_quantize", "d96_dequantize",
                              "d96_attention", "d192_quantize", "d192_dequantize", "d192_attention", "d256_attention",
+                             "long_attention",
                              "d256_quantize", "d256_dequantize"),
                     help="profiling case: launch only this kernel on a small workload")
     return ap.parse_args()
@@ -756,6 +760,8 @@ def run_case(args):
     kind = args.kernel.split("_")[-1]
     if args.kernel.startswith("gemma_"):
         w = I.GEMMA
+    elif args.kernel == "long_attention":  # long splits: 4 x 131072 tokens, 8 splits per (sequence, kv head)
+        w = I.DECODE.resized(n_outer=4)
     elif args.kernel[0] == "d" and args.kernel[1].isdigit():  # d80_, d96_, d192_, d256_ cases
         dk = int(args.kernel[1:].split("_")[0])
         w = I.DECODE.resized(n_outer=4, tokens=32768, d=dk) if attn else I.DECODE.resized(n_outer=2, d=dk)
@@ -780,11 +786,12 @@ def run_case(args):
         sk.x = sv.x = None
         q = I.query(w, device="cuda")
         out = torch.empty((B, Hq, d), dtype=torch.float32, device="cuda")
-        ws = torch.empty(K.q4kv_decode_attention_workspace_size(B, Hq, Hkv, d, T, 0), dtype=torch.uint8,
+        ns = 8 if args.kernel == "long_attention" else 0
+        ws = torch.empty(K.q4kv_decode_attention_workspace_size(B, Hq, Hkv, d, T, ns), dtype=torch.uint8,
                          device="cuda")
 
         def launch():
-            K.q4kv_decode_attention(q, out, sk, sv, B, Hq, Hkv, d, G, T, None, 0.0, seed, 0, ws)
+            K.q4kv_decode_attention(q, out, sk, sv, B, Hq, Hkv, d, G, T, None, 0.0, seed, ns, ws)
     for _ in range(args.warmup):
         launch()
     torch.cuda.synchronize()

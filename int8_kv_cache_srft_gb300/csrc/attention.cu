@@ -135,9 +135,15 @@ __device__ __forceinline__ void split_h2(float a, float b, uint32_t& hi, uint32_
 // next to the signal that nothing is lost to cancellation; the unit 2^-24 is
 // folded into the score and output scaling.
 constexpr float kSub = 16777216.f;  // 2^24
-__device__ __forceinline__ uint32_t u4_lo(uint32_t w) { return (w & 0x000F000Fu) ^ 0x00080008u; }  // nibbles 0, 16
-__device__ __forceinline__ uint32_t u4_hi(uint32_t w) { return (w & 0x00F000F0u) ^ 0x00800080u; }  // nibbles 4, 20
-__device__ __forceinline__ uint32_t u8_lo(uint32_t w) { return (w & 0x00FF00FFu) ^ 0x00800080u; }  // bytes 0, 2
+// The XOR to offset binary is taken once per loaded word (ob4 / ob8: every
+// nibble or byte at once, and it commutes with the >> 8 of the second pair),
+// so each extraction is a single AND: (w & m) ^ (0x8.. & m) as one logic op
+// would need two immediate operands, which one LOP3 cannot take.
+__device__ __forceinline__ uint32_t ob4(uint32_t w) { return w ^ 0x88888888u; }  // int4 nibbles -> offset binary
+__device__ __forceinline__ uint32_t ob8(uint32_t w) { return w ^ 0x80808080u; }  // int8 bytes -> offset binary
+__device__ __forceinline__ uint32_t u4_lo(uint32_t wx) { return wx & 0x000F000Fu; }  // nibbles 0, 16 of ob4(w)
+__device__ __forceinline__ uint32_t u4_hi(uint32_t wx) { return wx & 0x00F000F0u; }  // nibbles 4, 20 of ob4(w)
+__device__ __forceinline__ uint32_t u8_lo(uint32_t wx) { return wx & 0x00FF00FFu; }  // bytes 0, 2 of ob8(w)
 __device__ __forceinline__ float h2_sum(uint32_t h) {
     const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
     return f.x + f.y;
@@ -528,6 +534,8 @@ __device__ __forceinline__ void tile_scores(uint32_t kc, const LaneRow& LK, cons
         float a0 = 0.f, a1 = 0.f;
         // 32-dim chunk mm from its two 8-row matrices (rows 0-7, rows 8-15)
         auto chunk = [&](int mm, uint32_t rg, uint32_t rg8) {
+            rg = ob4(rg);
+            rg8 = ob4(rg8);
             const uint32_t rs = rg >> 8, rs8 = rg8 >> 8;
             const uint32_t x0 = u4_lo(rg), x1 = u4_lo(rg8), x2 = u4_hi(rg), x3 = u4_hi(rg8);
             const uint32_t y0 = u4_lo(rs), y1 = u4_lo(rs8), y2 = u4_hi(rs), y3 = u4_hi(rs8);
@@ -564,7 +572,7 @@ __device__ __forceinline__ void tile_scores(uint32_t kc, const LaneRow& LK, cons
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 const int mm = 2 * m2 + hh;
-                const uint32_t rg = r[2 * hh], rg8 = r[2 * hh + 1];
+                const uint32_t rg = ob8(r[2 * hh]), rg8 = ob8(r[2 * hh + 1]);
                 const uint32_t x0 = u8_lo(rg), x1 = u8_lo(rg8), x2 = u8_lo(rg >> 8), x3 = u8_lo(rg8 >> 8);
                 float d[4];
                 mma16816_c(d, x0, x1, x2, x3, qh[2 * mm], qh[2 * mm + 1], nb[mm], 0.f);
@@ -578,6 +586,8 @@ __device__ __forceinline__ void tile_scores(uint32_t kc, const LaneRow& LK, cons
             constexpr int mm = D / 16 - 1;
             uint32_t r[2];
             ldsm_x2(plane_addr<PK::RB, PK::SWZ, PK::RP>(kc, LK, tr, mm), r);
+            r[0] = ob8(r[0]);
+            r[1] = ob8(r[1]);
             const uint32_t x0 = u8_lo(r[0]), x1 = u8_lo(r[1]), x2 = u8_lo(r[0] >> 8), x3 = u8_lo(r[1] >> 8);
             float d[4];
             mma16816_c(d, x0, x1, x2, x3, qh[2 * mm], qh[2 * mm + 1], nb[mm], 0.f);
@@ -618,6 +628,8 @@ __device__ __forceinline__ void tile_scores_pair(uint32_t kc, const LaneRow& LK,
     const float* ks = reinterpret_cast<const float*>(ksb);
     float a[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // [pair g | g + 8][token parity]
     auto seg = [&](int sg, uint32_t rg, uint32_t rg8) {
+        rg = ob4(rg);
+        rg8 = ob4(rg8);
         const uint32_t rs = rg >> 8, rs8 = rg8 >> 8;
         const uint32_t x0 = u4_lo(rg), x1 = u4_lo(rg8), x2 = u4_hi(rg), x3 = u4_hi(rg8);
         const uint32_t y0 = u4_lo(rs), y1 = u4_lo(rs8), y2 = u4_hi(rs), y3 = u4_hi(rs8);
@@ -689,6 +701,8 @@ __device__ __forceinline__ void tile_pv(uint32_t vc, const LaneRow& LV, const ui
             uint32_t bh0, bl0, bh1, bl1;
             split_h2(b00, b10, bh0, bl0);
             split_h2(b01, b11, bh1, bl1);
+            R0 = ob4(R0);
+            R1 = ob4(R1);
             const uint32_t S0 = R0 >> 8, S1 = R1 >> 8;
             float(&a0)[4] = *reinterpret_cast<float(*)[4]>(&acc[8 * cb]);
             float(&a1)[4] = *reinterpret_cast<float(*)[4]>(&acc[8 * cb + 4]);
@@ -733,7 +747,7 @@ __device__ __forceinline__ void tile_pv(uint32_t vc, const LaneRow& LV, const ui
                 uint32_t bh0, bl0, bh1, bl1;
                 split_h2(b00, b10, bh0, bl0);
                 split_h2(b01, b11, bh1, bl1);
-                const uint32_t R0 = r[2 * hh], R1 = r[2 * hh + 1];
+                const uint32_t R0 = ob8(r[2 * hh]), R1 = ob8(r[2 * hh + 1]);
                 float(&a0)[4] = *reinterpret_cast<float(*)[4]>(&acc[4 * cb]);
                 const uint32_t x0 = u8_lo(R0), x1 = u8_lo(R0 >> 8), x2 = u8_lo(R1), x3 = u8_lo(R1 >> 8);
                 mma16816(a0, x0, x1, x2, x3, bh0, bh1);
@@ -753,6 +767,8 @@ __device__ __forceinline__ void tile_pv(uint32_t vc, const LaneRow& LV, const ui
             split_h2(b00, b10, bh0, bl0);
             split_h2(b01, b11, bh1, bl1);
             float(&a0)[4] = *reinterpret_cast<float(*)[4]>(&acc[4 * cb]);
+            r[0] = ob8(r[0]);
+            r[1] = ob8(r[1]);
             const uint32_t x0 = u8_lo(r[0]), x1 = u8_lo(r[0] >> 8), x2 = u8_lo(r[1]), x3 = u8_lo(r[1] >> 8);
             mma16816(a0, x0, x1, x2, x3, bh0, bh1);
             mma16816(a0, x0, x1, x2, x3, bl0, bl1);
@@ -808,6 +824,8 @@ __device__ __forceinline__ void tile_pv_pair(uint32_t vc, const LaneRow& LV, con
         uint32_t bh0, bl0, bh1, bl1;
         split_h2(b00, b10, bh0, bl0);
         split_h2(b01, b11, bh1, bl1);
+        R0 = ob4(R0);
+        R1 = ob4(R1);
         const uint32_t S0 = R0 >> 8, S1 = R1 >> 8;
         float(&a0)[4] = *reinterpret_cast<float(*)[4]>(&acc[8 * sg]);
         float(&a1)[4] = *reinterpret_cast<float(*)[4]>(&acc[8 * sg + 4]);
