@@ -555,6 +555,13 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         hout = torch.empty_like(out, device="cpu").pin_memory()
         h2d = hk.numel() * 2 + hv.numel() * 2 + hq.numel() * 2
         d2h = hout.numel() * 4
+        # one untimed step first, as for every other timed loop: the first copies out of freshly pinned
+        # buffers run slower than the link's steady rate
+        xk.copy_(hk, non_blocking=True)
+        xv.copy_(hv, non_blocking=True)
+        q.copy_(hq, non_blocking=True)
+        step(False)
+        hout.copy_(out, non_blocking=True)
         barrier()
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
