@@ -224,8 +224,8 @@ int q4kv_decode_attention(const void* q, float* out, const srftkv_side* k, const
  *    until the workspace (q4kv_decode_attention_workspace_size) fits in
  *    SRFTKV_STATIC_SCRATCH_BYTES; sizes whose workspace exceeds it even so
  *    (or with the n_splits given) are rejected with SRFTKV_ERR_INVALID.  The
- *    automatic choice at B=16, Hq=32, d=128 on a 152-SM GB300 needs about
- *    8 MB and is not lowered.
+ *    automatic choice at B=16, Hq=32, d=128 on a 152-SM GB300 (19 splits)
+ *    needs about 5.3 MB and is not lowered.
  *  - The first call in a CUDA context (for the runtime's primary context:
  *    the first call on a device) looks up the array's device address with
  *    that device current and caches it under the context's ID; make that

@@ -31,6 +31,7 @@
 // hi + lo and contracted twice, which keeps the products at ~22-bit accuracy.
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstring>
@@ -50,6 +51,7 @@ static std::atomic<int> g_poll_limit{-1};
 void attention_set_poll_limit(int polls) { g_poll_limit.store(polls < 0 ? -1 : polls); }
 
 constexpr int kAttnWarps = 4;
+constexpr int kFoldChunks = 64;  // a warp folds the V code offset out of its accumulators this often (a power of two)
 #ifndef SRFTKV_ATTN_STAGES
 #define SRFTKV_ATTN_STAGES 2  // TMA stages per warp (chunks in flight + 1)
 #endif
@@ -118,12 +120,30 @@ __device__ __forceinline__ void mma16816_c(float (&d)[4], uint32_t a0, uint32_t 
 // (a, b) ~= hi + lo with both halves fp16: the MMA then sees a and b to about
 // 22 bits instead of 11 (codes are exact in fp16, so this is the only rounding
 // of the contraction inputs).
+// The residuals a - hi.x and b - hi.y are exact in fp32 (hi is a rounding of
+// them to 11 bits); each is one mixed-precision FMA, hi.x * -1 + a, with the
+// fp16 half taken straight from the packed register instead of a widening
+// convert and a subtraction.
 __device__ __forceinline__ void split_h2(float a, float b, uint32_t& hi, uint32_t& lo) {
     const __half2 h = __floats2half2_rn(a, b);
-    const float2 f = __half22float2(h);
-    const __half2 l = __floats2half2_rn(a - f.x, b - f.y);
     hi = *reinterpret_cast<const uint32_t*>(&h);
+    float ra, rb;
+    asm("{\n\t.reg .f16 hx, hy, m1;\n\t"
+        "mov.b32 {hx, hy}, %2;\n\t"
+        "mov.b16 m1, 0xBC00;\n\t"
+        "fma.rn.f32.f16 %0, hx, m1, %3;\n\t"
+        "fma.rn.f32.f16 %1, hy, m1, %4;\n\t}"
+        : "=f"(ra), "=f"(rb)
+        : "r"(hi), "f"(a), "f"(b));
+    const __half2 l = __floats2half2_rn(ra, rb);
     lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+// Packed fp32 (one instruction for two lanes of work; IEEE rounding per lane).
+__device__ __forceinline__ float2 mul2(float a0, float a1, float b0, float b1) {
+    return __fmul2_rn(make_float2(a0, a1), make_float2(b0, b1));
+}
+__device__ __forceinline__ float2 fma2(float a0, float a1, float b0, float b1, float2 c) {
+    return __ffma2_rn(make_float2(a0, a1), make_float2(b0, b1), c);
 }
 
 // Codes -> fp16 pairs in one logic op.  Bits 0xF/0xF0000 (0xF0/0xF00000)
@@ -239,120 +259,148 @@ struct AttnCfg {
 // ---------------------------------------------------------------------------
 // 1. q preparation
 // ---------------------------------------------------------------------------
-template <int D, bool ROT>
-__global__ void __launch_bounds__(128) attn_prep_q_kernel(const __grid_constant__ AttnParams P) {
-    constexpr int N = D / 2;
+// fp16 cache (no rotation): q times the softmax scale, one thread per row.
+template <int D>
+__global__ void __launch_bounds__(128) attn_prep_q_raw_kernel(const __grid_constant__ AttnParams P) {
     const int row = blockIdx.x * 128 + threadIdx.x;
     if (row >= P.B * P.Hq) return;
-    const int b = row / P.Hq, hq = row - b * P.Hq, hkv = hq / P.rep;
     const uint4* xr = reinterpret_cast<const uint4*>(P.q + (long long)row * D);
     float4* yr = reinterpret_cast<float4*>(P.qt + (long long)row * D);
-    float p[D];
-    if constexpr (ROT) {
-        float zr[N], zi[N];
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-            const uint4 v = __ldg(xr + c);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const uint32_t s = w[e] ^ P.sign_mask[4 * c + e];
-                zr[4 * c + e] = __half2float(__ushort_as_half((unsigned short)(s & 0xFFFFu)));
-                zi[4 * c + e] = __half2float(__ushort_as_half((unsigned short)(s >> 16)));
-            }
-        }
-        if (P.tr_k == SRFTKV_TRANSFORM_SRHT) {
-            wht_pairs<N>(zr, zi);
-#pragma unroll
-            for (int n = 0; n < N; ++n) {
-                p[2 * n] = zr[n] * SplitConst<D>::inv_sqrt_d;
-                p[2 * n + 1] = zi[n] * SplitConst<D>::inv_sqrt_d;
-            }
-        } else {
-            fft<N, false>(zr, zi);
-            split_forward<D>(zr, zi, p);
-        }
-    } else {
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-            const uint4 v = __ldg(xr + c);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-                p[8 * c + 2 * e] = f.x;
-                p[8 * c + 2 * e + 1] = f.y;
-            }
-        }
+#pragma unroll 4
+    for (int c = 0; c < D / 8; ++c) {
+        const uint4 v = __ldg(xr + c);
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
+        const float2 bq = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+        const float2 cc = __half22float2(*reinterpret_cast<const __half2*>(&v.z));
+        const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&v.w));
+        yr[2 * c] = make_float4(a.x * P.qscale, a.y * P.qscale, bq.x * P.qscale, bq.y * P.qscale);
+        yr[2 * c + 1] = make_float4(cc.x * P.qscale, cc.y * P.qscale, dd.x * P.qscale, dd.y * P.qscale);
     }
-    if (ROT && P.lam_k != nullptr) {
-        const float4* lr = reinterpret_cast<const float4*>(P.lam_k + (long long)b * P.lam_k_stride + (long long)hkv * D);
-#pragma unroll
-        for (int c = 0; c < D / 4; ++c) {
-            const float4 l = __ldg(lr + c);
-            p[4 * c] *= P.qscale * __frcp_rn(l.x);
-            p[4 * c + 1] *= P.qscale * __frcp_rn(l.y);
-            p[4 * c + 2] *= P.qscale * __frcp_rn(l.z);
-            p[4 * c + 3] *= P.qscale * __frcp_rn(l.w);
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < D; ++i) p[i] *= P.qscale;
-    }
-#pragma unroll
-    for (int c = 0; c < D / 4; ++c) yr[c] = make_float4(p[4 * c], p[4 * c + 1], p[4 * c + 2], p[4 * c + 3]);
 }
 
-// Entry (n, k) of the packed unitary DFT R of length D (n the packed output
-// coordinate, k the input coordinate) from tables of cos / sin(2 pi m/D):
-// rows 0 and 1 are the real DC and Nyquist terms, rows 2j and 2j+1 the real
-// and imaginary parts of frequency j, times sqrt(2) for unitarity.
+// The packed unitary DFT R of length D (the SRFT's rotation, R diag(s)):
+// row 0 is the DC term 1/sqrt(D), row 1 the Nyquist term (-1)^k / sqrt(D),
+// rows 2f and 2f+1 (0 < f < D/2) sqrt(2/D) cos(2 pi f k / D) and
+// -sqrt(2/D) sin(2 pi f k / D).  The tables hold those two scaled functions
+// of m = f k mod D, in fp32 (sincospif is within one ulp).
 template <int D>
-__device__ __forceinline__ float dense_r(const float* tcs, const float* tsn, int n, int k) {
-    const float isd = rsqrtf((float)D);
-    if (n == 0) return isd;
-    if (n == 1) return (k & 1) ? -isd : isd;
-    const int m = ((n >> 1) * k) % D;
-    const float r2 = 1.41421356237309515f * isd;
-    return (n & 1) ? -r2 * tsn[m] : r2 * tcs[m];
-}
-template <int D>
-__device__ __forceinline__ void dense_tables(float* tcs, float* tsn) {
+__device__ __forceinline__ void dft_tables(float* tcs, float* tsn) {
+    const float c = sqrtf(2.f / (float)D);
     for (int m = threadIdx.x; m < D; m += blockDim.x) {
-        double sv, cv;
-        sincospi(2.0 * m / D, &sv, &cv);
-        tcs[m] = (float)cv;
-        tsn[m] = (float)sv;
+        float sv, cv;
+        sincospif((float)(2 * m) / (float)D, &sv, &cv);
+        tcs[m] = c * cv;
+        tsn[m] = -c * sv;
+    }
+}
+// m + f mod D for m, f < D
+template <int D>
+__device__ __forceinline__ int mod_add(int m, int f) {
+    if constexpr ((D & (D - 1)) == 0) return (m + f) & (D - 1);
+    else {
+        m += f;
+        return m >= D ? m - D : m;
     }
 }
 __device__ __forceinline__ bool sign_neg(const uint32_t* mask, int k) {
     return (mask[k >> 1] & ((k & 1) ? 0x80000000u : 0x8000u)) != 0u;
 }
-
-// q preparation for a head dimension that is not a power of two (d = 96):
-// the SRFT as the dense map p = R diag(s) q, one warp per query row, then
-// 1/lambda_K and the softmax scale as above.
+// Unnormalised Walsh-Hadamard transform (Sylvester natural order) of the D
+// values a warp holds, coordinate 32 j + lane in v[j]: butterflies over the
+// register index for the high bits, over the lanes (shuffles) for the low five.
 template <int D>
-__global__ void __launch_bounds__(128) attn_prep_q_dense_kernel(const __grid_constant__ AttnParams P) {
-    __shared__ float tcs[D], tsn[D], xs[4][D];
-    dense_tables<D>(tcs, tsn);
-    __syncthreads();
+__device__ __forceinline__ void wht_warp(float (&v)[D / 32], int lane) {
+#pragma unroll
+    for (int h = 1; h < D / 32; h <<= 1)
+#pragma unroll
+        for (int j = 0; j < D / 32; ++j)
+            if (!(j & h)) {
+                const float x = v[j], y = v[j + h];
+                v[j] = x + y;
+                v[j + h] = x - y;
+            }
+#pragma unroll
+    for (int s2 = 1; s2 < 32; s2 <<= 1)
+#pragma unroll
+        for (int j = 0; j < D / 32; ++j) {
+            const float o = __shfl_xor_sync(0xffffffffu, v[j], s2);
+            v[j] = (lane & s2) ? o - v[j] : v[j] + o;
+        }
+}
+
+// q preparation: p = R diag(s) q, times the softmax scale (log2 units) and
+// 1/lambda_K, into fp32 [B][Hq][D].  One block of four warps per query row.
+// SRFT: warp w takes the inputs k in [wD/4, (w+1)D/4), lane the frequencies
+// f = lane + 32 j (rows 2f, 2f+1), walking k with the table index f k mod D;
+// the four partial rows are summed through shared memory, and the Nyquist row
+// is a sum of (-1)^k x_k.  SRHT: the Walsh-Hadamard transform across one warp.
+template <int D>
+__global__ void __launch_bounds__(128) attn_prep_q_kernel(const __grid_constant__ AttnParams P) {
+    constexpr int NF = (D / 2 + 31) / 32, KQ = D / 4;
+    __shared__ float tcs[D], tsn[D], xs[D], part[4][D], nyq[4];
+    const bool srht = pow2_dim<D>() && P.tr_k == SRFTKV_TRANSFORM_SRHT;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row = blockIdx.x * 4 + warp;
-    if (row >= P.B * P.Hq) return;
+    if (!srht) dft_tables<D>(tcs, tsn);
+    const int row = blockIdx.x;
     const int b = row / P.Hq, hq = row - b * P.Hq, hkv = hq / P.rep;
     const __half* qr = reinterpret_cast<const __half*>(P.q) + (long long)row * D;
-    for (int k = lane; k < D; k += 32) {
-        const float v = __half2float(qr[k]);
-        xs[warp][k] = sign_neg(P.sign_mask, k) ? -v : v;
+    for (int k = threadIdx.x; k < D; k += blockDim.x) {
+        const float x = __half2float(qr[k]);
+        xs[k] = sign_neg(P.sign_mask, k) ? -x : x;
     }
-    __syncwarp();
-    for (int o = lane; o < D; o += 32) {
-        float a = 0.f;
-        for (int k = 0; k < D; ++k) a = fmaf(dense_r<D>(tcs, tsn, o, k), xs[warp][k], a);
-        float sc = P.qscale;
-        if (P.lam_k != nullptr) sc *= __frcp_rn(P.lam_k[(long long)b * P.lam_k_stride + (long long)hkv * D + o]);
-        P.qt[(long long)row * D + o] = a * sc;
+    __syncthreads();
+    const float* lam = P.lam_k ? P.lam_k + (long long)b * P.lam_k_stride + (long long)hkv * D : nullptr;
+    float* yr = P.qt + (long long)row * D;
+    auto emit = [&](int o, float a) { yr[o] = a * (lam ? P.qscale * __frcp_rn(lam[o]) : P.qscale); };
+    const float isd = rsqrtf((float)D);
+    if constexpr (pow2_dim<D>()) {
+        if (srht) {
+            if (warp != 0) return;
+            float v[D / 32];
+#pragma unroll
+            for (int j = 0; j < D / 32; ++j) v[j] = xs[32 * j + lane];
+            wht_warp<D>(v, lane);
+#pragma unroll
+            for (int j = 0; j < D / 32; ++j) emit(32 * j + lane, v[j] * isd);
+            return;
+        }
+    }
+    const int k0 = warp * KQ;
+    float re[NF], im[NF];
+    int m[NF], f[NF];
+#pragma unroll
+    for (int j = 0; j < NF; ++j) {
+        re[j] = im[j] = 0.f;
+        f[j] = min(lane + 32 * j, D - 1);  // lanes past D/2 compute a row nobody stores
+        m[j] = (f[j] * k0) % D;
+    }
+    float ny = 0.f;
+#pragma unroll 4
+    for (int kk = 0; kk < KQ; ++kk) {
+        const float x = xs[k0 + kk];
+        ny += ((k0 + kk) & 1) ? -x : x;
+#pragma unroll
+        for (int j = 0; j < NF; ++j) {
+            re[j] = fmaf(tcs[m[j]], x, re[j]);
+            im[j] = fmaf(tsn[m[j]], x, im[j]);
+            m[j] = mod_add<D>(m[j], f[j]);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < NF; ++j) {
+        const int fr = lane + 32 * j;
+        if (fr < D / 2) {
+            part[warp][2 * fr] = re[j];
+            part[warp][2 * fr + 1] = im[j];
+        }
+    }
+    if (lane == 0) nyq[warp] = ny;
+    __syncthreads();
+    for (int o = threadIdx.x; o < D; o += blockDim.x) {
+        float a = (part[0][o] + part[1][o]) + (part[2][o] + part[3][o]);
+        if (o == 0) a *= 0.70710678118654752f;  // sqrt(2/D) sum x / sqrt(2)
+        if (o == 1) a = ((nyq[0] + nyq[1]) + (nyq[2] + nyq[3])) * isd;
+        emit(o, a);
     }
 }
 
@@ -531,7 +579,8 @@ __device__ __forceinline__ void tile_scores(uint32_t kc, const LaneRow& LK, cons
         else return (r ? k1 : k0)[f];
     };
     if constexpr (BK == 4) {
-        float a0 = 0.f, a1 = 0.f;
+        // token g and token g+8: (half 0, half 1) partials, summed at the end
+        float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
         // 32-dim chunk mm from its two 8-row matrices (rows 0-7, rows 8-15)
         auto chunk = [&](int mm, uint32_t rg, uint32_t rg8) {
             rg = ob4(rg);
@@ -546,8 +595,8 @@ __device__ __forceinline__ void tile_scores(uint32_t kc, const LaneRow& LK, cons
             mma16816(d, y0, y1, y2, y3, ql[4 * mm + 2], ql[4 * mm + 3]);
             // d = (token g: half 0, half 1, token g+8: half 0, half 1) for head c
             const int ga = (32 * mm) >> lg, gb = (32 * mm + 16) >> lg;
-            a0 = fmaf(ksc(ga, 0), d[0], fmaf(ksc(gb, 0), d[1], a0));
-            a1 = fmaf(ksc(ga, 1), d[2], fmaf(ksc(gb, 1), d[3], a1));
+            a0 = fma2(ksc(ga, 0), ksc(gb, 0), d[0], d[1], a0);
+            a1 = fma2(ksc(ga, 1), ksc(gb, 1), d[2], d[3], a1);
         };
 #pragma unroll
         for (int m2 = 0; m2 < D / 64; ++m2) {
@@ -561,8 +610,8 @@ __device__ __forceinline__ void tile_scores(uint32_t kc, const LaneRow& LK, cons
             ldsm_x2(plane_addr<PK::RB, PK::SWZ, PK::RP>(kc, LK, tr, D / 32 - 1), r);
             chunk(D / 32 - 1, r[0], r[1]);
         }
-        s[0] = a0;
-        s[1] = a1;
+        s[0] = a0.x + a0.y;
+        s[1] = a1.x + a1.y;
     } else if constexpr (BK == 8) {
         float a0 = 0.f, a1 = 0.f;
 #pragma unroll
@@ -695,12 +744,13 @@ __device__ __forceinline__ void tile_pv(uint32_t vc, const LaneRow& LV, const ui
             // group 16: group 2cb + side lies in chunk cb/2 at float 2(cb%2) + side (side folded into vso)
             const int gv = G == 16 ? cb >> 1 : (32 * cb + 16 * side) >> lg;
             const int fc = 2 * (cb & 1);
-            const float b00 = p00 * vsc(gv, fc, 0), b10 = p10 * vsc(gv, fc, 1), b01 = p01 * vsc(gv, fc, 8),
-                        b11 = p11 * vsc(gv, fc, 9);
-            sv[cb] += (b00 + b10) + (b01 + b11);
+            const float2 b0 = mul2(p00, p10, vsc(gv, fc, 0), vsc(gv, fc, 1));  // tokens 2c, 2c+1
+            const float2 b1 = mul2(p01, p11, vsc(gv, fc, 8), vsc(gv, fc, 9));  // tokens 2c+8, 2c+9
+            const float2 bs = __fadd2_rn(b0, b1);
+            sv[cb] += bs.x + bs.y;
             uint32_t bh0, bl0, bh1, bl1;
-            split_h2(b00, b10, bh0, bl0);
-            split_h2(b01, b11, bh1, bl1);
+            split_h2(b0.x, b0.y, bh0, bl0);
+            split_h2(b1.x, b1.y, bh1, bl1);
             R0 = ob4(R0);
             R1 = ob4(R1);
             const uint32_t S0 = R0 >> 8, S1 = R1 >> 8;
@@ -907,7 +957,8 @@ __device__ __forceinline__ void attn_chunk(const AttnParams& P, uint8_t* __restr
                                            const uint32_t (&ql)[AttnCfg<D, BK, BV>::QB],
                                            const float (&nb)[AttnCfg<D, BK, BV>::NB], int nh,
                                            float (&acc)[AttnCfg<D, BK, BV>::ACC],
-                                           float (&sv)[AttnCfg<D, BK, BV>::NSV], float& m, float& l, float mu) {
+                                           float (&sv)[AttnCfg<D, BK, BV>::NSV], float& svt, float& m, float& l,
+                                           float mu) {
     using C = AttnCfg<D, BK, BV>;
     constexpr float SU = C::QK ? kSub : 1.f;  // scores come in units of 1/SU
     const int g = lane >> 2, c = lane & 3;
@@ -973,6 +1024,7 @@ __device__ __forceinline__ void attn_chunk(const AttnParams& P, uint8_t* __restr
         const float mn = fmaxf(m, mt);
         const float f = (mn == -INFINITY) ? 1.f : ex2(m - mn);  // head c's factor
         l *= f;
+        svt *= f;
 #pragma unroll
         for (int i = 0; i < C::ACC; ++i) acc[i] *= f;
         const float fs = __shfl_sync(0xffffffffu, f, g >> 1);  // head g/2's factor, for the column sums
@@ -1139,7 +1191,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, AttnCfg<D, BK, BV>::MINB)
     uint32_t kso[SCH], vso[SCH];
     scale_offsets<D, SCH>(g, 0, kso);                               // K: row g (and g + 8)
     scale_offsets<D, SCH>(2 * c, BV == 4 ? 4 * (g & 1) : 0, vso);  // V: rows 2c (+1, +8, +9), column half
-    float acc[C::ACC], sv[C::NSV];
+    float acc[C::ACC], sv[C::NSV], svt = 0.f;
     float m = -INFINITY, l = 0.f;  // online-softmax state for head c (log2 domain)
 
     const int plane_row = b * P.Hkv + hkv;  // this (batch, kv head)'s rows in the head-major planes
@@ -1193,6 +1245,44 @@ __global__ void __launch_bounds__(kAttnWarps * 32, AttnCfg<D, BK, BV>::MINB)
     float mu = 0.f;
     bool failed = false, undrained = false;
     int it = 0;
+    // ss[i] = the sum over the 16 token slots of B's column held by this thread's
+    // useful accumulators (head c; for 4-bit values its column half), in chunk i
+    auto column_sums = [&](float (&ss)[C::NSV]) {
+#pragma unroll
+        for (int i = 0; i < C::NSV; ++i) {
+            float t = sv[i];
+            t += __shfl_xor_sync(0xffffffffu, t, 1);
+            t += __shfl_xor_sync(0xffffffffu, t, 2);  // column g's sum
+            const int col = BV == 4 ? 2 * c + (g >= 4 ? 1 : 0) : 2 * c;
+            ss[i] = __shfl_sync(0xffffffffu, t, 4 * col);
+        }
+    };
+    // acc holds sums of (code + offset) * B in the code unit.  Taking the offset
+    // times the column sums out every kFoldChunks chunks (and resetting them)
+    // keeps acc near the size of its signal: over a long run of chunks the
+    // offset part grows far larger than the signal and its fp32 accumulation in
+    // the MMAs would lose the signal's low bits when it cancels at the end.
+    // svt keeps the column's running total of B for the V-range test.
+    auto fold_offset = [&]() {
+        if constexpr (C::QV) {
+            float ss[C::NSV];
+            column_sums(ss);
+#pragma unroll
+            for (int i = 0; i < C::NSV; ++i) {
+                svt += ss[i];
+                sv[i] = 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < C::ACC; ++i) {
+                if constexpr (BV == 4) {
+                    const float iu = ((i >> 1) & 1) ? -8.f / 1048576.f : -8.f / kSub;  // high-nibble rows: 2^-20
+                    acc[i] = fmaf(iu, ss[i >> 3], acc[i]);
+                } else {
+                    acc[i] = fmaf(-128.f / kSub, ss[i >> 2], acc[i]);
+                }
+            }
+        }
+    };
     // one pass over this warp's chunks with V unit 2^mu_p (the first pass is called with a literal 0, so its
     // loop is the plain one; the rare second pass is a separate copy)
     auto run_pass = [&](float mu_p) {
@@ -1200,6 +1290,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, AttnCfg<D, BK, BV>::MINB)
         for (int i = 0; i < C::ACC; ++i) acc[i] = 0.f;
 #pragma unroll
         for (int i = 0; i < C::NSV; ++i) sv[i] = 0.f;
+        svt = 0.f;
         m = -INFINITY;
         l = 0.f;
         for (int chunk = c_begin + warp; chunk < c_end; ++it, chunk += kAttnWarps) {
@@ -1223,35 +1314,33 @@ __global__ void __launch_bounds__(kAttnWarps * 32, AttnCfg<D, BK, BV>::MINB)
                 break;
             }
             attn_chunk<D, BK, BV, C::CH / 16, G>(P, wbase + st * C::STAGE, chunk * C::CH, L, lane, LK, LV, kso, vso,
-                                                 qh, ql, nb, nh, acc, sv, m, l, mu_p);
+                                                 qh, ql, nb, nh, acc, sv, svt, m, l, mu_p);
             __syncwarp();
+            if ((it & (kFoldChunks - 1)) == kFoldChunks - 1) fold_offset();
         }
     };
     run_pass(0.f);
     if (C::QV && !failed) {
         bool redo;
         {
-            bool bad = !isfinite(l);
+            bool bad = !isfinite(l) || !isfinite(svt);
 #pragma unroll
             for (int i = 0; i < C::ACC; ++i) bad |= !isfinite(acc[i]);
 #pragma unroll
             for (int i = 0; i < C::NSV; ++i) bad |= !isfinite(sv[i]);
             redo = __any_sync(0xffffffffu, bad);
             if (!redo) {
-                // p-weighted mean V scale of this thread's column (head c, its half) against 2^-14
-                float lt = l, smax = 0.f;
+                // p-weighted mean V scale of this thread's column (head c, its half), averaged over the
+                // column's groups, against 2^-14
+                float lt = l, ss[C::NSV], tot = svt;
 #pragma unroll
                 for (int off = 4; off < 32; off <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
+                column_sums(ss);
 #pragma unroll
-                for (int i = 0; i < C::NSV; ++i) {
-                    float t = sv[i];
-                    t += __shfl_xor_sync(0xffffffffu, t, 1);
-                    t += __shfl_xor_sync(0xffffffffu, t, 2);
-                    const int col = BV == 4 ? 2 * c + (g >= 4 ? 1 : 0) : 2 * c;
-                    smax = fmaxf(smax, __shfl_sync(0xffffffffu, t, 4 * col));
-                }
+                for (int i = 0; i < C::NSV; ++i) tot += ss[i];
                 const bool counts = c < nh && lt > 0.f;
-                redo = __any_sync(0xffffffffu, counts) && __all_sync(0xffffffffu, !counts || smax < lt * 6.103515625e-05f);
+                redo = __any_sync(0xffffffffu, counts) &&
+                       __all_sync(0xffffffffu, !counts || tot < (float)C::NSV * lt * 6.103515625e-05f);
             }
         }
         if (redo) {
@@ -1295,14 +1384,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, AttnCfg<D, BK, BV>::MINB)
     // ---- remove the code offset: acc holds sums of (code + offset) * B in the
     // code unit; the column sums of B (this thread's useful column) give the rest
     float ssum[C::NSV];
-#pragma unroll
-    for (int i = 0; i < C::NSV; ++i) {
-        float t = sv[i];
-        t += __shfl_xor_sync(0xffffffffu, t, 1);
-        t += __shfl_xor_sync(0xffffffffu, t, 2);  // column g's sum over the 16 token slots
-        const int col = BV == 4 ? 2 * c + (g >= 4 ? 1 : 0) : 2 * c;
-        ssum[i] = __shfl_sync(0xffffffffu, t, 4 * col);
-    }
+    column_sums(ssum);
 #pragma unroll
     for (int i = 0; i < C::ACC; ++i) {
         if constexpr (BV == 4) {
@@ -1386,88 +1468,107 @@ __global__ void __launch_bounds__(kAttnWarps * 32, AttnCfg<D, BK, BV>::MINB)
 // ---------------------------------------------------------------------------
 // 3. combine
 // ---------------------------------------------------------------------------
+// One block of four warps per output row (b, hq).  Merge: every warp takes
+// the running max M over the splits (split s in lane s mod 32), then warp w
+// accumulates splits w, w + 4, ... (dims lane + 32 j); the four partial rows
+// meet in shared memory.  Inverse SRFT x = diag(s) R^T p: warp w takes the
+// frequencies f = 1 + w + 4 i and lane the coordinates k = lane + 32 j,
+// walking f with the table index f k mod D; the DC and Nyquist terms are added
+// in the final sum.  SRHT: the Walsh-Hadamard transform across one warp.
 template <int D, bool ROT>
 __global__ void __launch_bounds__(128) attn_combine_kernel(const __grid_constant__ AttnParams P) {
-    constexpr int N = D / 2, PER = (D + 31) / 32;  // dims lane + 32 j (the last j partial at d = 80)
-    __shared__ float rows[4][D];
+    constexpr int PER = (D + 31) / 32;  // dims lane + 32 j (the last j partial at d = 80)
+    __shared__ __align__(16) float rows[D];
+    __shared__ float part[4][D], lw[4];
+    __shared__ float tcs[ROT ? D : 1], tsn[ROT ? D : 1];
+    const bool srht = ROT && pow2_dim<D>() && P.tr_v == SRFTKV_TRANSFORM_SRHT;
+    if (ROT && !srht) dft_tables<D>(tcs, tsn);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row = blockIdx.x * 4 + warp;  // (b, hq)
-    const bool active = row < P.B * P.Hq;
-    if (active) {
-        const float* ml = P.part_ml + (long long)row * P.n_splits * 2;
-        const float* ac = P.part_acc + (long long)row * P.n_splits * D;
-        float M = -INFINITY;
-        for (int s = 0; s < P.n_splits; ++s) M = fmaxf(M, ml[2 * s]);
-        float Lsum = 0.f, o[PER];
+    const int row = blockIdx.x;  // (b, hq)
+    const int b = row / P.Hq, hq = row - b * P.Hq, hkv = hq / P.rep;
+    const int ns = P.n_splits;
+    const float* ml = P.part_ml + (long long)row * ns * 2;
+    const float* ac = P.part_acc + (long long)row * ns * D;
+    float M = -INFINITY;
+    for (int s = lane; s < ns; s += 32) M = fmaxf(M, ml[2 * s]);
 #pragma unroll
-        for (int j = 0; j < PER; ++j) o[j] = 0.f;
-        if (M != -INFINITY) {
-            for (int s = 0; s < P.n_splits; ++s) {
-                const float f = ex2(ml[2 * s] - M);
-                Lsum += f * ml[2 * s + 1];
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float L = 0.f, o[PER];
 #pragma unroll
-                for (int j = 0; j < PER; ++j)
-                    if (lane + 32 * j < D) o[j] += f * ac[(long long)s * D + lane + 32 * j];
-            }
-        }
-        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-        const int b = row / P.Hq, hkv = (row - b * P.Hq) / P.rep;
+    for (int j = 0; j < PER; ++j) o[j] = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll 4
+        for (int s = warp; s < ns; s += 4) {
+            const float2 e = *reinterpret_cast<const float2*>(ml + 2 * s);
+            const float w = ex2(e.x - M);  // 0 for empty splits
+            L = fmaf(w, e.y, L);
+            const float* a = ac + (long long)s * D + lane;
 #pragma unroll
-        for (int j = 0; j < PER; ++j) {
-            const int dim = lane + 32 * j;
-            if (dim >= D) break;
-            float v = o[j] * inv;
-            if (ROT && P.lam_v != nullptr)
-                v *= __frcp_rn(P.lam_v[(long long)b * P.lam_v_stride + (long long)hkv * D + dim]);
-            rows[warp][dim] = v;
+            for (int j = 0; j < PER; ++j)
+                if (lane + 32 * j < D) o[j] = fmaf(w, a[32 * j], o[j]);
         }
     }
-    __syncwarp();
-    if (!active) return;
-    if constexpr (!ROT) {
+#pragma unroll
+    for (int j = 0; j < PER; ++j)
+        if (lane + 32 * j < D) part[warp][lane + 32 * j] = o[j];
+    if (lane == 0) lw[warp] = L;
+    __syncthreads();
+    const float Lsum = (lw[0] + lw[1]) + (lw[2] + lw[3]);
+    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+    float* yr = P.out + (long long)row * D;
+    for (int t = threadIdx.x; t < D; t += blockDim.x) {
+        float v = ((part[0][t] + part[1][t]) + (part[2][t] + part[3][t])) * inv;
+        if (ROT && P.lam_v != nullptr) v *= __frcp_rn(P.lam_v[(long long)b * P.lam_v_stride + (long long)hkv * D + t]);
+        if (ROT) rows[t] = v;
+        else yr[t] = v;
+    }
+    if constexpr (ROT) {
+        __syncthreads();
+        const float isd = rsqrtf((float)D);
+        if constexpr (pow2_dim<D>()) {
+            if (srht) {  // x = diag(s) H p / sqrt(D)
+                if (warp != 0) return;
+                float v[D / 32];
+#pragma unroll
+                for (int j = 0; j < D / 32; ++j) v[j] = rows[32 * j + lane];
+                wht_warp<D>(v, lane);
+#pragma unroll
+                for (int j = 0; j < D / 32; ++j) {
+                    const int k = 32 * j + lane;
+                    const float a = v[j] * isd;
+                    yr[k] = sign_neg(P.sign_mask, k) ? -a : a;
+                }
+                return;
+            }
+        }
+        float a[PER];
+        int m[PER], st[PER];
+        const int f0 = 1 + warp;
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+            const int k = min(lane + 32 * j, D - 1);  // lanes past D (d = 80) compute a coordinate nobody stores
+            a[j] = 0.f;
+            m[j] = (f0 * k) % D;
+            st[j] = (4 * k) % D;
+        }
+#pragma unroll 4
+        for (int f = f0; f < D / 2; f += 4) {
+            const float2 pf = *reinterpret_cast<const float2*>(rows + 2 * f);
+#pragma unroll
+            for (int j = 0; j < PER; ++j) {
+                a[j] = fmaf(tcs[m[j]], pf.x, a[j]);
+                a[j] = fmaf(tsn[m[j]], pf.y, a[j]);
+                m[j] = mod_add<D>(m[j], st[j]);
+            }
+        }
 #pragma unroll
         for (int j = 0; j < PER; ++j)
-            if (lane + 32 * j < D) P.out[(long long)row * D + lane + 32 * j] = rows[warp][lane + 32 * j];
-    } else if constexpr (!pow2_dim<D>()) {
-        // inverse SRFT as the dense map diag(s) R^T p, one output coordinate per lane at a time
-        __shared__ float tcs[4][D], tsn[4][D];  // per warp: warps past the last row have left the block
-        for (int m = lane; m < D; m += 32) {
-            double sv, cv;
-            sincospi(2.0 * m / D, &sv, &cv);
-            tcs[warp][m] = (float)cv;
-            tsn[warp][m] = (float)sv;
-        }
-        __syncwarp();
-        for (int k = lane; k < D; k += 32) {
-            float a = 0.f;
-            for (int n = 0; n < D; ++n) a = fmaf(dense_r<D>(tcs[warp], tsn[warp], n, k), rows[warp][n], a);
-            P.out[(long long)row * D + k] = sign_neg(P.sign_mask, k) ? -a : a;
-        }
-    } else {
-        if (lane != 0) return;
-        float p[D], zr[N], zi[N];
-#pragma unroll
-        for (int i = 0; i < D; ++i) p[i] = rows[warp][i];
-        if (P.tr_v == SRFTKV_TRANSFORM_SRHT) {
-#pragma unroll
-            for (int n = 0; n < N; ++n) {
-                zr[n] = p[2 * n] * SplitConst<D>::inv_sqrt_d;
-                zi[n] = p[2 * n + 1] * SplitConst<D>::inv_sqrt_d;
-            }
-            wht_pairs<N>(zr, zi);
-        } else {
-            split_inverse<D>(p, zr, zi);
-            fft<N, true>(zr, zi);
-        }
-        float4* yr = reinterpret_cast<float4*>(P.out + (long long)row * D);
-#pragma unroll
-        for (int c4 = 0; c4 < D / 4; ++c4) {
-            const int n0 = 2 * c4, n1 = 2 * c4 + 1;
-            const float a = u2f(f2u(zr[n0]) ^ ((P.sign_mask[n0] & 0x8000u) << 16));
-            const float bq = u2f(f2u(zi[n0]) ^ (P.sign_mask[n0] & 0x80000000u));
-            const float cc = u2f(f2u(zr[n1]) ^ ((P.sign_mask[n1] & 0x8000u) << 16));
-            const float dd = u2f(f2u(zi[n1]) ^ (P.sign_mask[n1] & 0x80000000u));
-            yr[c4] = make_float4(a, bq, cc, dd);
+            if (lane + 32 * j < D) part[warp][lane + 32 * j] = a[j];
+        __syncthreads();
+        for (int k = threadIdx.x; k < D; k += blockDim.x) {
+            const float x = ((part[0][k] + part[1][k]) + (part[2][k] + part[3][k])) +
+                            isd * (rows[0] + ((k & 1) ? -rows[1] : rows[1]));
+            yr[k] = sign_neg(P.sign_mask, k) ? -x : x;
         }
     }
 }
@@ -1515,6 +1616,17 @@ struct AttnLaunch {
     cudaStream_t stream;
 };
 
+// the split kernel's dynamic shared memory limit, once per instance
+template <int D, int BK, int BV, int G>
+static void split_kernel_attr() {
+    static bool done = false;
+    if (!done) {
+        cudaFuncSetAttribute(q4kv_attn_split_kernel<D, BK, BV, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             AttnCfg<D, BK, BV>::SMEM);
+        done = true;
+    }
+}
+
 template <int D, int BK, int BV>
 static int launch_split(const AttnLaunch& A) {
     using C = AttnCfg<D, BK, BV>;
@@ -1548,17 +1660,9 @@ static int launch_split(const AttnLaunch& A) {
                             : raw_plane(&tvs, A.v->scales, P.sf_v);
         if (!ok) return SRFTKV_ERR_CUDA;
     }
-    static bool attr[2] = {false, false};
     const bool g16 = P.group == 16;  // raw fp16 sides carry group 16
-    if (!attr[g16]) {
-        if (g16)
-            cudaFuncSetAttribute(q4kv_attn_split_kernel<D, BK, BV, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::SMEM);
-        else
-            cudaFuncSetAttribute(q4kv_attn_split_kernel<D, BK, BV, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::SMEM);
-        attr[g16] = true;
-    }
+    if (g16) split_kernel_attr<D, BK, BV, 16>();
+    else split_kernel_attr<D, BK, BV, 0>();
     const dim3 grid(P.n_splits, P.B * P.Hkv * P.n_hg);
     if (g16)
         q4kv_attn_split_kernel<D, BK, BV, 16><<<grid, kAttnWarps * 32, C::SMEM, A.stream>>>(tkc, tks, tvc, tvs, P);
@@ -1574,11 +1678,9 @@ static int launch_all(const AttnLaunch& A) {
     const bool rot = bk != 16;
     const int rows = P.B * P.Hq;
     if (!rot)
-        attn_prep_q_kernel<D, false><<<(rows + 127) / 128, 128, 0, A.stream>>>(P);
-    else if constexpr (pow2_dim<D>())
-        attn_prep_q_kernel<D, true><<<(rows + 127) / 128, 128, 0, A.stream>>>(P);
+        attn_prep_q_raw_kernel<D><<<(rows + 127) / 128, 128, 0, A.stream>>>(P);
     else
-        attn_prep_q_dense_kernel<D><<<(rows + 3) / 4, 128, 0, A.stream>>>(P);
+        attn_prep_q_kernel<D><<<rows, 128, 0, A.stream>>>(P);
     int rc;
     if (bk == 4 && bv == 4) rc = launch_split<D, 4, 4>(A);
     else if (bk == 8 && bv == 4) rc = launch_split<D, 8, 4>(A);
@@ -1587,9 +1689,9 @@ static int launch_all(const AttnLaunch& A) {
     else rc = launch_split<D, 16, 16>(A);
     if (rc) return rc;
     if (rot)
-        attn_combine_kernel<D, true><<<(rows + 3) / 4, 128, 0, A.stream>>>(P);
+        attn_combine_kernel<D, true><<<rows, 128, 0, A.stream>>>(P);
     else
-        attn_combine_kernel<D, false><<<(rows + 3) / 4, 128, 0, A.stream>>>(P);
+        attn_combine_kernel<D, false><<<rows, 128, 0, A.stream>>>(P);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("attention launch failed: %s", cudaGetErrorString(e));
@@ -1604,7 +1706,9 @@ static int heads_per_group(int rep) { return (rep + head_groups(rep) - 1) / head
 
 static int auto_splits(int B, int Hq, int Hkv, int t_cap) {
     const long long pairs = (long long)B * Hkv * head_groups(Hq / Hkv);
-    const long long target = 8ll * device_sm_count() * 3;  // about eight waves of resident CTAs
+    // about five waves of CTAs at three an SM: larger splits than eight waves cost less per split (the
+    // pipeline fill and the merge) and still leave the scheduler enough CTAs to even out the tail
+    const long long target = 16ll * device_sm_count();
     long long s = (target + pairs - 1) / pairs;
     const long long max_s = (t_cap + 255) / 256;
     if (s > max_s) s = max_s;
