@@ -276,6 +276,7 @@ __global__ void __launch_bounds__(128) attn_prep_q_raw_kernel(const __grid_const
         yr[2 * c] = make_float4(a.x * P.qscale, a.y * P.qscale, bq.x * P.qscale, bq.y * P.qscale);
         yr[2 * c + 1] = make_float4(cc.x * P.qscale, cc.y * P.qscale, dd.x * P.qscale, dd.y * P.qscale);
     }
+    ptx::griddep_launch_dependents();  // the split kernel may start launching (it waits for this grid's end)
 }
 
 // The packed unitary DFT R of length D (the SRFT's rotation, R diag(s)):
@@ -362,6 +363,7 @@ __global__ void __launch_bounds__(128) attn_prep_q_kernel(const __grid_constant_
             wht_warp<D>(v, lane);
 #pragma unroll
             for (int j = 0; j < D / 32; ++j) emit(32 * j + lane, v[j] * isd);
+            ptx::griddep_launch_dependents();
             return;
         }
     }
@@ -402,6 +404,9 @@ __global__ void __launch_bounds__(128) attn_prep_q_kernel(const __grid_constant_
         if (o == 1) a = ((nyq[0] + nyq[1]) + (nyq[2] + nyq[3])) * isd;
         emit(o, a);
     }
+    // the split kernel may start launching now (it waits for this grid's end before it reads q); signalling
+    // at the start placed a small split grid unevenly over the SMs the preparation still held
+    ptx::griddep_launch_dependents();
 }
 
 // ---------------------------------------------------------------------------
@@ -1174,10 +1179,6 @@ __global__ void __launch_bounds__(kAttnWarps * 32, AttnCfg<D, BK, BV>::MINB)
 
     uint32_t qh[C::QB], ql[C::QB];
     float nb[C::NB];
-    if constexpr (C::PK)
-        build_qb_pair<D>(P.qt + ((long long)b * P.Hq + (long long)hkv * P.rep + h0) * D, nh, g, c, qh, ql, nb);
-    else
-        build_qb<D, BK>(P.qt + ((long long)b * P.Hq + (long long)hkv * P.rep + h0) * D, nh, g, c, qh, ql, nb);
     // per-lane shared-memory addressing of the plane images
     using PK = PlaneT<D, BK>;
     using PV = PlaneT<D, BV>;
@@ -1232,7 +1233,15 @@ __global__ void __launch_bounds__(kAttnWarps * 32, AttnCfg<D, BK, BV>::MINB)
                 if (c_begin + warp + j * kAttnWarps < c_end) issue(c_begin + warp + j * kAttnWarps, (it0 + j) % NS);
         }
     };
+    // The cache copies do not depend on the q preparation, which may still be
+    // running (the kernel is launched as its programmatic dependent): the first
+    // chunks go out first, the prepared q is read after griddep_wait.
     prologue(0);
+    ptx::griddep_wait();
+    if constexpr (C::PK)
+        build_qb_pair<D>(P.qt + ((long long)b * P.Hq + (long long)hkv * P.rep + h0) * D, nh, g, c, qh, ql, nb);
+    else
+        build_qb<D, BK>(P.qt + ((long long)b * P.Hq + (long long)hkv * P.rep + h0) * D, nh, g, c, qh, ql, nb);
 
     // V unit.  P.V takes B = p * scale_V in fp16 with p <= 256 * 2^-mu, l and acc
     // accumulating in that unit, and the (m, l) the warp exports carry m + mu.
@@ -1371,6 +1380,9 @@ __global__ void __launch_bounds__(kAttnWarps * 32, AttnCfg<D, BK, BV>::MINB)
             }
         }
     }
+    // the combine may start launching once every CTA is this far (it waits for the grid's end); signalling
+    // earlier lets its CTAs sit on the SMs through the whole run when the grid is a single wave
+    ptx::griddep_launch_dependents();
     // the failure flag is per warp; every warp still joins the merge below
     if (failed) {
         m = -INFINITY;
@@ -1483,6 +1495,7 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const __grid_constant
     __shared__ float tcs[ROT ? D : 1], tsn[ROT ? D : 1];
     const bool srht = ROT && pow2_dim<D>() && P.tr_v == SRFTKV_TRANSFORM_SRHT;
     if (ROT && !srht) dft_tables<D>(tcs, tsn);
+    ptx::griddep_wait();  // launched as the split kernel's programmatic dependent: its partials first
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row = blockIdx.x;  // (b, hq)
     const int b = row / P.Hq, hq = row - b * P.Hq, hkv = hq / P.rep;
@@ -1616,6 +1629,25 @@ struct AttnLaunch {
     cudaStream_t stream;
 };
 
+// Launch as the programmatic dependent of the kernel before it in the stream:
+// it may start while that one finishes and waits for it with griddep_wait
+// (the split kernel after the q preparation, the combine after the split).
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                    Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // the split kernel's dynamic shared memory limit, once per instance
 template <int D, int BK, int BV, int G>
 static void split_kernel_attr() {
@@ -1664,10 +1696,14 @@ static int launch_split(const AttnLaunch& A) {
     if (g16) split_kernel_attr<D, BK, BV, 16>();
     else split_kernel_attr<D, BK, BV, 0>();
     const dim3 grid(P.n_splits, P.B * P.Hkv * P.n_hg);
-    if (g16)
-        q4kv_attn_split_kernel<D, BK, BV, 16><<<grid, kAttnWarps * 32, C::SMEM, A.stream>>>(tkc, tks, tvc, tvs, P);
-    else
-        q4kv_attn_split_kernel<D, BK, BV, 0><<<grid, kAttnWarps * 32, C::SMEM, A.stream>>>(tkc, tks, tvc, tvs, P);
+    const cudaError_t e = g16 ? launch_dependent(q4kv_attn_split_kernel<D, BK, BV, 16>, grid, dim3(kAttnWarps * 32),
+                                                 C::SMEM, A.stream, tkc, tks, tvc, tvs, P)
+                              : launch_dependent(q4kv_attn_split_kernel<D, BK, BV, 0>, grid, dim3(kAttnWarps * 32),
+                                                 C::SMEM, A.stream, tkc, tks, tvc, tvs, P);
+    if (e != cudaSuccess) {
+        set_error("attention launch failed: %s", cudaGetErrorString(e));
+        return SRFTKV_ERR_CUDA;
+    }
     return 0;
 }
 
@@ -1688,11 +1724,9 @@ static int launch_all(const AttnLaunch& A) {
     else if (bk == 8 && bv == 8) rc = launch_split<D, 8, 8>(A);
     else rc = launch_split<D, 16, 16>(A);
     if (rc) return rc;
-    if (rot)
-        attn_combine_kernel<D, true><<<rows, 128, 0, A.stream>>>(P);
-    else
-        attn_combine_kernel<D, false><<<rows, 128, 0, A.stream>>>(P);
-    const cudaError_t e = cudaGetLastError();
+    cudaError_t e = rot ? launch_dependent(attn_combine_kernel<D, true>, dim3(rows), dim3(128), 0, A.stream, P)
+                        : launch_dependent(attn_combine_kernel<D, false>, dim3(rows), dim3(128), 0, A.stream, P);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("attention launch failed: %s", cudaGetErrorString(e));
         return SRFTKV_ERR_CUDA;
