@@ -84,6 +84,15 @@ struct AttnParams {
 // ---------------------------------------------------------------------------
 // Small PTX helpers
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation may start while the kernel before it in the stream still runs;
+// griddep_wait blocks until that kernel has completed and its memory writes are
+// visible (a no-op for a kernel launched the ordinary way).  griddep_launch_dependents
+// lets the next such kernel start launching once every CTA of this one has
+// called it or exited.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -276,7 +285,7 @@ __global__ void __launch_bounds__(128) attn_prep_q_raw_kernel(const __grid_const
         yr[2 * c] = make_float4(a.x * P.qscale, a.y * P.qscale, bq.x * P.qscale, bq.y * P.qscale);
         yr[2 * c + 1] = make_float4(cc.x * P.qscale, cc.y * P.qscale, dd.x * P.qscale, dd.y * P.qscale);
     }
-    ptx::griddep_launch_dependents();  // the split kernel may start launching (it waits for this grid's end)
+    griddep_launch_dependents();  // the split kernel may start launching (it waits for this grid's end)
 }
 
 // The packed unitary DFT R of length D (the SRFT's rotation, R diag(s)):
@@ -363,7 +372,7 @@ __global__ void __launch_bounds__(128) attn_prep_q_kernel(const __grid_constant_
             wht_warp<D>(v, lane);
 #pragma unroll
             for (int j = 0; j < D / 32; ++j) emit(32 * j + lane, v[j] * isd);
-            ptx::griddep_launch_dependents();
+            griddep_launch_dependents();
             return;
         }
     }
@@ -406,7 +415,7 @@ __global__ void __launch_bounds__(128) attn_prep_q_kernel(const __grid_constant_
     }
     // the split kernel may start launching now (it waits for this grid's end before it reads q); signalling
     // at the start placed a small split grid unevenly over the SMs the preparation still held
-    ptx::griddep_launch_dependents();
+    griddep_launch_dependents();
 }
 
 // ---------------------------------------------------------------------------
@@ -1237,7 +1246,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, AttnCfg<D, BK, BV>::MINB)
     // running (the kernel is launched as its programmatic dependent): the first
     // chunks go out first, the prepared q is read after griddep_wait.
     prologue(0);
-    ptx::griddep_wait();
+    griddep_wait();
     if constexpr (C::PK)
         build_qb_pair<D>(P.qt + ((long long)b * P.Hq + (long long)hkv * P.rep + h0) * D, nh, g, c, qh, ql, nb);
     else
@@ -1382,7 +1391,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, AttnCfg<D, BK, BV>::MINB)
     }
     // the combine may start launching once every CTA is this far (it waits for the grid's end); signalling
     // earlier lets its CTAs sit on the SMs through the whole run when the grid is a single wave
-    ptx::griddep_launch_dependents();
+    griddep_launch_dependents();
     // the failure flag is per warp; every warp still joins the merge below
     if (failed) {
         m = -INFINITY;
@@ -1495,7 +1504,7 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const __grid_constant
     __shared__ float tcs[ROT ? D : 1], tsn[ROT ? D : 1];
     const bool srht = ROT && pow2_dim<D>() && P.tr_v == SRFTKV_TRANSFORM_SRHT;
     if (ROT && !srht) dft_tables<D>(tcs, tsn);
-    ptx::griddep_wait();  // launched as the split kernel's programmatic dependent: its partials first
+    griddep_wait();  // launched as the split kernel's programmatic dependent: its partials first
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row = blockIdx.x;  // (b, hq)
     const int b = row / P.Hq, hq = row - b * P.Hq, hkv = hq / P.rep;

@@ -142,13 +142,5 @@ namespace ptx {
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
-// Programmatic dependent launch.  A kernel launched with programmatic stream
-// serialisation may start while the kernel before it in the stream still runs;
-// griddep_wait blocks until that kernel has completed and its memory writes are
-// visible (a no-op for a kernel launched the ordinary way).  griddep_launch_dependents
-// lets the next such kernel start launching once every CTA of this one has
-// called it or exited.
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 }  // namespace ptx
 }  // namespace srftkv
