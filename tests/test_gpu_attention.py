@@ -259,3 +259,39 @@ def test_value_scales_spanning_many_binades_across_chunks():
         ref = oracle_attention(q, sk, sv, 16, seed, None)
         assert np.isfinite(out).all()
         assert np.abs(out - ref).max() <= 1e-4 * float(np.abs(ref).max())
+
+
+@pytest.mark.parametrize("bits", [4, 16])
+def test_attention_captured_in_a_cuda_graph_matches_eager(bits):
+    """The attention call (q preparation, split kernel and combine, the last two
+    launched as programmatic dependents of the kernel before them) captured in a
+    CUDA graph and replayed gives the eager call's output bit for bit, also
+    after the query and the sequence lengths change in place between replays."""
+    B, Hq, Hkv, d, T, G, seed = 3, 8, 2, 128, 2048, 16, 9
+    sk, sv = build_cache(B, Hkv, d, T, bits, bits, G, seed)
+    gen = torch.Generator(device="cuda").manual_seed(4)
+    q = torch.randn((B, Hq, d), generator=gen, device="cuda").to(torch.float16)
+    seq = torch.tensor([T, 1000, 17], dtype=torch.int32, device="cuda")
+    out = torch.empty((B, Hq, d), dtype=torch.float32, device="cuda")
+    ws = torch.empty(K.q4kv_decode_attention_workspace_size(B, Hq, Hkv, d, T, 0), dtype=torch.uint8, device="cuda")
+    call = lambda: K.q4kv_decode_attention(q, out, sk, sv, B, Hq, Hkv, d, G, T, seq, 0.0, seed, 0, ws)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call()  # the first call sets the kernels' attributes outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    for step in range(3):
+        if step:
+            q.copy_(torch.randn((B, Hq, d), generator=gen, device="cuda").to(torch.float16))
+            seq.copy_(torch.tensor([T - 7 * step, 1 + 300 * step, 2048 - 500 * step], dtype=torch.int32))
+        call()
+        torch.cuda.synchronize()
+        eager = out.clone()
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager), step
