@@ -10,18 +10,21 @@
 // output is rotated back once per (batch, query head), never per token.
 //
 // Three launches per call:
-//   1. prep: q_tilde = SRFT(q) / lambda_K * sm_scale * log2(e) (one thread per row);
-//   2. split: grid (n_splits, B*Hkv).  Each warp streams chunks of tokens of its
+//   1. prep: q_tilde = SRFT(q) / lambda_K * sm_scale * log2(e) (one block of four
+//      warps per row);
+//   2. split: grid (n_splits, B*Hkv*head groups), launched as the prep's
+//      programmatic dependent.  Each warp streams chunks of tokens of its
 //      split; a TMA copy per plane (codes and scales of K and V) lands each chunk
-//      in shared memory with 16 bytes of padding per row, so the ldmatrix reads
-//      that follow are bank-conflict free.  Codes are turned into exact fp16
+//      in shared memory, swizzled (or padded) so that the ldmatrix reads that
+//      follow are bank-conflict free.  Codes are turned into exact fp16
 //      integers in registers and contracted on the tensor cores
 //      (mma.sync m16n8k16, fp32 accumulate): S = codes_K . q_tilde per 16-token
 //      tile, the per-group scale applied to the fp32 partial of each group,
 //      then acc += codes_V^T . (p * scale_V).  The GQA query heads of one kv
 //      head share every tile.  Per-warp online softmax states are merged in
 //      shared memory into one partial (m, l, acc) per (query head, split);
-//   3. combine: merge the splits, divide by l and lambda_V, inverse SRFT.
+//   3. combine: merge the splits, divide by l and lambda_V, inverse SRFT (one
+//      block per row, launched as the split kernel's programmatic dependent).
 //
 // The contractions are tiny (4 query heads per kv head), so the tensor cores
 // are used for what they are here: a way to do the 2 x 4 multiply-adds per
@@ -31,7 +34,6 @@
 // hi + lo and contracted twice, which keeps the products at ~22-bit accuracy.
 #include <cuda_fp16.h>
 
-#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstring>
