@@ -137,7 +137,8 @@ typedef struct srftkv_side {
  * n_outer == 0 or n_tokens == 0 is a no-op that returns SRFTKV_OK.
  * d = 80 and 96 run as the 128-wide tensor-core contraction with R zero
  * outside its d x d block (any call size); d = 192 and 256 as the wide
- * tensor-core contraction for calls of 2^19 vectors and more, else as the
+ * tensor-core contraction for calls of 2^17 vectors and more (2^16 for
+ * srft_kv_dequantize), else as the
  * register transform (two threads per vector at d = 192).
  */
 int srft_kv_quantize(const srftkv_side* k, const srftkv_side* v, int n_outer, int n_tokens,

@@ -129,8 +129,8 @@ static int dispatch_codec(const CodecCall& c, bool quantize) {
 
 // Codec path: the tensor-core contraction (codec_tc.cu) for d = 128 when the
 // call is large enough to amortise building R_s in every CTA (measured on
-// GB300: from about 192 K vectors a call it beats the register FFT in both
-// directions, and is 1.5-1.8x faster at millions); to quantize a small d = 128
+// GB300: from about 150 K vectors a call for the quantize and 65 K for the
+// dequantize it beats the register FFT, and is 1.5-1.8x faster at millions); to quantize a small d = 128
 // call (a token append), one warp per vector (codec_small.cu), faster than
 // one thread per vector up to about 4 K vectors; the register FFT otherwise.
 // SRFTKV_QUANT_PATH=fft, =tc or =warp in the environment forces one path (tc
@@ -141,11 +141,20 @@ static int quant_path_override() {
     return !strcmp(e, "fft") ? 1 : !strcmp(e, "tc") ? 2 : !strcmp(e, "warp") ? 3 : 0;
 }
 constexpr long long kWarpPathMaxRows = 4096;
-constexpr long long kTensorCorePathMinRows = 3ll << 16;
-// d = 192 / 256: building R_s in every CTA costs more (N x d entries); the
-// Gemma-shaped cache (0.21 M vectors of d = 256) still quantizes faster on the
-// two-lane register path (measured 0.075 against 0.080 ms)
-constexpr long long kWideTensorCorePathMinRows = 1ll << 19;
+// d = 128: the tensor-core kernels' fixed cost (about 13 us a launch, most of it
+// the R_s block every CTA builds) against the register FFT: measured crossovers
+// about 150 K vectors for the quantize (0.21 M: 0.027 against 0.029 ms) and 65 K
+// for the dequantize (0.11 M: 0.019 against 0.021 ms)
+constexpr long long kTensorCoreQuantMinRows = 5ll << 15;
+constexpr long long kTensorCoreDequantMinRows = 1ll << 16;
+// d = 192 / 256: the tensor-core kernels pay a fixed cost (every CTA builds
+// its N x d block of R_s: about 20 us a launch at d = 256, 16-19 at d = 192)
+// that the two-lane register kernels do not.  Measured crossovers (vectors of
+// K and V together, L2 flushed): dequantize about 65 K at d = 256 and 32 K at
+// d = 192, quantize about 106 K at both (the Gemma-shaped 0.21 M vectors of
+// d = 256: quantize 0.064 against 0.068 ms, dequantize 0.048 against 0.077).
+constexpr long long kWideTensorCoreQuantMinRows = 1ll << 17;
+constexpr long long kWideTensorCoreDequantMinRows = 1ll << 16;
 
 // A call whose two sides use different transforms or scale formats runs as
 // two one-sided calls (the tensor-core kernels hold one transform matrix per
@@ -184,9 +193,9 @@ int codec_quantize(const CodecCall& c) {
     const int ov = quant_path_override();
     const long long rows = (long long)c.n_sides * c.n_outer * c.n_tokens * c.H;
     if ((c.d == 192 || c.d == 256) && c.group <= 32 &&  // a group must fit in one epilogue thread's 32 columns
-        (ov == 2 || (ov == 0 && rows >= kWideTensorCorePathMinRows)))
+        (ov == 2 || (ov == 0 && rows >= kWideTensorCoreQuantMinRows)))
         return c.d == 192 ? codec_quantize_tc_wide192(c) : codec_quantize_tc_wide256(c);
-    if (ov == 2 || (ov == 0 && rows >= kTensorCorePathMinRows)) {
+    if (ov == 2 || (ov == 0 && rows >= kTensorCoreQuantMinRows)) {
         const int rc = codec_quantize_tc(c);
         if (rc != 1) return rc;
     }
@@ -202,11 +211,11 @@ int codec_dequantize(const CodecCall& c) {
     if (c.d == 96 || c.d == 80) return tc_only(c, codec_dequantize_tc, "dequantize");
     const int ov = quant_path_override();
     const long long rows = (long long)c.n_sides * c.n_outer * c.n_tokens * c.H;
-    if ((c.d == 192 || c.d == 256) && (ov == 2 || (ov == 0 && rows >= kWideTensorCorePathMinRows))) {
+    if ((c.d == 192 || c.d == 256) && (ov == 2 || (ov == 0 && rows >= kWideTensorCoreDequantMinRows))) {
         const int rc = c.d == 192 ? codec_dequantize_tc_wide192(c) : codec_dequantize_tc_wide256(c);
         if (rc != 1) return rc;  // 1: a call the tensor-core kernel does not take (lambda, groups > 32, scale rows)
     }
-    if (ov == 2 || (ov == 0 && rows >= kTensorCorePathMinRows)) {
+    if (ov == 2 || (ov == 0 && rows >= kTensorCoreDequantMinRows)) {
         const int rc = codec_dequantize_tc(c);
         if (rc != 1) return rc;
     }

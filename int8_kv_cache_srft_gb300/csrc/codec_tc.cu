@@ -122,20 +122,25 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
         // angle tables (d < 128) in the x stages, which no copy has reached yet
         float* cs = reinterpret_cast<float*>(smem + T_OFF_A);
         float* sn = cs + TD;
-        if constexpr (DV != TD) {
-            r_tables(DV, cs, sn);
-            __syncthreads();
-        }
-        for (int idx = threadIdx.x; idx < TD * TD; idx += blockDim.x) {
-            const int n = idx >> 7, k = idx & 127;
-            float v = r_entry(n, k, DV, srht, cs, sn);
-            const uint32_t sbit = (k & 1) ? 0x80000000u : 0x8000u;
-            if (P.sign_mask[k >> 1] & sbit) v = -v;
-            const __half hi = __float2half_rn(v);
-            const __half lo = __float2half_rn(v - __half2float(hi));
-            const uint32_t off = sw128_offset(n, k);
-            *reinterpret_cast<__half*>(smem + off) = hi;
-            *reinterpret_cast<__half*>(smem + T_OFF_BLO + off) = lo;
+        uint32_t* smask = reinterpret_cast<uint32_t*>(sn + TD);
+        stage_sign_mask(smask, P.sign_mask, TD / 2);
+        if constexpr (DV != TD) r_tables(DV, cs, sn);
+        __syncthreads();
+        // one 16-byte chunk (8 consecutive k of row n) of R_hi and of R_lo a step
+        for (int c = threadIdx.x; c < TD * TD / 8; c += blockDim.x) {
+            const int n = c >> 4, k0 = (c & 15) << 3;
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int k = k0 + 2 * j;
+                float v0 = r_entry(n, k, DV, srht, cs, sn), v1 = r_entry(n, k + 1, DV, srht, cs, sn);
+                if (sign_flip(smask, k)) v0 = -v0;
+                if (sign_flip(smask, k + 1)) v1 = -v1;
+                split_pair_h2(v0, v1, hi[j], lo[j]);
+            }
+            const uint32_t off = sw128_offset(n, k0);
+            *reinterpret_cast<uint4*>(smem + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(smem + T_OFF_BLO + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
         ptx::fence_proxy_async_smem();  // generic writes -> tensor-core (async proxy) reads
     }
@@ -617,23 +622,33 @@ __global__ void __launch_bounds__(DQ_WARPS * 32, 1)
     static_assert(C::STAGES <= 4, "input stages");
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[19]);
     float* rbase = reinterpret_cast<float*>(smem + C::OFF_BASE);
+    static_assert(C::OFF_BASE % 16 == 0, "the fp32 copy of R_s is written as float4");
 
     {  // B[k][q] = s_k R[n][k] with n = dq_kperm(q) (zero outside d x d), in fp16; and in fp32 for the rebuilds
         const bool srht = P.side[0].transform == SRFTKV_TRANSFORM_SRHT;
         // angle tables (d < 128) in the output staging buffers, which no epilogue has reached yet
         float* cs = reinterpret_cast<float*>(smem + DQ_OFF_O);
         float* sn = cs + TD;
-        if constexpr (DV != TD) {
-            r_tables(DV, cs, sn);
-            __syncthreads();
-        }
-        for (int idx = threadIdx.x; idx < TD * TD; idx += blockDim.x) {
-            // B row k (output coordinate), K position q holding packed coordinate n
-            const int k = idx >> 7, q = idx & 127, n = dq_kperm(q);
-            float v = r_entry(n, k, DV, srht, cs, sn);
-            if (P.sign_mask[k >> 1] & ((k & 1) ? 0x80000000u : 0x8000u)) v = -v;
-            rbase[idx] = v;
-            *reinterpret_cast<__half*>(smem + sw128_offset(k, q)) = __float2half_rn(v);
+        uint32_t* smask = reinterpret_cast<uint32_t*>(sn + TD);
+        stage_sign_mask(smask, P.sign_mask, TD / 2);
+        if constexpr (DV != TD) r_tables(DV, cs, sn);
+        __syncthreads();
+        // one 16-byte chunk a step: B row k (output coordinate), K positions q0 .. q0+7 holding packed
+        // coordinates dq_kperm(q)
+        for (int c = threadIdx.x; c < TD * TD / 8; c += blockDim.x) {
+            const int k = c >> 4, q0 = (c & 15) << 3;
+            const bool flip = sign_flip(smask, k);
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                v[j] = r_entry(dq_kperm(q0 + j), k, DV, srht, cs, sn);
+                if (flip) v[j] = -v[j];
+            }
+            float4* rb = reinterpret_cast<float4*>(rbase + k * TD + q0);
+            rb[0] = make_float4(v[0], v[1], v[2], v[3]);
+            rb[1] = make_float4(v[4], v[5], v[6], v[7]);
+            *reinterpret_cast<uint4*>(smem + sw128_offset(k, q0)) =
+                make_uint4(pack_half2(v[0], v[1]), pack_half2(v[2], v[3]), pack_half2(v[4], v[5]), pack_half2(v[6], v[7]));
         }
         ptx::fence_proxy_async_smem();
     }

@@ -1,7 +1,8 @@
-// codec_tc_common.cuh -- helpers shared by the tensor-core dequantize kernels
-// (codec_tc.cu at d = 128 and 96, codec_tc_wide.cuh at d = 192 and 256): the
-// contraction's K order, exact fp16 pairs of signed codes, swizzled 16-byte
-// chunks of TMA-copied rows.
+// codec_tc_common.cuh -- helpers shared by the tensor-core codec kernels
+// (codec_tc.cu at d = 128, 96 and 80, codec_tc_wide.cuh at d = 192 and 256):
+// the dequantize contraction's K order, exact fp16 pairs of signed codes,
+// swizzled 16-byte chunks of TMA-copied rows, and the pieces every kernel's
+// prologue uses to build its block of R_s in shared memory.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -13,6 +14,29 @@ namespace srftkv {
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// (a, b) as fp16 hi + lo pairs: hi the fp16 rounding of each, lo the fp16
+// rounding of the fp32 residual (the same values as converting one entry at a
+// time; the even coordinate in the low half, as in memory)
+__device__ __forceinline__ void split_pair_h2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    const __half2 h = __floats2half2_rn(a, b);
+    const float2 f = __half22float2(h);
+    const __half2 l = __floats2half2_rn(a - f.x, b - f.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// The sign vector s as the kernel parameters carry it (word j: bit 15 for
+// coordinate 2j, bit 31 for 2j + 1), copied into shared memory before a
+// prologue builds R_s = R diag(s): read from the parameters with a per-lane
+// index, each lookup serialises over the distinct words a warp asks for (half
+// of the d = 128 prologue's time).  The caller synchronises the block.
+__device__ __forceinline__ void stage_sign_mask(uint32_t* dst, const uint32_t* mask, int words) {
+    for (int i = threadIdx.x; i < words; i += blockDim.x) dst[i] = mask[i];
+}
+__device__ __forceinline__ bool sign_flip(const uint32_t* smask, int k) {
+    return (smask[k >> 1] & ((k & 1) ? 0x80000000u : 0x8000u)) != 0u;
 }
 
 // 16-byte chunk c of row r of a buffer of RB-byte rows written by TMA with the

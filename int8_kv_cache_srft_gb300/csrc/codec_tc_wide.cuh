@@ -108,18 +108,19 @@ __global__ void __launch_bounds__(wide::WARPS * 32, 1)
         // cos / sin (2 pi m / d) for m < d, in double, in the x stages (not yet in use)
         float* cs = reinterpret_cast<float*>(smem + C::OFF_X);
         float* sn = cs + DV;
+        uint32_t* smask = reinterpret_cast<uint32_t*>(sn + DV);
         for (int m = threadIdx.x; m < DV; m += blockDim.x) {
             double sv, cv;
             sincospi(2.0 * m / DV, &sv, &cv);
             cs[m] = (float)cv;
             sn[m] = (float)sv;
         }
+        stage_sign_mask(smask, P.sign_mask, DV / 2);
         __syncthreads();
         const bool srht = P.side[0].transform == SRFTKV_TRANSFORM_SRHT;
         // entries times 2^RLOG2 (exact), so that the fp16 residual R_lo stays normal
         const float isd = (float)((1 << wide::RLOG2) / sqrt((double)DV)), r2 = (float)((1 << wide::RLOG2) * sqrt(2.0 / DV));
-        for (int idx = threadIdx.x; idx < C::N * DV; idx += blockDim.x) {
-            const int nl = idx / DV, k = idx - nl * DV, n = n0 + nl;
+        auto entry = [&](int n, int k) -> float {
             float v;
             if (srht) v = (__popc(n & k) & 1) ? -isd : isd;  // Hadamard entry / sqrt(d) (d a power of two)
             else if (n == 0) v = isd;
@@ -128,12 +129,17 @@ __global__ void __launch_bounds__(wide::WARPS * 32, 1)
                 const int m = ((n >> 1) * k) % DV;
                 v = (n & 1) ? -r2 * sn[m] : r2 * cs[m];
             }
-            if (P.sign_mask[k >> 1] & ((k & 1) ? 0x80000000u : 0x8000u)) v = -v;
-            const __half hi = __float2half_rn(v);
-            const __half lo = __float2half_rn(v - __half2float(hi));
-            const uint32_t off = wide::kb_offset<C::N>(nl, k);
-            *reinterpret_cast<__half*>(smem + off) = hi;
-            *reinterpret_cast<__half*>(smem + C::OFF_BLO + off) = lo;
+            return sign_flip(smask, k) ? -v : v;
+        };
+        // one 16-byte chunk (8 consecutive k of row n) of R_hi and of R_lo a step
+        for (int c = threadIdx.x; c < C::N * DV / 8; c += blockDim.x) {
+            const int nl = c / (DV / 8), k0 = (c - nl * (DV / 8)) * 8, n = n0 + nl;
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) split_pair_h2(entry(n, k0 + 2 * j), entry(n, k0 + 2 * j + 1), hi[j], lo[j]);
+            const uint32_t off = wide::kb_offset<C::N>(nl, k0);
+            *reinterpret_cast<uint4*>(smem + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(smem + C::OFF_BLO + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
         ptx::fence_proxy_async_smem();  // generic writes -> tensor-core and TMA (async proxy) accesses
     }
@@ -491,27 +497,42 @@ __global__ void __launch_bounds__(wide::DQ_WARPS * 32, 1)
     {  // B[k][q] = s_k R[n][k] with n = dq_kperm(q), fp16, in the MMA operand layout (k-blocks of DV rows)
         float* cs = reinterpret_cast<float*>(smem + C::OFF_IN);  // cos / sin (2 pi m/d) in the (unused) input stages
         float* sn = cs + DV;
+        uint32_t* smask = reinterpret_cast<uint32_t*>(sn + DV);
         for (int m = threadIdx.x; m < DV; m += blockDim.x) {
             double sv, cv;
             sincospi(2.0 * m / DV, &sv, &cv);
             cs[m] = (float)cv;
             sn[m] = (float)sv;
         }
+        stage_sign_mask(smask, P.sign_mask, DV / 2);
         __syncthreads();
         const bool srht = P.side[0].transform == SRFTKV_TRANSFORM_SRHT;
         const float isd = (float)(1.0 / sqrt((double)DV)), r2 = (float)sqrt(2.0 / DV);
-        for (int idx = threadIdx.x; idx < DV * DV; idx += blockDim.x) {
-            const int k = idx / DV, q = idx - k * DV, n = dq_kperm(q);  // B row k (output), K position q
-            float v;
-            if (srht) v = (__popc(n & k) & 1) ? -isd : isd;
-            else if (n == 0) v = isd;
-            else if (n == 1) v = (k & 1) ? -isd : isd;
-            else {
-                const int mm = ((n >> 1) * k) % DV;
-                v = (n & 1) ? -r2 * sn[mm] : r2 * cs[mm];
+        // one 16-byte chunk a step: B row k (output coordinate), K positions q0 .. q0+7 holding packed
+        // coordinates dq_kperm(q)
+        for (int c = threadIdx.x; c < DV * DV / 8; c += blockDim.x) {
+            const int k = c / (DV / 8), q0 = (c - k * (DV / 8)) * 8;
+            const bool flip = sign_flip(smask, k);
+            uint32_t h[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float v2[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int n = dq_kperm(q0 + 2 * j + e);
+                    float v;
+                    if (srht) v = (__popc(n & k) & 1) ? -isd : isd;
+                    else if (n == 0) v = isd;
+                    else if (n == 1) v = (k & 1) ? -isd : isd;
+                    else {
+                        const int mm = ((n >> 1) * k) % DV;
+                        v = (n & 1) ? -r2 * sn[mm] : r2 * cs[mm];
+                    }
+                    v2[e] = flip ? -v : v;
+                }
+                h[j] = pack_half2(v2[0], v2[1]);
             }
-            if (P.sign_mask[k >> 1] & ((k & 1) ? 0x80000000u : 0x8000u)) v = -v;
-            *reinterpret_cast<__half*>(smem + wide::kb_offset<DV>(k, q)) = __float2half_rn(v);
+            *reinterpret_cast<uint4*>(smem + wide::kb_offset<DV>(k, q0)) = make_uint4(h[0], h[1], h[2], h[3]);
         }
         ptx::fence_proxy_async_smem();
     }
