@@ -195,6 +195,11 @@ int srft_kv_dequantize(const srftkv_side* k, const srftkv_side* v, int n_outer, 
  * scale bytes to be a multiple of 16; int4 rows at d = 80 (40 bytes) are
  * read as rows of token pairs and need an even t_cap; d = 80, 96 and 192
  * sides use the SRFT.
+ * Launches: three kernels on `stream` (q preparation, the split kernel, the
+ * combine); the last two as programmatic dependents of the kernel before them
+ * (they start launching while it finishes and wait for its results on the
+ * device), so the call can be captured into a CUDA graph like any other
+ * stream work and orders with the caller's other work as one call would.
  * Range: the kernel forms p * scale_V in fp16.  A stretch of tokens whose
  * V scales overflow that (scales of 128 and more) or sit far below it
  * (p-weighted mean scale under 2^-14) is run a second time with the values
