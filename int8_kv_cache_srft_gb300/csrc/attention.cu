@@ -223,6 +223,13 @@ __host__ __device__ constexpr int swz_chunk(int r, int ch) {
 
 constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
+// d = 256 with 4-bit keys keeps the K-side B fragments of q (hi, lo and the
+// offset terms: 80 registers a thread) in shared memory instead of registers,
+// which lets the kernel run three CTAs an SM instead of two; each 32-dim chunk
+// reads them back with two 16-byte loads and one 8-byte load.
+template <int D, int BK>
+constexpr bool q_in_smem() { return D == 256 && BK == 4; }
+
 template <int D, int BK, int BV>
 struct AttnCfg {
     static constexpr bool QK = BK != 16, QV = BV != 16;
@@ -232,7 +239,8 @@ struct AttnCfg {
     // beat 16-token chunks at 3 (1.04 against 1.13 ms on the decode shape); d = 256 keeps 16 (1.48 against 1.79)
     static constexpr bool WIDE32 = D == 192 && STAGE32 <= 13824;
     static constexpr int CH = SRFTKV_ATTN_CH ? SRFTKV_ATTN_CH : (STAGE32 <= 9216 || WIDE32 ? 32 : 16);  // tokens per chunk
-    static constexpr int MINB = D >= 256 || WIDE32 ? 2 : (D == 96 && BK == 4 && BV == 4) ? 4 : 3;  // CTAs an SM the kernel is compiled for
+    static constexpr bool QSM = q_in_smem<D, BK>();
+    static constexpr int MINB = (D >= 256 && !QSM) || WIDE32 ? 2 : (D == 96 && BK == 4 && BV == 4) ? 4 : 3;  // CTAs an SM the kernel is compiled for
     static constexpr int NS = SRFTKV_ATTN_STAGES;
     // swizzled sub-buffers (code rows of <= 128 bytes, group-16 scale rows of
     // >= 32 bytes) start on a 1024-byte boundary, the others on 128 bytes
@@ -251,11 +259,15 @@ struct AttnCfg {
     static constexpr int WARP_BYTES = NS * STAGE;
     static constexpr int MERGE_BYTES = kAttnWarps * (4 * D + 8) * 4;
     static constexpr int BODY = kAttnWarps * WARP_BYTES > MERGE_BYTES ? kAttnWarps * WARP_BYTES : MERGE_BYTES;
-    static constexpr int BARS = BODY;                   // mbarriers after the body
-    static constexpr int SMEM = 1024 + BODY + 128;      // + slack to realign the base to 1024 bytes
+    // q fragments (QSM): hi and lo [D/32][32 lanes] x 16 bytes, offset terms [D/32][32] x 8 bytes
+    static constexpr int OFF_QF = BODY;
+    static constexpr int QF_BYTES = QSM ? (D / 32) * 32 * (16 + 16 + 8) : 0;
+    static constexpr int BARS = OFF_QF + QF_BYTES;      // mbarriers after the body (and the q fragments)
+    static constexpr int SMEM = 1024 + BARS + 128;      // + slack to realign the base to 1024 bytes
     static_assert(OFF_KC % 128 == 0 && OFF_KS % 128 == 0 && OFF_VC % 128 == 0 && OFF_VS % 128 == 0 &&
                       OFF_KR % 128 == 0 && OFF_VR % 128 == 0 && STAGE % 128 == 0,
                   "TMA destinations on 128-byte boundaries");
+    static_assert(OFF_QF % 16 == 0 && BARS % 8 == 0, "q fragments as 16-byte loads, mbarriers on 8 bytes");
     static constexpr bool PK = PlaneT<D, BK>::PAIR, PV = PlaneT<D, BV>::PAIR;
     static_assert(!(PK || PV) || CH == 32, "a chunk of token pairs is one 16-row MMA tile");
     // K-side B-fragment registers and code-offset terms: four and two per 32-dim chunk (int4), per 16-byte
@@ -583,7 +595,7 @@ template <int D, int BK, int G>
 __device__ __forceinline__ void tile_scores(uint32_t kc, const LaneRow& LK, const uint8_t* __restrict__ ksb,
                                             const uint32_t (&kso)[scale_chunks<D>()], int sp, int lg, int tr,
                                             int lane, const uint32_t (&qh)[D / 8], const uint32_t (&ql)[D / 8],
-                                            const float (&nb)[D / 16], float (&s)[2]) {
+                                            const float (&nb)[D / 16], const uint4* __restrict__ qf, float (&s)[2]) {
     using PK = PlaneT<D, BK>;
     constexpr int SRB = D / 4;
     const int g = lane >> 2;
@@ -599,16 +611,28 @@ __device__ __forceinline__ void tile_scores(uint32_t kc, const LaneRow& LK, cons
         float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
         // 32-dim chunk mm from its two 8-row matrices (rows 0-7, rows 8-15)
         auto chunk = [&](int mm, uint32_t rg, uint32_t rg8) {
+            // this chunk's q fragments: from registers, or from shared memory (q_in_smem)
+            uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
+            float n0, n1;
+            if constexpr (q_in_smem<D, BK>()) {
+                const uint4 H = qf[mm * 32 + lane], Lo = qf[(D / 32 + mm) * 32 + lane];
+                const float2 N = reinterpret_cast<const float2*>(qf + 2 * (D / 32) * 32)[mm * 32 + lane];
+                h0 = H.x, h1 = H.y, h2 = H.z, h3 = H.w, l0 = Lo.x, l1 = Lo.y, l2 = Lo.z, l3 = Lo.w, n0 = N.x, n1 = N.y;
+            } else {
+                h0 = qh[4 * mm], h1 = qh[4 * mm + 1], h2 = qh[4 * mm + 2], h3 = qh[4 * mm + 3];
+                l0 = ql[4 * mm], l1 = ql[4 * mm + 1], l2 = ql[4 * mm + 2], l3 = ql[4 * mm + 3];
+                n0 = nb[2 * mm], n1 = nb[2 * mm + 1];
+            }
             rg = ob4(rg);
             rg8 = ob4(rg8);
             const uint32_t rs = rg >> 8, rs8 = rg8 >> 8;
             const uint32_t x0 = u4_lo(rg), x1 = u4_lo(rg8), x2 = u4_hi(rg), x3 = u4_hi(rg8);
             const uint32_t y0 = u4_lo(rs), y1 = u4_lo(rs8), y2 = u4_hi(rs), y3 = u4_hi(rs8);
             float d[4];
-            mma16816_c(d, x0, x1, x2, x3, qh[4 * mm], qh[4 * mm + 1], nb[2 * mm], nb[2 * mm + 1]);
-            mma16816(d, y0, y1, y2, y3, qh[4 * mm + 2], qh[4 * mm + 3]);
-            mma16816(d, x0, x1, x2, x3, ql[4 * mm], ql[4 * mm + 1]);
-            mma16816(d, y0, y1, y2, y3, ql[4 * mm + 2], ql[4 * mm + 3]);
+            mma16816_c(d, x0, x1, x2, x3, h0, h1, n0, n1);
+            mma16816(d, y0, y1, y2, y3, h2, h3);
+            mma16816(d, x0, x1, x2, x3, l0, l1);
+            mma16816(d, y0, y1, y2, y3, l2, l3);
             // d = (token g: half 0, half 1, token g+8: half 0, half 1) for head c
             const int ga = (32 * mm) >> lg, gb = (32 * mm + 16) >> lg;
             a0 = fma2(ksc(ga, 0), ksc(gb, 0), d[0], d[1], a0);
@@ -971,7 +995,8 @@ __device__ __forceinline__ void attn_chunk(const AttnParams& P, uint8_t* __restr
                                            const uint32_t (&vso)[scale_chunks<D>()],
                                            const uint32_t (&qh)[AttnCfg<D, BK, BV>::QB],
                                            const uint32_t (&ql)[AttnCfg<D, BK, BV>::QB],
-                                           const float (&nb)[AttnCfg<D, BK, BV>::NB], int nh,
+                                           const float (&nb)[AttnCfg<D, BK, BV>::NB],
+                                           const uint4* __restrict__ qf, int nh,
                                            float (&acc)[AttnCfg<D, BK, BV>::ACC],
                                            float (&sv)[AttnCfg<D, BK, BV>::NSV], float& svt, float& m, float& l,
                                            float mu) {
@@ -1018,7 +1043,7 @@ __device__ __forceinline__ void attn_chunk(const AttnParams& P, uint8_t* __restr
 #pragma unroll
         for (int st = 0; st < NT; ++st) {
             if (16 * st < valid)
-                tile_scores<D, BK, G>(kc, LK, stage + C::OFF_KS, kso, sp, lg, 16 * st, lane, qh, ql, nb, s[st]);
+                tile_scores<D, BK, G>(kc, LK, stage + C::OFF_KS, kso, sp, lg, 16 * st, lane, qh, ql, nb, qf, s[st]);
             else s[st][0] = s[st][1] = 0.f;
             if (tail) {
                 if (16 * st + g >= valid) s[st][0] = -INFINITY;
@@ -1253,6 +1278,20 @@ __global__ void __launch_bounds__(kAttnWarps * 32, AttnCfg<D, BK, BV>::MINB)
         build_qb_pair<D>(P.qt + ((long long)b * P.Hq + (long long)hkv * P.rep + h0) * D, nh, g, c, qh, ql, nb);
     else
         build_qb<D, BK>(P.qt + ((long long)b * P.Hq + (long long)hkv * P.rep + h0) * D, nh, g, c, qh, ql, nb);
+    uint4* qf = reinterpret_cast<uint4*>(smem + C::OFF_QF);  // (read only when q_in_smem)
+    if constexpr (C::QSM) {
+        // every warp built the same fragments (same query heads, same lane layout): warp 0 stores them
+        if (warp == 0) {
+            float2* qn = reinterpret_cast<float2*>(qf + 2 * (D / 32) * 32);
+#pragma unroll
+            for (int mm = 0; mm < D / 32; ++mm) {
+                qf[mm * 32 + lane] = make_uint4(qh[4 * mm], qh[4 * mm + 1], qh[4 * mm + 2], qh[4 * mm + 3]);
+                qf[(D / 32 + mm) * 32 + lane] = make_uint4(ql[4 * mm], ql[4 * mm + 1], ql[4 * mm + 2], ql[4 * mm + 3]);
+                qn[mm * 32 + lane] = make_float2(nb[2 * mm], nb[2 * mm + 1]);
+            }
+        }
+        __syncthreads();
+    }
 
     // V unit.  P.V takes B = p * scale_V in fp16 with p <= 256 * 2^-mu, l and acc
     // accumulating in that unit, and the (m, l) the warp exports carry m + mu.
@@ -1334,7 +1373,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, AttnCfg<D, BK, BV>::MINB)
                 break;
             }
             attn_chunk<D, BK, BV, C::CH / 16, G>(P, wbase + st * C::STAGE, chunk * C::CH, L, lane, LK, LV, kso, vso,
-                                                 qh, ql, nb, nh, acc, sv, svt, m, l, mu_p);
+                                                 qh, ql, nb, qf, nh, acc, sv, svt, m, l, mu_p);
             __syncwarp();
             if ((it & (kFoldChunks - 1)) == kFoldChunks - 1) fold_offset();
         }
