@@ -295,3 +295,19 @@ def test_attention_captured_in_a_cuda_graph_matches_eager(bits):
         graph.replay()
         torch.cuda.synchronize()
         assert torch.equal(out, eager), step
+
+
+@pytest.mark.parametrize("group,rep,n_splits", [(32, 3, 0), (64, 4, 3), (16, 3, 1)])
+def test_d256_q_fragments_in_shared_memory(group, rep, n_splits):
+    """d = 256 with 4-bit keys keeps q's K-side fragments in shared memory: the generic-group instance (groups
+    32 and 64), a head group of three query heads (the fourth column padded) and single or few splits, with
+    lambda on both sides, against the oracle on the same quantised cache."""
+    B, Hkv, d, t_cap, seed = 2, 2, 256, 520, 13
+    Hq = Hkv * rep
+    sk, sv = build_cache(B, Hkv, d, t_cap, 4, 4, group, seed, lam=True, data_seed=group + rep)
+    q = I.query(I.Workload("q", n_outer=B, tokens=1, kv_heads=Hkv, d=d, q_heads=Hq, data_seed=group * rep),
+                device="cuda")
+    seq = torch.tensor([520, 77], dtype=torch.int32, device="cuda")
+    out = run_attention(q, sk, sv, B, Hq, Hkv, d, group, t_cap, seq, seed, n_splits=n_splits)
+    ref = oracle_attention(q, sk, sv, group, seed, seq)
+    assert np.abs(out - ref).max() <= ATTN_ATOL
