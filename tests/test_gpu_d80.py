@@ -1,8 +1,9 @@
 """GPU parity at the head dimension d = 80 against the fp64 oracle, through
 the C ABI.
 
-d = 80 is the smallest size the survey of the pages names beside 96 and
-192 for the SRFT's freedom from powers of two.  The SRFT is the packed
+d = 80 is the smallest of the head sizes that are not powers of two (80, 96,
+192) the library takes, sizes the SRFT covers where a Hadamard rotation
+cannot ([WQF] Methodology 1).  The SRFT is the packed
 unitary DFT of length 80 (the oracle's general even-d form); the library runs
 the codec as the tensor-core contraction padded to the 128-wide tile (R zero
 outside its 80 x 80 block) and the bare transform as a dense map.  The code
