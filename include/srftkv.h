@@ -299,6 +299,21 @@ int srftkv_device_fault(unsigned int* fault);
  */
 int srftkv_set_attention_poll_limit_for_testing(int polls);
 
+/*
+ * srftkv_set_codec_poll_limit_for_testing -- TEST HOOK, not for use in
+ * production.  The same for the codec's register-path quantize kernels (the
+ * one-thread-per-vector FFT / WHT kernel of d <= 128 and the two-lane kernel
+ * of d = 192 / 256): how many times a warp polls for its next tile of x
+ * before it gives up; negative restores the default (2^20 polls), 0 makes
+ * every warp give up at its first tile.  A warp that gives up sets bit 0 of
+ * the fault word, waits with the default bound for its own copies in flight
+ * and returns without storing, so the codes and scales of its tiles keep
+ * their previous contents.  Process-wide; the tensor-core codec kernels, the
+ * one-warp-per-vector append kernel (no asynchronous copies) and the
+ * dequantize kernels keep their bounds.  Always returns SRFTKV_OK.
+ */
+int srftkv_set_codec_poll_limit_for_testing(int polls);
+
 #ifdef __cplusplus
 }
 #endif

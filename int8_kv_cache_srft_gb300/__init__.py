@@ -75,9 +75,10 @@ def library() -> ctypes.CDLL:
     lib.srftkv_last_error.restype = ctypes.c_char_p
     lib.srftkv_device_fault.argtypes = [ctypes.POINTER(ctypes.c_uint)]
     lib.srftkv_set_attention_poll_limit_for_testing.argtypes = [i]
+    lib.srftkv_set_codec_poll_limit_for_testing.argtypes = [i]
     for name in ("srft_kv_quantize", "srft_kv_dequantize", "q4kv_decode_attention", "q4kv_decode_attention_static",
                  "srft_kv_vector_bytes", "srft_transform", "srht_transform", "srftkv_device_fault",
-                 "srftkv_set_attention_poll_limit_for_testing"):
+                 "srftkv_set_attention_poll_limit_for_testing", "srftkv_set_codec_poll_limit_for_testing"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -227,6 +228,13 @@ def srftkv_set_attention_poll_limit_for_testing(polls: int) -> None:
     0 = give up at the first chunk)."""
     _check("srftkv_set_attention_poll_limit_for_testing",
            library().srftkv_set_attention_poll_limit_for_testing(int(polls)))
+
+
+def srftkv_set_codec_poll_limit_for_testing(polls: int) -> None:
+    """Test hook: polls of the register-path quantize kernels' tile wait before a warp gives up (negative = the
+    default, 0 = give up at the first tile)."""
+    _check("srftkv_set_codec_poll_limit_for_testing",
+           library().srftkv_set_codec_poll_limit_for_testing(int(polls)))
 
 
 def srftkv_last_error() -> str:

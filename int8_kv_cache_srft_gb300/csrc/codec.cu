@@ -6,6 +6,7 @@
 // Apple Silicon", Methodology 1 (SRFT) and 2 (the fused kernel's steps).
 #include <cuda_fp16.h>
 
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -337,4 +338,18 @@ unsigned int codec_take_fault() {
     return v;
 }
 
+// Polls of a register-path quantize warp's wait for its next tile; -1 = the
+// default bound.  Set only by srftkv_set_codec_poll_limit_for_testing.
+static std::atomic<int> g_codec_poll_limit{-1};
+
+uint32_t codec_poll_limit() {
+    const int lim = g_codec_poll_limit.load();
+    return lim < 0 ? (1u << 20) : (uint32_t)lim;
+}
+
 }  // namespace srftkv
+
+extern "C" int srftkv_set_codec_poll_limit_for_testing(int polls) {
+    srftkv::g_codec_poll_limit.store(polls < 0 ? -1 : polls);
+    return SRFTKV_OK;
+}

@@ -73,6 +73,7 @@ struct CodecParams {
     int total_tiles;      // n_sides * tiles_per_side
     FastDiv div_side, div_head, div_H;  // by tiles_per_side, tiles_per_head, H
     unsigned int* fault;  // device fault word (bit 0: a bounded wait gave up)
+    uint32_t poll_limit;  // polls of a register-path warp's wait for its next tile (a test hook lowers it)
     uint32_t sign_mask[128];
 };
 
@@ -439,7 +440,7 @@ __global__ void __launch_bounds__(128, Geo<D>::MIN_BLOCKS)
         const int b = it & 1;
         const bool has_next = tile + stride < P.total_tiles;
         if (lane == 0 && has_next) issue(tile + stride, b ^ 1);
-        const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(b ? bar1 : bar0, (it >> 1) & 1));
+        const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(b ? bar1 : bar0, (it >> 1) & 1, P.poll_limit));
         if (!ok) {
             if (lane == 0) {
                 atomicOr(P.fault, 1u);
@@ -570,6 +571,7 @@ static inline void fill_params(const CodecCall& c, CodecParams& P) {
     P.lg_group = 0;
     while ((1 << P.lg_group) < c.group) ++P.lg_group;
     set_tile_grid(c, P, 32);
+    P.poll_limit = codec_poll_limit();
     for (int i = 0; i < 128; ++i) P.sign_mask[i] = 0;
     sign_masks(c.d, c.seed, P.sign_mask);
 }

@@ -589,7 +589,7 @@ __global__ void __launch_bounds__(128, PR_MIN_BLOCKS)
         const int b = it & 1;
         const bool has_next = tile + stride < P.total_tiles;
         if (lane == 0 && has_next) issue(tile + stride, b ^ 1);
-        const bool ok = __all_sync(FULL, ptx::mbar_wait_bounded(b ? bar1 : bar0, (it >> 1) & 1));
+        const bool ok = __all_sync(FULL, ptx::mbar_wait_bounded(b ? bar1 : bar0, (it >> 1) & 1, P.poll_limit));
         if (!ok) {
             if (lane == 0) {
                 atomicOr(P.fault, 1u);

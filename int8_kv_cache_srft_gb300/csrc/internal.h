@@ -55,6 +55,9 @@ int launch_codec_d256(const CodecCall& c, bool quantize);
 int transform_launch(const void* x, float* y, int n, int d, uint64_t seed, bool inverse, bool srht, cudaStream_t s);
 unsigned int codec_take_fault();
 unsigned int* codec_fault_word();  // device address of the codec fault word (current device)
+// polls of the register-path quantize kernels' wait for a tile before they give up (2^20 unless a test
+// lowered it with srftkv_set_codec_poll_limit_for_testing)
+uint32_t codec_poll_limit();
 
 void set_error(const char* fmt, ...);
 

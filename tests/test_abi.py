@@ -34,7 +34,8 @@ def test_header_declares_the_entry_points():
     names = header_functions()
     for n in ("srft_kv_quantize", "srft_kv_dequantize", "q4kv_decode_attention",
               "q4kv_decode_attention_workspace_size", "q4kv_decode_attention_static", "srft_kv_vector_bytes",
-              "srft_transform", "srht_transform", "srftkv_last_error", "srftkv_device_fault"):
+              "srft_transform", "srht_transform", "srftkv_last_error", "srftkv_device_fault",
+              "srftkv_set_attention_poll_limit_for_testing", "srftkv_set_codec_poll_limit_for_testing"):
         assert n in names
 
 

@@ -1,4 +1,5 @@
-"""The device give-up path of the attention kernel, on the GPU, without a fault.
+"""The device give-up paths of the attention kernel and of the register-path
+quantize kernels, on the GPU, without a fault.
 
 Every wait of the library's kernels on an asynchronous copy is bounded; a
 warp of the attention split kernel that gives up sets bit 8 of the fault word,
@@ -8,7 +9,11 @@ shortens only the chunk wait, so that every warp gives up at its first chunk
 while every copy it issued still lands: the call must finish, leave the fault
 word set (and clear it when read), write the empty result (zeros), and leave
 the context usable, so that the next call with the default limit is bitwise
-the one before.
+the one before.  srftkv_set_codec_poll_limit_for_testing does the same for
+the quantize kernels that stream x by asynchronous copies one warp per tile
+(the one-thread-per-vector FFT kernel of d <= 128, the two-lane kernel of
+d = 192 and 256): bit 0 of the fault word, no code or scale stored, and the
+next call bitwise the call before.
 """
 
 import numpy as np
@@ -34,6 +39,7 @@ def _lib():
     K = mod
     yield
     K.srftkv_set_attention_poll_limit_for_testing(-1)
+    K.srftkv_set_codec_poll_limit_for_testing(-1)
     assert K.srftkv_device_fault() == 0
 
 
@@ -79,3 +85,48 @@ def test_attention_gives_up_cleanly(d, static):
     after = call()
     assert K.srftkv_device_fault() == 0
     assert torch.equal(after, before), "the context is usable and the result unchanged after a give-up"
+
+
+# (d, forced path): d = 128 forced onto the one-thread-per-vector FFT kernel (a call this small would
+# otherwise take the one-warp-per-vector kernel, which has no asynchronous copies); at d = 192 and 256 a
+# call this small takes the two-lane register kernel by itself
+@pytest.mark.parametrize("d,path", [(128, "fft"), (192, None), (256, None)])
+def test_register_path_quantize_gives_up_cleanly(d, path, monkeypatch):
+    if path is not None:
+        monkeypatch.setenv("SRFTKV_QUANT_PATH", path)
+    w = I.Workload("give_up", n_outer=2, tokens=300, kv_heads=2, d=d, data_seed=d)
+    B, T, H, G, seed = w.n_outer, w.tokens, w.kv_heads, w.group, 5
+    xk, xv = I.kv_side(w, "k", device="cuda"), I.kv_side(w, "v", device="cuda")
+    sk, sv = K.alloc_side(B, T, H, d, 4, G), K.alloc_side(B, T, H, d, 4, G)
+    sk.x, sv.x = xk, xv
+
+    def call():
+        for side in (sk, sv):
+            side.codes.fill_(0xA5)
+            side.scales.view(torch.uint8).fill_(0x5A)
+        K.srft_kv_quantize(sk, sv, B, T, H, d, G, T, 0, seed)
+        torch.cuda.synchronize()
+        return [t.clone() for t in (sk.codes, sk.scales, sv.codes, sv.scales)]
+
+    assert K.srftkv_device_fault() == 0
+    before = call()
+    assert K.srftkv_device_fault() == 0
+    assert not torch.equal(before[0], torch.full_like(before[0], 0xA5)), "the reference call stored nothing"
+    try:
+        K.srftkv_set_codec_poll_limit_for_testing(0)
+        gave_up = call()
+    finally:
+        K.srftkv_set_codec_poll_limit_for_testing(-1)
+    fault = K.srftkv_device_fault()
+    assert fault & 1, f"fault word {fault:#x}: the codec bit is not set"
+    assert not fault & (1 << 8), "the attention bit is set"
+    assert K.srftkv_device_fault() == 0, "reading the fault word clears it"
+    for t in gave_up[0::2]:
+        assert torch.equal(t, torch.full_like(t, 0xA5)), "a warp that gave up stored codes"
+    for t in gave_up[1::2]:
+        raw = t.view(torch.uint8)
+        assert torch.equal(raw, torch.full_like(raw, 0x5A)), "a warp that gave up stored scales"
+    after = call()
+    assert K.srftkv_device_fault() == 0
+    for a, b in zip(after, before):
+        assert torch.equal(a, b), "the context is usable and the result unchanged after a give-up"
