@@ -137,11 +137,13 @@ def job_value(world: int, units_per_rank: int, ms_per_step: float) -> float:
 
 
 class ClockSampler:
-    """nvidia-smi clock and throttle-reason samples during the timed region."""
+    """nvidia-smi clock and throttle-reason samples; stop() keeps the samples whose timestamps fall inside the
+    timed region (the sampler starts earlier, since nvidia-smi takes a moment to print its first line)."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap,clocks.mem")
+    FIELDS = ("timestamp", "clocks.sm", "clocks.max.sm", "power.draw", "clocks.mem", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.idx = gpu_index
@@ -150,39 +152,56 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={','.join(self.FIELDS)}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
 
-    def stop(self):
+    @staticmethod
+    def _when(stamp: str):
+        import datetime
+
+        try:  # local time of this machine, as time.time() sees it
+            return datetime.datetime.strptime(stamp.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
+    def stop(self, t_begin: float, t_end: float):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         self.proc.terminate()
         out, _ = self.proc.communicate(timeout=10)
-        sm, mx, mem, pw, reasons = [], [], [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for line in out.strip().splitlines():
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < len(self.FIELDS):
                 continue
+            r = dict(zip(self.FIELDS, parts))
             try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
+                r["sm"], r["max"] = float(r["clocks.sm"]), float(r["clocks.max.sm"])
             except ValueError:
                 continue
-            try:  # the memory clock and the power draw explain spread in the memory-bound kernels
-                pw.append(float(parts[3]))
-                if len(parts) > 9:
-                    mem.append(float(parts[9]))
-            except ValueError:
-                pass
-            for n, v in zip(names, parts[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm),
-                "mem_mhz": statistics.median(mem) if mem else None, "power_w": statistics.median(pw) if pw else None}
+            r["t"] = self._when(r["timestamp"])
+            rows.append(r)
+        inside = [r for r in rows if r["t"] is not None and t_begin <= r["t"] <= t_end]
+        use = inside if inside else rows
+
+        def med(key):
+            vals = []
+            for r in use:
+                try:
+                    vals.append(float(r[key]))
+                except ValueError:
+                    pass
+            return statistics.median(vals) if vals else None
+
+        reasons = sorted({n for r in use for n in self.REASONS
+                          if r["clocks_event_reasons." + n].lower().startswith("active")})
+        return {"sm_mhz": med("sm"), "sm_max_mhz": max(r["max"] for r in use) if use else None,
+                "reasons": reasons, "samples": len(use),
+                "window": "timed region" if inside else "whole sampler run (no sample inside the timed region)",
+                "mem_mhz": med("clocks.mem"), "power_w": med("power.draw")}
 
 
 # ---------------------------------------------------------------------------
@@ -436,12 +455,14 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     clocks.start()
     time.sleep(0.3)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_begin = time.time()
     e0.record(stream)
     for _ in range(args.steps):
         step(False)
     e1.record(stream)
     torch.cuda.synchronize()
-    clk = clocks.stop()
+    t_end = time.time()
+    clk = clocks.stop(t_begin, t_end)
     barrier()
     ms_total = e0.elapsed_time(e1)
     ms_total = max_over_ranks(ms_total, dev)
