@@ -301,16 +301,21 @@ int srftkv_set_attention_poll_limit_for_testing(int polls);
 
 /*
  * srftkv_set_codec_poll_limit_for_testing -- TEST HOOK, not for use in
- * production.  The same for the codec's register-path quantize kernels (the
- * one-thread-per-vector FFT / WHT kernel of d <= 128 and the two-lane kernel
- * of d = 192 / 256): how many times a warp polls for its next tile of x
- * before it gives up; negative restores the default (2^20 polls), 0 makes
- * every warp give up at its first tile.  A warp that gives up sets bit 0 of
- * the fault word, waits with the default bound for its own copies in flight
- * and returns without storing, so the codes and scales of its tiles keep
- * their previous contents.  Process-wide; the tensor-core codec kernels, the
- * one-warp-per-vector append kernel (no asynchronous copies) and the
- * dequantize kernels keep their bounds.  Always returns SRFTKV_OK.
+ * production.  The same for the codec's quantize kernels that wait on
+ * asynchronous copies of x: how many times a warp of the register-path
+ * kernels (the one-thread-per-vector FFT / WHT kernel of d <= 128, the
+ * two-lane kernel of d = 192 / 256) polls for its next tile, and how many
+ * times the MMA-issuing thread of the tensor-core kernel of d = 80 / 96 / 128
+ * polls for its next x stage, before giving up; negative restores the default (2^20
+ * polls), 0 makes them give up at their first tile.  A warp that gives up
+ * sets bit 0 of the fault word, waits with the default bound for its own
+ * copies in flight and returns without storing; in the tensor-core kernel
+ * the MMA thread then issues nothing and the epilogue warps give up after
+ * their default bound (about a second), so such a call is slow.  Either way
+ * the codes and scales keep their previous contents.  Process-wide; the
+ * wide tensor-core kernels, the one-warp-per-vector append kernel (no
+ * asynchronous copies) and the dequantize kernels keep their bounds.
+ * Always returns SRFTKV_OK.
  */
 int srftkv_set_codec_poll_limit_for_testing(int polls);
 

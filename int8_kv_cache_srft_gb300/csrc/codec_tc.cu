@@ -186,7 +186,10 @@ __global__ void __launch_bounds__(T_WARPS * 32, 1)
         if (lane == 0) {
             for (int t = blockIdx.x, i = 0; t < P.total_tiles; t += stride, ++i) {
                 const int s = i % TSTAGES, a = i % T_NACC;
-                if (!ptx::mbar_wait_bounded(bar(X_FULL + s), (i / TSTAGES) & 1) ||
+                // (P.poll_limit: the default bound, or fewer polls from the test hook; if this wait gives up
+                // before any MMA was issued, no MMA is ever in flight when tensor memory is freed, and the
+                // producer's copies land while the other roles' waits run out)
+                if (!ptx::mbar_wait_bounded(bar(X_FULL + s), (i / TSTAGES) & 1, P.poll_limit) ||
                     (i >= T_NACC && !ptx::mbar_wait_bounded(bar(ACC_EMPTY + a), (i / T_NACC - 1) & 1))) {
                     failed = true;
                     break;

@@ -10,10 +10,12 @@ while every copy it issued still lands: the call must finish, leave the fault
 word set (and clear it when read), write the empty result (zeros), and leave
 the context usable, so that the next call with the default limit is bitwise
 the one before.  srftkv_set_codec_poll_limit_for_testing does the same for
-the quantize kernels that stream x by asynchronous copies one warp per tile
-(the one-thread-per-vector FFT kernel of d <= 128, the two-lane kernel of
-d = 192 and 256): bit 0 of the fault word, no code or scale stored, and the
-next call bitwise the call before.
+the quantize kernels that stream x by asynchronous copies (the
+one-thread-per-vector FFT kernel of d <= 128, the two-lane kernel of d = 192
+and 256, and the MMA-issuing thread of the d = 128 tensor-core kernel, which
+then issues no MMA while the epilogue warps' own waits run out): bit 0 of
+the fault word, no code or scale stored, and the next call bitwise the call
+before.
 """
 
 import numpy as np
@@ -88,10 +90,10 @@ def test_attention_gives_up_cleanly(d, static):
 
 
 # (d, forced path): d = 128 forced onto the one-thread-per-vector FFT kernel (a call this small would
-# otherwise take the one-warp-per-vector kernel, which has no asynchronous copies); at d = 192 and 256 a
-# call this small takes the two-lane register kernel by itself
-@pytest.mark.parametrize("d,path", [(128, "fft"), (192, None), (256, None)])
-def test_register_path_quantize_gives_up_cleanly(d, path, monkeypatch):
+# otherwise take the one-warp-per-vector kernel, which has no asynchronous copies) and onto the tensor-core
+# kernel; at d = 192 and 256 a call this small takes the two-lane register kernel by itself
+@pytest.mark.parametrize("d,path", [(128, "fft"), (128, "tc"), (192, None), (256, None)])
+def test_quantize_gives_up_cleanly(d, path, monkeypatch):
     if path is not None:
         monkeypatch.setenv("SRFTKV_QUANT_PATH", path)
     w = I.Workload("give_up", n_outer=2, tokens=300, kv_heads=2, d=d, data_seed=d)
