@@ -142,8 +142,8 @@ static int quant_path_override() {
     return !strcmp(e, "fft") ? 1 : !strcmp(e, "tc") ? 2 : !strcmp(e, "warp") ? 3 : 0;
 }
 constexpr long long kWarpPathMaxRows = 4096;
-// d = 128: the tensor-core kernels' fixed cost (about 13 us a launch, most of it
-// the R_s block every CTA builds) against the register FFT: measured crossovers
+// d = 128: the tensor-core kernels' fixed cost (about 13 us a launch, some 4 us
+// of it the R_s block every CTA builds) against the register FFT: measured crossovers
 // about 150 K vectors for the quantize (0.21 M: 0.027 against 0.029 ms) and 65 K
 // for the dequantize (0.11 M: 0.019 against 0.021 ms)
 constexpr long long kTensorCoreQuantMinRows = 5ll << 15;
