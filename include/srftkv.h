@@ -53,7 +53,8 @@
  *    compiled into the kernels, two device fault words (one per kernel
  *    family) and the fixed-size scratch array of
  *    q4kv_decode_attention_static (all file-scope __device__ data, held by
- *    every GPU that loads the library).
+ *    every GPU that loads the library), and the two process-wide poll
+ *    limits of the test hooks at the end of this header.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Work is enqueued without host synchronisation; device-side
  *    faults surface on the caller's next synchronisation.
